@@ -1,0 +1,185 @@
+/*
+ * pulsar.h -- C ABI of the GB300 (sm_103a) tile-based differentiable sphere
+ * renderer.
+ *
+ * The operation (Pulsar: Efficient Sphere-based Neural Rendering, Sec. 3.2
+ * and App. A "Prelude"): a scene of spheres -- position, radius, opacity and
+ * a feature payload (Sec. 3.1) -- and a pinhole camera (rotation R,
+ * translation t, intrinsics K) are mapped to a feature image.  Each pixel
+ * blends every sphere its ray hits, front to back, with weights
+ *     w = o * d * exp(o * z~ / gamma),  d = 1 - rho / r_eff,
+ *     z~ = (zfar - c.z) / (zfar - znear)  (normalised device depth),
+ * rho the orthogonal ray-to-centre distance, plus a background of weight
+ * exp(eps / gamma):  F = (sum w f + w_bg f_bg) / (sum w + w_bg).
+ * Gradients of a scalar loss flow to sphere position, radius, opacity,
+ * features and to R, t, K through only the first n_track hits of every
+ * pixel (Sec. 2, B.1.3, B.1.4, B.2).
+ *
+ * Call sequence per frame, all asynchronous on the caller's stream:
+ *     pulsar_project -> pulsar_bin -> pulsar_forward [-> pulsar_backward]
+ * No call synchronises the host except pulsar_status and pulsar_debug_copy
+ * into pageable host memory.
+ *
+ * Conventions for every entry point:
+ *   - Tensors are caller-owned, C-contiguous float32 DEVICE pointers unless
+ *     stated; streams are `cudaStream_t` values passed as `void*` (NULL = the
+ *     legacy default stream).
+ *   - The context owns only its workspace, allocated once by pulsar_create.
+ *   - Return 0 on success or a negative PULSAR_ERR_* code; nothing throws.
+ *     Argument errors are detected on the host before anything is enqueued.
+ *     Errors raised on the device (capacity overflow) are latched in the
+ *     context and returned by pulsar_status.
+ *   - Inputs passed to pulsar_project (pos) and pulsar_forward (features)
+ *     must stay valid and unmodified until the last call of the frame has
+ *     executed on the stream; the backward pass reads them again.
+ *   - One context renders one camera at a time; calls on one context must be
+ *     issued in order on one stream.
+ */
+#ifndef PULSAR_H_
+#define PULSAR_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------- error codes -- */
+#define PULSAR_OK            0
+#define PULSAR_ERR_ARG      -1  /* invalid argument (NULL, size, limit) */
+#define PULSAR_ERR_CUDA     -2  /* a CUDA runtime call failed */
+#define PULSAR_ERR_CAPACITY -3  /* more sphere-tile pairs than max_pairs */
+#define PULSAR_ERR_STATE    -4  /* call out of order (e.g. forward before bin) */
+#define PULSAR_ERR_NOMEM    -5  /* workspace allocation failed */
+
+/* --------------------------------------------------------------- flags -- */
+/* Drop position/radius gradients (and the sphere's share of the camera
+ * gradient) of spheres whose projected area pi*(f_min*r/c.z)^2 is at most
+ * geom_min_area px^2 (Pulsar Sec. 6, App. A: "more than three projected
+ * pixels").  Opacity and feature gradients are always kept. */
+#define PULSAR_FLAG_GEOM_CUTOFF   0x1u
+/* Also record the number of hits of every pixel (for tests; costs 4 B/px). */
+#define PULSAR_FLAG_COUNT_HITS    0x2u
+
+/* Pinhole camera, OpenCV axes (x right, y down, z forward).  R is the
+ * world->camera rotation, row-major: c = R p + t.  Pixel (x, y) has its
+ * centre at (x + 0.5, y + 0.5) and ray direction
+ * ((x + 0.5 - cx)/fx, (y + 0.5 - cy)/fy, 1).  Spheres are kept when
+ * znear < c.z < zfar.  (Pulsar Sec. 3.2: R, t, K; App. A.) */
+typedef struct pulsar_camera {
+    float R[9];
+    float t[3];
+    float fx, fy, cx, cy;
+    int32_t width, height;   /* 1 .. 65535 */
+    float znear, zfar;       /* 0 < znear < zfar */
+} pulsar_camera_t;
+
+/* Blend and gradient parameters. */
+typedef struct pulsar_params {
+    float gamma;          /* blend temperature, > 0 (0.1 in the shipped configs) */
+    float bg_eps;         /* background "depth" eps in exp(eps/gamma), >= 0 */
+    float stop_tau;       /* early-stop tolerance (Pulsar Sec. 3.2, B.1.3); 0 = exact */
+    float kappa;          /* minimum projected radius in px (Pulsar Sec. B.1.1), >= 0 */
+    float geom_min_area;  /* px^2 threshold of PULSAR_FLAG_GEOM_CUTOFF */
+    int32_t n_track;      /* hits per pixel that receive gradients, 1 .. max_track */
+    int32_t channels;     /* feature channels C, 1 .. max_channels */
+    uint32_t flags;       /* PULSAR_FLAG_* */
+} pulsar_params_t;
+
+typedef struct pulsar_ctx* pulsar_ctx_t;
+
+/* Create a context on CUDA device `device` and allocate its workspace for at
+ * most max_spheres spheres, max_pairs sphere-tile pairs, images up to
+ * max_width x max_height, max_channels channels and max_track tracked hits.
+ * The workspace is owned by the context and freed by pulsar_destroy.
+ * Errors: PULSAR_ERR_ARG (NULL out, non-positive limit, max_track > 16,
+ * max_channels > 64, max_pairs >= 2^32), PULSAR_ERR_NOMEM, PULSAR_ERR_CUDA. */
+int pulsar_create(pulsar_ctx_t* out, int device, int64_t max_spheres, int64_t max_pairs,
+                  int32_t max_width, int32_t max_height, int32_t max_channels,
+                  int32_t max_track);
+
+/* Release the context and its workspace (synchronises the device). */
+int pulsar_destroy(pulsar_ctx_t ctx);
+
+/* Step 0 of the forward pass (Pulsar Sec. B.1.1): for each of the n spheres
+ * compute its camera-space centre, cull it, floor its radius so it covers at
+ * least one pixel, project its centre, bound its pixel rectangle without
+ * trigonometry, and form its depth key c.z - r_eff; count its 16x16 tiles.
+ *   pos     [n,3]  world positions
+ *   radius  [n]    radii (> 0)
+ *   opacity [n]    opacities
+ * n may be 0.  Errors: PULSAR_ERR_ARG (NULL pointers with n > 0, n above
+ * max_spheres, image above the create limits, invalid params). */
+int pulsar_project(pulsar_ctx_t ctx, const float* pos, const float* radius,
+                   const float* opacity, int64_t n, const pulsar_camera_t* cam,
+                   const pulsar_params_t* params, void* stream);
+
+/* Tile binning (Pulsar Sec. 3.2 "sorted by earliest possible intersection",
+ * B.1.1, B.1.2): scan the tile counts, emit one (key, id) pair per covered
+ * tile and sort every tile's list by (key, sphere id).  The pair count M
+ * stays on the device; if M > max_pairs the frame is invalid and
+ * pulsar_status returns PULSAR_ERR_CAPACITY.  Errors: PULSAR_ERR_STATE if
+ * pulsar_project was not called for this frame. */
+int pulsar_bin(pulsar_ctx_t ctx, void* stream);
+
+/* Forward pass (Pulsar Sec. B.1.2-B.1.4): composite every pixel front to
+ * back and store the backward-information buffer (the ids of its first
+ * n_track hits, the stabiliser and the normaliser).
+ *   features [n,C]  per-sphere payload
+ *   bg       [C]    background feature f_bg
+ *   image    [H,W,C] output, overwritten
+ * Errors: PULSAR_ERR_ARG (NULL pointer), PULSAR_ERR_STATE (bin missing). */
+int pulsar_forward(pulsar_ctx_t ctx, const float* features, const float* bg, float* image,
+                   void* stream);
+
+/* Backward pass (Pulsar Sec. B.2): gradients of L = sum_pixels <G, F> through
+ * the tracked hits.  features, bg and image are those of pulsar_forward;
+ * grad_image [H,W,C] is G.  Outputs, each overwritten, each may be NULL
+ * (not requested; if all are NULL nothing is enqueued, Pulsar Sec. B.2):
+ *   grad_pos [n,3], grad_radius [n], grad_opacity [n], grad_features [n,C],
+ *   grad_cam [16] = dL/dR (9, row-major), dL/dt (3), dL/d(fx, fy, cx, cy).
+ * Errors: PULSAR_ERR_ARG, PULSAR_ERR_STATE (forward missing). */
+int pulsar_backward(pulsar_ctx_t ctx, const float* features, const float* bg,
+                    const float* image, const float* grad_image, float* grad_pos,
+                    float* grad_radius, float* grad_opacity, float* grad_features,
+                    float* grad_cam, void* stream);
+
+/* Synchronise `stream`, then report the latched device error of the last
+ * frame (PULSAR_OK, PULSAR_ERR_CAPACITY) and clear it.  n_pairs (M) and
+ * n_hits (hit pairs composited by the last forward) may be NULL. */
+int pulsar_status(pulsar_ctx_t ctx, void* stream, int64_t* n_pairs, int64_t* n_hits);
+
+/* Static string for an error code. */
+const char* pulsar_strerror(int code);
+
+/* Internal arrays of the last frame, for tests (layouts are not a stable
+ * interface).  Copies `bytes` bytes (at most the array's size for the frame)
+ * into dst (host or device; cudaMemcpyDefault).  Returns the array's size in
+ * bytes for the current frame if dst is NULL, else PULSAR_OK or an error.
+ *   PULSAR_DBG_REC0      [n] float4 (u_hi, u_lo, v_hi, v_lo) projected centre pair
+ *   PULSAR_DBG_REC1      [n] float4 (s2 = (r_eff/c.z)^2, c.z/r_eff, o, o*z~/gamma)
+ *   PULSAR_DBG_REC2      [n] float4 (c.z, r_eff, key, flags bits: 1 keep, 2 floor, 4 cut)
+ *   PULSAR_DBG_RECT      [n] uint32 x2 (x0 | x1 << 16, y0 | y1 << 16) pixel rectangle
+ *   PULSAR_DBG_TILE_OFFSETS [B+1] uint32 tile list offsets
+ *   PULSAR_DBG_TILE_IDS  [M] uint32 sorted tile lists
+ *   PULSAR_DBG_MG        [H*W] float  stabiliser m / gamma
+ *   PULSAR_DBG_WSUM      [H*W] float  normaliser in the exp(-m/gamma) frame
+ *   PULSAR_DBG_IDS       [n_track][H*W] int32 tracked ids, -1 padded
+ *   PULSAR_DBG_NHITS     [H*W] int32 hits per pixel (PULSAR_FLAG_COUNT_HITS) */
+#define PULSAR_DBG_REC0          1
+#define PULSAR_DBG_REC1          2
+#define PULSAR_DBG_REC2          3
+#define PULSAR_DBG_RECT          4
+#define PULSAR_DBG_TILE_OFFSETS  5
+#define PULSAR_DBG_TILE_IDS      6
+#define PULSAR_DBG_MG            7
+#define PULSAR_DBG_WSUM          8
+#define PULSAR_DBG_IDS           9
+#define PULSAR_DBG_NHITS        10
+int64_t pulsar_debug_copy(pulsar_ctx_t ctx, int what, void* dst, int64_t bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PULSAR_H_ */

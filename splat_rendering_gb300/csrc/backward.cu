@@ -1,0 +1,292 @@
+// Backward pass (Pulsar Sec. B.2): pixel-wise, reusing the forward pass's
+// backward-information buffer (Sec. B.1.4) so no intersection search is
+// repeated.  Gradients of L = sum_pixels <G, F> flow through the first
+// n_track hits of every pixel only (Sec. 2, B.1.3).
+//
+// k_backward  one block per 16x16 tile, one thread per pixel.  For tracked
+//             hit k the lanes of a warp that hold the same sphere are grouped
+//             (__match_any_sync) and their contributions tree-reduced, so one
+//             lane per distinct sphere issues the global atomics -- the
+//             warp-level aggregation of DISTWAR (arxiver abstract).  dL/dc and
+//             dL/dr go to a float4 accumulator with one vector reduction;
+//             opacity and feature gradients go straight to the caller's
+//             (zeroed) arrays.  The intrinsics' gradient is summed per thread,
+//             reduced per block and added to fp64 accumulators.
+// k_finalize  one thread per sphere (grid-stride): dL/dp = R^T dL/dc and
+//             dL/dr out of the accumulator (which it zeroes for the next
+//             frame); dL/dR = sum dL/dc p^T and dL/dt = sum dL/dc reduced
+//             per block into fp64 accumulators; the last block to finish
+//             writes grad_cam and clears the accumulators (Pulsar Sec. B.2:
+//             sphere-wise camera-gradient accumulation, then a device-wide
+//             reduction).
+#include "pulsar_internal.cuh"
+
+namespace pulsar {
+namespace {
+
+constexpr int kBwdThreads = kTilePix;
+constexpr int kFinThreads = 256;
+
+__device__ __forceinline__ void red_add_v4(float4* addr, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
+                 :: "l"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
+// Lane of the n-th (0-based) set bit of m.
+__device__ __forceinline__ int nth_lane(uint32_t m, int n) {
+    for (int q = 0; q < n; ++q) m &= m - 1;
+    return __ffs(m) - 1;
+}
+
+template <int CMAX, int TMAX>
+__global__ void __launch_bounds__(kBwdThreads)
+k_backward(Frame f, Workspace w, const float* __restrict__ features,
+           const float* __restrict__ image, const float* __restrict__ grad_image,
+           float* __restrict__ grad_opacity, float* __restrict__ grad_features, int want_geom) {
+    __shared__ float s_k[kBwdThreads / 32][4];
+    constexpr int NV = 5 + CMAX;   // gc.xyz, gr, go, gf[CMAX]
+    if (w.state->n_pairs > f.max_pairs) return;   // overflowed frame: no valid buffer
+    const int C = f.channels;
+    const int tile = blockIdx.x;
+    const int tyi = tile / f.tiles_x, txi = tile - tyi * f.tiles_x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int x = txi * kTile + (tid & 15), y = tyi * kTile + (tid >> 4);
+    const bool inside = x < f.width && y < f.height;
+    const int P = f.width * f.height;
+    const int p = inside ? y * f.width + x : 0;
+    const PixelRay ray = pixel_ray(x, y, f);
+    const float iqq = 1.0f / ray.qq;
+    const uint32_t lt_mask = (1u << lane) - 1u;
+
+    float G[CMAX], F[CMAX];
+#pragma unroll
+    for (int c = 0; c < CMAX; ++c) {
+        G[c] = (inside && c < C) ? grad_image[(size_t)p * C + c] : 0.0f;
+        F[c] = (inside && c < C) ? image[(size_t)p * C + c] : 0.0f;
+    }
+    const float mg = inside ? w.mg[p] : 0.0f;
+    const float iw = inside ? 1.0f / w.wsum[p] : 0.0f;
+    float gk[4] = {0.f, 0.f, 0.f, 0.f};   // d/d(fx, fy, cx, cy)
+
+    for (int k = 0; k < f.n_track; ++k) {
+        const int id = inside ? w.ids[(size_t)k * P + p] : -1;
+        if (__ballot_sync(0xffffffffu, id >= 0) == 0u) break;
+        float v[NV];
+#pragma unroll
+        for (int q = 0; q < NV; ++q) v[q] = 0.0f;
+        bool cut = true;
+        if (id >= 0) {
+            const float4 uv = w.rec0[id];
+            const float4 r1 = w.rec1[id];
+            const float4 r2 = w.rec2[id];
+            const uint32_t fl = __float_as_uint(r2.w);
+            cut = (fl & kFlagCut) != 0u;
+            float U, V;
+            const float Q = ray_offset_q(uv, ray, f.ifx, f.ify, &U, &V);
+            const float rq = sqrtf(Q * iqq);            // rho / c.z
+            const float d = 1.0f - rq * r1.y;
+            const float o = r1.z;
+            const float E = __expf(r1.w - mg);
+            const float wt = o * d * E;
+            float sdot = 0.0f;
+#pragma unroll
+            for (int c = 0; c < CMAX; ++c) {
+                if (c < C) {
+                    const float fc = features[(size_t)id * C + c];
+                    sdot += G[c] * (fc - F[c]);
+                    v[5 + c] = wt * iw * G[c];          // dL/df = (w / W) G
+                }
+            }
+            const float sj = sdot * iw;                 // dL/dw = <G, f - F> / W
+            v[4] = sj * d * E * (1.0f + r1.w);          // dw/do = d E (1 + o z~/gamma)
+            if (want_geom && !cut) {
+                const float Z = r2.x, reff = r2.y;
+                const float ireff = 1.0f / reff;
+                const float sE = sj * o * E;            // dL/dd
+                // depth factor: dw/dz~ = w o / gamma, dz~/dc.z = -1/(zfar - znear)
+                float gcz = -sj * wt * o * f.inv_gamma * f.inv_zrange;
+                const float rho = rq * Z;
+                const float g_rho = -sE * ireff;        // dd/drho = -1/r_eff
+                const float g_reff = sE * rho * ireff * ireff;
+                float gr = 0.0f;
+                if (fl & kFlagFloor) {
+                    // r_eff = kappa c.z / f_min
+                    gcz += g_reff * f.kappa / f.fmin;
+                    const float gf = -g_reff * f.kappa * Z / (f.fmin * f.fmin);
+                    if (f.fx <= f.fy) gk[0] += gf; else gk[1] += gf;
+                } else {
+                    gr = g_reff;
+                }
+                float gcx = 0.0f, gcy = 0.0f;
+                if (Q > 0.0f) {
+                    // drho/dc = e_perp / rho, e = c - c.z q = -c.z (U, V, 0)
+                    const float kq = (U * ray.a + V * ray.b) * iqq;
+                    const float irq = 1.0f / rq;
+                    const float n0 = -(U - kq * ray.a) * irq;
+                    const float n1 = -(V - kq * ray.b) * irq;
+                    const float n2 = kq * irq;
+                    gcx = g_rho * n0;
+                    gcy = g_rho * n1;
+                    gcz += g_rho * n2;
+                    // drho/dq = -(c.q / q.q) e_perp / rho with c.q / q.q = c.z (1 - kq);
+                    // q = ((px - cx)/fx, (py - cy)/fy, 1)
+                    const float sq = -Z * (1.0f - kq);
+                    const float ga = g_rho * sq * n0, gb = g_rho * sq * n1;
+                    gk[0] -= ga * ray.a * f.ifx;
+                    gk[1] -= gb * ray.b * f.ify;
+                    gk[2] -= ga * f.ifx;
+                    gk[3] -= gb * f.ify;
+                }
+                v[0] = gcx;
+                v[1] = gcy;
+                v[2] = gcz;
+                v[3] = gr;
+            }
+        }
+        // group the lanes that hold the same sphere and tree-reduce within groups
+        const uint32_t peers = __match_any_sync(0xffffffffu, id);
+        const int rank = __popc(peers & lt_mask);
+        const int gsz = __popc(peers);
+        const int gmax = __reduce_max_sync(0xffffffffu, gsz);
+        for (int off = 1; off < gmax; off <<= 1) {
+            const bool take = (rank & (2 * off - 1)) == 0 && rank + off < gsz;
+            const int src = take ? nth_lane(peers, rank + off) : lane;
+#pragma unroll
+            for (int q = 0; q < NV; ++q) {
+                const float o2 = __shfl_sync(0xffffffffu, v[q], src);
+                if (take) v[q] += o2;
+            }
+        }
+        if (rank == 0 && id >= 0) {
+            if (want_geom && !cut) red_add_v4(&w.gacc[id], v[0], v[1], v[2], v[3]);
+            if (grad_opacity) atomicAdd(&grad_opacity[id], v[4]);
+            if (grad_features) {
+#pragma unroll
+                for (int c = 0; c < CMAX; ++c)
+                    if (c < C) atomicAdd(&grad_features[(size_t)id * C + c], v[5 + c]);
+            }
+        }
+    }
+    if (!want_geom) return;
+    // block reduction of the intrinsics' gradient
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        float s = gk[q];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
+        if (lane == 0) s_k[warp][q] = s;
+    }
+    __syncthreads();
+    if (tid < 4) {
+        double s = 0.0;
+        for (int q = 0; q < kBwdThreads / 32; ++q) s += (double)s_k[q][tid];
+        if (s != 0.0) atomicAdd(&w.state->cam_acc[12 + tid], s);
+    }
+}
+
+__global__ void __launch_bounds__(kFinThreads)
+k_finalize(Frame f, Workspace w, const float* __restrict__ pos, float* __restrict__ grad_pos,
+           float* __restrict__ grad_radius, float* __restrict__ grad_cam) {
+    __shared__ double s_part[kFinThreads / 32][12];
+    __shared__ bool s_last;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float acc[12];
+#pragma unroll
+    for (int q = 0; q < 12; ++q) acc[q] = 0.0f;
+    for (int i = blockIdx.x * blockDim.x + tid; i < f.n; i += gridDim.x * blockDim.x) {
+        const float4 g = w.gacc[i];
+        w.gacc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (grad_pos) {
+            grad_pos[3 * i + 0] = f.R[0] * g.x + f.R[3] * g.y + f.R[6] * g.z;
+            grad_pos[3 * i + 1] = f.R[1] * g.x + f.R[4] * g.y + f.R[7] * g.z;
+            grad_pos[3 * i + 2] = f.R[2] * g.x + f.R[5] * g.y + f.R[8] * g.z;
+        }
+        if (grad_radius) grad_radius[i] = g.w;
+        if (g.x != 0.0f || g.y != 0.0f || g.z != 0.0f) {
+            const float px = pos[3 * i], py = pos[3 * i + 1], pz = pos[3 * i + 2];
+            acc[0] += g.x * px; acc[1] += g.x * py; acc[2] += g.x * pz;
+            acc[3] += g.y * px; acc[4] += g.y * py; acc[5] += g.y * pz;
+            acc[6] += g.z * px; acc[7] += g.z * py; acc[8] += g.z * pz;
+            acc[9] += g.x; acc[10] += g.y; acc[11] += g.z;
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < 12; ++q) {
+        float s = acc[q];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
+        if (lane == 0) s_part[warp][q] = (double)s;
+    }
+    __syncthreads();
+    if (tid < 12) {
+        double s = 0.0;
+        for (int q = 0; q < kFinThreads / 32; ++q) s += s_part[q][tid];
+        if (s != 0.0) atomicAdd(&w.state->cam_acc[tid], s);
+    }
+    // last block out writes the camera gradient and clears the accumulators
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(&w.state->ticket, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (s_last && tid < 16) {
+        __threadfence();
+        volatile double* cam = w.state->cam_acc;
+        const double v = cam[tid];
+        if (grad_cam) grad_cam[tid] = (float)v;
+        cam[tid] = 0.0;
+        if (tid == 0) w.state->ticket = 0u;
+    }
+}
+
+template <int CMAX, int TMAX>
+void launch_bwd_t(const Frame& f, const Workspace& w, const float* features, const float* image,
+                  const float* grad_image, float* grad_opacity, float* grad_features,
+                  int want_geom, cudaStream_t stream) {
+    k_backward<CMAX, TMAX><<<f.n_tiles, kBwdThreads, 0, stream>>>(
+        f, w, features, image, grad_image, grad_opacity, grad_features, want_geom);
+}
+
+template <int CMAX>
+void launch_bwd_c(const Frame& f, const Workspace& w, const float* features, const float* image,
+                  const float* grad_image, float* grad_opacity, float* grad_features,
+                  int want_geom, cudaStream_t stream) {
+    if (f.n_track <= 8)
+        launch_bwd_t<CMAX, 8>(f, w, features, image, grad_image, grad_opacity, grad_features,
+                              want_geom, stream);
+    else
+        launch_bwd_t<CMAX, kMaxTrack>(f, w, features, image, grad_image, grad_opacity,
+                                      grad_features, want_geom, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_backward(const Frame& f, const Workspace& w, const float* pos,
+                            const float* features, const float* image, const float* grad_image,
+                            float* grad_pos, float* grad_radius, float* grad_opacity,
+                            float* grad_features, float* grad_cam, cudaStream_t stream) {
+    const int want_geom = (grad_pos || grad_radius || grad_cam) ? 1 : 0;
+    if (f.channels <= 4)
+        launch_bwd_c<4>(f, w, features, image, grad_image, grad_opacity, grad_features,
+                        want_geom, stream);
+    else if (f.channels <= 8)
+        launch_bwd_c<8>(f, w, features, image, grad_image, grad_opacity, grad_features,
+                        want_geom, stream);
+    else if (f.channels <= 16)
+        launch_bwd_c<16>(f, w, features, image, grad_image, grad_opacity, grad_features,
+                         want_geom, stream);
+    else if (f.channels <= 32)
+        launch_bwd_c<32>(f, w, features, image, grad_image, grad_opacity, grad_features,
+                         want_geom, stream);
+    else
+        launch_bwd_c<kMaxChannels>(f, w, features, image, grad_image, grad_opacity,
+                                   grad_features, want_geom, stream);
+    if (want_geom) {
+        int blocks = (f.n + kFinThreads - 1) / kFinThreads;
+        blocks = blocks < 1 ? 1 : (blocks > 152 * 8 ? 152 * 8 : blocks);
+        k_finalize<<<blocks, kFinThreads, 0, stream>>>(f, w, pos, grad_pos, grad_radius,
+                                                       grad_cam);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace pulsar

@@ -1,0 +1,109 @@
+// Step 0 of the forward pass (Pulsar Sec. B.1.1, "Enclosing Rectangle
+// Calculation"): one thread per sphere computes the camera-space centre,
+// culls, floors the radius so every sphere covers at least one pixel,
+// projects the centre, bounds the pixel rectangle without trigonometry and
+// forms the depth key; the warp then counts the sphere-tile pairs per tile
+// cooperatively, so a sphere covering many tiles does not stall its lane.
+#include "pulsar_internal.cuh"
+
+namespace pulsar {
+namespace {
+
+constexpr int kProjectThreads = 256;
+
+__global__ void __launch_bounds__(kProjectThreads)
+k_project(Frame f, Workspace w, const float* __restrict__ pos, const float* __restrict__ radius,
+          const float* __restrict__ opacity) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    const int lane = threadIdx.x & 31;
+    int tx0 = 0, ty0 = 0, ntx = 0, count = 0;
+    if (i < f.n) {
+        const float px = pos[3 * i], py = pos[3 * i + 1], pz = pos[3 * i + 2];
+        const float r = radius[i], o = opacity[i];
+        const FPair cx = camera_row(f.R[0], f.R[1], f.R[2], f.t[0], px, py, pz);
+        const FPair cy = camera_row(f.R[3], f.R[4], f.R[5], f.t[1], px, py, pz);
+        const FPair cz = camera_row(f.R[6], f.R[7], f.R[8], f.t[2], px, py, pz);
+        const float Z = cz.hi;
+        // at-least-one-pixel floor of the radius
+        const float rfloor = __fdiv_rn(__fmul_rn(f.kappa, Z), f.fmin);
+        const bool on_floor = r < rfloor;
+        const float reff = on_floor ? rfloor : r;
+        bool keep = Z > f.znear && Z < f.zfar && reff < Z;
+        float4 r0 = make_float4(0.f, 0.f, 0.f, 0.f), r1 = r0;
+        uint2 rc = make_uint2(1u, 1u);   // empty: x0 = 1 > x1 = 0
+        uint32_t flags = 0;
+        float key = 0.f;
+        if (keep) {
+            const FPair u = pair_project(f.fx, f.cx, pair_quotient(cx, cz));
+            const FPair v = pair_project(f.fy, f.cy, pair_quotient(cy, cz));
+            int x0, x1, y0, y1;
+            keep = tangent_range(cx.hi, Z, reff, f.fx, f.cx, f.width, &x0, &x1) &&
+                   tangent_range(cy.hi, Z, reff, f.fy, f.cy, f.height, &y0, &y1);
+            if (keep) {
+                key = __fsub_rn(Z, reff);
+                const float tt = __fdiv_rn(reff, Z);
+                const float s2 = __fmul_rn(tt, tt);
+                const float g = __fdiv_rn(__fmul_rn(f.fmin, r), Z);
+                const float area = __fmul_rn(kPi, __fmul_rn(g, g));
+                const bool cut = (f.flags & 1u) && !(area > f.amin);
+                flags = kFlagKeep | (on_floor ? kFlagFloor : 0u) | (cut ? kFlagCut : 0u);
+                r0 = make_float4(u.hi, u.lo, v.hi, v.lo);
+                // value path: c.z / r_eff and o * z~ / gamma
+                const float zt = (f.zfar - Z) * f.inv_zrange;
+                r1 = make_float4(s2, Z / reff, o, o * zt * f.inv_gamma);
+                rc = make_uint2((uint32_t)x0 | ((uint32_t)x1 << 16),
+                                (uint32_t)y0 | ((uint32_t)y1 << 16));
+                tx0 = x0 / kTile;
+                ty0 = y0 / kTile;
+                ntx = x1 / kTile - tx0 + 1;
+                count = ntx * (y1 / kTile - ty0 + 1);
+            }
+        }
+        w.rec0[i] = r0;
+        w.rec1[i] = r1;
+        w.rec2[i] = make_float4(Z, reff, key, __uint_as_float(flags));
+        w.rect[i] = rc;
+    }
+    // warp-cooperative tile counting: flatten the warp's (sphere, tile) pairs
+    int incl = count;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    for (int j0 = 0; j0 < total; j0 += 32) {
+        const int j = j0 + lane;
+        // owner = first lane whose inclusive prefix exceeds j
+        int lo = 0, hi = 31;
+#pragma unroll
+        for (int s = 0; s < 5; ++s) {
+            const int mid = (lo + hi) >> 1;
+            const int pm = __shfl_sync(0xffffffffu, incl, mid);
+            if (pm > j) hi = mid; else lo = mid + 1;
+        }
+        const int own = lo;
+        const int own_incl = __shfl_sync(0xffffffffu, incl, own);
+        const int own_cnt = __shfl_sync(0xffffffffu, count, own);
+        const int own_tx0 = __shfl_sync(0xffffffffu, tx0, own);
+        const int own_ty0 = __shfl_sync(0xffffffffu, ty0, own);
+        const int own_ntx = __shfl_sync(0xffffffffu, ntx, own);
+        if (j < total) {
+            const int k = j - (own_incl - own_cnt);
+            const int tile = (own_ty0 + k / own_ntx) * f.tiles_x + own_tx0 + k % own_ntx;
+            atomicAdd(&w.tile_count[tile], 1u);
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_project(const Frame& f, const Workspace& w, const float* pos,
+                           const float* radius, const float* opacity, cudaStream_t stream) {
+    if (f.n == 0) return cudaSuccess;
+    const int blocks = (f.n + kProjectThreads - 1) / kProjectThreads;
+    k_project<<<blocks, kProjectThreads, 0, stream>>>(f, w, pos, radius, opacity);
+    return cudaGetLastError();
+}
+
+}  // namespace pulsar

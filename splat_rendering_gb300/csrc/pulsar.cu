@@ -1,0 +1,306 @@
+// C ABI of the sphere renderer: context, workspace and the per-frame call
+// sequence (project -> bin -> forward -> backward).  Every call validates its
+// arguments on the host, enqueues kernels on the caller's stream and returns
+// without synchronising; device-side errors are latched and reported by
+// pulsar_status.
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <new>
+
+#include "../../include/pulsar.h"
+#include "pulsar_internal.cuh"
+
+using namespace pulsar;
+
+struct pulsar_ctx {
+    int device = 0;
+    int64_t max_n = 0, max_pairs = 0;
+    int32_t max_w = 0, max_h = 0, max_c = 0, max_t = 0;
+    int64_t max_tiles = 0, max_pix = 0;
+    Workspace ws{};
+    DevState* host_state = nullptr;   // pinned mirror for pulsar_status
+    Frame frame{};
+    const float* pos = nullptr;        // inputs of the current frame
+    int stage = 0;                     // 0 none, 1 projected, 2 binned, 3 forward done
+    bool counts_dirty = false;         // tile counts hold a frame that was never binned
+    void* allocs[16] = {};
+    int n_allocs = 0;
+};
+
+namespace {
+
+cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+int cuda_err(cudaError_t e) { return e == cudaSuccess ? PULSAR_OK : PULSAR_ERR_CUDA; }
+
+struct DeviceGuard {
+    int prev = -1;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        if (prev != dev) cudaSetDevice(dev);
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+template <typename T>
+bool alloc(pulsar_ctx* c, T** p, size_t count) {
+    void* q = nullptr;
+    if (cudaMalloc(&q, count * sizeof(T) > 0 ? count * sizeof(T) : 16) != cudaSuccess) return false;
+    c->allocs[c->n_allocs++] = q;
+    *p = static_cast<T*>(q);
+    return true;
+}
+
+void free_all(pulsar_ctx* c) {
+    for (int i = 0; i < c->n_allocs; ++i) cudaFree(c->allocs[i]);
+    c->n_allocs = 0;
+    if (c->host_state) cudaFreeHost(c->host_state);
+    c->host_state = nullptr;
+}
+
+bool finite_pos(float v) { return v > 0.0f && v < 3.0e38f; }
+
+}  // namespace
+
+extern "C" {
+
+const char* pulsar_strerror(int code) {
+    switch (code) {
+        case PULSAR_OK: return "ok";
+        case PULSAR_ERR_ARG: return "invalid argument";
+        case PULSAR_ERR_CUDA: return "CUDA runtime error";
+        case PULSAR_ERR_CAPACITY: return "sphere-tile pairs exceed max_pairs";
+        case PULSAR_ERR_STATE: return "call out of order";
+        case PULSAR_ERR_NOMEM: return "workspace allocation failed";
+        default: return "unknown error";
+    }
+}
+
+int pulsar_create(pulsar_ctx_t* out, int device, int64_t max_spheres, int64_t max_pairs,
+                  int32_t max_width, int32_t max_height, int32_t max_channels,
+                  int32_t max_track) {
+    if (!out) return PULSAR_ERR_ARG;
+    *out = nullptr;
+    if (max_spheres < 0 || max_spheres > 0x7fffffffLL || max_pairs < 1 ||
+        max_pairs >= 0xffffffffLL || max_width < 1 || max_width > 65535 || max_height < 1 ||
+        max_height > 65535 || max_channels < 1 || max_channels > kMaxChannels ||
+        max_track < 1 || max_track > kMaxTrack)
+        return PULSAR_ERR_ARG;
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess) return PULSAR_ERR_CUDA;
+    if (device < 0 || device >= ndev) return PULSAR_ERR_ARG;
+    DeviceGuard guard(device);
+    pulsar_ctx* c = new (std::nothrow) pulsar_ctx();
+    if (!c) return PULSAR_ERR_NOMEM;
+    c->device = device;
+    c->max_n = max_spheres;
+    c->max_pairs = max_pairs;
+    c->max_w = max_width;
+    c->max_h = max_height;
+    c->max_c = max_channels;
+    c->max_t = max_track;
+    c->max_tiles = (int64_t)((max_width + kTile - 1) / kTile) * ((max_height + kTile - 1) / kTile);
+    c->max_pix = (int64_t)max_width * max_height;
+    const size_t N = (size_t)(max_spheres > 0 ? max_spheres : 1);
+    Workspace& w = c->ws;
+    bool ok = alloc(c, &w.rec0, N) && alloc(c, &w.rec1, N) && alloc(c, &w.rec2, N) &&
+              alloc(c, &w.rect, N) && alloc(c, &w.gacc, N) &&
+              alloc(c, &w.tile_count, (size_t)c->max_tiles) &&
+              alloc(c, &w.tile_start, (size_t)c->max_tiles + 1) &&
+              alloc(c, &w.pairs, (size_t)max_pairs) && alloc(c, &w.pairs_alt, (size_t)max_pairs) &&
+              alloc(c, &w.tile_ids, (size_t)max_pairs) && alloc(c, &w.mg, (size_t)c->max_pix) &&
+              alloc(c, &w.wsum, (size_t)c->max_pix) &&
+              alloc(c, &w.ids, (size_t)c->max_pix * max_track) &&
+              alloc(c, &w.nhits, (size_t)c->max_pix) && alloc(c, &w.state, 1);
+    if (ok) ok = cudaMallocHost(&c->host_state, sizeof(DevState)) == cudaSuccess;
+    // zero-between-frames invariants
+    if (ok)
+        ok = cudaMemset(w.gacc, 0, N * sizeof(float4)) == cudaSuccess &&
+             cudaMemset(w.tile_count, 0, (size_t)c->max_tiles * sizeof(uint32_t)) == cudaSuccess &&
+             cudaMemset(w.tile_start, 0, ((size_t)c->max_tiles + 1) * sizeof(uint32_t)) ==
+                 cudaSuccess &&
+             cudaMemset(w.state, 0, sizeof(DevState)) == cudaSuccess &&
+             cudaDeviceSynchronize() == cudaSuccess;
+    if (!ok) {
+        free_all(c);
+        delete c;
+        cudaGetLastError();
+        return PULSAR_ERR_NOMEM;
+    }
+    *out = c;
+    return PULSAR_OK;
+}
+
+int pulsar_destroy(pulsar_ctx_t c) {
+    if (!c) return PULSAR_ERR_ARG;
+    DeviceGuard guard(c->device);
+    cudaDeviceSynchronize();
+    free_all(c);
+    delete c;
+    return PULSAR_OK;
+}
+
+int pulsar_project(pulsar_ctx_t c, const float* pos, const float* radius, const float* opacity,
+                   int64_t n, const pulsar_camera_t* cam, const pulsar_params_t* prm,
+                   void* stream) {
+    if (!c || !cam || !prm || n < 0 || n > c->max_n) return PULSAR_ERR_ARG;
+    if (n > 0 && (!pos || !radius || !opacity)) return PULSAR_ERR_ARG;
+    if (cam->width < 1 || cam->height < 1 || cam->width > c->max_w || cam->height > c->max_h)
+        return PULSAR_ERR_ARG;
+    if (!finite_pos(cam->fx) || !finite_pos(cam->fy) || !(cam->znear > 0.0f) ||
+        !(cam->zfar > cam->znear))
+        return PULSAR_ERR_ARG;
+    if (!finite_pos(prm->gamma) || !(prm->bg_eps >= 0.0f) || !(prm->stop_tau >= 0.0f) ||
+        !(prm->kappa >= 0.0f) || !(prm->geom_min_area >= 0.0f) || prm->n_track < 1 ||
+        prm->n_track > c->max_t || prm->channels < 1 || prm->channels > c->max_c)
+        return PULSAR_ERR_ARG;
+    DeviceGuard guard(c->device);
+    cudaStream_t s = as_stream(stream);
+    if (c->counts_dirty) {
+        // a previous frame was projected but never binned: its counts are stale
+        cudaError_t e = cudaMemsetAsync(c->ws.tile_count, 0, (size_t)c->max_tiles * 4, s);
+        if (e != cudaSuccess) return PULSAR_ERR_CUDA;
+    }
+    Frame& f = c->frame;
+    std::memcpy(f.R, cam->R, sizeof(f.R));
+    std::memcpy(f.t, cam->t, sizeof(f.t));
+    f.fx = cam->fx; f.fy = cam->fy; f.cx = cam->cx; f.cy = cam->cy;
+    f.znear = cam->znear; f.zfar = cam->zfar;
+    f.ifx = 1.0f / cam->fx;
+    f.ify = 1.0f / cam->fy;
+    f.fmin = cam->fx <= cam->fy ? cam->fx : cam->fy;
+    f.gamma = prm->gamma;
+    f.inv_gamma = 1.0f / prm->gamma;
+    f.bg_eps = prm->bg_eps;
+    f.stop_tau = prm->stop_tau;
+    f.kappa = prm->kappa;
+    f.amin = prm->geom_min_area;
+    f.inv_zrange = 1.0f / (cam->zfar - cam->znear);
+    f.width = cam->width;
+    f.height = cam->height;
+    f.tiles_x = (cam->width + kTile - 1) / kTile;
+    f.tiles_y = (cam->height + kTile - 1) / kTile;
+    f.n_tiles = f.tiles_x * f.tiles_y;
+    f.n_track = prm->n_track;
+    f.channels = prm->channels;
+    f.n = (int)n;
+    f.flags = prm->flags;
+    f.max_pairs = (uint32_t)c->max_pairs;
+    c->pos = pos;
+    cudaError_t e = launch_project(f, c->ws, pos, radius, opacity, s);
+    if (e != cudaSuccess) return PULSAR_ERR_CUDA;
+    c->stage = 1;
+    c->counts_dirty = true;
+    return PULSAR_OK;
+}
+
+int pulsar_bin(pulsar_ctx_t c, void* stream) {
+    if (!c) return PULSAR_ERR_ARG;
+    if (c->stage < 1) return PULSAR_ERR_STATE;
+    if (c->stage >= 2) return PULSAR_ERR_STATE;   // counts were consumed by the first bin
+    DeviceGuard guard(c->device);
+    cudaError_t e = launch_bin(c->frame, c->ws, as_stream(stream));
+    if (e != cudaSuccess) return PULSAR_ERR_CUDA;
+    c->stage = 2;
+    c->counts_dirty = false;
+    return PULSAR_OK;
+}
+
+int pulsar_forward(pulsar_ctx_t c, const float* features, const float* bg, float* image,
+                   void* stream) {
+    if (!c || !bg || !image) return PULSAR_ERR_ARG;
+    if (c->frame.n > 0 && !features) return PULSAR_ERR_ARG;
+    if (c->stage < 2) return PULSAR_ERR_STATE;
+    DeviceGuard guard(c->device);
+    cudaError_t e = launch_forward(c->frame, c->ws, features, bg, image, 0, as_stream(stream));
+    if (e != cudaSuccess) return PULSAR_ERR_CUDA;
+    c->stage = 3;
+    return PULSAR_OK;
+}
+
+int pulsar_backward(pulsar_ctx_t c, const float* features, const float* bg, const float* image,
+                    const float* grad_image, float* grad_pos, float* grad_radius,
+                    float* grad_opacity, float* grad_features, float* grad_cam, void* stream) {
+    (void)bg;   // the background enters through the forward image only
+    if (!c) return PULSAR_ERR_ARG;
+    if (c->stage < 3) return PULSAR_ERR_STATE;
+    if (!grad_pos && !grad_radius && !grad_opacity && !grad_features && !grad_cam)
+        return PULSAR_OK;   // nothing requested (Pulsar Sec. B.2)
+    if (!image || !grad_image || (c->frame.n > 0 && !features)) return PULSAR_ERR_ARG;
+    DeviceGuard guard(c->device);
+    cudaStream_t s = as_stream(stream);
+    const Frame& f = c->frame;
+    const size_t n = (size_t)f.n;
+    if (grad_opacity && n && cudaMemsetAsync(grad_opacity, 0, n * 4, s) != cudaSuccess)
+        return PULSAR_ERR_CUDA;
+    if (grad_features && n &&
+        cudaMemsetAsync(grad_features, 0, n * (size_t)f.channels * 4, s) != cudaSuccess)
+        return PULSAR_ERR_CUDA;
+    cudaError_t e = launch_backward(f, c->ws, c->pos, features, image, grad_image, grad_pos,
+                                    grad_radius, grad_opacity, grad_features, grad_cam, s);
+    return cuda_err(e);
+}
+
+int pulsar_status(pulsar_ctx_t c, void* stream, int64_t* n_pairs, int64_t* n_hits) {
+    if (!c) return PULSAR_ERR_ARG;
+    DeviceGuard guard(c->device);
+    cudaStream_t s = as_stream(stream);
+    if (cudaMemcpyAsync(c->host_state, c->ws.state, sizeof(DevState), cudaMemcpyDeviceToHost,
+                        s) != cudaSuccess)
+        return PULSAR_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PULSAR_ERR_CUDA;
+    const DevState& h = *c->host_state;
+    if (n_pairs) *n_pairs = (int64_t)h.n_pairs;
+    if (n_hits) *n_hits = (int64_t)h.hits;
+    if (h.error) {
+        const uint32_t zero = 0;
+        cudaMemcpy(&c->ws.state->error, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+        if (h.error & kErrCapacity) return PULSAR_ERR_CAPACITY;
+    }
+    return PULSAR_OK;
+}
+
+int64_t pulsar_debug_copy(pulsar_ctx_t c, int what, void* dst, int64_t bytes, void* stream) {
+    if (!c || bytes < 0) return PULSAR_ERR_ARG;
+    DeviceGuard guard(c->device);
+    cudaStream_t s = as_stream(stream);
+    const Frame& f = c->frame;
+    const int64_t n = f.n, P = (int64_t)f.width * f.height;
+    const void* src = nullptr;
+    int64_t size = 0;
+    switch (what) {
+        case PULSAR_DBG_REC0: src = c->ws.rec0; size = n * 16; break;
+        case PULSAR_DBG_REC1: src = c->ws.rec1; size = n * 16; break;
+        case PULSAR_DBG_REC2: src = c->ws.rec2; size = n * 16; break;
+        case PULSAR_DBG_RECT: src = c->ws.rect; size = n * 8; break;
+        case PULSAR_DBG_TILE_OFFSETS: src = c->ws.tile_start; size = (int64_t)(f.n_tiles + 1) * 4; break;
+        case PULSAR_DBG_TILE_IDS: {
+            uint32_t m = 0;
+            if (cudaMemcpyAsync(&m, &c->ws.state->n_pairs, 4, cudaMemcpyDeviceToHost, s) !=
+                    cudaSuccess ||
+                cudaStreamSynchronize(s) != cudaSuccess)
+                return PULSAR_ERR_CUDA;
+            src = c->ws.tile_ids;
+            size = (int64_t)(m < c->max_pairs ? m : c->max_pairs) * 4;
+            break;
+        }
+        case PULSAR_DBG_MG: src = c->ws.mg; size = P * 4; break;
+        case PULSAR_DBG_WSUM: src = c->ws.wsum; size = P * 4; break;
+        case PULSAR_DBG_IDS: src = c->ws.ids; size = P * f.n_track * 4; break;
+        case PULSAR_DBG_NHITS: src = c->ws.nhits; size = P * 4; break;
+        default: return PULSAR_ERR_ARG;
+    }
+    if (!dst) return size;
+    if (bytes > size) return PULSAR_ERR_ARG;
+    if (bytes == 0) return PULSAR_OK;
+    if (cudaMemcpyAsync(dst, src, (size_t)bytes, cudaMemcpyDefault, s) != cudaSuccess)
+        return PULSAR_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PULSAR_ERR_CUDA;
+    return PULSAR_OK;
+}
+
+}  // extern "C"

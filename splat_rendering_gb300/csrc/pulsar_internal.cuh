@@ -1,0 +1,198 @@
+// Internal definitions shared by the CUDA kernels of the sphere renderer.
+//
+// Decisions (cull, pixel rectangle, tile lists, hit set, tracked ids) are a
+// fixed sequence of correctly rounded fp32 operations written with the
+// explicit round-to-nearest intrinsics (__fadd_rn, __fmul_rn, __fdiv_rn,
+// __fsqrt_rn, __fmaf_rn), which the compiler never contracts or reorders.
+// Values (weights, image, gradients) are ordinary fp32 arithmetic.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pulsar {
+
+constexpr int kTile = 16;           // 16x16 pixel tiles (Pulsar Sec. B.1.2)
+constexpr int kTilePix = kTile * kTile;
+constexpr int kMaxTrack = 16;
+constexpr int kMaxChannels = 64;
+constexpr uint32_t kFlagKeep = 1u, kFlagFloor = 2u, kFlagCut = 4u;
+constexpr float kPi = 3.14159265358979f;
+
+// Device error bits (latched in DevState::error).
+constexpr uint32_t kErrCapacity = 1u;
+
+// Per-frame constants, passed by value to every kernel.
+struct Frame {
+    float R[9], t[3];
+    float fx, fy, cx, cy, znear, zfar;
+    float ifx, ify;       // 1/fx, 1/fy (RN)
+    float fmin;           // min(fx, fy); fx on ties
+    float gamma, inv_gamma, bg_eps, stop_tau, kappa, amin;
+    float inv_zrange;     // 1/(zfar - znear)
+    int width, height, tiles_x, tiles_y, n_tiles;
+    int n_track, channels;
+    int n;
+    uint32_t flags;
+    uint32_t max_pairs;
+};
+
+// Small device-resident counters.
+struct DevState {
+    unsigned long long hits;    // hit pairs composited by the last forward
+    uint32_t n_pairs;           // M of the last bin
+    uint32_t error;             // latched kErr* bits
+    uint32_t ticket;            // last-block election in the finalize kernel
+    uint32_t pad;
+    double cam_acc[16];         // camera gradient accumulators (zero between frames)
+};
+
+// ------------------------------------------------ error-free transforms --
+// TwoProduct via FMA, Knuth's TwoSum, Dekker's FastTwoSum (as used by
+// Ogita, Rump and Oishi for compensated dot products, SIAM J. Sci. Comput.
+// 2005).
+struct FPair { float hi, lo; };
+
+__device__ __forceinline__ FPair ef_prod(float a, float b) {
+    const float p = __fmul_rn(a, b);
+    return {p, __fmaf_rn(a, b, -p)};
+}
+__device__ __forceinline__ FPair ef_sum(float a, float b) {
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    return {s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb))};
+}
+__device__ __forceinline__ FPair ef_fast_sum(float a, float b) {
+    const float s = __fadd_rn(a, b);
+    return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+
+// Row k of c = R p + t as hi + lo: compensated three-term dot product plus t.
+__device__ __forceinline__ FPair camera_row(float r0, float r1, float r2, float tk,
+                                            float px, float py, float pz) {
+    const FPair a = ef_prod(r0, px);
+    const FPair b = ef_prod(r1, py);
+    const FPair s1 = ef_sum(a.hi, b.hi);
+    float err = __fadd_rn(__fadd_rn(a.lo, b.lo), s1.lo);
+    const FPair c = ef_prod(r2, pz);
+    const FPair s2 = ef_sum(s1.hi, c.hi);
+    err = __fadd_rn(__fadd_rn(err, c.lo), s2.lo);
+    const FPair s3 = ef_sum(s2.hi, tk);
+    err = __fadd_rn(err, s3.lo);
+    return ef_sum(s3.hi, err);
+}
+
+// (x.hi + x.lo) / (z.hi + z.lo) as a pair: one Newton correction of the
+// quotient with the exact FMA remainder.
+__device__ __forceinline__ FPair pair_quotient(FPair x, FPair z) {
+    const float q1 = __fdiv_rn(x.hi, z.hi);
+    float rem = __fmaf_rn(-q1, z.hi, x.hi);
+    rem = __fadd_rn(rem, x.lo);
+    rem = __fmaf_rn(-q1, z.lo, rem);
+    return ef_fast_sum(q1, __fdiv_rn(rem, z.hi));
+}
+
+// c0 + f * q as a pair: the projected centre in pixels.
+__device__ __forceinline__ FPair pair_project(float f, float c0, FPair q) {
+    const FPair p = ef_prod(f, q.hi);
+    const float plo = __fmaf_rn(f, q.lo, p.lo);
+    const FPair s = ef_sum(c0, p.hi);
+    return ef_sum(s.hi, __fadd_rn(s.lo, plo));
+}
+
+// Pixel range [lo, hi] along one image axis (n pixels) covered by the tangent
+// cone of a sphere with centre coordinate X along the axis, depth Z and
+// radius rr: the two tangent directions in the (axis, z) plane,
+// u = c0 + f (X L +- rr Z) / (Z L -+ X rr), L = sqrt(X^2 + Z^2 - rr^2)
+// (the tan(a +- b) identity; Pulsar Sec. B.1.1 avoids trigonometry).
+// Returns false if the range is empty.
+__device__ __forceinline__ bool tangent_range(float X, float Z, float rr, float f, float c0,
+                                              int n, int* lo, int* hi) {
+    const float L = __fsqrt_rn(__fsub_rn(__fadd_rn(__fmul_rn(X, X), __fmul_rn(Z, Z)),
+                                         __fmul_rn(rr, rr)));
+    const float zl = __fmul_rn(Z, L), xr = __fmul_rn(X, rr);
+    const float xl = __fmul_rn(X, L), rz = __fmul_rn(rr, Z);
+    const float dhi = __fsub_rn(zl, xr);
+    const float dlo = __fadd_rn(zl, xr);
+    const float uhi = dhi > 0.0f ? __fadd_rn(c0, __fmul_rn(f, __fdiv_rn(__fadd_rn(xl, rz), dhi)))
+                                 : __int_as_float(0x7f800000);
+    const float ulo = dlo > 0.0f ? __fadd_rn(c0, __fmul_rn(f, __fdiv_rn(__fsub_rn(xl, rz), dlo)))
+                                 : __int_as_float(0xff800000);
+    float a = ceilf(__fsub_rn(ulo, 0.5f));
+    float b = floorf(__fsub_rn(uhi, 0.5f));
+    const float top = (float)(n - 1);
+    a = a < 0.0f ? 0.0f : a;
+    b = b > top ? top : b;
+    if (!(a <= b)) return false;
+    *lo = (int)a;
+    *hi = (int)b;
+    return true;
+}
+
+// Per-pixel ray constants of the decision path.
+struct PixelRay {
+    float px, py;   // pixel centre
+    float a, b;     // ray slopes (px - cx)/fx, (py - cy)/fy
+    float qq;       // 1 + a^2 + b^2
+};
+
+__device__ __forceinline__ PixelRay pixel_ray(int x, int y, const Frame& f) {
+    PixelRay r;
+    r.px = __fadd_rn(__int2float_rn(x), 0.5f);
+    r.py = __fadd_rn(__int2float_rn(y), 0.5f);
+    r.a = __fdiv_rn(__fsub_rn(r.px, f.cx), f.fx);
+    r.b = __fdiv_rn(__fsub_rn(r.py, f.cy), f.fy);
+    r.qq = __fadd_rn(__fadd_rn(1.0f, __fmul_rn(r.a, r.a)), __fmul_rn(r.b, r.b));
+    return r;
+}
+
+// Q = (rho / c.z)^2 * qq evaluated from pixel offsets to the projected centre
+// (u_hi + u_lo, v_hi + v_lo); also returns the slopes U, V of the offset.
+__device__ __forceinline__ float ray_offset_q(const float4& uv, const PixelRay& r, float ifx,
+                                              float ify, float* U, float* V) {
+    const float du = __fsub_rn(__fsub_rn(r.px, uv.x), uv.y);
+    const float dv = __fsub_rn(__fsub_rn(r.py, uv.z), uv.w);
+    *U = __fmul_rn(du, ifx);
+    *V = __fmul_rn(dv, ify);
+    const float X = __fmaf_rn(*U, r.b, -__fmul_rn(*V, r.a));
+    return __fmaf_rn(*U, *U, __fmaf_rn(*V, *V, __fmul_rn(X, X)));
+}
+
+__device__ __forceinline__ bool rect_contains(uint2 rc, int x, int y) {
+    return x >= (int)(rc.x & 0xffffu) && x <= (int)(rc.x >> 16) && y >= (int)(rc.y & 0xffffu) &&
+           y <= (int)(rc.y >> 16);
+}
+
+// ---------------------------------------------------------- workspace --
+struct Workspace {
+    float4* rec0;      // [maxN] u_hi, u_lo, v_hi, v_lo
+    float4* rec1;      // [maxN] s2, c.z/r_eff, o, o*z~/gamma
+    float4* rec2;      // [maxN] c.z, r_eff, key, flags
+    uint2* rect;       // [maxN] pixel rectangle (x0 | x1<<16, y0 | y1<<16)
+    float4* gacc;      // [maxN] dL/dc.xyz, dL/dr accumulators (zero between frames)
+    uint32_t* tile_count;   // [maxB] (zero between frames)
+    uint32_t* tile_start;   // [maxB+1]
+    unsigned long long* pairs;      // [max_pairs] (key bits << 32 | id), bucketed by tile
+    unsigned long long* pairs_alt;  // [max_pairs] merge scratch for long tiles
+    uint32_t* tile_ids;     // [max_pairs] sorted tile lists
+    float* mg;              // [maxP]
+    float* wsum;            // [maxP]
+    int32_t* ids;           // [maxT][maxP]
+    int32_t* nhits;         // [maxP]
+    DevState* state;
+};
+
+// ---------------------------------------------------------- launchers --
+// (defined in the .cu files; all enqueue on `stream` and never synchronise)
+cudaError_t launch_project(const Frame& f, const Workspace& w, const float* pos,
+                           const float* radius, const float* opacity, cudaStream_t stream);
+cudaError_t launch_bin(const Frame& f, const Workspace& w, cudaStream_t stream);
+cudaError_t launch_forward(const Frame& f, const Workspace& w, const float* features,
+                           const float* bg, float* image, int max_pairs_stride,
+                           cudaStream_t stream);
+cudaError_t launch_backward(const Frame& f, const Workspace& w, const float* pos,
+                            const float* features, const float* image, const float* grad_image,
+                            float* grad_pos, float* grad_radius, float* grad_opacity,
+                            float* grad_features, float* grad_cam, cudaStream_t stream);
+
+}  // namespace pulsar

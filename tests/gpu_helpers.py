@@ -1,0 +1,128 @@
+"""Run the CUDA path through the C ABI and compare it with the oracle (tests only)."""
+from __future__ import annotations
+
+from dataclasses import replace
+
+import numpy as np
+
+# tolerances: forward 1e-5 relative / 1e-6 absolute, gradients 1e-4 / 1e-5
+FWD_RTOL, FWD_ATOL = 1e-5, 1e-6
+GRAD_RTOL, GRAD_ATOL = 1e-4, 1e-5
+
+
+def _t(a, dev="cuda"):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev)
+
+
+def run_gpu(scene, cam_index=0, grad_image=None, max_pairs=None, count_hits=True, want=None,
+            prm=None, renderer=None, debug=True):
+    """Render (and differentiate) one camera of `scene` on cuda:0.  Returns a
+    dict of numpy arrays: image, grads, and the debug arrays."""
+    import torch
+    from splat_rendering_gb300 import pulsar as pl
+
+    cam = scene.cameras[cam_index]
+    p = scene.params if prm is None else prm
+    n = scene.n
+    if max_pairs is None:
+        max_pairs = max(1 << 16, 16 * n)
+    r = renderer or pl.Renderer(max_spheres=max(n, 1), max_pairs=max_pairs, max_width=cam.width,
+                                max_height=cam.height, max_channels=p.channels,
+                                max_track=max(p.n_track, 1))
+    pos, rad, opa, feat = (_t(scene.pos.reshape(-1, 3)), _t(scene.radius), _t(scene.opacity),
+                           _t(scene.features.reshape(n, p.channels)))
+    bg = _t(scene.bg)
+    c, q = pl.camera(cam), pl.params(p, count_hits=count_hits)
+    img = r.render(pos, rad, opa, feat, c, q, bg)
+    out = {}
+    G = scene.grad_images[cam_index] if grad_image is None else grad_image
+    if want is not False:
+        grads = r.backward(_t(G), want=want or ("pos", "radius", "opacity", "features", "cam"))
+        out.update({f"grad_{k}": v.cpu().numpy() for k, v in grads.items()})
+    code, m, h = r.status(raise_on_error=False)
+    torch.cuda.synchronize()
+    out.update(code=code, n_pairs=m, hits=h, image=img.cpu().numpy())
+    if debug and code == 0:
+        P = cam.width * cam.height
+        out["rec0"] = r.debug("rec0").view(np.float32).reshape(n, 4) if n else np.zeros((0, 4), np.float32)
+        out["rec1"] = r.debug("rec1").view(np.float32).reshape(n, 4) if n else np.zeros((0, 4), np.float32)
+        out["rec2"] = r.debug("rec2").view(np.float32).reshape(n, 4) if n else np.zeros((0, 4), np.float32)
+        out["rect"] = r.debug("rect").view(np.uint32).reshape(n, 2) if n else np.zeros((0, 2), np.uint32)
+        out["tile_offsets"] = r.debug("tile_offsets").view(np.uint32)
+        out["tile_ids"] = r.debug("tile_ids").view(np.uint32)[:m] if m else np.zeros(0, np.uint32)
+        out["mg"] = r.debug("mg").view(np.float32).reshape(cam.height, cam.width)
+        out["wsum"] = r.debug("wsum").view(np.float32).reshape(cam.height, cam.width)
+        ids = r.debug("ids").view(np.int32).reshape(p.n_track, cam.height, cam.width)
+        out["ids"] = np.moveaxis(ids, 0, -1)
+        if count_hits:
+            out["nhits"] = r.debug("nhits").view(np.int32).reshape(cam.height, cam.width)
+        del P
+    out["renderer"] = r
+    return out
+
+
+def close_report(gpu, ref, rtol, atol):
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    err = np.abs(gpu - ref)
+    bound = atol + rtol * np.abs(ref)
+    bad = err > bound
+    worst = float((err / bound).max()) if err.size else 0.0
+    return int(bad.sum()), worst
+
+
+def assert_close(gpu, ref, rtol, atol, what):
+    nbad, worst = close_report(gpu, ref, rtol, atol)
+    assert nbad == 0, f"{what}: {nbad} of {np.size(ref)} outside tolerance (worst {worst:.3g}x bound)"
+
+
+def assert_decisions_equal(g, d):
+    """Per-sphere fp32 decision quantities bit for bit (oracle.project output d)."""
+    keep = (g["rec2"][:, 3].view(np.uint32) & 1).astype(bool)
+    assert np.array_equal(keep, d["keep"] == 1), "keep flags differ"
+    k = keep
+    assert np.array_equal(g["rec0"][k].view(np.uint32), d["uv"][k].view(np.uint32)), "centre pair"
+    assert np.array_equal(g["rec2"][k, 1].view(np.uint32), d["reff"][k].view(np.uint32)), "r_eff"
+    assert np.array_equal(g["rec2"][k, 2].view(np.uint32), d["key"][k].view(np.uint32)), "key"
+    assert np.array_equal(g["rec1"][k, 0].view(np.uint32), d["s2"][k].view(np.uint32)), "s2"
+    fl = g["rec2"][:, 3].view(np.uint32)
+    assert np.array_equal(((fl >> 1) & 1)[k], d["floor"][k]), "floor flags"
+    assert np.array_equal(((fl >> 2) & 1)[k], d["cut"][k]), "cutoff flags"
+    rect = g["rect"][k]
+    got = np.stack([rect[:, 0] & 0xffff, rect[:, 0] >> 16, rect[:, 1] & 0xffff, rect[:, 1] >> 16], 1)
+    assert np.array_equal(got.astype(np.int64), d["rect"][k].astype(np.int64)), "rectangles"
+
+
+def compare_frame(g, o, what="", window=None, grads=True):
+    """Image, buffer and (optionally) gradients of a GPU frame vs the oracle."""
+    if window is None:
+        sl = (slice(None), slice(None))
+    else:
+        x0, y0, x1, y1 = window
+        sl = (slice(y0, y1), slice(x0, x1))
+    assert np.array_equal(g["ids"][sl], o["ids"]), f"{what}: tracked ids differ"
+    if "nhits" in g:
+        assert np.array_equal(g["nhits"][sl], o["nhits"]), f"{what}: hit counts differ"
+    assert_close(g["image"][sl], o["image"], FWD_RTOL, FWD_ATOL, f"{what} image")
+    assert_close(g["mg"][sl], o["mg"], FWD_RTOL, FWD_ATOL, f"{what} stabiliser")
+    # normaliser compared in one frame: W exp(mg)
+    wg = g["wsum"][sl].astype(np.float64) * np.exp(g["mg"][sl].astype(np.float64) - o["mg"])
+    assert_close(wg, o["wsum"], FWD_RTOL, 0.0, f"{what} normaliser")
+    if grads:
+        for k in ("grad_pos", "grad_radius", "grad_opacity", "grad_features", "grad_cam"):
+            if k in g:
+                assert_close(g[k], o[k], GRAD_RTOL, GRAD_ATOL, f"{what} {k}")
+
+
+def windowed_grad(scene, cam_index, window):
+    """Upstream gradient that is zero outside the pixel window, so full-frame
+    gradients equal the window's."""
+    G = np.zeros_like(scene.grad_images[cam_index])
+    x0, y0, x1, y1 = window
+    G[y0:y1, x0:x1] = scene.grad_images[cam_index][y0:y1, x0:x1]
+    return G
+
+
+def with_params(scene, **kw):
+    return replace(scene, params=replace(scene.params, **kw))

@@ -1,0 +1,228 @@
+"""CUDA path vs the CPU oracle, through the C ABI, on seeded inputs.
+
+Bit-exact: per-sphere fp32 decisions, tile lists, tracked ids, hit counts.
+Within tolerance: image, stabiliser and normaliser (1e-5 relative / 1e-6
+absolute), gradients (1e-4 relative / 1e-5 absolute).
+"""
+from __future__ import annotations
+
+from dataclasses import replace
+
+import numpy as np
+import pytest
+
+import gpu_helpers as gh
+from splat_rendering_gb300 import scenes
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_all(oracle_lib, sc, cam_index=0, window=None, grad_image=None):
+    cam = sc.cameras[cam_index]
+    G = sc.grad_images[cam_index] if grad_image is None else grad_image
+    o = oracle_lib.render(sc.pos, sc.radius, sc.opacity, sc.features, cam, sc.params, sc.bg,
+                          grad_image=G, window=window)
+    d = oracle_lib.project(sc.pos, sc.radius, sc.opacity, cam, sc.params)
+    offs, ids = oracle_lib.tile_lists(sc.pos, sc.radius, sc.opacity, cam, sc.params)
+    return o, d, offs, ids
+
+
+def _check_lists(g, offs, ids):
+    assert np.array_equal(g["tile_offsets"].astype(np.int64), offs), "tile offsets differ"
+    assert np.array_equal(g["tile_ids"].astype(np.int64), ids.astype(np.int64)), "tile lists differ"
+
+
+@pytest.mark.parametrize("name", ["tiny", "medium", "headline", "neural"])
+def test_config_full_frame(oracle_lib, name):
+    sc = scenes.make(name)
+    o, d, offs, ids = _oracle_all(oracle_lib, sc)
+    g = gh.run_gpu(sc, max_pairs=len(ids) + 1024)
+    assert g["code"] == 0
+    assert g["n_pairs"] == len(ids)
+    assert g["hits"] == o["hits"]
+    gh.assert_decisions_equal(g, d)
+    _check_lists(g, offs, ids)
+    gh.compare_frame(g, o, name)
+
+
+@pytest.mark.parametrize("cam_index", range(6))
+def test_driving_cameras(oracle_lib, cam_index):
+    """Driving rig: full-frame decisions and tile lists; image and gradients on
+    a 320x192 window (the upstream gradient is zero outside it)."""
+    sc = scenes.driving()
+    cam = sc.cameras[cam_index]
+    win = (800, 560, 1120, 752)
+    G = gh.windowed_grad(sc, cam_index, win)
+    d = oracle_lib.project(sc.pos, sc.radius, sc.opacity, cam, sc.params)
+    offs, ids = oracle_lib.tile_lists(sc.pos, sc.radius, sc.opacity, cam, sc.params)
+    o = oracle_lib.render(sc.pos, sc.radius, sc.opacity, sc.features, cam, sc.params, sc.bg,
+                          grad_image=G, window=win)
+    g = gh.run_gpu(sc, cam_index, grad_image=G, max_pairs=len(ids) + 1024)
+    assert g["code"] == 0 and g["n_pairs"] == len(ids)
+    gh.assert_decisions_equal(g, d)
+    _check_lists(g, offs, ids)
+    gh.compare_frame(g, o, f"driving cam{cam_index}", window=win)
+
+
+EDGE = {
+    # ragged image, rotated and translated camera, fx != fy, off-centre principal point
+    "ragged": dict(seed=51, n=300, width=37, height=23, rot_deg=15, shift=(0.2, -0.1, 0.3),
+                   f=30.0, fy=41.0, cx=15.3, cy=9.1, rrange=(0.01, 0.3)),
+    "one_channel": dict(seed=52, n=400, width=48, height=40, channels=1, n_track=1),
+    "wide_payload": dict(seed=53, n=300, width=40, height=33, channels=33, n_track=16),
+    "five_channels": dict(seed=54, n=300, width=50, height=30, channels=5, n_track=9),
+    "no_cutoff": dict(seed=55, n=500, width=64, height=48, geom_cutoff=False, rrange=(0.005, 0.2)),
+    # big spheres: tile lists longer than one shared-memory sort (merge path)
+    "long_lists": dict(seed=56, n=6000, width=64, height=64, f=64.0, zrange=(2.5, 6.5),
+                       rrange=(0.3, 1.0), spread=1.5),
+    "spill_outside": dict(seed=57, n=2000, width=80, height=60, spread=2.5, rrange=(0.01, 0.5)),
+}
+
+
+@pytest.mark.parametrize("case", sorted(EDGE))
+def test_edge_cases(oracle_lib, case):
+    sc = scenes.random_scene(**EDGE[case])
+    o, d, offs, ids = _oracle_all(oracle_lib, sc)
+    g = gh.run_gpu(sc, max_pairs=len(ids) + 64)
+    assert g["code"] == 0
+    gh.assert_decisions_equal(g, d)
+    _check_lists(g, offs, ids)
+    gh.compare_frame(g, o, case)
+    if case == "long_lists":
+        assert np.diff(offs).max() > 2048
+
+
+def test_zero_opacity_spheres(oracle_lib):
+    sc = scenes.random_scene(58, 400, 48, 48, rrange=(0.02, 0.3))
+    sc.opacity[::3] = 0.0
+    o, d, offs, ids = _oracle_all(oracle_lib, sc)
+    g = gh.run_gpu(sc)
+    gh.assert_decisions_equal(g, d)
+    gh.compare_frame(g, o, "zero opacity")
+
+
+def test_empty_scene(oracle_lib):
+    sc = scenes.random_scene(1, 0, 33, 17)
+    sc.bg[:] = [0.5, -2.0, 1.25]
+    g = gh.run_gpu(sc)
+    assert g["code"] == 0 and g["n_pairs"] == 0 and g["hits"] == 0
+    assert np.array_equal(g["image"], np.broadcast_to(sc.bg, g["image"].shape))
+    assert (g["ids"] == -1).all()
+    assert not g["grad_cam"].any()
+
+
+def test_everything_culled(oracle_lib):
+    sc = scenes.random_scene(2, 500, 40, 40)
+    sc.pos[:, 2] *= -1.0
+    g = gh.run_gpu(sc)
+    assert g["code"] == 0 and g["n_pairs"] == 0 and g["hits"] == 0
+    assert not g["grad_pos"].any() and not g["grad_cam"].any()
+
+
+def test_early_stop_bound(oracle_lib):
+    """With a small gamma the forward stops early once n_track hits are tracked;
+    the image stays within tau * max|f - F| (plus fp32 rounding of the
+    exponent, 2^-24 * 8 / gamma) of the exact blend and the tracked ids equal
+    the oracle's (Pulsar Sec. 3.2, B.1.3)."""
+    sc = scenes.random_scene(60, 20000, 48, 48, rrange=(0.05, 0.4), zrange=(2, 6),
+                             gamma=0.01, n_track=2)
+    sc.params.stop_tau = 1e-4
+    o = oracle_lib.render(sc.pos, sc.radius, sc.opacity, sc.features, sc.cameras[0], sc.params,
+                          sc.bg)
+    g = gh.run_gpu(sc, want=False)
+    assert np.array_equal(g["ids"], o["ids"])
+    assert (g["nhits"] < o["nhits"]).any(), "early stop never triggered"
+    spread = np.abs(sc.features).max() + np.abs(o["image"]).max()
+    tol = 1e-4 * spread + 2.0 ** -24 * 8 / 0.01 * spread + 1e-6
+    assert np.abs(g["image"] - o["image"]).max() <= tol
+
+
+def test_capacity_overflow_and_recovery(oracle_lib):
+    """Too many sphere-tile pairs: the frame reports PULSAR_ERR_CAPACITY without
+    faulting; the same context then renders a fitting frame correctly."""
+    from splat_rendering_gb300 import pulsar as pl
+    big = scenes.random_scene(61, 3000, 64, 64, rrange=(0.1, 0.6))
+    offs, ids = oracle_lib.tile_lists(big.pos, big.radius, big.opacity, big.cameras[0], big.params)
+    r = pl.Renderer(max_spheres=3000, max_pairs=len(ids) // 2, max_width=64, max_height=64,
+                    max_channels=3, max_track=5)
+    g = gh.run_gpu(big, renderer=r, want=False, debug=False)
+    assert g["code"] == pl.ERR_CAPACITY
+    small = scenes.random_scene(62, 200, 64, 64, rrange=(0.01, 0.1))
+    o, d, offs2, ids2 = _oracle_all(oracle_lib, small)
+    assert len(ids2) <= len(ids) // 2
+    g2 = gh.run_gpu(small, renderer=r)
+    assert g2["code"] == 0
+    _check_lists(g2, offs2, ids2)
+    gh.compare_frame(g2, o, "after overflow")
+
+
+def test_call_order_and_arguments():
+    import torch
+    from splat_rendering_gb300 import pulsar as pl
+    r = pl.Renderer(max_spheres=10, max_pairs=100, max_width=16, max_height=16)
+    img = torch.zeros((16, 16, 3), device="cuda")
+    bg = torch.zeros(3, device="cuda")
+    with pytest.raises(pl.PulsarError) as e:
+        pl.forward(r.ctx, None, bg, img)
+    assert e.value.code == pl.ERR_STATE
+    with pytest.raises(pl.PulsarError) as e:
+        pl.bin(r.ctx)
+    assert e.value.code == pl.ERR_STATE
+    sc = scenes.random_scene(3, 10, 16, 16)
+    cam, prm = pl.camera(sc.cameras[0]), pl.params(sc.params)
+    pos = torch.from_numpy(sc.pos).cuda()
+    rad = torch.from_numpy(sc.radius).cuda()
+    opa = torch.from_numpy(sc.opacity).cuda()
+    with pytest.raises(pl.PulsarError) as e:
+        pl.project(r.ctx, pos, rad, opa, 11, cam, prm)   # above max_spheres
+    assert e.value.code == pl.ERR_ARG
+    big = pl.camera(replace(sc.cameras[0], width=17))
+    with pytest.raises(pl.PulsarError) as e:
+        pl.project(r.ctx, pos, rad, opa, 10, big, prm)
+    assert e.value.code == pl.ERR_ARG
+    bad = pl.params(sc.params)
+    bad.n_track = 9
+    with pytest.raises(pl.PulsarError) as e:
+        pl.project(r.ctx, pos, rad, opa, 10, cam, bad)
+    assert e.value.code == pl.ERR_ARG
+    pl.project(r.ctx, pos, rad, opa, 10, cam, prm)
+    with pytest.raises(pl.PulsarError) as e:
+        pl.backward(r.ctx, None, bg, img, img, grad_cam=torch.zeros(16, device="cuda"))
+    assert e.value.code == pl.ERR_STATE
+    pl.bin(r.ctx)
+    with pytest.raises(pl.PulsarError) as e:
+        pl.bin(r.ctx)
+    assert e.value.code == pl.ERR_STATE
+    assert r.status()[0] == 0
+
+
+def test_partial_gradient_requests(oracle_lib):
+    """Only the requested gradients are written (Pulsar Sec. B.2)."""
+    sc = scenes.random_scene(63, 500, 48, 40, rrange=(0.02, 0.3))
+    o, _, _, _ = _oracle_all(oracle_lib, sc)
+    g = gh.run_gpu(sc, want=("opacity",))
+    assert set(k for k in g if k.startswith("grad_")) == {"grad_opacity"}
+    gh.assert_close(g["grad_opacity"], o["grad_opacity"], gh.GRAD_RTOL, gh.GRAD_ATOL, "opacity")
+    g = gh.run_gpu(sc, want=("cam", "features"))
+    gh.assert_close(g["grad_cam"], o["grad_cam"], gh.GRAD_RTOL, gh.GRAD_ATOL, "cam")
+    gh.assert_close(g["grad_features"], o["grad_features"], gh.GRAD_RTOL, gh.GRAD_ATOL, "feat")
+
+
+def test_repeat_frames_and_determinism(oracle_lib):
+    """One context, frames of different scenes and cameras in a row: the
+    zero-between-frames workspace invariants hold, and repeating a frame
+    reproduces lists and image bit for bit."""
+    from splat_rendering_gb300 import pulsar as pl
+    r = pl.Renderer(max_spheres=5000, max_pairs=200000, max_width=96, max_height=80,
+                    max_channels=4, max_track=8)
+    a = scenes.random_scene(64, 3000, 96, 80, rrange=(0.01, 0.2), rot_deg=5)
+    b = scenes.random_scene(65, 1000, 70, 50, channels=4, n_track=8, rrange=(0.02, 0.3))
+    ga1 = gh.run_gpu(a, renderer=r)
+    gb = gh.run_gpu(b, renderer=r)
+    ga2 = gh.run_gpu(a, renderer=r)
+    for k in ("tile_ids", "tile_offsets", "ids", "image", "mg", "wsum"):
+        assert np.array_equal(ga1[k], ga2[k]), k
+    for k in ("grad_pos", "grad_opacity", "grad_cam"):
+        gh.assert_close(ga2[k], ga1[k], 1e-5, 1e-6, k)
+    o, _, _, _ = _oracle_all(oracle_lib, b)
+    gh.compare_frame(gb, o, "second scene")
