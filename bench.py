@@ -1,0 +1,411 @@
+#!/usr/bin/env python
+"""Benchmark of the tile-based differentiable sphere renderer on one GB300.
+
+Metric: forward + backward frames/s (and Msphere-pixel/s = hit pairs / time)
+on the 1,000,000-sphere 1024x1024 scene (3 channels, n_track 5, camera R/t/K
+gradients) -- the scale of the Pulsar paper's 1M-sphere timings (Sec. 1,
+Table 2).  One step = project -> bin -> forward -> backward (all kernels of
+the path) over one frame, replayed from a CUDA graph, inputs resident in HBM,
+L2 flushed between steps by a 256 MB write.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+With N > 1 (torchrun) every rank renders its own frame: replicas, weak
+scaling, no collective on the data path.  `--impl reference` times the CPU
+oracle (fp64, all host cores) on a bounded sample of the same frame.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "headline: 1,000,000 spheres, 1024x1024, 3 channels, n_track 5, R/t/K gradients"
+METRIC = "fwd+bwd frames/s at 1M spheres 1024^2"
+UNIT = "frames/s"
+KERNELS_PER_STEP = 7   # project, tile_scan, emit, tile_sort, forward, backward, finalize
+
+
+def args_parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ------------------------------------------------------------------ clocks --
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.dev)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        self.p.terminate()
+        try:
+            out, _ = self.p.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+            out, _ = self.p.communicate()
+        sm, mx, reasons = [], 0.0, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# -------------------------------------------------------------- roofline --
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "sm_max_mhz": 2070.0}, "fallback"
+
+
+def algorithmic_bytes(stage, N, M, P, C, T, Ht):
+    """Compulsory bytes of one launch of each stage (each array moved once).
+    N spheres, M sphere-tile pairs, P pixels, C channels, T tracked hits per
+    pixel, Ht tracked hit pairs."""
+    if stage == "project":
+        return 20 * N + 60 * N
+    if stage == "bin":
+        return 8 * N + 12 * M + 8 * M + 4 * M
+    if stage == "forward":
+        return (4 + 44 + 4 * C) * M + (4 * C + 8 + 4 * T) * P
+    if stage == "backward":
+        return 8 * C * P + (8 + 4 * T) * P + (52 + 4 * C) * Ht + (16 + 16 + 4 + 4 * C) * N + 12 * N
+    raise KeyError(stage)
+
+
+def traffic_from_profile(kernel_file: str, workload: str):
+    """DRAM bytes per launch recorded by the committed ncu summary, if it was
+    taken on the current source of the kernel; else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_file}_{workload}.txt")
+    src = os.path.join(ROOT, "splat_rendering_gb300", "csrc")
+    try:
+        with open(path) as f:
+            kv = dict(l.split(":", 1) for l in f.read().splitlines() if ":" in l)
+        h = hashlib.sha256()
+        for name in ("pulsar_internal.cuh", f"{kernel_file}.cu"):
+            with open(os.path.join(src, name), "rb") as g:
+                h.update(g.read())
+        if kv.get("source_sha256", "").strip() != h.hexdigest():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------- reference --
+def oracle_sample(scene, target_s: float, rows: int | None = None):
+    """Time the CPU oracle on a band of rows of the frame (forward + backward).
+    With rows=None the band grows until it takes about target_s.
+    Returns (frames/s extrapolated by the pixel fraction, rows, seconds, cores)."""
+    import numpy as np
+    import oracle
+    cam = scene.cameras[0]
+    fixed = rows is not None
+    rows = rows or 16
+    while True:
+        win = (0, 0, cam.width, rows)
+        G = np.zeros_like(scene.grad_images[0])
+        G[:rows] = scene.grad_images[0][:rows]
+        t0 = time.perf_counter()
+        oracle.render(scene.pos, scene.radius, scene.opacity, scene.features, cam, scene.params,
+                      scene.bg, grad_image=G, window=win)
+        dt = time.perf_counter() - t0
+        if fixed or dt >= 0.5 * target_s or rows >= cam.height:
+            break
+        rows = min(cam.height, max(rows * 2, int(rows * 0.6 * target_s / max(dt, 1e-3))))
+    frac = rows / cam.height
+    return frac / dt, rows, dt, oracle.num_threads()
+
+
+def run_reference(a):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from splat_rendering_gb300 import scenes
+    scene = scenes.headline()
+    vals = []
+    per_step = max(1.0, a.cpu_seconds / max(1, a.steps))
+    rows = None
+    for i in range(a.warmup + a.steps):
+        v, rows, dt, cores = oracle_sample(scene, per_step, rows)
+        if i >= a.warmup:
+            vals.append(v)
+    value = statistics.median(vals)
+    sample = (f"oracle fp64 fwd+bwd on rows [0,{rows}) x 1024 of the headline frame, "
+              f"scaled by the pixel fraction {rows}/1024")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
+            "ms_per_step": 1e3 / value, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "parallelism": "replicas"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- gb300 --
+def run_gb300(a):
+    import numpy as np
+    import torch
+
+    from splat_rendering_gb300 import build as pbuild
+    from splat_rendering_gb300 import pulsar as pl
+    from splat_rendering_gb300 import scenes
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    pbuild.build()
+    pl.load()
+    dev = torch.device("cuda", local)
+
+    scene = scenes.headline()
+    cam, prm = scene.cameras[0], scene.params
+    N, C, T = scene.n, prm.channels, prm.n_track
+    P = cam.width * cam.height
+
+    def dev_t(x):
+        return torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+
+    pos, rad, opa, feat = dev_t(scene.pos), dev_t(scene.radius), dev_t(scene.opacity), \
+        dev_t(scene.features)
+    bg, G = dev_t(scene.bg), dev_t(scene.grad_images[0])
+    c_cam, c_prm = pl.camera(cam), pl.params(prm)
+    image = torch.empty((cam.height, cam.width, C), device=dev)
+    grads = {"pos": torch.empty((N, 3), device=dev), "radius": torch.empty(N, device=dev),
+             "opacity": torch.empty(N, device=dev), "features": torch.empty((N, C), device=dev),
+             "cam": torch.empty(16, device=dev)}
+    cap = 4 * N
+    r = pl.Renderer(max_spheres=N, max_pairs=cap, max_width=cam.width, max_height=cam.height,
+                    max_channels=C, max_track=T, device=local)
+
+    def step():
+        r.render(pos, rad, opa, feat, c_cam, c_prm, bg, image=image)
+        r.backward(G, out=grads)
+
+    step()
+    code, M, H = r.status(raise_on_error=False)
+    if code == pl.ERR_CAPACITY:
+        r.close()
+        r = pl.Renderer(max_spheres=N, max_pairs=2 * M, max_width=cam.width,
+                        max_height=cam.height, max_channels=C, max_track=T, device=local)
+        step()
+        code, M, H = r.status()
+    assert code == 0, pl.strerror(code)
+    ids = torch.from_numpy(r.debug("ids").view(np.int32))
+    Ht = int((ids >= 0).sum())
+
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.int32, device=dev)   # 256 MB > L2
+
+    # ---- CUDA graph of one step
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(2):
+            step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    torch.cuda.synchronize()
+
+    for _ in range(a.warmup):
+        flush.zero_()
+        graph.replay()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(a.steps)]
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record()
+        graph.replay()
+        e1.record()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    total_ms = sum(step_ms)
+    if dist:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+        dist.barrier()
+
+    # ---- per-stage breakdown (same kernels, eager, events between ABI calls)
+    stages = ("project", "bin", "forward", "backward")
+    per = {k: [] for k in stages}
+    for _ in range(a.steps):
+        flush.zero_()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        ev[0].record()
+        pl.project(r.ctx, pos, rad, opa, N, c_cam, c_prm)
+        ev[1].record()
+        pl.bin(r.ctx)
+        ev[2].record()
+        pl.forward(r.ctx, feat, bg, image)
+        ev[3].record()
+        pl.backward(r.ctx, feat, bg, image, G, grads["pos"], grads["radius"], grads["opacity"],
+                    grads["features"], grads["cam"])
+        ev[4].record()
+        torch.cuda.synchronize()
+        for i, k in enumerate(stages):
+            per[k].append(ev[i].elapsed_time(ev[i + 1]))
+    clk = clocks.stop()
+    breakdown = {k: statistics.median(v) for k, v in per.items()}
+
+    # ---- end to end through the API with host buffers (pinned), copies timed
+    host_in = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in
+               (("pos", scene.pos), ("radius", scene.radius), ("opacity", scene.opacity),
+                ("features", scene.features), ("G", scene.grad_images[0]))}
+    host_out = {"image": torch.empty(image.shape).pin_memory()}
+    for k, v in grads.items():
+        host_out[k] = torch.empty(v.shape).pin_memory()
+    d_in = {k: torch.empty(v.shape, device=dev) for k, v in host_in.items()}
+    h2d = sum(v.numel() * 4 for v in host_in.values())
+    d2h = sum(v.numel() * 4 for v in host_out.values())
+
+    def e2e_step():
+        for k, v in host_in.items():
+            d_in[k].copy_(v, non_blocking=True)
+        r.render(d_in["pos"], d_in["radius"], d_in["opacity"], d_in["features"], c_cam, c_prm,
+                 bg, image=image)
+        r.backward(d_in["G"], out=grads)
+        host_out["image"].copy_(image, non_blocking=True)
+        for k, v in grads.items():
+            host_out[k].copy_(v, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for _ in range(a.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        e2e_step()
+        e1.record()
+        torch.cuda.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+    e2e_total = sum(e2e_ms)
+    if dist:
+        tt = torch.tensor([e2e_total], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_total = float(tt.item())
+
+    # ---- roofline of the dominant single-kernel stage
+    peaks, peak_src = measured_peaks()
+    dom = max(("project", "forward"), key=lambda k: breakdown[k])
+    dom_bytes = algorithmic_bytes(dom, N, M, P, C, T, Ht)
+    achieved = dom_bytes / (breakdown[dom] * 1e-3) / 1e9
+    peak = float(peaks["hbm_gbs"])
+    traffic = traffic_from_profile(dom, "headline")
+    roofline = {"bound": "hbm", "kernel": f"k_{dom}", "achieved": achieved, "peak": peak,
+                "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                "algorithmic_bytes": dom_bytes, "peak_source": f"{peak_src} hbm_gbs"}
+    path_bytes = sum(algorithmic_bytes(k, N, M, P, C, T, Ht) for k in stages)
+
+    value = world * a.steps / (total_ms * 1e-3)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": total_ms / a.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}",
+                       "l2": "flushed between steps (256 MB write, outside the timed events)",
+                       "timing": "CUDA events around a CUDA-graph replay of one step"},
+            "msphere_pixel_per_s": world * H / (total_ms / a.steps * 1e-3) / 1e6,
+            "hits_per_frame": H, "pairs_per_frame": M, "tracked_hits_per_frame": Ht,
+            "breakdown_ms": breakdown,
+            "path_roofline": {"algorithmic_bytes": path_bytes,
+                              "hbm_time_ms": path_bytes / (peak * 1e9) * 1e3,
+                              "frac_of_step": path_bytes / (peak * 1e9) * 1e3 /
+                              (total_ms / a.steps)},
+            "roofline": roofline,
+            "e2e": {"value": world * a.steps / (e2e_total * 1e-3), "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": KERNELS_PER_STEP * a.steps,
+            "clocks": clk, "wall_s_timed": t_wall}
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        v, rows, dt, cores = oracle_sample(scene, a.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": f"fp64 oracle fwd+bwd on rows [0,{rows}) x 1024 of "
+                                          f"the same frame ({dt:.1f} s), scaled by {rows}/1024"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    r.close()
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    a = args_parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_gb300(a)
+
+
+if __name__ == "__main__":
+    main()

@@ -79,14 +79,14 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
             const float4 uv = w.rec0[id];
             const float4 r1 = w.rec1[id];
             const float4 r2 = w.rec2[id];
-            const uint32_t fl = __float_as_uint(r2.w);
+            const uint32_t fl = w.sflags[id];
             cut = (fl & kFlagCut) != 0u;
             float U, V;
             const float Q = ray_offset_q(uv, ray, f.ifx, f.ify, &U, &V);
             const float rq = sqrtf(Q * iqq);            // rho / c.z
             const float d = 1.0f - rq * r1.y;
-            const float o = r1.z;
-            const float E = __expf(r1.w - mg);
+            const float o = r2.x;
+            const float E = expf(__fsub_rn(r1.z, mg) + r1.w);
             const float wt = o * d * E;
             float sdot = 0.0f;
 #pragma unroll
@@ -98,9 +98,9 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
                 }
             }
             const float sj = sdot * iw;                 // dL/dw = <G, f - F> / W
-            v[4] = sj * d * E * (1.0f + r1.w);          // dw/do = d E (1 + o z~/gamma)
+            v[4] = sj * d * E * (1.0f + r1.z);          // dw/do = d E (1 + o z~/gamma)
             if (want_geom && !cut) {
-                const float Z = r2.x, reff = r2.y;
+                const float Z = r2.y, reff = r2.z;
                 const float ireff = 1.0f / reff;
                 const float sE = sj * o * E;            // dL/dd
                 // depth factor: dw/dz~ = w o / gamma, dz~/dc.z = -1/(zfar - znear)

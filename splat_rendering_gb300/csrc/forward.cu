@@ -34,6 +34,7 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
     constexpr int NB = Batch<CMAX>::n;
     __shared__ float4 s_uv[NB];
     __shared__ float4 s_r1[NB];
+    __shared__ float s_o[NB];
     __shared__ uint2 s_rect[NB];
     __shared__ int s_id[NB];
     __shared__ uint32_t s_wmask[NB];
@@ -57,7 +58,8 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
     end = min(end, f.max_pairs);
     start = min(start, end);
 
-    float mg = f.bg_eps * f.inv_gamma;   // running max of eps/gamma and o*z~/gamma
+    // running max of eps/gamma and o z~/gamma, as a float pair
+    float mg = f.eg_hi, mgl = f.eg_lo;
     float wsum = 1.0f;                   // exp(eps/gamma - mg): background weight, shifted
     float acc[CMAX];
 #pragma unroll
@@ -78,6 +80,7 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
             s_id[tid] = id;
             s_uv[tid] = w.rec0[id];
             s_r1[tid] = w.rec1[id];
+            s_o[tid] = reinterpret_cast<const float*>(w.rec2)[4 * id];
             s_rect[tid] = rc;
             const int r0 = max((int)(rc.y & 0xffffu) - tyi * kTile, 0);
             const int r1 = min((int)(rc.y >> 16) - tyi * kTile, kTile - 1);
@@ -88,7 +91,7 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
         }
         if (tid == 0) {
             const uint32_t nx = b0 + NB;
-            s_next_key = nx < end ? w.rec2[w.tile_ids[nx]].z : 0.0f;
+            s_next_key = nx < end ? w.rec2[w.tile_ids[nx]].w : 0.0f;
         }
         __syncthreads();
         const int nb = (int)min((uint32_t)NB, end - b0);
@@ -107,15 +110,15 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
                     if (!(Q < __fmul_rn(r1.x, ray.qq))) continue;
                     // hit: d = 1 - rho / r_eff with rho / c.z = sqrt(Q / qq)
                     const float d = 1.0f - sqrtf(Q * iqq) * r1.y;
-                    const float e = r1.w;
-                    if (e > mg) {
-                        const float sc = __expf(mg - e);
+                    if (r1.z > mg || (r1.z == mg && r1.w > mgl)) {
+                        const float sc = expf(__fsub_rn(mg, r1.z) + __fsub_rn(mgl, r1.w));
                         wsum *= sc;
 #pragma unroll
                         for (int c = 0; c < CMAX; ++c) acc[c] *= sc;
-                        mg = e;
+                        mg = r1.z;
+                        mgl = r1.w;
                     }
-                    const float wt = r1.z * d * __expf(e - mg);
+                    const float wt = s_o[j] * d * expf(__fsub_rn(r1.z, mg) + __fsub_rn(r1.w, mgl));
                     wsum += wt;
 #pragma unroll
                     for (int c = 0; c < CMAX; ++c)
@@ -135,7 +138,7 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
             if (!done && nh >= f.n_track) {
                 const float zt = fmaxf((f.zfar - s_next_key) * f.inv_zrange, 0.0f);
                 const float rem = (float)(end - (b0 + NB));
-                done = rem * __expf(zt * f.inv_gamma - mg) <= f.stop_tau * wsum;
+                done = rem * expf(zt * f.inv_gamma - mg) <= f.stop_tau * wsum;
             }
             if (__syncthreads_and(done)) break;
         }
@@ -148,8 +151,9 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
 #pragma unroll
         for (int c = 0; c < CMAX; ++c)
             if (c < C) image[(size_t)p * C + c] = acc[c] * iw;
+        // store the stabiliser's high part; fold its low part into the normaliser
         w.mg[p] = mg;
-        w.wsum[p] = wsum;
+        w.wsum[p] = wsum * expf(mgl);
 #pragma unroll
         for (int k = 0; k < TMAX; ++k)
             if (k < f.n_track) w.ids[(size_t)k * P + p] = ids[k];

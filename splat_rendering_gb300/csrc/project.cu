@@ -48,9 +48,17 @@ k_project(Frame f, Workspace w, const float* __restrict__ pos, const float* __re
                 const bool cut = (f.flags & 1u) && !(area > f.amin);
                 flags = kFlagKeep | (on_floor ? kFlagFloor : 0u) | (cut ? kFlagCut : 0u);
                 r0 = make_float4(u.hi, u.lo, v.hi, v.lo);
-                // value path: c.z / r_eff and o * z~ / gamma
-                const float zt = (f.zfar - Z) * f.inv_zrange;
-                r1 = make_float4(s2, Z / reff, o, o * zt * f.inv_gamma);
+                // value path: the exponent o z~ / gamma = o (zfar - c.z) / ((zfar - znear) gamma)
+                // as a float pair; its magnitude reaches 1/gamma, so a single float would
+                // carry ~1e-6 absolute error into every weight through exp()
+                const FPair nz = ef_sum(f.zfar, -cz.hi);
+                const FPair n = ef_fast_sum(nz.hi, __fsub_rn(nz.lo, cz.lo));
+                FPair on = ef_prod(o, n.hi);
+                on.lo = __fmaf_rn(o, n.lo, on.lo);
+                FPair e = ef_prod(on.hi, f.zk_hi);
+                e.lo = __fmaf_rn(on.hi, f.zk_lo, __fmaf_rn(on.lo, f.zk_hi, e.lo));
+                e = ef_fast_sum(e.hi, e.lo);
+                r1 = make_float4(s2, Z / reff, e.hi, e.lo);
                 rc = make_uint2((uint32_t)x0 | ((uint32_t)x1 << 16),
                                 (uint32_t)y0 | ((uint32_t)y1 << 16));
                 tx0 = x0 / kTile;
@@ -61,7 +69,8 @@ k_project(Frame f, Workspace w, const float* __restrict__ pos, const float* __re
         }
         w.rec0[i] = r0;
         w.rec1[i] = r1;
-        w.rec2[i] = make_float4(Z, reff, key, __uint_as_float(flags));
+        w.rec2[i] = make_float4(o, Z, reff, key);
+        w.sflags[i] = flags;
         w.rect[i] = rc;
     }
     // warp-cooperative tile counting: flatten the warp's (sphere, tile) pairs

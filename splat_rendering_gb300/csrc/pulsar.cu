@@ -108,7 +108,7 @@ int pulsar_create(pulsar_ctx_t* out, int device, int64_t max_spheres, int64_t ma
     const size_t N = (size_t)(max_spheres > 0 ? max_spheres : 1);
     Workspace& w = c->ws;
     bool ok = alloc(c, &w.rec0, N) && alloc(c, &w.rec1, N) && alloc(c, &w.rec2, N) &&
-              alloc(c, &w.rect, N) && alloc(c, &w.gacc, N) &&
+              alloc(c, &w.rect, N) && alloc(c, &w.gacc, N) && alloc(c, &w.sflags, N) &&
               alloc(c, &w.tile_count, (size_t)c->max_tiles) &&
               alloc(c, &w.tile_start, (size_t)c->max_tiles + 1) &&
               alloc(c, &w.pairs, (size_t)max_pairs) && alloc(c, &w.pairs_alt, (size_t)max_pairs) &&
@@ -180,6 +180,12 @@ int pulsar_project(pulsar_ctx_t c, const float* pos, const float* radius, const 
     f.kappa = prm->kappa;
     f.amin = prm->geom_min_area;
     f.inv_zrange = 1.0f / (cam->zfar - cam->znear);
+    const double zk = 1.0 / (((double)cam->zfar - (double)cam->znear) * (double)prm->gamma);
+    f.zk_hi = (float)zk;
+    f.zk_lo = (float)(zk - (double)f.zk_hi);
+    const double eg = (double)prm->bg_eps / (double)prm->gamma;
+    f.eg_hi = (float)eg;
+    f.eg_lo = (float)(eg - (double)f.eg_hi);
     f.width = cam->width;
     f.height = cam->height;
     f.tiles_x = (cam->width + kTile - 1) / kTile;
@@ -277,6 +283,7 @@ int64_t pulsar_debug_copy(pulsar_ctx_t c, int what, void* dst, int64_t bytes, vo
         case PULSAR_DBG_REC1: src = c->ws.rec1; size = n * 16; break;
         case PULSAR_DBG_REC2: src = c->ws.rec2; size = n * 16; break;
         case PULSAR_DBG_RECT: src = c->ws.rect; size = n * 8; break;
+        case PULSAR_DBG_FLAGS: src = c->ws.sflags; size = n * 4; break;
         case PULSAR_DBG_TILE_OFFSETS: src = c->ws.tile_start; size = (int64_t)(f.n_tiles + 1) * 4; break;
         case PULSAR_DBG_TILE_IDS: {
             uint32_t m = 0;

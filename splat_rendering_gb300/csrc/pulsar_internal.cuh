@@ -30,6 +30,8 @@ struct Frame {
     float fmin;           // min(fx, fy); fx on ties
     float gamma, inv_gamma, bg_eps, stop_tau, kappa, amin;
     float inv_zrange;     // 1/(zfar - znear)
+    float zk_hi, zk_lo;   // 1/((zfar - znear) gamma) as a float pair
+    float eg_hi, eg_lo;   // eps/gamma as a float pair
     int width, height, tiles_x, tiles_y, n_tiles;
     int n_track, channels;
     int n;
@@ -166,8 +168,9 @@ __device__ __forceinline__ bool rect_contains(uint2 rc, int x, int y) {
 // ---------------------------------------------------------- workspace --
 struct Workspace {
     float4* rec0;      // [maxN] u_hi, u_lo, v_hi, v_lo
-    float4* rec1;      // [maxN] s2, c.z/r_eff, o, o*z~/gamma
-    float4* rec2;      // [maxN] c.z, r_eff, key, flags
+    float4* rec1;      // [maxN] s2, c.z/r_eff, (o z~/gamma) as hi, lo
+    float4* rec2;      // [maxN] o, c.z, r_eff, key
+    uint32_t* sflags;  // [maxN] kFlag* bits
     uint2* rect;       // [maxN] pixel rectangle (x0 | x1<<16, y0 | y1<<16)
     float4* gacc;      // [maxN] dL/dc.xyz, dL/dr accumulators (zero between frames)
     uint32_t* tile_count;   // [maxB] (zero between frames)

@@ -49,6 +49,7 @@ def run_gpu(scene, cam_index=0, grad_image=None, max_pairs=None, count_hits=True
         out["rec1"] = r.debug("rec1").view(np.float32).reshape(n, 4) if n else np.zeros((0, 4), np.float32)
         out["rec2"] = r.debug("rec2").view(np.float32).reshape(n, 4) if n else np.zeros((0, 4), np.float32)
         out["rect"] = r.debug("rect").view(np.uint32).reshape(n, 2) if n else np.zeros((0, 2), np.uint32)
+        out["flags"] = r.debug("flags").view(np.uint32) if n else np.zeros(0, np.uint32)
         out["tile_offsets"] = r.debug("tile_offsets").view(np.uint32)
         out["tile_ids"] = r.debug("tile_ids").view(np.uint32)[:m] if m else np.zeros(0, np.uint32)
         out["mg"] = r.debug("mg").view(np.float32).reshape(cam.height, cam.width)
@@ -79,14 +80,14 @@ def assert_close(gpu, ref, rtol, atol, what):
 
 def assert_decisions_equal(g, d):
     """Per-sphere fp32 decision quantities bit for bit (oracle.project output d)."""
-    keep = (g["rec2"][:, 3].view(np.uint32) & 1).astype(bool)
+    fl = g["flags"]
+    keep = (fl & 1).astype(bool)
     assert np.array_equal(keep, d["keep"] == 1), "keep flags differ"
     k = keep
     assert np.array_equal(g["rec0"][k].view(np.uint32), d["uv"][k].view(np.uint32)), "centre pair"
-    assert np.array_equal(g["rec2"][k, 1].view(np.uint32), d["reff"][k].view(np.uint32)), "r_eff"
-    assert np.array_equal(g["rec2"][k, 2].view(np.uint32), d["key"][k].view(np.uint32)), "key"
+    assert np.array_equal(g["rec2"][k, 2].view(np.uint32), d["reff"][k].view(np.uint32)), "r_eff"
+    assert np.array_equal(g["rec2"][k, 3].view(np.uint32), d["key"][k].view(np.uint32)), "key"
     assert np.array_equal(g["rec1"][k, 0].view(np.uint32), d["s2"][k].view(np.uint32)), "s2"
-    fl = g["rec2"][:, 3].view(np.uint32)
     assert np.array_equal(((fl >> 1) & 1)[k], d["floor"][k]), "floor flags"
     assert np.array_equal(((fl >> 2) & 1)[k], d["cut"][k]), "cutoff flags"
     rect = g["rect"][k]
