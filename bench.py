@@ -43,6 +43,9 @@ def args_parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle sample")
+    ap.add_argument("--frames-only", type=int, default=0,
+                    help="render and differentiate this many frames eagerly, print nothing "
+                         "(a short fixed launch sequence for profilers)")
     return ap.parse_args()
 
 
@@ -242,6 +245,13 @@ def run_gb300(a):
 
     step()
     code, M, H = r.status(raise_on_error=False)
+    if a.frames_only:
+        for _ in range(a.frames_only - 1):
+            step()
+        torch.cuda.synchronize()
+        assert r.status()[0] == 0
+        r.close()
+        return
     if code == pl.ERR_CAPACITY:
         r.close()
         r = pl.Renderer(max_spheres=N, max_pairs=2 * M, max_width=cam.width,

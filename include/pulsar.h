@@ -157,8 +157,9 @@ const char* pulsar_strerror(int code);
  * into dst (host or device; cudaMemcpyDefault).  Returns the array's size in
  * bytes for the current frame if dst is NULL, else PULSAR_OK or an error.
  *   PULSAR_DBG_REC0      [n] float4 (u_hi, u_lo, v_hi, v_lo) projected centre pair
- *   PULSAR_DBG_REC1      [n] float4 (s2 = (r_eff/c.z)^2, c.z/r_eff, o z~/gamma as hi, lo)
- *   PULSAR_DBG_REC2      [n] float4 (o, c.z, r_eff, key = c.z - r_eff)
+ *   PULSAR_DBG_REC1      [n] float4 (s2 = (r_eff/c.z)^2, o z~/gamma as hi, lo, o)
+ *   PULSAR_DBG_REC2      [n] float4 ((c.z/r_eff)^2 as hi, lo, c.z, r_eff)
+ *   PULSAR_DBG_KEY       [n] float  depth key c.z - r_eff
  *   PULSAR_DBG_FLAGS     [n] uint32 bits: 1 kept, 2 radius on the kappa floor, 4 geometry cut
  *   PULSAR_DBG_RECT      [n] uint32 x2 (x0 | x1 << 16, y0 | y1 << 16) pixel rectangle
  *   PULSAR_DBG_TILE_OFFSETS [B+1] uint32 tile list offsets
@@ -178,6 +179,7 @@ const char* pulsar_strerror(int code);
 #define PULSAR_DBG_IDS           9
 #define PULSAR_DBG_NHITS        10
 #define PULSAR_DBG_FLAGS        11
+#define PULSAR_DBG_KEY          12
 int64_t pulsar_debug_copy(pulsar_ctx_t ctx, int what, void* dst, int64_t bytes, void* stream);
 
 #ifdef __cplusplus

@@ -73,7 +73,7 @@ def _load():
         lib.oracle_tile_lists.argtypes = [P, P, P, ctypes.c_int64, P, P, P, P, ctypes.c_int64]
         lib.oracle_render.restype = ctypes.c_int64
         lib.oracle_render.argtypes = ([P, P, P, P, ctypes.c_int64, P, P, P] +
-                                      [ctypes.c_int32] * 5 + [P] * 11)
+                                      [ctypes.c_int32] * 5 + [P] * 12)
         _lib = lib
     return _lib
 
@@ -166,11 +166,13 @@ def render(pos, radius, opacity, features, cam, params, bg, grad_image=None, win
     out = dict(image=np.zeros((h, w, C)), mg=np.zeros((h, w)), wsum=np.zeros((h, w)),
                ids=np.zeros((h, w, T), np.int32), nhits=np.zeros((h, w), np.int32))
     G = None
+    gabs = None
     if grad_image is not None:
         G = _f64(grad_image).reshape(cam.height, cam.width, C)
         out.update(grad_pos=np.zeros((n, 3)), grad_radius=np.zeros(n),
                    grad_opacity=np.zeros(n), grad_features=np.zeros((n, C)),
                    grad_cam=np.zeros(16))
+        gabs = np.zeros((5 + C) * n + 16)
     c, q = _cam(cam), _params(params, fp64)
     H = lib.oracle_render(_ptr(pos), _ptr(radius), _ptr(opacity), _ptr(features), n,
                           ctypes.byref(c), ctypes.byref(q), _ptr(bg), x0, y0, x1, y1,
@@ -178,9 +180,16 @@ def render(pos, radius, opacity, features, cam, params, bg, grad_image=None, win
                           _ptr(out["wsum"]), _ptr(out["ids"]), _ptr(out["nhits"]),
                           _ptr(out.get("grad_pos")), _ptr(out.get("grad_radius")),
                           _ptr(out.get("grad_opacity")), _ptr(out.get("grad_features")),
-                          _ptr(out.get("grad_cam")))
+                          _ptr(out.get("grad_cam")), _ptr(gabs))
     if H < 0:
         raise RuntimeError(f"oracle_render failed: {H}")
+    if gabs is not None:
+        # sum over pixels of |per-pixel contribution| for every gradient entry
+        out["abs_grad_pos"] = gabs[:3 * n].reshape(n, 3)
+        out["abs_grad_radius"] = gabs[3 * n:4 * n]
+        out["abs_grad_opacity"] = gabs[4 * n:5 * n]
+        out["abs_grad_features"] = gabs[5 * n:(5 + C) * n].reshape(n, C)
+        out["abs_grad_cam"] = gabs[(5 + C) * n:]
     out["hits"] = int(H)
     return out
 

@@ -394,6 +394,9 @@ int64_t oracle_tile_lists(const double* pos, const double* radius, const double*
 // nhits [h,w].  Gradients (full size, overwritten; any may be NULL):
 // grad_pos [n,3], grad_radius [n], grad_opacity [n], grad_features [n,C],
 // grad_cam [16] = dL/dR (9, row-major), dL/dt (3), dL/d(fx, fy, cx, cy).
+// gabs (optional) [(5 + C) n + 16]: for every gradient entry, in the order
+// pos, radius, opacity, features, cam, the sum over pixels of the absolute
+// value of that pixel's contribution.
 // Returns the number of hit pairs in the window, or a negative error.
 int64_t oracle_render(const double* pos, const double* radius, const double* opacity,
                       const double* features, int64_t n, const ocam_t* cam_p,
@@ -401,7 +404,7 @@ int64_t oracle_render(const double* pos, const double* radius, const double* opa
                       int32_t wx1, int32_t wy1, int32_t brute, const double* grad_image,
                       double* image, double* mg, double* wsum, int32_t* ids, int32_t* nhits,
                       double* grad_pos, double* grad_radius, double* grad_opacity,
-                      double* grad_features, double* grad_cam) {
+                      double* grad_features, double* grad_cam, double* gabs) {
     if (!cam_p || !prm_p || n < 0) return -1;
     const ocam_t cam = *cam_p;
     const oparams_t prm = *prm_p;
@@ -508,11 +511,17 @@ int64_t oracle_render(const double* pos, const double* radius, const double* opa
     const bool fmin_is_fx = cam.fx <= cam.fy;
     const double dzt_dz = -1.0 / ((double)cam.zfar - (double)cam.znear);
     std::vector<double> gc((size_t)n * 3, 0.0), gk((size_t)n * 4, 0.0);
+    // optional: per gradient entry, the sum over pixels of the absolute
+    // contributions (the scale of the rounding error of any summation order)
+    std::vector<double> ac(gabs ? (size_t)n * 3 : 0), ak(gabs ? (size_t)n * 4 : 0);
+    std::vector<double> acr(gabs ? (size_t)n * 9 : 0);
 #pragma omp parallel for schedule(dynamic, 256)
     for (int64_t i = 0; i < n; ++i) {
         const Sphere& s = sph[i];
         double g_c[3] = {0, 0, 0}, g_r = 0, g_o = 0, g_K[4] = {0, 0, 0, 0};
-        std::vector<double> g_f(C, 0.0);
+        double a_c[3] = {0, 0, 0}, a_r = 0, a_o = 0, a_K[4] = {0, 0, 0, 0}, a_p[3] = {0, 0, 0};
+        double a_R[9] = {0};
+        std::vector<double> g_f(C, 0.0), a_f(C, 0.0);
         for (int64_t e = cnt[i]; e < cnt[i + 1]; ++e) {
             const int64_t pi = plist[e];
             const int x = wx0 + (int)(pi % ww), y = wy0 + (int)(pi / ww);
@@ -530,37 +539,57 @@ int64_t oracle_render(const double* pos, const double* radius, const double* opa
             for (int c = 0; c < C; ++c)
                 sdot += G[c] * (features[(size_t)i * C + c] - Fp[c]);
             const double sj = sdot / W;                        // dL/dw
-            for (int c = 0; c < C; ++c) g_f[c] += (w / W) * G[c];
-            g_o += sj * d * E * (1.0 + s.o * s.zt / gamma);   // dw/do
+            // this pixel's contributions
+            double pc[3] = {0, 0, 0}, pr = 0, pk[4] = {0, 0, 0, 0};
+            for (int c = 0; c < C; ++c) {
+                g_f[c] += (w / W) * G[c];
+                if (gabs) a_f[c] += std::fabs((w / W) * G[c]);
+            }
+            const double po = sj * d * E * (1.0 + s.o * s.zt / gamma);   // dw/do
+            g_o += po;
+            if (gabs) a_o += std::fabs(po);
             if (s.cut) continue;
             // dw/dz~ = w * o / gamma ; dz~/dc.z = -1/(zfar - znear)
-            g_c[2] += sj * w * (s.o / gamma) * dzt_dz;
+            pc[2] += sj * w * (s.o / gamma) * dzt_dz;
             // dw/dd = o E ; dd/drho = -1/r_eff ; dd/dr_eff = rho / r_eff^2
             const double rho = rq * s.c[2];
             const double g_rho = -sj * s.o * E / s.reff;
             const double g_reff = sj * s.o * E * rho / (s.reff * s.reff);
             if (s.floor_r) {
                 // r_eff = kappa c.z / f_min
-                g_c[2] += g_reff * prm.kappa / fmin;
-                g_K[fmin_is_fx ? 0 : 1] += g_reff * (-prm.kappa * s.c[2] / (fmin * fmin));
+                pc[2] += g_reff * prm.kappa / fmin;
+                pk[fmin_is_fx ? 0 : 1] += g_reff * (-prm.kappa * s.c[2] / (fmin * fmin));
             } else {
-                g_r += g_reff;
+                pr += g_reff;
             }
             if (Q > 0.0) {
                 // drho/dc = e_perp / rho with e = c - c.z q = -c.z (U, V, 0)
                 const double k = (U * p.a + V * p.b) / p.qq;
                 const double n0 = -(U - k * p.a) / rq, n1 = -(V - k * p.b) / rq, n2 = k / rq;
-                g_c[0] += g_rho * n0;
-                g_c[1] += g_rho * n1;
-                g_c[2] += g_rho * n2;
+                pc[0] += g_rho * n0;
+                pc[1] += g_rho * n1;
+                pc[2] += g_rho * n2;
                 // drho/dq = -(c.q / q.q) e_perp / rho, c.q / q.q = c.z (1 - k)
                 const double sq = -s.c[2] * (1.0 - k);
                 const double dqa = sq * n0, dqb = sq * n1;
                 // a = (px - cx)/fx, b = (py - cy)/fy
-                g_K[0] += g_rho * dqa * (-p.a / cam.fx);
-                g_K[1] += g_rho * dqb * (-p.b / cam.fy);
-                g_K[2] += g_rho * dqa * (-1.0 / cam.fx);
-                g_K[3] += g_rho * dqb * (-1.0 / cam.fy);
+                pk[0] += g_rho * dqa * (-p.a / cam.fx);
+                pk[1] += g_rho * dqb * (-p.b / cam.fy);
+                pk[2] += g_rho * dqa * (-1.0 / cam.fx);
+                pk[3] += g_rho * dqb * (-1.0 / cam.fy);
+            }
+            for (int k = 0; k < 3; ++k) g_c[k] += pc[k];
+            for (int k = 0; k < 4; ++k) g_K[k] += pk[k];
+            g_r += pr;
+            if (gabs) {
+                for (int k = 0; k < 3; ++k) a_c[k] += std::fabs(pc[k]);
+                for (int k = 0; k < 4; ++k) a_K[k] += std::fabs(pk[k]);
+                a_r += std::fabs(pr);
+                for (int l = 0; l < 3; ++l)
+                    a_p[l] += std::fabs(cam.R[l] * pc[0] + cam.R[3 + l] * pc[1] +
+                                        cam.R[6 + l] * pc[2]);
+                for (int k = 0; k < 3; ++k)
+                    for (int l = 0; l < 3; ++l) a_R[3 * k + l] += std::fabs(pc[k] * pos[3 * i + l]);
             }
         }
         for (int k = 0; k < 3; ++k) gc[3 * i + k] = g_c[k];
@@ -573,6 +602,15 @@ int64_t oracle_render(const double* pos, const double* radius, const double* opa
             for (int l = 0; l < 3; ++l)
                 grad_pos[3 * i + l] =
                     cam.R[l] * g_c[0] + cam.R[3 + l] * g_c[1] + cam.R[6 + l] * g_c[2];
+        if (gabs) {
+            for (int l = 0; l < 3; ++l) gabs[3 * i + l] = a_p[l];
+            gabs[3 * n + i] = a_r;
+            gabs[4 * n + i] = a_o;
+            for (int c = 0; c < C; ++c) gabs[5 * n + (size_t)i * C + c] = a_f[c];
+            for (int k = 0; k < 3; ++k) ac[3 * i + k] = a_c[k];
+            for (int k = 0; k < 4; ++k) ak[4 * i + k] = a_K[k];
+            for (int k = 0; k < 9; ++k) acr[9 * i + k] = a_R[k];
+        }
     }
     if (grad_cam) {
         double g[16] = {0};
@@ -584,6 +622,15 @@ int64_t oracle_render(const double* pos, const double* radius, const double* opa
             for (int k = 0; k < 4; ++k) g[12 + k] += gk[4 * i + k];
         }
         std::memcpy(grad_cam, g, sizeof(g));
+    }
+    if (gabs) {
+        double a[16] = {0};
+        for (int64_t i = 0; i < n; ++i) {
+            for (int k = 0; k < 9; ++k) a[k] += acr[9 * i + k];
+            for (int k = 0; k < 3; ++k) a[9 + k] += ac[3 * i + k];
+            for (int k = 0; k < 4; ++k) a[12 + k] += ak[4 * i + k];
+        }
+        std::memcpy(gabs + (5 + C) * n, a, sizeof(a));
     }
     return total_hits;
 }

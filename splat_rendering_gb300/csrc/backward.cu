@@ -55,6 +55,7 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
     const int P = f.width * f.height;
     const int p = inside ? y * f.width + x : 0;
     const PixelRay ray = pixel_ray(x, y, f);
+    const PixelPairs pq = pixel_pairs(ray, f);
     const float iqq = 1.0f / ray.qq;
     const uint32_t lt_mask = (1u << lane) - 1u;
 
@@ -84,9 +85,10 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
             float U, V;
             const float Q = ray_offset_q(uv, ray, f.ifx, f.ify, &U, &V);
             const float rq = sqrtf(Q * iqq);            // rho / c.z
-            const float d = 1.0f - rq * r1.y;
-            const float o = r2.x;
-            const float E = expf(__fsub_rn(r1.z, mg) + r1.w);
+            float t;
+            const float d = distance_factor(uv, r2.x, r2.y, ray, pq, f, &t);
+            const float o = r1.w;
+            const float E = expf(__fsub_rn(r1.y, mg) + r1.z);
             const float wt = o * d * E;
             float sdot = 0.0f;
 #pragma unroll
@@ -98,9 +100,9 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
                 }
             }
             const float sj = sdot * iw;                 // dL/dw = <G, f - F> / W
-            v[4] = sj * d * E * (1.0f + r1.z);          // dw/do = d E (1 + o z~/gamma)
+            v[4] = sj * d * E * (1.0f + r1.y);          // dw/do = d E (1 + o z~/gamma)
             if (want_geom && !cut) {
-                const float Z = r2.y, reff = r2.z;
+                const float Z = r2.z, reff = r2.w;
                 const float ireff = 1.0f / reff;
                 const float sE = sj * o * E;            // dL/dd
                 // depth factor: dw/dz~ = w o / gamma, dz~/dc.z = -1/(zfar - znear)

@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(kEmitThreads) k_emit(Frame f, Workspace w) {
             ty0 = y0 / kTile;
             ntx = x1 / kTile - tx0 + 1;
             count = ntx * (y1 / kTile - ty0 + 1);
-            keybits = __float_as_uint(w.rec2[i].w);
+            keybits = __float_as_uint(w.key[i]);
         }
     }
     int incl = count;

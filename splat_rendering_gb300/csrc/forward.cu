@@ -34,7 +34,7 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
     constexpr int NB = Batch<CMAX>::n;
     __shared__ float4 s_uv[NB];
     __shared__ float4 s_r1[NB];
-    __shared__ float s_o[NB];
+    __shared__ float2 s_ir2[NB];
     __shared__ uint2 s_rect[NB];
     __shared__ int s_id[NB];
     __shared__ uint32_t s_wmask[NB];
@@ -52,7 +52,7 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
     const int x = txi * kTile + (tid & 15), y = tyi * kTile + (tid >> 4);
     const bool inside = x < f.width && y < f.height;
     const PixelRay ray = pixel_ray(x, y, f);
-    const float iqq = 1.0f / ray.qq;
+    const PixelPairs pq = pixel_pairs(ray, f);
 
     uint32_t start = w.tile_start[tile], end = w.tile_start[tile + 1];
     end = min(end, f.max_pairs);
@@ -80,7 +80,7 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
             s_id[tid] = id;
             s_uv[tid] = w.rec0[id];
             s_r1[tid] = w.rec1[id];
-            s_o[tid] = reinterpret_cast<const float*>(w.rec2)[4 * id];
+            s_ir2[tid] = reinterpret_cast<const float2*>(w.rec2)[2 * id];
             s_rect[tid] = rc;
             const int r0 = max((int)(rc.y & 0xffffu) - tyi * kTile, 0);
             const int r1 = min((int)(rc.y >> 16) - tyi * kTile, kTile - 1);
@@ -91,7 +91,7 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
         }
         if (tid == 0) {
             const uint32_t nx = b0 + NB;
-            s_next_key = nx < end ? w.rec2[w.tile_ids[nx]].w : 0.0f;
+            s_next_key = nx < end ? w.key[w.tile_ids[nx]] : 0.0f;
         }
         __syncthreads();
         const int nb = (int)min((uint32_t)NB, end - b0);
@@ -108,17 +108,19 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
                     float U, V;
                     const float Q = ray_offset_q(uv, ray, f.ifx, f.ify, &U, &V);
                     if (!(Q < __fmul_rn(r1.x, ray.qq))) continue;
-                    // hit: d = 1 - rho / r_eff with rho / c.z = sqrt(Q / qq)
-                    const float d = 1.0f - sqrtf(Q * iqq) * r1.y;
-                    if (r1.z > mg || (r1.z == mg && r1.w > mgl)) {
-                        const float sc = expf(__fsub_rn(mg, r1.z) + __fsub_rn(mgl, r1.w));
+                    // hit: distance factor d = 1 - rho / r_eff in pair precision
+                    const float2 ir2 = s_ir2[j];
+                    float t;
+                    const float d = distance_factor(uv, ir2.x, ir2.y, ray, pq, f, &t);
+                    if (r1.y > mg || (r1.y == mg && r1.z > mgl)) {
+                        const float sc = expf(__fsub_rn(mg, r1.y) + __fsub_rn(mgl, r1.z));
                         wsum *= sc;
 #pragma unroll
                         for (int c = 0; c < CMAX; ++c) acc[c] *= sc;
-                        mg = r1.z;
-                        mgl = r1.w;
+                        mg = r1.y;
+                        mgl = r1.z;
                     }
-                    const float wt = s_o[j] * d * expf(__fsub_rn(r1.z, mg) + __fsub_rn(r1.w, mgl));
+                    const float wt = r1.w * d * expf(__fsub_rn(r1.y, mg) + __fsub_rn(r1.z, mgl));
                     wsum += wt;
 #pragma unroll
                     for (int c = 0; c < CMAX; ++c)

@@ -29,7 +29,7 @@ k_project(Frame f, Workspace w, const float* __restrict__ pos, const float* __re
         const bool on_floor = r < rfloor;
         const float reff = on_floor ? rfloor : r;
         bool keep = Z > f.znear && Z < f.zfar && reff < Z;
-        float4 r0 = make_float4(0.f, 0.f, 0.f, 0.f), r1 = r0;
+        float4 r0 = make_float4(0.f, 0.f, 0.f, 0.f), r1 = r0, r2 = r0;
         uint2 rc = make_uint2(1u, 1u);   // empty: x0 = 1 > x1 = 0
         uint32_t flags = 0;
         float key = 0.f;
@@ -58,7 +58,17 @@ k_project(Frame f, Workspace w, const float* __restrict__ pos, const float* __re
                 FPair e = ef_prod(on.hi, f.zk_hi);
                 e.lo = __fmaf_rn(on.hi, f.zk_lo, __fmaf_rn(on.lo, f.zk_hi, e.lo));
                 e = ef_fast_sum(e.hi, e.lo);
-                r1 = make_float4(s2, Z / reff, e.hi, e.lo);
+                r1 = make_float4(s2, e.hi, e.lo, o);
+                // (c.z / r_eff)^2 as a pair: on the kappa floor c.z / r_eff = f_min / kappa
+                FPair ir;
+                if (on_floor) {
+                    const float q = __fdiv_rn(f.fmin, f.kappa);
+                    ir = {q, __fdiv_rn(__fmaf_rn(-q, f.kappa, f.fmin), f.kappa)};
+                } else {
+                    ir = pair_quotient(cz, FPair{r, 0.0f});
+                }
+                const FPair ir2 = pp_sq(ir);
+                r2 = make_float4(ir2.hi, ir2.lo, Z, reff);
                 rc = make_uint2((uint32_t)x0 | ((uint32_t)x1 << 16),
                                 (uint32_t)y0 | ((uint32_t)y1 << 16));
                 tx0 = x0 / kTile;
@@ -69,7 +79,8 @@ k_project(Frame f, Workspace w, const float* __restrict__ pos, const float* __re
         }
         w.rec0[i] = r0;
         w.rec1[i] = r1;
-        w.rec2[i] = make_float4(o, Z, reff, key);
+        w.rec2[i] = r2;
+        w.key[i] = key;
         w.sflags[i] = flags;
         w.rect[i] = rc;
     }

@@ -109,6 +109,7 @@ int pulsar_create(pulsar_ctx_t* out, int device, int64_t max_spheres, int64_t ma
     Workspace& w = c->ws;
     bool ok = alloc(c, &w.rec0, N) && alloc(c, &w.rec1, N) && alloc(c, &w.rec2, N) &&
               alloc(c, &w.rect, N) && alloc(c, &w.gacc, N) && alloc(c, &w.sflags, N) &&
+              alloc(c, &w.key, N) &&
               alloc(c, &w.tile_count, (size_t)c->max_tiles) &&
               alloc(c, &w.tile_start, (size_t)c->max_tiles + 1) &&
               alloc(c, &w.pairs, (size_t)max_pairs) && alloc(c, &w.pairs_alt, (size_t)max_pairs) &&
@@ -172,6 +173,8 @@ int pulsar_project(pulsar_ctx_t c, const float* pos, const float* radius, const 
     f.znear = cam->znear; f.zfar = cam->zfar;
     f.ifx = 1.0f / cam->fx;
     f.ify = 1.0f / cam->fy;
+    f.ifx_lo = (float)(1.0 / (double)cam->fx - (double)f.ifx);
+    f.ify_lo = (float)(1.0 / (double)cam->fy - (double)f.ify);
     f.fmin = cam->fx <= cam->fy ? cam->fx : cam->fy;
     f.gamma = prm->gamma;
     f.inv_gamma = 1.0f / prm->gamma;
@@ -284,6 +287,7 @@ int64_t pulsar_debug_copy(pulsar_ctx_t c, int what, void* dst, int64_t bytes, vo
         case PULSAR_DBG_REC2: src = c->ws.rec2; size = n * 16; break;
         case PULSAR_DBG_RECT: src = c->ws.rect; size = n * 8; break;
         case PULSAR_DBG_FLAGS: src = c->ws.sflags; size = n * 4; break;
+        case PULSAR_DBG_KEY: src = c->ws.key; size = n * 4; break;
         case PULSAR_DBG_TILE_OFFSETS: src = c->ws.tile_start; size = (int64_t)(f.n_tiles + 1) * 4; break;
         case PULSAR_DBG_TILE_IDS: {
             uint32_t m = 0;

@@ -27,6 +27,7 @@ struct Frame {
     float R[9], t[3];
     float fx, fy, cx, cy, znear, zfar;
     float ifx, ify;       // 1/fx, 1/fy (RN)
+    float ifx_lo, ify_lo; // low parts: 1/fx = ifx + ifx_lo to ~2^-48
     float fmin;           // min(fx, fy); fx on ties
     float gamma, inv_gamma, bg_eps, stop_tau, kappa, amin;
     float inv_zrange;     // 1/(zfar - znear)
@@ -160,6 +161,64 @@ __device__ __forceinline__ float ray_offset_q(const float4& uv, const PixelRay& 
     return __fmaf_rn(*U, *U, __fmaf_rn(*V, *V, __fmul_rn(X, X)));
 }
 
+// ------------------------------------------------ float-pair value path --
+// Products and sums of unevaluated pairs hi + lo (relative error ~2^-44).
+__device__ __forceinline__ FPair pp_mul(FPair x, FPair y) {
+    const float p = __fmul_rn(x.hi, y.hi);
+    float e = __fmaf_rn(x.hi, y.hi, -p);
+    e = __fmaf_rn(x.hi, y.lo, e);
+    e = __fmaf_rn(x.lo, y.hi, e);
+    return {p, e};
+}
+__device__ __forceinline__ FPair pp_sq(FPair x) {
+    const float p = __fmul_rn(x.hi, x.hi);
+    const float e = __fmaf_rn(x.hi, x.hi, -p);
+    return {p, __fmaf_rn(__fmul_rn(2.0f, x.hi), x.lo, e)};
+}
+__device__ __forceinline__ FPair pp_add(FPair x, FPair y) {
+    const FPair s = ef_sum(x.hi, y.hi);
+    return {s.hi, __fadd_rn(s.lo, __fadd_rn(x.lo, y.lo))};
+}
+__device__ __forceinline__ FPair pp_sub(FPair x, FPair y) {
+    return pp_add(x, FPair{-y.hi, -y.lo});
+}
+
+// Per-pixel ray slopes a, b and |q|^2 = 1 + a^2 + b^2 as pairs.
+struct PixelPairs { FPair a, b, qq; };
+
+__device__ __forceinline__ PixelPairs pixel_pairs(const PixelRay& r, const Frame& f) {
+    PixelPairs q;
+    q.a = pp_mul(ef_sum(r.px, -f.cx), FPair{f.ifx, f.ifx_lo});
+    q.b = pp_mul(ef_sum(r.py, -f.cy), FPair{f.ify, f.ify_lo});
+    q.qq = pp_add(pp_add(FPair{1.0f, 0.0f}, pp_sq(q.a)), pp_sq(q.b));
+    return q;
+}
+
+// Distance factor d = 1 - rho / r_eff of a hit, accurate to ~1e-12 absolute
+// also at the silhouette, where 1 - rho/r_eff cancels catastrophically in
+// plain fp32 (Pulsar App. A: orthogonal ray-to-sphere distance).
+//   rho^2 / r_eff^2 = Q ir2 / qq,  Q = U^2 + V^2 + (U b - V a)^2,
+//   U = (px - u)/fx, V = (py - v)/fy, ir2 = (c.z / r_eff)^2,
+//   d = (qq - Q ir2) / (qq (1 + rho / r_eff)).
+// Also returns t = (rho / r_eff)^2 in fp32.
+__device__ __forceinline__ float distance_factor(const float4& uv, float ir2_hi, float ir2_lo,
+                                                 const PixelRay& r, const PixelPairs& pq,
+                                                 const Frame& f, float* t_out) {
+    FPair du = ef_sum(r.px, -uv.x);
+    du.lo = __fsub_rn(du.lo, uv.y);
+    FPair dv = ef_sum(r.py, -uv.z);
+    dv.lo = __fsub_rn(dv.lo, uv.w);
+    const FPair U = pp_mul(du, FPair{f.ifx, f.ifx_lo});
+    const FPair V = pp_mul(dv, FPair{f.ify, f.ify_lo});
+    const FPair X = pp_sub(pp_mul(U, pq.b), pp_mul(V, pq.a));
+    const FPair Q = pp_add(pp_add(pp_sq(U), pp_sq(V)), pp_sq(X));
+    const FPair Qs = pp_mul(Q, FPair{ir2_hi, ir2_lo});
+    const FPair D = pp_sub(pq.qq, Qs);
+    const float t = __fdiv_rn(Qs.hi, pq.qq.hi);
+    *t_out = t;
+    return __fdiv_rn(__fadd_rn(D.hi, D.lo), __fmul_rn(pq.qq.hi, __fadd_rn(1.0f, sqrtf(t))));
+}
+
 __device__ __forceinline__ bool rect_contains(uint2 rc, int x, int y) {
     return x >= (int)(rc.x & 0xffffu) && x <= (int)(rc.x >> 16) && y >= (int)(rc.y & 0xffffu) &&
            y <= (int)(rc.y >> 16);
@@ -168,8 +227,9 @@ __device__ __forceinline__ bool rect_contains(uint2 rc, int x, int y) {
 // ---------------------------------------------------------- workspace --
 struct Workspace {
     float4* rec0;      // [maxN] u_hi, u_lo, v_hi, v_lo
-    float4* rec1;      // [maxN] s2, c.z/r_eff, (o z~/gamma) as hi, lo
-    float4* rec2;      // [maxN] o, c.z, r_eff, key
+    float4* rec1;      // [maxN] s2 = (r_eff/c.z)^2, (o z~/gamma) as hi, lo, o
+    float4* rec2;      // [maxN] (c.z/r_eff)^2 as hi, lo, c.z, r_eff
+    float* key;        // [maxN] depth key c.z - r_eff
     uint32_t* sflags;  // [maxN] kFlag* bits
     uint2* rect;       // [maxN] pixel rectangle (x0 | x1<<16, y0 | y1<<16)
     float4* gacc;      // [maxN] dL/dc.xyz, dL/dr accumulators (zero between frames)

@@ -5,9 +5,13 @@ from dataclasses import replace
 
 import numpy as np
 
-# tolerances: forward 1e-5 relative / 1e-6 absolute, gradients 1e-4 / 1e-5
+# tolerances: forward 1e-5 relative / 1e-6 absolute, gradients 1e-4 / 1e-5.
+# A gradient entry is a sum of per-pixel contributions; where they cancel,
+# fp32 rounding scales with the sum of their absolute values A (the oracle
+# reports it), so the relative part is taken against max(|value|, A/10).
 FWD_RTOL, FWD_ATOL = 1e-5, 1e-6
 GRAD_RTOL, GRAD_ATOL = 1e-4, 1e-5
+COND_FRACTION = 0.1
 
 
 def _t(a, dev="cuda"):
@@ -50,6 +54,7 @@ def run_gpu(scene, cam_index=0, grad_image=None, max_pairs=None, count_hits=True
         out["rec2"] = r.debug("rec2").view(np.float32).reshape(n, 4) if n else np.zeros((0, 4), np.float32)
         out["rect"] = r.debug("rect").view(np.uint32).reshape(n, 2) if n else np.zeros((0, 2), np.uint32)
         out["flags"] = r.debug("flags").view(np.uint32) if n else np.zeros(0, np.uint32)
+        out["key"] = r.debug("key").view(np.float32) if n else np.zeros(0, np.float32)
         out["tile_offsets"] = r.debug("tile_offsets").view(np.uint32)
         out["tile_ids"] = r.debug("tile_ids").view(np.uint32)[:m] if m else np.zeros(0, np.uint32)
         out["mg"] = r.debug("mg").view(np.float32).reshape(cam.height, cam.width)
@@ -63,18 +68,21 @@ def run_gpu(scene, cam_index=0, grad_image=None, max_pairs=None, count_hits=True
     return out
 
 
-def close_report(gpu, ref, rtol, atol):
+def close_report(gpu, ref, rtol, atol, abs_sum=None):
     gpu = np.asarray(gpu, np.float64)
     ref = np.asarray(ref, np.float64)
     err = np.abs(gpu - ref)
-    bound = atol + rtol * np.abs(ref)
+    scale = np.abs(ref)
+    if abs_sum is not None:
+        scale = np.maximum(scale, COND_FRACTION * np.asarray(abs_sum, np.float64))
+    bound = atol + rtol * scale
     bad = err > bound
     worst = float((err / bound).max()) if err.size else 0.0
     return int(bad.sum()), worst
 
 
-def assert_close(gpu, ref, rtol, atol, what):
-    nbad, worst = close_report(gpu, ref, rtol, atol)
+def assert_close(gpu, ref, rtol, atol, what, abs_sum=None):
+    nbad, worst = close_report(gpu, ref, rtol, atol, abs_sum)
     assert nbad == 0, f"{what}: {nbad} of {np.size(ref)} outside tolerance (worst {worst:.3g}x bound)"
 
 
@@ -85,8 +93,8 @@ def assert_decisions_equal(g, d):
     assert np.array_equal(keep, d["keep"] == 1), "keep flags differ"
     k = keep
     assert np.array_equal(g["rec0"][k].view(np.uint32), d["uv"][k].view(np.uint32)), "centre pair"
-    assert np.array_equal(g["rec2"][k, 2].view(np.uint32), d["reff"][k].view(np.uint32)), "r_eff"
-    assert np.array_equal(g["rec2"][k, 3].view(np.uint32), d["key"][k].view(np.uint32)), "key"
+    assert np.array_equal(g["rec2"][k, 3].view(np.uint32), d["reff"][k].view(np.uint32)), "r_eff"
+    assert np.array_equal(g["key"][k].view(np.uint32), d["key"][k].view(np.uint32)), "key"
     assert np.array_equal(g["rec1"][k, 0].view(np.uint32), d["s2"][k].view(np.uint32)), "s2"
     assert np.array_equal(((fl >> 1) & 1)[k], d["floor"][k]), "floor flags"
     assert np.array_equal(((fl >> 2) & 1)[k], d["cut"][k]), "cutoff flags"
@@ -113,7 +121,7 @@ def compare_frame(g, o, what="", window=None, grads=True):
     if grads:
         for k in ("grad_pos", "grad_radius", "grad_opacity", "grad_features", "grad_cam"):
             if k in g:
-                assert_close(g[k], o[k], GRAD_RTOL, GRAD_ATOL, f"{what} {k}")
+                assert_close(g[k], o[k], GRAD_RTOL, GRAD_ATOL, f"{what} {k}", o.get("abs_" + k))
 
 
 def windowed_grad(scene, cam_index, window):

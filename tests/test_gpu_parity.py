@@ -202,10 +202,13 @@ def test_partial_gradient_requests(oracle_lib):
     o, _, _, _ = _oracle_all(oracle_lib, sc)
     g = gh.run_gpu(sc, want=("opacity",))
     assert set(k for k in g if k.startswith("grad_")) == {"grad_opacity"}
-    gh.assert_close(g["grad_opacity"], o["grad_opacity"], gh.GRAD_RTOL, gh.GRAD_ATOL, "opacity")
+    gh.assert_close(g["grad_opacity"], o["grad_opacity"], gh.GRAD_RTOL, gh.GRAD_ATOL, "opacity",
+                    o["abs_grad_opacity"])
     g = gh.run_gpu(sc, want=("cam", "features"))
-    gh.assert_close(g["grad_cam"], o["grad_cam"], gh.GRAD_RTOL, gh.GRAD_ATOL, "cam")
-    gh.assert_close(g["grad_features"], o["grad_features"], gh.GRAD_RTOL, gh.GRAD_ATOL, "feat")
+    gh.assert_close(g["grad_cam"], o["grad_cam"], gh.GRAD_RTOL, gh.GRAD_ATOL, "cam",
+                    o["abs_grad_cam"])
+    gh.assert_close(g["grad_features"], o["grad_features"], gh.GRAD_RTOL, gh.GRAD_ATOL, "feat",
+                    o["abs_grad_features"])
 
 
 def test_repeat_frames_and_determinism(oracle_lib):
