@@ -98,9 +98,12 @@ def _cam(cam) -> _Cam:
 
 
 def _params(p, fp64: bool) -> _Params:
+    """Blend parameters as the float32 values the renderer's interface carries
+    (fp64 decisions: as given)."""
     q = _Params()
-    q.gamma, q.bg_eps = float(p.gamma), float(p.bg_eps)
-    q.kappa, q.geom_min_area = float(p.kappa), float(p.geom_min_area)
+    r = (lambda v: float(v)) if fp64 else (lambda v: float(np.float32(v)))
+    q.gamma, q.bg_eps = r(p.gamma), r(p.bg_eps)
+    q.kappa, q.geom_min_area = r(p.kappa), r(p.geom_min_area)
     q.n_track, q.channels = int(p.n_track), int(p.channels)
     q.geom_cutoff = 1 if p.geom_cutoff else 0
     q.fp64_decisions = 1 if fp64 else 0

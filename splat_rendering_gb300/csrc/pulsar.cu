@@ -24,7 +24,8 @@ struct pulsar_ctx {
     const float* pos = nullptr;        // inputs of the current frame
     int stage = 0;                     // 0 none, 1 projected, 2 binned, 3 forward done
     bool counts_dirty = false;         // tile counts hold a frame that was never binned
-    void* allocs[16] = {};
+    static constexpr int kMaxAllocs = 32;
+    void* allocs[kMaxAllocs] = {};
     int n_allocs = 0;
 };
 
@@ -48,6 +49,7 @@ struct DeviceGuard {
 
 template <typename T>
 bool alloc(pulsar_ctx* c, T** p, size_t count) {
+    if (c->n_allocs >= pulsar_ctx::kMaxAllocs) return false;
     void* q = nullptr;
     if (cudaMalloc(&q, count * sizeof(T) > 0 ? count * sizeof(T) : 16) != cudaSuccess) return false;
     c->allocs[c->n_allocs++] = q;

@@ -204,17 +204,19 @@ __device__ __forceinline__ PixelPairs pixel_pairs(const PixelRay& r, const Frame
 __device__ __forceinline__ float distance_factor(const float4& uv, float ir2_hi, float ir2_lo,
                                                  const PixelRay& r, const PixelPairs& pq,
                                                  const Frame& f, float* t_out) {
+    // offsets to the projected centre, renormalised so that every hi part below
+    // is the rounded value of its pair (px - u_hi is exact but coarse)
     FPair du = ef_sum(r.px, -uv.x);
-    du.lo = __fsub_rn(du.lo, uv.y);
+    du = ef_sum(du.hi, __fsub_rn(du.lo, uv.y));
     FPair dv = ef_sum(r.py, -uv.z);
-    dv.lo = __fsub_rn(dv.lo, uv.w);
+    dv = ef_sum(dv.hi, __fsub_rn(dv.lo, uv.w));
     const FPair U = pp_mul(du, FPair{f.ifx, f.ifx_lo});
     const FPair V = pp_mul(dv, FPair{f.ify, f.ify_lo});
     const FPair X = pp_sub(pp_mul(U, pq.b), pp_mul(V, pq.a));
     const FPair Q = pp_add(pp_add(pp_sq(U), pp_sq(V)), pp_sq(X));
     const FPair Qs = pp_mul(Q, FPair{ir2_hi, ir2_lo});
     const FPair D = pp_sub(pq.qq, Qs);
-    const float t = __fdiv_rn(Qs.hi, pq.qq.hi);
+    const float t = __fdiv_rn(__fadd_rn(Qs.hi, Qs.lo), pq.qq.hi);
     *t_out = t;
     return __fdiv_rn(__fadd_rn(D.hi, D.lo), __fmul_rn(pq.qq.hi, __fadd_rn(1.0f, sqrtf(t))));
 }
