@@ -175,7 +175,7 @@ def render(pos, radius, opacity, features, cam, params, bg, grad_image=None, win
         out.update(grad_pos=np.zeros((n, 3)), grad_radius=np.zeros(n),
                    grad_opacity=np.zeros(n), grad_features=np.zeros((n, C)),
                    grad_cam=np.zeros(16))
-        gabs = np.zeros((5 + C) * n + 16)
+        gabs = np.zeros(2 * ((5 + C) * n + 16))
     c, q = _cam(cam), _params(params, fp64)
     H = lib.oracle_render(_ptr(pos), _ptr(radius), _ptr(opacity), _ptr(features), n,
                           ctypes.byref(c), ctypes.byref(q), _ptr(bg), x0, y0, x1, y1,
@@ -187,12 +187,15 @@ def render(pos, radius, opacity, features, cam, params, bg, grad_image=None, win
     if H < 0:
         raise RuntimeError(f"oracle_render failed: {H}")
     if gabs is not None:
-        # sum over pixels of |per-pixel contribution| for every gradient entry
-        out["abs_grad_pos"] = gabs[:3 * n].reshape(n, 3)
-        out["abs_grad_radius"] = gabs[3 * n:4 * n]
-        out["abs_grad_opacity"] = gabs[4 * n:5 * n]
-        out["abs_grad_features"] = gabs[5 * n:(5 + C) * n].reshape(n, C)
-        out["abs_grad_cam"] = gabs[(5 + C) * n:]
+        # per gradient entry: sum over pixels of |per-pixel contribution| (abs_*)
+        # and of its L1 sensitivity to the input image F (sens_*)
+        L = (5 + C) * n + 16
+        for pre, buf in (("abs_", gabs[:L]), ("sens_", gabs[L:])):
+            out[pre + "grad_pos"] = buf[:3 * n].reshape(n, 3)
+            out[pre + "grad_radius"] = buf[3 * n:4 * n]
+            out[pre + "grad_opacity"] = buf[4 * n:5 * n]
+            out[pre + "grad_features"] = buf[5 * n:(5 + C) * n].reshape(n, C)
+            out[pre + "grad_cam"] = buf[(5 + C) * n:]
     out["hits"] = int(H)
     return out
 

@@ -394,9 +394,11 @@ int64_t oracle_tile_lists(const double* pos, const double* radius, const double*
 // nhits [h,w].  Gradients (full size, overwritten; any may be NULL):
 // grad_pos [n,3], grad_radius [n], grad_opacity [n], grad_features [n,C],
 // grad_cam [16] = dL/dR (9, row-major), dL/dt (3), dL/d(fx, fy, cx, cy).
-// gabs (optional) [(5 + C) n + 16]: for every gradient entry, in the order
-// pos, radius, opacity, features, cam, the sum over pixels of the absolute
-// value of that pixel's contribution.
+// gabs (optional) [2 ((5 + C) n + 16)]: for every gradient entry, in the
+// order pos, radius, opacity, features, cam, (1) the sum over pixels of the
+// absolute value of that pixel's contribution, then (2) the sum over pixels of
+// sum_c |d contribution / d F_c|, its sensitivity to the image F that the
+// backward takes as input (zero for the feature gradients).
 // Returns the number of hit pairs in the window, or a negative error.
 int64_t oracle_render(const double* pos, const double* radius, const double* opacity,
                       const double* features, int64_t n, const ocam_t* cam_p,
@@ -515,12 +517,16 @@ int64_t oracle_render(const double* pos, const double* radius, const double* opa
     // contributions (the scale of the rounding error of any summation order)
     std::vector<double> ac(gabs ? (size_t)n * 3 : 0), ak(gabs ? (size_t)n * 4 : 0);
     std::vector<double> acr(gabs ? (size_t)n * 9 : 0);
+    std::vector<double> sc_(gabs ? (size_t)n * 3 : 0), sk(gabs ? (size_t)n * 4 : 0);
+    std::vector<double> scr(gabs ? (size_t)n * 9 : 0);
 #pragma omp parallel for schedule(dynamic, 256)
     for (int64_t i = 0; i < n; ++i) {
         const Sphere& s = sph[i];
         double g_c[3] = {0, 0, 0}, g_r = 0, g_o = 0, g_K[4] = {0, 0, 0, 0};
         double a_c[3] = {0, 0, 0}, a_r = 0, a_o = 0, a_K[4] = {0, 0, 0, 0}, a_p[3] = {0, 0, 0};
         double a_R[9] = {0};
+        double s_c[3] = {0, 0, 0}, s_r = 0, s_o = 0, s_K[4] = {0, 0, 0, 0}, s_p[3] = {0, 0, 0};
+        double s_R[9] = {0};
         std::vector<double> g_f(C, 0.0), a_f(C, 0.0);
         for (int64_t e = cnt[i]; e < cnt[i + 1]; ++e) {
             const int64_t pi = plist[e];
@@ -539,57 +545,78 @@ int64_t oracle_render(const double* pos, const double* radius, const double* opa
             for (int c = 0; c < C; ++c)
                 sdot += G[c] * (features[(size_t)i * C + c] - Fp[c]);
             const double sj = sdot / W;                        // dL/dw
-            // this pixel's contributions
-            double pc[3] = {0, 0, 0}, pr = 0, pk[4] = {0, 0, 0, 0};
+            // This pixel's contributions, except to the features, are sj times
+            // a factor; the factors ("per unit sj") are formed first, so that
+            // the sensitivity of each contribution to the image F
+            // (d sj / dF_c = -G_c / W) is available as well.
+            double uc[3] = {0, 0, 0}, ur = 0, uk[4] = {0, 0, 0, 0};
+            double gl1 = 0.0;
             for (int c = 0; c < C; ++c) {
                 g_f[c] += (w / W) * G[c];
                 if (gabs) a_f[c] += std::fabs((w / W) * G[c]);
+                gl1 += std::fabs(G[c]);
             }
-            const double po = sj * d * E * (1.0 + s.o * s.zt / gamma);   // dw/do
-            g_o += po;
-            if (gabs) a_o += std::fabs(po);
+            const double sens = gl1 / W;                      // sum_c |d sj / dF_c|
+            const double uo = d * E * (1.0 + s.o * s.zt / gamma);   // dw/do
+            g_o += sj * uo;
+            if (gabs) {
+                a_o += std::fabs(sj * uo);
+                s_o += std::fabs(uo) * sens;
+            }
             if (s.cut) continue;
             // dw/dz~ = w * o / gamma ; dz~/dc.z = -1/(zfar - znear)
-            pc[2] += sj * w * (s.o / gamma) * dzt_dz;
+            uc[2] += w * (s.o / gamma) * dzt_dz;
             // dw/dd = o E ; dd/drho = -1/r_eff ; dd/dr_eff = rho / r_eff^2
             const double rho = rq * s.c[2];
-            const double g_rho = -sj * s.o * E / s.reff;
-            const double g_reff = sj * s.o * E * rho / (s.reff * s.reff);
+            const double u_rho = -s.o * E / s.reff;
+            const double u_reff = s.o * E * rho / (s.reff * s.reff);
             if (s.floor_r) {
                 // r_eff = kappa c.z / f_min
-                pc[2] += g_reff * prm.kappa / fmin;
-                pk[fmin_is_fx ? 0 : 1] += g_reff * (-prm.kappa * s.c[2] / (fmin * fmin));
+                uc[2] += u_reff * prm.kappa / fmin;
+                uk[fmin_is_fx ? 0 : 1] += u_reff * (-prm.kappa * s.c[2] / (fmin * fmin));
             } else {
-                pr += g_reff;
+                ur += u_reff;
             }
             if (Q > 0.0) {
                 // drho/dc = e_perp / rho with e = c - c.z q = -c.z (U, V, 0)
                 const double k = (U * p.a + V * p.b) / p.qq;
                 const double n0 = -(U - k * p.a) / rq, n1 = -(V - k * p.b) / rq, n2 = k / rq;
-                pc[0] += g_rho * n0;
-                pc[1] += g_rho * n1;
-                pc[2] += g_rho * n2;
+                uc[0] += u_rho * n0;
+                uc[1] += u_rho * n1;
+                uc[2] += u_rho * n2;
                 // drho/dq = -(c.q / q.q) e_perp / rho, c.q / q.q = c.z (1 - k)
                 const double sq = -s.c[2] * (1.0 - k);
                 const double dqa = sq * n0, dqb = sq * n1;
                 // a = (px - cx)/fx, b = (py - cy)/fy
-                pk[0] += g_rho * dqa * (-p.a / cam.fx);
-                pk[1] += g_rho * dqb * (-p.b / cam.fy);
-                pk[2] += g_rho * dqa * (-1.0 / cam.fx);
-                pk[3] += g_rho * dqb * (-1.0 / cam.fy);
+                uk[0] += u_rho * dqa * (-p.a / cam.fx);
+                uk[1] += u_rho * dqb * (-p.b / cam.fy);
+                uk[2] += u_rho * dqa * (-1.0 / cam.fx);
+                uk[3] += u_rho * dqb * (-1.0 / cam.fy);
             }
-            for (int k = 0; k < 3; ++k) g_c[k] += pc[k];
-            for (int k = 0; k < 4; ++k) g_K[k] += pk[k];
-            g_r += pr;
+            for (int k = 0; k < 3; ++k) g_c[k] += sj * uc[k];
+            for (int k = 0; k < 4; ++k) g_K[k] += sj * uk[k];
+            g_r += sj * ur;
             if (gabs) {
-                for (int k = 0; k < 3; ++k) a_c[k] += std::fabs(pc[k]);
-                for (int k = 0; k < 4; ++k) a_K[k] += std::fabs(pk[k]);
-                a_r += std::fabs(pr);
-                for (int l = 0; l < 3; ++l)
-                    a_p[l] += std::fabs(cam.R[l] * pc[0] + cam.R[3 + l] * pc[1] +
-                                        cam.R[6 + l] * pc[2]);
+                for (int k = 0; k < 3; ++k) {
+                    a_c[k] += std::fabs(sj * uc[k]);
+                    s_c[k] += std::fabs(uc[k]) * sens;
+                }
+                for (int k = 0; k < 4; ++k) {
+                    a_K[k] += std::fabs(sj * uk[k]);
+                    s_K[k] += std::fabs(uk[k]) * sens;
+                }
+                a_r += std::fabs(sj * ur);
+                s_r += std::fabs(ur) * sens;
+                for (int l = 0; l < 3; ++l) {
+                    const double up = cam.R[l] * uc[0] + cam.R[3 + l] * uc[1] + cam.R[6 + l] * uc[2];
+                    a_p[l] += std::fabs(sj * up);
+                    s_p[l] += std::fabs(up) * sens;
+                }
                 for (int k = 0; k < 3; ++k)
-                    for (int l = 0; l < 3; ++l) a_R[3 * k + l] += std::fabs(pc[k] * pos[3 * i + l]);
+                    for (int l = 0; l < 3; ++l) {
+                        a_R[3 * k + l] += std::fabs(sj * uc[k] * pos[3 * i + l]);
+                        s_R[3 * k + l] += std::fabs(uc[k] * pos[3 * i + l]) * sens;
+                    }
             }
         }
         for (int k = 0; k < 3; ++k) gc[3 * i + k] = g_c[k];
@@ -610,6 +637,13 @@ int64_t oracle_render(const double* pos, const double* radius, const double* opa
             for (int k = 0; k < 3; ++k) ac[3 * i + k] = a_c[k];
             for (int k = 0; k < 4; ++k) ak[4 * i + k] = a_K[k];
             for (int k = 0; k < 9; ++k) acr[9 * i + k] = a_R[k];
+            double* sens_out = gabs + (5 + C) * n + 16;
+            for (int l = 0; l < 3; ++l) sens_out[3 * i + l] = s_p[l];
+            sens_out[3 * n + i] = s_r;
+            sens_out[4 * n + i] = s_o;
+            for (int k = 0; k < 3; ++k) sc_[3 * i + k] = s_c[k];
+            for (int k = 0; k < 4; ++k) sk[4 * i + k] = s_K[k];
+            for (int k = 0; k < 9; ++k) scr[9 * i + k] = s_R[k];
         }
     }
     if (grad_cam) {
@@ -631,6 +665,14 @@ int64_t oracle_render(const double* pos, const double* radius, const double* opa
             for (int k = 0; k < 4; ++k) a[12 + k] += ak[4 * i + k];
         }
         std::memcpy(gabs + (5 + C) * n, a, sizeof(a));
+        double sa[16] = {0};
+        for (int64_t i = 0; i < n; ++i) {
+            for (int k = 0; k < 9; ++k) sa[k] += scr[9 * i + k];
+            for (int k = 0; k < 3; ++k) sa[9 + k] += sc_[3 * i + k];
+            for (int k = 0; k < 4; ++k) sa[12 + k] += sk[4 * i + k];
+        }
+        double* sens_out = gabs + (5 + C) * n + 16;
+        std::memcpy(sens_out + (5 + C) * n, sa, sizeof(sa));
     }
     return total_hits;
 }

@@ -9,6 +9,9 @@ import numpy as np
 # A gradient entry is a sum of per-pixel contributions; where they cancel,
 # fp32 rounding scales with the sum of their absolute values A (the oracle
 # reports it), so the relative part is taken against max(|value|, A/10).
+# The backward also takes the forward's image F as input, which is itself only
+# within the forward tolerance: the bound adds FWD_ATOL times the entry's L1
+# sensitivity to F (also reported by the oracle).
 FWD_RTOL, FWD_ATOL = 1e-5, 1e-6
 GRAD_RTOL, GRAD_ATOL = 1e-4, 1e-5
 COND_FRACTION = 0.1
@@ -68,7 +71,7 @@ def run_gpu(scene, cam_index=0, grad_image=None, max_pairs=None, count_hits=True
     return out
 
 
-def close_report(gpu, ref, rtol, atol, abs_sum=None):
+def close_report(gpu, ref, rtol, atol, abs_sum=None, sens=None):
     gpu = np.asarray(gpu, np.float64)
     ref = np.asarray(ref, np.float64)
     err = np.abs(gpu - ref)
@@ -76,13 +79,15 @@ def close_report(gpu, ref, rtol, atol, abs_sum=None):
     if abs_sum is not None:
         scale = np.maximum(scale, COND_FRACTION * np.asarray(abs_sum, np.float64))
     bound = atol + rtol * scale
+    if sens is not None:
+        bound = bound + FWD_ATOL * np.asarray(sens, np.float64)
     bad = err > bound
     worst = float((err / bound).max()) if err.size else 0.0
     return int(bad.sum()), worst
 
 
-def assert_close(gpu, ref, rtol, atol, what, abs_sum=None):
-    nbad, worst = close_report(gpu, ref, rtol, atol, abs_sum)
+def assert_close(gpu, ref, rtol, atol, what, abs_sum=None, sens=None):
+    nbad, worst = close_report(gpu, ref, rtol, atol, abs_sum, sens)
     assert nbad == 0, f"{what}: {nbad} of {np.size(ref)} outside tolerance (worst {worst:.3g}x bound)"
 
 
@@ -121,7 +126,8 @@ def compare_frame(g, o, what="", window=None, grads=True):
     if grads:
         for k in ("grad_pos", "grad_radius", "grad_opacity", "grad_features", "grad_cam"):
             if k in g:
-                assert_close(g[k], o[k], GRAD_RTOL, GRAD_ATOL, f"{what} {k}", o.get("abs_" + k))
+                assert_close(g[k], o[k], GRAD_RTOL, GRAD_ATOL, f"{what} {k}", o.get("abs_" + k),
+                             o.get("sens_" + k))
 
 
 def windowed_grad(scene, cam_index, window):

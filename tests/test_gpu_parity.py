@@ -73,8 +73,8 @@ EDGE = {
     "five_channels": dict(seed=54, n=300, width=50, height=30, channels=5, n_track=9),
     "no_cutoff": dict(seed=55, n=500, width=64, height=48, geom_cutoff=False, rrange=(0.005, 0.2)),
     # big spheres: tile lists longer than one shared-memory sort (merge path)
-    "long_lists": dict(seed=56, n=6000, width=64, height=64, f=64.0, zrange=(2.5, 6.5),
-                       rrange=(0.3, 1.0), spread=1.5),
+    "long_lists": dict(seed=56, n=20000, width=64, height=64, f=64.0, zrange=(2.5, 6.5),
+                       rrange=(0.5, 1.5), spread=1.5),
     "spill_outside": dict(seed=57, n=2000, width=80, height=60, spread=2.5, rrange=(0.01, 0.5)),
 }
 
@@ -203,12 +203,12 @@ def test_partial_gradient_requests(oracle_lib):
     g = gh.run_gpu(sc, want=("opacity",))
     assert set(k for k in g if k.startswith("grad_")) == {"grad_opacity"}
     gh.assert_close(g["grad_opacity"], o["grad_opacity"], gh.GRAD_RTOL, gh.GRAD_ATOL, "opacity",
-                    o["abs_grad_opacity"])
+                    o["abs_grad_opacity"], o["sens_grad_opacity"])
     g = gh.run_gpu(sc, want=("cam", "features"))
     gh.assert_close(g["grad_cam"], o["grad_cam"], gh.GRAD_RTOL, gh.GRAD_ATOL, "cam",
-                    o["abs_grad_cam"])
+                    o["abs_grad_cam"], o["sens_grad_cam"])
     gh.assert_close(g["grad_features"], o["grad_features"], gh.GRAD_RTOL, gh.GRAD_ATOL, "feat",
-                    o["abs_grad_features"])
+                    o["abs_grad_features"], o["sens_grad_features"])
 
 
 def test_repeat_frames_and_determinism(oracle_lib):
