@@ -156,30 +156,26 @@ const char* pulsar_strerror(int code);
  * interface).  Copies `bytes` bytes (at most the array's size for the frame)
  * into dst (host or device; cudaMemcpyDefault).  Returns the array's size in
  * bytes for the current frame if dst is NULL, else PULSAR_OK or an error.
- *   PULSAR_DBG_REC0      [n] float4 (u_hi, u_lo, v_hi, v_lo) projected centre pair
- *   PULSAR_DBG_REC1      [n] float4 (s2 = (r_eff/c.z)^2, o z~/gamma as hi, lo, o)
- *   PULSAR_DBG_REC2      [n] float4 ((c.z/r_eff)^2 as hi, lo, c.z, r_eff)
- *   PULSAR_DBG_KEY       [n] float  depth key c.z - r_eff
- *   PULSAR_DBG_FLAGS     [n] uint32 bits: 1 kept, 2 radius on the kappa floor, 4 geometry cut
- *   PULSAR_DBG_RECT      [n] uint32 x2 (x0 | x1 << 16, y0 | y1 << 16) pixel rectangle
+ *   PULSAR_DBG_RECORDS   [n] 64-byte sphere records, 16 x 32-bit words:
+ *                        0-3   u_hi, u_lo, v_hi, v_lo  projected centre (float pairs)
+ *                        4-6   exponent o z~/gamma as hi, lo; opacity o
+ *                        7     flags: 1 kept, 2 radius on the kappa floor, 4 geometry cut
+ *                        8-11  (c.z/r_eff)^2 as hi, lo; c.z; r_eff
+ *                        12-13 pixel rectangle x0 | x1 << 16, y0 | y1 << 16
+ *                        14-15 s2 = (r_eff/c.z)^2, depth key c.z - r_eff
  *   PULSAR_DBG_TILE_OFFSETS [B+1] uint32 tile list offsets
  *   PULSAR_DBG_TILE_IDS  [M] uint32 sorted tile lists
  *   PULSAR_DBG_MG        [H*W] float  stabiliser m / gamma
  *   PULSAR_DBG_WSUM      [H*W] float  normaliser in the exp(-m/gamma) frame
  *   PULSAR_DBG_IDS       [n_track][H*W] int32 tracked ids, -1 padded
  *   PULSAR_DBG_NHITS     [H*W] int32 hits per pixel (PULSAR_FLAG_COUNT_HITS) */
-#define PULSAR_DBG_REC0          1
-#define PULSAR_DBG_REC1          2
-#define PULSAR_DBG_REC2          3
-#define PULSAR_DBG_RECT          4
+#define PULSAR_DBG_RECORDS       1
 #define PULSAR_DBG_TILE_OFFSETS  5
 #define PULSAR_DBG_TILE_IDS      6
 #define PULSAR_DBG_MG            7
 #define PULSAR_DBG_WSUM          8
 #define PULSAR_DBG_IDS           9
 #define PULSAR_DBG_NHITS        10
-#define PULSAR_DBG_FLAGS        11
-#define PULSAR_DBG_KEY          12
 int64_t pulsar_debug_copy(pulsar_ctx_t ctx, int what, void* dst, int64_t bytes, void* stream);
 
 #ifdef __cplusplus

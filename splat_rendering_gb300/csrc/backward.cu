@@ -39,7 +39,7 @@ __device__ __forceinline__ int nth_lane(uint32_t m, int n) {
 }
 
 template <int CMAX, int TMAX>
-__global__ void __launch_bounds__(kBwdThreads)
+__global__ void __launch_bounds__(kBwdThreads, CMAX <= 4 ? 4 : (CMAX <= 16 ? 2 : 1))
 k_backward(Frame f, Workspace w, const float* __restrict__ features,
            const float* __restrict__ image, const float* __restrict__ grad_image,
            float* __restrict__ grad_opacity, float* __restrict__ grad_features, int want_geom) {
@@ -77,18 +77,19 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
         for (int q = 0; q < NV; ++q) v[q] = 0.0f;
         bool cut = true;
         if (id >= 0) {
-            const float4 uv = w.rec0[id];
-            const float4 r1 = w.rec1[id];
-            const float4 r2 = w.rec2[id];
-            const uint32_t fl = w.sflags[id];
+            const SphereRec* rp = w.rec + id;
+            const float4 uv = rp->uv;
+            const float4 ex = rp->ex;
+            const float4 geo = rp->geo;
+            const uint32_t fl = __float_as_uint(ex.w);
             cut = (fl & kFlagCut) != 0u;
             float U, V;
             const float Q = ray_offset_q(uv, ray, f.ifx, f.ify, &U, &V);
             const float rq = sqrtf(Q * iqq);            // rho / c.z
             float t;
-            const float d = distance_factor(uv, r2.x, r2.y, ray, pq, f, &t);
-            const float o = r1.w;
-            const float E = expf(__fsub_rn(r1.y, mg) + r1.z);
+            const float d = distance_factor(uv, geo.x, geo.y, ray, pq, f, &t);
+            const float o = ex.z;
+            const float E = expf(__fsub_rn(ex.x, mg) + ex.y);
             const float wt = o * d * E;
             float sdot = 0.0f;
 #pragma unroll
@@ -100,9 +101,9 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
                 }
             }
             const float sj = sdot * iw;                 // dL/dw = <G, f - F> / W
-            v[4] = sj * d * E * (1.0f + r1.y);          // dw/do = d E (1 + o z~/gamma)
+            v[4] = sj * d * E * (1.0f + ex.x);          // dw/do = d E (1 + o z~/gamma)
             if (want_geom && !cut) {
-                const float Z = r2.z, reff = r2.w;
+                const float Z = geo.z, reff = geo.w;
                 const float ireff = 1.0f / reff;
                 const float sE = sj * o * E;            // dL/dd
                 // depth factor: dw/dz~ = w o / gamma, dz~/dc.z = -1/(zfar - znear)

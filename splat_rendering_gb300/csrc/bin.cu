@@ -71,14 +71,14 @@ __global__ void __launch_bounds__(kEmitThreads) k_emit(Frame f, Workspace w) {
     int tx0 = 0, ty0 = 0, ntx = 0, count = 0;
     uint32_t keybits = 0;
     if (i < f.n) {
-        const uint2 rc = w.rect[i];
-        const int x0 = rc.x & 0xffff, x1 = rc.x >> 16, y0 = rc.y & 0xffff, y1 = rc.y >> 16;
+        const uint4 rk = w.rec[i].rk;
+        const int x0 = rk.x & 0xffff, x1 = rk.x >> 16, y0 = rk.y & 0xffff, y1 = rk.y >> 16;
         if (x0 <= x1 && y0 <= y1) {
             tx0 = x0 / kTile;
             ty0 = y0 / kTile;
             ntx = x1 / kTile - tx0 + 1;
             count = ntx * (y1 / kTile - ty0 + 1);
-            keybits = __float_as_uint(w.key[i]);
+            keybits = rk.w;
         }
     }
     int incl = count;
@@ -117,12 +117,13 @@ __global__ void __launch_bounds__(kEmitThreads) k_emit(Frame f, Workspace w) {
 }
 
 // In-place ascending bitonic sort of s[0, np) (np a power of two), all
-// threads of the block participating.
+// threads of the block participating.  j is a power of two, so the pair index
+// is formed with masks: lo = 2 j floor(t / j) + t mod j.
 __device__ void block_bitonic(unsigned long long* s, int np) {
     for (int k = 2; k <= np; k <<= 1) {
         for (int j = k >> 1; j > 0; j >>= 1) {
             for (int t = threadIdx.x; t < (np >> 1); t += blockDim.x) {
-                const int lo = ((t / j) * (j << 1)) + (t % j);
+                const int lo = ((t & ~(j - 1)) << 1) | (t & (j - 1));
                 const int hi = lo + j;
                 const unsigned long long a = s[lo], b = s[hi];
                 const bool up = (lo & k) == 0;

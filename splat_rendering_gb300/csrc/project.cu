@@ -32,7 +32,7 @@ k_project(Frame f, Workspace w, const float* __restrict__ pos, const float* __re
         float4 r0 = make_float4(0.f, 0.f, 0.f, 0.f), r1 = r0, r2 = r0;
         uint2 rc = make_uint2(1u, 1u);   // empty: x0 = 1 > x1 = 0
         uint32_t flags = 0;
-        float key = 0.f;
+        float key = 0.f, s2 = 0.f;
         if (keep) {
             const FPair u = pair_project(f.fx, f.cx, pair_quotient(cx, cz));
             const FPair v = pair_project(f.fy, f.cy, pair_quotient(cy, cz));
@@ -42,7 +42,7 @@ k_project(Frame f, Workspace w, const float* __restrict__ pos, const float* __re
             if (keep) {
                 key = __fsub_rn(Z, reff);
                 const float tt = __fdiv_rn(reff, Z);
-                const float s2 = __fmul_rn(tt, tt);
+                s2 = __fmul_rn(tt, tt);
                 const float g = __fdiv_rn(__fmul_rn(f.fmin, r), Z);
                 const float area = __fmul_rn(kPi, __fmul_rn(g, g));
                 const bool cut = (f.flags & 1u) && !(area > f.amin);
@@ -58,7 +58,7 @@ k_project(Frame f, Workspace w, const float* __restrict__ pos, const float* __re
                 FPair e = ef_prod(on.hi, f.zk_hi);
                 e.lo = __fmaf_rn(on.hi, f.zk_lo, __fmaf_rn(on.lo, f.zk_hi, e.lo));
                 e = ef_fast_sum(e.hi, e.lo);
-                r1 = make_float4(s2, e.hi, e.lo, o);
+                r1 = make_float4(e.hi, e.lo, o, 0.0f);
                 // (c.z / r_eff)^2 as a pair: on the kappa floor c.z / r_eff = f_min / kappa
                 FPair ir;
                 if (on_floor) {
@@ -77,12 +77,12 @@ k_project(Frame f, Workspace w, const float* __restrict__ pos, const float* __re
                 count = ntx * (y1 / kTile - ty0 + 1);
             }
         }
-        w.rec0[i] = r0;
-        w.rec1[i] = r1;
-        w.rec2[i] = r2;
-        w.key[i] = key;
-        w.sflags[i] = flags;
-        w.rect[i] = rc;
+        r1.w = __uint_as_float(flags);
+        SphereRec* out = w.rec + i;
+        out->uv = r0;
+        out->ex = r1;
+        out->geo = r2;
+        out->rk = make_uint4(rc.x, rc.y, __float_as_uint(s2), __float_as_uint(key));
     }
     // warp-cooperative tile counting: flatten the warp's (sphere, tile) pairs
     int incl = count;

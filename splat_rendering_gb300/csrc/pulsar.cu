@@ -109,9 +109,7 @@ int pulsar_create(pulsar_ctx_t* out, int device, int64_t max_spheres, int64_t ma
     c->max_pix = (int64_t)max_width * max_height;
     const size_t N = (size_t)(max_spheres > 0 ? max_spheres : 1);
     Workspace& w = c->ws;
-    bool ok = alloc(c, &w.rec0, N) && alloc(c, &w.rec1, N) && alloc(c, &w.rec2, N) &&
-              alloc(c, &w.rect, N) && alloc(c, &w.gacc, N) && alloc(c, &w.sflags, N) &&
-              alloc(c, &w.key, N) &&
+    bool ok = alloc(c, &w.rec, N) && alloc(c, &w.gacc, N) &&
               alloc(c, &w.tile_count, (size_t)c->max_tiles) &&
               alloc(c, &w.tile_start, (size_t)c->max_tiles + 1) &&
               alloc(c, &w.pairs, (size_t)max_pairs) && alloc(c, &w.pairs_alt, (size_t)max_pairs) &&
@@ -284,12 +282,7 @@ int64_t pulsar_debug_copy(pulsar_ctx_t c, int what, void* dst, int64_t bytes, vo
     const void* src = nullptr;
     int64_t size = 0;
     switch (what) {
-        case PULSAR_DBG_REC0: src = c->ws.rec0; size = n * 16; break;
-        case PULSAR_DBG_REC1: src = c->ws.rec1; size = n * 16; break;
-        case PULSAR_DBG_REC2: src = c->ws.rec2; size = n * 16; break;
-        case PULSAR_DBG_RECT: src = c->ws.rect; size = n * 8; break;
-        case PULSAR_DBG_FLAGS: src = c->ws.sflags; size = n * 4; break;
-        case PULSAR_DBG_KEY: src = c->ws.key; size = n * 4; break;
+        case PULSAR_DBG_RECORDS: src = c->ws.rec; size = n * (int64_t)sizeof(SphereRec); break;
         case PULSAR_DBG_TILE_OFFSETS: src = c->ws.tile_start; size = (int64_t)(f.n_tiles + 1) * 4; break;
         case PULSAR_DBG_TILE_IDS: {
             uint32_t m = 0;

@@ -227,13 +227,22 @@ __device__ __forceinline__ bool rect_contains(uint2 rc, int x, int y) {
 }
 
 // ---------------------------------------------------------- workspace --
+// Per-sphere record written by the projection: 64 bytes, i.e. two 32-byte
+// sectors, so a gather by sphere id moves no byte it does not use.
+//   uv  : u_hi, u_lo, v_hi, v_lo             projected centre as float pairs
+//   ex  : e_hi, e_lo, o, flags (bits)         exponent o z~/gamma as a pair
+//   geo : ir2_hi, ir2_lo, c.z, r_eff          ir2 = (c.z / r_eff)^2 as a pair
+//   rk  : x0 | x1 << 16, y0 | y1 << 16, bits of s2 = (r_eff/c.z)^2, bits of
+//         the depth key c.z - r_eff           (decision quantities)
+struct __align__(16) SphereRec {
+    float4 uv;
+    float4 ex;
+    float4 geo;
+    uint4 rk;
+};
+
 struct Workspace {
-    float4* rec0;      // [maxN] u_hi, u_lo, v_hi, v_lo
-    float4* rec1;      // [maxN] s2 = (r_eff/c.z)^2, (o z~/gamma) as hi, lo, o
-    float4* rec2;      // [maxN] (c.z/r_eff)^2 as hi, lo, c.z, r_eff
-    float* key;        // [maxN] depth key c.z - r_eff
-    uint32_t* sflags;  // [maxN] kFlag* bits
-    uint2* rect;       // [maxN] pixel rectangle (x0 | x1<<16, y0 | y1<<16)
+    SphereRec* rec;    // [maxN]
     float4* gacc;      // [maxN] dL/dc.xyz, dL/dr accumulators (zero between frames)
     uint32_t* tile_count;   // [maxB] (zero between frames)
     uint32_t* tile_start;   // [maxB+1]

@@ -24,8 +24,7 @@ LIB_PATH = os.path.join(_HERE, "libpulsar.so")
 OK, ERR_ARG, ERR_CUDA, ERR_CAPACITY, ERR_STATE, ERR_NOMEM = 0, -1, -2, -3, -4, -5
 FLAG_GEOM_CUTOFF = 0x1
 FLAG_COUNT_HITS = 0x2
-DBG = dict(rec0=1, rec1=2, rec2=3, rect=4, tile_offsets=5, tile_ids=6, mg=7, wsum=8, ids=9,
-           nhits=10, flags=11, key=12)
+DBG = dict(records=1, tile_offsets=5, tile_ids=6, mg=7, wsum=8, ids=9, nhits=10)
 
 _lib = None
 

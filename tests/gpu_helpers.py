@@ -52,12 +52,8 @@ def run_gpu(scene, cam_index=0, grad_image=None, max_pairs=None, count_hits=True
     out.update(code=code, n_pairs=m, hits=h, image=img.cpu().numpy())
     if debug and code == 0:
         P = cam.width * cam.height
-        out["rec0"] = r.debug("rec0").view(np.float32).reshape(n, 4) if n else np.zeros((0, 4), np.float32)
-        out["rec1"] = r.debug("rec1").view(np.float32).reshape(n, 4) if n else np.zeros((0, 4), np.float32)
-        out["rec2"] = r.debug("rec2").view(np.float32).reshape(n, 4) if n else np.zeros((0, 4), np.float32)
-        out["rect"] = r.debug("rect").view(np.uint32).reshape(n, 2) if n else np.zeros((0, 2), np.uint32)
-        out["flags"] = r.debug("flags").view(np.uint32) if n else np.zeros(0, np.uint32)
-        out["key"] = r.debug("key").view(np.float32) if n else np.zeros(0, np.float32)
+        rec = r.debug("records").view(np.uint32).reshape(n, 16) if n else np.zeros((0, 16), np.uint32)
+        out["records"] = rec
         out["tile_offsets"] = r.debug("tile_offsets").view(np.uint32)
         out["tile_ids"] = r.debug("tile_ids").view(np.uint32)[:m] if m else np.zeros(0, np.uint32)
         out["mg"] = r.debug("mg").view(np.float32).reshape(cam.height, cam.width)
@@ -93,17 +89,18 @@ def assert_close(gpu, ref, rtol, atol, what, abs_sum=None, sens=None):
 
 def assert_decisions_equal(g, d):
     """Per-sphere fp32 decision quantities bit for bit (oracle.project output d)."""
-    fl = g["flags"]
+    rec = g["records"]
+    fl = rec[:, 7]
     keep = (fl & 1).astype(bool)
     assert np.array_equal(keep, d["keep"] == 1), "keep flags differ"
     k = keep
-    assert np.array_equal(g["rec0"][k].view(np.uint32), d["uv"][k].view(np.uint32)), "centre pair"
-    assert np.array_equal(g["rec2"][k, 3].view(np.uint32), d["reff"][k].view(np.uint32)), "r_eff"
-    assert np.array_equal(g["key"][k].view(np.uint32), d["key"][k].view(np.uint32)), "key"
-    assert np.array_equal(g["rec1"][k, 0].view(np.uint32), d["s2"][k].view(np.uint32)), "s2"
+    assert np.array_equal(rec[k, 0:4], d["uv"][k].view(np.uint32)), "centre pair"
+    assert np.array_equal(rec[k, 11], d["reff"][k].view(np.uint32)), "r_eff"
+    assert np.array_equal(rec[k, 15], d["key"][k].view(np.uint32)), "key"
+    assert np.array_equal(rec[k, 14], d["s2"][k].view(np.uint32)), "s2"
     assert np.array_equal(((fl >> 1) & 1)[k], d["floor"][k]), "floor flags"
     assert np.array_equal(((fl >> 2) & 1)[k], d["cut"][k]), "cutoff flags"
-    rect = g["rect"][k]
+    rect = rec[k, 12:14]
     got = np.stack([rect[:, 0] & 0xffff, rect[:, 0] >> 16, rect[:, 1] & 0xffff, rect[:, 1] >> 16], 1)
     assert np.array_equal(got.astype(np.int64), d["rect"][k].astype(np.int64)), "rectangles"
 
