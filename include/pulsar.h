@@ -158,14 +158,14 @@ const char* pulsar_strerror(int code);
  * bytes for the current frame if dst is NULL, else PULSAR_OK or an error.
  *   PULSAR_DBG_RECORDS   [n] 64-byte sphere records, 16 x 32-bit words:
  *                        0-3   u_hi, u_lo, v_hi, v_lo  projected centre (float pairs)
- *                        4-6   exponent o z~/gamma as hi, lo; opacity o
+ *                        4-6   exponent log2(e) o z~/gamma as hi, lo; opacity o
  *                        7     flags: 1 kept, 2 radius on the kappa floor, 4 geometry cut
  *                        8-11  (c.z/r_eff)^2 as hi, lo; c.z; r_eff
  *                        12-13 pixel rectangle x0 | x1 << 16, y0 | y1 << 16
  *                        14-15 s2 = (r_eff/c.z)^2, depth key c.z - r_eff
  *   PULSAR_DBG_TILE_OFFSETS [B+1] uint32 tile list offsets
  *   PULSAR_DBG_TILE_IDS  [M] uint32 sorted tile lists
- *   PULSAR_DBG_MG        [H*W] float  stabiliser m / gamma
+ *   PULSAR_DBG_MG        [H*W] float  stabiliser log2(e) m / gamma
  *   PULSAR_DBG_WSUM      [H*W] float  normaliser in the exp(-m/gamma) frame
  *   PULSAR_DBG_IDS       [n_track][H*W] int32 tracked ids, -1 padded
  *   PULSAR_DBG_NHITS     [H*W] int32 hits per pixel (PULSAR_FLAG_COUNT_HITS) */

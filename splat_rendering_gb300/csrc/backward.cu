@@ -56,7 +56,7 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
     const int p = inside ? y * f.width + x : 0;
     const PixelRay ray = pixel_ray(x, y, f);
     const PixelPairs pq = pixel_pairs(ray, f);
-    const float iqq = 1.0f / ray.qq;
+    const float iqq = pq.iqq;
     const uint32_t lt_mask = (1u << lane) - 1u;
 
     float G[CMAX], F[CMAX];
@@ -86,10 +86,9 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
             float U, V;
             const float Q = ray_offset_q(uv, ray, f.ifx, f.ify, &U, &V);
             const float rq = sqrtf(Q * iqq);            // rho / c.z
-            float t;
-            const float d = distance_factor(uv, geo.x, geo.y, ray, pq, f, &t);
+            const float d = distance_factor(uv, geo.x, geo.y, ray.px, ray.py, pq, f);
             const float o = ex.z;
-            const float E = expf(__fsub_rn(ex.x, mg) + ex.y);
+            const float E = exp2f(__fsub_rn(ex.x, mg) + ex.y);   // exponents in log2 units
             const float wt = o * d * E;
             float sdot = 0.0f;
 #pragma unroll
@@ -101,7 +100,7 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
                 }
             }
             const float sj = sdot * iw;                 // dL/dw = <G, f - F> / W
-            v[4] = sj * d * E * (1.0f + ex.x);          // dw/do = d E (1 + o z~/gamma)
+            v[4] = sj * d * E * (1.0f + ex.x * 0.693147181f);   // dw/do = d E (1 + o z~/gamma)
             if (want_geom && !cut) {
                 const float Z = geo.z, reff = geo.w;
                 const float ireff = 1.0f / reff;
@@ -183,14 +182,14 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
     if (tid < 4) {
         double s = 0.0;
         for (int q = 0; q < kBwdThreads / 32; ++q) s += (double)s_k[q][tid];
-        if (s != 0.0) atomicAdd(&w.state->cam_acc[12 + tid], s);
+        w.kpart[4 * tile + tid] = s;
     }
 }
 
 __global__ void __launch_bounds__(kFinThreads)
 k_finalize(Frame f, Workspace w, const float* __restrict__ pos, float* __restrict__ grad_pos,
            float* __restrict__ grad_radius, float* __restrict__ grad_cam) {
-    __shared__ double s_part[kFinThreads / 32][12];
+    __shared__ double s_part[kFinThreads / 32][16];
     __shared__ bool s_last;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float acc[12];
@@ -224,19 +223,39 @@ k_finalize(Frame f, Workspace w, const float* __restrict__ pos, float* __restric
     if (tid < 12) {
         double s = 0.0;
         for (int q = 0; q < kFinThreads / 32; ++q) s += s_part[q][tid];
-        if (s != 0.0) atomicAdd(&w.state->cam_acc[tid], s);
+        w.rtpart[12 * blockIdx.x + tid] = s;
     }
-    // last block out writes the camera gradient and clears the accumulators
+    // The last block to finish sums the per-block (R, t) and per-tile K
+    // partials in a fixed order -- no same-address atomics, deterministic.
     __threadfence();
     __syncthreads();
     if (tid == 0) s_last = atomicAdd(&w.state->ticket, 1u) == gridDim.x - 1;
     __syncthreads();
-    if (s_last && tid < 16) {
-        __threadfence();
-        volatile double* cam = w.state->cam_acc;
-        const double v = cam[tid];
-        if (grad_cam) grad_cam[tid] = (float)v;
-        cam[tid] = 0.0;
+    if (!s_last) return;
+    __threadfence();
+    double v[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) v[q] = 0.0;
+    const volatile double* rt = w.rtpart;
+    const volatile double* kp = w.kpart;
+    for (int b = tid; b < (int)gridDim.x; b += blockDim.x)
+#pragma unroll
+        for (int q = 0; q < 12; ++q) v[q] += rt[12 * b + q];
+    for (int b = tid; b < f.n_tiles; b += blockDim.x)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[12 + q] += kp[4 * b + q];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+        double s = v[q];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
+        if (lane == 0) s_part[warp][q] = s;
+    }
+    __syncthreads();
+    if (tid < 16) {
+        double s = 0.0;
+        for (int q = 0; q < kFinThreads / 32; ++q) s += s_part[q][tid];
+        if (grad_cam) grad_cam[tid] = (float)s;
         if (tid == 0) w.state->ticket = 0u;
     }
 }
@@ -285,7 +304,7 @@ cudaError_t launch_backward(const Frame& f, const Workspace& w, const float* pos
                                    grad_features, want_geom, stream);
     if (want_geom) {
         int blocks = (f.n + kFinThreads - 1) / kFinThreads;
-        blocks = blocks < 1 ? 1 : (blocks > 152 * 8 ? 152 * 8 : blocks);
+        blocks = blocks < 1 ? 1 : (blocks > kFinBlocks ? kFinBlocks : blocks);
         k_finalize<<<blocks, kFinThreads, 0, stream>>>(f, w, pos, grad_pos, grad_radius,
                                                        grad_cam);
     }

@@ -2,11 +2,10 @@
 // intersection; Sec. B.1.1 depth sort; Sec. B.1.2 16x16 blocks).
 //
 //   k_tile_scan  one block: exclusive scan of the per-tile pair counts -> tile
-//                offsets and M; latches a capacity error if M > max_pairs.
-//   k_emit       one thread per sphere, warp-cooperative over the warp's
-//                (sphere, tile) pairs: each pair takes a slot in its tile's
-//                bucket by counting the tile's counter back down to zero
-//                (so the counters are zero again for the next frame).
+//                offsets and M (the counters are cleared for the next frame);
+//                latches a capacity error if M > max_pairs.
+//   k_emit       one thread per staged pair (the projection gave each pair
+//                its slot in its tile): scatter (key, id) to offset + slot.
 //   k_tile_sort  one block per tile: sort the bucket by the 64-bit key
 //                (f32 bits of c.z - r_eff) << 32 | sphere id, which is unique,
 //                so the list does not depend on the bucket's arrival order.
@@ -22,8 +21,9 @@ namespace {
 
 constexpr int kScanThreads = 1024;
 constexpr int kEmitThreads = 256;
-constexpr int kSortThreads = 256;
+constexpr int kSortThreads = 128;
 constexpr int kSortCap = 2048;
+constexpr int kRegSortMax = 4 * kSortThreads;   // lists sorted in registers
 
 __global__ void __launch_bounds__(kScanThreads) k_tile_scan(Frame f, Workspace w) {
     __shared__ uint32_t s_warp[kScanThreads / 32];
@@ -56,63 +56,24 @@ __global__ void __launch_bounds__(kScanThreads) k_tile_scan(Frame f, Workspace w
     for (int b = b0; b < b1; ++b) {
         w.tile_start[b] = run;
         run += w.tile_count[b];
+        w.tile_count[b] = 0u;
     }
     if (tid == kScanThreads - 1) {
         w.tile_start[f.n_tiles] = run;
         w.state->n_pairs = run;
         w.state->hits = 0ull;
+        w.state->pair_cursor = 0u;
         if (run > f.max_pairs) atomicOr(&w.state->error, kErrCapacity);
     }
 }
 
 __global__ void __launch_bounds__(kEmitThreads) k_emit(Frame f, Workspace w) {
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    const int lane = threadIdx.x & 31;
-    int tx0 = 0, ty0 = 0, ntx = 0, count = 0;
-    uint32_t keybits = 0;
-    if (i < f.n) {
-        const uint4 rk = w.rec[i].rk;
-        const int x0 = rk.x & 0xffff, x1 = rk.x >> 16, y0 = rk.y & 0xffff, y1 = rk.y >> 16;
-        if (x0 <= x1 && y0 <= y1) {
-            tx0 = x0 / kTile;
-            ty0 = y0 / kTile;
-            ntx = x1 / kTile - tx0 + 1;
-            count = ntx * (y1 / kTile - ty0 + 1);
-            keybits = rk.w;
-        }
-    }
-    int incl = count;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-    }
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
-    const int warp_first = i - lane;
-    for (int j0 = 0; j0 < total; j0 += 32) {
-        const int j = j0 + lane;
-        int lo = 0, hi = 31;
-#pragma unroll
-        for (int s = 0; s < 5; ++s) {
-            const int mid = (lo + hi) >> 1;
-            const int pm = __shfl_sync(0xffffffffu, incl, mid);
-            if (pm > j) hi = mid; else lo = mid + 1;
-        }
-        const int own = lo;
-        const int own_incl = __shfl_sync(0xffffffffu, incl, own);
-        const int own_cnt = __shfl_sync(0xffffffffu, count, own);
-        const int own_tx0 = __shfl_sync(0xffffffffu, tx0, own);
-        const int own_ty0 = __shfl_sync(0xffffffffu, ty0, own);
-        const int own_ntx = __shfl_sync(0xffffffffu, ntx, own);
-        const uint32_t own_key = __shfl_sync(0xffffffffu, keybits, own);
-        if (j < total) {
-            const int k = j - (own_incl - own_cnt);
-            const int tile = (own_ty0 + k / own_ntx) * f.tiles_x + own_tx0 + k % own_ntx;
-            const uint32_t slot = atomicSub(&w.tile_count[tile], 1u) - 1u;
-            const uint32_t at = w.tile_start[tile] + slot;
-            if (at < f.max_pairs)
-                w.pairs[at] = ((unsigned long long)own_key << 32) | (uint32_t)(warp_first + own);
-        }
+    const uint32_t m = w.state->n_pairs;
+    if (m > f.max_pairs) return;   // overflowed frame: the capacity error is latched
+    for (uint32_t p = blockIdx.x * blockDim.x + threadIdx.x; p < m; p += gridDim.x * blockDim.x) {
+        const uint4 s = w.staged[p];
+        const uint32_t at = w.tile_start[s.x] + s.y;
+        if (at < m) w.pairs[at] = ((unsigned long long)s.z << 32) | s.w;
     }
 }
 
@@ -155,12 +116,82 @@ __device__ int merge_split(const unsigned long long* a, int la, const unsigned l
     return lo;
 }
 
+__device__ __forceinline__ unsigned long long cmp_keep(unsigned long long mine,
+                                                       unsigned long long other, bool take_min) {
+    return take_min ? (mine < other ? mine : other) : (mine < other ? other : mine);
+}
+
+__device__ __forceinline__ void cas_pair(unsigned long long& a, unsigned long long& b, bool up) {
+    if ((a > b) == up) {
+        const unsigned long long tmp = a;
+        a = b;
+        b = tmp;
+    }
+}
+
+// Ascending bitonic sort of up to kRegSortMax keys held in registers, four
+// per thread (thread t holds elements 4t .. 4t+3): stages with partner
+// distance 1 and 2 stay inside the thread, distances up to 64 use warp
+// shuffles, only the longer ones go through shared memory.
+__device__ void register_bitonic(unsigned long long (&e)[4], int np, unsigned long long* s) {
+    const int t = threadIdx.x;
+    for (int k = 2; k <= np; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            if (j >= 4 * 32) {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) s[4 * t + r] = e[r];
+                __syncthreads();
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int i = 4 * t + r;
+                    const unsigned long long p = s[i ^ j];
+                    e[r] = cmp_keep(e[r], p, ((i & j) == 0) == ((i & k) == 0));
+                }
+                __syncthreads();
+            } else if (j >= 4) {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int i = 4 * t + r;
+                    const unsigned long long p = __shfl_xor_sync(0xffffffffu, e[r], j >> 2);
+                    e[r] = cmp_keep(e[r], p, ((i & j) == 0) == ((i & k) == 0));
+                }
+            } else {
+                // inside the thread: pairs (0,1),(2,3) for j = 1; (0,2),(1,3) for j = 2;
+                // each pair's direction comes from its lower index
+                if (j == 1) {
+                    cas_pair(e[0], e[1], ((4 * t) & k) == 0);
+                    cas_pair(e[2], e[3], ((4 * t + 2) & k) == 0);
+                } else {
+                    cas_pair(e[0], e[2], ((4 * t) & k) == 0);
+                    cas_pair(e[1], e[3], ((4 * t + 1) & k) == 0);
+                }
+            }
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kSortThreads) k_tile_sort(Frame f, Workspace w) {
     __shared__ unsigned long long s[kSortCap];
     const int tile = blockIdx.x;
     const uint32_t start = w.tile_start[tile], end = w.tile_start[tile + 1];
     if (end > f.max_pairs || end <= start) return;   // capacity error already latched
     const int n = (int)(end - start);
+    if (n <= kRegSortMax) {
+        const int np = max(next_pow2(n), 128);
+        unsigned long long e[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int i = 4 * threadIdx.x + r;
+            e[r] = i < n ? w.pairs[start + i] : ~0ull;
+        }
+        register_bitonic(e, np, s);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int i = 4 * threadIdx.x + r;
+            if (i < n) w.tile_ids[start + i] = (uint32_t)e[r];
+        }
+        return;
+    }
     if (n <= kSortCap) {
         const int np = next_pow2(n);
         for (int t = threadIdx.x; t < np; t += blockDim.x)
@@ -213,8 +244,7 @@ __global__ void __launch_bounds__(kSortThreads) k_tile_sort(Frame f, Workspace w
 cudaError_t launch_bin(const Frame& f, const Workspace& w, cudaStream_t stream) {
     k_tile_scan<<<1, kScanThreads, 0, stream>>>(f, w);
     if (f.n > 0) {
-        const int blocks = (f.n + kEmitThreads - 1) / kEmitThreads;
-        k_emit<<<blocks, kEmitThreads, 0, stream>>>(f, w);
+        k_emit<<<152 * 8, kEmitThreads, 0, stream>>>(f, w);
         k_tile_sort<<<f.n_tiles, kSortThreads, 0, stream>>>(f, w);
     }
     return cudaGetLastError();

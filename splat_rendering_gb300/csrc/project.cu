@@ -2,8 +2,10 @@
 // Calculation"): one thread per sphere computes the camera-space centre,
 // culls, floors the radius so every sphere covers at least one pixel,
 // projects the centre, bounds the pixel rectangle without trigonometry and
-// forms the depth key; the warp then counts the sphere-tile pairs per tile
-// cooperatively, so a sphere covering many tiles does not stall its lane.
+// forms the depth key.  The warp then walks its (sphere, tile) pairs
+// cooperatively, so a sphere covering many tiles does not stall its lane:
+// each pair takes the next slot of its tile's counter and is staged, with
+// that slot, for the binning pass.
 #include "pulsar_internal.cuh"
 
 namespace pulsar {
@@ -17,6 +19,7 @@ k_project(Frame f, Workspace w, const float* __restrict__ pos, const float* __re
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     const int lane = threadIdx.x & 31;
     int tx0 = 0, ty0 = 0, ntx = 0, count = 0;
+    float key_out = 0.0f;
     if (i < f.n) {
         const float px = pos[3 * i], py = pos[3 * i + 1], pz = pos[3 * i + 2];
         const float r = radius[i], o = opacity[i];
@@ -48,9 +51,10 @@ k_project(Frame f, Workspace w, const float* __restrict__ pos, const float* __re
                 const bool cut = (f.flags & 1u) && !(area > f.amin);
                 flags = kFlagKeep | (on_floor ? kFlagFloor : 0u) | (cut ? kFlagCut : 0u);
                 r0 = make_float4(u.hi, u.lo, v.hi, v.lo);
-                // value path: the exponent o z~ / gamma = o (zfar - c.z) / ((zfar - znear) gamma)
-                // as a float pair; its magnitude reaches 1/gamma, so a single float would
-                // carry ~1e-6 absolute error into every weight through exp()
+                // value path: the exponent o z~ / gamma in log2 units,
+                // log2(e) o (zfar - c.z) / ((zfar - znear) gamma), as a float pair; its
+                // magnitude reaches 1.44/gamma, so a single float would carry ~1e-6
+                // absolute error into every weight through exp2()
                 const FPair nz = ef_sum(f.zfar, -cz.hi);
                 const FPair n = ef_fast_sum(nz.hi, __fsub_rn(nz.lo, cz.lo));
                 FPair on = ef_prod(o, n.hi);
@@ -75,6 +79,7 @@ k_project(Frame f, Workspace w, const float* __restrict__ pos, const float* __re
                 ty0 = y0 / kTile;
                 ntx = x1 / kTile - tx0 + 1;
                 count = ntx * (y1 / kTile - ty0 + 1);
+                key_out = key;
             }
         }
         r1.w = __uint_as_float(flags);
@@ -92,6 +97,10 @@ k_project(Frame f, Workspace w, const float* __restrict__ pos, const float* __re
         if (lane >= o) incl += v;
     }
     const int total = __shfl_sync(0xffffffffu, incl, 31);
+    uint32_t base = 0;
+    if (lane == 0 && total > 0) base = atomicAdd(&w.state->pair_cursor, (uint32_t)total);
+    base = __shfl_sync(0xffffffffu, base, 0);
+    const int warp_first = (blockIdx.x * blockDim.x + threadIdx.x) - lane;
     for (int j0 = 0; j0 < total; j0 += 32) {
         const int j = j0 + lane;
         // owner = first lane whose inclusive prefix exceeds j
@@ -108,10 +117,14 @@ k_project(Frame f, Workspace w, const float* __restrict__ pos, const float* __re
         const int own_tx0 = __shfl_sync(0xffffffffu, tx0, own);
         const int own_ty0 = __shfl_sync(0xffffffffu, ty0, own);
         const int own_ntx = __shfl_sync(0xffffffffu, ntx, own);
+        const uint32_t own_key = __shfl_sync(0xffffffffu, __float_as_uint(key_out), own);
         if (j < total) {
             const int k = j - (own_incl - own_cnt);
             const int tile = (own_ty0 + k / own_ntx) * f.tiles_x + own_tx0 + k % own_ntx;
-            atomicAdd(&w.tile_count[tile], 1u);
+            const uint32_t slot = atomicAdd(&w.tile_count[tile], 1u);
+            const uint32_t at = base + (uint32_t)j;
+            if (at < f.max_pairs)
+                w.staged[at] = make_uint4((uint32_t)tile, slot, own_key, (uint32_t)(warp_first + own));
         }
     }
 }

@@ -112,12 +112,16 @@ int pulsar_create(pulsar_ctx_t* out, int device, int64_t max_spheres, int64_t ma
     bool ok = alloc(c, &w.rec, N) && alloc(c, &w.gacc, N) &&
               alloc(c, &w.tile_count, (size_t)c->max_tiles) &&
               alloc(c, &w.tile_start, (size_t)c->max_tiles + 1) &&
+              alloc(c, &w.staged, (size_t)max_pairs) &&
               alloc(c, &w.pairs, (size_t)max_pairs) && alloc(c, &w.pairs_alt, (size_t)max_pairs) &&
               alloc(c, &w.tile_ids, (size_t)max_pairs) && alloc(c, &w.mg, (size_t)c->max_pix) &&
               alloc(c, &w.wsum, (size_t)c->max_pix) &&
               alloc(c, &w.ids, (size_t)c->max_pix * max_track) &&
-              alloc(c, &w.nhits, (size_t)c->max_pix) && alloc(c, &w.state, 1);
+              alloc(c, &w.nhits, (size_t)c->max_pix) &&
+              alloc(c, &w.kpart, (size_t)c->max_tiles * 4) &&
+              alloc(c, &w.rtpart, (size_t)kFinBlocks * 12) && alloc(c, &w.state, 1);
     if (ok) ok = cudaMallocHost(&c->host_state, sizeof(DevState)) == cudaSuccess;
+    if (ok) ok = prepare_forward() == cudaSuccess;
     // zero-between-frames invariants
     if (ok)
         ok = cudaMemset(w.gacc, 0, N * sizeof(float4)) == cudaSuccess &&
@@ -162,8 +166,11 @@ int pulsar_project(pulsar_ctx_t c, const float* pos, const float* radius, const 
     DeviceGuard guard(c->device);
     cudaStream_t s = as_stream(stream);
     if (c->counts_dirty) {
-        // a previous frame was projected but never binned: its counts are stale
+        // a previous frame was projected but never binned: its counts and staged
+        // pair cursor are stale
         cudaError_t e = cudaMemsetAsync(c->ws.tile_count, 0, (size_t)c->max_tiles * 4, s);
+        if (e == cudaSuccess)
+            e = cudaMemsetAsync(&c->ws.state->pair_cursor, 0, sizeof(uint32_t), s);
         if (e != cudaSuccess) return PULSAR_ERR_CUDA;
     }
     Frame& f = c->frame;
@@ -183,10 +190,12 @@ int pulsar_project(pulsar_ctx_t c, const float* pos, const float* radius, const 
     f.kappa = prm->kappa;
     f.amin = prm->geom_min_area;
     f.inv_zrange = 1.0f / (cam->zfar - cam->znear);
-    const double zk = 1.0 / (((double)cam->zfar - (double)cam->znear) * (double)prm->gamma);
+    // exponents are kept in log2 units (exp2 is the cheap hardware exponential)
+    const double log2e = 1.4426950408889634073599;
+    const double zk = log2e / (((double)cam->zfar - (double)cam->znear) * (double)prm->gamma);
     f.zk_hi = (float)zk;
     f.zk_lo = (float)(zk - (double)f.zk_hi);
-    const double eg = (double)prm->bg_eps / (double)prm->gamma;
+    const double eg = log2e * (double)prm->bg_eps / (double)prm->gamma;
     f.eg_hi = (float)eg;
     f.eg_lo = (float)(eg - (double)f.eg_hi);
     f.width = cam->width;

@@ -31,8 +31,8 @@ struct Frame {
     float fmin;           // min(fx, fy); fx on ties
     float gamma, inv_gamma, bg_eps, stop_tau, kappa, amin;
     float inv_zrange;     // 1/(zfar - znear)
-    float zk_hi, zk_lo;   // 1/((zfar - znear) gamma) as a float pair
-    float eg_hi, eg_lo;   // eps/gamma as a float pair
+    float zk_hi, zk_lo;   // log2(e)/((zfar - znear) gamma) as a float pair
+    float eg_hi, eg_lo;   // log2(e) eps/gamma as a float pair
     int width, height, tiles_x, tiles_y, n_tiles;
     int n_track, channels;
     int n;
@@ -45,9 +45,8 @@ struct DevState {
     unsigned long long hits;    // hit pairs composited by the last forward
     uint32_t n_pairs;           // M of the last bin
     uint32_t error;             // latched kErr* bits
-    uint32_t ticket;            // last-block election in the finalize kernel
-    uint32_t pad;
-    double cam_acc[16];         // camera gradient accumulators (zero between frames)
+    uint32_t ticket;            // last-block election in the finalize kernel (zero between frames)
+    uint32_t pair_cursor;       // staged pairs reserved by the projection (zero between frames)
 };
 
 // ------------------------------------------------ error-free transforms --
@@ -183,32 +182,44 @@ __device__ __forceinline__ FPair pp_sub(FPair x, FPair y) {
     return pp_add(x, FPair{-y.hi, -y.lo});
 }
 
-// Per-pixel ray slopes a, b and |q|^2 = 1 + a^2 + b^2 as pairs.
-struct PixelPairs { FPair a, b, qq; };
+// Per-pixel ray slopes a, b and |q|^2 = 1 + a^2 + b^2 as pairs, and 1/|q|^2.
+struct PixelPairs { FPair a, b, qq; float iqq; };
 
-__device__ __forceinline__ PixelPairs pixel_pairs(const PixelRay& r, const Frame& f) {
+__device__ __forceinline__ FPair slope_pair(float p, float c0, float ifl, float ifl_lo) {
+    return pp_mul(ef_sum(p, -c0), FPair{ifl, ifl_lo});
+}
+
+__device__ __forceinline__ PixelPairs pixel_pairs(FPair a, FPair b) {
     PixelPairs q;
-    q.a = pp_mul(ef_sum(r.px, -f.cx), FPair{f.ifx, f.ifx_lo});
-    q.b = pp_mul(ef_sum(r.py, -f.cy), FPair{f.ify, f.ify_lo});
-    q.qq = pp_add(pp_add(FPair{1.0f, 0.0f}, pp_sq(q.a)), pp_sq(q.b));
+    q.a = a;
+    q.b = b;
+    q.qq = pp_add(pp_add(FPair{1.0f, 0.0f}, pp_sq(a)), pp_sq(b));
+    q.iqq = __frcp_rn(q.qq.hi);
     return q;
 }
 
-// Distance factor d = 1 - rho / r_eff of a hit, accurate to ~1e-12 absolute
-// also at the silhouette, where 1 - rho/r_eff cancels catastrophically in
-// plain fp32 (Pulsar App. A: orthogonal ray-to-sphere distance).
+__device__ __forceinline__ PixelPairs pixel_pairs(const PixelRay& r, const Frame& f) {
+    return pixel_pairs(slope_pair(r.px, f.cx, f.ifx, f.ifx_lo),
+                       slope_pair(r.py, f.cy, f.ify, f.ify_lo));
+}
+
+// Distance factor d = 1 - rho / r_eff of a hit at pixel centre (px, py),
+// accurate to ~1e-12 absolute also at the silhouette, where 1 - rho/r_eff
+// cancels catastrophically in plain fp32 (Pulsar App. A: orthogonal
+// ray-to-sphere distance).
 //   rho^2 / r_eff^2 = Q ir2 / qq,  Q = U^2 + V^2 + (U b - V a)^2,
 //   U = (px - u)/fx, V = (py - v)/fy, ir2 = (c.z / r_eff)^2,
 //   d = (qq - Q ir2) / (qq (1 + rho / r_eff)).
-// Also returns t = (rho / r_eff)^2 in fp32.
+// The difference qq - Q ir2 is formed in pair arithmetic; the final scaling
+// is plain fp32 (a few ulps relative).
 __device__ __forceinline__ float distance_factor(const float4& uv, float ir2_hi, float ir2_lo,
-                                                 const PixelRay& r, const PixelPairs& pq,
-                                                 const Frame& f, float* t_out) {
+                                                 float px, float py, const PixelPairs& pq,
+                                                 const Frame& f) {
     // offsets to the projected centre, renormalised so that every hi part below
     // is the rounded value of its pair (px - u_hi is exact but coarse)
-    FPair du = ef_sum(r.px, -uv.x);
+    FPair du = ef_sum(px, -uv.x);
     du = ef_sum(du.hi, __fsub_rn(du.lo, uv.y));
-    FPair dv = ef_sum(r.py, -uv.z);
+    FPair dv = ef_sum(py, -uv.z);
     dv = ef_sum(dv.hi, __fsub_rn(dv.lo, uv.w));
     const FPair U = pp_mul(du, FPair{f.ifx, f.ifx_lo});
     const FPair V = pp_mul(dv, FPair{f.ify, f.ify_lo});
@@ -216,9 +227,9 @@ __device__ __forceinline__ float distance_factor(const float4& uv, float ir2_hi,
     const FPair Q = pp_add(pp_add(pp_sq(U), pp_sq(V)), pp_sq(X));
     const FPair Qs = pp_mul(Q, FPair{ir2_hi, ir2_lo});
     const FPair D = pp_sub(pq.qq, Qs);
-    const float t = __fdiv_rn(__fadd_rn(Qs.hi, Qs.lo), pq.qq.hi);
-    *t_out = t;
-    return __fdiv_rn(__fadd_rn(D.hi, D.lo), __fmul_rn(pq.qq.hi, __fadd_rn(1.0f, sqrtf(t))));
+    const float t = __fmul_rn(__fadd_rn(Qs.hi, Qs.lo), pq.iqq);   // (rho / r_eff)^2
+    const float Dq = __fmul_rn(__fadd_rn(D.hi, D.lo), pq.iqq);    // 1 - t
+    return __fmul_rn(Dq, __frcp_rn(__fadd_rn(1.0f, __fsqrt_rn(fmaxf(t, 0.0f)))));
 }
 
 __device__ __forceinline__ bool rect_contains(uint2 rc, int x, int y) {
@@ -246,6 +257,7 @@ struct Workspace {
     float4* gacc;      // [maxN] dL/dc.xyz, dL/dr accumulators (zero between frames)
     uint32_t* tile_count;   // [maxB] (zero between frames)
     uint32_t* tile_start;   // [maxB+1]
+    uint4* staged;          // [max_pairs] (tile, slot in tile, key bits, id) from the projection
     unsigned long long* pairs;      // [max_pairs] (key bits << 32 | id), bucketed by tile
     unsigned long long* pairs_alt;  // [max_pairs] merge scratch for long tiles
     uint32_t* tile_ids;     // [max_pairs] sorted tile lists
@@ -253,14 +265,19 @@ struct Workspace {
     float* wsum;            // [maxP]
     int32_t* ids;           // [maxT][maxP]
     int32_t* nhits;         // [maxP]
+    double* kpart;          // [maxB][4] per-tile partial dL/d(fx, fy, cx, cy)
+    double* rtpart;         // [kFinBlocks][12] per-block partial dL/dR, dL/dt
     DevState* state;
 };
+
+constexpr int kFinBlocks = 152 * 8;   // finalize grid (grid-stride over spheres)
 
 // ---------------------------------------------------------- launchers --
 // (defined in the .cu files; all enqueue on `stream` and never synchronise)
 cudaError_t launch_project(const Frame& f, const Workspace& w, const float* pos,
                            const float* radius, const float* opacity, cudaStream_t stream);
 cudaError_t launch_bin(const Frame& f, const Workspace& w, cudaStream_t stream);
+cudaError_t prepare_forward();   // opt the forward kernels into their shared memory
 cudaError_t launch_forward(const Frame& f, const Workspace& w, const float* features,
                            const float* bg, float* image, int max_pairs_stride,
                            cudaStream_t stream);

@@ -56,7 +56,9 @@ def run_gpu(scene, cam_index=0, grad_image=None, max_pairs=None, count_hits=True
         out["records"] = rec
         out["tile_offsets"] = r.debug("tile_offsets").view(np.uint32)
         out["tile_ids"] = r.debug("tile_ids").view(np.uint32)[:m] if m else np.zeros(0, np.uint32)
-        out["mg"] = r.debug("mg").view(np.float32).reshape(cam.height, cam.width)
+        # the stabiliser is stored in log2 units: m / gamma = mg2 ln 2
+        out["mg"] = r.debug("mg").view(np.float32).reshape(cam.height, cam.width).astype(
+            np.float64) * np.log(2.0)
         out["wsum"] = r.debug("wsum").view(np.float32).reshape(cam.height, cam.width)
         ids = r.debug("ids").view(np.int32).reshape(p.n_track, cam.height, cam.width)
         out["ids"] = np.moveaxis(ids, 0, -1)
