@@ -8,11 +8,12 @@
 // warp owns two pixel rows of the tile and first compacts, in list order, the
 // batch's candidates whose pixel rectangle touches its rows (cooperative
 // filtering at warp level).  Then, 32 candidates at a time:
-//   phase 1 (one lane per candidate): the lane runs the fp32 hit test of its
-//           candidate on every pixel of the warp's rows inside the
-//           candidate's rectangle; on a hit it evaluates the distance factor
-//           in pair precision, parks it in the warp's 32x32 d-matrix and sets
-//           the candidate's bit in the pixel's hit mask;
+//   phase 1 (flattened): the (candidate, pixel) pairs of the warp's rows
+//           inside each candidate's rectangle are numbered by a warp prefix
+//           sum and tested one per lane per round with the fp32 hit test; on
+//           a hit the lane evaluates the distance factor in pair precision,
+//           parks it in the warp's 32x32 d-matrix and sets the candidate's bit
+//           in the pixel's hit mask;
 //   phase 2 (one lane per pixel): the lane walks its mask bits in increasing
 //           order -- candidate order, i.e. earliest possible intersection
 //           first -- and blends each hit into its max-shifted running sums,
@@ -174,45 +175,73 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
             for (int k0 = 0; k0 < cnt; k0 += 32) {
                 s_hmask[warp][lane] = 0u;
                 __syncwarp();
-                // phase 1: one lane per candidate, over the warp's rows of its rectangle
+                // phase 1: the chunk's (candidate, pixel) tests, flattened over the warp:
+                // lane c describes candidate c's part of the warp's rows, a prefix sum
+                // numbers the tests, and each lane takes one test per round
+                int xa = 0, ya = 0, wd = 0, nt = 0, jc = 0;
                 if (k0 + lane < cnt) {
-                    const int j = s_list[warp][k0 + lane];
-                    const uint2 rc = s_rect[j];
-                    const float4 uv = s_uv[j];
-                    const float s2 = s_s2[j];
-                    const float2 ir2 = s_ir2[j];
-                    const int xa = max((int)(rc.x & 0xffffu), tx0);
+                    jc = s_list[warp][k0 + lane];
+                    const uint2 rc = s_rect[jc];
+                    xa = max((int)(rc.x & 0xffffu), tx0);
+                    ya = max((int)(rc.y & 0xffffu), row0);
                     const int xb = min((int)(rc.x >> 16), tx0 + kTile - 1);
-                    const int ya = max((int)(rc.y & 0xffffu), row0);
                     const int yb = min((int)(rc.y >> 16), row0 + 1);
-                    for (int yy = ya; yy <= yb; ++yy) {
+                    wd = xb - xa + 1;
+                    nt = (wd > 0 && yb >= ya) ? wd * (yb - ya + 1) : 0;
+                }
+                int incl = nt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += v;
+                }
+                const int total = __shfl_sync(0xffffffffu, incl, 31);
+                for (int t0 = 0; t0 < total; t0 += 32) {
+                    const int t = t0 + lane;
+                    int lo = 0, hi = 31;
+#pragma unroll
+                    for (int st = 0; st < 5; ++st) {
+                        const int mid = (lo + hi) >> 1;
+                        if (__shfl_sync(0xffffffffu, incl, mid) > t) hi = mid; else lo = mid + 1;
+                    }
+                    const int own = lo;
+                    const int o_first = __shfl_sync(0xffffffffu, incl - nt, own);
+                    const int o_xa = __shfl_sync(0xffffffffu, xa, own);
+                    const int o_ya = __shfl_sync(0xffffffffu, ya, own);
+                    const int o_wd = __shfl_sync(0xffffffffu, wd, own);
+                    const int o_j = __shfl_sync(0xffffffffu, jc, own);
+                    if (t < total) {
+                        // at most two rows: test q of the owner is (q mod wd, q div wd)
+                        const int q = t - o_first;
+                        const int second = q >= o_wd ? 1 : 0;
+                        const int xx = o_xa + q - second * o_wd;
+                        const int yy = o_ya + second;
+                        const float4 uv = s_uv[o_j];
+                        // the decision test of the specification, term by term
+                        const float a = s_a[xx - tx0];
                         const float b = s_b[yy - ty0];
+                        const float px = __fadd_rn(__int2float_rn(xx), 0.5f);
                         const float py = __fadd_rn(__int2float_rn(yy), 0.5f);
+                        const float U = __fmul_rn(__fsub_rn(__fsub_rn(px, uv.x), uv.y), f.ifx);
                         const float V = __fmul_rn(__fsub_rn(__fsub_rn(py, uv.z), uv.w), f.ify);
-                        const float bb = __fmul_rn(b, b);
-                        const float2 bpv = s_bp[yy - ty0];
-                        for (int xx = xa; xx <= xb; ++xx) {
-                            // the decision test of the specification, term by term
-                            const float a = s_a[xx - tx0];
-                            const float px = __fadd_rn(__int2float_rn(xx), 0.5f);
-                            const float U = __fmul_rn(__fsub_rn(__fsub_rn(px, uv.x), uv.y), f.ifx);
-                            const float X = __fmaf_rn(U, b, -__fmul_rn(V, a));
-                            const float Q = __fmaf_rn(U, U, __fmaf_rn(V, V, __fmul_rn(X, X)));
-                            const float qq = __fadd_rn(__fadd_rn(1.0f, __fmul_rn(a, a)), bb);
-                            if (Q < __fmul_rn(s2, qq)) {
-                                const int pl = (yy - ty0) * kTile + (xx - tx0);   // pixel in tile
-                                const int pw = (yy - row0) * kTile + (xx - tx0);  // pixel in warp
-                                PixelPairs pq;
-                                const float2 apv = s_ap[xx - tx0];
-                                const float2 qqv = s_qq[pl];
-                                pq.a = {apv.x, apv.y};
-                                pq.b = {bpv.x, bpv.y};
-                                pq.qq = {qqv.x, qqv.y};
-                                pq.iqq = s_iqq[pl];
-                                s_dmat[warp][pw][lane ^ pw] =
-                                    distance_factor(uv, ir2.x, ir2.y, px, py, pq, f);
-                                atomicOr(&s_hmask[warp][pw], 1u << lane);
-                            }
+                        const float X = __fmaf_rn(U, b, -__fmul_rn(V, a));
+                        const float Q = __fmaf_rn(U, U, __fmaf_rn(V, V, __fmul_rn(X, X)));
+                        const float qq = __fadd_rn(__fadd_rn(1.0f, __fmul_rn(a, a)), __fmul_rn(b, b));
+                        if (Q < __fmul_rn(s_s2[o_j], qq)) {
+                            const int pl = (yy - ty0) * kTile + (xx - tx0);   // pixel in tile
+                            const int pw = (yy - row0) * kTile + (xx - tx0);  // pixel in warp
+                            const float2 apv = s_ap[xx - tx0];
+                            const float2 bpv = s_bp[yy - ty0];
+                            const float2 qqv = s_qq[pl];
+                            const float2 ir2 = s_ir2[o_j];
+                            PixelPairs pq;
+                            pq.a = {apv.x, apv.y};
+                            pq.b = {bpv.x, bpv.y};
+                            pq.qq = {qqv.x, qqv.y};
+                            pq.iqq = s_iqq[pl];
+                            s_dmat[warp][pw][own ^ pw] =
+                                distance_factor(uv, ir2.x, ir2.y, px, py, pq, f);
+                            atomicOr(&s_hmask[warp][pw], 1u << own);
                         }
                     }
                 }
