@@ -55,8 +55,7 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
     const int P = f.width * f.height;
     const int p = inside ? y * f.width + x : 0;
     const PixelRay ray = pixel_ray(x, y, f);
-    const PixelPairs pq = pixel_pairs(ray, f);
-    const float iqq = pq.iqq;
+    const float iqq = __frcp_rn(ray.qq);
     const uint32_t lt_mask = (1u << lane) - 1u;
 
     float G[CMAX], F[CMAX];
@@ -86,7 +85,7 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
             float U, V;
             const float Q = ray_offset_q(uv, ray, f.ifx, f.ify, &U, &V);
             const float rq = sqrtf(Q * iqq);            // rho / c.z
-            const float d = distance_factor(uv, geo.x, geo.y, ray.px, ray.py, pq, f);
+            const float d = w.dtr[(size_t)k * P + p];     // stored by the forward pass
             const float o = ex.z;
             const float E = exp2f(__fsub_rn(ex.x, mg) + ex.y);   // exponents in log2 units
             const float wt = o * d * E;
@@ -145,8 +144,9 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
                 v[3] = gr;
             }
         }
-        // group the lanes that hold the same sphere and tree-reduce within groups
-        const uint32_t peers = __match_any_sync(0xffffffffu, id);
+        // group the lanes that hold the same sphere and tree-reduce within groups;
+        // lanes without a k-th hit get distinct keys, so they form no group
+        const uint32_t peers = __match_any_sync(0xffffffffu, id >= 0 ? id : -1 - lane);
         const int rank = __popc(peers & lt_mask);
         const int gsz = __popc(peers);
         const int gmax = __reduce_max_sync(0xffffffffu, gsz);
@@ -236,14 +236,21 @@ k_finalize(Frame f, Workspace w, const float* __restrict__ pos, float* __restric
     double v[16];
 #pragma unroll
     for (int q = 0; q < 16; ++q) v[q] = 0.0;
-    const volatile double* rt = w.rtpart;
-    const volatile double* kp = w.kpart;
+    // L2 loads (the partials were written by other blocks), independent of one
+    // another so that many are in flight at once
+#pragma unroll 2
     for (int b = tid; b < (int)gridDim.x; b += blockDim.x)
 #pragma unroll
-        for (int q = 0; q < 12; ++q) v[q] += rt[12 * b + q];
-    for (int b = tid; b < f.n_tiles; b += blockDim.x)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) v[12 + q] += kp[4 * b + q];
+        for (int q = 0; q < 12; ++q) v[q] += __ldcg(w.rtpart + 12 * b + q);
+#pragma unroll 4
+    for (int b = tid; b < f.n_tiles; b += blockDim.x) {
+        const double2 k01 = __ldcg(reinterpret_cast<const double2*>(w.kpart) + 2 * b);
+        const double2 k23 = __ldcg(reinterpret_cast<const double2*>(w.kpart) + 2 * b + 1);
+        v[12] += k01.x;
+        v[13] += k01.y;
+        v[14] += k23.x;
+        v[15] += k23.y;
+    }
 #pragma unroll
     for (int q = 0; q < 16; ++q) {
         double s = v[q];

@@ -126,9 +126,8 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
     float acc[CMAX];
 #pragma unroll
     for (int c = 0; c < CMAX; ++c) acc[c] = c < C ? bg[c] : 0.0f;
-    int ids[TMAX];
-#pragma unroll
-    for (int k = 0; k < TMAX; ++k) ids[k] = -1;
+    const int P = f.width * f.height;
+    const int p = inside ? y * f.width + x : 0;
     int nh = 0;
     bool done = !inside;
     if (tid == 0) *s_hits = 0ull;
@@ -268,9 +267,9 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
                     for (int c = 0; c < CMAX; ++c)
                         if (c < C) acc[c] += wt * s_feat[j * CMAX + c];
                     if (nh < f.n_track) {
-#pragma unroll
-                        for (int k = 0; k < TMAX; ++k)
-                            if (k == nh) ids[k] = s_id[j];
+                        // backward-information buffer: id and distance factor of the hit
+                        w.ids[(size_t)nh * P + p] = s_id[j];
+                        w.dtr[(size_t)nh * P + p] = d;
                     }
                     ++nh;
                 }
@@ -290,8 +289,6 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
     }
 
     if (inside) {
-        const int P = f.width * f.height;
-        const int p = y * f.width + x;
         const float iw = 1.0f / wsum;
 #pragma unroll
         for (int c = 0; c < CMAX; ++c)
@@ -299,9 +296,7 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
         // store the stabiliser's high part; fold its low part into the normaliser
         w.mg[p] = mg;
         w.wsum[p] = wsum * exp2f(mgl);
-#pragma unroll
-        for (int k = 0; k < TMAX; ++k)
-            if (k < f.n_track) w.ids[(size_t)k * P + p] = ids[k];
+        for (int k = nh; k < f.n_track; ++k) w.ids[(size_t)k * P + p] = -1;
         if (f.flags & 2u) w.nhits[p] = nh;
     }
     // hit count of the frame

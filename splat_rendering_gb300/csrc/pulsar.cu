@@ -117,6 +117,7 @@ int pulsar_create(pulsar_ctx_t* out, int device, int64_t max_spheres, int64_t ma
               alloc(c, &w.tile_ids, (size_t)max_pairs) && alloc(c, &w.mg, (size_t)c->max_pix) &&
               alloc(c, &w.wsum, (size_t)c->max_pix) &&
               alloc(c, &w.ids, (size_t)c->max_pix * max_track) &&
+              alloc(c, &w.dtr, (size_t)c->max_pix * max_track) &&
               alloc(c, &w.nhits, (size_t)c->max_pix) &&
               alloc(c, &w.kpart, (size_t)c->max_tiles * 4) &&
               alloc(c, &w.rtpart, (size_t)kFinBlocks * 12) && alloc(c, &w.state, 1);

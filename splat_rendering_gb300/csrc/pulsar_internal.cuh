@@ -263,7 +263,8 @@ struct Workspace {
     uint32_t* tile_ids;     // [max_pairs] sorted tile lists
     float* mg;              // [maxP]
     float* wsum;            // [maxP]
-    int32_t* ids;           // [maxT][maxP]
+    int32_t* ids;           // [maxT][maxP] tracked sphere ids, -1 padded
+    float* dtr;             // [maxT][maxP] distance factor d of each tracked hit
     int32_t* nhits;         // [maxP]
     double* kpart;          // [maxB][4] per-tile partial dL/d(fx, fy, cx, cy)
     double* rtpart;         // [kFinBlocks][12] per-block partial dL/dR, dL/dt
