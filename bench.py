@@ -31,7 +31,7 @@ sys.path.insert(0, ROOT)
 WORKLOAD = "headline: 1,000,000 spheres, 1024x1024, 3 channels, n_track 5, R/t/K gradients"
 METRIC = "fwd+bwd frames/s at 1M spheres 1024^2"
 UNIT = "frames/s"
-KERNELS_PER_STEP = 7   # project, tile_scan, emit, tile_sort, forward, backward, finalize
+KERNELS_PER_STEP = 8   # project, tile_scan, emit, tile_sort, forward, backward, finalize, camera_reduce
 
 
 def args_parse():

@@ -12,13 +12,12 @@
 //             opacity and feature gradients go straight to the caller's
 //             (zeroed) arrays.  The intrinsics' gradient is summed per thread,
 //             reduced per block and added to fp64 accumulators.
-// k_finalize  one thread per sphere (grid-stride): dL/dp = R^T dL/dc and
-//             dL/dr out of the accumulator (which it zeroes for the next
-//             frame); dL/dR = sum dL/dc p^T and dL/dt = sum dL/dc reduced
-//             per block into fp64 accumulators; the last block to finish
-//             writes grad_cam and clears the accumulators (Pulsar Sec. B.2:
-//             sphere-wise camera-gradient accumulation, then a device-wide
-//             reduction).
+// k_finalize  one thread per sphere: dL/dp = R^T dL/dc and dL/dr out of the
+//             accumulator (which it zeroes for the next frame);
+//             dL/dR = sum dL/dc p^T and dL/dt = sum dL/dc reduced per block
+//             (Pulsar Sec. B.2: sphere-wise camera-gradient accumulation).
+// k_camera_reduce  one block sums all per-block partials in a fixed order
+//             into grad_cam (the device-wide reduction).
 #include "pulsar_internal.cuh"
 
 namespace pulsar {
@@ -26,6 +25,7 @@ namespace {
 
 constexpr int kBwdThreads = kTilePix;
 constexpr int kFinThreads = 256;
+constexpr int kCamThreads = 1024;
 
 __device__ __forceinline__ void red_add_v4(float4* addr, float a, float b, float c, float d) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
@@ -188,15 +188,17 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
 
 __global__ void __launch_bounds__(kFinThreads)
 k_finalize(Frame f, Workspace w, const float* __restrict__ pos, float* __restrict__ grad_pos,
-           float* __restrict__ grad_radius, float* __restrict__ grad_cam) {
-    __shared__ double s_part[kFinThreads / 32][16];
-    __shared__ bool s_last;
+           float* __restrict__ grad_radius) {
+    __shared__ float s_part[kFinThreads / 32][12];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int i = blockIdx.x * blockDim.x + tid;
     float acc[12];
 #pragma unroll
     for (int q = 0; q < 12; ++q) acc[q] = 0.0f;
-    for (int i = blockIdx.x * blockDim.x + tid; i < f.n; i += gridDim.x * blockDim.x) {
+    if (i < f.n) {
+        // both loads issued together; the accumulator is cleared for the next frame
         const float4 g = w.gacc[i];
+        const float px = pos[3 * i], py = pos[3 * i + 1], pz = pos[3 * i + 2];
         w.gacc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (grad_pos) {
             grad_pos[3 * i + 0] = f.R[0] * g.x + f.R[3] * g.y + f.R[6] * g.z;
@@ -204,53 +206,42 @@ k_finalize(Frame f, Workspace w, const float* __restrict__ pos, float* __restric
             grad_pos[3 * i + 2] = f.R[2] * g.x + f.R[5] * g.y + f.R[8] * g.z;
         }
         if (grad_radius) grad_radius[i] = g.w;
-        if (g.x != 0.0f || g.y != 0.0f || g.z != 0.0f) {
-            const float px = pos[3 * i], py = pos[3 * i + 1], pz = pos[3 * i + 2];
-            acc[0] += g.x * px; acc[1] += g.x * py; acc[2] += g.x * pz;
-            acc[3] += g.y * px; acc[4] += g.y * py; acc[5] += g.y * pz;
-            acc[6] += g.z * px; acc[7] += g.z * py; acc[8] += g.z * pz;
-            acc[9] += g.x; acc[10] += g.y; acc[11] += g.z;
-        }
+        acc[0] = g.x * px; acc[1] = g.x * py; acc[2] = g.x * pz;
+        acc[3] = g.y * px; acc[4] = g.y * py; acc[5] = g.y * pz;
+        acc[6] = g.z * px; acc[7] = g.z * py; acc[8] = g.z * pz;
+        acc[9] = g.x; acc[10] = g.y; acc[11] = g.z;
     }
 #pragma unroll
     for (int q = 0; q < 12; ++q) {
         float s = acc[q];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
-        if (lane == 0) s_part[warp][q] = (double)s;
+        if (lane == 0) s_part[warp][q] = s;
     }
     __syncthreads();
     if (tid < 12) {
         double s = 0.0;
-        for (int q = 0; q < kFinThreads / 32; ++q) s += s_part[q][tid];
+        for (int q = 0; q < kFinThreads / 32; ++q) s += (double)s_part[q][tid];
         w.rtpart[12 * blockIdx.x + tid] = s;
     }
-    // The last block to finish sums the per-block (R, t) and per-tile K
-    // partials in a fixed order -- no same-address atomics, deterministic.
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_last = atomicAdd(&w.state->ticket, 1u) == gridDim.x - 1;
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
+}
+
+// One block: dL/dR and dL/dt from the finalize blocks' partials and
+// dL/d(fx, fy, cx, cy) from the backward tiles' partials, summed in a fixed
+// order (deterministic; Pulsar Sec. B.2's device-wide camera reduction).
+__global__ void __launch_bounds__(kCamThreads)
+k_camera_reduce(Frame f, Workspace w, int fin_blocks, float* __restrict__ grad_cam) {
+    __shared__ double s_part[kCamThreads / 32][16];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     double v[16];
 #pragma unroll
     for (int q = 0; q < 16; ++q) v[q] = 0.0;
-    // L2 loads (the partials were written by other blocks), independent of one
-    // another so that many are in flight at once
-#pragma unroll 2
-    for (int b = tid; b < (int)gridDim.x; b += blockDim.x)
+    for (int b = tid; b < fin_blocks; b += kCamThreads)
 #pragma unroll
-        for (int q = 0; q < 12; ++q) v[q] += __ldcg(w.rtpart + 12 * b + q);
-#pragma unroll 4
-    for (int b = tid; b < f.n_tiles; b += blockDim.x) {
-        const double2 k01 = __ldcg(reinterpret_cast<const double2*>(w.kpart) + 2 * b);
-        const double2 k23 = __ldcg(reinterpret_cast<const double2*>(w.kpart) + 2 * b + 1);
-        v[12] += k01.x;
-        v[13] += k01.y;
-        v[14] += k23.x;
-        v[15] += k23.y;
-    }
+        for (int q = 0; q < 12; ++q) v[q] += w.rtpart[12 * b + q];
+    for (int b = tid; b < f.n_tiles; b += kCamThreads)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[12 + q] += w.kpart[4 * b + q];
 #pragma unroll
     for (int q = 0; q < 16; ++q) {
         double s = v[q];
@@ -261,9 +252,8 @@ k_finalize(Frame f, Workspace w, const float* __restrict__ pos, float* __restric
     __syncthreads();
     if (tid < 16) {
         double s = 0.0;
-        for (int q = 0; q < kFinThreads / 32; ++q) s += s_part[q][tid];
+        for (int q = 0; q < kCamThreads / 32; ++q) s += s_part[q][tid];
         if (grad_cam) grad_cam[tid] = (float)s;
-        if (tid == 0) w.state->ticket = 0u;
     }
 }
 
@@ -310,10 +300,10 @@ cudaError_t launch_backward(const Frame& f, const Workspace& w, const float* pos
         launch_bwd_c<kMaxChannels>(f, w, features, image, grad_image, grad_opacity,
                                    grad_features, want_geom, stream);
     if (want_geom) {
-        int blocks = (f.n + kFinThreads - 1) / kFinThreads;
-        blocks = blocks < 1 ? 1 : (blocks > kFinBlocks ? kFinBlocks : blocks);
-        k_finalize<<<blocks, kFinThreads, 0, stream>>>(f, w, pos, grad_pos, grad_radius,
-                                                       grad_cam);
+        const int blocks = (f.n + kFinThreads - 1) / kFinThreads;
+        if (blocks > 0)
+            k_finalize<<<blocks, kFinThreads, 0, stream>>>(f, w, pos, grad_pos, grad_radius);
+        k_camera_reduce<<<1, kCamThreads, 0, stream>>>(f, w, blocks, grad_cam);
     }
     return cudaGetLastError();
 }

@@ -120,7 +120,7 @@ int pulsar_create(pulsar_ctx_t* out, int device, int64_t max_spheres, int64_t ma
               alloc(c, &w.dtr, (size_t)c->max_pix * max_track) &&
               alloc(c, &w.nhits, (size_t)c->max_pix) &&
               alloc(c, &w.kpart, (size_t)c->max_tiles * 4) &&
-              alloc(c, &w.rtpart, (size_t)kFinBlocks * 12) && alloc(c, &w.state, 1);
+              alloc(c, &w.rtpart, (N + 255) / 256 * 12) && alloc(c, &w.state, 1);
     if (ok) ok = cudaMallocHost(&c->host_state, sizeof(DevState)) == cudaSuccess;
     if (ok) ok = prepare_forward() == cudaSuccess;
     // zero-between-frames invariants

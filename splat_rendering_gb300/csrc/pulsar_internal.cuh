@@ -45,7 +45,7 @@ struct DevState {
     unsigned long long hits;    // hit pairs composited by the last forward
     uint32_t n_pairs;           // M of the last bin
     uint32_t error;             // latched kErr* bits
-    uint32_t ticket;            // last-block election in the finalize kernel (zero between frames)
+    uint32_t pad;
     uint32_t pair_cursor;       // staged pairs reserved by the projection (zero between frames)
 };
 
@@ -267,11 +267,9 @@ struct Workspace {
     float* dtr;             // [maxT][maxP] distance factor d of each tracked hit
     int32_t* nhits;         // [maxP]
     double* kpart;          // [maxB][4] per-tile partial dL/d(fx, fy, cx, cy)
-    double* rtpart;         // [kFinBlocks][12] per-block partial dL/dR, dL/dt
+    double* rtpart;         // [ceil(maxN/256)][12] per-block partial dL/dR, dL/dt
     DevState* state;
 };
-
-constexpr int kFinBlocks = 152 * 8;   // finalize grid (grid-stride over spheres)
 
 // ---------------------------------------------------------- launchers --
 // (defined in the .cu files; all enqueue on `stream` and never synchronise)
