@@ -180,9 +180,11 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
     }
     __syncthreads();
     if (tid < 4) {
-        double s = 0.0;
-        for (int q = 0; q < kBwdThreads / 32; ++q) s += (double)s_k[q][tid];
-        w.kpart[4 * tile + tid] = s;
+        // compensated (float pair) sum of the warp partials; this GPU's fp64
+        // pipe is far too slow even for reductions
+        FPair s = {0.0f, 0.0f};
+        for (int q = 0; q < kBwdThreads / 32; ++q) s = pp_add(s, FPair{s_k[q][tid], 0.0f});
+        w.kpart[4 * tile + tid] = make_float2(s.hi, s.lo);
     }
 }
 
@@ -220,40 +222,54 @@ k_finalize(Frame f, Workspace w, const float* __restrict__ pos, float* __restric
     }
     __syncthreads();
     if (tid < 12) {
-        double s = 0.0;
-        for (int q = 0; q < kFinThreads / 32; ++q) s += (double)s_part[q][tid];
-        w.rtpart[12 * blockIdx.x + tid] = s;
+        FPair s = {0.0f, 0.0f};
+        for (int q = 0; q < kFinThreads / 32; ++q) s = pp_add(s, FPair{s_part[q][tid], 0.0f});
+        w.rtpart[12 * blockIdx.x + tid] = make_float2(s.hi, s.lo);
     }
 }
 
 // One block: dL/dR and dL/dt from the finalize blocks' partials and
 // dL/d(fx, fy, cx, cy) from the backward tiles' partials, summed in a fixed
-// order (deterministic; Pulsar Sec. B.2's device-wide camera reduction).
+// order in float-pair arithmetic (deterministic, ~1e-14 relative; Pulsar
+// Sec. B.2's device-wide camera reduction).
 __global__ void __launch_bounds__(kCamThreads)
 k_camera_reduce(Frame f, Workspace w, int fin_blocks, float* __restrict__ grad_cam) {
-    __shared__ double s_part[kCamThreads / 32][16];
+    __shared__ float2 s_part[kCamThreads / 32][16];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    double v[16];
+    FPair v[16];
 #pragma unroll
-    for (int q = 0; q < 16; ++q) v[q] = 0.0;
+    for (int q = 0; q < 16; ++q) v[q] = {0.0f, 0.0f};
     for (int b = tid; b < fin_blocks; b += kCamThreads)
 #pragma unroll
-        for (int q = 0; q < 12; ++q) v[q] += w.rtpart[12 * b + q];
+        for (int q = 0; q < 12; ++q) {
+            const float2 t = w.rtpart[12 * b + q];
+            v[q] = pp_add(v[q], FPair{t.x, t.y});
+        }
     for (int b = tid; b < f.n_tiles; b += kCamThreads)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) v[12 + q] += w.kpart[4 * b + q];
+        for (int q = 0; q < 4; ++q) {
+            const float2 t = w.kpart[4 * b + q];
+            v[12 + q] = pp_add(v[12 + q], FPair{t.x, t.y});
+        }
 #pragma unroll
     for (int q = 0; q < 16; ++q) {
-        double s = v[q];
+        FPair s = v[q];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
-        if (lane == 0) s_part[warp][q] = s;
+        for (int o = 16; o > 0; o >>= 1) {
+            const FPair t = {__shfl_down_sync(0xffffffffu, s.hi, o),
+                             __shfl_down_sync(0xffffffffu, s.lo, o)};
+            s = pp_add(s, t);
+        }
+        if (lane == 0) s_part[warp][q] = make_float2(s.hi, s.lo);
     }
     __syncthreads();
     if (tid < 16) {
-        double s = 0.0;
-        for (int q = 0; q < kCamThreads / 32; ++q) s += s_part[q][tid];
-        if (grad_cam) grad_cam[tid] = (float)s;
+        FPair s = {0.0f, 0.0f};
+        for (int q = 0; q < kCamThreads / 32; ++q) {
+            const float2 t = s_part[q][tid];
+            s = pp_add(s, FPair{t.x, t.y});
+        }
+        if (grad_cam) grad_cam[tid] = __fadd_rn(s.hi, s.lo);
     }
 }
 

@@ -266,8 +266,8 @@ struct Workspace {
     int32_t* ids;           // [maxT][maxP] tracked sphere ids, -1 padded
     float* dtr;             // [maxT][maxP] distance factor d of each tracked hit
     int32_t* nhits;         // [maxP]
-    double* kpart;          // [maxB][4] per-tile partial dL/d(fx, fy, cx, cy)
-    double* rtpart;         // [ceil(maxN/256)][12] per-block partial dL/dR, dL/dt
+    float2* kpart;          // [maxB][4] per-tile partial dL/d(fx, fy, cx, cy), float pairs
+    float2* rtpart;         // [ceil(maxN/256)][12] per-block partial dL/dR, dL/dt, float pairs
     DevState* state;
 };
 
