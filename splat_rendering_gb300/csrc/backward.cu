@@ -188,30 +188,64 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
     }
 }
 
+// Finalize of one sphere; adds its share of dL/dR and dL/dt to acc.
+__device__ __forceinline__ void finalize_one(const Frame& f, float4 g, float px, float py, float pz,
+                                             float* gp, float* acc) {
+    gp[0] = f.R[0] * g.x + f.R[3] * g.y + f.R[6] * g.z;
+    gp[1] = f.R[1] * g.x + f.R[4] * g.y + f.R[7] * g.z;
+    gp[2] = f.R[2] * g.x + f.R[5] * g.y + f.R[8] * g.z;
+    acc[0] += g.x * px; acc[1] += g.x * py; acc[2] += g.x * pz;
+    acc[3] += g.y * px; acc[4] += g.y * py; acc[5] += g.y * pz;
+    acc[6] += g.z * px; acc[7] += g.z * py; acc[8] += g.z * pz;
+    acc[9] += g.x; acc[10] += g.y; acc[11] += g.z;
+}
+
+// Four consecutive spheres per thread with 16-byte loads and stores, so each
+// thread has seven independent loads in flight.
 __global__ void __launch_bounds__(kFinThreads)
 k_finalize(Frame f, Workspace w, const float* __restrict__ pos, float* __restrict__ grad_pos,
-           float* __restrict__ grad_radius) {
+           float* __restrict__ grad_radius, int vec_ok) {
     __shared__ float s_part[kFinThreads / 32][12];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int i = blockIdx.x * blockDim.x + tid;
+    const int i0 = 4 * (blockIdx.x * blockDim.x + tid);
     float acc[12];
 #pragma unroll
     for (int q = 0; q < 12; ++q) acc[q] = 0.0f;
-    if (i < f.n) {
-        // both loads issued together; the accumulator is cleared for the next frame
-        const float4 g = w.gacc[i];
-        const float px = pos[3 * i], py = pos[3 * i + 1], pz = pos[3 * i + 2];
-        w.gacc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (vec_ok && i0 + 3 < f.n) {
+        float4 g[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) g[k] = w.gacc[i0 + k];
+        const float4* p4 = reinterpret_cast<const float4*>(pos + 3 * i0);
+        const float4 pa = p4[0], pb = p4[1], pc = p4[2];
+        const float p[12] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w, pc.x, pc.y, pc.z, pc.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) w.gacc[i0 + k] = z4;
+        float gp[12];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            finalize_one(f, g[k], p[3 * k], p[3 * k + 1], p[3 * k + 2], gp + 3 * k, acc);
         if (grad_pos) {
-            grad_pos[3 * i + 0] = f.R[0] * g.x + f.R[3] * g.y + f.R[6] * g.z;
-            grad_pos[3 * i + 1] = f.R[1] * g.x + f.R[4] * g.y + f.R[7] * g.z;
-            grad_pos[3 * i + 2] = f.R[2] * g.x + f.R[5] * g.y + f.R[8] * g.z;
+            float4* o4 = reinterpret_cast<float4*>(grad_pos + 3 * i0);
+            o4[0] = make_float4(gp[0], gp[1], gp[2], gp[3]);
+            o4[1] = make_float4(gp[4], gp[5], gp[6], gp[7]);
+            o4[2] = make_float4(gp[8], gp[9], gp[10], gp[11]);
         }
-        if (grad_radius) grad_radius[i] = g.w;
-        acc[0] = g.x * px; acc[1] = g.x * py; acc[2] = g.x * pz;
-        acc[3] = g.y * px; acc[4] = g.y * py; acc[5] = g.y * pz;
-        acc[6] = g.z * px; acc[7] = g.z * py; acc[8] = g.z * pz;
-        acc[9] = g.x; acc[10] = g.y; acc[11] = g.z;
+        if (grad_radius)
+            *reinterpret_cast<float4*>(grad_radius + i0) = make_float4(g[0].w, g[1].w, g[2].w, g[3].w);
+    } else {
+        for (int i = i0; i < min(i0 + 4, f.n); ++i) {   // ragged tail or unaligned arrays
+            const float4 g = w.gacc[i];
+            w.gacc[i] = z4;
+            float gp[3];
+            finalize_one(f, g, pos[3 * i], pos[3 * i + 1], pos[3 * i + 2], gp, acc);
+            if (grad_pos) {
+                grad_pos[3 * i] = gp[0];
+                grad_pos[3 * i + 1] = gp[1];
+                grad_pos[3 * i + 2] = gp[2];
+            }
+            if (grad_radius) grad_radius[i] = g.w;
+        }
     }
 #pragma unroll
     for (int q = 0; q < 12; ++q) {
@@ -316,9 +350,12 @@ cudaError_t launch_backward(const Frame& f, const Workspace& w, const float* pos
         launch_bwd_c<kMaxChannels>(f, w, features, image, grad_image, grad_opacity,
                                    grad_features, want_geom, stream);
     if (want_geom) {
-        const int blocks = (f.n + kFinThreads - 1) / kFinThreads;
+        const int blocks = (f.n + 4 * kFinThreads - 1) / (4 * kFinThreads);
+        // 16-byte accesses need 16-byte aligned arrays (true for torch allocations)
+        const int vec_ok = ((reinterpret_cast<uintptr_t>(pos) | reinterpret_cast<uintptr_t>(grad_pos) |
+                             reinterpret_cast<uintptr_t>(grad_radius)) & 15u) == 0;
         if (blocks > 0)
-            k_finalize<<<blocks, kFinThreads, 0, stream>>>(f, w, pos, grad_pos, grad_radius);
+            k_finalize<<<blocks, kFinThreads, 0, stream>>>(f, w, pos, grad_pos, grad_radius, vec_ok);
         k_camera_reduce<<<1, kCamThreads, 0, stream>>>(f, w, blocks, grad_cam);
     }
     return cudaGetLastError();

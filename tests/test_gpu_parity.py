@@ -231,3 +231,27 @@ def test_repeat_frames_and_determinism(oracle_lib):
     gh.compare_frame(ga2, oa, "repeated run")
     o, _, _, _ = _oracle_all(oracle_lib, b)
     gh.compare_frame(gb, o, "second scene")
+
+
+def test_unaligned_gradient_arrays(oracle_lib):
+    """Gradient outputs that are not 16-byte aligned take the scalar path of the
+    finalize kernel and give the same result."""
+    import torch
+    from splat_rendering_gb300 import pulsar as pl
+    sc = scenes.random_scene(66, 777, 48, 40, rrange=(0.02, 0.3), rot_deg=8)
+    o, _, _, _ = _oracle_all(oracle_lib, sc)
+    r = pl.Renderer(max_spheres=sc.n, max_pairs=1 << 16, max_width=48, max_height=40)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    pos, feat, bg = t(sc.pos), t(sc.features), t(sc.bg)
+    img = r.render(pos, t(sc.radius), t(sc.opacity), feat, pl.camera(sc.cameras[0]),
+                   pl.params(sc.params), bg)
+    buf = torch.zeros(3 * sc.n + 1, device="cuda")
+    gpos = buf[1:].view(sc.n, 3)                      # 4-byte offset
+    rbuf = torch.zeros(sc.n + 1, device="cuda")
+    grad = rbuf[1:]
+    pl.backward(r.ctx, feat, bg, img, t(sc.grad_images[0]), grad_pos=gpos, grad_radius=grad)
+    assert r.status()[0] == 0
+    gh.assert_close(gpos.cpu().numpy(), o["grad_pos"], gh.GRAD_RTOL, gh.GRAD_ATOL, "pos",
+                    o["abs_grad_pos"], o["sens_grad_pos"])
+    gh.assert_close(grad.cpu().numpy(), o["grad_radius"], gh.GRAD_RTOL, gh.GRAD_ATOL, "radius",
+                    o["abs_grad_radius"], o["sens_grad_radius"])
