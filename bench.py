@@ -113,31 +113,55 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "sm_max_mhz": 2070.0}, "fallback"
 
 
-def algorithmic_bytes(stage, N, M, P, C, T, Ht):
-    """Compulsory bytes of one launch of each stage (each array moved once).
-    N spheres, M sphere-tile pairs, P pixels, C channels, T tracked hits per
-    pixel, Ht tracked hit pairs."""
+# FP32 peak of the ALU-bound kernels: 152 SMs x 128 FP32 lanes x 2 flops (FMA) at
+# the maximum SM clock of MEASURED_PEAKS (2070 MHz) = 80.5 TFLOP/s.
+SMS, FP32_LANES = 152, 128
+
+
+def fp32_peak_tflops(peaks) -> float:
+    return SMS * FP32_LANES * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
+
+
+def algorithmic_bytes(stage, N, M, P, C, T):
+    """Compulsory bytes of one launch of each stage: every array moved once,
+    sphere records gathered once per sphere-tile pair in the forward and once
+    per sphere in the backward (the per-unit figures of the hot-path table)."""
     if stage == "project":
-        return 20 * N + 60 * N
+        return 20 * N + 44 * N
     if stage == "bin":
-        return 8 * N + 12 * M + 8 * M + 4 * M
+        return 8 * N + 12 * N + 12 * M + 24 * M + 8 * M
     if stage == "forward":
-        return (4 + 44 + 4 * C) * M + (4 * C + 8 + 4 * T) * P
+        return 4 * M + (32 + 4 * C) * M + 4 * C * P + (8 + 4 * T) * P
     if stage == "backward":
-        return 8 * C * P + (8 + 4 * T) * P + (52 + 4 * C) * Ht + (16 + 16 + 4 + 4 * C) * N + 12 * N
+        return (8 * C * P + (8 + 4 * T) * P + (32 + 4 * C) * N + (20 + 4 * C) * N + 12 * N
+                + 24 * N + 12 * N)
     raise KeyError(stage)
 
 
-def traffic_from_profile(kernel_file: str, workload: str):
-    """DRAM bytes per launch recorded by the committed ncu summary, if it was
-    taken on the current source of the kernel; else None."""
-    path = os.path.join(ROOT, "profiles", f"{kernel_file}_{workload}.txt")
+def algorithmic_flops(stage, N, M, P, C, T, H, Ht):
+    """FP32 work of the method (FMA = 2): the cooperative candidate test of
+    every tile pair at every pixel of its 16x16 tile (~14 flops), the blend of
+    every hit (12 + 2C), the tracked-hit gradient (70 + 6C), the projection
+    (~100 per sphere)."""
+    if stage == "project":
+        return 100 * N
+    if stage == "forward":
+        return 14 * M * 256 + (12 + 2 * C) * H
+    if stage == "backward":
+        return (70 + 6 * C) * Ht
+    return 0
+
+
+def traffic_from_profile(kernel: str, source: str, workload: str):
+    """DRAM bytes per launch recorded by the committed ncu summary of `kernel`,
+    if it was taken on the current source; else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
     src = os.path.join(ROOT, "splat_rendering_gb300", "csrc")
     try:
         with open(path) as f:
             kv = dict(l.split(":", 1) for l in f.read().splitlines() if ":" in l)
         h = hashlib.sha256()
-        for name in ("pulsar_internal.cuh", f"{kernel_file}.cu"):
+        for name in ("pulsar_internal.cuh", source):
             with open(os.path.join(src, name), "rb") as g:
                 h.update(g.read())
         if kv.get("source_sha256", "").strip() != h.hexdigest():
@@ -366,17 +390,29 @@ def run_gb300(a):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_total = float(tt.item())
 
-    # ---- roofline of the dominant single-kernel stage
+    # ---- roofline of the dominant kernel (the forward) and of the whole path
     peaks, peak_src = measured_peaks()
-    dom = max(("project", "forward"), key=lambda k: breakdown[k])
-    dom_bytes = algorithmic_bytes(dom, N, M, P, C, T, Ht)
-    achieved = dom_bytes / (breakdown[dom] * 1e-3) / 1e9
-    peak = float(peaks["hbm_gbs"])
-    traffic = traffic_from_profile(dom, "headline")
-    roofline = {"bound": "hbm", "kernel": f"k_{dom}", "achieved": achieved, "peak": peak,
-                "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
-                "algorithmic_bytes": dom_bytes, "peak_source": f"{peak_src} hbm_gbs"}
-    path_bytes = sum(algorithmic_bytes(k, N, M, P, C, T, Ht) for k in stages)
+    hbm = float(peaks["hbm_gbs"])
+    fp32 = fp32_peak_tflops(peaks)
+    fwd_flops = algorithmic_flops("forward", N, M, P, C, T, H, Ht)
+    fwd_bytes = algorithmic_bytes("forward", N, M, P, C, T)
+    fwd_s = breakdown["forward"] * 1e-3
+    achieved = fwd_flops / fwd_s / 1e12
+    roofline = {"bound": "alu", "kernel": "k_forward", "achieved": achieved, "peak": fp32,
+                "unit": "TFLOP/s", "frac": achieved / fp32,
+                "traffic": traffic_from_profile("k_forward", "forward.cu", "headline"),
+                "algorithmic_flops": fwd_flops, "algorithmic_bytes": fwd_bytes,
+                "hbm_frac": fwd_bytes / fwd_s / 1e9 / hbm,
+                "peak_source": f"FP32: {SMS} SMs x {FP32_LANES} lanes x 2 x "
+                               f"{peaks.get('sm_max_mhz', 2070.0)} MHz ({peak_src} clock); "
+                               f"HBM: {peak_src} hbm_gbs {hbm}"}
+    path_bytes = sum(algorithmic_bytes(k, N, M, P, C, T) for k in stages)
+    path_flops = sum(algorithmic_flops(k, N, M, P, C, T, H, Ht) for k in stages)
+    path_time = max(path_bytes / (hbm * 1e9), path_flops / (fp32 * 1e12))
+    path = {"algorithmic_bytes": path_bytes, "algorithmic_flops": path_flops,
+            "hbm_time_ms": path_bytes / (hbm * 1e9) * 1e3,
+            "fp32_time_ms": path_flops / (fp32 * 1e12) * 1e3,
+            "frac": path_time * 1e3 / (total_ms / a.steps)}
 
     value = world * a.steps / (total_ms * 1e-3)
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
@@ -388,10 +424,7 @@ def run_gb300(a):
             "msphere_pixel_per_s": world * H / (total_ms / a.steps * 1e-3) / 1e6,
             "hits_per_frame": H, "pairs_per_frame": M, "tracked_hits_per_frame": Ht,
             "breakdown_ms": breakdown,
-            "path_roofline": {"algorithmic_bytes": path_bytes,
-                              "hbm_time_ms": path_bytes / (peak * 1e9) * 1e3,
-                              "frac_of_step": path_bytes / (peak * 1e9) * 1e3 /
-                              (total_ms / a.steps)},
+            "path_roofline": path,
             "roofline": roofline,
             "e2e": {"value": world * a.steps / (e2e_total * 1e-3), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
