@@ -178,6 +178,30 @@ const char* pulsar_strerror(int code);
 #define PULSAR_DBG_NHITS        10
 int64_t pulsar_debug_copy(pulsar_ctx_t ctx, int what, void* dst, int64_t bytes, void* stream);
 
+/* Forward render of one small frame that allocates no memory (the pages have
+ * no counterpart: this entry point exists for callers that cannot call
+ * cudaMalloc -- code running while a stream is captured into a graph,
+ * plugins whose host framework owns the device memory budget, fixed-footprint
+ * real-time renderers).  It runs the kernels of pulsar_project, pulsar_bin and
+ * pulsar_forward with all intermediate arrays in one static device arena of
+ * about 8 MB that the library reserves on every GPU that loads it, until the
+ * process exits.  No context is needed; inputs and outputs are as for
+ * pulsar_project and pulsar_forward.
+ *   Limits: n <= 16384 spheres, at most 65536 sphere-tile pairs, width and
+ *   height <= 256, n_track <= 8, channels <= 64.  Larger sizes return
+ *   PULSAR_ERR_ARG without enqueueing anything; a frame with more pairs returns
+ *   PULSAR_ERR_CAPACITY (the image is then not written).
+ *   All calls share the arena, which keeps the last call's contents; each call
+ *   clears what must start at zero.  Calls that overlap on the GPU race: the
+ *   caller must serialise them.
+ *   The first call on a device looks up the arena's device address and
+ *   prepares the kernels; make it before capturing any stream.  The call
+ *   synchronises `stream` at its end to read the frame's status. */
+int pulsar_render_noalloc(const float* pos, const float* radius, const float* opacity,
+                          const float* features, int64_t n, const pulsar_camera_t* cam,
+                          const pulsar_params_t* params, const float* bg, float* image,
+                          void* stream);
+
 #ifdef __cplusplus
 }
 #endif

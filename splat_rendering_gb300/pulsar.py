@@ -51,7 +51,7 @@ class Params(ctypes.Structure):
 
 EXPORTS = ("pulsar_create", "pulsar_destroy", "pulsar_project", "pulsar_bin",
            "pulsar_forward", "pulsar_backward", "pulsar_status", "pulsar_strerror",
-           "pulsar_debug_copy")
+           "pulsar_debug_copy", "pulsar_render_noalloc")
 
 
 def load(path: str = LIB_PATH):
@@ -76,6 +76,8 @@ def load(path: str = LIB_PATH):
     lib.pulsar_strerror.restype = ctypes.c_char_p
     lib.pulsar_debug_copy.argtypes = [P, ctypes.c_int, P, I64, P]
     lib.pulsar_debug_copy.restype = I64
+    lib.pulsar_render_noalloc.argtypes = [P, P, P, P, I64, ctypes.POINTER(Camera),
+                                          ctypes.POINTER(Params), P, P, P]
     for name in EXPORTS:
         if name not in ("pulsar_strerror", "pulsar_debug_copy"):
             getattr(lib, name).restype = ctypes.c_int
@@ -180,6 +182,16 @@ def status(ctx, stream=None, raise_on_error: bool = True):
     if raise_on_error:
         _check(code, "pulsar_status")
     return code, m.value, h.value
+
+
+def render_noalloc(pos, radius, opacity, features, n: int, cam: Camera, prm: Params, bg, image,
+                   stream=None):
+    """Forward render of a small frame without any memory allocation (see
+    pulsar_render_noalloc in include/pulsar.h for its limits).  For callers
+    that cannot allocate device memory at render time; synchronises the stream."""
+    _check(load().pulsar_render_noalloc(_ptr(pos), _ptr(radius), _ptr(opacity), _ptr(features),
+                                        int(n), ctypes.byref(cam), ctypes.byref(prm), _ptr(bg),
+                                        _ptr(image), _stream(stream)), "pulsar_render_noalloc")
 
 
 def debug_copy(ctx, what: str, stream=None) -> np.ndarray:
