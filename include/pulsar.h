@@ -167,7 +167,8 @@ const char* pulsar_strerror(int code);
  *   PULSAR_DBG_TILE_IDS  [M] uint32 sorted tile lists
  *   PULSAR_DBG_MG        [H*W] float  stabiliser log2(e) m / gamma
  *   PULSAR_DBG_WSUM      [H*W] float  normaliser in the exp(-m/gamma) frame
- *   PULSAR_DBG_IDS       [n_track][H*W] int32 tracked ids, -1 padded
+ *   PULSAR_DBG_IDS       [n_track][H*W] int32 tracked sphere ids, -1 padded (the buffer
+ *                        itself holds list positions; they are translated here)
  *   PULSAR_DBG_NHITS     [H*W] int32 hits per pixel (PULSAR_FLAG_COUNT_HITS) */
 #define PULSAR_DBG_RECORDS       1
 #define PULSAR_DBG_TILE_OFFSETS  5

@@ -3,15 +3,19 @@
 // repeated.  Gradients of L = sum_pixels <G, F> flow through the first
 // n_track hits of every pixel only (Sec. 2, B.1.3).
 //
-// k_backward  one block per 16x16 tile, one thread per pixel.  For tracked
-//             hit k the lanes of a warp that hold the same sphere are grouped
-//             (__match_any_sync) and their contributions tree-reduced, so one
-//             lane per distinct sphere issues the global atomics -- the
-//             warp-level aggregation of DISTWAR (arxiver abstract).  dL/dc and
-//             dL/dr go to a float4 accumulator with one vector reduction;
-//             opacity and feature gradients go straight to the caller's
-//             (zeroed) arrays.  The intrinsics' gradient is summed per thread,
-//             reduced per block and added to fp64 accumulators.
+// k_backward  one block per 16x16 tile, one thread per pixel.  The tile's
+//             candidates are staged through shared memory in batches (as in
+//             the forward), each pixel finds its tracked hits among them by
+//             their list positions (stored by the forward), and every
+//             contribution is added to the candidate's shared-memory
+//             accumulator; after the batch one thread per touched candidate
+//             flushes the tile's sums with global reductions -- aggregation
+//             before the global atomics, as DISTWAR (arxiver abstract) argues,
+//             here at tile rather than warp level.  dL/dc and dL/dr go to a
+//             float4 accumulator with one vector reduction; opacity and
+//             feature gradients go straight to the caller's (zeroed) arrays.
+//             The intrinsics' gradient is summed per thread and reduced per
+//             block.
 // k_finalize  one thread per sphere: dL/dp = R^T dL/dc and dL/dr out of the
 //             accumulator (which it zeroes for the next frame);
 //             dL/dR = sum dL/dc p^T and dL/dt = sum dL/dc reduced per block
@@ -38,13 +42,29 @@ __device__ __forceinline__ int nth_lane(uint32_t m, int n) {
     return __ffs(m) - 1;
 }
 
+// Shared-memory batch of the backward: candidates staged per batch and their
+// per-sphere gradient accumulators (static smem < 48 KB).
+template <int CMAX>
+struct BwdBatch {
+    static constexpr int NV = 5 + CMAX;   // dL/dc.xyz, dL/dr, dL/do, dL/df[CMAX]
+    static constexpr int n = CMAX <= 4 ? 384 : (CMAX <= 16 ? 192 : (CMAX <= 32 ? 128 : 64));
+};
+
 template <int CMAX, int TMAX>
 __global__ void __launch_bounds__(kBwdThreads, CMAX <= 4 ? 4 : (CMAX <= 16 ? 2 : 1))
 k_backward(Frame f, Workspace w, const float* __restrict__ features,
            const float* __restrict__ image, const float* __restrict__ grad_image,
            float* __restrict__ grad_opacity, float* __restrict__ grad_features, int want_geom) {
+    constexpr int NB = BwdBatch<CMAX>::n;
+    constexpr int NV = BwdBatch<CMAX>::NV;
+    __shared__ float4 s_uv[NB];
+    __shared__ float4 s_ex[NB];          // exponent hi, lo, o, flags
+    __shared__ float4 s_geo[NB];         // (c.z/r_eff)^2 hi, lo, c.z, r_eff
+    __shared__ int s_id[NB];
+    __shared__ int s_touched[NB];
+    __shared__ float s_feat[NB * CMAX];
+    __shared__ float s_acc[NB * NV];
     __shared__ float s_k[kBwdThreads / 32][4];
-    constexpr int NV = 5 + CMAX;   // gc.xyz, gr, go, gf[CMAX]
     if (w.state->n_pairs > f.max_pairs) return;   // overflowed frame: no valid buffer
     const int C = f.channels;
     const int tile = blockIdx.x;
@@ -56,7 +76,6 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
     const int p = inside ? y * f.width + x : 0;
     const PixelRay ray = pixel_ray(x, y, f);
     const float iqq = __frcp_rn(ray.qq);
-    const uint32_t lt_mask = (1u << lane) - 1u;
 
     float G[CMAX], F[CMAX];
 #pragma unroll
@@ -68,46 +87,67 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
     const float iw = inside ? 1.0f / w.wsum[p] : 0.0f;
     float gk[4] = {0.f, 0.f, 0.f, 0.f};   // d/d(fx, fy, cx, cy)
 
-    for (int k = 0; k < f.n_track; ++k) {
-        const int id = inside ? w.ids[(size_t)k * P + p] : -1;
-        if (__ballot_sync(0xffffffffu, id >= 0) == 0u) break;
-        float v[NV];
-#pragma unroll
-        for (int q = 0; q < NV; ++q) v[q] = 0.0f;
-        bool cut = true;
-        if (id >= 0) {
+    uint32_t start = w.tile_start[tile], end = w.tile_start[tile + 1];
+    end = min(end, f.max_pairs);
+    start = min(start, end);
+    for (uint32_t b0 = start; b0 < end; b0 += NB) {
+        __syncthreads();   // previous batch flushed
+        const int nb = (int)min((uint32_t)NB, end - b0);
+        for (int t = tid; t < nb; t += kBwdThreads) {
+            const int id = (int)w.tile_ids[b0 + t];
             const SphereRec* rp = w.rec + id;
-            const float4 uv = rp->uv;
-            const float4 ex = rp->ex;
-            const float4 geo = rp->geo;
+            s_id[t] = id;
+            s_uv[t] = rp->uv;
+            s_ex[t] = rp->ex;
+            s_geo[t] = rp->geo;
+            s_touched[t] = 0;
+#pragma unroll
+            for (int c = 0; c < CMAX; ++c)
+                if (c < C) s_feat[t * CMAX + c] = features[(size_t)id * C + c];
+#pragma unroll
+            for (int q = 0; q < NV; ++q) s_acc[t * NV + q] = 0.0f;
+        }
+        __syncthreads();
+        // this pixel's tracked hits whose list position falls in the batch
+        const int base = (int)(b0 - start);
+        for (int k = 0; k < f.n_track; ++k) {
+            const int pos = inside ? w.ids[(size_t)k * P + p] : -1;
+            if (pos < 0) break;   // positions are -1 padded at the end
+            const int j = pos - base;
+            if (j < 0 || j >= nb) continue;
+            const float4 uv = s_uv[j];
+            const float4 ex = s_ex[j];
+            const float4 geo = s_geo[j];
             const uint32_t fl = __float_as_uint(ex.w);
-            cut = (fl & kFlagCut) != 0u;
+            const bool cut = (fl & kFlagCut) != 0u;
             float U, V;
             const float Q = ray_offset_q(uv, ray, f.ifx, f.ify, &U, &V);
-            const float rq = sqrtf(Q * iqq);            // rho / c.z
-            const float d = w.dtr[(size_t)k * P + p];     // stored by the forward pass
+            const float rq = sqrtf(Q * iqq);                 // rho / c.z
+            const float d = w.dtr[(size_t)k * P + p];        // stored by the forward pass
             const float o = ex.z;
             const float E = exp2f(__fsub_rn(ex.x, mg) + ex.y);   // exponents in log2 units
             const float wt = o * d * E;
             float sdot = 0.0f;
+            float* acc = s_acc + j * NV;
 #pragma unroll
             for (int c = 0; c < CMAX; ++c) {
                 if (c < C) {
-                    const float fc = features[(size_t)id * C + c];
+                    const float fc = s_feat[j * CMAX + c];
                     sdot += G[c] * (fc - F[c]);
-                    v[5 + c] = wt * iw * G[c];          // dL/df = (w / W) G
+                    atomicAdd(&acc[5 + c], wt * iw * G[c]);   // dL/df = (w / W) G
                 }
             }
-            const float sj = sdot * iw;                 // dL/dw = <G, f - F> / W
-            v[4] = sj * d * E * (1.0f + ex.x * 0.693147181f);   // dw/do = d E (1 + o z~/gamma)
+            const float sj = sdot * iw;                      // dL/dw = <G, f - F> / W
+            atomicAdd(&acc[4], sj * d * E * (1.0f + ex.x * 0.693147181f));   // dw/do
+            s_touched[j] = 1;
             if (want_geom && !cut) {
                 const float Z = geo.z, reff = geo.w;
                 const float ireff = 1.0f / reff;
-                const float sE = sj * o * E;            // dL/dd
+                const float sE = sj * o * E;                 // dL/dd
                 // depth factor: dw/dz~ = w o / gamma, dz~/dc.z = -1/(zfar - znear)
                 float gcz = -sj * wt * o * f.inv_gamma * f.inv_zrange;
                 const float rho = rq * Z;
-                const float g_rho = -sE * ireff;        // dd/drho = -1/r_eff
+                const float g_rho = -sE * ireff;             // dd/drho = -1/r_eff
                 const float g_reff = sE * rho * ireff * ireff;
                 float gr = 0.0f;
                 if (fl & kFlagFloor) {
@@ -138,34 +178,25 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
                     gk[2] -= ga * f.ifx;
                     gk[3] -= gb * f.ify;
                 }
-                v[0] = gcx;
-                v[1] = gcy;
-                v[2] = gcz;
-                v[3] = gr;
+                atomicAdd(&acc[0], gcx);
+                atomicAdd(&acc[1], gcy);
+                atomicAdd(&acc[2], gcz);
+                if (gr != 0.0f) atomicAdd(&acc[3], gr);
             }
         }
-        // group the lanes that hold the same sphere and tree-reduce within groups;
-        // lanes without a k-th hit get distinct keys, so they form no group
-        const uint32_t peers = __match_any_sync(0xffffffffu, id >= 0 ? id : -1 - lane);
-        const int rank = __popc(peers & lt_mask);
-        const int gsz = __popc(peers);
-        const int gmax = __reduce_max_sync(0xffffffffu, gsz);
-        for (int off = 1; off < gmax; off <<= 1) {
-            const bool take = (rank & (2 * off - 1)) == 0 && rank + off < gsz;
-            const int src = take ? nth_lane(peers, rank + off) : lane;
-#pragma unroll
-            for (int q = 0; q < NV; ++q) {
-                const float o2 = __shfl_sync(0xffffffffu, v[q], src);
-                if (take) v[q] += o2;
-            }
-        }
-        if (rank == 0 && id >= 0) {
-            if (want_geom && !cut) red_add_v4(&w.gacc[id], v[0], v[1], v[2], v[3]);
-            if (grad_opacity) atomicAdd(&grad_opacity[id], v[4]);
+        __syncthreads();
+        // one flush per (sphere, tile): the sums of all this tile's pixels
+        for (int t = tid; t < nb; t += kBwdThreads) {
+            if (!s_touched[t]) continue;
+            const int id = s_id[t];
+            const float* acc = s_acc + t * NV;
+            const bool cut = (__float_as_uint(s_ex[t].w) & kFlagCut) != 0u;
+            if (want_geom && !cut) red_add_v4(&w.gacc[id], acc[0], acc[1], acc[2], acc[3]);
+            if (grad_opacity) atomicAdd(&grad_opacity[id], acc[4]);
             if (grad_features) {
 #pragma unroll
                 for (int c = 0; c < CMAX; ++c)
-                    if (c < C) atomicAdd(&grad_features[(size_t)id * C + c], v[5 + c]);
+                    if (c < C) atomicAdd(&grad_features[(size_t)id * C + c], acc[5 + c]);
             }
         }
     }

@@ -267,8 +267,9 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
                     for (int c = 0; c < CMAX; ++c)
                         if (c < C) acc[c] += wt * s_feat[j * CMAX + c];
                     if (nh < f.n_track) {
-                        // backward-information buffer: id and distance factor of the hit
-                        w.ids[(size_t)nh * P + p] = s_id[j];
+                        // backward-information buffer: the hit's position in the tile
+                        // list and its distance factor
+                        w.ids[(size_t)nh * P + p] = (int)(b0 - start) + j;
                         w.dtr[(size_t)nh * P + p] = d;
                     }
                     ++nh;

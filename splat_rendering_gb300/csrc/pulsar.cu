@@ -7,6 +7,7 @@
 
 #include <cstring>
 #include <new>
+#include <vector>
 
 #include "../../include/pulsar.h"
 #include "pulsar_internal.cuh"
@@ -306,7 +307,40 @@ int64_t pulsar_debug_copy(pulsar_ctx_t c, int what, void* dst, int64_t bytes, vo
         }
         case PULSAR_DBG_MG: src = c->ws.mg; size = P * 4; break;
         case PULSAR_DBG_WSUM: src = c->ws.wsum; size = P * 4; break;
-        case PULSAR_DBG_IDS: src = c->ws.ids; size = P * f.n_track * 4; break;
+        case PULSAR_DBG_IDS: {
+            // the buffer holds each tracked hit's position in its tile list;
+            // report sphere ids
+            size = P * f.n_track * 4;
+            if (!dst) return size;
+            if (bytes > size) return PULSAR_ERR_ARG;
+            std::vector<int32_t> pos((size_t)P * f.n_track);
+            std::vector<uint32_t> starts((size_t)f.n_tiles + 1);
+            uint32_t m = 0;
+            if (cudaMemcpyAsync(pos.data(), c->ws.ids, (size_t)size, cudaMemcpyDeviceToHost, s) !=
+                    cudaSuccess ||
+                cudaMemcpyAsync(starts.data(), c->ws.tile_start, starts.size() * 4,
+                                cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+                cudaMemcpyAsync(&m, &c->ws.state->n_pairs, 4, cudaMemcpyDeviceToHost, s) !=
+                    cudaSuccess ||
+                cudaStreamSynchronize(s) != cudaSuccess)
+                return PULSAR_ERR_CUDA;
+            m = m < c->max_pairs ? m : (uint32_t)c->max_pairs;
+            std::vector<uint32_t> list(m > 0 ? m : 1);
+            if (m > 0 && (cudaMemcpy(list.data(), c->ws.tile_ids, (size_t)m * 4,
+                                     cudaMemcpyDeviceToHost) != cudaSuccess))
+                return PULSAR_ERR_CUDA;
+            for (int64_t q = 0; q < (int64_t)pos.size(); ++q) {
+                if (pos[q] < 0) continue;
+                const int64_t px = q % P;
+                const int tile = (int)((px / f.width) / kTile) * f.tiles_x + (int)((px % f.width) / kTile);
+                const uint64_t at = (uint64_t)starts[tile] + (uint64_t)pos[q];
+                pos[q] = at < m ? (int32_t)list[at] : -1;
+            }
+            if (bytes > 0 &&
+                cudaMemcpy(dst, pos.data(), (size_t)bytes, cudaMemcpyDefault) != cudaSuccess)
+                return PULSAR_ERR_CUDA;
+            return PULSAR_OK;
+        }
         case PULSAR_DBG_NHITS: src = c->ws.nhits; size = P * 4; break;
         default: return PULSAR_ERR_ARG;
     }

@@ -263,7 +263,7 @@ struct Workspace {
     uint32_t* tile_ids;     // [max_pairs] sorted tile lists
     float* mg;              // [maxP]
     float* wsum;            // [maxP]
-    int32_t* ids;           // [maxT][maxP] tracked sphere ids, -1 padded
+    int32_t* ids;           // [maxT][maxP] tracked hits' positions in their tile list, -1 padded
     float* dtr;             // [maxT][maxP] distance factor d of each tracked hit
     int32_t* nhits;         // [maxP]
     float2* kpart;          // [maxB][4] per-tile partial dL/d(fx, fy, cx, cy), float pairs
