@@ -5,17 +5,16 @@
 //
 // k_backward  one block per 16x16 tile, one thread per pixel.  The tile's
 //             candidates are staged through shared memory in batches (as in
-//             the forward), each pixel finds its tracked hits among them by
-//             their list positions (stored by the forward), and every
-//             contribution is added to the candidate's shared-memory
-//             accumulator; after the batch one thread per touched candidate
-//             flushes the tile's sums with global reductions -- aggregation
-//             before the global atomics, as DISTWAR (arxiver abstract) argues,
-//             here at tile rather than warp level.  dL/dc and dL/dr go to a
-//             float4 accumulator with one vector reduction; opacity and
-//             feature gradients go straight to the caller's (zeroed) arrays.
-//             The intrinsics' gradient is summed per thread and reduced per
-//             block.
+//             the forward) and each pixel finds its tracked hits among them by
+//             their list positions (stored by the forward).  For tracked hit
+//             k the lanes of a warp that hold the same candidate are grouped
+//             (__match_any_sync) and their contributions tree-reduced, so one
+//             lane per distinct sphere issues the global atomics -- the
+//             warp-level aggregation of DISTWAR (arxiver abstract).  dL/dc and
+//             dL/dr go to a float4 accumulator with one vector reduction;
+//             opacity and feature gradients go straight to the caller's
+//             (zeroed) arrays.  The intrinsics' gradient is summed per thread
+//             and reduced per block.
 // k_finalize  one thread per sphere: dL/dp = R^T dL/dc and dL/dr out of the
 //             accumulator (which it zeroes for the next frame);
 //             dL/dR = sum dL/dc p^T and dL/dt = sum dL/dc reduced per block
@@ -42,12 +41,11 @@ __device__ __forceinline__ int nth_lane(uint32_t m, int n) {
     return __ffs(m) - 1;
 }
 
-// Shared-memory batch of the backward: candidates staged per batch and their
-// per-sphere gradient accumulators (static smem < 48 KB).
+// Shared-memory batch of the backward: candidates staged per batch (static
+// smem < 48 KB).
 template <int CMAX>
 struct BwdBatch {
-    static constexpr int NV = 5 + CMAX;   // dL/dc.xyz, dL/dr, dL/do, dL/df[CMAX]
-    static constexpr int n = CMAX <= 4 ? 384 : (CMAX <= 16 ? 192 : (CMAX <= 32 ? 128 : 64));
+    static constexpr int n = CMAX <= 4 ? 512 : (CMAX <= 16 ? 256 : (CMAX <= 32 ? 192 : 128));
 };
 
 template <int CMAX, int TMAX>
@@ -56,14 +54,12 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
            const float* __restrict__ image, const float* __restrict__ grad_image,
            float* __restrict__ grad_opacity, float* __restrict__ grad_features, int want_geom) {
     constexpr int NB = BwdBatch<CMAX>::n;
-    constexpr int NV = BwdBatch<CMAX>::NV;
+    constexpr int NV = 5 + CMAX;   // dL/dc.xyz, dL/dr, dL/do, dL/df[CMAX]
     __shared__ float4 s_uv[NB];
     __shared__ float4 s_ex[NB];          // exponent hi, lo, o, flags
     __shared__ float4 s_geo[NB];         // (c.z/r_eff)^2 hi, lo, c.z, r_eff
     __shared__ int s_id[NB];
-    __shared__ int s_touched[NB];
     __shared__ float s_feat[NB * CMAX];
-    __shared__ float s_acc[NB * NV];
     __shared__ float s_k[kBwdThreads / 32][4];
     if (w.state->n_pairs > f.max_pairs) return;   // overflowed frame: no valid buffer
     const int C = f.channels;
@@ -76,6 +72,7 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
     const int p = inside ? y * f.width + x : 0;
     const PixelRay ray = pixel_ray(x, y, f);
     const float iqq = __frcp_rn(ray.qq);
+    const uint32_t lt_mask = (1u << lane) - 1u;
 
     float G[CMAX], F[CMAX];
 #pragma unroll
@@ -91,7 +88,7 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
     end = min(end, f.max_pairs);
     start = min(start, end);
     for (uint32_t b0 = start; b0 < end; b0 += NB) {
-        __syncthreads();   // previous batch flushed
+        __syncthreads();   // previous batch done
         const int nb = (int)min((uint32_t)NB, end - b0);
         for (int t = tid; t < nb; t += kBwdThreads) {
             const int id = (int)w.tile_ids[b0 + t];
@@ -100,103 +97,114 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
             s_uv[t] = rp->uv;
             s_ex[t] = rp->ex;
             s_geo[t] = rp->geo;
-            s_touched[t] = 0;
 #pragma unroll
             for (int c = 0; c < CMAX; ++c)
                 if (c < C) s_feat[t * CMAX + c] = features[(size_t)id * C + c];
-#pragma unroll
-            for (int q = 0; q < NV; ++q) s_acc[t * NV + q] = 0.0f;
         }
         __syncthreads();
-        // this pixel's tracked hits whose list position falls in the batch
         const int base = (int)(b0 - start);
         for (int k = 0; k < f.n_track; ++k) {
+            // this pixel's k-th tracked hit, if its list position is in the batch
             const int pos = inside ? w.ids[(size_t)k * P + p] : -1;
-            if (pos < 0) break;   // positions are -1 padded at the end
+            if (__ballot_sync(0xffffffffu, pos >= 0) == 0u) break;   // -1 padded at the end
             const int j = pos - base;
-            if (j < 0 || j >= nb) continue;
-            const float4 uv = s_uv[j];
-            const float4 ex = s_ex[j];
-            const float4 geo = s_geo[j];
-            const uint32_t fl = __float_as_uint(ex.w);
-            const bool cut = (fl & kFlagCut) != 0u;
-            float U, V;
-            const float Q = ray_offset_q(uv, ray, f.ifx, f.ify, &U, &V);
-            const float rq = sqrtf(Q * iqq);                 // rho / c.z
-            const float d = w.dtr[(size_t)k * P + p];        // stored by the forward pass
-            const float o = ex.z;
-            const float E = exp2f(__fsub_rn(ex.x, mg) + ex.y);   // exponents in log2 units
-            const float wt = o * d * E;
-            float sdot = 0.0f;
-            float* acc = s_acc + j * NV;
+            const bool valid = pos >= 0 && j >= 0 && j < nb;
+            float v[NV];
 #pragma unroll
-            for (int c = 0; c < CMAX; ++c) {
-                if (c < C) {
-                    const float fc = s_feat[j * CMAX + c];
-                    sdot += G[c] * (fc - F[c]);
-                    atomicAdd(&acc[5 + c], wt * iw * G[c]);   // dL/df = (w / W) G
+            for (int q = 0; q < NV; ++q) v[q] = 0.0f;
+            bool cut = true;
+            if (valid) {
+                const float4 uv = s_uv[j];
+                const float4 ex = s_ex[j];
+                const float4 geo = s_geo[j];
+                const uint32_t fl = __float_as_uint(ex.w);
+                cut = (fl & kFlagCut) != 0u;
+                float U, V;
+                const float Q = ray_offset_q(uv, ray, f.ifx, f.ify, &U, &V);
+                const float rq = sqrtf(Q * iqq);                 // rho / c.z
+                const float d = w.dtr[(size_t)k * P + p];        // stored by the forward pass
+                const float o = ex.z;
+                const float E = exp2f(__fsub_rn(ex.x, mg) + ex.y);   // exponents in log2 units
+                const float wt = o * d * E;
+                float sdot = 0.0f;
+#pragma unroll
+                for (int c = 0; c < CMAX; ++c) {
+                    if (c < C) {
+                        const float fc = s_feat[j * CMAX + c];
+                        sdot += G[c] * (fc - F[c]);
+                        v[5 + c] = wt * iw * G[c];               // dL/df = (w / W) G
+                    }
+                }
+                const float sj = sdot * iw;                      // dL/dw = <G, f - F> / W
+                v[4] = sj * d * E * (1.0f + ex.x * 0.693147181f);   // dw/do = d E (1 + o z~/gamma)
+                if (want_geom && !cut) {
+                    const float Z = geo.z, reff = geo.w;
+                    const float ireff = 1.0f / reff;
+                    const float sE = sj * o * E;                 // dL/dd
+                    // depth factor: dw/dz~ = w o / gamma, dz~/dc.z = -1/(zfar - znear)
+                    float gcz = -sj * wt * o * f.inv_gamma * f.inv_zrange;
+                    const float rho = rq * Z;
+                    const float g_rho = -sE * ireff;             // dd/drho = -1/r_eff
+                    const float g_reff = sE * rho * ireff * ireff;
+                    float gr = 0.0f;
+                    if (fl & kFlagFloor) {
+                        // r_eff = kappa c.z / f_min
+                        gcz += g_reff * f.kappa / f.fmin;
+                        const float gf = -g_reff * f.kappa * Z / (f.fmin * f.fmin);
+                        if (f.fx <= f.fy) gk[0] += gf; else gk[1] += gf;
+                    } else {
+                        gr = g_reff;
+                    }
+                    float gcx = 0.0f, gcy = 0.0f;
+                    if (Q > 0.0f) {
+                        // drho/dc = e_perp / rho, e = c - c.z q = -c.z (U, V, 0)
+                        const float kq = (U * ray.a + V * ray.b) * iqq;
+                        const float irq = 1.0f / rq;
+                        const float n0 = -(U - kq * ray.a) * irq;
+                        const float n1 = -(V - kq * ray.b) * irq;
+                        const float n2 = kq * irq;
+                        gcx = g_rho * n0;
+                        gcy = g_rho * n1;
+                        gcz += g_rho * n2;
+                        // drho/dq = -(c.q / q.q) e_perp / rho with c.q / q.q = c.z (1 - kq);
+                        // q = ((px - cx)/fx, (py - cy)/fy, 1)
+                        const float sq = -Z * (1.0f - kq);
+                        const float ga = g_rho * sq * n0, gb = g_rho * sq * n1;
+                        gk[0] -= ga * ray.a * f.ifx;
+                        gk[1] -= gb * ray.b * f.ify;
+                        gk[2] -= ga * f.ifx;
+                        gk[3] -= gb * f.ify;
+                    }
+                    v[0] = gcx;
+                    v[1] = gcy;
+                    v[2] = gcz;
+                    v[3] = gr;
                 }
             }
-            const float sj = sdot * iw;                      // dL/dw = <G, f - F> / W
-            atomicAdd(&acc[4], sj * d * E * (1.0f + ex.x * 0.693147181f));   // dw/do
-            s_touched[j] = 1;
-            if (want_geom && !cut) {
-                const float Z = geo.z, reff = geo.w;
-                const float ireff = 1.0f / reff;
-                const float sE = sj * o * E;                 // dL/dd
-                // depth factor: dw/dz~ = w o / gamma, dz~/dc.z = -1/(zfar - znear)
-                float gcz = -sj * wt * o * f.inv_gamma * f.inv_zrange;
-                const float rho = rq * Z;
-                const float g_rho = -sE * ireff;             // dd/drho = -1/r_eff
-                const float g_reff = sE * rho * ireff * ireff;
-                float gr = 0.0f;
-                if (fl & kFlagFloor) {
-                    // r_eff = kappa c.z / f_min
-                    gcz += g_reff * f.kappa / f.fmin;
-                    const float gf = -g_reff * f.kappa * Z / (f.fmin * f.fmin);
-                    if (f.fx <= f.fy) gk[0] += gf; else gk[1] += gf;
-                } else {
-                    gr = g_reff;
-                }
-                float gcx = 0.0f, gcy = 0.0f;
-                if (Q > 0.0f) {
-                    // drho/dc = e_perp / rho, e = c - c.z q = -c.z (U, V, 0)
-                    const float kq = (U * ray.a + V * ray.b) * iqq;
-                    const float irq = 1.0f / rq;
-                    const float n0 = -(U - kq * ray.a) * irq;
-                    const float n1 = -(V - kq * ray.b) * irq;
-                    const float n2 = kq * irq;
-                    gcx = g_rho * n0;
-                    gcy = g_rho * n1;
-                    gcz += g_rho * n2;
-                    // drho/dq = -(c.q / q.q) e_perp / rho with c.q / q.q = c.z (1 - kq);
-                    // q = ((px - cx)/fx, (py - cy)/fy, 1)
-                    const float sq = -Z * (1.0f - kq);
-                    const float ga = g_rho * sq * n0, gb = g_rho * sq * n1;
-                    gk[0] -= ga * ray.a * f.ifx;
-                    gk[1] -= gb * ray.b * f.ify;
-                    gk[2] -= ga * f.ifx;
-                    gk[3] -= gb * f.ify;
-                }
-                atomicAdd(&acc[0], gcx);
-                atomicAdd(&acc[1], gcy);
-                atomicAdd(&acc[2], gcz);
-                if (gr != 0.0f) atomicAdd(&acc[3], gr);
-            }
-        }
-        __syncthreads();
-        // one flush per (sphere, tile): the sums of all this tile's pixels
-        for (int t = tid; t < nb; t += kBwdThreads) {
-            if (!s_touched[t]) continue;
-            const int id = s_id[t];
-            const float* acc = s_acc + t * NV;
-            const bool cut = (__float_as_uint(s_ex[t].w) & kFlagCut) != 0u;
-            if (want_geom && !cut) red_add_v4(&w.gacc[id], acc[0], acc[1], acc[2], acc[3]);
-            if (grad_opacity) atomicAdd(&grad_opacity[id], acc[4]);
-            if (grad_features) {
+            // group the lanes that hold the same candidate and tree-reduce within
+            // groups; lanes without a hit here get distinct keys (no group)
+            const uint32_t peers = __match_any_sync(0xffffffffu, valid ? j : -1 - lane);
+            const int rank = __popc(peers & lt_mask);
+            const int gsz = __popc(peers);
+            const int gmax = __reduce_max_sync(0xffffffffu, gsz);
+            for (int off = 1; off < gmax; off <<= 1) {
+                const bool take = (rank & (2 * off - 1)) == 0 && rank + off < gsz;
+                const int src = take ? nth_lane(peers, rank + off) : lane;
 #pragma unroll
-                for (int c = 0; c < CMAX; ++c)
-                    if (c < C) atomicAdd(&grad_features[(size_t)id * C + c], acc[5 + c]);
+                for (int q = 0; q < NV; ++q) {
+                    const float o2 = __shfl_sync(0xffffffffu, v[q], src);
+                    if (take) v[q] += o2;
+                }
+            }
+            if (rank == 0 && valid) {
+                const int id = s_id[j];
+                if (want_geom && !cut) red_add_v4(&w.gacc[id], v[0], v[1], v[2], v[3]);
+                if (grad_opacity) atomicAdd(&grad_opacity[id], v[4]);
+                if (grad_features) {
+#pragma unroll
+                    for (int c = 0; c < CMAX; ++c)
+                        if (c < C) atomicAdd(&grad_features[(size_t)id * C + c], v[5 + c]);
+                }
             }
         }
     }
