@@ -103,10 +103,18 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
         }
         __syncthreads();
         const int base = (int)(b0 - start);
+        // slot k+1's position and distance factor are loaded while slot k is processed
+        int pos_next = inside ? w.ids[p] : -1;
+        float d_next = inside ? w.dtr[p] : 0.0f;
         for (int k = 0; k < f.n_track; ++k) {
             // this pixel's k-th tracked hit, if its list position is in the batch
-            const int pos = inside ? w.ids[(size_t)k * P + p] : -1;
+            const int pos = pos_next;
+            const float d = d_next;
             if (__ballot_sync(0xffffffffu, pos >= 0) == 0u) break;   // -1 padded at the end
+            if (k + 1 < f.n_track && inside) {
+                pos_next = w.ids[(size_t)(k + 1) * P + p];
+                d_next = w.dtr[(size_t)(k + 1) * P + p];
+            }
             const int j = pos - base;
             const bool valid = pos >= 0 && j >= 0 && j < nb;
             float v[NV];
@@ -122,7 +130,6 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
                 float U, V;
                 const float Q = ray_offset_q(uv, ray, f.ifx, f.ify, &U, &V);
                 const float rq = sqrtf(Q * iqq);                 // rho / c.z
-                const float d = w.dtr[(size_t)k * P + p];        // stored by the forward pass
                 const float o = ex.z;
                 const float E = exp2f(__fsub_rn(ex.x, mg) + ex.y);   // exponents in log2 units
                 const float wt = o * d * E;
