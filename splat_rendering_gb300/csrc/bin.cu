@@ -116,14 +116,15 @@ __device__ int merge_split(const unsigned long long* a, int la, const unsigned l
     return lo;
 }
 
-__device__ __forceinline__ unsigned long long cmp_keep(unsigned long long mine,
-                                                       unsigned long long other, bool take_min) {
+template <typename K>
+__device__ __forceinline__ K cmp_keep(K mine, K other, bool take_min) {
     return take_min ? (mine < other ? mine : other) : (mine < other ? other : mine);
 }
 
-__device__ __forceinline__ void cas_pair(unsigned long long& a, unsigned long long& b, bool up) {
+template <typename K>
+__device__ __forceinline__ void cas_pair(K& a, K& b, bool up) {
     if ((a > b) == up) {
-        const unsigned long long tmp = a;
+        const K tmp = a;
         a = b;
         b = tmp;
     }
@@ -133,7 +134,8 @@ __device__ __forceinline__ void cas_pair(unsigned long long& a, unsigned long lo
 // per thread (thread t holds elements 4t .. 4t+3): stages with partner
 // distance 1 and 2 stay inside the thread, distances up to 64 use warp
 // shuffles, only the longer ones go through shared memory.
-__device__ void register_bitonic(unsigned long long (&e)[4], int np, unsigned long long* s) {
+template <typename K>
+__device__ void register_bitonic(K (&e)[4], int np, K* s) {
     const int t = threadIdx.x;
     for (int k = 2; k <= np; k <<= 1) {
         for (int j = k >> 1; j > 0; j >>= 1) {
@@ -144,7 +146,7 @@ __device__ void register_bitonic(unsigned long long (&e)[4], int np, unsigned lo
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
                     const int i = 4 * t + r;
-                    const unsigned long long p = s[i ^ j];
+                    const K p = s[i ^ j];
                     e[r] = cmp_keep(e[r], p, ((i & j) == 0) == ((i & k) == 0));
                 }
                 __syncthreads();
@@ -152,7 +154,7 @@ __device__ void register_bitonic(unsigned long long (&e)[4], int np, unsigned lo
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
                     const int i = 4 * t + r;
-                    const unsigned long long p = __shfl_xor_sync(0xffffffffu, e[r], j >> 2);
+                    const K p = __shfl_xor_sync(0xffffffffu, e[r], j >> 2);
                     e[r] = cmp_keep(e[r], p, ((i & j) == 0) == ((i & k) == 0));
                 }
             } else {
@@ -177,19 +179,79 @@ __global__ void __launch_bounds__(kSortThreads) k_tile_sort(Frame f, Workspace w
     if (end > f.max_pairs || end <= start) return;   // capacity error already latched
     const int n = (int)(end - start);
     if (n <= kRegSortMax) {
+        // Sort 32-bit keys: the tile's key bits (positive floats, so their bit
+        // patterns are monotone) minus the tile minimum, shifted to 23 bits,
+        // above the element's 9-bit local index.  Equal shifted keys are
+        // ordered by local index; such rare runs are put in exact (key, id)
+        // order by the fix-up below, so the result is the (key, id) order.
+        unsigned long long* s64 = s;                                 // [512] input pairs
+        uint32_t* s32 = reinterpret_cast<uint32_t*>(s + kRegSortMax);  // [512] sorted keys
+        __shared__ uint32_t s_min, s_max;
+        if (threadIdx.x == 0) {
+            s_min = 0xffffffffu;
+            s_max = 0u;
+        }
+        unsigned long long e64[4];
+        uint32_t kmin = 0xffffffffu, kmax = 0u;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int i = 4 * threadIdx.x + r;
+            e64[r] = i < n ? w.pairs[start + i] : ~0ull;
+            if (i < n) {
+                s64[i] = e64[r];
+                const uint32_t kb = (uint32_t)(e64[r] >> 32);
+                kmin = min(kmin, kb);
+                kmax = max(kmax, kb);
+            }
+        }
+        __syncthreads();
+        atomicMin(&s_min, kmin);
+        atomicMax(&s_max, kmax);
+        __syncthreads();
+        const uint32_t lo = s_min, span = s_max - s_min;
+        const int shift = max(0, 32 - __clz((int)span) - 23);
+        uint32_t e[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int i = 4 * threadIdx.x + r;
+            e[r] = i < n ? ((((uint32_t)(e64[r] >> 32) - lo) >> shift) << 9) | (uint32_t)i
+                         : 0xffffffffu;
+        }
         const int np = max(next_pow2(n), 128);
-        unsigned long long e[4];
+        register_bitonic(e, np, s32);
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < 4; ++r) s32[4 * threadIdx.x + r] = e[r];
+        __syncthreads();
+        bool tie = false;
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int i = 4 * threadIdx.x + r;
-            e[r] = i < n ? w.pairs[start + i] : ~0ull;
+            if (i > 0 && i < n) tie |= (s32[i] >> 9) == (s32[i - 1] >> 9);
         }
-        register_bitonic(e, np, s);
+        const bool any_tie = __syncthreads_or(tie);
+        unsigned long long* sorted = s + kRegSortMax + kRegSortMax / 2;  // [512]
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int i = 4 * threadIdx.x + r;
-            if (i < n) w.tile_ids[start + i] = (uint32_t)e[r];
+            if (i < n) sorted[i] = s64[e[r] & 511u];
         }
+        __syncthreads();
+        if (any_tie && threadIdx.x == 0) {
+            // the array is sorted except inside runs of equal shifted keys:
+            // insertion sort on the exact 64-bit (key, id) finishes it
+            for (int i = 1; i < n; ++i) {
+                const unsigned long long v = sorted[i];
+                int q = i - 1;
+                while (q >= 0 && sorted[q] > v) {
+                    sorted[q + 1] = sorted[q];
+                    --q;
+                }
+                sorted[q + 1] = v;
+            }
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < n; i += blockDim.x) w.tile_ids[start + i] = (uint32_t)sorted[i];
         return;
     }
     if (n <= kSortCap) {
