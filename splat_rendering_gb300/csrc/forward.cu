@@ -1,26 +1,31 @@
-// Forward pass (Pulsar Sec. B.1.2-B.1.4): one block per 16x16 tile; pixel
-// parallel in the sense of the paper (no two threads ever write one pixel,
-// Sec. B.1), but the work inside a warp is split in two phases so that the
-// expensive part never runs with most lanes idle.
+// Forward pass (Pulsar Sec. B.1.2-B.1.4): one block per 16x16 tile, one
+// thread per pixel; pixel parallel in the sense of the paper (no two threads
+// ever write one pixel, Sec. B.1), with the work of a warp split in two
+// phases so that the expensive part never runs with most lanes idle.
 //
-// The tile's sorted candidate list is staged through shared memory in
-// batches (coalesced id read, one 64-byte record gather per candidate).  Each
-// warp owns two pixel rows of the tile and first compacts, in list order, the
-// batch's candidates whose pixel rectangle touches its rows (cooperative
-// filtering at warp level).  Then, 32 candidates at a time:
-//   phase 1 (flattened): the (candidate, pixel) pairs of the warp's rows
-//           inside each candidate's rectangle are numbered by a warp prefix
-//           sum and tested one per lane per round with the fp32 hit test; on
-//           a hit the lane evaluates the distance factor in pair precision,
-//           parks it in the warp's 32x32 d-matrix and sets the candidate's bit
-//           in the pixel's hit mask;
+// The tile's sorted candidate list streams through shared memory in batches
+// of NB candidates, double buffered: while the warps work on batch i, the
+// 64-byte records and features of batch i+1 are already being copied by
+// cp.async (the ids of batch i+2 are read meanwhile), so one block barrier
+// per batch is all the synchronisation there is.  Each warp owns two pixel
+// rows of the tile and compacts, in list order, the batch's candidates whose
+// pixel rectangle touches its rows (cooperative filtering at warp level).
+// Then, a chunk of at most 32 candidates and kTestCap tests at a time:
+//   phase 1 (flattened): the (candidate, pixel) tests of the chunk -- the
+//           pixels of the warp's rows inside each candidate's rectangle --
+//           are numbered by a warp prefix sum and taken one per lane per
+//           round with the fp32 hit test; on a hit the lane evaluates the
+//           distance factor in pair precision, stores it under the test's
+//           number and sets the candidate's bit in the pixel's hit mask;
 //   phase 2 (one lane per pixel): the lane walks its mask bits in increasing
-//           order -- candidate order, i.e. earliest possible intersection
-//           first -- and blends each hit into its max-shifted running sums,
-//           tracking the first n_track ids.
-// Between batches the block votes on the early-stop bound (Sec. 3.2, Fig. 3;
-// B.1.3).  The pixel's result and its backward-information buffer (tracked
-// ids, stabiliser, normaliser; Sec. B.1.4) are written at the end.
+//           order -- list order, i.e. earliest possible intersection first --
+//           finds each hit's test number from the candidate's rectangle, and
+//           blends the hit into its max-shifted running sums, recording the
+//           first n_track hits.
+// At each batch barrier the block votes on the early-stop bound (Sec. 3.2,
+// Fig. 3; B.1.3).  The pixel's result and its backward-information buffer
+// (tracked list positions and distance factors, stabiliser, normaliser; Sec.
+// B.1.4) are written at the end.
 #include "pulsar_internal.cuh"
 
 namespace pulsar {
@@ -28,49 +33,63 @@ namespace {
 
 constexpr int kFwdThreads = kTilePix;
 constexpr int kWarps = kFwdThreads / 32;
+constexpr int kTestCap = 256;     // tests per chunk: entries of a warp's d buffer
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(s), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
 
 // Shared-memory layout of one block (dynamic, 16-byte aligned pieces).
 template <int CMAX>
 struct FwdSmem {
-    static constexpr int NB = CMAX <= 4 ? 128 : (CMAX <= 16 ? 64 : 32);   // batch
-    static constexpr int dmat = 0;                                         // float [8][32][32]
-    static constexpr int uv = dmat + kWarps * 32 * 32 * 4;                 // float4 [NB]
-    static constexpr int ex = uv + NB * 16;                                // float4 [NB]
-    static constexpr int ir2 = ex + NB * 16;                               // float2 [NB]
-    static constexpr int rect = ir2 + NB * 8;                              // uint2 [NB]
-    static constexpr int s2 = rect + NB * 8;                               // float [NB]
-    static constexpr int id = s2 + NB * 4;                                 // int [NB]
-    static constexpr int feat = id + NB * 4;                               // float [NB][CMAX]
-    static constexpr int list = feat + NB * CMAX * 4;                      // u16 [8][NB]
-    static constexpr int wmask = list + kWarps * NB * 2;                   // u8 [NB]
-    static constexpr int hmask = (wmask + NB + 15) / 16 * 16;              // u32 [8][32]
-    static constexpr int pqq = hmask + kWarps * 32 * 4;                    // float2 [256]
-    static constexpr int piqq = pqq + kTilePix * 8;                        // float [256]
-    static constexpr int ap = piqq + kTilePix * 4;                         // float2 [16]
-    static constexpr int bp = ap + kTile * 8;                              // float2 [16]
-    static constexpr int a = bp + kTile * 8;                               // float [16]
-    static constexpr int b = a + kTile * 4;                                // float [16]
-    static constexpr int misc = b + kTile * 4;                             // next key, hits
+    static constexpr int NB = 128;                   // candidates per batch
+    static constexpr bool kStageFeat = CMAX <= 16;   // wider features are read from global
+    static constexpr int FS = kStageFeat ? CMAX : 0;
+    // two batch buffers, each: uv, ex, geo, rk (float4 / uint4 [NB]) of the
+    // record, then features float [NB][FS] and ids int [NB]
+    static constexpr int rec_uv = 0;
+    static constexpr int rec_ex = NB * 16;
+    static constexpr int rec_geo = 2 * NB * 16;
+    static constexpr int rec_rk = 3 * NB * 16;
+    static constexpr int rec_feat = 4 * NB * 16;
+    static constexpr int rec_id = rec_feat + NB * FS * 4;
+    static constexpr int buf_bytes = rec_id + NB * 4;
+    static constexpr int list = 2 * buf_bytes;                       // u16 [8][NB]
+    static constexpr int dbuf = list + kWarps * NB * 2;              // float [8][kTestCap]
+    static constexpr int desc = dbuf + kWarps * kTestCap * 4;        // u32 [8][32]
+    static constexpr int hmask = desc + kWarps * 32 * 4;             // u32 [8][32]
+    static constexpr int pqq = hmask + kWarps * 32 * 4;              // float2 [256]
+    static constexpr int piqq = pqq + kTilePix * 8;                  // float [256]
+    static constexpr int ap = piqq + kTilePix * 4;                   // float2 [16]
+    static constexpr int bp = ap + kTile * 8;                        // float2 [16]
+    static constexpr int a = bp + kTile * 8;                         // float [16]
+    static constexpr int b = a + kTile * 4;                          // float [16]
+    static constexpr int misc = b + kTile * 4;                       // hit counter
     static constexpr int bytes = misc + 16;
 };
 
-template <int CMAX, int TMAX>
+template <int CMAX>
 __global__ void __launch_bounds__(kFwdThreads, CMAX <= 4 ? 4 : (CMAX <= 16 ? 2 : 1))
 k_forward(Frame f, Workspace w, const float* __restrict__ features, const float* __restrict__ bg,
           float* __restrict__ image) {
     using L = FwdSmem<CMAX>;
     constexpr int NB = L::NB;
+    constexpr int FS = L::FS;
     extern __shared__ __align__(16) unsigned char smem[];
-    float (*s_dmat)[32][32] = reinterpret_cast<float (*)[32][32]>(smem + L::dmat);
-    float4* s_uv = reinterpret_cast<float4*>(smem + L::uv);
-    float4* s_ex = reinterpret_cast<float4*>(smem + L::ex);    // exponent hi, lo, o, flags
-    float2* s_ir2 = reinterpret_cast<float2*>(smem + L::ir2);
-    uint2* s_rect = reinterpret_cast<uint2*>(smem + L::rect);
-    float* s_s2 = reinterpret_cast<float*>(smem + L::s2);
-    int* s_id = reinterpret_cast<int*>(smem + L::id);
-    float* s_feat = reinterpret_cast<float*>(smem + L::feat);
     uint16_t (*s_list)[NB] = reinterpret_cast<uint16_t (*)[NB]>(smem + L::list);
-    uint8_t* s_wmask = smem + L::wmask;
+    float (*s_dbuf)[kTestCap] = reinterpret_cast<float (*)[kTestCap]>(smem + L::dbuf);
+    uint32_t (*s_desc)[32] = reinterpret_cast<uint32_t (*)[32]>(smem + L::desc);
     uint32_t (*s_hmask)[32] = reinterpret_cast<uint32_t (*)[32]>(smem + L::hmask);
     float2* s_qq = reinterpret_cast<float2*>(smem + L::pqq);
     float* s_iqq = reinterpret_cast<float*>(smem + L::piqq);
@@ -78,8 +97,7 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
     float2* s_bp = reinterpret_cast<float2*>(smem + L::bp);
     float* s_a = reinterpret_cast<float*>(smem + L::a);
     float* s_b = reinterpret_cast<float*>(smem + L::b);
-    float* s_next_key = reinterpret_cast<float*>(smem + L::misc);
-    unsigned long long* s_hits = reinterpret_cast<unsigned long long*>(smem + L::misc + 8);
+    unsigned long long* s_hits = reinterpret_cast<unsigned long long*>(smem + L::misc);
 
     // a frame whose pairs overflowed max_pairs has unsorted lists: render nothing
     // (the capacity error is latched and reported by pulsar_status)
@@ -115,10 +133,32 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
         s_qq[tid] = make_float2(pq.qq.hi, pq.qq.lo);
         s_iqq[tid] = pq.iqq;
     }
+    if (tid == 0) *s_hits = 0ull;
 
     uint32_t start = w.tile_start[tile], end = w.tile_start[tile + 1];
     end = min(end, f.max_pairs);
     start = min(start, end);
+
+    // thread t < NB stages candidate t of every batch: the record's four
+    // 16-byte pieces and the features by cp.async, the id by a plain store
+    auto stage = [&](int buf, int id) {
+        unsigned char* B = smem + buf * L::buf_bytes;
+        const float4* src = reinterpret_cast<const float4*>(w.rec + id);
+        cp_async16(B + L::rec_uv + tid * 16, src + 0);
+        cp_async16(B + L::rec_ex + tid * 16, src + 1);
+        cp_async16(B + L::rec_geo + tid * 16, src + 2);
+        cp_async16(B + L::rec_rk + tid * 16, src + 3);
+        if (L::kStageFeat) {
+#pragma unroll
+            for (int c = 0; c < FS; ++c)
+                if (c < C)
+                    cp_async4(B + L::rec_feat + (tid * FS + c) * 4, features + (size_t)id * C + c);
+        }
+        reinterpret_cast<int*>(B + L::rec_id)[tid] = id;
+    };
+    if (tid < NB && start + tid < end) stage(0, (int)w.tile_ids[start + tid]);
+    cp_async_commit();
+    int id_next = (tid < NB && start + NB + tid < end) ? (int)w.tile_ids[start + NB + tid] : -1;
 
     // running max of eps/gamma and o z~/gamma (log2 units), as a float pair
     float mg = f.eg_hi, mgl = f.eg_lo;
@@ -130,57 +170,54 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
     const int p = inside ? y * f.width + x : 0;
     int nh = 0;
     bool done = !inside;
-    if (tid == 0) *s_hits = 0ull;
+    const int lx = lane & 15, ly = lane >> 4;     // the lane's pixel within the warp's rows
 
-    for (uint32_t b0 = start; b0 < end; b0 += NB) {
-        __syncthreads();   // previous batch fully consumed (and the tile constants written)
-        const uint32_t kk = b0 + tid;
-        if (tid < NB && kk < end) {
-            const int id = (int)w.tile_ids[kk];
-            const SphereRec* rp = w.rec + id;
-            const uint4 rk = rp->rk;
-            const float4 geo = rp->geo;
-            const uint2 rc = make_uint2(rk.x, rk.y);
-            s_id[tid] = id;
-            s_uv[tid] = rp->uv;
-            s_ex[tid] = rp->ex;
-            s_ir2[tid] = make_float2(geo.x, geo.y);
-            s_rect[tid] = rc;
-            s_s2[tid] = __uint_as_float(rk.z);
-            const int r0 = max((int)(rc.y & 0xffffu) - ty0, 0);
-            const int r1 = min((int)(rc.y >> 16) - ty0, kTile - 1);
-            s_wmask[tid] = (uint8_t)((0xffu << (r0 >> 1)) & (0xffu >> (7 - (r1 >> 1))));
-#pragma unroll
-            for (int c = 0; c < CMAX; ++c)
-                if (c < C) s_feat[tid * CMAX + c] = features[(size_t)id * C + c];
+    int buf = 0;
+    for (uint32_t b0 = start; b0 < end; b0 += NB, buf ^= 1) {
+        cp_async_wait_all();
+        // batch b0 has landed everywhere, the previous batch is fully consumed
+        // (so its buffer may be refilled), and the tile constants are written;
+        // the vote ends the tile once every pixel has stopped
+        if (__syncthreads_and(done)) break;
+        if (b0 + NB < end) {
+            if (id_next >= 0) stage(buf ^ 1, id_next);
+            cp_async_commit();
+            const uint32_t k2 = b0 + 2 * NB + tid;
+            id_next = (tid < NB && k2 < end) ? (int)w.tile_ids[k2] : -1;
         }
-        if (tid == 0) {
-            const uint32_t nx = b0 + NB;
-            *s_next_key = nx < end ? __uint_as_float(w.rec[w.tile_ids[nx]].rk.w) : 0.0f;
-        }
-        __syncthreads();
+        const unsigned char* B = smem + buf * L::buf_bytes;
+        const float4* s_uv = reinterpret_cast<const float4*>(B + L::rec_uv);
+        const float4* s_ex = reinterpret_cast<const float4*>(B + L::rec_ex);
+        const float4* s_geo = reinterpret_cast<const float4*>(B + L::rec_geo);
+        const uint4* s_rk = reinterpret_cast<const uint4*>(B + L::rec_rk);
+        const float* s_feat = reinterpret_cast<const float*>(B + L::rec_feat);
+        const int* s_id = reinterpret_cast<const int*>(B + L::rec_id);
         const int nb = (int)min((uint32_t)NB, end - b0);
+
         // compact this warp's candidates, in list order
         int cnt = 0;
         for (int g0 = 0; g0 < nb; g0 += 32) {
             const int ci = g0 + lane;
-            const bool rel = ci < nb && ((s_wmask[ci] >> warp) & 1u);
+            bool rel = false;
+            if (ci < nb) {
+                const uint2 rc = *reinterpret_cast<const uint2*>(&s_rk[ci]);
+                // the rectangle clipped to the tile's columns and the warp's rows
+                // is not empty (exactly when the chunk code below finds nt > 0)
+                rel = max((int)(rc.x & 0xffffu), tx0) <= min((int)(rc.x >> 16), tx0 + kTile - 1) &&
+                      max((int)(rc.y & 0xffffu), row0) <= min((int)(rc.y >> 16), row0 + 1);
+            }
             const uint32_t bits = __ballot_sync(0xffffffffu, rel);
             if (rel) s_list[warp][cnt + __popc(bits & lt_mask)] = (uint16_t)ci;
             cnt += __popc(bits);
         }
         __syncwarp();
         if (__any_sync(0xffffffffu, !done)) {
-            for (int k0 = 0; k0 < cnt; k0 += 32) {
-                s_hmask[warp][lane] = 0u;
-                __syncwarp();
-                // phase 1: the chunk's (candidate, pixel) tests, flattened over the warp:
-                // lane c describes candidate c's part of the warp's rows, a prefix sum
-                // numbers the tests, and each lane takes one test per round
-                int xa = 0, ya = 0, wd = 0, nt = 0, jc = 0;
+            for (int k0 = 0; k0 < cnt;) {
+                // lane c describes list entry k0 + c: its part of the warp's rows
+                // (columns xa.., rows ya.., width wd, nt tests)
+                int xa = 0, ya = 0, wd = 0, nt = 0;
                 if (k0 + lane < cnt) {
-                    jc = s_list[warp][k0 + lane];
-                    const uint2 rc = s_rect[jc];
+                    const uint2 rc = *reinterpret_cast<const uint2*>(&s_rk[s_list[warp][k0 + lane]]);
                     xa = max((int)(rc.x & 0xffffu), tx0);
                     ya = max((int)(rc.y & 0xffffu), row0);
                     const int xb = min((int)(rc.x >> 16), tx0 + kTile - 1);
@@ -194,28 +231,38 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
                     const int v = __shfl_up_sync(0xffffffffu, incl, o);
                     if (lane >= o) incl += v;
                 }
-                const int total = __shfl_sync(0xffffffffu, incl, 31);
+                // the chunk: the longest prefix with at most kTestCap tests (one
+                // candidate has at most 32, so the chunk is never empty)
+                const int nc = __popc(__ballot_sync(0xffffffffu, k0 + lane < cnt && incl <= kTestCap));
+                if (lane >= nc) nt = 0;
+                const int total = __shfl_sync(0xffffffffu, incl, nc - 1);
+                const int first = incl - nt;
+                if (lane < nc)
+                    s_desc[warp][lane] = (uint32_t)first | (uint32_t)(xa - tx0) << 9 |
+                                         (uint32_t)(ya - row0) << 13 | (uint32_t)wd << 14;
+                s_hmask[warp][lane] = 0u;
+                __syncwarp();
+                // phase 1: each lane takes one test per round and finds its
+                // candidate by counting the candidates that start at or before it
                 for (int t0 = 0; t0 < total; t0 += 32) {
-                    const int t = t0 + lane;
-                    int lo = 0, hi = 31;
-#pragma unroll
-                    for (int st = 0; st < 5; ++st) {
-                        const int mid = (lo + hi) >> 1;
-                        if (__shfl_sync(0xffffffffu, incl, mid) > t) hi = mid; else lo = mid + 1;
-                    }
-                    const int own = lo;
-                    const int o_first = __shfl_sync(0xffffffffu, incl - nt, own);
+                    const int rel = first - t0;
+                    const bool starts_here = nt > 0 && rel >= 0 && rel < 32;
+                    const uint32_t sb = __reduce_or_sync(0xffffffffu, starts_here ? 1u << rel : 0u);
+                    const int before = __popc(__ballot_sync(0xffffffffu, nt > 0 && rel < 0));
+                    const int own = max(before - 1 + __popc(sb & (0xffffffffu >> (31 - lane))), 0);
+                    const int o_first = __shfl_sync(0xffffffffu, first, own);
                     const int o_xa = __shfl_sync(0xffffffffu, xa, own);
                     const int o_ya = __shfl_sync(0xffffffffu, ya, own);
                     const int o_wd = __shfl_sync(0xffffffffu, wd, own);
-                    const int o_j = __shfl_sync(0xffffffffu, jc, own);
+                    const int t = t0 + lane;
                     if (t < total) {
                         // at most two rows: test q of the owner is (q mod wd, q div wd)
+                        const int j = s_list[warp][k0 + own];
                         const int q = t - o_first;
                         const int second = q >= o_wd ? 1 : 0;
                         const int xx = o_xa + q - second * o_wd;
                         const int yy = o_ya + second;
-                        const float4 uv = s_uv[o_j];
+                        const float4 uv = s_uv[j];
                         // the decision test of the specification, term by term
                         const float a = s_a[xx - tx0];
                         const float b = s_b[yy - ty0];
@@ -226,46 +273,54 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
                         const float X = __fmaf_rn(U, b, -__fmul_rn(V, a));
                         const float Q = __fmaf_rn(U, U, __fmaf_rn(V, V, __fmul_rn(X, X)));
                         const float qq = __fadd_rn(__fadd_rn(1.0f, __fmul_rn(a, a)), __fmul_rn(b, b));
-                        if (Q < __fmul_rn(s_s2[o_j], qq)) {
+                        if (Q < __fmul_rn(__uint_as_float(s_rk[j].z), qq)) {
                             const int pl = (yy - ty0) * kTile + (xx - tx0);   // pixel in tile
-                            const int pw = (yy - row0) * kTile + (xx - tx0);  // pixel in warp
                             const float2 apv = s_ap[xx - tx0];
                             const float2 bpv = s_bp[yy - ty0];
                             const float2 qqv = s_qq[pl];
-                            const float2 ir2 = s_ir2[o_j];
+                            const float4 geo = s_geo[j];
                             PixelPairs pq;
                             pq.a = {apv.x, apv.y};
                             pq.b = {bpv.x, bpv.y};
                             pq.qq = {qqv.x, qqv.y};
                             pq.iqq = s_iqq[pl];
-                            s_dmat[warp][pw][own ^ pw] =
-                                distance_factor(uv, ir2.x, ir2.y, px, py, pq, f);
-                            atomicOr(&s_hmask[warp][pw], 1u << own);
+                            s_dbuf[warp][t] = distance_factor(uv, geo.x, geo.y, px, py, pq, f);
+                            atomicOr(&s_hmask[warp][(yy - row0) * kTile + (xx - tx0)], 1u << own);
                         }
                     }
                 }
                 __syncwarp();
-                // phase 2: one lane per pixel, hits in candidate order
+                // phase 2: one lane per pixel, hits in list order
                 uint32_t m = done ? 0u : s_hmask[warp][lane];
                 while (m) {
-                    const int bit = __ffs(m) - 1;
+                    const int c = __ffs(m) - 1;
                     m &= m - 1;
-                    const int j = s_list[warp][k0 + bit];
-                    const float d = s_dmat[warp][lane][bit ^ lane];
+                    const uint32_t dc = s_desc[warp][c];
+                    const int ti = (int)(dc & 511u) + (ly - (int)((dc >> 13) & 1u)) * (int)(dc >> 14) +
+                                   (lx - (int)((dc >> 9) & 15u));
+                    const float d = s_dbuf[warp][ti];
+                    const int j = s_list[warp][k0 + c];
                     const float4 ex = s_ex[j];
                     if (ex.x > mg || (ex.x == mg && ex.y > mgl)) {
                         const float sc = exp2f(__fsub_rn(mg, ex.x) + __fsub_rn(mgl, ex.y));
                         wsum *= sc;
 #pragma unroll
-                        for (int c = 0; c < CMAX; ++c) acc[c] *= sc;
+                        for (int cc = 0; cc < CMAX; ++cc) acc[cc] *= sc;
                         mg = ex.x;
                         mgl = ex.y;
                     }
                     const float wt = ex.z * d * exp2f(__fsub_rn(ex.x, mg) + __fsub_rn(ex.y, mgl));
                     wsum += wt;
+                    if (L::kStageFeat) {
 #pragma unroll
-                    for (int c = 0; c < CMAX; ++c)
-                        if (c < C) acc[c] += wt * s_feat[j * CMAX + c];
+                        for (int cc = 0; cc < CMAX; ++cc)
+                            if (cc < C) acc[cc] += wt * s_feat[j * FS + cc];
+                    } else {
+                        const float* fp = features + (size_t)s_id[j] * C;
+#pragma unroll
+                        for (int cc = 0; cc < CMAX; ++cc)
+                            if (cc < C) acc[cc] += wt * __ldg(fp + cc);
+                    }
                     if (nh < f.n_track) {
                         // backward-information buffer: the hit's position in the tile
                         // list and its distance factor
@@ -274,20 +329,21 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
                     }
                     ++nh;
                 }
-                __syncwarp();
+                __syncwarp();   // the chunk's descriptors, masks and d buffer are free
+                k0 += nc;
             }
         }
         // early stop (allowed once n_track hits are tracked): every remaining
-        // candidate has key >= the next key, hence z~ <= z~(key), o <= 1, d <= 1
-        if (f.stop_tau > 0.0f && b0 + NB < end) {
-            if (!done && nh >= f.n_track) {
-                const float zt = fmaxf((f.zfar - *s_next_key) * f.inv_zrange, 0.0f);
-                const float rem = (float)(end - (b0 + NB));
-                done = rem * exp2f(zt * f.inv_gamma * 1.44269504f - mg) <= f.stop_tau * wsum;
-            }
-            if (__syncthreads_and(done)) break;
+        // candidate comes later in the list, so its key is >= the key of this
+        // batch's last candidate: z~ <= z~(key), o <= 1, d <= 1
+        if (f.stop_tau > 0.0f && b0 + NB < end && !done && nh >= f.n_track) {
+            const float key = __uint_as_float(s_rk[nb - 1].w);
+            const float zt = fmaxf((f.zfar - key) * f.inv_zrange, 0.0f);
+            const float rem = (float)(end - (b0 + NB));
+            done = rem * exp2f(zt * f.inv_gamma * 1.44269504f - mg) <= f.stop_tau * wsum;
         }
     }
+    cp_async_wait_all();   // nothing may be in flight when the block ends
 
     if (inside) {
         const float iw = 1.0f / wsum;
@@ -310,31 +366,18 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
     if (tid == 0 && *s_hits) atomicAdd(&w.state->hits, *s_hits);
 }
 
-template <int CMAX, int TMAX>
-cudaError_t launch_t(const Frame& f, const Workspace& w, const float* features, const float* bg,
-                     float* image, cudaStream_t stream) {
-    constexpr int bytes = FwdSmem<CMAX>::bytes;
-    k_forward<CMAX, TMAX><<<f.n_tiles, kFwdThreads, bytes, stream>>>(f, w, features, bg, image);
-    return cudaGetLastError();
-}
-
-template <int CMAX, int TMAX>
-cudaError_t prepare_t() {
-    return cudaFuncSetAttribute(k_forward<CMAX, TMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                FwdSmem<CMAX>::bytes);
-}
-
 template <int CMAX>
 cudaError_t launch_c(const Frame& f, const Workspace& w, const float* features, const float* bg,
                      float* image, cudaStream_t stream) {
-    if (f.n_track <= 8) return launch_t<CMAX, 8>(f, w, features, bg, image, stream);
-    return launch_t<CMAX, kMaxTrack>(f, w, features, bg, image, stream);
+    constexpr int bytes = FwdSmem<CMAX>::bytes;
+    k_forward<CMAX><<<f.n_tiles, kFwdThreads, bytes, stream>>>(f, w, features, bg, image);
+    return cudaGetLastError();
 }
 
 template <int CMAX>
 cudaError_t prepare_c() {
-    const cudaError_t e = prepare_t<CMAX, 8>();
-    return e != cudaSuccess ? e : prepare_t<CMAX, kMaxTrack>();
+    return cudaFuncSetAttribute(k_forward<CMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                FwdSmem<CMAX>::bytes);
 }
 
 }  // namespace
