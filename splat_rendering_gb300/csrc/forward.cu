@@ -43,6 +43,13 @@ __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
     const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(dst));
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(s), "l"(src) : "memory");
 }
+// 2^x by the approximate base-2 exponential of the PTX ISA (a few ulps; the
+// value path's tolerance is orders of magnitude wider).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
@@ -53,7 +60,7 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // Shared-memory layout of one block (dynamic, 16-byte aligned pieces).
 template <int CMAX>
 struct FwdSmem {
-    static constexpr int NB = 128;                   // candidates per batch
+    static constexpr int NB = 192;                   // candidates per batch
     static constexpr bool kStageFeat = CMAX <= 16;   // wider features are read from global
     static constexpr int FS = kStageFeat ? CMAX : 0;
     // two batch buffers, each: uv, ex, geo, rk (float4 / uint4 [NB]) of the
@@ -302,14 +309,14 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
                     const int j = s_list[warp][k0 + c];
                     const float4 ex = s_ex[j];
                     if (ex.x > mg || (ex.x == mg && ex.y > mgl)) {
-                        const float sc = exp2f(__fsub_rn(mg, ex.x) + __fsub_rn(mgl, ex.y));
+                        const float sc = ex2_approx(__fsub_rn(mg, ex.x) + __fsub_rn(mgl, ex.y));
                         wsum *= sc;
 #pragma unroll
                         for (int cc = 0; cc < CMAX; ++cc) acc[cc] *= sc;
                         mg = ex.x;
                         mgl = ex.y;
                     }
-                    const float wt = ex.z * d * exp2f(__fsub_rn(ex.x, mg) + __fsub_rn(ex.y, mgl));
+                    const float wt = ex.z * d * ex2_approx(__fsub_rn(ex.x, mg) + __fsub_rn(ex.y, mgl));
                     wsum += wt;
                     if (L::kStageFeat) {
 #pragma unroll
@@ -340,7 +347,7 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
             const float key = __uint_as_float(s_rk[nb - 1].w);
             const float zt = fmaxf((f.zfar - key) * f.inv_zrange, 0.0f);
             const float rem = (float)(end - (b0 + NB));
-            done = rem * exp2f(zt * f.inv_gamma * 1.44269504f - mg) <= f.stop_tau * wsum;
+            done = rem * ex2_approx(zt * f.inv_gamma * 1.44269504f - mg) <= f.stop_tau * wsum;
         }
     }
     cp_async_wait_all();   // nothing may be in flight when the block ends
@@ -352,7 +359,7 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
             if (c < C) image[(size_t)p * C + c] = acc[c] * iw;
         // store the stabiliser's high part; fold its low part into the normaliser
         w.mg[p] = mg;
-        w.wsum[p] = wsum * exp2f(mgl);
+        w.wsum[p] = wsum * ex2_approx(mgl);
         for (int k = nh; k < f.n_track; ++k) w.ids[(size_t)k * P + p] = -1;
         if (f.flags & 2u) w.nhits[p] = nh;
     }

@@ -211,7 +211,8 @@ __device__ __forceinline__ PixelPairs pixel_pairs(const PixelRay& r, const Frame
 //   U = (px - u)/fx, V = (py - v)/fy, ir2 = (c.z / r_eff)^2,
 //   d = (qq - Q ir2) / (qq (1 + rho / r_eff)).
 // The difference qq - Q ir2 is formed in pair arithmetic; the final scaling
-// is plain fp32 (a few ulps relative).
+// 1 / (1 + sqrt(t)) uses the approximate reciprocal square root and division
+// (a few ulps relative).
 __device__ __forceinline__ float distance_factor(const float4& uv, float ir2_hi, float ir2_lo,
                                                  float px, float py, const PixelPairs& pq,
                                                  const Frame& f) {
@@ -229,7 +230,8 @@ __device__ __forceinline__ float distance_factor(const float4& uv, float ir2_hi,
     const FPair D = pp_sub(pq.qq, Qs);
     const float t = __fmul_rn(__fadd_rn(Qs.hi, Qs.lo), pq.iqq);   // (rho / r_eff)^2
     const float Dq = __fmul_rn(__fadd_rn(D.hi, D.lo), pq.iqq);    // 1 - t
-    return __fmul_rn(Dq, __frcp_rn(__fadd_rn(1.0f, __fsqrt_rn(fmaxf(t, 0.0f)))));
+    const float s = t > 0.0f ? t * rsqrtf(t) : 0.0f;
+    return __fdividef(Dq, 1.0f + s);
 }
 
 __device__ __forceinline__ bool rect_contains(uint2 rc, int x, int y) {
