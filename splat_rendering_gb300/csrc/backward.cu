@@ -70,6 +70,27 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
     const bool inside = x < f.width && y < f.height;
     const int P = f.width * f.height;
     const int p = inside ? y * f.width + x : 0;
+    uint32_t start = w.tile_start[tile], end = w.tile_start[tile + 1];
+    end = min(end, f.max_pairs);
+    start = min(start, end);
+    // a batch's records and features are copied by cp.async; the first batch
+    // is started before the per-pixel loads so that the two latencies overlap
+    auto stage = [&](uint32_t b0, int nb) {
+        for (int t = tid; t < nb; t += kBwdThreads) {
+            const int id = (int)w.tile_ids[b0 + t];
+            const float4* src = reinterpret_cast<const float4*>(w.rec + id);
+            cp_async16(&s_uv[t], src + 0);
+            cp_async16(&s_ex[t], src + 1);
+            cp_async16(&s_geo[t], src + 2);
+            s_id[t] = id;
+#pragma unroll
+            for (int c = 0; c < CMAX; ++c)
+                if (c < C) cp_async4(&s_feat[t * CMAX + c], features + (size_t)id * C + c);
+        }
+        cp_async_commit();
+    };
+    if (start < end) stage(start, (int)min((uint32_t)NB, end - start));
+
     const PixelRay ray = pixel_ray(x, y, f);
     const float iqq = __frcp_rn(ray.qq);
     const uint32_t lt_mask = (1u << lane) - 1u;
@@ -83,29 +104,21 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
     const float mg = inside ? w.mg[p] : 0.0f;
     const float iw = inside ? 1.0f / w.wsum[p] : 0.0f;
     float gk[4] = {0.f, 0.f, 0.f, 0.f};   // d/d(fx, fy, cx, cy)
+    const int pos0 = inside ? w.ids[p] : -1;     // slot 0 of the backward-information buffer
+    const float d0 = inside ? w.dtr[p] : 0.0f;
 
-    uint32_t start = w.tile_start[tile], end = w.tile_start[tile + 1];
-    end = min(end, f.max_pairs);
-    start = min(start, end);
     for (uint32_t b0 = start; b0 < end; b0 += NB) {
-        __syncthreads();   // previous batch done
         const int nb = (int)min((uint32_t)NB, end - b0);
-        for (int t = tid; t < nb; t += kBwdThreads) {
-            const int id = (int)w.tile_ids[b0 + t];
-            const SphereRec* rp = w.rec + id;
-            s_id[t] = id;
-            s_uv[t] = rp->uv;
-            s_ex[t] = rp->ex;
-            s_geo[t] = rp->geo;
-#pragma unroll
-            for (int c = 0; c < CMAX; ++c)
-                if (c < C) s_feat[t * CMAX + c] = features[(size_t)id * C + c];
+        if (b0 != start) {
+            __syncthreads();   // previous batch done
+            stage(b0, nb);
         }
+        cp_async_wait_all();
         __syncthreads();
         const int base = (int)(b0 - start);
         // slot k+1's position and distance factor are loaded while slot k is processed
-        int pos_next = inside ? w.ids[p] : -1;
-        float d_next = inside ? w.dtr[p] : 0.0f;
+        int pos_next = pos0;
+        float d_next = d0;
         for (int k = 0; k < f.n_track; ++k) {
             // this pixel's k-th tracked hit, if its list position is in the batch
             const int pos = pos_next;
@@ -380,7 +393,10 @@ cudaError_t launch_backward(const Frame& f, const Workspace& w, const float* pos
                             float* grad_pos, float* grad_radius, float* grad_opacity,
                             float* grad_features, float* grad_cam, cudaStream_t stream) {
     const int want_geom = (grad_pos || grad_radius || grad_cam) ? 1 : 0;
-    if (f.channels <= 4)
+    if (f.channels == 3)
+        launch_bwd_c<3>(f, w, features, image, grad_image, grad_opacity, grad_features,
+                        want_geom, stream);
+    else if (f.channels <= 4)
         launch_bwd_c<4>(f, w, features, image, grad_image, grad_opacity, grad_features,
                         want_geom, stream);
     else if (f.channels <= 8)

@@ -35,28 +35,6 @@ constexpr int kFwdThreads = kTilePix;
 constexpr int kWarps = kFwdThreads / 32;
 constexpr int kTestCap = 256;     // tests per chunk: entries of a warp's d buffer
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(dst));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
-    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(dst));
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(s), "l"(src) : "memory");
-}
-// 2^x by the approximate base-2 exponential of the PTX ISA (a few ulps; the
-// value path's tolerance is orders of magnitude wider).
-__device__ __forceinline__ float ex2_approx(float x) {
-    float y;
-    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.wait_all;" ::: "memory");
-}
-
 // Shared-memory layout of one block (dynamic, 16-byte aligned pieces).
 template <int CMAX>
 struct FwdSmem {
@@ -390,7 +368,8 @@ cudaError_t prepare_c() {
 }  // namespace
 
 cudaError_t prepare_forward() {
-    cudaError_t e = prepare_c<4>();
+    cudaError_t e = prepare_c<3>();
+    if (e == cudaSuccess) e = prepare_c<4>();
     if (e == cudaSuccess) e = prepare_c<8>();
     if (e == cudaSuccess) e = prepare_c<16>();
     if (e == cudaSuccess) e = prepare_c<32>();
@@ -401,6 +380,7 @@ cudaError_t prepare_forward() {
 cudaError_t launch_forward(const Frame& f, const Workspace& w, const float* features,
                            const float* bg, float* image, int /*max_pairs_stride*/,
                            cudaStream_t stream) {
+    if (f.channels == 3) return launch_c<3>(f, w, features, bg, image, stream);
     if (f.channels <= 4) return launch_c<4>(f, w, features, bg, image, stream);
     if (f.channels <= 8) return launch_c<8>(f, w, features, bg, image, stream);
     if (f.channels <= 16) return launch_c<16>(f, w, features, bg, image, stream);

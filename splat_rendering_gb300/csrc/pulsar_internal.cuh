@@ -239,6 +239,32 @@ __device__ __forceinline__ bool rect_contains(uint2 rc, int x, int y) {
            y <= (int)(rc.y >> 16);
 }
 
+// ------------------------------------------------------------ cp.async --
+// Asynchronous global -> shared copies (PTX cp.async): 16-byte pieces bypass
+// L1, 4-byte ones go through it; a thread's copies complete at its wait.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(s), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// 2^x by the approximate base-2 exponential of the PTX ISA (a few ulps; the
+// value path's tolerance is orders of magnitude wider).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ---------------------------------------------------------- workspace --
 // Per-sphere record written by the projection: 64 bytes, i.e. two 32-byte
 // sectors, so a gather by sphere id moves no byte it does not use.
