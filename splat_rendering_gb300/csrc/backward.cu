@@ -7,10 +7,11 @@
 //             candidates are staged through shared memory in batches (as in
 //             the forward) and each pixel finds its tracked hits among them by
 //             their list positions (stored by the forward).  For tracked hit
-//             k the lanes of a warp that hold the same candidate are grouped
-//             (__match_any_sync) and their contributions tree-reduced, so one
-//             lane per distinct sphere issues the global atomics -- the
-//             warp-level aggregation of DISTWAR (arxiver abstract).  dL/dc and
+//             k, runs of adjacent lanes that hold the same candidate are
+//             tree-reduced, so one lane per run issues the global atomics --
+//             the warp-level aggregation of DISTWAR (arxiver abstract); a
+//             warp's two pixel rows are interleaved column by column, so the
+//             footprint of a small sphere is a single run.  dL/dc and
 //             dL/dr go to a float4 accumulator with one vector reduction;
 //             opacity and feature gradients go straight to the caller's
 //             (zeroed) arrays.  The intrinsics' gradient is summed per thread
@@ -33,12 +34,6 @@ constexpr int kCamThreads = 1024;
 __device__ __forceinline__ void red_add_v4(float4* addr, float a, float b, float c, float d) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
                  :: "l"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
-}
-
-// Lane of the n-th (0-based) set bit of m.
-__device__ __forceinline__ int nth_lane(uint32_t m, int n) {
-    for (int q = 0; q < n; ++q) m &= m - 1;
-    return __ffs(m) - 1;
 }
 
 // Shared-memory batch of the backward: candidates staged per batch (static
@@ -66,7 +61,9 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
     const int tile = blockIdx.x;
     const int tyi = tile / f.tiles_x, txi = tile - tyi * f.tiles_x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int x = txi * kTile + (tid & 15), y = tyi * kTile + (tid >> 4);
+    // warp w covers rows 2w, 2w+1 of the tile with the two rows of a column in
+    // adjacent lanes, so a small sphere's footprint is one run of lanes
+    const int x = txi * kTile + (lane >> 1), y = tyi * kTile + 2 * warp + (lane & 1);
     const bool inside = x < f.width && y < f.height;
     const int P = f.width * f.height;
     const int p = inside ? y * f.width + x : 0;
@@ -93,7 +90,6 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
 
     const PixelRay ray = pixel_ray(x, y, f);
     const float iqq = __frcp_rn(ray.qq);
-    const uint32_t lt_mask = (1u << lane) - 1u;
 
     float G[CMAX], F[CMAX];
 #pragma unroll
@@ -201,18 +197,24 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
                     v[3] = gr;
                 }
             }
-            // group the lanes that hold the same candidate and tree-reduce within
-            // groups; lanes without a hit here get distinct keys (no group)
-            const uint32_t peers = __match_any_sync(0xffffffffu, valid ? j : -1 - lane);
-            const int rank = __popc(peers & lt_mask);
-            const int gsz = __popc(peers);
+            // runs of lanes that hold the same candidate are tree-reduced; one
+            // lane per run issues the atomics (lanes without a hit here get
+            // distinct keys, so they form runs of one)
+            const int key = valid ? j : -1 - lane;
+            const int prevk = __shfl_up_sync(0xffffffffu, key, 1);
+            const bool head = lane == 0 || prevk != key;
+            const uint32_t heads = __ballot_sync(0xffffffffu, head);
+            const int hl = 31 - __clz(heads & (0xffffffffu >> (31 - lane)));
+            const int rank = lane - hl;
+            const uint32_t above = lane == 31 ? 0u : (heads & (0xfffffffeu << lane));
+            const int nexth = above ? __ffs(above) - 1 : 32;
+            const int gsz = nexth - hl;
             const int gmax = __reduce_max_sync(0xffffffffu, gsz);
             for (int off = 1; off < gmax; off <<= 1) {
                 const bool take = (rank & (2 * off - 1)) == 0 && rank + off < gsz;
-                const int src = take ? nth_lane(peers, rank + off) : lane;
 #pragma unroll
                 for (int q = 0; q < NV; ++q) {
-                    const float o2 = __shfl_sync(0xffffffffu, v[q], src);
+                    const float o2 = __shfl_down_sync(0xffffffffu, v[q], off);
                     if (take) v[q] += o2;
                 }
             }
