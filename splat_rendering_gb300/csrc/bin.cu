@@ -6,12 +6,14 @@
 //                latches a capacity error if M > max_pairs.
 //   k_emit       one thread per staged pair (the projection gave each pair
 //                its slot in its tile): scatter (key, id) to offset + slot.
-//   k_tile_sort  one block per tile: sort the bucket by the 64-bit key
+//   k_tile_sort  one warp per tile: sort the bucket by the 64-bit key
 //                (f32 bits of c.z - r_eff) << 32 | sphere id, which is unique,
 //                so the list does not depend on the bucket's arrival order.
-//                Lists up to kSortCap entries are sorted in shared memory
-//                (bitonic network); longer lists are sorted in chunks and
-//                merged pairwise through global memory (merge path).
+//                Lists up to kWarpSortMax entries are sorted in registers as
+//                packed 32-bit keys (bitonic network); longer ones by the
+//                warp's block, in shared memory up to kSortCap entries, and
+//                beyond that in chunks merged pairwise through global memory
+//                (merge path).
 //
 // The pairs live in L2-sized buffers for the shipped workloads (M ~ 1e6).
 #include "pulsar_internal.cuh"
@@ -22,8 +24,9 @@ namespace {
 constexpr int kScanThreads = 1024;
 constexpr int kEmitThreads = 256;
 constexpr int kSortThreads = 128;
+constexpr int kTilesPerSortBlock = kSortThreads / 32;
 constexpr int kSortCap = 2048;
-constexpr int kRegSortMax = 4 * kSortThreads;   // lists sorted in registers
+constexpr int kWarpSortMax = 512;   // lists sorted by one warp in registers
 
 __global__ void __launch_bounds__(kScanThreads) k_tile_scan(Frame f, Workspace w) {
     __shared__ uint32_t s_warp[kScanThreads / 32];
@@ -116,144 +119,123 @@ __device__ int merge_split(const unsigned long long* a, int la, const unsigned l
     return lo;
 }
 
-template <typename K>
-__device__ __forceinline__ K cmp_keep(K mine, K other, bool take_min) {
-    return take_min ? (mine < other ? mine : other) : (mine < other ? other : mine);
-}
-
-template <typename K>
-__device__ __forceinline__ void cas_pair(K& a, K& b, bool up) {
-    if ((a > b) == up) {
-        const K tmp = a;
-        a = b;
-        b = tmp;
-    }
-}
-
-// Ascending bitonic sort of up to kRegSortMax keys held in registers, four
-// per thread (thread t holds elements 4t .. 4t+3): stages with partner
-// distance 1 and 2 stay inside the thread, distances up to 64 use warp
-// shuffles, only the longer ones go through shared memory.
-template <typename K>
-__device__ void register_bitonic(K (&e)[4], int np, K* s) {
-    const int t = threadIdx.x;
-    for (int k = 2; k <= np; k <<= 1) {
+// Ascending bitonic network over a warp's 32 E keys held in registers,
+// element E * lane + r in e[r]: partners less than E apart are in the same
+// thread, the others one shuffle away.  Every stage's direction is a
+// compile-time constant or uniform over the lane's elements.
+template <int E>
+__device__ __forceinline__ void warp_bitonic(uint32_t (&e)[16], int lane) {
+#pragma unroll
+    for (int k = 2; k <= 32 * E; k <<= 1) {
+#pragma unroll
         for (int j = k >> 1; j > 0; j >>= 1) {
-            if (j >= 4 * 32) {
+            if (j >= E) {
+                const int pl = j / E;
+                const bool keep_min = ((lane & pl) == 0) == (((lane * E) & k) == 0);
 #pragma unroll
-                for (int r = 0; r < 4; ++r) s[4 * t + r] = e[r];
-                __syncthreads();
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int i = 4 * t + r;
-                    const K p = s[i ^ j];
-                    e[r] = cmp_keep(e[r], p, ((i & j) == 0) == ((i & k) == 0));
-                }
-                __syncthreads();
-            } else if (j >= 4) {
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int i = 4 * t + r;
-                    const K p = __shfl_xor_sync(0xffffffffu, e[r], j >> 2);
-                    e[r] = cmp_keep(e[r], p, ((i & j) == 0) == ((i & k) == 0));
+                for (int r = 0; r < E; ++r) {
+                    const uint32_t p = __shfl_xor_sync(0xffffffffu, e[r], pl);
+                    e[r] = keep_min ? min(e[r], p) : max(e[r], p);
                 }
             } else {
-                // inside the thread: pairs (0,1),(2,3) for j = 1; (0,2),(1,3) for j = 2;
-                // each pair's direction comes from its lower index
-                if (j == 1) {
-                    cas_pair(e[0], e[1], ((4 * t) & k) == 0);
-                    cas_pair(e[2], e[3], ((4 * t + 2) & k) == 0);
-                } else {
-                    cas_pair(e[0], e[2], ((4 * t) & k) == 0);
-                    cas_pair(e[1], e[3], ((4 * t + 1) & k) == 0);
+                const bool up_lane = ((lane * E) & k) == 0;
+#pragma unroll
+                for (int r = 0; r < E; ++r) {
+                    if ((r & j) == 0) {
+                        const bool up = k < E ? (r & k) == 0 : up_lane;
+                        const uint32_t a = e[r], b = e[r + j];
+                        const uint32_t lo = min(a, b), hi = max(a, b);
+                        e[r] = up ? lo : hi;
+                        e[r + j] = up ? hi : lo;
+                    }
                 }
             }
         }
     }
 }
 
-__global__ void __launch_bounds__(kSortThreads) k_tile_sort(Frame f, Workspace w) {
-    __shared__ unsigned long long s[kSortCap];
-    const int tile = blockIdx.x;
-    const uint32_t start = w.tile_start[tile], end = w.tile_start[tile + 1];
-    if (end > f.max_pairs || end <= start) return;   // capacity error already latched
-    const int n = (int)(end - start);
-    if (n <= kRegSortMax) {
-        // Sort 32-bit keys: the tile's key bits (positive floats, so their bit
-        // patterns are monotone) minus the tile minimum, shifted to 23 bits,
-        // above the element's 9-bit local index.  Equal shifted keys are
-        // ordered by local index; such rare runs are put in exact (key, id)
-        // order by the fix-up below, so the result is the (key, id) order.
-        unsigned long long* s64 = s;                                 // [512] input pairs
-        uint32_t* s32 = reinterpret_cast<uint32_t*>(s + kRegSortMax);  // [512] sorted keys
-        __shared__ uint32_t s_min, s_max;
-        if (threadIdx.x == 0) {
-            s_min = 0xffffffffu;
-            s_max = 0u;
-        }
-        unsigned long long e64[4];
-        uint32_t kmin = 0xffffffffu, kmax = 0u;
+// One warp sorts one tile's n <= 32 E pairs (key bits << 32 | id).  It sorts
+// 32-bit keys: the key bits (positive floats, so their bit patterns are
+// monotone) minus the tile minimum, shifted down to 23 bits, above the
+// element's 9-bit position in the bucket.  Equal shifted keys come out
+// ordered by position; such rare runs are put in exact (key, id) order by an
+// insertion pass, so the result is the (key, id) order.  s64 holds the
+// bucket (512 entries), s32 the transposition buffer (512 words), whose
+// XOR swizzle keeps both the coalesced and the lane-major access free of
+// bank conflicts; it then holds the sorted positions.
+template <int E>
+__device__ void warp_sort_tile(const Workspace& w, uint32_t start, int n,
+                               unsigned long long* s64, uint32_t* s32, int lane) {
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int i = 4 * threadIdx.x + r;
-            e64[r] = i < n ? w.pairs[start + i] : ~0ull;
-            if (i < n) {
-                s64[i] = e64[r];
-                const uint32_t kb = (uint32_t)(e64[r] >> 32);
-                kmin = min(kmin, kb);
-                kmax = max(kmax, kb);
-            }
+    for (int r = 0; r < E; ++r) {
+        const int i = 32 * r + lane;
+        if (i < n) {
+            const unsigned long long v = w.pairs[start + i];
+            s64[i] = v;
+            const uint32_t kb = (uint32_t)(v >> 32);
+            kmin = min(kmin, kb);
+            kmax = max(kmax, kb);
         }
-        __syncthreads();
-        atomicMin(&s_min, kmin);
-        atomicMax(&s_max, kmax);
-        __syncthreads();
-        const uint32_t lo = s_min, span = s_max - s_min;
-        const int shift = max(0, 32 - __clz((int)span) - 23);
-        uint32_t e[4];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int i = 4 * threadIdx.x + r;
-            e[r] = i < n ? ((((uint32_t)(e64[r] >> 32) - lo) >> shift) << 9) | (uint32_t)i
-                         : 0xffffffffu;
-        }
-        const int np = max(next_pow2(n), 128);
-        register_bitonic(e, np, s32);
-        __syncthreads();
-#pragma unroll
-        for (int r = 0; r < 4; ++r) s32[4 * threadIdx.x + r] = e[r];
-        __syncthreads();
-        bool tie = false;
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int i = 4 * threadIdx.x + r;
-            if (i > 0 && i < n) tie |= (s32[i] >> 9) == (s32[i - 1] >> 9);
-        }
-        const bool any_tie = __syncthreads_or(tie);
-        unsigned long long* sorted = s + kRegSortMax + kRegSortMax / 2;  // [512]
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int i = 4 * threadIdx.x + r;
-            if (i < n) sorted[i] = s64[e[r] & 511u];
-        }
-        __syncthreads();
-        if (any_tie && threadIdx.x == 0) {
-            // the array is sorted except inside runs of equal shifted keys:
-            // insertion sort on the exact 64-bit (key, id) finishes it
-            for (int i = 1; i < n; ++i) {
-                const unsigned long long v = sorted[i];
-                int q = i - 1;
-                while (q >= 0 && sorted[q] > v) {
-                    sorted[q + 1] = sorted[q];
-                    --q;
-                }
-                sorted[q + 1] = v;
-            }
-        }
-        __syncthreads();
-        for (int i = threadIdx.x; i < n; i += blockDim.x) w.tile_ids[start + i] = (uint32_t)sorted[i];
-        return;
     }
+    const uint32_t lo = __reduce_min_sync(0xffffffffu, kmin);
+    const uint32_t span = __reduce_max_sync(0xffffffffu, kmax) - lo;
+    const int shift = max(0, 32 - __clz((int)span) - 23);
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < E; ++r) {
+        const int i = 32 * r + lane;
+        const uint32_t key =
+            i < n ? ((((uint32_t)(s64[i] >> 32) - lo) >> shift) << 9) | (uint32_t)i : 0xffffffffu;
+        s32[i ^ (r & (E - 1))] = key;
+    }
+    __syncwarp();
+    uint32_t e[16];
+#pragma unroll
+    for (int r = 0; r < E; ++r) {
+        const int i = E * lane + r;
+        e[r] = s32[i ^ ((i >> 5) & (E - 1))];
+    }
+    warp_bitonic<E>(e, lane);
+    // equal shifted keys next to each other (ranks below n)?
+    const uint32_t prev_last = __shfl_up_sync(0xffffffffu, e[E - 1], 1);
+    bool tie = false;
+#pragma unroll
+    for (int r = 0; r < E; ++r) {
+        const int i = E * lane + r;
+        const uint32_t prev = r == 0 ? prev_last : e[r - 1];
+        tie |= i > 0 && i < n && (prev >> 9) == (e[r] >> 9);
+    }
+    const bool any_tie = __any_sync(0xffffffffu, tie);
+    uint16_t* s_pos = reinterpret_cast<uint16_t*>(s32);
+#pragma unroll
+    for (int r = 0; r < E; ++r) {
+        const int i = E * lane + r;
+        if (i < n) s_pos[i] = (uint16_t)(e[r] & 511u);
+    }
+    __syncwarp();
+    if (any_tie && lane == 0) {
+        // sorted except inside runs of equal shifted keys: insertion sort on
+        // the exact 64-bit (key, id) finishes it
+        for (int i = 1; i < n; ++i) {
+            const uint16_t v = s_pos[i];
+            const unsigned long long kv = s64[v];
+            int q = i - 1;
+            while (q >= 0 && s64[s_pos[q]] > kv) {
+                s_pos[q + 1] = s_pos[q];
+                --q;
+            }
+            s_pos[q + 1] = v;
+        }
+    }
+    __syncwarp();
+    for (int i = lane; i < n; i += 32) w.tile_ids[start + i] = (uint32_t)s64[s_pos[i]];
+}
+
+// A list longer than kWarpSortMax, sorted by the whole block: up to kSortCap
+// entries in shared memory (bitonic network on the 64-bit keys); longer ones
+// in chunks of kSortCap, merged pairwise through global memory (merge path).
+__device__ void block_sort_long(const Workspace& w, uint32_t start, int n, unsigned long long* s) {
     if (n <= kSortCap) {
         const int np = next_pow2(n);
         for (int t = threadIdx.x; t < np; t += blockDim.x)
@@ -263,7 +245,6 @@ __global__ void __launch_bounds__(kSortThreads) k_tile_sort(Frame f, Workspace w
         for (int t = threadIdx.x; t < n; t += blockDim.x) w.tile_ids[start + t] = (uint32_t)s[t];
         return;
     }
-    // long list: sort chunks of kSortCap in shared memory ...
     unsigned long long* src = w.pairs + start;
     unsigned long long* dst = w.pairs_alt + start;
     for (int c0 = 0; c0 < n; c0 += kSortCap) {
@@ -301,13 +282,49 @@ __global__ void __launch_bounds__(kSortThreads) k_tile_sort(Frame f, Workspace w
     for (int t = threadIdx.x; t < n; t += blockDim.x) w.tile_ids[start + t] = (uint32_t)src[t];
 }
 
+// Block b covers tiles 4b .. 4b+3: first each warp sorts its own tile if the
+// list has at most kWarpSortMax entries, then the block sorts the longer ones
+// together.
+__global__ void __launch_bounds__(kSortThreads) k_tile_sort(Frame f, Workspace w) {
+    __shared__ unsigned long long s[kSortCap];                        // 16 KB
+    __shared__ uint32_t s_keys[kTilesPerSortBlock][kWarpSortMax];      // 8 KB
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tile0 = blockIdx.x * kTilesPerSortBlock;
+    {
+        const int tile = tile0 + warp;
+        if (tile < f.n_tiles) {
+            const uint32_t start = w.tile_start[tile], end = w.tile_start[tile + 1];
+            // (a frame over capacity has its error latched; its lists are not sorted)
+            if (end <= f.max_pairs && end > start && end - start <= (uint32_t)kWarpSortMax) {
+                const int n = (int)(end - start);
+                unsigned long long* s64 = s + warp * kWarpSortMax;
+                uint32_t* s32 = s_keys[warp];
+                if (n <= 32) warp_sort_tile<1>(w, start, n, s64, s32, lane);
+                else if (n <= 64) warp_sort_tile<2>(w, start, n, s64, s32, lane);
+                else if (n <= 128) warp_sort_tile<4>(w, start, n, s64, s32, lane);
+                else if (n <= 256) warp_sort_tile<8>(w, start, n, s64, s32, lane);
+                else warp_sort_tile<16>(w, start, n, s64, s32, lane);
+            }
+        }
+    }
+    for (int q = 0; q < kTilesPerSortBlock; ++q) {
+        const int tile = tile0 + q;
+        if (tile >= f.n_tiles) break;
+        const uint32_t start = w.tile_start[tile], end = w.tile_start[tile + 1];
+        if (end > f.max_pairs || end <= start || end - start <= (uint32_t)kWarpSortMax) continue;
+        __syncthreads();   // the shared buffer is free
+        block_sort_long(w, start, (int)(end - start), s);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_bin(const Frame& f, const Workspace& w, cudaStream_t stream) {
     k_tile_scan<<<1, kScanThreads, 0, stream>>>(f, w);
     if (f.n > 0) {
         k_emit<<<152 * 8, kEmitThreads, 0, stream>>>(f, w);
-        k_tile_sort<<<f.n_tiles, kSortThreads, 0, stream>>>(f, w);
+        k_tile_sort<<<(f.n_tiles + kTilesPerSortBlock - 1) / kTilesPerSortBlock, kSortThreads, 0,
+                      stream>>>(f, w);
     }
     return cudaGetLastError();
 }
