@@ -50,7 +50,8 @@ class _Cam(ctypes.Structure):
     _fields_ = [("R", ctypes.c_double * 9), ("t", ctypes.c_double * 3),
                 ("fx", ctypes.c_double), ("fy", ctypes.c_double), ("cx", ctypes.c_double),
                 ("cy", ctypes.c_double), ("znear", ctypes.c_double), ("zfar", ctypes.c_double),
-                ("width", ctypes.c_int32), ("height", ctypes.c_int32)]
+                ("width", ctypes.c_int32), ("height", ctypes.c_int32),
+                ("orthographic", ctypes.c_int32)]
 
 
 class _Params(ctypes.Structure):
@@ -94,6 +95,7 @@ def _cam(cam) -> _Cam:
     for k in ("fx", "fy", "cx", "cy", "znear", "zfar"):
         setattr(c, k, float(getattr(cam, k)))
     c.width, c.height = int(cam.width), int(cam.height)
+    c.orthographic = 1 if getattr(cam, "orthographic", False) else 0
     return c
 
 

@@ -35,6 +35,16 @@
 // evaluated with every exponent shifted by m = max(eps, max_hits o*z~);
 // r_eff = max(r, kappa * c.z / min(fx, fy)); key = c.z - r_eff.
 //
+// Orthographic camera (Sec. B.1.1 bounds sphere projections for orthogonal
+// as well as pinhole cameras; the model is not printed, so this reading):
+// pixel (x, y) is the ray from (X, Y, 0) along +z in camera space, with
+// X = (x + 1/2 - cx)/fx, Y = (y + 1/2 - cy)/fy (fx, fy in pixels per world
+// unit); rho = |(c.x - X, c.y - Y)|; r_eff = max(r, kappa / min(fx, fy));
+// the pixel rectangle is [ceil(cx + fx (c.x - r_eff) - 1/2),
+// floor(cx + fx (c.x + r_eff) - 1/2)] (and likewise in y); the cull, key,
+// z~, weights and tracked set are the pinhole's; the cutoff area is
+// pi (min(fx, fy) r)^2.
+//
 // Decisions (cull, pixel rectangle, tile lists, hit set, tracked ids) are
 // taken in fp32 by a fixed sequence of correctly rounded operations (this
 // file is built with -ffp-contract=off), so the GPU can match them bit for
@@ -59,6 +69,7 @@ typedef struct {
     double t[3];
     double fx, fy, cx, cy, znear, zfar;
     int32_t width, height;
+    int32_t orthographic;    // 0: pinhole, 1: orthographic
 } ocam_t;
 
 typedef struct {
@@ -131,6 +142,22 @@ F2 project32(float f, float c0, F2 q) {
     return two_sum(s.hi, e);
 }
 
+// Orthographic camera: pixel range [ceil(u - f r - 1/2), floor(u + f r - 1/2)]
+// of a sphere with centre coordinate X along the axis and radius Rr, clamped
+// to the image (u = c0 + f X).
+template <typename T>
+void ortho_range(T X, T Rr, T f, T c0, int n, int* lo, int* hi) {
+    T umin = c0 + f * (X - Rr);
+    T umax = c0 + f * (X + Rr);
+    T a = std::ceil(umin - T(0.5));
+    T b = std::floor(umax - T(0.5));
+    T af = a < T(0) ? T(0) : a;
+    T bf = b > T(n - 1) ? T(n - 1) : b;
+    if (!(af <= bf)) { *lo = 1; *hi = 0; return; }
+    *lo = (int)af;
+    *hi = (int)bf;
+}
+
 // Pixel range along one image axis covered by the tangent cone of a sphere
 // (centre X along the axis, depth Z, radius Rr): the two tangent directions
 // from the camera in the (axis, z) plane, written without trigonometry
@@ -169,6 +196,7 @@ struct Sphere {
 // The camera as float32 values, for the fp32 decision sequence.
 struct Cam32 {
     float R[9], t[3], fx, fy, cx, cy, znear, zfar, kappa, amin;
+    int ortho;
 };
 Cam32 cam32(const ocam_t& cam, const oparams_t& prm) {
     Cam32 c;
@@ -177,6 +205,7 @@ Cam32 cam32(const ocam_t& cam, const oparams_t& prm) {
     c.fx = (float)cam.fx; c.fy = (float)cam.fy; c.cx = (float)cam.cx; c.cy = (float)cam.cy;
     c.znear = (float)cam.znear; c.zfar = (float)cam.zfar;
     c.kappa = (float)prm.kappa; c.amin = (float)prm.geom_min_area;
+    c.ortho = cam.orthographic != 0;
     return c;
 }
 
@@ -200,61 +229,82 @@ Sphere decide(const double* pd, double rd, double o, const ocam_t& cam, const Ca
         F2 cz = cam_row32(c32.R + 6, c32.t[2], p);
         float Z = cz.hi;
         float fmin = c32.fx <= c32.fy ? c32.fx : c32.fy;
-        float rf = (c32.kappa * Z) / fmin;
+        float rf = c32.ortho ? c32.kappa / fmin : (c32.kappa * Z) / fmin;
         s.floor_r = r < rf;
         float reff = s.floor_r ? rf : r;
         s.keep = Z > c32.znear && Z < c32.zfar && reff < Z;
         if (!s.keep) return s;
-        F2 u = project32(c32.fx, c32.cx, pair_div32(cx, cz));
-        F2 v = project32(c32.fy, c32.cy, pair_div32(cy, cz));
+        F2 u = project32(c32.fx, c32.cx, c32.ortho ? cx : pair_div32(cx, cz));
+        F2 v = project32(c32.fy, c32.cy, c32.ortho ? cy : pair_div32(cy, cz));
         s.u_hi = u.hi; s.u_lo = u.lo; s.v_hi = v.hi; s.v_lo = v.lo;
-        axis_range<float>(cx.hi, Z, reff, c32.fx, c32.cx, cam.width, &s.x0, &s.x1);
-        axis_range<float>(cy.hi, Z, reff, c32.fy, c32.cy, cam.height, &s.y0, &s.y1);
+        if (c32.ortho) {
+            ortho_range<float>(cx.hi, reff, c32.fx, c32.cx, cam.width, &s.x0, &s.x1);
+            ortho_range<float>(cy.hi, reff, c32.fy, c32.cy, cam.height, &s.y0, &s.y1);
+        } else {
+            axis_range<float>(cx.hi, Z, reff, c32.fx, c32.cx, cam.width, &s.x0, &s.x1);
+            axis_range<float>(cy.hi, Z, reff, c32.fy, c32.cy, cam.height, &s.y0, &s.y1);
+        }
         s.keep = s.x0 <= s.x1 && s.y0 <= s.y1;
         s.reff32 = reff;
         s.key32 = Z - reff;
-        float tt = reff / Z;
+        float tt = c32.ortho ? reff : reff / Z;
         s.s2_32 = tt * tt;
-        float g = (fmin * r) / Z;
+        float g = c32.ortho ? fmin * r : (fmin * r) / Z;
         float area = kPiF * (g * g);
         s.cut = prm.geom_cutoff && !(area > c32.amin);
     } else {
         const double r = rd;
+        const bool ortho = cam.orthographic != 0;
         double Z = s.c[2];
-        double rf = (double)prm.kappa * Z / fmin64;
+        double rf = ortho ? (double)prm.kappa / fmin64 : (double)prm.kappa * Z / fmin64;
         s.floor_r = r < rf;
         double reff = s.floor_r ? rf : (double)r;
         s.keep = Z > cam.znear && Z < cam.zfar && reff < Z;
         if (!s.keep) return s;
-        s.u64 = cam.cx + (double)cam.fx * (s.c[0] / Z);
-        s.v64 = cam.cy + (double)cam.fy * (s.c[1] / Z);
-        axis_range<double>(s.c[0], Z, reff, cam.fx, cam.cx, cam.width, &s.x0, &s.x1);
-        axis_range<double>(s.c[1], Z, reff, cam.fy, cam.cy, cam.height, &s.y0, &s.y1);
+        if (ortho) {
+            s.u64 = cam.cx + (double)cam.fx * s.c[0];
+            s.v64 = cam.cy + (double)cam.fy * s.c[1];
+            ortho_range<double>(s.c[0], reff, cam.fx, cam.cx, cam.width, &s.x0, &s.x1);
+            ortho_range<double>(s.c[1], reff, cam.fy, cam.cy, cam.height, &s.y0, &s.y1);
+        } else {
+            s.u64 = cam.cx + (double)cam.fx * (s.c[0] / Z);
+            s.v64 = cam.cy + (double)cam.fy * (s.c[1] / Z);
+            axis_range<double>(s.c[0], Z, reff, cam.fx, cam.cx, cam.width, &s.x0, &s.x1);
+            axis_range<double>(s.c[1], Z, reff, cam.fy, cam.cy, cam.height, &s.y0, &s.y1);
+        }
         s.keep = s.x0 <= s.x1 && s.y0 <= s.y1;
         s.key64 = Z - reff;
-        s.s2_64 = (reff / Z) * (reff / Z);
-        double g = fmin64 * r / Z;
+        s.s2_64 = ortho ? reff * reff : (reff / Z) * (reff / Z);
+        double g = ortho ? fmin64 * r : fmin64 * r / Z;
         s.cut = prm.geom_cutoff && !(M_PI * g * g > prm.geom_min_area);
     }
     // value path: exact geometry, branch of r_eff taken by the decision above
     const double Z = s.c[2];
-    s.u = cam.cx + (double)cam.fx * (s.c[0] / Z);
-    s.v = cam.cy + (double)cam.fy * (s.c[1] / Z);
-    s.reff = s.floor_r ? prm.kappa * Z / fmin64 : rd;
+    if (cam.orthographic) {
+        s.u = cam.cx + (double)cam.fx * s.c[0];
+        s.v = cam.cy + (double)cam.fy * s.c[1];
+        s.reff = s.floor_r ? prm.kappa / fmin64 : rd;
+    } else {
+        s.u = cam.cx + (double)cam.fx * (s.c[0] / Z);
+        s.v = cam.cy + (double)cam.fy * (s.c[1] / Z);
+        s.reff = s.floor_r ? prm.kappa * Z / fmin64 : rd;
+    }
     s.zt = ((double)cam.zfar - Z) / ((double)cam.zfar - (double)cam.znear);
     return s;
 }
 
-// Per-pixel ray constants.
+// Per-pixel ray constants: direction q = (a, b, 1) and origin (ox, oy, 0);
+// pinhole: a = (px - cx)/fx, b = (py - cy)/fy, origin 0; orthographic: a = b
+// = 0, ox = (px - cx)/fx, oy = (py - cy)/fy.
 struct Pix32 { float px, py, a, b, qq; };
-struct Pix64 { double px, py, a, b, qq; };
+struct Pix64 { double px, py, a, b, qq, ox, oy; };
 
 Pix32 pix32(int x, int y, const Cam32& cam) {
     Pix32 q;
     q.px = (float)x + 0.5f;
     q.py = (float)y + 0.5f;
-    q.a = (q.px - cam.cx) / cam.fx;
-    q.b = (q.py - cam.cy) / cam.fy;
+    q.a = cam.ortho ? 0.0f : (q.px - cam.cx) / cam.fx;
+    q.b = cam.ortho ? 0.0f : (q.py - cam.cy) / cam.fy;
     q.qq = (1.0f + q.a * q.a) + q.b * q.b;
     return q;
 }
@@ -262,8 +312,11 @@ Pix64 pix64(int x, int y, const ocam_t& cam) {
     Pix64 q;
     q.px = x + 0.5;
     q.py = y + 0.5;
-    q.a = (q.px - cam.cx) / cam.fx;
-    q.b = (q.py - cam.cy) / cam.fy;
+    const double sa = (q.px - cam.cx) / cam.fx, sb = (q.py - cam.cy) / cam.fy;
+    q.a = cam.orthographic ? 0.0 : sa;
+    q.b = cam.orthographic ? 0.0 : sb;
+    q.ox = cam.orthographic ? sa : 0.0;
+    q.oy = cam.orthographic ? sb : 0.0;
     q.qq = 1.0 + q.a * q.a + q.b * q.b;
     return q;
 }
@@ -290,6 +343,8 @@ bool hit_test(const Sphere& s, int x, int y, const Pix32& p32, const Pix64& p64,
 }
 
 // fp64 geometry of sphere s at pixel p: returns Q and sets U, V.
+// Pinhole: rho = c.z sqrt(Q / qq); orthographic (a = b = 0, U = X - c.x,
+// V = Y - c.y): rho = sqrt(Q).
 double value_Q(const Sphere& s, const Pix64& p, const ocam_t& cam, double* U, double* V) {
     *U = (p.px - s.u) / cam.fx;
     *V = (p.py - s.v) / cam.fy;
@@ -297,9 +352,13 @@ double value_Q(const Sphere& s, const Pix64& p, const ocam_t& cam, double* U, do
     return *U * *U + *V * *V + X * X;
 }
 
-// distance factor d = 1 - rho / r_eff with rho = c.z * sqrt(Q / qq)
-double dist_factor(const Sphere& s, double Q, double qq) {
-    return 1.0 - std::sqrt(Q / qq) * s.c[2] / s.reff;
+double ray_rho(const Sphere& s, double Q, double qq, const ocam_t& cam) {
+    return cam.orthographic ? std::sqrt(Q) : std::sqrt(Q / qq) * s.c[2];
+}
+
+// distance factor d = 1 - rho / r_eff
+double dist_factor(const Sphere& s, double Q, double qq, const ocam_t& cam) {
+    return 1.0 - ray_rho(s, Q, qq, cam) / s.reff;
 }
 
 struct HitKey {
@@ -474,7 +533,7 @@ int64_t oracle_render(const double* pos, const double* radius, const double* opa
                 const Sphere& s = sph[h.id];
                 double U, V;
                 double Q = value_Q(s, p64, cam, &U, &V);
-                double d = dist_factor(s, Q, p64.qq);
+                double d = dist_factor(s, Q, p64.qq, cam);
                 double w = s.o * d * std::exp((s.o * s.zt - m) / gamma);
                 W += w;
                 for (int c = 0; c < C; ++c) acc[c] += w * features[(size_t)h.id * C + c];
@@ -537,8 +596,10 @@ int64_t oracle_render(const double* pos, const double* radius, const double* opa
             const double W = Wn[pi], m = M[pi];
             double U, V;
             const double Q = value_Q(s, p, cam, &U, &V);
-            const double rq = std::sqrt(Q / p.qq);           // rho / c.z
-            const double d = 1.0 - rq * s.c[2] / s.reff;
+            const bool ortho = cam.orthographic != 0;
+            const double rho = ray_rho(s, Q, p.qq, cam);
+            const double rq = ortho ? rho : std::sqrt(Q / p.qq);   // rho (orthographic), rho / c.z
+            const double d = 1.0 - rho / s.reff;
             const double E = std::exp((s.o * s.zt - m) / gamma);
             const double w = s.o * d * E;
             double sdot = 0.0;                                 // <G, f - F>
@@ -567,17 +628,30 @@ int64_t oracle_render(const double* pos, const double* radius, const double* opa
             // dw/dz~ = w * o / gamma ; dz~/dc.z = -1/(zfar - znear)
             uc[2] += w * (s.o / gamma) * dzt_dz;
             // dw/dd = o E ; dd/drho = -1/r_eff ; dd/dr_eff = rho / r_eff^2
-            const double rho = rq * s.c[2];
             const double u_rho = -s.o * E / s.reff;
             const double u_reff = s.o * E * rho / (s.reff * s.reff);
             if (s.floor_r) {
-                // r_eff = kappa c.z / f_min
-                uc[2] += u_reff * prm.kappa / fmin;
-                uk[fmin_is_fx ? 0 : 1] += u_reff * (-prm.kappa * s.c[2] / (fmin * fmin));
+                if (ortho) {
+                    // r_eff = kappa / f_min
+                    uk[fmin_is_fx ? 0 : 1] += u_reff * (-prm.kappa / (fmin * fmin));
+                } else {
+                    // r_eff = kappa c.z / f_min
+                    uc[2] += u_reff * prm.kappa / fmin;
+                    uk[fmin_is_fx ? 0 : 1] += u_reff * (-prm.kappa * s.c[2] / (fmin * fmin));
+                }
             } else {
                 ur += u_reff;
             }
-            if (Q > 0.0) {
+            if (Q > 0.0 && ortho) {
+                // rho = |(c.x - X, c.y - Y)|, c.x - X = -U, c.y - Y = -V
+                uc[0] += u_rho * (-U / rho);
+                uc[1] += u_rho * (-V / rho);
+                // drho/dX = U / rho, X = (px - cx)/fx: dX/dfx = -X/fx, dX/dcx = -1/fx
+                uk[0] += u_rho * (U / rho) * (-p.ox / cam.fx);
+                uk[1] += u_rho * (V / rho) * (-p.oy / cam.fy);
+                uk[2] += u_rho * (U / rho) * (-1.0 / cam.fx);
+                uk[3] += u_rho * (V / rho) * (-1.0 / cam.fy);
+            } else if (Q > 0.0) {
                 // drho/dc = e_perp / rho with e = c - c.z q = -c.z (U, V, 0)
                 const double k = (U * p.a + V * p.b) / p.qq;
                 const double n0 = -(U - k * p.a) / rq, n1 = -(V - k * p.b) / rq, n2 = k / rq;

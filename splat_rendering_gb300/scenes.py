@@ -47,6 +47,7 @@ class Camera:
     height: int
     znear: float
     zfar: float
+    orthographic: bool = False   # rays along +z from (X, Y, 0); fx, fy in pixels per unit
 
     def packed(self) -> np.ndarray:
         """[R(9), t(3), fx, fy, cx, cy, znear, zfar] as float32."""
@@ -103,13 +104,15 @@ def _rotation(axis, angle) -> np.ndarray:
                      [z * x * C - y * s, z * y * C + x * s, c + z * z * C]])
 
 
-def _camera(R, t, f, width, height, znear, zfar, fy=None, cx=None, cy=None) -> Camera:
+def _camera(R, t, f, width, height, znear, zfar, fy=None, cx=None, cy=None,
+            orthographic=False) -> Camera:
     return Camera(R=_f32(np.asarray(R).reshape(9)), t=_f32(np.asarray(t).reshape(3)),
                   fx=float(np.float32(f)), fy=float(np.float32(f if fy is None else fy)),
                   cx=float(np.float32(width / 2 if cx is None else cx)),
                   cy=float(np.float32(height / 2 if cy is None else cy)),
                   width=int(width), height=int(height),
-                  znear=float(np.float32(znear)), zfar=float(np.float32(zfar)))
+                  znear=float(np.float32(znear)), zfar=float(np.float32(zfar)),
+                  orthographic=bool(orthographic))
 
 
 def _grads(rng, cams, C):
@@ -212,14 +215,17 @@ def random_scene(seed: int, n: int, width: int, height: int, *, channels: int = 
                  spread: float = 1.0, rot_deg: float = 0.0, shift=(0.0, 0.0, 0.0),
                  cx: float | None = None, cy: float | None = None,
                  znear: float = 1.0, zfar: float = 7.0, gamma: float = GAMMA,
-                 geom_cutoff: bool = True) -> Scene:
-    """A small scene for edge-case and property tests (same draw order)."""
+                 geom_cutoff: bool = True, orthographic: bool = False) -> Scene:
+    """A small scene for edge-case and property tests (same draw order).  With
+    an orthographic camera, f is in pixels per world unit and the spheres fill
+    the image's box instead of its frustum."""
     rng = np.random.default_rng(seed)
     f = float(max(width, height)) if f is None else f
     z = rng.uniform(zrange[0], zrange[1], n)
     hx = spread * (width / 2) / f
     hy = spread * (height / 2) / (f if fy is None else fy)
-    pos = np.stack([rng.uniform(-1, 1, n) * hx * z, rng.uniform(-1, 1, n) * hy * z, z], 1)
+    sz = np.ones_like(z) if orthographic else z
+    pos = np.stack([rng.uniform(-1, 1, n) * hx * sz, rng.uniform(-1, 1, n) * hy * sz, z], 1)
     rad = _log_uniform(rng, rrange[0], rrange[1], n) if n else np.zeros(0)
     opa = rng.uniform(orange[0], orange[1], n)
     feat = rng.uniform(0.0, 1.0, (n, channels))
@@ -232,7 +238,8 @@ def random_scene(seed: int, n: int, width: int, height: int, *, channels: int = 
     # a camera transform that keeps the sampled camera-space positions: p_world = R^T (p_cam - t)
     t = np.asarray(shift, dtype=np.float64)
     pos_w = (pos - t) @ R
-    cams = [_camera(R, t, f, width, height, znear, zfar, fy=fy, cx=cx, cy=cy)]
+    cams = [_camera(R, t, f, width, height, znear, zfar, fy=fy, cx=cx, cy=cy,
+                    orthographic=orthographic)]
     p = Params(n_track=n_track, channels=channels, gamma=gamma, geom_cutoff=geom_cutoff)
     return Scene(f"random{seed}", _f32(pos_w), _f32(rad), _f32(opa), _f32(feat), cams, p,
                  _f32(np.zeros(channels)), _grads(rng, cams, channels))

@@ -83,3 +83,45 @@ def render(pos, radius, opacity, features, cam, params, bg):
         for y, x in zip(*np.nonzero(m)):
             hits[y][x].append(int(i))
     return num / den[..., None], hits
+
+
+def render_ortho(pos, radius, opacity, features, cam, params, bg):
+    """Orthographic counterpart of render(): pixel (x, y) is the camera-space
+    ray o + s e_z from o = (X, Y, 0), X = (x + 0.5 - cx)/fx, Y = (y + 0.5 -
+    cy)/fy; the ray-to-centre distance is taken as the 3-D distance from the
+    centre c to its closest point on the ray, o + ((c - o).e_z) e_z, instead
+    of from pixel offsets to the projected centre.  Returns image [H,W,C] and
+    per-pixel hit ids in (key, id) order."""
+    c = camera_space(pos, cam)
+    r = np.maximum(np.asarray(radius, np.float64), params.kappa / min(cam.fx, cam.fy))
+    H, W = cam.height, cam.width
+    X = (np.arange(W) + 0.5 - cam.cx) / cam.fx
+    Y = (np.arange(H) + 0.5 - cam.cy) / cam.fy
+    Xg, Yg = np.meshgrid(X, Y)
+    org = np.stack([Xg, Yg, np.zeros_like(Xg)], -1)            # [H,W,3]
+    ez = np.array([0.0, 0.0, 1.0])
+    C = features.shape[1]
+    zt = (cam.zfar - c[:, 2]) / (cam.zfar - cam.znear)
+    o = np.asarray(opacity, np.float64)
+    num = np.zeros((H, W, C)) + math.exp(params.bg_eps / params.gamma) * np.asarray(bg, np.float64)
+    den = np.zeros((H, W)) + math.exp(params.bg_eps / params.gamma)
+    hits = [[[] for _ in range(W)] for _ in range(H)]
+    keyv = c[:, 2] - r
+    order = np.lexsort((np.arange(len(keyv)), keyv))
+    for i in order:
+        z = c[i, 2]
+        if not (cam.znear < z < cam.zfar and r[i] < z):
+            continue
+        dvec = c[i] - org
+        closest = org + (dvec @ ez)[..., None] * ez
+        rho = np.linalg.norm(c[i] - closest, axis=-1)
+        m = rho < r[i]
+        if not m.any():
+            continue
+        d = 1.0 - rho / r[i]
+        w = np.where(m, o[i] * d * math.exp(o[i] * zt[i] / params.gamma), 0.0)
+        num += w[..., None] * np.asarray(features[i], np.float64)
+        den += w
+        for y, x in zip(*np.nonzero(m)):
+            hits[y][x].append(int(i))
+    return num / den[..., None], hits
