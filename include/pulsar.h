@@ -54,24 +54,30 @@ extern "C" {
 
 /* --------------------------------------------------------------- flags -- */
 /* Drop position/radius gradients (and the sphere's share of the camera
- * gradient) of spheres whose projected area pi*(f_min*r/c.z)^2 is at most
+ * gradient) of spheres whose projected area pi*(f_min*r/c.z)^2 (pinhole;
+ * pi*(f_min*r)^2 orthographic) is at most
  * geom_min_area px^2 (Pulsar Sec. 6, App. A: "more than three projected
  * pixels").  Opacity and feature gradients are always kept. */
 #define PULSAR_FLAG_GEOM_CUTOFF   0x1u
 /* Also record the number of hits of every pixel (for tests; costs 4 B/px). */
 #define PULSAR_FLAG_COUNT_HITS    0x2u
 
-/* Pinhole camera, OpenCV axes (x right, y down, z forward).  R is the
- * world->camera rotation, row-major: c = R p + t.  Pixel (x, y) has its
- * centre at (x + 0.5, y + 0.5) and ray direction
- * ((x + 0.5 - cx)/fx, (y + 0.5 - cy)/fy, 1).  Spheres are kept when
- * znear < c.z < zfar.  (Pulsar Sec. 3.2: R, t, K; App. A.) */
+/* Camera, OpenCV axes (x right, y down, z forward).  R is the world->camera
+ * rotation, row-major: c = R p + t.  Pixel (x, y) has its centre at
+ * (x + 0.5, y + 0.5).  Pinhole (orthographic = 0): the pixel's ray leaves the
+ * origin along ((x + 0.5 - cx)/fx, (y + 0.5 - cy)/fy, 1); fx, fy in pixels.
+ * Orthographic (orthographic = 1; Pulsar Sec. B.1.1 bounds projections for
+ * both): the ray leaves ((x + 0.5 - cx)/fx, (y + 0.5 - cy)/fy, 0) along +z;
+ * fx, fy in pixels per world unit, and the kappa floor of the radius is
+ * kappa/min(fx, fy).  Spheres are kept when znear < c.z < zfar and
+ * r_eff < c.z.  (Pulsar Sec. 3.2: R, t, K; App. A.) */
 typedef struct pulsar_camera {
     float R[9];
     float t[3];
     float fx, fy, cx, cy;
     int32_t width, height;   /* 1 .. 65535 */
     float znear, zfar;       /* 0 < znear < zfar */
+    int32_t orthographic;    /* 0: pinhole, 1: orthographic; other values: PULSAR_ERR_ARG */
 } pulsar_camera_t;
 
 /* Blend and gradient parameters. */

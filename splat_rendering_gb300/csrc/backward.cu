@@ -138,7 +138,7 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
                 cut = (fl & kFlagCut) != 0u;
                 float U, V;
                 const float Q = ray_offset_q(uv, ray, f.ifx, f.ify, &U, &V);
-                const float rq = sqrtf(Q * iqq);                 // rho / c.z
+                const float rq = sqrtf(Q * iqq);                 // rho / c.z (orthographic: rho)
                 const float o = ex.z;
                 const float E = exp2f(__fsub_rn(ex.x, mg) + ex.y);   // exponents in log2 units
                 const float wt = o * d * E;
@@ -159,14 +159,14 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
                     const float sE = sj * o * E;                 // dL/dd
                     // depth factor: dw/dz~ = w o / gamma, dz~/dc.z = -1/(zfar - znear)
                     float gcz = -sj * wt * o * f.inv_gamma * f.inv_zrange;
-                    const float rho = rq * Z;
+                    const float rho = f.ortho ? rq : rq * Z;
                     const float g_rho = -sE * ireff;             // dd/drho = -1/r_eff
                     const float g_reff = sE * rho * ireff * ireff;
                     float gr = 0.0f;
                     if (fl & kFlagFloor) {
-                        // r_eff = kappa c.z / f_min
-                        gcz += g_reff * f.kappa / f.fmin;
-                        const float gf = -g_reff * f.kappa * Z / (f.fmin * f.fmin);
+                        // r_eff = kappa c.z / f_min (orthographic: kappa / f_min)
+                        if (!f.ortho) gcz += g_reff * f.kappa / f.fmin;
+                        const float gf = -g_reff * f.kappa * (f.ortho ? 1.0f : Z) / (f.fmin * f.fmin);
                         if (f.fx <= f.fy) gk[0] += gf; else gk[1] += gf;
                     } else {
                         gr = g_reff;
@@ -183,11 +183,12 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
                         gcy = g_rho * n1;
                         gcz += g_rho * n2;
                         // drho/dq = -(c.q / q.q) e_perp / rho with c.q / q.q = c.z (1 - kq);
-                        // q = ((px - cx)/fx, (py - cy)/fy, 1)
-                        const float sq = -Z * (1.0f - kq);
+                        // q = ((px - cx)/fx, (py - cy)/fy, 1).  Orthographic: drho/do =
+                        // -e_perp / rho for the origin o = ((px - cx)/fx, (py - cy)/fy, 0)
+                        const float sq = f.ortho ? -1.0f : -Z * (1.0f - kq);
                         const float ga = g_rho * sq * n0, gb = g_rho * sq * n1;
-                        gk[0] -= ga * ray.a * f.ifx;
-                        gk[1] -= gb * ray.b * f.ify;
+                        gk[0] -= ga * (f.ortho ? ray.ox : ray.a) * f.ifx;
+                        gk[1] -= gb * (f.ortho ? ray.oy : ray.b) * f.ify;
                         gk[2] -= ga * f.ifx;
                         gk[3] -= gb * f.ify;
                     }

@@ -98,23 +98,26 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
     const uint32_t lt_mask = (1u << lane) - 1u;
     // per-tile ray constants: decision slopes (fp32) and value slopes (pairs)
     // of the 16 columns and 16 rows, |q|^2 of every pixel
+    // (orthographic rays are parallel: all slopes are 0)
     if (tid < kTile) {
         const float px = __fadd_rn(__int2float_rn(tx0 + tid), 0.5f);
-        s_a[tid] = __fdiv_rn(__fsub_rn(px, f.cx), f.fx);
-        const FPair ap = slope_pair(px, f.cx, f.ifx, f.ifx_lo);
+        s_a[tid] = f.ortho ? 0.0f : __fdiv_rn(__fsub_rn(px, f.cx), f.fx);
+        const FPair ap = f.ortho ? FPair{0.0f, 0.0f} : slope_pair(px, f.cx, f.ifx, f.ifx_lo);
         s_ap[tid] = make_float2(ap.hi, ap.lo);
     } else if (tid < 2 * kTile) {
         const int r = tid - kTile;
         const float py = __fadd_rn(__int2float_rn(ty0 + r), 0.5f);
-        s_b[r] = __fdiv_rn(__fsub_rn(py, f.cy), f.fy);
-        const FPair bp = slope_pair(py, f.cy, f.ify, f.ify_lo);
+        s_b[r] = f.ortho ? 0.0f : __fdiv_rn(__fsub_rn(py, f.cy), f.fy);
+        const FPair bp = f.ortho ? FPair{0.0f, 0.0f} : slope_pair(py, f.cy, f.ify, f.ify_lo);
         s_bp[r] = make_float2(bp.hi, bp.lo);
     }
     {
         const float px = __fadd_rn(__int2float_rn(x), 0.5f);
         const float py = __fadd_rn(__int2float_rn(y), 0.5f);
-        const PixelPairs pq = pixel_pairs(slope_pair(px, f.cx, f.ifx, f.ifx_lo),
-                                          slope_pair(py, f.cy, f.ify, f.ify_lo));
+        const FPair zero = {0.0f, 0.0f};
+        const PixelPairs pq =
+            pixel_pairs(f.ortho ? zero : slope_pair(px, f.cx, f.ifx, f.ifx_lo),
+                        f.ortho ? zero : slope_pair(py, f.cy, f.ify, f.ify_lo));
         s_qq[tid] = make_float2(pq.qq.hi, pq.qq.lo);
         s_iqq[tid] = pq.iqq;
     }

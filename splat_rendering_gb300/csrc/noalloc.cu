@@ -100,7 +100,7 @@ extern "C" int pulsar_render_noalloc(const float* pos, const float* radius, cons
     if (cam->width < 1 || cam->height < 1 || cam->width > kMaxSide || cam->height > kMaxSide)
         return PULSAR_ERR_ARG;
     if (!positive(cam->fx) || !positive(cam->fy) || !(cam->znear > 0.0f) ||
-        !(cam->zfar > cam->znear))
+        !(cam->zfar > cam->znear) || (cam->orthographic != 0 && cam->orthographic != 1))
         return PULSAR_ERR_ARG;
     if (!positive(prm->gamma) || !(prm->bg_eps >= 0.0f) || !(prm->stop_tau >= 0.0f) ||
         !(prm->kappa >= 0.0f) || !(prm->geom_min_area >= 0.0f) || prm->n_track < 1 ||
@@ -164,6 +164,7 @@ extern "C" int pulsar_render_noalloc(const float* pos, const float* radius, cons
     f.n = (int)n;
     f.flags = prm->flags;
     f.max_pairs = (uint32_t)kMaxPairs;
+    f.ortho = cam->orthographic;
 
     // the arena keeps the previous call's contents: clear what must start at zero
     if (cudaMemsetAsync(w.tile_count, 0, 4 * (size_t)kMaxTilesNA, s) != cudaSuccess ||

@@ -28,7 +28,9 @@ k_project(Frame f, Workspace w, const float* __restrict__ pos, const float* __re
         const FPair cz = camera_row(f.R[6], f.R[7], f.R[8], f.t[2], px, py, pz);
         const float Z = cz.hi;
         // at-least-one-pixel floor of the radius
-        const float rfloor = __fdiv_rn(__fmul_rn(f.kappa, Z), f.fmin);
+        // (orthographic: kappa / f_min)
+        const float rfloor = f.ortho ? __fdiv_rn(f.kappa, f.fmin)
+                                     : __fdiv_rn(__fmul_rn(f.kappa, Z), f.fmin);
         const bool on_floor = r < rfloor;
         const float reff = on_floor ? rfloor : r;
         bool keep = Z > f.znear && Z < f.zfar && reff < Z;
@@ -37,16 +39,22 @@ k_project(Frame f, Workspace w, const float* __restrict__ pos, const float* __re
         uint32_t flags = 0;
         float key = 0.f, s2 = 0.f;
         if (keep) {
-            const FPair u = pair_project(f.fx, f.cx, pair_quotient(cx, cz));
-            const FPair v = pair_project(f.fy, f.cy, pair_quotient(cy, cz));
+            // projected centre c0 + f c.x / c.z (orthographic: c0 + f c.x)
+            const FPair u = pair_project(f.fx, f.cx, f.ortho ? cx : pair_quotient(cx, cz));
+            const FPair v = pair_project(f.fy, f.cy, f.ortho ? cy : pair_quotient(cy, cz));
             int x0, x1, y0, y1;
-            keep = tangent_range(cx.hi, Z, reff, f.fx, f.cx, f.width, &x0, &x1) &&
-                   tangent_range(cy.hi, Z, reff, f.fy, f.cy, f.height, &y0, &y1);
+            if (f.ortho)
+                keep = ortho_range(cx.hi, reff, f.fx, f.cx, f.width, &x0, &x1) &&
+                       ortho_range(cy.hi, reff, f.fy, f.cy, f.height, &y0, &y1);
+            else
+                keep = tangent_range(cx.hi, Z, reff, f.fx, f.cx, f.width, &x0, &x1) &&
+                       tangent_range(cy.hi, Z, reff, f.fy, f.cy, f.height, &y0, &y1);
             if (keep) {
                 key = __fsub_rn(Z, reff);
-                const float tt = __fdiv_rn(reff, Z);
+                // s = r_eff / c.z (orthographic: r_eff, rays parallel)
+                const float tt = f.ortho ? reff : __fdiv_rn(reff, Z);
                 s2 = __fmul_rn(tt, tt);
-                const float g = __fdiv_rn(__fmul_rn(f.fmin, r), Z);
+                const float g = f.ortho ? __fmul_rn(f.fmin, r) : __fdiv_rn(__fmul_rn(f.fmin, r), Z);
                 const float area = __fmul_rn(kPi, __fmul_rn(g, g));
                 const bool cut = (f.flags & 1u) && !(area > f.amin);
                 flags = kFlagKeep | (on_floor ? kFlagFloor : 0u) | (cut ? kFlagCut : 0u);
@@ -63,13 +71,14 @@ k_project(Frame f, Workspace w, const float* __restrict__ pos, const float* __re
                 e.lo = __fmaf_rn(on.hi, f.zk_lo, __fmaf_rn(on.lo, f.zk_hi, e.lo));
                 e = ef_fast_sum(e.hi, e.lo);
                 r1 = make_float4(e.hi, e.lo, o, 0.0f);
-                // (c.z / r_eff)^2 as a pair: on the kappa floor c.z / r_eff = f_min / kappa
+                // (c.z / r_eff)^2 (orthographic: 1 / r_eff^2) as a pair; on the
+                // kappa floor c.z / r_eff (orthographic: 1 / r_eff) = f_min / kappa
                 FPair ir;
                 if (on_floor) {
                     const float q = __fdiv_rn(f.fmin, f.kappa);
                     ir = {q, __fdiv_rn(__fmaf_rn(-q, f.kappa, f.fmin), f.kappa)};
                 } else {
-                    ir = pair_quotient(cz, FPair{r, 0.0f});
+                    ir = pair_quotient(f.ortho ? FPair{1.0f, 0.0f} : cz, FPair{r, 0.0f});
                 }
                 const FPair ir2 = pp_sq(ir);
                 r2 = make_float4(ir2.hi, ir2.lo, Z, reff);

@@ -159,7 +159,7 @@ int pulsar_project(pulsar_ctx_t c, const float* pos, const float* radius, const 
     if (cam->width < 1 || cam->height < 1 || cam->width > c->max_w || cam->height > c->max_h)
         return PULSAR_ERR_ARG;
     if (!finite_pos(cam->fx) || !finite_pos(cam->fy) || !(cam->znear > 0.0f) ||
-        !(cam->zfar > cam->znear))
+        !(cam->zfar > cam->znear) || (cam->orthographic != 0 && cam->orthographic != 1))
         return PULSAR_ERR_ARG;
     if (!finite_pos(prm->gamma) || !(prm->bg_eps >= 0.0f) || !(prm->stop_tau >= 0.0f) ||
         !(prm->kappa >= 0.0f) || !(prm->geom_min_area >= 0.0f) || prm->n_track < 1 ||
@@ -210,6 +210,7 @@ int pulsar_project(pulsar_ctx_t c, const float* pos, const float* radius, const 
     f.n = (int)n;
     f.flags = prm->flags;
     f.max_pairs = (uint32_t)c->max_pairs;
+    f.ortho = cam->orthographic;
     c->pos = pos;
     cudaError_t e = launch_project(f, c->ws, pos, radius, opacity, s);
     if (e != cudaSuccess) return PULSAR_ERR_CUDA;

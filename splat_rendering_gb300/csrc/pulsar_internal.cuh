@@ -38,6 +38,7 @@ struct Frame {
     int n;
     uint32_t flags;
     uint32_t max_pairs;
+    int ortho;            // orthographic camera: rays along +z, slopes a = b = 0
 };
 
 // Small device-resident counters.
@@ -131,21 +132,46 @@ __device__ __forceinline__ bool tangent_range(float X, float Z, float rr, float 
     return true;
 }
 
-// Per-pixel ray constants of the decision path.
+// Per-pixel ray constants of the decision path: direction (a, b, 1), origin
+// (ox, oy, 0).  Pinhole: a = (px - cx)/fx, b = (py - cy)/fy, origin 0;
+// orthographic: a = b = 0, ox = (px - cx)/fx, oy = (py - cy)/fy.
 struct PixelRay {
     float px, py;   // pixel centre
-    float a, b;     // ray slopes (px - cx)/fx, (py - cy)/fy
+    float a, b;     // ray slopes
     float qq;       // 1 + a^2 + b^2
+    float ox, oy;   // ray origin
 };
 
 __device__ __forceinline__ PixelRay pixel_ray(int x, int y, const Frame& f) {
     PixelRay r;
     r.px = __fadd_rn(__int2float_rn(x), 0.5f);
     r.py = __fadd_rn(__int2float_rn(y), 0.5f);
-    r.a = __fdiv_rn(__fsub_rn(r.px, f.cx), f.fx);
-    r.b = __fdiv_rn(__fsub_rn(r.py, f.cy), f.fy);
+    const float sa = __fdiv_rn(__fsub_rn(r.px, f.cx), f.fx);
+    const float sb = __fdiv_rn(__fsub_rn(r.py, f.cy), f.fy);
+    r.a = f.ortho ? 0.0f : sa;
+    r.b = f.ortho ? 0.0f : sb;
+    r.ox = f.ortho ? sa : 0.0f;
+    r.oy = f.ortho ? sb : 0.0f;
     r.qq = __fadd_rn(__fadd_rn(1.0f, __fmul_rn(r.a, r.a)), __fmul_rn(r.b, r.b));
     return r;
+}
+
+// Orthographic pixel range [ceil(c0 + f (X - rr) - 1/2), floor(c0 + f (X +
+// rr) - 1/2)] along one image axis (n pixels), clamped to the image.
+// Returns false if the range is empty.
+__device__ __forceinline__ bool ortho_range(float X, float rr, float f, float c0, int n,
+                                            int* lo, int* hi) {
+    const float umin = __fadd_rn(c0, __fmul_rn(f, __fsub_rn(X, rr)));
+    const float umax = __fadd_rn(c0, __fmul_rn(f, __fadd_rn(X, rr)));
+    float a = ceilf(__fsub_rn(umin, 0.5f));
+    float b = floorf(__fsub_rn(umax, 0.5f));
+    const float top = (float)(n - 1);
+    a = a < 0.0f ? 0.0f : a;
+    b = b > top ? top : b;
+    if (!(a <= b)) return false;
+    *lo = (int)a;
+    *hi = (int)b;
+    return true;
 }
 
 // Q = (rho / c.z)^2 * qq evaluated from pixel offsets to the projected centre

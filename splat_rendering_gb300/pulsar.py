@@ -39,7 +39,8 @@ class Camera(ctypes.Structure):
     _fields_ = [("R", ctypes.c_float * 9), ("t", ctypes.c_float * 3),
                 ("fx", ctypes.c_float), ("fy", ctypes.c_float), ("cx", ctypes.c_float),
                 ("cy", ctypes.c_float), ("width", ctypes.c_int32), ("height", ctypes.c_int32),
-                ("znear", ctypes.c_float), ("zfar", ctypes.c_float)]
+                ("znear", ctypes.c_float), ("zfar", ctypes.c_float),
+                ("orthographic", ctypes.c_int32)]
 
 
 class Params(ctypes.Structure):
@@ -117,13 +118,14 @@ def _check(code: int, what: str):
 
 def camera(cam) -> Camera:
     """Camera struct from any object with R, t, fx, fy, cx, cy, width, height,
-    znear, zfar attributes."""
+    znear, zfar attributes (and optionally orthographic)."""
     c = Camera()
     c.R[:] = [float(v) for v in np.asarray(cam.R, np.float32).reshape(9)]
     c.t[:] = [float(v) for v in np.asarray(cam.t, np.float32).reshape(3)]
     for k in ("fx", "fy", "cx", "cy", "znear", "zfar"):
         setattr(c, k, float(getattr(cam, k)))
     c.width, c.height = int(cam.width), int(cam.height)
+    c.orthographic = 1 if getattr(cam, "orthographic", False) else 0
     return c
 
 

@@ -55,8 +55,9 @@ def test_strerror_and_host_side_argument_errors(lib):
 
 def test_struct_layouts_match_header():
     from splat_rendering_gb300 import pulsar as pl
-    assert ctypes.sizeof(pl.Camera) == 4 * (9 + 3 + 4) + 4 * 2 + 4 * 2
+    assert ctypes.sizeof(pl.Camera) == 4 * (9 + 3 + 4) + 4 * 2 + 4 * 2 + 4
     assert pl.Camera.width.offset == 64 and pl.Camera.znear.offset == 72
+    assert pl.Camera.orthographic.offset == 80
     assert ctypes.sizeof(pl.Params) == 4 * 5 + 4 * 3
 
 

@@ -32,12 +32,14 @@ def _noalloc_image(sc):
 
 
 def test_noalloc_render_matches_context_path_on_consecutive_calls():
-    # two different frames in a row (different sizes, channels and n_track),
-    # then the first again: each must match the context path
+    # different frames in a row (different sizes, channels, n_track, an
+    # orthographic camera), then the first again: each must match the context path
     first = scenes.random_scene(71, 3000, 200, 150, rot_deg=9, rrange=(0.01, 0.3))
     second = scenes.random_scene(72, 800, 96, 120, channels=5, n_track=7, fy=130.0, cx=40.0,
                                  rrange=(0.02, 0.4))
-    for sc in (first, second, first):
+    third = scenes.random_scene(74, 1500, 120, 100, f=40.0, orthographic=True, rot_deg=12,
+                                rrange=(0.01, 0.2))
+    for sc in (first, second, third, first):
         ref = gh.run_gpu(sc, want=False, debug=False)
         assert ref["code"] == 0
         img = _noalloc_image(sc)
