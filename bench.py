@@ -29,6 +29,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 WORKLOAD = "headline: 1,000,000 spheres, 1024x1024, 3 channels, n_track 5, R/t/K gradients"
+WORKLOADS = {
+    "headline": WORKLOAD,
+    "headline_ortho": "headline sizes, orthographic camera: 1,000,000 spheres, 1024x1024, "
+                      "3 channels, n_track 5, R/t/K gradients",
+    "neural": "neural: 1,000,000 spheres, 1024x1024, 16 channels, n_track 8, R/t/K gradients",
+}
 METRIC = "fwd+bwd frames/s at 1M spheres 1024^2"
 UNIT = "frames/s"
 KERNELS_PER_STEP = 8   # project, tile_scan, emit, tile_sort, forward, backward, finalize, camera_reduce
@@ -43,6 +49,8 @@ def args_parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle sample")
+    ap.add_argument("--scene", default="headline", choices=sorted(WORKLOADS),
+                    help="workload (the default is the headline configuration)")
     ap.add_argument("--frames-only", type=int, default=0,
                     help="render and differentiate this many frames eagerly, print nothing "
                          "(a short fixed launch sequence for profilers)")
@@ -243,7 +251,7 @@ def run_gb300(a):
     pl.load()
     dev = torch.device("cuda", local)
 
-    scene = scenes.headline()
+    scene = scenes.make(a.scene)
     cam, prm = scene.cameras[0], scene.params
     N, C, T = scene.n, prm.channels, prm.n_track
     P = cam.width * cam.height
@@ -400,7 +408,8 @@ def run_gb300(a):
     achieved = fwd_flops / fwd_s / 1e12
     roofline = {"bound": "alu", "kernel": "k_forward", "achieved": achieved, "peak": fp32,
                 "unit": "TFLOP/s", "frac": achieved / fp32,
-                "traffic": traffic_from_profile("k_forward", "forward.cu", "headline"),
+                "traffic": (traffic_from_profile("k_forward", "forward.cu", "headline")
+                            if a.scene == "headline" else None),
                 "algorithmic_flops": fwd_flops, "algorithmic_bytes": fwd_bytes,
                 "hbm_frac": fwd_bytes / fwd_s / 1e9 / hbm,
                 "peak_source": f"FP32: {SMS} SMs x {FP32_LANES} lanes x 2 x "
@@ -418,7 +427,7 @@ def run_gb300(a):
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
             "warmup": a.warmup, "ms_per_step": total_ms / a.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}",
+            "config": {"workload": WORKLOADS[a.scene], "parallelism": f"replicas x{world}",
                        "l2": "flushed between steps (256 MB write, outside the timed events)",
                        "timing": "CUDA events around a CUDA-graph replay of one step"},
             "msphere_pixel_per_s": world * H / (total_ms / a.steps * 1e-3) / 1e6,

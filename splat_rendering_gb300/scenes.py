@@ -166,6 +166,22 @@ def headline(seed: int = 2, n: int = 1_000_000) -> Scene:
                  Params(n_track=5, channels=3), _f32(np.zeros(3)), _grads(rng, cams, 3))
 
 
+def headline_ortho(seed: int = 2, n: int = 1_000_000) -> Scene:
+    """The headline scene's sizes seen by an orthographic camera: 1M spheres
+    uniform in the box |x|, |y| <= 7, z in [1, 20], 1024 x 1024 pixels at
+    1024/14 px per unit (so projected radii match the headline's median
+    depth), same radius, opacity and feature distributions."""
+    rng = np.random.default_rng(seed)
+    pos = np.stack([rng.uniform(-7.0, 7.0, n), rng.uniform(-7.0, 7.0, n),
+                    rng.uniform(1.0, 20.0, n)], 1)
+    rad = _log_uniform(rng, 0.001, 0.03, n)
+    opa = rng.uniform(0.05, 1.0, n)
+    feat = rng.uniform(0.0, 1.0, (n, 3))
+    cams = [_camera(np.eye(3), np.zeros(3), 1024 / 14, 1024, 1024, 0.5, 21.0, orthographic=True)]
+    return Scene("headline_ortho", _f32(pos), _f32(rad), _f32(opa), _f32(feat), cams,
+                 Params(n_track=5, channels=3), _f32(np.zeros(3)), _grads(rng, cams, 3))
+
+
 def neural(seed: int = 3, n: int = 1_000_000) -> Scene:
     rng = np.random.default_rng(seed)
     pos = _frustum_volume(rng, n, 1.0, 20.0, 0.5)
@@ -249,6 +265,7 @@ CONFIGS = {
     "tiny": tiny,
     "medium": medium,
     "headline": headline,
+    "headline_ortho": headline_ortho,
     "neural": neural,
     "driving": driving,
 }

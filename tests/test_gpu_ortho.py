@@ -79,3 +79,16 @@ def test_ortho_and_pinhole_share_a_context(oracle_lib):
         _check_lists(g, offs, ids)
         gh.compare_frame(g, o, f"shared context {sc.cameras[0].orthographic}")
     r.close()
+
+
+def test_ortho_headline_full_frame(oracle_lib):
+    """The headline sizes with an orthographic camera (1M spheres, 1024 x 1024,
+    the workload `bench.py --scene headline_ortho` times): decisions, tile
+    lists, image and gradients over the full frame."""
+    sc = scenes.make("headline_ortho")
+    o, d, offs, ids = _oracle_all(oracle_lib, sc)
+    g = gh.run_gpu(sc, max_pairs=len(ids) + 1024)
+    assert g["code"] == 0 and g["n_pairs"] == len(ids) and g["hits"] == o["hits"]
+    gh.assert_decisions_equal(g, d)
+    _check_lists(g, offs, ids)
+    gh.compare_frame(g, o, "headline ortho")
