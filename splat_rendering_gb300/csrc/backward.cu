@@ -47,7 +47,11 @@ template <int CMAX, int TMAX>
 __global__ void __launch_bounds__(kBwdThreads, CMAX <= 4 ? 4 : (CMAX <= 16 ? 2 : 1))
 k_backward(Frame f, Workspace w, const float* __restrict__ features,
            const float* __restrict__ image, const float* __restrict__ grad_image,
-           float* __restrict__ grad_opacity, float* __restrict__ grad_features, int want_geom) {
+           float* __restrict__ grad_opacity, float* __restrict__ grad_features, int mode) {
+    // mode bit 0: geometry gradients wanted; bit 1: feature gradient rows are
+    // 16-byte aligned with C a multiple of 4 (vector reductions)
+    const bool want_geom = (mode & 1) != 0;
+    const bool feat_v4 = (mode & 2) != 0;
     constexpr int NB = BwdBatch<CMAX>::n;
     constexpr int NV = 5 + CMAX;   // dL/dc.xyz, dL/dr, dL/do, dL/df[CMAX]
     __shared__ float4 s_uv[NB];
@@ -224,9 +228,23 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
                 if (want_geom && !cut) red_add_v4(&w.gacc[id], v[0], v[1], v[2], v[3]);
                 if (grad_opacity) atomicAdd(&grad_opacity[id], v[4]);
                 if (grad_features) {
+                    float* gf = grad_features + (size_t)id * C;
+                    bool done_v4 = false;
+                    if constexpr (CMAX % 4 == 0) {
+                        if (feat_v4) {
 #pragma unroll
-                    for (int c = 0; c < CMAX; ++c)
-                        if (c < C) atomicAdd(&grad_features[(size_t)id * C + c], v[5 + c]);
+                            for (int c = 0; c < CMAX; c += 4)
+                                if (c < C)
+                                    red_add_v4(reinterpret_cast<float4*>(gf + c), v[5 + c],
+                                               v[6 + c], v[7 + c], v[8 + c]);
+                            done_v4 = true;
+                        }
+                    }
+                    if (!done_v4) {
+#pragma unroll
+                        for (int c = 0; c < CMAX; ++c)
+                            if (c < C) atomicAdd(&gf[c], v[5 + c]);
+                    }
                 }
             }
         }
@@ -372,21 +390,21 @@ k_camera_reduce(Frame f, Workspace w, int fin_blocks, float* __restrict__ grad_c
 template <int CMAX, int TMAX>
 void launch_bwd_t(const Frame& f, const Workspace& w, const float* features, const float* image,
                   const float* grad_image, float* grad_opacity, float* grad_features,
-                  int want_geom, cudaStream_t stream) {
+                  int mode, cudaStream_t stream) {
     k_backward<CMAX, TMAX><<<f.n_tiles, kBwdThreads, 0, stream>>>(
-        f, w, features, image, grad_image, grad_opacity, grad_features, want_geom);
+        f, w, features, image, grad_image, grad_opacity, grad_features, mode);
 }
 
 template <int CMAX>
 void launch_bwd_c(const Frame& f, const Workspace& w, const float* features, const float* image,
                   const float* grad_image, float* grad_opacity, float* grad_features,
-                  int want_geom, cudaStream_t stream) {
+                  int mode, cudaStream_t stream) {
     if (f.n_track <= 8)
         launch_bwd_t<CMAX, 8>(f, w, features, image, grad_image, grad_opacity, grad_features,
-                              want_geom, stream);
+                              mode, stream);
     else
         launch_bwd_t<CMAX, kMaxTrack>(f, w, features, image, grad_image, grad_opacity,
-                                      grad_features, want_geom, stream);
+                                      grad_features, mode, stream);
 }
 
 }  // namespace
@@ -396,24 +414,27 @@ cudaError_t launch_backward(const Frame& f, const Workspace& w, const float* pos
                             float* grad_pos, float* grad_radius, float* grad_opacity,
                             float* grad_features, float* grad_cam, cudaStream_t stream) {
     const int want_geom = (grad_pos || grad_radius || grad_cam) ? 1 : 0;
+    const int feat_v4 = (f.channels % 4 == 0 && grad_features &&
+                         (reinterpret_cast<uintptr_t>(grad_features) & 15u) == 0) ? 2 : 0;
+    const int mode = want_geom | feat_v4;
     if (f.channels == 3)
         launch_bwd_c<3>(f, w, features, image, grad_image, grad_opacity, grad_features,
-                        want_geom, stream);
+                        mode, stream);
     else if (f.channels <= 4)
         launch_bwd_c<4>(f, w, features, image, grad_image, grad_opacity, grad_features,
-                        want_geom, stream);
+                        mode, stream);
     else if (f.channels <= 8)
         launch_bwd_c<8>(f, w, features, image, grad_image, grad_opacity, grad_features,
-                        want_geom, stream);
+                        mode, stream);
     else if (f.channels <= 16)
         launch_bwd_c<16>(f, w, features, image, grad_image, grad_opacity, grad_features,
-                         want_geom, stream);
+                         mode, stream);
     else if (f.channels <= 32)
         launch_bwd_c<32>(f, w, features, image, grad_image, grad_opacity, grad_features,
-                         want_geom, stream);
+                         mode, stream);
     else
         launch_bwd_c<kMaxChannels>(f, w, features, image, grad_image, grad_opacity,
-                                   grad_features, want_geom, stream);
+                                   grad_features, mode, stream);
     if (want_geom) {
         const int blocks = (f.n + 4 * kFinThreads - 1) / (4 * kFinThreads);
         // 16-byte accesses need 16-byte aligned arrays (true for torch allocations)
