@@ -58,7 +58,8 @@ class _Params(ctypes.Structure):
     _fields_ = [("gamma", ctypes.c_double), ("bg_eps", ctypes.c_double),
                 ("kappa", ctypes.c_double), ("geom_min_area", ctypes.c_double),
                 ("n_track", ctypes.c_int32), ("channels", ctypes.c_int32),
-                ("geom_cutoff", ctypes.c_int32), ("fp64_decisions", ctypes.c_int32)]
+                ("geom_cutoff", ctypes.c_int32), ("fp64_decisions", ctypes.c_int32),
+                ("normalize", ctypes.c_int32)]
 
 
 def _load():
@@ -109,6 +110,7 @@ def _params(p, fp64: bool) -> _Params:
     q.n_track, q.channels = int(p.n_track), int(p.channels)
     q.geom_cutoff = 1 if p.geom_cutoff else 0
     q.fp64_decisions = 1 if fp64 else 0
+    q.normalize = 1 if getattr(p, "normalize_grads", False) else 0
     return q
 
 

@@ -45,6 +45,15 @@
 // z~, weights and tracked set are the pinhole's; the cutoff area is
 // pi (min(fx, fy) r)^2.
 //
+// Normalised gradients (Sec. B.2: sphere gradients averaged over the
+// contributing pixels, camera gradients normalised by the projected sphere
+// area and 1e-3; not a gradient of anything, so PARITY UNPINNED -- only the
+// CUDA path is checked against it): with n_j the number of pixels whose
+// tracked set holds sphere j, its position, radius, opacity and feature
+// gradients are divided by n_j; its share of the R, t and K gradients is
+// multiplied by 1e-3 / A_j, A_j = pi (f_min r_eff / c.z)^2 (orthographic:
+// pi (f_min r_eff)^2), the area in px^2 of the disc it is rendered with.
+//
 // Decisions (cull, pixel rectangle, tile lists, hit set, tracked ids) are
 // taken in fp32 by a fixed sequence of correctly rounded operations (this
 // file is built with -ffp-contract=off), so the GPU can match them bit for
@@ -77,6 +86,7 @@ typedef struct {
     int32_t n_track, channels;
     int32_t geom_cutoff;     // 1: drop position/radius/camera grads of small spheres
     int32_t fp64_decisions;  // 1: all decisions in fp64 instead of the fp32 sequence
+    int32_t normalize;       // 1: normalised gradients (Sec. B.2; see below)
 } oparams_t;
 
 }  // extern "C"
@@ -693,31 +703,40 @@ int64_t oracle_render(const double* pos, const double* radius, const double* opa
                     }
             }
         }
-        for (int k = 0; k < 3; ++k) gc[3 * i + k] = g_c[k];
-        for (int k = 0; k < 4; ++k) gk[4 * i + k] = g_K[k];
-        if (grad_radius) grad_radius[i] = g_r;
-        if (grad_opacity) grad_opacity[i] = g_o;
+        // camera shares (R, t through g_c; K) and sphere gradients
+        double cam_scale = 1.0, sph_scale = 1.0;
+        if (prm.normalize && s.keep) {
+            const double nj = (double)(cnt[i + 1] - cnt[i]);
+            sph_scale = nj > 0 ? 1.0 / nj : 1.0;
+            const double rz = cam.orthographic ? s.reff : s.reff / s.c[2];
+            const double A = M_PI * (fmin * rz) * (fmin * rz);
+            cam_scale = 1e-3 / A;
+        }
+        for (int k = 0; k < 3; ++k) gc[3 * i + k] = g_c[k] * cam_scale;
+        for (int k = 0; k < 4; ++k) gk[4 * i + k] = g_K[k] * cam_scale;
+        if (grad_radius) grad_radius[i] = g_r * sph_scale;
+        if (grad_opacity) grad_opacity[i] = g_o * sph_scale;
         if (grad_features)
-            for (int c = 0; c < C; ++c) grad_features[(size_t)i * C + c] = g_f[c];
+            for (int c = 0; c < C; ++c) grad_features[(size_t)i * C + c] = g_f[c] * sph_scale;
         if (grad_pos)
             for (int l = 0; l < 3; ++l)
                 grad_pos[3 * i + l] =
-                    cam.R[l] * g_c[0] + cam.R[3 + l] * g_c[1] + cam.R[6 + l] * g_c[2];
+                    (cam.R[l] * g_c[0] + cam.R[3 + l] * g_c[1] + cam.R[6 + l] * g_c[2]) * sph_scale;
         if (gabs) {
-            for (int l = 0; l < 3; ++l) gabs[3 * i + l] = a_p[l];
-            gabs[3 * n + i] = a_r;
-            gabs[4 * n + i] = a_o;
-            for (int c = 0; c < C; ++c) gabs[5 * n + (size_t)i * C + c] = a_f[c];
-            for (int k = 0; k < 3; ++k) ac[3 * i + k] = a_c[k];
-            for (int k = 0; k < 4; ++k) ak[4 * i + k] = a_K[k];
-            for (int k = 0; k < 9; ++k) acr[9 * i + k] = a_R[k];
+            for (int l = 0; l < 3; ++l) gabs[3 * i + l] = a_p[l] * sph_scale;
+            gabs[3 * n + i] = a_r * sph_scale;
+            gabs[4 * n + i] = a_o * sph_scale;
+            for (int c = 0; c < C; ++c) gabs[5 * n + (size_t)i * C + c] = a_f[c] * sph_scale;
+            for (int k = 0; k < 3; ++k) ac[3 * i + k] = a_c[k] * cam_scale;
+            for (int k = 0; k < 4; ++k) ak[4 * i + k] = a_K[k] * cam_scale;
+            for (int k = 0; k < 9; ++k) acr[9 * i + k] = a_R[k] * cam_scale;
             double* sens_out = gabs + (5 + C) * n + 16;
-            for (int l = 0; l < 3; ++l) sens_out[3 * i + l] = s_p[l];
-            sens_out[3 * n + i] = s_r;
-            sens_out[4 * n + i] = s_o;
-            for (int k = 0; k < 3; ++k) sc_[3 * i + k] = s_c[k];
-            for (int k = 0; k < 4; ++k) sk[4 * i + k] = s_K[k];
-            for (int k = 0; k < 9; ++k) scr[9 * i + k] = s_R[k];
+            for (int l = 0; l < 3; ++l) sens_out[3 * i + l] = s_p[l] * sph_scale;
+            sens_out[3 * n + i] = s_r * sph_scale;
+            sens_out[4 * n + i] = s_o * sph_scale;
+            for (int k = 0; k < 3; ++k) sc_[3 * i + k] = s_c[k] * cam_scale;
+            for (int k = 0; k < 4; ++k) sk[4 * i + k] = s_K[k] * cam_scale;
+            for (int k = 0; k < 9; ++k) scr[9 * i + k] = s_R[k] * cam_scale;
         }
     }
     if (grad_cam) {

@@ -67,6 +67,7 @@ class Params:
     n_track: int = 5
     channels: int = 3
     geom_cutoff: bool = True
+    normalize_grads: bool = False   # averaged sphere / area-normalised camera gradients
 
 
 @dataclass
