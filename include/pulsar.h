@@ -61,6 +61,13 @@ extern "C" {
 #define PULSAR_FLAG_GEOM_CUTOFF   0x1u
 /* Also record the number of hits of every pixel (for tests; costs 4 B/px). */
 #define PULSAR_FLAG_COUNT_HITS    0x2u
+/* Normalised gradients (Pulsar Sec. B.2): a sphere's position, radius,
+ * opacity and feature gradients are divided by the number of pixels whose
+ * tracked set holds it; its share of the R, t and K gradients is multiplied by
+ * 1e-3 / A, A = pi*(f_min*r_eff/c.z)^2 px^2 (orthographic: pi*(f_min*r_eff)^2),
+ * the area of the disc it is rendered with.  Not the derivative of anything:
+ * an optimisation aid, off by default. */
+#define PULSAR_FLAG_NORMALIZE_GRADS 0x4u
 
 /* Camera, OpenCV axes (x right, y down, z forward).  R is the world->camera
  * rotation, row-major: c = R p + t.  Pixel (x, y) has its centre at

@@ -160,6 +160,14 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
                 if (want_geom && !cut) {
                     const float Z = geo.z, reff = geo.w;
                     const float ireff = 1.0f / reff;
+                    // normalised gradients: the sphere's share of the K gradient
+                    // is scaled by 1e-3 / A, A = pi (f_min r_eff / c.z)^2 px^2
+                    // (orthographic: pi (f_min r_eff)^2)
+                    float ks = 1.0f;
+                    if (f.flags & kParamNormalize) {
+                        const float rz = f.fmin * (f.ortho ? reff : reff / Z);
+                        ks = 1e-3f / (kPi * rz * rz);
+                    }
                     const float sE = sj * o * E;                 // dL/dd
                     // depth factor: dw/dz~ = w o / gamma, dz~/dc.z = -1/(zfar - znear)
                     float gcz = -sj * wt * o * f.inv_gamma * f.inv_zrange;
@@ -171,7 +179,7 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
                         // r_eff = kappa c.z / f_min (orthographic: kappa / f_min)
                         if (!f.ortho) gcz += g_reff * f.kappa / f.fmin;
                         const float gf = -g_reff * f.kappa * (f.ortho ? 1.0f : Z) / (f.fmin * f.fmin);
-                        if (f.fx <= f.fy) gk[0] += gf; else gk[1] += gf;
+                        if (f.fx <= f.fy) gk[0] += ks * gf; else gk[1] += ks * gf;
                     } else {
                         gr = g_reff;
                     }
@@ -190,7 +198,7 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
                         // q = ((px - cx)/fx, (py - cy)/fy, 1).  Orthographic: drho/do =
                         // -e_perp / rho for the origin o = ((px - cx)/fx, (py - cy)/fy, 0)
                         const float sq = f.ortho ? -1.0f : -Z * (1.0f - kq);
-                        const float ga = g_rho * sq * n0, gb = g_rho * sq * n1;
+                        const float ga = ks * g_rho * sq * n0, gb = ks * g_rho * sq * n1;
                         gk[0] -= ga * (f.ortho ? ray.ox : ray.a) * f.ifx;
                         gk[1] -= gb * (f.ortho ? ray.oy : ray.b) * f.ify;
                         gk[2] -= ga * f.ifx;
@@ -225,6 +233,7 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
             }
             if (rank == 0 && valid) {
                 const int id = s_id[j];
+                if (f.flags & kParamNormalize) atomicAdd(&w.hitcnt[id], (float)gsz);
                 if (want_geom && !cut) red_add_v4(&w.gacc[id], v[0], v[1], v[2], v[3]);
                 if (grad_opacity) atomicAdd(&grad_opacity[id], v[4]);
                 if (grad_features) {
@@ -281,10 +290,14 @@ __device__ __forceinline__ void finalize_one(const Frame& f, float4 g, float px,
 }
 
 // Four consecutive spheres per thread with 16-byte loads and stores, so each
-// thread has seven independent loads in flight.
+// thread has seven independent loads in flight.  With normalised gradients
+// (Pulsar Sec. B.2) a sphere's gradients are divided by the number of pixels
+// tracking it and its share of dL/dR, dL/dt is scaled by 1e-3 / A (A its
+// rendered disc's area in px^2, as for dL/dK in the backward).
 __global__ void __launch_bounds__(kFinThreads)
 k_finalize(Frame f, Workspace w, const float* __restrict__ pos, float* __restrict__ grad_pos,
-           float* __restrict__ grad_radius, int vec_ok) {
+           float* __restrict__ grad_radius, float* __restrict__ grad_opacity,
+           float* __restrict__ grad_features, int vec_ok) {
     __shared__ float s_part[kFinThreads / 32][12];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int i0 = 4 * (blockIdx.x * blockDim.x + tid);
@@ -292,7 +305,8 @@ k_finalize(Frame f, Workspace w, const float* __restrict__ pos, float* __restric
 #pragma unroll
     for (int q = 0; q < 12; ++q) acc[q] = 0.0f;
     const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (vec_ok && i0 + 3 < f.n) {
+    const bool norm = (f.flags & kParamNormalize) != 0;
+    if (!norm && vec_ok && i0 + 3 < f.n) {
         float4 g[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) g[k] = w.gacc[i0 + k];
@@ -314,17 +328,32 @@ k_finalize(Frame f, Workspace w, const float* __restrict__ pos, float* __restric
         if (grad_radius)
             *reinterpret_cast<float4*>(grad_radius + i0) = make_float4(g[0].w, g[1].w, g[2].w, g[3].w);
     } else {
-        for (int i = i0; i < min(i0 + 4, f.n); ++i) {   // ragged tail or unaligned arrays
-            const float4 g = w.gacc[i];
+        // ragged tail, unaligned arrays or normalised gradients
+        for (int i = i0; i < min(i0 + 4, f.n); ++i) {
+            float4 g = w.gacc[i];
             w.gacc[i] = z4;
-            float gp[3];
-            finalize_one(f, g, pos[3 * i], pos[3 * i + 1], pos[3 * i + 2], gp, acc);
-            if (grad_pos) {
-                grad_pos[3 * i] = gp[0];
-                grad_pos[3 * i + 1] = gp[1];
-                grad_pos[3 * i + 2] = gp[2];
+            float sph = 1.0f, cams = 1.0f;
+            if (norm) {
+                const float cnt = w.hitcnt[i];
+                w.hitcnt[i] = 0.0f;
+                sph = cnt > 0.0f ? 1.0f / cnt : 1.0f;
+                const float4 geo = w.rec[i].geo;          // c.z in z, r_eff in w (0: culled)
+                const float rz = f.fmin * (f.ortho ? geo.w : geo.w / geo.z);
+                cams = rz > 0.0f ? 1e-3f / (kPi * rz * rz) : 0.0f;
+                if (grad_opacity) grad_opacity[i] *= sph;
+                if (grad_features)
+                    for (int c = 0; c < f.channels; ++c) grad_features[(size_t)i * f.channels + c] *= sph;
             }
-            if (grad_radius) grad_radius[i] = g.w;
+            float gp[3];
+            const float4 gc = make_float4(g.x * cams, g.y * cams, g.z * cams, g.w);
+            finalize_one(f, gc, pos[3 * i], pos[3 * i + 1], pos[3 * i + 2], gp, acc);
+            if (grad_pos) {
+                // R^T dL/dc of the unscaled g, averaged
+                grad_pos[3 * i] = (f.R[0] * g.x + f.R[3] * g.y + f.R[6] * g.z) * sph;
+                grad_pos[3 * i + 1] = (f.R[1] * g.x + f.R[4] * g.y + f.R[7] * g.z) * sph;
+                grad_pos[3 * i + 2] = (f.R[2] * g.x + f.R[5] * g.y + f.R[8] * g.z) * sph;
+            }
+            if (grad_radius) grad_radius[i] = g.w * sph;
         }
     }
 #pragma unroll
@@ -435,14 +464,16 @@ cudaError_t launch_backward(const Frame& f, const Workspace& w, const float* pos
     else
         launch_bwd_c<kMaxChannels>(f, w, features, image, grad_image, grad_opacity,
                                    grad_features, mode, stream);
-    if (want_geom) {
+    const bool norm = (f.flags & kParamNormalize) != 0;
+    if (want_geom || norm) {
         const int blocks = (f.n + 4 * kFinThreads - 1) / (4 * kFinThreads);
         // 16-byte accesses need 16-byte aligned arrays (true for torch allocations)
         const int vec_ok = ((reinterpret_cast<uintptr_t>(pos) | reinterpret_cast<uintptr_t>(grad_pos) |
                              reinterpret_cast<uintptr_t>(grad_radius)) & 15u) == 0;
         if (blocks > 0)
-            k_finalize<<<blocks, kFinThreads, 0, stream>>>(f, w, pos, grad_pos, grad_radius, vec_ok);
-        k_camera_reduce<<<1, kCamThreads, 0, stream>>>(f, w, blocks, grad_cam);
+            k_finalize<<<blocks, kFinThreads, 0, stream>>>(f, w, pos, grad_pos, grad_radius,
+                                                           grad_opacity, grad_features, vec_ok);
+        if (want_geom) k_camera_reduce<<<1, kCamThreads, 0, stream>>>(f, w, blocks, grad_cam);
     }
     return cudaGetLastError();
 }

@@ -114,6 +114,7 @@ extern "C" int pulsar_render_noalloc(const float* pos, const float* radius, cons
     Workspace w{};
     w.rec = reinterpret_cast<SphereRec*>(a + kOffRec);
     w.gacc = nullptr;   // forward only
+    w.hitcnt = nullptr;
     w.tile_count = reinterpret_cast<uint32_t*>(a + kOffCount);
     w.tile_start = reinterpret_cast<uint32_t*>(a + kOffStart);
     w.staged = reinterpret_cast<uint4*>(a + kOffStaged);

@@ -110,7 +110,7 @@ int pulsar_create(pulsar_ctx_t* out, int device, int64_t max_spheres, int64_t ma
     c->max_pix = (int64_t)max_width * max_height;
     const size_t N = (size_t)(max_spheres > 0 ? max_spheres : 1);
     Workspace& w = c->ws;
-    bool ok = alloc(c, &w.rec, N) && alloc(c, &w.gacc, N) &&
+    bool ok = alloc(c, &w.rec, N) && alloc(c, &w.gacc, N) && alloc(c, &w.hitcnt, N) &&
               alloc(c, &w.tile_count, (size_t)c->max_tiles) &&
               alloc(c, &w.tile_start, (size_t)c->max_tiles + 1) &&
               alloc(c, &w.staged, (size_t)max_pairs) &&
@@ -127,6 +127,7 @@ int pulsar_create(pulsar_ctx_t* out, int device, int64_t max_spheres, int64_t ma
     // zero-between-frames invariants
     if (ok)
         ok = cudaMemset(w.gacc, 0, N * sizeof(float4)) == cudaSuccess &&
+             cudaMemset(w.hitcnt, 0, N * sizeof(float)) == cudaSuccess &&
              cudaMemset(w.tile_count, 0, (size_t)c->max_tiles * sizeof(uint32_t)) == cudaSuccess &&
              cudaMemset(w.tile_start, 0, ((size_t)c->max_tiles + 1) * sizeof(uint32_t)) ==
                  cudaSuccess &&

@@ -16,7 +16,8 @@ constexpr int kTile = 16;           // 16x16 pixel tiles (Pulsar Sec. B.1.2)
 constexpr int kTilePix = kTile * kTile;
 constexpr int kMaxTrack = 16;
 constexpr int kMaxChannels = 64;
-constexpr uint32_t kFlagKeep = 1u, kFlagFloor = 2u, kFlagCut = 4u;
+constexpr uint32_t kFlagKeep = 1u, kFlagFloor = 2u, kFlagCut = 4u;   // per-sphere record flags
+constexpr uint32_t kParamNormalize = 4u;   // Frame::flags bit: normalised gradients
 constexpr float kPi = 3.14159265358979f;
 
 // Device error bits (latched in DevState::error).
@@ -309,6 +310,8 @@ struct __align__(16) SphereRec {
 struct Workspace {
     SphereRec* rec;    // [maxN]
     float4* gacc;      // [maxN] dL/dc.xyz, dL/dr accumulators (zero between frames)
+    float* hitcnt;     // [maxN] pixels tracking each sphere, for normalised gradients
+                       // (zero between frames)
     uint32_t* tile_count;   // [maxB] (zero between frames)
     uint32_t* tile_start;   // [maxB+1]
     uint4* staged;          // [max_pairs] (tile, slot in tile, key bits, id) from the projection
