@@ -111,6 +111,16 @@ int pulsar_create(pulsar_ctx_t* out, int device, int64_t max_spheres, int64_t ma
                   int32_t max_width, int32_t max_height, int32_t max_channels,
                   int32_t max_track);
 
+/* As pulsar_create, for batches of up to max_cams cameras (1 .. 8) rendered
+ * together by pulsar_project_cams (every per-camera buffer of the workspace
+ * is allocated max_cams times).  pulsar_create(...) is
+ * pulsar_create_cams(..., 1).  Errors: as pulsar_create, and PULSAR_ERR_ARG
+ * if max_cams is out of range or max_cams * max_spheres or
+ * max_cams * max_width * max_height * max_track reaches 2^32. */
+int pulsar_create_cams(pulsar_ctx_t* out, int device, int64_t max_spheres, int64_t max_pairs,
+                       int32_t max_width, int32_t max_height, int32_t max_channels,
+                       int32_t max_track, int32_t max_cams);
+
 /* Release the context and its workspace (synchronises the device). */
 int pulsar_destroy(pulsar_ctx_t ctx);
 
@@ -126,6 +136,22 @@ int pulsar_destroy(pulsar_ctx_t ctx);
 int pulsar_project(pulsar_ctx_t ctx, const float* pos, const float* radius,
                    const float* opacity, int64_t n, const pulsar_camera_t* cam,
                    const pulsar_params_t* params, void* stream);
+
+/* Batched form of pulsar_project: the same spheres seen by n_cams cameras
+ * (1 .. the context's max_cams, equal width and height; host array cams
+ * [n_cams]) in one launch that loads every sphere once.  pulsar_bin,
+ * pulsar_forward and pulsar_backward then cover all cameras in one launch
+ * each: the tiles of all cameras share one list space and the blocks run
+ * over all of them.  Image-shaped arrays (image, grad_image) become
+ * [n_cams,H,W,C], grad_cam becomes [n_cams,16], and the sphere gradients are
+ * summed over the cameras (L = sum over cameras and pixels of <G, F>).
+ * pulsar_project(...) is pulsar_project_cams with one camera.  Errors: as
+ * pulsar_project, and PULSAR_ERR_ARG for n_cams out of range, cameras of
+ * different sizes, or PULSAR_FLAG_NORMALIZE_GRADS with more than one camera
+ * (normalised gradients are defined per image). */
+int pulsar_project_cams(pulsar_ctx_t ctx, const float* pos, const float* radius,
+                        const float* opacity, int64_t n, const pulsar_camera_t* cams,
+                        int32_t n_cams, const pulsar_params_t* params, void* stream);
 
 /* Tile binning (Pulsar Sec. 3.2 "sorted by earliest possible intersection",
  * B.1.1, B.1.2): scan the tile counts, emit one (key, id) pair per covered
@@ -169,6 +195,9 @@ const char* pulsar_strerror(int code);
  * interface).  Copies `bytes` bytes (at most the array's size for the frame)
  * into dst (host or device; cudaMemcpyDefault).  Returns the array's size in
  * bytes for the current frame if dst is NULL, else PULSAR_OK or an error.
+ * For a batch of K cameras every array holds K per-camera blocks, camera
+ * after camera (records [K][n], tiles [K*B], pixels [K*H*W]); the tile lists
+ * of all cameras share one offsets array.
  *   PULSAR_DBG_RECORDS   [n] 64-byte sphere records, 16 x 32-bit words:
  *                        0-3   u_hi, u_lo, v_hi, v_lo  projected centre (float pairs)
  *                        4-6   exponent log2(e) o z~/gamma as hi, lo; opacity o

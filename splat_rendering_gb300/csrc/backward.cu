@@ -16,12 +16,14 @@
 //             opacity and feature gradients go straight to the caller's
 //             (zeroed) arrays.  The intrinsics' gradient is summed per thread
 //             and reduced per block.
-// k_finalize  one thread per sphere: dL/dp = R^T dL/dc and dL/dr out of the
-//             accumulator (which it zeroes for the next frame);
-//             dL/dR = sum dL/dc p^T and dL/dt = sum dL/dc reduced per block
-//             (Pulsar Sec. B.2: sphere-wise camera-gradient accumulation).
-// k_camera_reduce  one block sums all per-block partials in a fixed order
-//             into grad_cam (the device-wide reduction).
+// k_finalize_one_cam, k_finalize_cams  four spheres per thread: dL/dp =
+//             R^T dL/dc and dL/dr out of the accumulator (which it zeroes for
+//             the next frame), summed over the cameras of a batch;
+//             dL/dR = sum dL/dc p^T and dL/dt = sum dL/dc of every camera
+//             reduced per block (Pulsar Sec. B.2: sphere-wise camera-gradient
+//             accumulation).
+// k_camera_reduce  one block per camera sums all its per-block partials in a
+//             fixed order into its grad_cam (the device-wide reduction).
 #include "pulsar_internal.cuh"
 
 namespace pulsar {
@@ -43,9 +45,9 @@ struct BwdBatch {
     static constexpr int n = CMAX <= 4 ? 512 : (CMAX <= 16 ? 256 : (CMAX <= 32 ? 192 : 128));
 };
 
-template <int CMAX, int TMAX>
+template <int CMAX, bool MULTI>
 __global__ void __launch_bounds__(kBwdThreads, CMAX <= 4 ? 4 : (CMAX <= 16 ? 2 : 1))
-k_backward(Frame f, Workspace w, const float* __restrict__ features,
+k_backward(Frames fs, Workspace w, const float* __restrict__ features,
            const float* __restrict__ image, const float* __restrict__ grad_image,
            float* __restrict__ grad_opacity, float* __restrict__ grad_features, int mode) {
     // mode bit 0: geometry gradients wanted; bit 1: feature gradient rows are
@@ -60,18 +62,26 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
     __shared__ int s_id[NB];
     __shared__ float s_feat[NB * CMAX];
     __shared__ float s_k[kBwdThreads / 32][4];
+    // the block's camera and its tile in that camera's image (a single camera
+    // is indexed statically, so its constants stay instruction operands)
+    const int tile_g = blockIdx.x;
+    const int cam = MULTI ? tile_g / fs.f[0].n_tiles : 0;
+    const Frame& f = fs.f[MULTI ? cam : 0];
+    const int tile = tile_g - cam * f.n_tiles;
     if (w.state->n_pairs > f.max_pairs) return;   // overflowed frame: no valid buffer
     const int C = f.channels;
-    const int tile = blockIdx.x;
     const int tyi = tile / f.tiles_x, txi = tile - tyi * f.tiles_x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // warp w covers rows 2w, 2w+1 of the tile with the two rows of a column in
     // adjacent lanes, so a small sphere's footprint is one run of lanes
     const int x = txi * kTile + (lane >> 1), y = tyi * kTile + 2 * warp + (lane & 1);
     const bool inside = x < f.width && y < f.height;
-    const int P = f.width * f.height;
-    const int p = inside ? y * f.width + x : 0;
-    uint32_t start = w.tile_start[tile], end = w.tile_start[tile + 1];
+    // the pixel in the batch's buffers; planes of ids / d are pix_all apart
+    const uint32_t P = f.pix_all;
+    const uint32_t p = f.pix_base + (uint32_t)(inside ? y * f.width + x : 0);
+    uint32_t start = w.tile_start[tile_g], end = w.tile_start[tile_g + 1];
+    const SphereRec* __restrict__ rec = w.rec + f.rec_base;   // this camera's records
+    float4* __restrict__ gacc = w.gacc + f.rec_base;
     end = min(end, f.max_pairs);
     start = min(start, end);
     // a batch's records and features are copied by cp.async; the first batch
@@ -79,7 +89,7 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
     auto stage = [&](uint32_t b0, int nb) {
         for (int t = tid; t < nb; t += kBwdThreads) {
             const int id = (int)w.tile_ids[b0 + t];
-            const float4* src = reinterpret_cast<const float4*>(w.rec + id);
+            const float4* src = reinterpret_cast<const float4*>(rec + id);
             cp_async16(&s_uv[t], src + 0);
             cp_async16(&s_ex[t], src + 1);
             cp_async16(&s_geo[t], src + 2);
@@ -125,8 +135,8 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
             const float d = d_next;
             if (__ballot_sync(0xffffffffu, pos >= 0) == 0u) break;   // -1 padded at the end
             if (k + 1 < f.n_track && inside) {
-                pos_next = w.ids[(size_t)(k + 1) * P + p];
-                d_next = w.dtr[(size_t)(k + 1) * P + p];
+                pos_next = w.ids[(uint32_t)(k + 1) * P + p];
+                d_next = w.dtr[(uint32_t)(k + 1) * P + p];
             }
             const int j = pos - base;
             const bool valid = pos >= 0 && j >= 0 && j < nb;
@@ -233,8 +243,8 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
             }
             if (rank == 0 && valid) {
                 const int id = s_id[j];
-                if (f.flags & kParamNormalize) atomicAdd(&w.hitcnt[id], (float)gsz);
-                if (want_geom && !cut) red_add_v4(&w.gacc[id], v[0], v[1], v[2], v[3]);
+                if (f.flags & kParamNormalize) atomicAdd(&w.hitcnt[f.rec_base + id], (float)gsz);
+                if (want_geom && !cut) red_add_v4(&gacc[id], v[0], v[1], v[2], v[3]);
                 if (grad_opacity) atomicAdd(&grad_opacity[id], v[4]);
                 if (grad_features) {
                     float* gf = grad_features + (size_t)id * C;
@@ -273,7 +283,7 @@ k_backward(Frame f, Workspace w, const float* __restrict__ features,
         // pipe is far too slow even for reductions
         FPair s = {0.0f, 0.0f};
         for (int q = 0; q < kBwdThreads / 32; ++q) s = pp_add(s, FPair{s_k[q][tid], 0.0f});
-        w.kpart[4 * tile + tid] = make_float2(s.hi, s.lo);
+        w.kpart[4 * tile_g + tid] = make_float2(s.hi, s.lo);
     }
 }
 
@@ -289,16 +299,17 @@ __device__ __forceinline__ void finalize_one(const Frame& f, float4 g, float px,
     acc[9] += g.x; acc[10] += g.y; acc[11] += g.z;
 }
 
-// Four consecutive spheres per thread with 16-byte loads and stores, so each
-// thread has seven independent loads in flight.  With normalised gradients
+// One camera: four consecutive spheres per thread with 16-byte loads and
+// stores, so each thread has seven independent loads in flight.  With normalised gradients
 // (Pulsar Sec. B.2) a sphere's gradients are divided by the number of pixels
 // tracking it and its share of dL/dR, dL/dt is scaled by 1e-3 / A (A its
 // rendered disc's area in px^2, as for dL/dK in the backward).
 __global__ void __launch_bounds__(kFinThreads)
-k_finalize(Frame f, Workspace w, const float* __restrict__ pos, float* __restrict__ grad_pos,
+k_finalize_one_cam(Frames fs, Workspace w, const float* __restrict__ pos, float* __restrict__ grad_pos,
            float* __restrict__ grad_radius, float* __restrict__ grad_opacity,
            float* __restrict__ grad_features, int vec_ok) {
     __shared__ float s_part[kFinThreads / 32][12];
+    const Frame& f = fs.f[0];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int i0 = 4 * (blockIdx.x * blockDim.x + tid);
     float acc[12];
@@ -371,13 +382,138 @@ k_finalize(Frame f, Workspace w, const float* __restrict__ pos, float* __restric
     }
 }
 
-// One block: dL/dR and dL/dt from the finalize blocks' partials and
-// dL/d(fx, fy, cx, cy) from the backward tiles' partials, summed in a fixed
-// order in float-pair arithmetic (deterministic, ~1e-14 relative; Pulsar
-// Sec. B.2's device-wide camera reduction).
+// A batch of cameras: four consecutive spheres per thread with 16-byte
+// loads and stores.  For every camera of the batch: dL/dp += R^T dL/dc, dL/dr += its part, and the sphere's share of
+// that camera's dL/dR = sum dL/dc p^T, dL/dt = sum dL/dc goes into per-block
+// partials.  With normalised gradients (Pulsar Sec. B.2; one camera) a
+// sphere's gradients are divided by the number of pixels tracking it and its
+// share of dL/dR, dL/dt is scaled by 1e-3 / A (A its rendered disc's area in
+// px^2, as for dL/dK in the backward).
+__global__ void __launch_bounds__(kFinThreads, 4)
+k_finalize_cams(Frames fs, Workspace w, const float* __restrict__ pos, float* __restrict__ grad_pos,
+           float* __restrict__ grad_radius, float* __restrict__ grad_opacity,
+           float* __restrict__ grad_features, int vec_ok) {
+    __shared__ float s_part[kFinThreads / 32][12];
+    const Frame& f0 = fs.f[0];
+    const int n = f0.n, n_cams = f0.n_cams;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int i0 = 4 * (blockIdx.x * blockDim.x + tid);
+    const int cnt = i0 < n ? min(4, n - i0) : 0;
+    const bool norm = (f0.flags & kParamNormalize) != 0;
+    const bool vec = vec_ok && cnt == 4;
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    float p[12];
+    if (vec) {
+        const float4* p4 = reinterpret_cast<const float4*>(pos + 3 * i0);
+        const float4 pa = p4[0], pb = p4[1], pc = p4[2];
+        p[0] = pa.x; p[1] = pa.y; p[2] = pa.z; p[3] = pa.w;
+        p[4] = pb.x; p[5] = pb.y; p[6] = pb.z; p[7] = pb.w;
+        p[8] = pc.x; p[9] = pc.y; p[10] = pc.z; p[11] = pc.w;
+    } else {
+#pragma unroll
+        for (int q = 0; q < 12; ++q) p[q] = q < 3 * cnt ? pos[3 * i0 + q] : 0.0f;
+    }
+    for (int cam = 0; cam < n_cams; ++cam) {
+        const Frame& f = fs.f[cam];
+        float4 g[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) g[k] = k < cnt ? w.gacc[f.rec_base + i0 + k] : z4;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (k < cnt) w.gacc[f.rec_base + i0 + k] = z4;
+        float acc[12], gp[12], gr[4];
+#pragma unroll
+        for (int q = 0; q < 12; ++q) acc[q] = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float sph = 1.0f, cams = 1.0f;
+            if (norm && k < cnt) {
+                const int i = i0 + k;
+                const float c = w.hitcnt[f.rec_base + i];
+                w.hitcnt[f.rec_base + i] = 0.0f;
+                sph = c > 0.0f ? 1.0f / c : 1.0f;
+                const float4 geo = w.rec[f.rec_base + i].geo;   // c.z in z, r_eff in w (0: culled)
+                const float rz = f.fmin * (f.ortho ? geo.w : geo.w / geo.z);
+                cams = rz > 0.0f ? 1e-3f / (kPi * rz * rz) : 0.0f;
+                if (grad_opacity) grad_opacity[i] *= sph;
+                if (grad_features)
+                    for (int ch = 0; ch < f.channels; ++ch)
+                        grad_features[(size_t)i * f.channels + ch] *= sph;
+            }
+            const float4 gk = g[k];
+            gp[3 * k + 0] = (f.R[0] * gk.x + f.R[3] * gk.y + f.R[6] * gk.z) * sph;
+            gp[3 * k + 1] = (f.R[1] * gk.x + f.R[4] * gk.y + f.R[7] * gk.z) * sph;
+            gp[3 * k + 2] = (f.R[2] * gk.x + f.R[5] * gk.y + f.R[8] * gk.z) * sph;
+            gr[k] = gk.w * sph;
+            const float cx = gk.x * cams, cy = gk.y * cams, cz = gk.z * cams;
+            const float px = p[3 * k], py = p[3 * k + 1], pz = p[3 * k + 2];
+            acc[0] += cx * px; acc[1] += cx * py; acc[2] += cx * pz;
+            acc[3] += cy * px; acc[4] += cy * py; acc[5] += cy * pz;
+            acc[6] += cz * px; acc[7] += cz * py; acc[8] += cz * pz;
+            acc[9] += cx; acc[10] += cy; acc[11] += cz;
+        }
+        // dL/dp and dL/dr: the first camera writes, the others add
+        if (vec) {
+            if (grad_pos) {
+                float4* o4 = reinterpret_cast<float4*>(grad_pos + 3 * i0);
+                if (cam > 0) {
+                    const float4 a = o4[0], b = o4[1], c = o4[2];
+                    gp[0] += a.x; gp[1] += a.y; gp[2] += a.z; gp[3] += a.w;
+                    gp[4] += b.x; gp[5] += b.y; gp[6] += b.z; gp[7] += b.w;
+                    gp[8] += c.x; gp[9] += c.y; gp[10] += c.z; gp[11] += c.w;
+                }
+                o4[0] = make_float4(gp[0], gp[1], gp[2], gp[3]);
+                o4[1] = make_float4(gp[4], gp[5], gp[6], gp[7]);
+                o4[2] = make_float4(gp[8], gp[9], gp[10], gp[11]);
+            }
+            if (grad_radius) {
+                float4* r4 = reinterpret_cast<float4*>(grad_radius + i0);
+                float4 v = make_float4(gr[0], gr[1], gr[2], gr[3]);
+                if (cam > 0) {
+                    const float4 a = *r4;
+                    v.x += a.x; v.y += a.y; v.z += a.z; v.w += a.w;
+                }
+                *r4 = v;
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if (k < cnt) {
+                    const int i = i0 + k;
+                    if (grad_pos)
+                        for (int l = 0; l < 3; ++l)
+                            grad_pos[3 * i + l] = gp[3 * k + l] + (cam > 0 ? grad_pos[3 * i + l] : 0.0f);
+                    if (grad_radius) grad_radius[i] = gr[k] + (cam > 0 ? grad_radius[i] : 0.0f);
+                }
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 12; ++q) {
+            float s = acc[q];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
+            if (lane == 0) s_part[warp][q] = s;
+        }
+        __syncthreads();
+        if (tid < 12) {
+            FPair s = {0.0f, 0.0f};
+            for (int q = 0; q < kFinThreads / 32; ++q) s = pp_add(s, FPair{s_part[q][tid], 0.0f});
+            w.rtpart[(blockIdx.x * n_cams + cam) * 12 + tid] = make_float2(s.hi, s.lo);
+        }
+        __syncthreads();   // s_part is reused by the next camera
+    }
+}
+
+// One block per camera: its dL/dR and dL/dt from the finalize blocks'
+// partials and dL/d(fx, fy, cx, cy) from its tiles' partials, summed in a
+// fixed order in float-pair arithmetic (deterministic, ~1e-14 relative;
+// Pulsar Sec. B.2's device-wide camera reduction).
 __global__ void __launch_bounds__(kCamThreads)
-k_camera_reduce(Frame f, Workspace w, int fin_blocks, float* __restrict__ grad_cam) {
+k_camera_reduce(Frames fs, Workspace w, int fin_blocks, float* __restrict__ grad_cam) {
     __shared__ float2 s_part[kCamThreads / 32][16];
+    const int cam = blockIdx.x;
+    const Frame& f = fs.f[cam];
+    const int n_cams = fs.f[0].n_cams;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     FPair v[16];
 #pragma unroll
@@ -385,13 +521,13 @@ k_camera_reduce(Frame f, Workspace w, int fin_blocks, float* __restrict__ grad_c
     for (int b = tid; b < fin_blocks; b += kCamThreads)
 #pragma unroll
         for (int q = 0; q < 12; ++q) {
-            const float2 t = w.rtpart[12 * b + q];
+            const float2 t = w.rtpart[(b * n_cams + cam) * 12 + q];
             v[q] = pp_add(v[q], FPair{t.x, t.y});
         }
     for (int b = tid; b < f.n_tiles; b += kCamThreads)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const float2 t = w.kpart[4 * b + q];
+            const float2 t = w.kpart[4 * (f.tile_base + b) + q];
             v[12 + q] = pp_add(v[12 + q], FPair{t.x, t.y});
         }
 #pragma unroll
@@ -412,57 +548,50 @@ k_camera_reduce(Frame f, Workspace w, int fin_blocks, float* __restrict__ grad_c
             const float2 t = s_part[q][tid];
             s = pp_add(s, FPair{t.x, t.y});
         }
-        if (grad_cam) grad_cam[tid] = __fadd_rn(s.hi, s.lo);
+        if (grad_cam) grad_cam[16 * cam + tid] = __fadd_rn(s.hi, s.lo);
     }
 }
 
-template <int CMAX, int TMAX>
-void launch_bwd_t(const Frame& f, const Workspace& w, const float* features, const float* image,
-                  const float* grad_image, float* grad_opacity, float* grad_features,
-                  int mode, cudaStream_t stream) {
-    k_backward<CMAX, TMAX><<<f.n_tiles, kBwdThreads, 0, stream>>>(
-        f, w, features, image, grad_image, grad_opacity, grad_features, mode);
-}
-
 template <int CMAX>
-void launch_bwd_c(const Frame& f, const Workspace& w, const float* features, const float* image,
+void launch_bwd_c(const Frames& fs, const Workspace& w, const float* features, const float* image,
                   const float* grad_image, float* grad_opacity, float* grad_features,
                   int mode, cudaStream_t stream) {
-    if (f.n_track <= 8)
-        launch_bwd_t<CMAX, 8>(f, w, features, image, grad_image, grad_opacity, grad_features,
-                              mode, stream);
+    if (fs.f[0].n_cams == 1)
+        k_backward<CMAX, false><<<fs.f[0].n_tiles_all, kBwdThreads, 0, stream>>>(
+            fs, w, features, image, grad_image, grad_opacity, grad_features, mode);
     else
-        launch_bwd_t<CMAX, kMaxTrack>(f, w, features, image, grad_image, grad_opacity,
-                                      grad_features, mode, stream);
+        k_backward<CMAX, true><<<fs.f[0].n_tiles_all, kBwdThreads, 0, stream>>>(
+            fs, w, features, image, grad_image, grad_opacity, grad_features, mode);
 }
 
 }  // namespace
 
-cudaError_t launch_backward(const Frame& f, const Workspace& w, const float* pos,
+cudaError_t launch_backward(const Frames& fs, const Workspace& w, const float* pos,
                             const float* features, const float* image, const float* grad_image,
                             float* grad_pos, float* grad_radius, float* grad_opacity,
                             float* grad_features, float* grad_cam, cudaStream_t stream) {
+    const Frame& f = fs.f[0];
     const int want_geom = (grad_pos || grad_radius || grad_cam) ? 1 : 0;
     const int feat_v4 = (f.channels % 4 == 0 && grad_features &&
                          (reinterpret_cast<uintptr_t>(grad_features) & 15u) == 0) ? 2 : 0;
     const int mode = want_geom | feat_v4;
     if (f.channels == 3)
-        launch_bwd_c<3>(f, w, features, image, grad_image, grad_opacity, grad_features,
+        launch_bwd_c<3>(fs, w, features, image, grad_image, grad_opacity, grad_features,
                         mode, stream);
     else if (f.channels <= 4)
-        launch_bwd_c<4>(f, w, features, image, grad_image, grad_opacity, grad_features,
+        launch_bwd_c<4>(fs, w, features, image, grad_image, grad_opacity, grad_features,
                         mode, stream);
     else if (f.channels <= 8)
-        launch_bwd_c<8>(f, w, features, image, grad_image, grad_opacity, grad_features,
+        launch_bwd_c<8>(fs, w, features, image, grad_image, grad_opacity, grad_features,
                         mode, stream);
     else if (f.channels <= 16)
-        launch_bwd_c<16>(f, w, features, image, grad_image, grad_opacity, grad_features,
+        launch_bwd_c<16>(fs, w, features, image, grad_image, grad_opacity, grad_features,
                          mode, stream);
     else if (f.channels <= 32)
-        launch_bwd_c<32>(f, w, features, image, grad_image, grad_opacity, grad_features,
+        launch_bwd_c<32>(fs, w, features, image, grad_image, grad_opacity, grad_features,
                          mode, stream);
     else
-        launch_bwd_c<kMaxChannels>(f, w, features, image, grad_image, grad_opacity,
+        launch_bwd_c<kMaxChannels>(fs, w, features, image, grad_image, grad_opacity,
                                    grad_features, mode, stream);
     const bool norm = (f.flags & kParamNormalize) != 0;
     if (want_geom || norm) {
@@ -470,10 +599,14 @@ cudaError_t launch_backward(const Frame& f, const Workspace& w, const float* pos
         // 16-byte accesses need 16-byte aligned arrays (true for torch allocations)
         const int vec_ok = ((reinterpret_cast<uintptr_t>(pos) | reinterpret_cast<uintptr_t>(grad_pos) |
                              reinterpret_cast<uintptr_t>(grad_radius)) & 15u) == 0;
-        if (blocks > 0)
-            k_finalize<<<blocks, kFinThreads, 0, stream>>>(f, w, pos, grad_pos, grad_radius,
-                                                           grad_opacity, grad_features, vec_ok);
-        if (want_geom) k_camera_reduce<<<1, kCamThreads, 0, stream>>>(f, w, blocks, grad_cam);
+        if (blocks > 0 && f.n_cams == 1)
+            k_finalize_one_cam<<<blocks, kFinThreads, 0, stream>>>(
+                fs, w, pos, grad_pos, grad_radius, grad_opacity, grad_features, vec_ok);
+        else if (blocks > 0)
+            k_finalize_cams<<<blocks, kFinThreads, 0, stream>>>(
+                fs, w, pos, grad_pos, grad_radius, grad_opacity, grad_features, vec_ok);
+        if (want_geom)
+            k_camera_reduce<<<f.n_cams, kCamThreads, 0, stream>>>(fs, w, blocks, grad_cam);
     }
     return cudaGetLastError();
 }

@@ -28,12 +28,14 @@ constexpr int kTilesPerSortBlock = kSortThreads / 32;
 constexpr int kSortCap = 2048;
 constexpr int kWarpSortMax = 512;   // lists sorted by one warp in registers
 
-__global__ void __launch_bounds__(kScanThreads) k_tile_scan(Frame f, Workspace w) {
+__global__ void __launch_bounds__(kScanThreads) k_tile_scan(Frames fs, Workspace w) {
     __shared__ uint32_t s_warp[kScanThreads / 32];
+    const Frame& f = fs.f[0];
+    const int n_tiles = (int)f.n_tiles_all;   // every camera's tiles, camera after camera
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int per = (f.n_tiles + kScanThreads - 1) / kScanThreads;
+    const int per = (n_tiles + kScanThreads - 1) / kScanThreads;
     const int b0 = tid * per;
-    const int b1 = min(b0 + per, f.n_tiles);
+    const int b1 = min(b0 + per, n_tiles);
     uint32_t local = 0;
     for (int b = b0; b < b1; ++b) local += w.tile_count[b];
     uint32_t incl = local;
@@ -62,7 +64,7 @@ __global__ void __launch_bounds__(kScanThreads) k_tile_scan(Frame f, Workspace w
         w.tile_count[b] = 0u;
     }
     if (tid == kScanThreads - 1) {
-        w.tile_start[f.n_tiles] = run;
+        w.tile_start[n_tiles] = run;
         w.state->n_pairs = run;
         w.state->hits = 0ull;
         w.state->pair_cursor = 0u;
@@ -70,7 +72,8 @@ __global__ void __launch_bounds__(kScanThreads) k_tile_scan(Frame f, Workspace w
     }
 }
 
-__global__ void __launch_bounds__(kEmitThreads) k_emit(Frame f, Workspace w) {
+__global__ void __launch_bounds__(kEmitThreads) k_emit(Frames fs, Workspace w) {
+    const Frame& f = fs.f[0];
     const uint32_t m = w.state->n_pairs;
     if (m > f.max_pairs) return;   // overflowed frame: the capacity error is latched
     for (uint32_t p = blockIdx.x * blockDim.x + threadIdx.x; p < m; p += gridDim.x * blockDim.x) {
@@ -285,14 +288,16 @@ __device__ void block_sort_long(const Workspace& w, uint32_t start, int n, unsig
 // Block b covers tiles 4b .. 4b+3: first each warp sorts its own tile if the
 // list has at most kWarpSortMax entries, then the block sorts the longer ones
 // together.
-__global__ void __launch_bounds__(kSortThreads) k_tile_sort(Frame f, Workspace w) {
+__global__ void __launch_bounds__(kSortThreads) k_tile_sort(Frames fs, Workspace w) {
+    const Frame& f = fs.f[0];
+    const int n_tiles = (int)f.n_tiles_all;
     __shared__ unsigned long long s[kSortCap];                        // 16 KB
     __shared__ uint32_t s_keys[kTilesPerSortBlock][kWarpSortMax];      // 8 KB
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile0 = blockIdx.x * kTilesPerSortBlock;
     {
         const int tile = tile0 + warp;
-        if (tile < f.n_tiles) {
+        if (tile < n_tiles) {
             const uint32_t start = w.tile_start[tile], end = w.tile_start[tile + 1];
             // (a frame over capacity has its error latched; its lists are not sorted)
             if (end <= f.max_pairs && end > start && end - start <= (uint32_t)kWarpSortMax) {
@@ -309,7 +314,7 @@ __global__ void __launch_bounds__(kSortThreads) k_tile_sort(Frame f, Workspace w
     }
     for (int q = 0; q < kTilesPerSortBlock; ++q) {
         const int tile = tile0 + q;
-        if (tile >= f.n_tiles) break;
+        if (tile >= n_tiles) break;
         const uint32_t start = w.tile_start[tile], end = w.tile_start[tile + 1];
         if (end > f.max_pairs || end <= start || end - start <= (uint32_t)kWarpSortMax) continue;
         __syncthreads();   // the shared buffer is free
@@ -319,12 +324,13 @@ __global__ void __launch_bounds__(kSortThreads) k_tile_sort(Frame f, Workspace w
 
 }  // namespace
 
-cudaError_t launch_bin(const Frame& f, const Workspace& w, cudaStream_t stream) {
-    k_tile_scan<<<1, kScanThreads, 0, stream>>>(f, w);
+cudaError_t launch_bin(const Frames& fs, const Workspace& w, cudaStream_t stream) {
+    const Frame& f = fs.f[0];
+    k_tile_scan<<<1, kScanThreads, 0, stream>>>(fs, w);
     if (f.n > 0) {
-        k_emit<<<152 * 8, kEmitThreads, 0, stream>>>(f, w);
-        k_tile_sort<<<(f.n_tiles + kTilesPerSortBlock - 1) / kTilesPerSortBlock, kSortThreads, 0,
-                      stream>>>(f, w);
+        k_emit<<<152 * 8, kEmitThreads, 0, stream>>>(fs, w);
+        k_tile_sort<<<((int)f.n_tiles_all + kTilesPerSortBlock - 1) / kTilesPerSortBlock,
+                      kSortThreads, 0, stream>>>(fs, w);
     }
     return cudaGetLastError();
 }

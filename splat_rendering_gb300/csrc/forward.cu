@@ -64,9 +64,9 @@ struct FwdSmem {
     static constexpr int bytes = misc + 16;
 };
 
-template <int CMAX>
+template <int CMAX, bool MULTI>
 __global__ void __launch_bounds__(kFwdThreads, CMAX <= 4 ? 4 : (CMAX <= 16 ? 2 : 1))
-k_forward(Frame f, Workspace w, const float* __restrict__ features, const float* __restrict__ bg,
+k_forward(Frames fs, Workspace w, const float* __restrict__ features, const float* __restrict__ bg,
           float* __restrict__ image) {
     using L = FwdSmem<CMAX>;
     constexpr int NB = L::NB;
@@ -84,11 +84,16 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
     float* s_b = reinterpret_cast<float*>(smem + L::b);
     unsigned long long* s_hits = reinterpret_cast<unsigned long long*>(smem + L::misc);
 
+    // the block's camera and its tile in that camera's image (a single camera
+    // is indexed statically, so its constants stay instruction operands)
+    const int tile_g = blockIdx.x;
+    const int cam = MULTI ? tile_g / fs.f[0].n_tiles : 0;
+    const Frame& f = fs.f[MULTI ? cam : 0];
+    const int tile = tile_g - cam * f.n_tiles;
     // a frame whose pairs overflowed max_pairs has unsorted lists: render nothing
     // (the capacity error is latched and reported by pulsar_status)
     if (w.state->n_pairs > f.max_pairs) return;
     const int C = f.channels;
-    const int tile = blockIdx.x;
     const int tyi = tile / f.tiles_x, txi = tile - tyi * f.tiles_x;
     const int tx0 = txi * kTile, ty0 = tyi * kTile;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -123,7 +128,8 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
     }
     if (tid == 0) *s_hits = 0ull;
 
-    uint32_t start = w.tile_start[tile], end = w.tile_start[tile + 1];
+    uint32_t start = w.tile_start[tile_g], end = w.tile_start[tile_g + 1];
+    const SphereRec* __restrict__ rec = w.rec + f.rec_base;   // this camera's records
     end = min(end, f.max_pairs);
     start = min(start, end);
 
@@ -131,7 +137,7 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
     // 16-byte pieces and the features by cp.async, the id by a plain store
     auto stage = [&](int buf, int id) {
         unsigned char* B = smem + buf * L::buf_bytes;
-        const float4* src = reinterpret_cast<const float4*>(w.rec + id);
+        const float4* src = reinterpret_cast<const float4*>(rec + id);
         cp_async16(B + L::rec_uv + tid * 16, src + 0);
         cp_async16(B + L::rec_ex + tid * 16, src + 1);
         cp_async16(B + L::rec_geo + tid * 16, src + 2);
@@ -154,8 +160,9 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
     float acc[CMAX];
 #pragma unroll
     for (int c = 0; c < CMAX; ++c) acc[c] = c < C ? bg[c] : 0.0f;
-    const int P = f.width * f.height;
-    const int p = inside ? y * f.width + x : 0;
+    // the pixel in the batch's buffers; planes of ids / d are pix_all apart
+    const uint32_t P = f.pix_all;
+    const uint32_t p = f.pix_base + (uint32_t)(inside ? y * f.width + x : 0);
     int nh = 0;
     bool done = !inside;
     const int lx = lane & 15, ly = lane >> 4;     // the lane's pixel within the warp's rows
@@ -312,8 +319,8 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
                     if (nh < f.n_track) {
                         // backward-information buffer: the hit's position in the tile
                         // list and its distance factor
-                        w.ids[(size_t)nh * P + p] = (int)(b0 - start) + j;
-                        w.dtr[(size_t)nh * P + p] = d;
+                        w.ids[(uint32_t)nh * P + p] = (int)(b0 - start) + j;
+                        w.dtr[(uint32_t)nh * P + p] = d;
                     }
                     ++nh;
                 }
@@ -341,7 +348,7 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
         // store the stabiliser's high part; fold its low part into the normaliser
         w.mg[p] = mg;
         w.wsum[p] = wsum * ex2_approx(mgl);
-        for (int k = nh; k < f.n_track; ++k) w.ids[(size_t)k * P + p] = -1;
+        for (int k = nh; k < f.n_track; ++k) w.ids[(uint32_t)k * P + p] = -1;
         if (f.flags & 2u) w.nhits[p] = nh;
     }
     // hit count of the frame
@@ -355,17 +362,27 @@ k_forward(Frame f, Workspace w, const float* __restrict__ features, const float*
 }
 
 template <int CMAX>
-cudaError_t launch_c(const Frame& f, const Workspace& w, const float* features, const float* bg,
+cudaError_t launch_c(const Frames& fs, const Workspace& w, const float* features, const float* bg,
                      float* image, cudaStream_t stream) {
     constexpr int bytes = FwdSmem<CMAX>::bytes;
-    k_forward<CMAX><<<f.n_tiles, kFwdThreads, bytes, stream>>>(f, w, features, bg, image);
+    if (fs.f[0].n_cams == 1)
+        k_forward<CMAX, false><<<fs.f[0].n_tiles_all, kFwdThreads, bytes, stream>>>(
+            fs, w, features, bg, image);
+    else
+        k_forward<CMAX, true><<<fs.f[0].n_tiles_all, kFwdThreads, bytes, stream>>>(
+            fs, w, features, bg, image);
     return cudaGetLastError();
 }
 
 template <int CMAX>
 cudaError_t prepare_c() {
-    return cudaFuncSetAttribute(k_forward<CMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                FwdSmem<CMAX>::bytes);
+    cudaError_t e = cudaFuncSetAttribute(k_forward<CMAX, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         FwdSmem<CMAX>::bytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_forward<CMAX, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 FwdSmem<CMAX>::bytes);
+    return e;
 }
 
 }  // namespace
@@ -380,15 +397,15 @@ cudaError_t prepare_forward() {
     return e;
 }
 
-cudaError_t launch_forward(const Frame& f, const Workspace& w, const float* features,
+cudaError_t launch_forward(const Frames& fs, const Workspace& w, const float* features,
                            const float* bg, float* image, int /*max_pairs_stride*/,
                            cudaStream_t stream) {
-    if (f.channels == 3) return launch_c<3>(f, w, features, bg, image, stream);
-    if (f.channels <= 4) return launch_c<4>(f, w, features, bg, image, stream);
-    if (f.channels <= 8) return launch_c<8>(f, w, features, bg, image, stream);
-    if (f.channels <= 16) return launch_c<16>(f, w, features, bg, image, stream);
-    if (f.channels <= 32) return launch_c<32>(f, w, features, bg, image, stream);
-    return launch_c<kMaxChannels>(f, w, features, bg, image, stream);
+    if (fs.f[0].channels == 3) return launch_c<3>(fs, w, features, bg, image, stream);
+    if (fs.f[0].channels <= 4) return launch_c<4>(fs, w, features, bg, image, stream);
+    if (fs.f[0].channels <= 8) return launch_c<8>(fs, w, features, bg, image, stream);
+    if (fs.f[0].channels <= 16) return launch_c<16>(fs, w, features, bg, image, stream);
+    if (fs.f[0].channels <= 32) return launch_c<32>(fs, w, features, bg, image, stream);
+    return launch_c<kMaxChannels>(fs, w, features, bg, image, stream);
 }
 
 }  // namespace pulsar

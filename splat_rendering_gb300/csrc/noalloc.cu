@@ -131,49 +131,19 @@ extern "C" int pulsar_render_noalloc(const float* pos, const float* radius, cons
     w.state = reinterpret_cast<DevState*>(a + kOffState);
 
     // the per-frame constants, formed exactly as pulsar_project forms them
-    Frame f{};
-    std::memcpy(f.R, cam->R, sizeof(f.R));
-    std::memcpy(f.t, cam->t, sizeof(f.t));
-    f.fx = cam->fx; f.fy = cam->fy; f.cx = cam->cx; f.cy = cam->cy;
-    f.znear = cam->znear; f.zfar = cam->zfar;
-    f.ifx = 1.0f / cam->fx;
-    f.ify = 1.0f / cam->fy;
-    f.ifx_lo = (float)(1.0 / (double)cam->fx - (double)f.ifx);
-    f.ify_lo = (float)(1.0 / (double)cam->fy - (double)f.ify);
-    f.fmin = cam->fx <= cam->fy ? cam->fx : cam->fy;
-    f.gamma = prm->gamma;
-    f.inv_gamma = 1.0f / prm->gamma;
-    f.bg_eps = prm->bg_eps;
-    f.stop_tau = prm->stop_tau;
-    f.kappa = prm->kappa;
-    f.amin = prm->geom_min_area;
-    f.inv_zrange = 1.0f / (cam->zfar - cam->znear);
-    const double log2e = 1.4426950408889634073599;
-    const double zk = log2e / (((double)cam->zfar - (double)cam->znear) * (double)prm->gamma);
-    f.zk_hi = (float)zk;
-    f.zk_lo = (float)(zk - (double)f.zk_hi);
-    const double eg = log2e * (double)prm->bg_eps / (double)prm->gamma;
-    f.eg_hi = (float)eg;
-    f.eg_lo = (float)(eg - (double)f.eg_hi);
-    f.width = cam->width;
-    f.height = cam->height;
-    f.tiles_x = (cam->width + kTile - 1) / kTile;
-    f.tiles_y = (cam->height + kTile - 1) / kTile;
-    f.n_tiles = f.tiles_x * f.tiles_y;
-    f.n_track = prm->n_track;
-    f.channels = prm->channels;
-    f.n = (int)n;
-    f.flags = prm->flags;
-    f.max_pairs = (uint32_t)kMaxPairs;
-    f.ortho = cam->orthographic;
+    Frames fs{};
+    fill_frame(fs.f[0], cam->R, cam->t, cam->fx, cam->fy, cam->cx, cam->cy, cam->width,
+               cam->height, cam->znear, cam->zfar, cam->orthographic, prm->gamma, prm->bg_eps,
+               prm->stop_tau, prm->kappa, prm->geom_min_area, prm->n_track, prm->channels,
+               prm->flags, (int)n, (uint32_t)kMaxPairs, 0, 1);
 
     // the arena keeps the previous call's contents: clear what must start at zero
     if (cudaMemsetAsync(w.tile_count, 0, 4 * (size_t)kMaxTilesNA, s) != cudaSuccess ||
         cudaMemsetAsync(w.state, 0, sizeof(DevState), s) != cudaSuccess)
         return PULSAR_ERR_CUDA;
-    if (launch_project(f, w, pos, radius, opacity, s) != cudaSuccess ||
-        launch_bin(f, w, s) != cudaSuccess ||
-        launch_forward(f, w, features, bg, image, 0, s) != cudaSuccess)
+    if (launch_project(fs, w, pos, radius, opacity, s) != cudaSuccess ||
+        launch_bin(fs, w, s) != cudaSuccess ||
+        launch_forward(fs, w, features, bg, image, 0, s) != cudaSuccess)
         return PULSAR_ERR_CUDA;
     DevState st;
     if (cudaMemcpyAsync(&st, w.state, sizeof(DevState), cudaMemcpyDeviceToHost, s) != cudaSuccess ||

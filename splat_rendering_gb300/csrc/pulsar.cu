@@ -17,11 +17,12 @@ using namespace pulsar;
 struct pulsar_ctx {
     int device = 0;
     int64_t max_n = 0, max_pairs = 0;
-    int32_t max_w = 0, max_h = 0, max_c = 0, max_t = 0;
-    int64_t max_tiles = 0, max_pix = 0;
+    int32_t max_w = 0, max_h = 0, max_c = 0, max_t = 0, max_cams = 1;
+    int64_t max_tiles = 0, max_pix = 0;   // per camera
     Workspace ws{};
     DevState* host_state = nullptr;   // pinned mirror for pulsar_status
-    Frame frame{};
+    Frames frames{};                   // the cameras of the current frame
+    int n_cams = 0;
     const float* pos = nullptr;        // inputs of the current frame
     int stage = 0;                     // 0 none, 1 projected, 2 binned, 3 forward done
     bool counts_dirty = false;         // tile counts hold a frame that was never binned
@@ -86,12 +87,23 @@ const char* pulsar_strerror(int code) {
 int pulsar_create(pulsar_ctx_t* out, int device, int64_t max_spheres, int64_t max_pairs,
                   int32_t max_width, int32_t max_height, int32_t max_channels,
                   int32_t max_track) {
+    return pulsar_create_cams(out, device, max_spheres, max_pairs, max_width, max_height,
+                              max_channels, max_track, 1);
+}
+
+int pulsar_create_cams(pulsar_ctx_t* out, int device, int64_t max_spheres, int64_t max_pairs,
+                       int32_t max_width, int32_t max_height, int32_t max_channels,
+                       int32_t max_track, int32_t max_cams) {
     if (!out) return PULSAR_ERR_ARG;
     *out = nullptr;
     if (max_spheres < 0 || max_spheres > 0x7fffffffLL || max_pairs < 1 ||
         max_pairs >= 0xffffffffLL || max_width < 1 || max_width > 65535 || max_height < 1 ||
         max_height > 65535 || max_channels < 1 || max_channels > kMaxChannels ||
-        max_track < 1 || max_track > kMaxTrack)
+        max_track < 1 || max_track > kMaxTrack || max_cams < 1 || max_cams > kMaxCams)
+        return PULSAR_ERR_ARG;
+    // every per-camera buffer holds max_cams blocks, and indices into them are 32-bit
+    if ((double)max_cams * (double)max_spheres >= 4294967296.0 ||
+        (double)max_cams * max_width * max_height * max_track >= 4294967296.0)
         return PULSAR_ERR_ARG;
     int ndev = 0;
     if (cudaGetDeviceCount(&ndev) != cudaSuccess) return PULSAR_ERR_CUDA;
@@ -106,31 +118,30 @@ int pulsar_create(pulsar_ctx_t* out, int device, int64_t max_spheres, int64_t ma
     c->max_h = max_height;
     c->max_c = max_channels;
     c->max_t = max_track;
+    c->max_cams = max_cams;
     c->max_tiles = (int64_t)((max_width + kTile - 1) / kTile) * ((max_height + kTile - 1) / kTile);
     c->max_pix = (int64_t)max_width * max_height;
+    const size_t K = (size_t)max_cams;
     const size_t N = (size_t)(max_spheres > 0 ? max_spheres : 1);
+    const size_t B = (size_t)c->max_tiles, P = (size_t)c->max_pix;
     Workspace& w = c->ws;
-    bool ok = alloc(c, &w.rec, N) && alloc(c, &w.gacc, N) && alloc(c, &w.hitcnt, N) &&
-              alloc(c, &w.tile_count, (size_t)c->max_tiles) &&
-              alloc(c, &w.tile_start, (size_t)c->max_tiles + 1) &&
+    bool ok = alloc(c, &w.rec, K * N) && alloc(c, &w.gacc, K * N) && alloc(c, &w.hitcnt, K * N) &&
+              alloc(c, &w.tile_count, K * B) && alloc(c, &w.tile_start, K * B + 1) &&
               alloc(c, &w.staged, (size_t)max_pairs) &&
               alloc(c, &w.pairs, (size_t)max_pairs) && alloc(c, &w.pairs_alt, (size_t)max_pairs) &&
-              alloc(c, &w.tile_ids, (size_t)max_pairs) && alloc(c, &w.mg, (size_t)c->max_pix) &&
-              alloc(c, &w.wsum, (size_t)c->max_pix) &&
-              alloc(c, &w.ids, (size_t)c->max_pix * max_track) &&
-              alloc(c, &w.dtr, (size_t)c->max_pix * max_track) &&
-              alloc(c, &w.nhits, (size_t)c->max_pix) &&
-              alloc(c, &w.kpart, (size_t)c->max_tiles * 4) &&
-              alloc(c, &w.rtpart, (N + 255) / 256 * 12) && alloc(c, &w.state, 1);
+              alloc(c, &w.tile_ids, (size_t)max_pairs) && alloc(c, &w.mg, K * P) &&
+              alloc(c, &w.wsum, K * P) && alloc(c, &w.ids, K * P * max_track) &&
+              alloc(c, &w.dtr, K * P * max_track) && alloc(c, &w.nhits, K * P) &&
+              alloc(c, &w.kpart, K * B * 4) && alloc(c, &w.rtpart, (N + 255) / 256 * K * 12) &&
+              alloc(c, &w.state, 1);
     if (ok) ok = cudaMallocHost(&c->host_state, sizeof(DevState)) == cudaSuccess;
     if (ok) ok = prepare_forward() == cudaSuccess;
     // zero-between-frames invariants
     if (ok)
-        ok = cudaMemset(w.gacc, 0, N * sizeof(float4)) == cudaSuccess &&
-             cudaMemset(w.hitcnt, 0, N * sizeof(float)) == cudaSuccess &&
-             cudaMemset(w.tile_count, 0, (size_t)c->max_tiles * sizeof(uint32_t)) == cudaSuccess &&
-             cudaMemset(w.tile_start, 0, ((size_t)c->max_tiles + 1) * sizeof(uint32_t)) ==
-                 cudaSuccess &&
+        ok = cudaMemset(w.gacc, 0, K * N * sizeof(float4)) == cudaSuccess &&
+             cudaMemset(w.hitcnt, 0, K * N * sizeof(float)) == cudaSuccess &&
+             cudaMemset(w.tile_count, 0, K * B * sizeof(uint32_t)) == cudaSuccess &&
+             cudaMemset(w.tile_start, 0, (K * B + 1) * sizeof(uint32_t)) == cudaSuccess &&
              cudaMemset(w.state, 0, sizeof(DevState)) == cudaSuccess &&
              cudaDeviceSynchronize() == cudaSuccess;
     if (!ok) {
@@ -155,65 +166,52 @@ int pulsar_destroy(pulsar_ctx_t c) {
 int pulsar_project(pulsar_ctx_t c, const float* pos, const float* radius, const float* opacity,
                    int64_t n, const pulsar_camera_t* cam, const pulsar_params_t* prm,
                    void* stream) {
-    if (!c || !cam || !prm || n < 0 || n > c->max_n) return PULSAR_ERR_ARG;
+    return pulsar_project_cams(c, pos, radius, opacity, n, cam, 1, prm, stream);
+}
+
+int pulsar_project_cams(pulsar_ctx_t c, const float* pos, const float* radius,
+                        const float* opacity, int64_t n, const pulsar_camera_t* cams,
+                        int32_t n_cams, const pulsar_params_t* prm, void* stream) {
+    if (!c || !cams || !prm || n < 0 || n > c->max_n || n_cams < 1 || n_cams > c->max_cams)
+        return PULSAR_ERR_ARG;
     if (n > 0 && (!pos || !radius || !opacity)) return PULSAR_ERR_ARG;
-    if (cam->width < 1 || cam->height < 1 || cam->width > c->max_w || cam->height > c->max_h)
-        return PULSAR_ERR_ARG;
-    if (!finite_pos(cam->fx) || !finite_pos(cam->fy) || !(cam->znear > 0.0f) ||
-        !(cam->zfar > cam->znear) || (cam->orthographic != 0 && cam->orthographic != 1))
-        return PULSAR_ERR_ARG;
+    for (int k = 0; k < n_cams; ++k) {
+        const pulsar_camera_t* cam = cams + k;
+        if (cam->width < 1 || cam->height < 1 || cam->width > c->max_w || cam->height > c->max_h ||
+            cam->width != cams[0].width || cam->height != cams[0].height)
+            return PULSAR_ERR_ARG;
+        if (!finite_pos(cam->fx) || !finite_pos(cam->fy) || !(cam->znear > 0.0f) ||
+            !(cam->zfar > cam->znear) || (cam->orthographic != 0 && cam->orthographic != 1))
+            return PULSAR_ERR_ARG;
+    }
     if (!finite_pos(prm->gamma) || !(prm->bg_eps >= 0.0f) || !(prm->stop_tau >= 0.0f) ||
         !(prm->kappa >= 0.0f) || !(prm->geom_min_area >= 0.0f) || prm->n_track < 1 ||
         prm->n_track > c->max_t || prm->channels < 1 || prm->channels > c->max_c)
         return PULSAR_ERR_ARG;
+    // normalised gradients are defined per image: one camera at a time
+    if ((prm->flags & PULSAR_FLAG_NORMALIZE_GRADS) && n_cams > 1) return PULSAR_ERR_ARG;
     DeviceGuard guard(c->device);
     cudaStream_t s = as_stream(stream);
     if (c->counts_dirty) {
         // a previous frame was projected but never binned: its counts and staged
         // pair cursor are stale
-        cudaError_t e = cudaMemsetAsync(c->ws.tile_count, 0, (size_t)c->max_tiles * 4, s);
+        cudaError_t e = cudaMemsetAsync(c->ws.tile_count, 0,
+                                        (size_t)c->max_tiles * c->max_cams * 4, s);
         if (e == cudaSuccess)
             e = cudaMemsetAsync(&c->ws.state->pair_cursor, 0, sizeof(uint32_t), s);
         if (e != cudaSuccess) return PULSAR_ERR_CUDA;
     }
-    Frame& f = c->frame;
-    std::memcpy(f.R, cam->R, sizeof(f.R));
-    std::memcpy(f.t, cam->t, sizeof(f.t));
-    f.fx = cam->fx; f.fy = cam->fy; f.cx = cam->cx; f.cy = cam->cy;
-    f.znear = cam->znear; f.zfar = cam->zfar;
-    f.ifx = 1.0f / cam->fx;
-    f.ify = 1.0f / cam->fy;
-    f.ifx_lo = (float)(1.0 / (double)cam->fx - (double)f.ifx);
-    f.ify_lo = (float)(1.0 / (double)cam->fy - (double)f.ify);
-    f.fmin = cam->fx <= cam->fy ? cam->fx : cam->fy;
-    f.gamma = prm->gamma;
-    f.inv_gamma = 1.0f / prm->gamma;
-    f.bg_eps = prm->bg_eps;
-    f.stop_tau = prm->stop_tau;
-    f.kappa = prm->kappa;
-    f.amin = prm->geom_min_area;
-    f.inv_zrange = 1.0f / (cam->zfar - cam->znear);
-    // exponents are kept in log2 units (exp2 is the cheap hardware exponential)
-    const double log2e = 1.4426950408889634073599;
-    const double zk = log2e / (((double)cam->zfar - (double)cam->znear) * (double)prm->gamma);
-    f.zk_hi = (float)zk;
-    f.zk_lo = (float)(zk - (double)f.zk_hi);
-    const double eg = log2e * (double)prm->bg_eps / (double)prm->gamma;
-    f.eg_hi = (float)eg;
-    f.eg_lo = (float)(eg - (double)f.eg_hi);
-    f.width = cam->width;
-    f.height = cam->height;
-    f.tiles_x = (cam->width + kTile - 1) / kTile;
-    f.tiles_y = (cam->height + kTile - 1) / kTile;
-    f.n_tiles = f.tiles_x * f.tiles_y;
-    f.n_track = prm->n_track;
-    f.channels = prm->channels;
-    f.n = (int)n;
-    f.flags = prm->flags;
-    f.max_pairs = (uint32_t)c->max_pairs;
-    f.ortho = cam->orthographic;
+    for (int k = 0; k < n_cams; ++k) {
+        const pulsar_camera_t* cam = cams + k;
+        fill_frame(c->frames.f[k], cam->R, cam->t, cam->fx, cam->fy, cam->cx, cam->cy,
+                   cam->width, cam->height, cam->znear, cam->zfar, cam->orthographic,
+                   prm->gamma, prm->bg_eps, prm->stop_tau, prm->kappa, prm->geom_min_area,
+                   prm->n_track, prm->channels, prm->flags, (int)n, (uint32_t)c->max_pairs, k,
+                   n_cams);
+    }
+    c->n_cams = n_cams;
     c->pos = pos;
-    cudaError_t e = launch_project(f, c->ws, pos, radius, opacity, s);
+    cudaError_t e = launch_project(c->frames, c->ws, pos, radius, opacity, s);
     if (e != cudaSuccess) return PULSAR_ERR_CUDA;
     c->stage = 1;
     c->counts_dirty = true;
@@ -225,7 +223,7 @@ int pulsar_bin(pulsar_ctx_t c, void* stream) {
     if (c->stage < 1) return PULSAR_ERR_STATE;
     if (c->stage >= 2) return PULSAR_ERR_STATE;   // counts were consumed by the first bin
     DeviceGuard guard(c->device);
-    cudaError_t e = launch_bin(c->frame, c->ws, as_stream(stream));
+    cudaError_t e = launch_bin(c->frames, c->ws, as_stream(stream));
     if (e != cudaSuccess) return PULSAR_ERR_CUDA;
     c->stage = 2;
     c->counts_dirty = false;
@@ -235,10 +233,10 @@ int pulsar_bin(pulsar_ctx_t c, void* stream) {
 int pulsar_forward(pulsar_ctx_t c, const float* features, const float* bg, float* image,
                    void* stream) {
     if (!c || !bg || !image) return PULSAR_ERR_ARG;
-    if (c->frame.n > 0 && !features) return PULSAR_ERR_ARG;
+    if (c->frames.f[0].n > 0 && !features) return PULSAR_ERR_ARG;
     if (c->stage < 2) return PULSAR_ERR_STATE;
     DeviceGuard guard(c->device);
-    cudaError_t e = launch_forward(c->frame, c->ws, features, bg, image, 0, as_stream(stream));
+    cudaError_t e = launch_forward(c->frames, c->ws, features, bg, image, 0, as_stream(stream));
     if (e != cudaSuccess) return PULSAR_ERR_CUDA;
     c->stage = 3;
     return PULSAR_OK;
@@ -252,17 +250,17 @@ int pulsar_backward(pulsar_ctx_t c, const float* features, const float* bg, cons
     if (c->stage < 3) return PULSAR_ERR_STATE;
     if (!grad_pos && !grad_radius && !grad_opacity && !grad_features && !grad_cam)
         return PULSAR_OK;   // nothing requested (Pulsar Sec. B.2)
-    if (!image || !grad_image || (c->frame.n > 0 && !features)) return PULSAR_ERR_ARG;
+    if (!image || !grad_image || (c->frames.f[0].n > 0 && !features)) return PULSAR_ERR_ARG;
     DeviceGuard guard(c->device);
     cudaStream_t s = as_stream(stream);
-    const Frame& f = c->frame;
+    const Frame& f = c->frames.f[0];
     const size_t n = (size_t)f.n;
     if (grad_opacity && n && cudaMemsetAsync(grad_opacity, 0, n * 4, s) != cudaSuccess)
         return PULSAR_ERR_CUDA;
     if (grad_features && n &&
         cudaMemsetAsync(grad_features, 0, n * (size_t)f.channels * 4, s) != cudaSuccess)
         return PULSAR_ERR_CUDA;
-    cudaError_t e = launch_backward(f, c->ws, c->pos, features, image, grad_image, grad_pos,
+    cudaError_t e = launch_backward(c->frames, c->ws, c->pos, features, image, grad_image, grad_pos,
                                     grad_radius, grad_opacity, grad_features, grad_cam, s);
     return cuda_err(e);
 }
@@ -290,13 +288,16 @@ int64_t pulsar_debug_copy(pulsar_ctx_t c, int what, void* dst, int64_t bytes, vo
     if (!c || bytes < 0) return PULSAR_ERR_ARG;
     DeviceGuard guard(c->device);
     cudaStream_t s = as_stream(stream);
-    const Frame& f = c->frame;
-    const int64_t n = f.n, P = (int64_t)f.width * f.height;
+    const Frame& f = c->frames.f[0];
+    const int K = c->n_cams > 0 ? c->n_cams : 1;
+    // every per-camera array covers the batch's cameras, camera after camera
+    const int64_t n = f.n, P1 = (int64_t)f.width * f.height, P = P1 * K;
+    const int64_t B = (int64_t)f.n_tiles * K;
     const void* src = nullptr;
     int64_t size = 0;
     switch (what) {
-        case PULSAR_DBG_RECORDS: src = c->ws.rec; size = n * (int64_t)sizeof(SphereRec); break;
-        case PULSAR_DBG_TILE_OFFSETS: src = c->ws.tile_start; size = (int64_t)(f.n_tiles + 1) * 4; break;
+        case PULSAR_DBG_RECORDS: src = c->ws.rec; size = n * K * (int64_t)sizeof(SphereRec); break;
+        case PULSAR_DBG_TILE_OFFSETS: src = c->ws.tile_start; size = (B + 1) * 4; break;
         case PULSAR_DBG_TILE_IDS: {
             uint32_t m = 0;
             if (cudaMemcpyAsync(&m, &c->ws.state->n_pairs, 4, cudaMemcpyDeviceToHost, s) !=
@@ -316,7 +317,7 @@ int64_t pulsar_debug_copy(pulsar_ctx_t c, int what, void* dst, int64_t bytes, vo
             if (!dst) return size;
             if (bytes > size) return PULSAR_ERR_ARG;
             std::vector<int32_t> pos((size_t)P * f.n_track);
-            std::vector<uint32_t> starts((size_t)f.n_tiles + 1);
+            std::vector<uint32_t> starts((size_t)B + 1);
             uint32_t m = 0;
             if (cudaMemcpyAsync(pos.data(), c->ws.ids, (size_t)size, cudaMemcpyDeviceToHost, s) !=
                     cudaSuccess ||
@@ -333,8 +334,10 @@ int64_t pulsar_debug_copy(pulsar_ctx_t c, int what, void* dst, int64_t bytes, vo
                 return PULSAR_ERR_CUDA;
             for (int64_t q = 0; q < (int64_t)pos.size(); ++q) {
                 if (pos[q] < 0) continue;
-                const int64_t px = q % P;
-                const int tile = (int)((px / f.width) / kTile) * f.tiles_x + (int)((px % f.width) / kTile);
+                const int64_t pg = q % P;               // pixel of the batch
+                const int64_t cam = pg / P1, px = pg % P1;
+                const int64_t tile = cam * f.n_tiles + ((px / f.width) / kTile) * f.tiles_x +
+                                     (px % f.width) / kTile;
                 const uint64_t at = (uint64_t)starts[tile] + (uint64_t)pos[q];
                 pos[q] = at < m ? (int32_t)list[at] : -1;
             }

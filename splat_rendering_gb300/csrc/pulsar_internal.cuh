@@ -16,6 +16,7 @@ constexpr int kTile = 16;           // 16x16 pixel tiles (Pulsar Sec. B.1.2)
 constexpr int kTilePix = kTile * kTile;
 constexpr int kMaxTrack = 16;
 constexpr int kMaxChannels = 64;
+constexpr int kMaxCams = 8;         // cameras of one batched frame
 constexpr uint32_t kFlagKeep = 1u, kFlagFloor = 2u, kFlagCut = 4u;   // per-sphere record flags
 constexpr uint32_t kParamNormalize = 4u;   // Frame::flags bit: normalised gradients
 constexpr float kPi = 3.14159265358979f;
@@ -23,7 +24,8 @@ constexpr float kPi = 3.14159265358979f;
 // Device error bits (latched in DevState::error).
 constexpr uint32_t kErrCapacity = 1u;
 
-// Per-frame constants, passed by value to every kernel.
+// Per-camera constants of a frame (all cameras of a batch share the image
+// size, the parameters and the spheres).
 struct Frame {
     float R[9], t[3];
     float fx, fy, cx, cy, znear, zfar;
@@ -40,6 +42,19 @@ struct Frame {
     uint32_t flags;
     uint32_t max_pairs;
     int ortho;            // orthographic camera: rays along +z, slopes a = b = 0
+    // the camera's place in the batch
+    int cam, n_cams;
+    uint32_t tile_base;   // cam * n_tiles: its first tile in the batch's tile lists
+    uint32_t pix_base;    // cam * width * height: its first pixel in the pixel buffers
+    uint32_t rec_base;    // cam * n: its first sphere record / gradient accumulator
+    uint32_t n_tiles_all; // n_cams * n_tiles
+    uint32_t pix_all;     // n_cams * width * height: plane stride of ids / d
+};
+
+// The cameras of a frame, passed by value to every kernel (f[0] also holds
+// the batch-wide fields); a block finds its camera from its tile.
+struct Frames {
+    Frame f[kMaxCams];
 };
 
 // Small device-resident counters.
@@ -309,6 +324,7 @@ struct __align__(16) SphereRec {
 
 struct Workspace {
     SphereRec* rec;    // [maxN]
+    // per camera of a batch: [maxCams][...] blocks, camera after camera
     float4* gacc;      // [maxN] dL/dc.xyz, dL/dr accumulators (zero between frames)
     float* hitcnt;     // [maxN] pixels tracking each sphere, for normalised gradients
                        // (zero between frames)
@@ -328,16 +344,67 @@ struct Workspace {
     DevState* state;
 };
 
+// ------------------------------------------------------- host helpers --
+// Per-camera frame constants from the ABI structs (host side).  log2 units:
+// exponents are kept in base 2 (exp2 is the cheap hardware exponential).
+inline void fill_frame(Frame& f, const float R[9], const float t[3], float fx, float fy,
+                       float cx, float cy, int width, int height, float znear, float zfar,
+                       int ortho, float gamma, float bg_eps, float stop_tau, float kappa,
+                       float amin, int n_track, int channels, uint32_t flags, int n,
+                       uint32_t max_pairs, int cam, int n_cams) {
+    for (int k = 0; k < 9; ++k) f.R[k] = R[k];
+    for (int k = 0; k < 3; ++k) f.t[k] = t[k];
+    f.fx = fx; f.fy = fy; f.cx = cx; f.cy = cy;
+    f.znear = znear; f.zfar = zfar;
+    f.ifx = 1.0f / fx;
+    f.ify = 1.0f / fy;
+    f.ifx_lo = (float)(1.0 / (double)fx - (double)f.ifx);
+    f.ify_lo = (float)(1.0 / (double)fy - (double)f.ify);
+    f.fmin = fx <= fy ? fx : fy;
+    f.gamma = gamma;
+    f.inv_gamma = 1.0f / gamma;
+    f.bg_eps = bg_eps;
+    f.stop_tau = stop_tau;
+    f.kappa = kappa;
+    f.amin = amin;
+    f.inv_zrange = 1.0f / (zfar - znear);
+    const double log2e = 1.4426950408889634073599;
+    const double zk = log2e / (((double)zfar - (double)znear) * (double)gamma);
+    f.zk_hi = (float)zk;
+    f.zk_lo = (float)(zk - (double)f.zk_hi);
+    const double eg = log2e * (double)bg_eps / (double)gamma;
+    f.eg_hi = (float)eg;
+    f.eg_lo = (float)(eg - (double)f.eg_hi);
+    f.width = width;
+    f.height = height;
+    f.tiles_x = (width + kTile - 1) / kTile;
+    f.tiles_y = (height + kTile - 1) / kTile;
+    f.n_tiles = f.tiles_x * f.tiles_y;
+    f.n_track = n_track;
+    f.channels = channels;
+    f.n = n;
+    f.flags = flags;
+    f.max_pairs = max_pairs;
+    f.ortho = ortho;
+    f.cam = cam;
+    f.n_cams = n_cams;
+    f.tile_base = (uint32_t)(cam * f.n_tiles);
+    f.pix_base = (uint32_t)cam * (uint32_t)(width * height);
+    f.rec_base = (uint32_t)cam * (uint32_t)n;
+    f.n_tiles_all = (uint32_t)(n_cams * f.n_tiles);
+    f.pix_all = (uint32_t)n_cams * (uint32_t)(width * height);
+}
+
 // ---------------------------------------------------------- launchers --
 // (defined in the .cu files; all enqueue on `stream` and never synchronise)
-cudaError_t launch_project(const Frame& f, const Workspace& w, const float* pos,
+cudaError_t launch_project(const Frames& fs, const Workspace& w, const float* pos,
                            const float* radius, const float* opacity, cudaStream_t stream);
-cudaError_t launch_bin(const Frame& f, const Workspace& w, cudaStream_t stream);
+cudaError_t launch_bin(const Frames& fs, const Workspace& w, cudaStream_t stream);
 cudaError_t prepare_forward();   // opt the forward kernels into their shared memory
-cudaError_t launch_forward(const Frame& f, const Workspace& w, const float* features,
+cudaError_t launch_forward(const Frames& fs, const Workspace& w, const float* features,
                            const float* bg, float* image, int max_pairs_stride,
                            cudaStream_t stream);
-cudaError_t launch_backward(const Frame& f, const Workspace& w, const float* pos,
+cudaError_t launch_backward(const Frames& fs, const Workspace& w, const float* pos,
                             const float* features, const float* image, const float* grad_image,
                             float* grad_pos, float* grad_radius, float* grad_opacity,
                             float* grad_features, float* grad_cam, cudaStream_t stream);

@@ -51,7 +51,8 @@ class Params(ctypes.Structure):
                 ("channels", ctypes.c_int32), ("flags", ctypes.c_uint32)]
 
 
-EXPORTS = ("pulsar_create", "pulsar_destroy", "pulsar_project", "pulsar_bin",
+EXPORTS = ("pulsar_create", "pulsar_create_cams", "pulsar_destroy", "pulsar_project",
+           "pulsar_project_cams", "pulsar_bin",
            "pulsar_forward", "pulsar_backward", "pulsar_status", "pulsar_strerror",
            "pulsar_debug_copy", "pulsar_render_noalloc")
 
@@ -67,9 +68,13 @@ def load(path: str = LIB_PATH):
     lib = ctypes.CDLL(path)
     P, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
     lib.pulsar_create.argtypes = [ctypes.POINTER(P), ctypes.c_int, I64, I64, I32, I32, I32, I32]
+    lib.pulsar_create_cams.argtypes = [ctypes.POINTER(P), ctypes.c_int, I64, I64, I32, I32, I32,
+                                       I32, I32]
     lib.pulsar_destroy.argtypes = [P]
     lib.pulsar_project.argtypes = [P, P, P, P, I64, ctypes.POINTER(Camera),
                                    ctypes.POINTER(Params), P]
+    lib.pulsar_project_cams.argtypes = [P, P, P, P, I64, ctypes.POINTER(Camera), I32,
+                                        ctypes.POINTER(Params), P]
     lib.pulsar_bin.argtypes = [P, P]
     lib.pulsar_forward.argtypes = [P, P, P, P, P]
     lib.pulsar_backward.argtypes = [P] + [P] * 9 + [P]
@@ -146,10 +151,15 @@ def params(p, count_hits: bool = False) -> Params:
 
 # ------------------------------------------------------------ C entry points --
 def create(device: int, max_spheres: int, max_pairs: int, max_width: int, max_height: int,
-           max_channels: int, max_track: int) -> int:
+           max_channels: int, max_track: int, max_cams: int = 1) -> int:
     h = ctypes.c_void_p()
-    _check(load().pulsar_create(ctypes.byref(h), device, max_spheres, max_pairs, max_width,
-                                max_height, max_channels, max_track), "pulsar_create")
+    if max_cams == 1:
+        _check(load().pulsar_create(ctypes.byref(h), device, max_spheres, max_pairs, max_width,
+                                    max_height, max_channels, max_track), "pulsar_create")
+    else:
+        _check(load().pulsar_create_cams(ctypes.byref(h), device, max_spheres, max_pairs,
+                                         max_width, max_height, max_channels, max_track,
+                                         max_cams), "pulsar_create_cams")
     return h.value
 
 
@@ -161,6 +171,14 @@ def project(ctx, pos, radius, opacity, n: int, cam: Camera, prm: Params, stream=
     _check(load().pulsar_project(ctx, _ptr(pos), _ptr(radius), _ptr(opacity), int(n),
                                  ctypes.byref(cam), ctypes.byref(prm), _stream(stream)),
            "pulsar_project")
+
+
+def project_cams(ctx, pos, radius, opacity, n: int, cams, prm: Params, stream=None):
+    """Project the spheres for a batch of cameras (list of Camera structs)."""
+    arr = (Camera * len(cams))(*cams)
+    _check(load().pulsar_project_cams(ctx, _ptr(pos), _ptr(radius), _ptr(opacity), int(n), arr,
+                                      len(cams), ctypes.byref(prm), _stream(stream)),
+           "pulsar_project_cams")
 
 
 def bin(ctx, stream=None):  # noqa: A001  (same name as the C entry point)
@@ -222,10 +240,11 @@ class Renderer:
     """
 
     def __init__(self, max_spheres: int, max_pairs: int, max_width: int, max_height: int,
-                 max_channels: int = 3, max_track: int = 8, device: int = 0):
+                 max_channels: int = 3, max_track: int = 8, device: int = 0,
+                 max_cams: int = 1):
         self.device = device
         self.ctx = create(device, max_spheres, max_pairs, max_width, max_height, max_channels,
-                          max_track)
+                          max_track, max_cams)
         self._frame = None
 
     def close(self):
@@ -239,28 +258,36 @@ class Renderer:
         except Exception:
             pass
 
-    def render(self, pos, radius, opacity, features, cam: Camera, prm: Params, bg, image=None,
+    def render(self, pos, radius, opacity, features, cam, prm: Params, bg, image=None,
                stream=None):
+        """Render one camera (a Camera struct; image [H,W,C]) or a batch (a list
+        of Camera structs of equal size; image [K,H,W,C])."""
         import torch
         n = int(pos.shape[0])
         C = int(prm.channels)
+        batch = isinstance(cam, (list, tuple))
+        first = cam[0] if batch else cam
+        shape = ((len(cam),) if batch else ()) + (first.height, first.width, C)
         if image is None:
-            image = torch.empty((cam.height, cam.width, C), device=f"cuda:{self.device}",
-                                dtype=torch.float32)
-        project(self.ctx, pos, radius, opacity, n, cam, prm, stream)
+            image = torch.empty(shape, device=f"cuda:{self.device}", dtype=torch.float32)
+        if batch:
+            project_cams(self.ctx, pos, radius, opacity, n, list(cam), prm, stream)
+        else:
+            project(self.ctx, pos, radius, opacity, n, cam, prm, stream)
         bin(self.ctx, stream)
         forward(self.ctx, features, bg, image, stream)
-        self._frame = (pos, features, bg, image, n, C)
+        self._frame = (pos, features, bg, image, n, C, len(cam) if batch else 0)
         return image
 
     def backward(self, grad_image, want=("pos", "radius", "opacity", "features", "cam"),
                  out=None, stream=None):
         import torch
-        pos, features, bg, image, n, C = self._frame
+        pos, features, bg, image, n, C, K = self._frame
         dev = image.device
         if out is None:
             out = {}
-            shapes = dict(pos=(n, 3), radius=(n,), opacity=(n,), features=(n, C), cam=(16,))
+            shapes = dict(pos=(n, 3), radius=(n,), opacity=(n,), features=(n, C),
+                          cam=(K, 16) if K else (16,))
             for k in want:
                 out[k] = torch.empty(shapes[k], device=dev, dtype=torch.float32)
         backward(self.ctx, features, bg, image, grad_image, out.get("pos"), out.get("radius"),
