@@ -34,6 +34,8 @@ WORKLOADS = {
     "headline_ortho": "headline sizes, orthographic camera: 1,000,000 spheres, 1024x1024, "
                       "3 channels, n_track 5, R/t/K gradients",
     "neural": "neural: 1,000,000 spheres, 1024x1024, 16 channels, n_track 8, R/t/K gradients",
+    "driving": "driving rig: 2,000,000 spheres, six 1920x1080 cameras in one batched launch, "
+               "3 channels, n_track 5, R/t/K gradients; value in camera frames/s",
 }
 METRIC = "fwd+bwd frames/s at 1M spheres 1024^2"
 UNIT = "frames/s"
@@ -252,24 +254,29 @@ def run_gb300(a):
     dev = torch.device("cuda", local)
 
     scene = scenes.make(a.scene)
-    cam, prm = scene.cameras[0], scene.params
+    # the driving rig renders its six cameras as one batch; the others one camera
+    cams = scene.cameras if a.scene == "driving" else scene.cameras[:1]
+    K = len(cams)
+    cam, prm = cams[0], scene.params
     N, C, T = scene.n, prm.channels, prm.n_track
-    P = cam.width * cam.height
+    P = cam.width * cam.height * K
 
     def dev_t(x):
         return torch.from_numpy(np.ascontiguousarray(x)).to(dev)
 
     pos, rad, opa, feat = dev_t(scene.pos), dev_t(scene.radius), dev_t(scene.opacity), \
         dev_t(scene.features)
-    bg, G = dev_t(scene.bg), dev_t(scene.grad_images[0])
-    c_cam, c_prm = pl.camera(cam), pl.params(prm)
-    image = torch.empty((cam.height, cam.width, C), device=dev)
+    G_host = np.stack(scene.grad_images[:K]) if K > 1 else scene.grad_images[0]
+    bg, G = dev_t(scene.bg), dev_t(G_host)
+    c_cam = [pl.camera(c) for c in cams] if K > 1 else pl.camera(cam)
+    c_prm = pl.params(prm)
+    image = torch.empty(((K,) if K > 1 else ()) + (cam.height, cam.width, C), device=dev)
     grads = {"pos": torch.empty((N, 3), device=dev), "radius": torch.empty(N, device=dev),
              "opacity": torch.empty(N, device=dev), "features": torch.empty((N, C), device=dev),
-             "cam": torch.empty(16, device=dev)}
+             "cam": torch.empty(((K,) if K > 1 else ()) + (16,), device=dev)}
     cap = 4 * N
     r = pl.Renderer(max_spheres=N, max_pairs=cap, max_width=cam.width, max_height=cam.height,
-                    max_channels=C, max_track=T, device=local)
+                    max_channels=C, max_track=T, device=local, max_cams=K)
 
     def step():
         r.render(pos, rad, opa, feat, c_cam, c_prm, bg, image=image)
@@ -287,7 +294,8 @@ def run_gb300(a):
     if code == pl.ERR_CAPACITY:
         r.close()
         r = pl.Renderer(max_spheres=N, max_pairs=2 * M, max_width=cam.width,
-                        max_height=cam.height, max_channels=C, max_track=T, device=local)
+                        max_height=cam.height, max_channels=C, max_track=T, device=local,
+                        max_cams=K)
         step()
         code, M, H = r.status()
     assert code == 0, pl.strerror(code)
@@ -344,7 +352,10 @@ def run_gb300(a):
         flush.zero_()
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
         ev[0].record()
-        pl.project(r.ctx, pos, rad, opa, N, c_cam, c_prm)
+        if K > 1:
+            pl.project_cams(r.ctx, pos, rad, opa, N, c_cam, c_prm)
+        else:
+            pl.project(r.ctx, pos, rad, opa, N, c_cam, c_prm)
         ev[1].record()
         pl.bin(r.ctx)
         ev[2].record()
@@ -362,7 +373,7 @@ def run_gb300(a):
     # ---- end to end through the API with host buffers (pinned), copies timed
     host_in = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in
                (("pos", scene.pos), ("radius", scene.radius), ("opacity", scene.opacity),
-                ("features", scene.features), ("G", scene.grad_images[0]))}
+                ("features", scene.features), ("G", G_host))}
     host_out = {"image": torch.empty(image.shape).pin_memory()}
     for k, v in grads.items():
         host_out[k] = torch.empty(v.shape).pin_memory()
@@ -423,7 +434,45 @@ def run_gb300(a):
             "fp32_time_ms": path_flops / (fp32 * 1e12) * 1e3,
             "frac": path_time * 1e3 / (total_ms / a.steps)}
 
-    value = world * a.steps / (total_ms * 1e-3)
+    value = world * K * a.steps / (total_ms * 1e-3)   # camera frames (K per step)
+    per_cam_loop = None
+    if K > 1:
+        # the same rig rendered camera by camera through one single-camera
+        # context (a graph of K render + backward calls), timed the same way
+        r1 = pl.Renderer(max_spheres=N, max_pairs=cap, max_width=cam.width,
+                         max_height=cam.height, max_channels=C, max_track=T, device=local)
+        singles = [pl.camera(c) for c in cams]
+        g1 = {k: (v[0] if k == "cam" else v) for k, v in grads.items()}
+
+        def loop_step():
+            for k in range(K):
+                r1.render(pos, rad, opa, feat, singles[k], c_prm, bg, image=image[k])
+                r1.backward(G[k], out=g1)
+
+        s1 = torch.cuda.Stream(device=dev)
+        s1.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s1):
+            for _ in range(2):
+                loop_step()
+        torch.cuda.current_stream().wait_stream(s1)
+        torch.cuda.synchronize()
+        graph1 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph1):
+            loop_step()
+        for _ in range(a.warmup):
+            flush.zero_()
+            graph1.replay()
+        torch.cuda.synchronize()
+        ev1 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(a.steps)]
+        for e0, e1 in ev1:
+            flush.zero_()
+            e0.record()
+            graph1.replay()
+            e1.record()
+        torch.cuda.synchronize()
+        per_cam_loop = sum(e0.elapsed_time(e1) for e0, e1 in ev1) / a.steps
+        r1.close()
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
             "warmup": a.warmup, "ms_per_step": total_ms / a.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
@@ -431,11 +480,13 @@ def run_gb300(a):
                        "l2": "flushed between steps (256 MB write, outside the timed events)",
                        "timing": "CUDA events around a CUDA-graph replay of one step"},
             "msphere_pixel_per_s": world * H / (total_ms / a.steps * 1e-3) / 1e6,
+            **({"cameras_per_step": K, "camera_by_camera_ms_per_step": per_cam_loop}
+               if K > 1 else {}),
             "hits_per_frame": H, "pairs_per_frame": M, "tracked_hits_per_frame": Ht,
             "breakdown_ms": breakdown,
             "path_roofline": path,
             "roofline": roofline,
-            "e2e": {"value": world * a.steps / (e2e_total * 1e-3), "unit": UNIT,
+            "e2e": {"value": world * K * a.steps / (e2e_total * 1e-3), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": KERNELS_PER_STEP * a.steps,
             "clocks": clk, "wall_s_timed": t_wall}
