@@ -66,6 +66,23 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(value: float, dist, device) -> float:
+    """The largest of every rank's value (the slowest replica's time); the
+    value itself for a single process (dist None)."""
+    if not dist:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, units_per_rank_step: int, steps: int, total_ms: float) -> float:
+    """Whole-job throughput: the units all replicas processed over the slowest
+    replica's time (replicas render independent frames; no data-path exchange)."""
+    return world * units_per_rank_step * steps / (total_ms * 1e-3)
+
+
 # ------------------------------------------------------------------ clocks --
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -338,11 +355,8 @@ def run_gb300(a):
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
     step_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
-    total_ms = sum(step_ms)
+    total_ms = max_over_ranks(sum(step_ms), dist, dev)
     if dist:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
         dist.barrier()
 
     # ---- per-stage breakdown (same kernels, eager, events between ABI calls)
@@ -403,11 +417,7 @@ def run_gb300(a):
         e1.record()
         torch.cuda.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
-    e2e_total = sum(e2e_ms)
-    if dist:
-        tt = torch.tensor([e2e_total], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_total = float(tt.item())
+    e2e_total = max_over_ranks(sum(e2e_ms), dist, dev)
 
     # ---- roofline of the dominant kernel (the forward) and of the whole path
     peaks, peak_src = measured_peaks()
@@ -434,7 +444,7 @@ def run_gb300(a):
             "fp32_time_ms": path_flops / (fp32 * 1e12) * 1e3,
             "frac": path_time * 1e3 / (total_ms / a.steps)}
 
-    value = world * K * a.steps / (total_ms * 1e-3)   # camera frames (K per step)
+    value = job_rate(world, K, a.steps, total_ms)   # camera frames (K per step)
     per_cam_loop = None
     if K > 1:
         # the same rig rendered camera by camera through one single-camera
@@ -486,7 +496,7 @@ def run_gb300(a):
             "breakdown_ms": breakdown,
             "path_roofline": path,
             "roofline": roofline,
-            "e2e": {"value": world * K * a.steps / (e2e_total * 1e-3), "unit": UNIT,
+            "e2e": {"value": job_rate(world, K, a.steps, e2e_total), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": KERNELS_PER_STEP * a.steps,
             "clocks": clk, "wall_s_timed": t_wall}
