@@ -283,7 +283,7 @@ k_backward(Frames fs, Workspace w, const float* __restrict__ features,
         // pipe is far too slow even for reductions
         FPair s = {0.0f, 0.0f};
         for (int q = 0; q < kBwdThreads / 32; ++q) s = pp_add(s, FPair{s_k[q][tid], 0.0f});
-        w.kpart[4 * tile_g + tid] = make_float2(s.hi, s.lo);
+        w.kpart[(size_t)tid * f.n_tiles_all + tile_g] = make_float2(s.hi, s.lo);
     }
 }
 
@@ -378,7 +378,7 @@ k_finalize_one_cam(Frames fs, Workspace w, const float* __restrict__ pos, float*
     if (tid < 12) {
         FPair s = {0.0f, 0.0f};
         for (int q = 0; q < kFinThreads / 32; ++q) s = pp_add(s, FPair{s_part[q][tid], 0.0f});
-        w.rtpart[12 * blockIdx.x + tid] = make_float2(s.hi, s.lo);
+        w.rtpart[(size_t)tid * gridDim.x + blockIdx.x] = make_float2(s.hi, s.lo);
     }
 }
 
@@ -498,7 +498,7 @@ k_finalize_cams(Frames fs, Workspace w, const float* __restrict__ pos, float* __
         if (tid < 12) {
             FPair s = {0.0f, 0.0f};
             for (int q = 0; q < kFinThreads / 32; ++q) s = pp_add(s, FPair{s_part[q][tid], 0.0f});
-            w.rtpart[(blockIdx.x * n_cams + cam) * 12 + tid] = make_float2(s.hi, s.lo);
+            w.rtpart[((size_t)cam * 12 + tid) * gridDim.x + blockIdx.x] = make_float2(s.hi, s.lo);
         }
         __syncthreads();   // s_part is reused by the next camera
     }
@@ -507,47 +507,44 @@ k_finalize_cams(Frames fs, Workspace w, const float* __restrict__ pos, float* __
 // One block per camera: its dL/dR and dL/dt from the finalize blocks'
 // partials and dL/d(fx, fy, cx, cy) from its tiles' partials, summed in a
 // fixed order in float-pair arithmetic (deterministic, ~1e-14 relative;
-// Pulsar Sec. B.2's device-wide camera reduction).
+// Pulsar Sec. B.2's device-wide camera reduction).  The partials of each of
+// the 16 outputs are contiguous; two warps sum each output with coalesced
+// loads and combine through shared memory.
 __global__ void __launch_bounds__(kCamThreads)
 k_camera_reduce(Frames fs, Workspace w, int fin_blocks, float* __restrict__ grad_cam) {
-    __shared__ float2 s_part[kCamThreads / 32][16];
+    static_assert(kCamThreads == 1024, "two warps per output");
+    __shared__ float2 s_half[16][2];
     const int cam = blockIdx.x;
     const Frame& f = fs.f[cam];
-    const int n_cams = fs.f[0].n_cams;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    FPair v[16];
-#pragma unroll
-    for (int q = 0; q < 16; ++q) v[q] = {0.0f, 0.0f};
-    for (int b = tid; b < fin_blocks; b += kCamThreads)
-#pragma unroll
-        for (int q = 0; q < 12; ++q) {
-            const float2 t = w.rtpart[(b * n_cams + cam) * 12 + q];
-            v[q] = pp_add(v[q], FPair{t.x, t.y});
-        }
-    for (int b = tid; b < f.n_tiles; b += kCamThreads)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float2 t = w.kpart[4 * (f.tile_base + b) + q];
-            v[12 + q] = pp_add(v[12 + q], FPair{t.x, t.y});
-        }
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
-        FPair s = v[q];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const FPair t = {__shfl_down_sync(0xffffffffu, s.hi, o),
-                             __shfl_down_sync(0xffffffffu, s.lo, o)};
-            s = pp_add(s, t);
-        }
-        if (lane == 0) s_part[warp][q] = make_float2(s.hi, s.lo);
+    const int q = warp >> 1, half = warp & 1;
+    const float2* src;
+    int len;
+    if (q < 12) {
+        src = w.rtpart + ((size_t)cam * 12 + q) * fin_blocks;
+        len = fin_blocks;
+    } else {
+        src = w.kpart + (size_t)(q - 12) * f.n_tiles_all + f.tile_base;
+        len = f.n_tiles;
     }
+    const int lo = half ? len / 2 : 0, hi = half ? len : len / 2;
+    FPair v = {0.0f, 0.0f};
+#pragma unroll 4
+    for (int b = lo + lane; b < hi; b += 32) {
+        const float2 t = src[b];
+        v = pp_add(v, FPair{t.x, t.y});
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const FPair t = {__shfl_down_sync(0xffffffffu, v.hi, o),
+                         __shfl_down_sync(0xffffffffu, v.lo, o)};
+        v = pp_add(v, t);
+    }
+    if (lane == 0) s_half[q][half] = make_float2(v.hi, v.lo);
     __syncthreads();
     if (tid < 16) {
-        FPair s = {0.0f, 0.0f};
-        for (int q = 0; q < kCamThreads / 32; ++q) {
-            const float2 t = s_part[q][tid];
-            s = pp_add(s, FPair{t.x, t.y});
-        }
+        const float2 a = s_half[tid][0], b = s_half[tid][1];
+        const FPair s = pp_add(FPair{a.x, a.y}, FPair{b.x, b.y});
         if (grad_cam) grad_cam[16 * cam + tid] = __fadd_rn(s.hi, s.lo);
     }
 }

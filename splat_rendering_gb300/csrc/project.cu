@@ -15,7 +15,9 @@ namespace {
 
 constexpr int kProjectThreads = 256;
 
-__global__ void __launch_bounds__(kProjectThreads)
+// 8 blocks per SM (32 registers): the kernel waits on memory and atomics, so
+// resident warps count for more than the few registers spilled to L1
+__global__ void __launch_bounds__(kProjectThreads, 8)
 k_project(Frames fs, Workspace w, const float* __restrict__ pos, const float* __restrict__ radius,
           const float* __restrict__ opacity) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;

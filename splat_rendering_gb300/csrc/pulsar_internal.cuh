@@ -339,8 +339,9 @@ struct Workspace {
     int32_t* ids;           // [maxT][maxP] tracked hits' positions in their tile list, -1 padded
     float* dtr;             // [maxT][maxP] distance factor d of each tracked hit
     int32_t* nhits;         // [maxP]
-    float2* kpart;          // [maxB][4] per-tile partial dL/d(fx, fy, cx, cy), float pairs
-    float2* rtpart;         // [ceil(maxN/256)][12] per-block partial dL/dR, dL/dt, float pairs
+    float2* kpart;          // [4][maxB] per-tile partial dL/d(fx, fy, cx, cy), float pairs
+    float2* rtpart;         // [cameras][12][finalize blocks] per-block partial dL/dR, dL/dt,
+                            // float pairs
     DevState* state;
 };
 
