@@ -59,7 +59,7 @@ class _Params(ctypes.Structure):
                 ("kappa", ctypes.c_double), ("geom_min_area", ctypes.c_double),
                 ("n_track", ctypes.c_int32), ("channels", ctypes.c_int32),
                 ("geom_cutoff", ctypes.c_int32), ("fp64_decisions", ctypes.c_int32),
-                ("normalize", ctypes.c_int32)]
+                ("normalize", ctypes.c_int32), ("gaussian", ctypes.c_int32)]
 
 
 def _load():
@@ -111,6 +111,7 @@ def _params(p, fp64: bool) -> _Params:
     q.geom_cutoff = 1 if p.geom_cutoff else 0
     q.fp64_decisions = 1 if fp64 else 0
     q.normalize = 1 if getattr(p, "normalize_grads", False) else 0
+    q.gaussian = 1 if getattr(p, "gaussian", False) else 0
     return q
 
 

@@ -45,6 +45,13 @@
 // z~, weights and tracked set are the pinhole's; the cutoff area is
 // pi (min(fx, fy) r)^2.
 //
+// Gaussian footprint (the splat variant named by the NuRec pages, whose kernel
+// is not printed; reading): the distance factor becomes an isotropic
+// Gaussian of sigma = r_eff / 3 over the same support rho < r_eff, shifted
+// and scaled to be 1 at the centre and 0 at the rim (so the image stays
+// continuous):  d = (exp(-9 rho^2 / (2 r_eff^2)) - e^-4.5) / (1 - e^-4.5).
+// Decisions (support, lists, order) are the sphere renderer's unchanged.
+//
 // Normalised gradients (Sec. B.2: sphere gradients averaged over the
 // contributing pixels, camera gradients normalised by the projected sphere
 // area and 1e-3; not a gradient of anything, so PARITY UNPINNED -- only the
@@ -87,6 +94,7 @@ typedef struct {
     int32_t geom_cutoff;     // 1: drop position/radius/camera grads of small spheres
     int32_t fp64_decisions;  // 1: all decisions in fp64 instead of the fp32 sequence
     int32_t normalize;       // 1: normalised gradients (Sec. B.2; see below)
+    int32_t gaussian;        // 1: Gaussian footprint instead of the linear one (see below)
 } oparams_t;
 
 }  // extern "C"
@@ -366,9 +374,17 @@ double ray_rho(const Sphere& s, double Q, double qq, const ocam_t& cam) {
     return cam.orthographic ? std::sqrt(Q) : std::sqrt(Q / qq) * s.c[2];
 }
 
-// distance factor d = 1 - rho / r_eff
-double dist_factor(const Sphere& s, double Q, double qq, const ocam_t& cam) {
-    return 1.0 - ray_rho(s, Q, qq, cam) / s.reff;
+// distance factor d(rho / r_eff): linear 1 - x, or the Gaussian footprint
+const double kGaussTail = std::exp(-4.5);
+double footprint(double x, bool gaussian) {
+    return gaussian ? (std::exp(-4.5 * x * x) - kGaussTail) / (1.0 - kGaussTail) : 1.0 - x;
+}
+// its derivative with respect to x = rho / r_eff
+double footprint_dx(double x, bool gaussian) {
+    return gaussian ? -9.0 * x * std::exp(-4.5 * x * x) / (1.0 - kGaussTail) : -1.0;
+}
+double dist_factor(const Sphere& s, double Q, double qq, const ocam_t& cam, bool gaussian) {
+    return footprint(ray_rho(s, Q, qq, cam) / s.reff, gaussian);
 }
 
 struct HitKey {
@@ -543,7 +559,7 @@ int64_t oracle_render(const double* pos, const double* radius, const double* opa
                 const Sphere& s = sph[h.id];
                 double U, V;
                 double Q = value_Q(s, p64, cam, &U, &V);
-                double d = dist_factor(s, Q, p64.qq, cam);
+                double d = dist_factor(s, Q, p64.qq, cam, prm.gaussian != 0);
                 double w = s.o * d * std::exp((s.o * s.zt - m) / gamma);
                 W += w;
                 for (int c = 0; c < C; ++c) acc[c] += w * features[(size_t)h.id * C + c];
@@ -609,7 +625,8 @@ int64_t oracle_render(const double* pos, const double* radius, const double* opa
             const bool ortho = cam.orthographic != 0;
             const double rho = ray_rho(s, Q, p.qq, cam);
             const double rq = ortho ? rho : std::sqrt(Q / p.qq);   // rho (orthographic), rho / c.z
-            const double d = 1.0 - rho / s.reff;
+            const bool gauss = prm.gaussian != 0;
+            const double d = footprint(rho / s.reff, gauss);
             const double E = std::exp((s.o * s.zt - m) / gamma);
             const double w = s.o * d * E;
             double sdot = 0.0;                                 // <G, f - F>
@@ -637,9 +654,11 @@ int64_t oracle_render(const double* pos, const double* radius, const double* opa
             if (s.cut) continue;
             // dw/dz~ = w * o / gamma ; dz~/dc.z = -1/(zfar - znear)
             uc[2] += w * (s.o / gamma) * dzt_dz;
-            // dw/dd = o E ; dd/drho = -1/r_eff ; dd/dr_eff = rho / r_eff^2
-            const double u_rho = -s.o * E / s.reff;
-            const double u_reff = s.o * E * rho / (s.reff * s.reff);
+            // dw/dd = o E ; with x = rho / r_eff: dd/drho = d'(x) / r_eff,
+            // dd/dr_eff = -d'(x) rho / r_eff^2 (linear: d' = -1)
+            const double ddx = footprint_dx(rho / s.reff, gauss);
+            const double u_rho = s.o * E * ddx / s.reff;
+            const double u_reff = -s.o * E * ddx * rho / (s.reff * s.reff);
             if (s.floor_r) {
                 if (ortho) {
                     // r_eff = kappa / f_min

@@ -68,6 +68,7 @@ class Params:
     channels: int = 3
     geom_cutoff: bool = True
     normalize_grads: bool = False   # averaged sphere / area-normalised camera gradients
+    gaussian: bool = False          # Gaussian footprint (sigma = r_eff / 3) instead of linear
 
 
 @dataclass

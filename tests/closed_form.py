@@ -54,8 +54,11 @@ def tangent_bounds(X, Z, Rr, f, c0):
     return umin, umax
 
 
-def render(pos, radius, opacity, features, cam, params, bg):
-    """Returns image [H,W,C], per-pixel sorted hit ids (list of lists), weights."""
+def render(pos, radius, opacity, features, cam, params, bg, gaussian=False):
+    """Returns image [H,W,C], per-pixel sorted hit ids (list of lists), weights.
+    gaussian: the distance factor is a Gaussian of standard deviation r/3 over
+    the same support, shifted and scaled to run from 1 at the centre to 0 at
+    the rim."""
     c = camera_space(pos, cam)
     r = reff(radius, c, cam, params.kappa)
     q = pixel_rays(cam)
@@ -76,7 +79,12 @@ def render(pos, radius, opacity, features, cam, params, bg):
         m = rho < r[i]
         if not m.any():
             continue
-        d = 1.0 - rho / r[i]
+        if gaussian:
+            sigma = r[i] / 3.0
+            tail = math.exp(-0.5 * 9.0)
+            d = (np.exp(-0.5 * (rho / sigma) ** 2) - tail) / (1.0 - tail)
+        else:
+            d = 1.0 - rho / r[i]
         w = np.where(m, o[i] * d * math.exp(o[i] * zt[i] / params.gamma), 0.0)
         num += w[..., None] * np.asarray(features[i], np.float64)
         den += w
