@@ -68,6 +68,12 @@ extern "C" {
  * the area of the disc it is rendered with.  Not the derivative of anything:
  * an optimisation aid, off by default. */
 #define PULSAR_FLAG_NORMALIZE_GRADS 0x4u
+/* Gaussian footprint (the splat variant of the NuRec pages): the distance
+ * factor d = 1 - rho/r_eff is replaced by an isotropic Gaussian of sigma =
+ * r_eff/3 over the same support, shifted and scaled to run from 1 at the
+ * centre to 0 at the rim: d = (exp(-4.5 (rho/r_eff)^2) - e^-4.5) /
+ * (1 - e^-4.5).  Decisions (support, tile lists, tracked ids) unchanged. */
+#define PULSAR_FLAG_GAUSSIAN      0x8u
 
 /* Camera, OpenCV axes (x right, y down, z forward).  R is the world->camera
  * rotation, row-major: c = R p + t.  Pixel (x, y) has its centre at

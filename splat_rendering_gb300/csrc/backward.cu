@@ -182,8 +182,14 @@ k_backward(Frames fs, Workspace w, const float* __restrict__ features,
                     // depth factor: dw/dz~ = w o / gamma, dz~/dc.z = -1/(zfar - znear)
                     float gcz = -sj * wt * o * f.inv_gamma * f.inv_zrange;
                     const float rho = f.ortho ? rq : rq * Z;
-                    const float g_rho = -sE * ireff;             // dd/drho = -1/r_eff
-                    const float g_reff = sE * rho * ireff * ireff;
+                    // with x = rho / r_eff: dd/drho = d'(x) / r_eff, dd/dr_eff =
+                    // -d'(x) rho / r_eff^2; linear d' = -1, Gaussian d' = -9 x exp(-4.5
+                    // x^2) / (1 - e^-4.5) = -9 x (d + e^-4.5 / (1 - e^-4.5))
+                    const float ddx = (f.flags & kParamGaussian)
+                                          ? -9.0f * rho * ireff * (d + kGaussTailRatio)
+                                          : -1.0f;
+                    const float g_rho = sE * ddx * ireff;
+                    const float g_reff = -sE * ddx * rho * ireff * ireff;
                     float gr = 0.0f;
                     if (fl & kFlagFloor) {
                         // r_eff = kappa c.z / f_min (orthographic: kappa / f_min)

@@ -279,7 +279,8 @@ k_forward(Frames fs, Workspace w, const float* __restrict__ features, const floa
                             pq.b = {bpv.x, bpv.y};
                             pq.qq = {qqv.x, qqv.y};
                             pq.iqq = s_iqq[pl];
-                            s_dbuf[warp][t] = distance_factor(uv, geo.x, geo.y, px, py, pq, f);
+                            s_dbuf[warp][t] = distance_factor(uv, geo.x, geo.y, px, py, pq, f,
+                                                              (f.flags & kParamGaussian) != 0);
                             atomicOr(&s_hmask[warp][(yy - row0) * kTile + (xx - tx0)], 1u << own);
                         }
                     }

@@ -19,6 +19,10 @@ constexpr int kMaxChannels = 64;
 constexpr int kMaxCams = 8;         // cameras of one batched frame
 constexpr uint32_t kFlagKeep = 1u, kFlagFloor = 2u, kFlagCut = 4u;   // per-sphere record flags
 constexpr uint32_t kParamNormalize = 4u;   // Frame::flags bit: normalised gradients
+constexpr uint32_t kParamGaussian = 8u;    // Frame::flags bit: Gaussian footprint
+// Gaussian footprint d = (exp(-4.5 x^2) - e^-4.5) / (1 - e^-4.5), x = rho / r_eff:
+// e^-4.5 / (1 - e^-4.5)
+constexpr float kGaussTailRatio = 0.0112337927f;
 constexpr float kPi = 3.14159265358979f;
 
 // Device error bits (latched in DevState::error).
@@ -257,7 +261,7 @@ __device__ __forceinline__ PixelPairs pixel_pairs(const PixelRay& r, const Frame
 // (a few ulps relative).
 __device__ __forceinline__ float distance_factor(const float4& uv, float ir2_hi, float ir2_lo,
                                                  float px, float py, const PixelPairs& pq,
-                                                 const Frame& f) {
+                                                 const Frame& f, bool gaussian) {
     // offsets to the projected centre, renormalised so that every hi part below
     // is the rounded value of its pair (px - u_hi is exact but coarse)
     FPair du = ef_sum(px, -uv.x);
@@ -272,6 +276,11 @@ __device__ __forceinline__ float distance_factor(const float4& uv, float ir2_hi,
     const FPair D = pp_sub(pq.qq, Qs);
     const float t = __fmul_rn(__fadd_rn(Qs.hi, Qs.lo), pq.iqq);   // (rho / r_eff)^2
     const float Dq = __fmul_rn(__fadd_rn(D.hi, D.lo), pq.iqq);    // 1 - t
+    if (gaussian) {
+        // Gaussian footprint: exp(-4.5 t) - e^-4.5 = e^-4.5 expm1(4.5 (1 - t)),
+        // accurate at the rim from the pair-precision 1 - t
+        return kGaussTailRatio * expm1f(4.5f * Dq);
+    }
     const float s = t > 0.0f ? t * rsqrtf(t) : 0.0f;
     return __fdividef(Dq, 1.0f + s);
 }

@@ -25,6 +25,7 @@ OK, ERR_ARG, ERR_CUDA, ERR_CAPACITY, ERR_STATE, ERR_NOMEM = 0, -1, -2, -3, -4, -
 FLAG_GEOM_CUTOFF = 0x1
 FLAG_COUNT_HITS = 0x2
 FLAG_NORMALIZE_GRADS = 0x4
+FLAG_GAUSSIAN = 0x8
 DBG = dict(records=1, tile_offsets=5, tile_ids=6, mg=7, wsum=8, ids=9, nhits=10)
 
 _lib = None
@@ -138,14 +139,15 @@ def camera(cam) -> Camera:
 def params(p, count_hits: bool = False) -> Params:
     """Params struct from any object with gamma, bg_eps, stop_tau, kappa,
     geom_min_area, n_track, channels, geom_cutoff (and optionally
-    normalize_grads) attributes."""
+    normalize_grads, gaussian) attributes."""
     q = Params()
     q.gamma, q.bg_eps, q.stop_tau = float(p.gamma), float(p.bg_eps), float(p.stop_tau)
     q.kappa, q.geom_min_area = float(p.kappa), float(p.geom_min_area)
     q.n_track, q.channels = int(p.n_track), int(p.channels)
     q.flags = (FLAG_GEOM_CUTOFF if getattr(p, "geom_cutoff", True) else 0) | \
               (FLAG_COUNT_HITS if count_hits else 0) | \
-              (FLAG_NORMALIZE_GRADS if getattr(p, "normalize_grads", False) else 0)
+              (FLAG_NORMALIZE_GRADS if getattr(p, "normalize_grads", False) else 0) | \
+              (FLAG_GAUSSIAN if getattr(p, "gaussian", False) else 0)
     return q
 
 
