@@ -263,6 +263,17 @@ def random_scene(seed: int, n: int, width: int, height: int, *, channels: int = 
                  _f32(np.zeros(channels)), _grads(rng, cams, channels))
 
 
+def shading_mlp(seed: int = 5) -> np.ndarray:
+    """Seeded weights of the per-pixel shading MLP (16 features + 3 view
+    direction -> 64 -> 64 -> 3), flat float32 in the order W1 [64,19], b1,
+    W2 [64,64], b2, W3 [3,64], b3; He-normal weights, small biases."""
+    rng = np.random.default_rng(seed)
+    parts = [rng.standard_normal((64, 19)) * math.sqrt(2.0 / 19), rng.uniform(-0.1, 0.1, 64),
+             rng.standard_normal((64, 64)) * math.sqrt(2.0 / 64), rng.uniform(-0.1, 0.1, 64),
+             rng.standard_normal((3, 64)) * math.sqrt(1.0 / 64), rng.uniform(-0.1, 0.1, 3)]
+    return _f32(np.concatenate([np.asarray(q).reshape(-1) for q in parts]))
+
+
 CONFIGS = {
     "tiny": tiny,
     "medium": medium,
