@@ -51,6 +51,7 @@ extern "C" {
 #define PULSAR_ERR_CAPACITY -3  /* more sphere-tile pairs than max_pairs */
 #define PULSAR_ERR_STATE    -4  /* call out of order (e.g. forward before bin) */
 #define PULSAR_ERR_NOMEM    -5  /* workspace allocation failed */
+#define PULSAR_ERR_TIMEOUT  -6  /* a bounded wait on the tensor cores gave up (frame invalid) */
 
 /* --------------------------------------------------------------- flags -- */
 /* Drop position/radius gradients (and the sphere's share of the camera
@@ -193,6 +194,26 @@ int pulsar_backward(pulsar_ctx_t ctx, const float* features, const float* bg,
  * frame (PULSAR_OK, PULSAR_ERR_CAPACITY) and clear it.  n_pairs (M) and
  * n_hits (hit pairs composited by the last forward) may be NULL. */
 int pulsar_status(pulsar_ctx_t ctx, void* stream, int64_t* n_pairs, int64_t* n_hits);
+
+/* Per-pixel neural shading (Pulsar Sec. 3.3: a per-pixel network turns the
+ * rendered feature map into RGB; Sec. 5.2: a shared fully-connected model
+ * conditioned on the pixel's view direction) of the current frame's cameras,
+ * on the tensor cores.  The network (the pages print none; a reading):
+ *   x = [F_p (16 channels), v_p (unit view direction in camera space)],
+ *   h1 = ReLU(W1 x + b1), h2 = ReLU(W2 h1 + b2), y = W3 h2 + b3,
+ *   19 -> 64 -> 64 -> 3, every matrix operand rounded to bfloat16 (nearest
+ *   even), fp32 accumulation and biases.
+ *   features [K,H,W,16]  feature images of the frame's K cameras (K >= 1),
+ *                        16-byte aligned; the frame must have 16 channels
+ *   params   [5635]      W1 [64,19], b1 [64], W2 [64,64], b2 [64], W3 [3,64],
+ *                        b3 [3], float32, row-major, concatenated
+ *   rgb      [K,H,W,3]   output, overwritten
+ * Requires pulsar_project (it takes the cameras from the frame).  Errors:
+ * PULSAR_ERR_ARG (NULL, misaligned features, channels != 16),
+ * PULSAR_ERR_STATE (no frame); a tensor-core wait that gives up is latched
+ * and reported by pulsar_status as PULSAR_ERR_TIMEOUT. */
+int pulsar_shade_forward(pulsar_ctx_t ctx, const float* features, const float* params,
+                         float* rgb, void* stream);
 
 /* Static string for an error code. */
 const char* pulsar_strerror(int code);

@@ -20,7 +20,8 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpulsar.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["project.cu", "bin.cu", "forward.cu", "backward.cu", "pulsar.cu", "noalloc.cu"]
+SOURCES = ["project.cu", "bin.cu", "forward.cu", "backward.cu", "shade.cu", "pulsar.cu",
+           "noalloc.cu"]
 
 
 def nvcc() -> str:

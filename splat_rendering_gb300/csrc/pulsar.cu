@@ -23,6 +23,7 @@ struct pulsar_ctx {
     DevState* host_state = nullptr;   // pinned mirror for pulsar_status
     Frames frames{};                   // the cameras of the current frame
     int n_cams = 0;
+    int n_sms = 1;
     const float* pos = nullptr;        // inputs of the current frame
     int stage = 0;                     // 0 none, 1 projected, 2 binned, 3 forward done
     bool counts_dirty = false;         // tile counts hold a frame that was never binned
@@ -80,6 +81,7 @@ const char* pulsar_strerror(int code) {
         case PULSAR_ERR_CAPACITY: return "sphere-tile pairs exceed max_pairs";
         case PULSAR_ERR_STATE: return "call out of order";
         case PULSAR_ERR_NOMEM: return "workspace allocation failed";
+        case PULSAR_ERR_TIMEOUT: return "a bounded wait on the tensor cores gave up";
         default: return "unknown error";
     }
 }
@@ -135,7 +137,9 @@ int pulsar_create_cams(pulsar_ctx_t* out, int device, int64_t max_spheres, int64
               alloc(c, &w.kpart, K * B * 4) && alloc(c, &w.rtpart, (N + 255) / 256 * K * 12) &&
               alloc(c, &w.state, 1);
     if (ok) ok = cudaMallocHost(&c->host_state, sizeof(DevState)) == cudaSuccess;
-    if (ok) ok = prepare_forward() == cudaSuccess;
+    if (ok) ok = prepare_forward() == cudaSuccess && prepare_shade() == cudaSuccess;
+    if (ok) ok = cudaDeviceGetAttribute(&c->n_sms, cudaDevAttrMultiProcessorCount, device) ==
+                 cudaSuccess;
     // zero-between-frames invariants
     if (ok)
         ok = cudaMemset(w.gacc, 0, K * N * sizeof(float4)) == cudaSuccess &&
@@ -265,6 +269,17 @@ int pulsar_backward(pulsar_ctx_t c, const float* features, const float* bg, cons
     return cuda_err(e);
 }
 
+int pulsar_shade_forward(pulsar_ctx_t c, const float* features, const float* params, float* rgb,
+                         void* stream) {
+    if (!c || !features || !params || !rgb) return PULSAR_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(features) & 15u) != 0) return PULSAR_ERR_ARG;
+    if (c->stage < 1) return PULSAR_ERR_STATE;
+    if (c->frames.f[0].channels != 16) return PULSAR_ERR_ARG;
+    DeviceGuard guard(c->device);
+    return cuda_err(launch_shade_forward(c->frames, c->ws, features, params, rgb, c->n_sms,
+                                         as_stream(stream)));
+}
+
 int pulsar_status(pulsar_ctx_t c, void* stream, int64_t* n_pairs, int64_t* n_hits) {
     if (!c) return PULSAR_ERR_ARG;
     DeviceGuard guard(c->device);
@@ -280,6 +295,7 @@ int pulsar_status(pulsar_ctx_t c, void* stream, int64_t* n_pairs, int64_t* n_hit
         const uint32_t zero = 0;
         cudaMemcpy(&c->ws.state->error, &zero, sizeof(zero), cudaMemcpyHostToDevice);
         if (h.error & kErrCapacity) return PULSAR_ERR_CAPACITY;
+        if (h.error & kErrTimeout) return PULSAR_ERR_TIMEOUT;
     }
     return PULSAR_OK;
 }

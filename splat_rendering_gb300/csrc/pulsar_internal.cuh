@@ -27,6 +27,7 @@ constexpr float kPi = 3.14159265358979f;
 
 // Device error bits (latched in DevState::error).
 constexpr uint32_t kErrCapacity = 1u;
+constexpr uint32_t kErrTimeout = 2u;    // a bounded wait on the tensor cores gave up
 
 // Per-camera constants of a frame (all cameras of a batch share the image
 // size, the parameters and the spheres).
@@ -414,6 +415,9 @@ cudaError_t prepare_forward();   // opt the forward kernels into their shared me
 cudaError_t launch_forward(const Frames& fs, const Workspace& w, const float* features,
                            const float* bg, float* image, int max_pairs_stride,
                            cudaStream_t stream);
+cudaError_t prepare_shade();   // opt the shading kernels into their shared memory
+cudaError_t launch_shade_forward(const Frames& fs, const Workspace& w, const float* features,
+                                 const float* params, float* rgb, int n_sms, cudaStream_t stream);
 cudaError_t launch_backward(const Frames& fs, const Workspace& w, const float* pos,
                             const float* features, const float* image, const float* grad_image,
                             float* grad_pos, float* grad_radius, float* grad_opacity,

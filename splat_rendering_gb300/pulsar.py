@@ -21,7 +21,7 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpulsar.so")
 
-OK, ERR_ARG, ERR_CUDA, ERR_CAPACITY, ERR_STATE, ERR_NOMEM = 0, -1, -2, -3, -4, -5
+OK, ERR_ARG, ERR_CUDA, ERR_CAPACITY, ERR_STATE, ERR_NOMEM, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5, -6
 FLAG_GEOM_CUTOFF = 0x1
 FLAG_COUNT_HITS = 0x2
 FLAG_NORMALIZE_GRADS = 0x4
@@ -53,7 +53,7 @@ class Params(ctypes.Structure):
 
 
 EXPORTS = ("pulsar_create", "pulsar_create_cams", "pulsar_destroy", "pulsar_project",
-           "pulsar_project_cams", "pulsar_bin",
+           "pulsar_project_cams", "pulsar_bin", "pulsar_shade_forward",
            "pulsar_forward", "pulsar_backward", "pulsar_status", "pulsar_strerror",
            "pulsar_debug_copy", "pulsar_render_noalloc")
 
@@ -77,6 +77,7 @@ def load(path: str = LIB_PATH):
     lib.pulsar_project_cams.argtypes = [P, P, P, P, I64, ctypes.POINTER(Camera), I32,
                                         ctypes.POINTER(Params), P]
     lib.pulsar_bin.argtypes = [P, P]
+    lib.pulsar_shade_forward.argtypes = [P, P, P, P, P]
     lib.pulsar_forward.argtypes = [P, P, P, P, P]
     lib.pulsar_backward.argtypes = [P] + [P] * 9 + [P]
     lib.pulsar_status.argtypes = [P, P, ctypes.POINTER(I64), ctypes.POINTER(I64)]
@@ -181,6 +182,13 @@ def project_cams(ctx, pos, radius, opacity, n: int, cams, prm: Params, stream=No
     _check(load().pulsar_project_cams(ctx, _ptr(pos), _ptr(radius), _ptr(opacity), int(n), arr,
                                       len(cams), ctypes.byref(prm), _stream(stream)),
            "pulsar_project_cams")
+
+
+def shade_forward(ctx, features, params, rgb, stream=None):
+    """Per-pixel shading MLP of the frame's feature images (see
+    pulsar_shade_forward in include/pulsar.h)."""
+    _check(load().pulsar_shade_forward(ctx, _ptr(features), _ptr(params), _ptr(rgb),
+                                       _stream(stream)), "pulsar_shade_forward")
 
 
 def bin(ctx, stream=None):  # noqa: A001  (same name as the C entry point)
@@ -295,6 +303,16 @@ class Renderer:
         backward(self.ctx, features, bg, image, grad_image, out.get("pos"), out.get("radius"),
                  out.get("opacity"), out.get("features"), out.get("cam"), stream)
         return out
+
+    def shade(self, features, params, rgb=None, stream=None):
+        """RGB of the per-pixel shading MLP over feature images [..., H, W, 16]
+        of the current frame's camera(s)."""
+        import torch
+        if rgb is None:
+            rgb = torch.empty(tuple(features.shape[:-1]) + (3,), device=features.device,
+                              dtype=torch.float32)
+        shade_forward(self.ctx, features, params, rgb, stream)
+        return rgb
 
     def status(self, stream=None, raise_on_error: bool = True):
         return status(self.ctx, stream, raise_on_error)
