@@ -215,6 +215,26 @@ int pulsar_status(pulsar_ctx_t ctx, void* stream, int64_t* n_pairs, int64_t* n_h
 int pulsar_shade_forward(pulsar_ctx_t ctx, const float* features, const float* params,
                          float* rgb, void* stream);
 
+/* Gradients of L = sum_p <grad_rgb_p, y_p> for the shading above, on the
+ * tensor cores (the same bf16 operands; the roundings are passed straight
+ * through):
+ *   g2 = (W3^T dY) * [z2 > 0],  g1 = (W2^T g2) * [z1 > 0],  dF = (W1^T g1)[:16],
+ *   dW1 = sum_p g1 x^T, db1 = sum_p g1, dW2 = sum_p g2 h1^T, db2 = sum_p g2,
+ *   dW3 = sum_p dY h2^T, db3 = sum_p dY   (z the pre-activations),
+ * with dY, g2, g1 rounded to bfloat16 where they enter a product.
+ *   features      [K,H,W,16]  as for pulsar_shade_forward (16-byte aligned)
+ *   params        [5635]      as for pulsar_shade_forward
+ *   grad_rgb      [K,H,W,3]   dL/d rgb
+ *   grad_features [K,H,W,16]  output dL/dF, overwritten; 16-byte aligned;
+ *                             NULL skips it
+ *   grad_params   [5635]      output dL/d params, overwritten (same layout as
+ *                             params; summed in a fixed order: reproducible)
+ * Errors as for pulsar_shade_forward (PULSAR_ERR_ARG also for NULL grad_rgb
+ * or grad_params and a misaligned grad_features). */
+int pulsar_shade_backward(pulsar_ctx_t ctx, const float* features, const float* params,
+                          const float* grad_rgb, float* grad_features, float* grad_params,
+                          void* stream);
+
 /* Static string for an error code. */
 const char* pulsar_strerror(int code);
 

@@ -106,7 +106,8 @@ def forward(features, cam, params, exact: bool = False) -> dict:
 def backward(features, cam, params, grad_y, exact: bool = False) -> dict:
     """Gradients of L = sum_p <grad_y_p, y_p>: dF [H*W, 16] and the flat
     weight gradient (same layout as params), plus their per-entry sums of
-    absolute per-pixel contributions (the scale of any summation's rounding)."""
+    absolute per-pixel contributions (the scale of any summation's rounding),
+    the rounded dY and the unrounded g2, g1 (where a rounding decision lies)."""
     P = unpack(params)
     fw = forward(features, cam, params, exact)
     W1, W2, W3 = (_q(P[k], exact) for k in ("W1", "W2", "W3"))
@@ -122,4 +123,4 @@ def backward(features, cam, params, grad_y, exact: bool = False) -> dict:
                 W2=np.abs(g2q).T @ np.abs(fw["h1"]), b2=np.abs(g2q).sum(0),
                 W3=np.abs(dy).T @ np.abs(fw["h2"]), b3=np.abs(dy).sum(0))
     return dict(grad_features=dx[:, :N_FEAT], grad_params=pack(grads), abs_params=pack(absg),
-                abs_features=np.abs(g1q) @ np.abs(W1)[:, :N_FEAT], **fw)
+                abs_features=np.abs(g1q) @ np.abs(W1)[:, :N_FEAT], dy=dy, g2=g2, g1=g1, **fw)

@@ -24,6 +24,7 @@ struct pulsar_ctx {
     Frames frames{};                   // the cameras of the current frame
     int n_cams = 0;
     int n_sms = 1;
+    ShadeLaunch shade{};
     const float* pos = nullptr;        // inputs of the current frame
     int stage = 0;                     // 0 none, 1 projected, 2 binned, 3 forward done
     bool counts_dirty = false;         // tile counts hold a frame that was never binned
@@ -137,9 +138,12 @@ int pulsar_create_cams(pulsar_ctx_t* out, int device, int64_t max_spheres, int64
               alloc(c, &w.kpart, K * B * 4) && alloc(c, &w.rtpart, (N + 255) / 256 * K * 12) &&
               alloc(c, &w.state, 1);
     if (ok) ok = cudaMallocHost(&c->host_state, sizeof(DevState)) == cudaSuccess;
-    if (ok) ok = prepare_forward() == cudaSuccess && prepare_shade() == cudaSuccess;
+    if (ok) ok = prepare_forward() == cudaSuccess && prepare_shade(&c->shade) == cudaSuccess;
     if (ok) ok = cudaDeviceGetAttribute(&c->n_sms, cudaDevAttrMultiProcessorCount, device) ==
                  cudaSuccess;
+    if (ok)
+        ok = alloc(c, &w.shade_part, (size_t)c->shade.bwd_per_sm * c->n_sms * kShadeParams) &&
+             alloc(c, &w.shade_img, shade_image_bytes());
     // zero-between-frames invariants
     if (ok)
         ok = cudaMemset(w.gacc, 0, K * N * sizeof(float4)) == cudaSuccess &&
@@ -276,8 +280,23 @@ int pulsar_shade_forward(pulsar_ctx_t c, const float* features, const float* par
     if (c->stage < 1) return PULSAR_ERR_STATE;
     if (c->frames.f[0].channels != 16) return PULSAR_ERR_ARG;
     DeviceGuard guard(c->device);
-    return cuda_err(launch_shade_forward(c->frames, c->ws, features, params, rgb, c->n_sms,
-                                         as_stream(stream)));
+    return cuda_err(launch_shade_forward(c->frames, c->ws, features, params, rgb,
+                                         c->shade.fwd_per_sm * c->n_sms, as_stream(stream)));
+}
+
+int pulsar_shade_backward(pulsar_ctx_t c, const float* features, const float* params,
+                          const float* grad_rgb, float* grad_features, float* grad_params,
+                          void* stream) {
+    if (!c || !features || !params || !grad_rgb || !grad_params) return PULSAR_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(features) & 15u) != 0 ||
+        (reinterpret_cast<uintptr_t>(grad_features) & 15u) != 0)
+        return PULSAR_ERR_ARG;
+    if (c->stage < 1) return PULSAR_ERR_STATE;
+    if (c->frames.f[0].channels != 16) return PULSAR_ERR_ARG;
+    DeviceGuard guard(c->device);
+    return cuda_err(launch_shade_backward(c->frames, c->ws, features, params, grad_rgb,
+                                          grad_features, grad_params,
+                                          c->shade.bwd_per_sm * c->n_sms, as_stream(stream)));
 }
 
 int pulsar_status(pulsar_ctx_t c, void* stream, int64_t* n_pairs, int64_t* n_hits) {

@@ -17,6 +17,7 @@ constexpr int kTilePix = kTile * kTile;
 constexpr int kMaxTrack = 16;
 constexpr int kMaxChannels = 64;
 constexpr int kMaxCams = 8;         // cameras of one batched frame
+constexpr int kShadeParams = 5635;  // shading MLP: W1 [64,19], b1, W2 [64,64], b2, W3 [3,64], b3
 constexpr uint32_t kFlagKeep = 1u, kFlagFloor = 2u, kFlagCut = 4u;   // per-sphere record flags
 constexpr uint32_t kParamNormalize = 4u;   // Frame::flags bit: normalised gradients
 constexpr uint32_t kParamGaussian = 8u;    // Frame::flags bit: Gaussian footprint
@@ -352,6 +353,9 @@ struct Workspace {
     float2* kpart;          // [4][maxB] per-tile partial dL/d(fx, fy, cx, cy), float pairs
     float2* rtpart;         // [cameras][12][finalize blocks] per-block partial dL/dR, dL/dt,
                             // float pairs
+    float* shade_part;      // [CTAs][kShadeParams] per-CTA weight-gradient shares of the
+                            // shading backward
+    unsigned char* shade_img;   // the shading weights as the kernels stage them (bf16)
     DevState* state;
 };
 
@@ -415,9 +419,19 @@ cudaError_t prepare_forward();   // opt the forward kernels into their shared me
 cudaError_t launch_forward(const Frames& fs, const Workspace& w, const float* features,
                            const float* bg, float* image, int max_pairs_stride,
                            cudaStream_t stream);
-cudaError_t prepare_shade();   // opt the shading kernels into their shared memory
+// resident CTAs per SM of the shading kernels (their grid caps are these x SMs)
+struct ShadeLaunch {
+    int fwd_per_sm = 0, bwd_per_sm = 0;
+};
+cudaError_t prepare_shade(ShadeLaunch* sl);
+size_t shade_image_bytes();   // bytes of Workspace::shade_img   // opt the shading kernels into their shared memory
 cudaError_t launch_shade_forward(const Frames& fs, const Workspace& w, const float* features,
-                                 const float* params, float* rgb, int n_sms, cudaStream_t stream);
+                                 const float* params, float* rgb, int grid_cap,
+                                 cudaStream_t stream);
+cudaError_t launch_shade_backward(const Frames& fs, const Workspace& w, const float* features,
+                                  const float* params, const float* grad_rgb,
+                                  float* grad_features, float* grad_params, int grid_cap,
+                                  cudaStream_t stream);
 cudaError_t launch_backward(const Frames& fs, const Workspace& w, const float* pos,
                             const float* features, const float* image, const float* grad_image,
                             float* grad_pos, float* grad_radius, float* grad_opacity,

@@ -1,24 +1,30 @@
 // Per-pixel neural shading (Pulsar Sec. 3.3: a per-pixel network turns the
 // rendered feature map into RGB; Sec. 5.2: a shared per-pixel fully
 // connected model conditioned on the view direction) on the 5th-generation
-// tensor cores.
+// tensor cores, forward and backward.
 //
 //   x  = [F_p (16 channels), v_p (unit view direction)]
 //   h1 = ReLU(W1 x + b1), h2 = ReLU(W2 h1 + b2), y = W3 h2 + b3
 //   (19 -> 64 -> 64 -> 3; matrix operands bfloat16, fp32 accumulation,
 //   fp32 biases)
 //
-// k_shade_forward  persistent CTAs of 128 threads, one 128-pixel tile at a
-//     time, one thread per pixel: the thread writes its pixel's bf16 inputs
-//     into the tile's A operand in shared memory (no-swizzle K-major layout:
-//     8-row x 16-byte core matrices, 128 B apart along K), one thread issues
-//     the layer's tcgen05.mma (M = 128, K = 16 per instruction) into the
-//     CTA's tensor memory and commits to an mbarrier, and every thread reads
-//     its row back with tcgen05.ld, adds the bias, applies the ReLU and
-//     writes the next layer's A operand.  Weights are staged once per CTA as
-//     the B operands (N x K, K-major).  Every mbarrier wait is bounded: on
-//     timeout the CTA latches an error, stops issuing and frees its tensor
-//     memory.
+// Both kernels run persistent CTAs of 128 threads over 128-pixel tiles, one
+// thread per pixel (one row of M = 128).  A thread writes its row of a
+// layer's A operand into shared memory (no-swizzle K-major layout: 8-row x
+// 16-byte core matrices), one thread issues the layer's tcgen05.mma into the
+// CTA's tensor memory and commits to an mbarrier, and every thread reads its
+// row of the accumulator back with tcgen05.ld for the epilogue (bias, ReLU,
+// bf16 rounding) that writes the next operand.  Weights are staged once per
+// CTA as B operands (N x K, K-major).  Every mbarrier wait is bounded: on
+// timeout the CTA latches an error, stops issuing and frees its tensor
+// memory.
+//
+// The backward contracts over pixels for the weight gradients: the
+// activation tiles the thread rows wrote (pixel x unit, K-major) are the
+// same bytes as (unit x pixel) MN-major operands, so the MMA reads them in
+// place and accumulates the CTA's share of dW in tensor memory across all
+// its tiles; a ones column in the x and h2 tiles turns the same MMAs into
+// the bias gradients.
 #include "pulsar_internal.cuh"
 
 #include <cuda_bf16.h>
@@ -26,12 +32,19 @@
 namespace pulsar {
 namespace {
 
-constexpr int kShadeThreads = 128;   // one thread per pixel of a tile (M = 128)
+constexpr int kRows = 128;           // pixels per tile (M = 128), one thread each
 constexpr int kIn = 32;              // 19 inputs, zero padded to two K = 16 steps
 constexpr int kHid = 64;
 constexpr int kOutPad = 16;          // 3 outputs padded to the smallest N for M = 128
-constexpr int kTmemCols = 128;       // D1 / D3 in columns 0.., D2 in 64..
 constexpr uint32_t kWaitLimit = 1u << 24;
+
+// flat parameter layout: W1 [64][19], b1 [64], W2 [64][64], b2 [64], W3 [3][64], b3 [3]
+constexpr int kOffB1 = kHid * 19;
+constexpr int kOffW2 = kOffB1 + kHid;
+constexpr int kOffB2 = kOffW2 + kHid * kHid;
+constexpr int kOffW3 = kOffB2 + kHid;
+constexpr int kOffB3 = kOffW3 + 3 * kHid;
+static_assert(kOffB3 + 3 == kShadeParams, "shading parameter layout");
 
 // ------------------------------------------------------------ tcgen05 --
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -39,18 +52,19 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 }
 
 // Shared-memory matrix descriptor, no swizzle: start address, the byte offset
-// of the next core matrix along K (lbo) and along M/N (sbo), descriptor
-// version 1 (bit 46).
+// between core matrices along K (lbo) and along M/N (sbo) -- the same roles
+// for K-major and MN-major operands -- and descriptor version 1 (bit 46).
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
 }
 
-// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
-// K-major, N >> 3 at bit 17, M >> 4 at bit 24.
-__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
-           ((uint32_t)(m >> 4) << 24);
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B,
+// K-major unless mn_major (bits 15 and 16 mark A and B MN-major), N >> 3 at
+// bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, bool mn_major = false) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (mn_major ? (3u << 15) : 0u) |
+           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
@@ -84,9 +98,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity) {
 }
 
 // 16 consecutive fp32 columns of this thread's TMEM lane (warp w owns lanes
-// 32w .. 32w + 31).
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
+// 32w .. 32w + 31); the values are valid after tmem_wait_ld().
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
         "%14,%15}, [%16];"
@@ -94,9 +107,9 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
           "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -108,6 +121,25 @@ __device__ __forceinline__ void tc_fence_after() {
 // generic-proxy shared-memory writes become visible to the tensor cores
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// The operands the threads wrote are complete, and every thread's earlier
+// tensor-memory reads are ordered before the MMAs issued next.
+__device__ __forceinline__ void operands_ready() {
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* s_taddr, uint32_t cols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(s_taddr)),
+                 "r"(cols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols));
 }
 
 // Byte offset of element (row, k) in a no-swizzle K-major operand with K
@@ -129,46 +161,25 @@ __device__ __forceinline__ uint4 pack8(const float* v) {
     return u;
 }
 
-struct ShadeSmem {
-    static constexpr int w1 = 0;                                   // B [64 x 32]
-    static constexpr int w2 = w1 + kHid * kIn * 2;                 // B [64 x 64]
-    static constexpr int w3 = w2 + kHid * kHid * 2;                // B [16 x 64]
-    static constexpr int x = w3 + kOutPad * kHid * 2;              // A [128 x 32]
-    static constexpr int h1 = x + kShadeThreads * kIn * 2;         // A [128 x 64]
-    static constexpr int h2 = h1 + kShadeThreads * kHid * 2;       // A [128 x 64]
-    static constexpr int bias = h2 + kShadeThreads * kHid * 2;     // fp32 b1[64] b2[64] b3[16]
-    static constexpr int mbar = bias + (2 * kHid + kOutPad) * 4;   // u64
-    static constexpr int taddr = mbar + 8;                         // u32
-    static constexpr int bytes = taddr + 8;
-};
+__device__ __forceinline__ void put8(unsigned char* tile, int row, int k, int K, const float* v) {
+    *reinterpret_cast<uint4*>(tile + kmajor_off(row, k, K)) = pack8(v);
+}
 
-// Stage the weights as B operands (N x K, K-major, zero padded) and the biases.
-__device__ void stage_weights(unsigned char* smem, const float* __restrict__ params) {
-    using L = ShadeSmem;
-    const float* W1 = params;                        // [64][19]
-    const float* b1 = W1 + kHid * 19;
-    const float* W2 = b1 + kHid;                     // [64][64]
-    const float* b2 = W2 + kHid * kHid;
-    const float* W3 = b2 + kHid;                     // [3][64]
-    const float* b3 = W3 + 3 * kHid;
-    __nv_bfloat16* s1 = reinterpret_cast<__nv_bfloat16*>(smem + L::w1);
-    __nv_bfloat16* s2 = reinterpret_cast<__nv_bfloat16*>(smem + L::w2);
-    __nv_bfloat16* s3 = reinterpret_cast<__nv_bfloat16*>(smem + L::w3);
-    for (int e = threadIdx.x; e < kHid * kIn; e += blockDim.x) {
-        const int n = e / kIn, k = e % kIn;
-        s1[kmajor_off(n, k, kIn) / 2] = __float2bfloat16_rn(k < 19 ? W1[n * 19 + k] : 0.0f);
-    }
-    for (int e = threadIdx.x; e < kHid * kHid; e += blockDim.x) {
-        const int n = e / kHid, k = e % kHid;
-        s2[kmajor_off(n, k, kHid) / 2] = __float2bfloat16_rn(W2[n * kHid + k]);
-    }
-    for (int e = threadIdx.x; e < kOutPad * kHid; e += blockDim.x) {
-        const int n = e / kHid, k = e % kHid;
-        s3[kmajor_off(n, k, kHid) / 2] = __float2bfloat16_rn(n < 3 ? W3[n * kHid + k] : 0.0f);
-    }
-    float* sb = reinterpret_cast<float*>(smem + L::bias);
-    for (int e = threadIdx.x; e < 2 * kHid + kOutPad; e += blockDim.x)
-        sb[e] = e < kHid ? b1[e] : (e < 2 * kHid ? b2[e - kHid] : (e - 2 * kHid < 3 ? b3[e - 2 * kHid] : 0.0f));
+// Bulk copy (TMA engine) of `bytes` bytes global -> shared, completing on mbar.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* mbar) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(mbar)),
+                 "r"(bytes)
+                 : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(mbar))
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* mbar) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(mbar)));
 }
 
 // The pixel's unit view direction (camera space) from its camera.
@@ -187,172 +198,614 @@ __device__ __forceinline__ void view_dir(const Frame& f, uint32_t local, float* 
     v[2] = inv;
 }
 
-__global__ void __launch_bounds__(kShadeThreads)
+__device__ __forceinline__ void load_features(const float* __restrict__ features, uint64_t p,
+                                              bool valid, float4 (&f)[4]) {
+    const float4* fp = reinterpret_cast<const float4*>(features + p * 16);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) f[q] = valid ? fp[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// Layer input row: 16 features, the view direction, ones at columns 19-21,
+// zeros.  The ones meet the three bf16 parts of each bias in the B operands
+// (the tensor cores add the fp32 bias exactly, inside the fp32 sum), and
+// column 19 turns the backward's weight-gradient contraction into the bias
+// gradient.
+__device__ __forceinline__ void input_row(const Frames& fs, uint32_t P1, uint64_t p, bool valid,
+                                          const float4 (&f)[4], float (&in)[kIn]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        in[4 * q] = f[q].x;
+        in[4 * q + 1] = f[q].y;
+        in[4 * q + 2] = f[q].z;
+        in[4 * q + 3] = f[q].w;
+    }
+#pragma unroll
+    for (int k = 16; k < kIn; ++k) in[k] = (k >= 19 && k <= 21) ? 1.0f : 0.0f;
+    if (valid) {
+        const uint32_t cam = (uint32_t)(p / P1);
+        view_dir(fs.f[cam], (uint32_t)(p - (uint64_t)cam * P1), in + 16);
+    }
+}
+
+// Two fp32 values as one bf16x2 word (the first in the low half), rounded to
+// nearest even; the relu form turns negative values into 0.
+__device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+__device__ __forceinline__ uint32_t bf16x2_relu(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.relu.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+// 0xFFFF in each half of a bf16x2 word of ReLU outputs that is not +-0, else
+// 0: the magnitude plus 0x7FFF carries into the half's top bit exactly when
+// it is non-zero, and prmt replicates that bit across the half.
+__device__ __forceinline__ uint32_t nonzero_mask(uint32_t h) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, 0, 0xBB99;" : "=r"(d) : "r"((h & 0x7FFF7FFFu) + 0x7FFF7FFFu));
+    return d;
+}
+
+__device__ __forceinline__ void st_row16(unsigned char* tile, int row, int k, int K,
+                                         const uint32_t* w) {
+    *reinterpret_cast<uint4*>(tile + kmajor_off(row, k, K)) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Hidden layer epilogue: h = bf16(ReLU(D)) (D holds the bias) of this
+// thread's row into columns k0 .. k0 + 63 of a K-column A operand; the bf16x2
+// words stay in h for the backward's ReLU masks.
+__device__ __forceinline__ void relu_row(uint32_t taddr, unsigned char* tile, int row, int K,
+                                         int k0, uint32_t (&h)[kHid / 2]) {
+#pragma unroll
+    for (int c0 = 0; c0 < kHid; c0 += 32) {
+        uint32_t r[2][16];
+        tmem_ld16(taddr + (uint32_t)c0, r[0]);
+        tmem_ld16(taddr + (uint32_t)(c0 + 16), r[1]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            h[c0 / 2 + j] = bf16x2_relu(__uint_as_float(r[j / 8][(2 * j) % 16]),
+                                        __uint_as_float(r[j / 8][(2 * j + 1) % 16]));
+#pragma unroll
+        for (int q = 0; q < 4; ++q) st_row16(tile, row, k0 + c0 + 8 * q, K, h + c0 / 2 + 4 * q);
+    }
+}
+
+// Backward epilogue: Q(D * [h > 0]) of this thread's row into columns
+// k0 .. k0 + 63 (h: the layer's ReLU output words).
+__device__ __forceinline__ void masked_row(uint32_t taddr, const uint32_t (&h)[kHid / 2],
+                                           unsigned char* tile, int row, int K, int k0) {
+#pragma unroll
+    for (int c0 = 0; c0 < kHid; c0 += 32) {
+        uint32_t r[2][16];
+        tmem_ld16(taddr + (uint32_t)c0, r[0]);
+        tmem_ld16(taddr + (uint32_t)(c0 + 16), r[1]);
+        tmem_wait_ld();
+        uint32_t g[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            g[j] = bf16x2(__uint_as_float(r[j / 8][(2 * j) % 16]),
+                          __uint_as_float(r[j / 8][(2 * j + 1) % 16])) &
+                   nonzero_mask(h[c0 / 2 + j]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) st_row16(tile, row, k0 + c0 + 8 * q, K, g + 4 * q);
+    }
+}
+
+// ================================================================ weights --
+// The weights as the kernels hold them in shared memory: bf16 B operands
+// (N x K, K-major, zero padded), one image per kernel, written once per call
+// and bulk-copied by every CTA.  Each fp32 bias b is split exactly into three
+// bf16 parts (b = hi + mid + lo: 8 + 8 + 8 significant bits) placed where the
+// A operand holds ones: columns 19-21 of layer 1's x, and for layers 2 and 3
+// an extra K step over x's columns 16-31 (view direction, ones, zeros) in
+// front of the hidden units.
+constexpr int kKB = 16 + kHid;   // layers 2, 3: the bias K step, then the 64 units
+
+struct FwdImage {   // W1 | b1 [64 x 32], b2 | W2 [64 x 80], b3 | W3 [16 x 80]
+    static constexpr int w1 = 0;
+    static constexpr int w2 = w1 + kHid * kIn * 2;
+    static constexpr int w3 = w2 + kHid * kKB * 2;
+    static constexpr int bytes = w3 + kOutPad * kKB * 2;
+};
+struct BwdImage {   // W1 | b1, b2 | W2, W3^T [64 x 16], W2^T [64 x 64], W1^T [16 x 64]
+    static constexpr int w1 = 0;
+    static constexpr int w2 = w1 + kHid * kIn * 2;
+    static constexpr int w3t = w2 + kHid * kKB * 2;
+    static constexpr int w2t = w3t + kHid * 16 * 2;
+    static constexpr int w1t = w2t + kHid * kHid * 2;
+    static constexpr int bytes = w1t + 16 * kHid * 2;
+};
+static_assert(FwdImage::bytes % 16 == 0 && BwdImage::bytes % 16 == 0, "bulk copy sizes");
+constexpr int kImageBytes = FwdImage::bytes + BwdImage::bytes;
+
+// Part i (0 hi, 1 mid, 2 lo) of the exact three-way bf16 split of b (each
+// remainder is exact in fp32).
+__device__ __forceinline__ float bias_part(float b, int i) {
+    const float hi = __bfloat162float(__float2bfloat16_rn(b));
+    if (i == 0) return hi;
+    const float r = b - hi;
+    const float mid = __bfloat162float(__float2bfloat16_rn(r));
+    return i == 1 ? mid : r - mid;
+}
+
+enum Operand { kW1b, kW2b, kW3b, kW3t, kW2t, kW1t };
+
+// Element (n, k) of a B operand.
+__device__ float operand_value(Operand o, int n, int k, const float* __restrict__ prm) {
+    const float* W1 = prm;
+    const float* W2 = prm + kOffW2;
+    const float* W3 = prm + kOffW3;
+    switch (o) {
+        case kW1b:   // [64 x 32]: W1 (19), the parts of b1, zeros
+            return k < 19 ? W1[n * 19 + k] : (k <= 21 ? bias_part(prm[kOffB1 + n], k - 19) : 0.0f);
+        case kW2b:   // [64 x 80]: parts of b2 at 3-5 of the bias step, then W2
+            return k >= 16 ? W2[n * kHid + k - 16]
+                           : (k >= 3 && k <= 5 ? bias_part(prm[kOffB2 + n], k - 3) : 0.0f);
+        case kW3b:   // [16 x 80]: rows 0-2 as kW2b with b3 and W3
+            if (n >= 3) return 0.0f;
+            return k >= 16 ? W3[n * kHid + k - 16]
+                           : (k >= 3 && k <= 5 ? bias_part(prm[kOffB3 + n], k - 3) : 0.0f);
+        case kW3t: return k < 3 ? W3[k * kHid + n] : 0.0f;   // [64 x 16]
+        case kW2t: return W2[k * kHid + n];                   // [64 x 64]
+        default:   return W1[k * 19 + n];                     // [16 x 64] kW1t
+    }
+}
+
+struct PackSeg {
+    int offset, rows, K;
+    Operand o;
+};
+__device__ constexpr PackSeg kPack[] = {
+    {FwdImage::w1, kHid, kIn, kW1b},
+    {FwdImage::w2, kHid, kKB, kW2b},
+    {FwdImage::w3, kOutPad, kKB, kW3b},
+    {FwdImage::bytes + BwdImage::w1, kHid, kIn, kW1b},
+    {FwdImage::bytes + BwdImage::w2, kHid, kKB, kW2b},
+    {FwdImage::bytes + BwdImage::w3t, kHid, 16, kW3t},
+    {FwdImage::bytes + BwdImage::w2t, kHid, kHid, kW2t},
+    {FwdImage::bytes + BwdImage::w1t, 16, kHid, kW1t},
+};
+constexpr int kPackElems = kHid * kIn * 2 + kHid * kKB * 2 + kOutPad * kKB + kHid * 16 +
+                           kHid * kHid + 16 * kHid;
+
+__global__ void k_shade_pack(const float* __restrict__ params, unsigned char* __restrict__ img) {
+    int e = blockIdx.x * blockDim.x + threadIdx.x;
+#pragma unroll
+    for (int s = 0; s < (int)(sizeof(kPack) / sizeof(kPack[0])); ++s) {
+        const PackSeg g = kPack[s];
+        if (e < g.rows * g.K) {
+            const int n = e / g.K, k = e % g.K;
+            reinterpret_cast<__nv_bfloat16*>(img + g.offset)[kmajor_off(n, k, g.K) / 2] =
+                __float2bfloat16_rn(operand_value(g.o, n, k, params));
+            return;
+        }
+        e -= g.rows * g.K;
+    }
+}
+
+// ================================================================ forward --
+constexpr int kFwdCols = 64;   // every layer's accumulator at column 0
+constexpr int kXH = kIn + kHid;   // A tile columns: x (32), then the hidden units (64)
+
+struct FwdSmem {
+    static constexpr int act = 0;                         // A [128 x 96]: x | h1, then x | h2
+    static constexpr int img = act + kRows * kXH * 2;     // FwdImage
+    static constexpr int w1 = img + FwdImage::w1;
+    static constexpr int w2 = img + FwdImage::w2;
+    static constexpr int w3 = img + FwdImage::w3;
+    static constexpr int mbar = img + FwdImage::bytes;    // u64: MMA completion
+    static constexpr int wbar = mbar + 8;                 // u64: weights landed
+    static constexpr int taddr = wbar + 8;                // u32
+    static constexpr int bytes = taddr + 8;
+};
+
+// Issue one layer: D = A[:, a_k0 .. a_k0 + K) B^T over K / 16 steps (A rows
+// are kXH columns wide; B is N x K).
+__device__ __forceinline__ void issue_layer(uint32_t d, uint32_t a, int a_k0, int a_cols,
+                                            uint32_t b, int K, int N) {
+    for (int k0 = 0; k0 < K; k0 += 16)
+        mma_bf16(d, smem_desc(a + ((a_k0 + k0) / 8) * 128, 128, (a_cols / 8) * 128),
+                 smem_desc(b + (k0 / 8) * 128, 128, (K / 8) * 128), idesc_bf16(kRows, N), k0 > 0);
+}
+
+__global__ void __launch_bounds__(kRows)
 k_shade_forward(Frames fs, Workspace w, const float* __restrict__ features,
-                const float* __restrict__ params, float* __restrict__ rgb) {
-    using L = ShadeSmem;
+                const unsigned char* __restrict__ img, float* __restrict__ rgb) {
+    using L = FwdSmem;
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + L::mbar);
+    uint64_t* wbar = reinterpret_cast<uint64_t*>(smem + L::wbar);
     uint32_t* s_taddr = reinterpret_cast<uint32_t*>(smem + L::taddr);
-    const float* sb = reinterpret_cast<const float*>(smem + L::bias);
     const int tid = threadIdx.x, warp = tid >> 5;
     const Frame& f0 = fs.f[0];
-    const uint32_t n_pix = f0.pix_all;
+    const uint64_t n_pix = f0.pix_all;
     const uint32_t P1 = (uint32_t)(f0.width * f0.height);
-    const uint32_t n_tiles = (n_pix + kShadeThreads - 1) / kShadeThreads;
+    const uint32_t n_tiles = (uint32_t)((n_pix + kRows - 1) / kRows);
+    const uint64_t stride = (uint64_t)gridDim.x * kRows;
 
-    stage_weights(smem, params);
-    if (tid == 0) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(mbar)));
-    if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_u32(s_taddr)),
-                     "r"(kTmemCols));
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    if (tid == 0) {
+        mbar_init(mbar);
+        mbar_init(wbar);
+        fence_async_smem();
+        bulk_load(smem + L::img, img, FwdImage::bytes, wbar);
     }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
+    if (warp == 0) tmem_alloc(s_taddr, kFwdCols);
+    operands_ready();
     const uint32_t tmem = *s_taddr;
-    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;   // this warp's TMEM lanes
-    const uint32_t sx = smem_u32(smem + L::x), sh1 = smem_u32(smem + L::h1),
-                   sh2 = smem_u32(smem + L::h2);
+    const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);   // this warp's TMEM lanes
+    const uint32_t sact = smem_u32(smem + L::act);
     const uint32_t sw1 = smem_u32(smem + L::w1), sw2 = smem_u32(smem + L::w2),
                    sw3 = smem_u32(smem + L::w3);
     uint32_t phase = 0;
     bool ok = true;
+    uint32_t h[kHid / 2];
 
-    for (uint32_t tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-        const uint32_t p = tile * kShadeThreads + tid;
+    uint64_t p = (uint64_t)blockIdx.x * kRows + tid;
+    float4 fcur[4];
+    load_features(features, p, p < n_pix, fcur);
+    ok = __syncthreads_and(mbar_wait(wbar, 0));   // the weights are in
+    for (uint32_t tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, p += stride) {
         const bool valid = p < n_pix;
-        // ---- layer 1 input: 16 features and the view direction, bf16
         {
             float in[kIn];
+            input_row(fs, P1, p, valid, fcur, in);
 #pragma unroll
-            for (int k = 0; k < kIn; ++k) in[k] = 0.0f;
-            if (valid) {
-                const float4* fp = reinterpret_cast<const float4*>(features + (size_t)p * 16);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float4 t = fp[q];
-                    in[4 * q] = t.x;
-                    in[4 * q + 1] = t.y;
-                    in[4 * q + 2] = t.z;
-                    in[4 * q + 3] = t.w;
-                }
-                const uint32_t cam = p / P1;
-                view_dir(fs.f[cam], p - cam * P1, in + 16);
-            }
-#pragma unroll
-            for (int j = 0; j < kIn / 8; ++j)
-                *reinterpret_cast<uint4*>(smem + L::x + kmajor_off(tid, 8 * j, kIn)) = pack8(in + 8 * j);
+            for (int j = 0; j < kIn / 8; ++j) put8(smem + L::act, tid, 8 * j, kXH, in + 8 * j);
         }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
+        // the next tile's features load while this tile runs through the tensor cores
+        load_features(features, p + stride, p + stride < n_pix, fcur);
+        operands_ready();
         if (tid == 0) {
-            for (int k0 = 0; k0 < kIn; k0 += 16)
-                mma_bf16(tmem, smem_desc(sx + (k0 / 8) * 128, 128, (kIn / 8) * 128),
-                         smem_desc(sw1 + (k0 / 8) * 128, 128, (kIn / 8) * 128),
-                         idesc_bf16(128, kHid), k0 > 0);
+            issue_layer(tmem, sact, 0, kXH, sw1, kIn, kHid);
             mma_commit(mbar);
         }
         ok = __syncthreads_and(mbar_wait(mbar, phase & 1));   // one decision for all
         ++phase;
         tc_fence_after();
         if (!ok) break;
-        // ---- h1 = ReLU(D1 + b1) -> A of layer 2
-#pragma unroll
-        for (int c0 = 0; c0 < kHid; c0 += 16) {
-            float v[16];
-            tmem_ld16(tmem + lane_base + (uint32_t)c0, v);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = fmaxf(v[j] + sb[c0 + j], 0.0f);
-            *reinterpret_cast<uint4*>(smem + L::h1 + kmajor_off(tid, c0, kHid)) = pack8(v);
-            *reinterpret_cast<uint4*>(smem + L::h1 + kmajor_off(tid, c0 + 8, kHid)) = pack8(v + 8);
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
+        relu_row(trow, smem + L::act, tid, kXH, kIn, h);   // h1 (layer 1 is complete)
+        operands_ready();
         if (tid == 0) {
-            for (int k0 = 0; k0 < kHid; k0 += 16)
-                mma_bf16(tmem + kHid, smem_desc(sh1 + (k0 / 8) * 128, 128, (kHid / 8) * 128),
-                         smem_desc(sw2 + (k0 / 8) * 128, 128, (kHid / 8) * 128),
-                         idesc_bf16(128, kHid), k0 > 0);
+            issue_layer(tmem, sact, 16, kXH, sw2, kKB, kHid);
             mma_commit(mbar);
         }
-        ok = __syncthreads_and(mbar_wait(mbar, phase & 1));   // one decision for all
+        ok = __syncthreads_and(mbar_wait(mbar, phase & 1));
         ++phase;
         tc_fence_after();
         if (!ok) break;
-        // ---- h2 = ReLU(D2 + b2) -> A of layer 3
-#pragma unroll
-        for (int c0 = 0; c0 < kHid; c0 += 16) {
-            float v[16];
-            tmem_ld16(tmem + lane_base + (uint32_t)(kHid + c0), v);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = fmaxf(v[j] + sb[kHid + c0 + j], 0.0f);
-            *reinterpret_cast<uint4*>(smem + L::h2 + kmajor_off(tid, c0, kHid)) = pack8(v);
-            *reinterpret_cast<uint4*>(smem + L::h2 + kmajor_off(tid, c0 + 8, kHid)) = pack8(v + 8);
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
+        relu_row(trow, smem + L::act, tid, kXH, kIn, h);   // h2 replaces h1 (layer 2 is complete)
+        operands_ready();
         if (tid == 0) {
-            for (int k0 = 0; k0 < kHid; k0 += 16)
-                mma_bf16(tmem, smem_desc(sh2 + (k0 / 8) * 128, 128, (kHid / 8) * 128),
-                         smem_desc(sw3 + (k0 / 8) * 128, 128, (kHid / 8) * 128),
-                         idesc_bf16(128, kOutPad), k0 > 0);
+            issue_layer(tmem, sact, 16, kXH, sw3, kKB, kOutPad);
             mma_commit(mbar);
         }
-        ok = __syncthreads_and(mbar_wait(mbar, phase & 1));   // one decision for all
+        ok = __syncthreads_and(mbar_wait(mbar, phase & 1));
         ++phase;
         tc_fence_after();
         if (!ok) break;
-        // ---- y = D3 + b3
-        {
-            float v[16];
-            tmem_ld16(tmem + lane_base, v);
-            if (valid) {
+        // y = D3; the next tile's operand writes need no further barrier:
+        // layer 3 is complete and this row's accumulator is read here
+        uint32_t r[16];
+        tmem_ld16(trow, r);
+        tmem_wait_ld();
+        if (valid) {
 #pragma unroll
-                for (int o = 0; o < 3; ++o) rgb[(size_t)p * 3 + o] = v[o] + sb[2 * kHid + o];
-            }
+            for (int o = 0; o < 3; ++o) rgb[p * 3 + o] = __uint_as_float(r[o]);
         }
-        tc_fence_before();
-        __syncthreads();   // the tile's operands and accumulators are free
-        tc_fence_after();
     }
     if (!ok) {
-        // an MMA did not complete in time: report it, give it one more
-        // bounded wait, then release the tensor memory regardless
+        // a copy or an MMA did not complete in time: report it, give both
+        // one more bounded wait, then release the tensor memory regardless
         if (tid == 0) atomicOr(&w.state->error, kErrTimeout);
-        mbar_wait(mbar, (phase - 1) & 1);
+        mbar_wait(wbar, 0);
+        if (phase > 0) mbar_wait(mbar, (phase - 1) & 1);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"(kTmemCols));
+    if (warp == 0) tmem_dealloc(tmem, kFwdCols);
+}
+
+// =============================================================== backward --
+// Gradients of L = sum_p <dY_p, y_p>, straight through the bf16 roundings:
+//   g2 = (W3^T Q(dY)) * [z2 > 0],  g1 = (W2^T Q(g2)) * [z1 > 0],  dF = (W1^T Q(g1))[:16]
+//   rows 0..63 / 64..127 of  sum_p [Q(g1) ; Q(g2)] [Q(x), 1 | Q(h1)]^T  hold
+//     [dW1 | db1 | .] and [. | db2 | dW2]
+//   rows 0..63 / 64 of  sum_p [Q(h2) ; 1] Q(dY)^T  hold dW3^T and db3^T
+// ([z > 0] is read as [Q(ReLU(z)) != 0]: they differ only for 0 < z below
+// the smallest bfloat16, far inside the fp32 error of z.)
+constexpr int kBwdCols = 256;
+constexpr int kGG = 128;    // Q(g1) (64), Q(g2) (64)
+constexpr int kH2 = 72;     // Q(h2) (64), 1, zero pad
+constexpr int kDY = 16;     // Q(dY) (3), zero pad
+constexpr uint32_t kColZ1 = 0, kColZ2 = 64, kColG2 = 0, kColG1 = 64, kColDX = 0;
+constexpr uint32_t kColAccXH = 128;   // 96 columns
+constexpr uint32_t kColAccY = 224;    // 16 columns
+
+struct BwdSmem {
+    static constexpr int xh = 0;                            // [128 x 96]: x | h1
+    static constexpr int gg = xh + kRows * kXH * 2;         // [128 x 128]
+    static constexpr int h2 = gg + kRows * kGG * 2;         // [128 x 72]
+    static constexpr int dy = h2 + kRows * kH2 * 2;         // [128 x 16]
+    static constexpr int img = dy + kRows * kDY * 2;        // BwdImage
+    static constexpr int w1 = img + BwdImage::w1;
+    static constexpr int w2 = img + BwdImage::w2;
+    static constexpr int w3t = img + BwdImage::w3t;
+    static constexpr int w2t = img + BwdImage::w2t;
+    static constexpr int w1t = img + BwdImage::w1t;
+    static constexpr int mbar = img + BwdImage::bytes;      // u64: MMA completion
+    static constexpr int wbar = mbar + 8;                   // u64: weights landed
+    static constexpr int taddr = wbar + 8;
+    static constexpr int bytes = taddr + 8;
+};
+// Read MN-major, the [Q(h2) | 1] tile spans 16 groups of 8 units per pixel
+// group of which it holds 9: the last instruction's reads end 19328 bytes
+// from its start, inside the dy tile that follows.
+static_assert(BwdSmem::dy + kRows * kDY * 2 - BwdSmem::h2 >=
+                  7 * (2 * kH2 * 16) + 15 * 128 + kH2 * 16 + 128,
+              "MN-major read of the h2 tile stays inside shared memory");
+
+__global__ void __launch_bounds__(kRows, 2)
+k_shade_backward(Frames fs, Workspace w, const float* __restrict__ features,
+                 const unsigned char* __restrict__ img, const float* __restrict__ grad_rgb,
+                 float* __restrict__ grad_features, float* __restrict__ part) {
+    using L = BwdSmem;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + L::mbar);
+    uint64_t* wbar = reinterpret_cast<uint64_t*>(smem + L::wbar);
+    uint32_t* s_taddr = reinterpret_cast<uint32_t*>(smem + L::taddr);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const Frame& f0 = fs.f[0];
+    const uint64_t n_pix = f0.pix_all;
+    const uint32_t P1 = (uint32_t)(f0.width * f0.height);
+    const uint32_t n_tiles = (uint32_t)((n_pix + kRows - 1) / kRows);
+    const uint64_t stride = (uint64_t)gridDim.x * kRows;
+
+    {   // the constant [1, 0, ...] group of the h2 tile
+        const float one[8] = {1.0f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        put8(smem + L::h2, tid, kHid, kH2, one);
+    }
+    if (tid == 0) {
+        mbar_init(mbar);
+        mbar_init(wbar);
+        fence_async_smem();
+        bulk_load(smem + L::img, img, BwdImage::bytes, wbar);
+    }
+    if (warp == 0) tmem_alloc(s_taddr, kBwdCols);
+    operands_ready();
+    const uint32_t tmem = *s_taddr;
+    const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
+    const uint32_t sxh = smem_u32(smem + L::xh), sgg = smem_u32(smem + L::gg),
+                   sh2 = smem_u32(smem + L::h2), sdy = smem_u32(smem + L::dy);
+    const uint32_t sw1 = smem_u32(smem + L::w1), sw2 = smem_u32(smem + L::w2),
+                   sw3t = smem_u32(smem + L::w3t), sw2t = smem_u32(smem + L::w2t),
+                   sw1t = smem_u32(smem + L::w1t);
+    uint32_t phase = 0;
+    bool ok = true;
+    uint32_t acc = 0;   // 0 until the first tile's weight-gradient MMAs are issued
+    uint32_t h1[kHid / 2], h2[kHid / 2];
+
+    uint64_t p = (uint64_t)blockIdx.x * kRows + tid;
+    float4 fcur[4];
+    float dcur[3];
+    load_features(features, p, p < n_pix, fcur);
+#pragma unroll
+    for (int o = 0; o < 3; ++o) dcur[o] = p < n_pix ? grad_rgb[p * 3 + o] : 0.0f;
+    ok = __syncthreads_and(mbar_wait(wbar, 0));   // the weights are in
+    for (uint32_t tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, p += stride) {
+        const bool valid = p < n_pix;
+        {
+            float in[kIn];
+            input_row(fs, P1, p, valid, fcur, in);
+#pragma unroll
+            for (int j = 0; j < kIn / 8; ++j) put8(smem + L::xh, tid, 8 * j, kXH, in + 8 * j);
+            const uint32_t d[8] = {bf16x2(dcur[0], dcur[1]), bf16x2(dcur[2], 0.0f), 0u, 0u,
+                                   0u, 0u, 0u, 0u};
+            st_row16(smem + L::dy, tid, 0, kDY, d);
+            st_row16(smem + L::dy, tid, 8, kDY, d + 4);
+        }
+        {   // the next tile's inputs load while this tile runs through the tensor cores
+            const uint64_t pn = p + stride;
+            const bool vn = pn < n_pix;
+            load_features(features, pn, vn, fcur);
+#pragma unroll
+            for (int o = 0; o < 3; ++o) dcur[o] = vn ? grad_rgb[pn * 3 + o] : 0.0f;
+        }
+        operands_ready();
+        // ---- round 1: z1 = W1 Q(x) + b1
+        if (tid == 0) {
+            issue_layer(tmem + kColZ1, sxh, 0, kXH, sw1, kIn, kHid);
+            mma_commit(mbar);
+        }
+        ok = __syncthreads_and(mbar_wait(mbar, phase & 1));
+        ++phase;
+        tc_fence_after();
+        if (!ok) break;
+        relu_row(trow + kColZ1, smem + L::xh, tid, kXH, kIn, h1);
+        operands_ready();
+        // ---- round 2: z2 = W2 Q(h1) + b2, and W3^T Q(dY)
+        if (tid == 0) {
+            issue_layer(tmem + kColZ2, sxh, 16, kXH, sw2, kKB, kHid);
+            mma_bf16(tmem + kColG2, smem_desc(sdy, 128, (kDY / 8) * 128),
+                     smem_desc(sw3t, 128, (kDY / 8) * 128), idesc_bf16(kRows, kHid), 0);
+            mma_commit(mbar);
+        }
+        ok = __syncthreads_and(mbar_wait(mbar, phase & 1));
+        ++phase;
+        tc_fence_after();
+        if (!ok) break;
+        relu_row(trow + kColZ2, smem + L::h2, tid, kH2, 0, h2);
+        masked_row(trow + kColG2, h2, smem + L::gg, tid, kGG, kHid);   // Q(g2)
+        operands_ready();
+        // ---- round 3: W2^T Q(g2); accumulate [Q(h2) ; 1] Q(dY)^T over the tile's pixels
+        if (tid == 0) {
+            issue_layer(tmem + kColG1, sgg, kHid, kGG, sw2t, kHid, kHid);
+            // MN-major: groups of 8 units 128 B apart, groups of 8 pixels one
+            // row block of the tile apart; K = 16 pixels per instruction
+            for (int q = 0; q < kRows; q += 16)
+                mma_bf16(tmem + kColAccY,
+                         smem_desc(sh2 + (q / 8) * (kH2 / 8) * 128, (kH2 / 8) * 128, 128),
+                         smem_desc(sdy + (q / 8) * (kDY / 8) * 128, (kDY / 8) * 128, 128),
+                         idesc_bf16(kRows, kDY, true), acc | (uint32_t)(q > 0));
+            mma_commit(mbar);
+        }
+        ok = __syncthreads_and(mbar_wait(mbar, phase & 1));
+        ++phase;
+        tc_fence_after();
+        if (!ok) break;
+        masked_row(trow + kColG1, h1, smem + L::gg, tid, kGG, 0);   // Q(g1)
+        operands_ready();
+        // ---- round 4: dF = (W1^T Q(g1))[:16]; accumulate [Q(g1) ; Q(g2)] [Q(x), 1 | Q(h1)]^T
+        if (tid == 0) {
+            issue_layer(tmem + kColDX, sgg, 0, kGG, sw1t, kHid, 16);
+            for (int q = 0; q < kRows; q += 16)
+                mma_bf16(tmem + kColAccXH,
+                         smem_desc(sgg + (q / 8) * (kGG / 8) * 128, (kGG / 8) * 128, 128),
+                         smem_desc(sxh + (q / 8) * (kXH / 8) * 128, (kXH / 8) * 128, 128),
+                         idesc_bf16(kRows, kXH, true), acc | (uint32_t)(q > 0));
+            mma_commit(mbar);
+        }
+        acc = 1;
+        ok = __syncthreads_and(mbar_wait(mbar, phase & 1));
+        ++phase;
+        tc_fence_after();
+        if (!ok) break;
+        {
+            uint32_t r[16];
+            tmem_ld16(trow + kColDX, r);
+            tmem_wait_ld();
+            if (valid && grad_features) {
+                float4* gf = reinterpret_cast<float4*>(grad_features + p * 16);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    gf[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                        __uint_as_float(r[4 * q + 2]),
+                                        __uint_as_float(r[4 * q + 3]));
+            }
+        }
+    }
+    // ---- this CTA's share of the weight gradients: TMEM lane = output row
+    float* mine = part + (size_t)blockIdx.x * kShadeParams;
+    if (ok) {
+        const int m = tid & (kHid - 1);
+        const bool lower = tid < kHid;   // rows of Q(g1), else of Q(g2)
+#pragma unroll 1
+        for (int c0 = 0; c0 < kXH; c0 += 16) {
+            uint32_t r[16];
+            tmem_ld16(trow + kColAccXH + (uint32_t)c0, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int col = c0 + j;
+                const float v = __uint_as_float(r[j]);
+                if (col < 19 && lower) mine[m * 19 + col] = v;
+                if (col == 19) mine[(lower ? kOffB1 : kOffB2) + m] = v;
+                if (col >= kIn && !lower) mine[kOffW2 + m * kHid + (col - kIn)] = v;
+            }
+        }
+        uint32_t r[16];
+        tmem_ld16(trow + kColAccY, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int o = 0; o < 3; ++o) {
+            if (lower) mine[kOffW3 + o * kHid + m] = __uint_as_float(r[o]);
+            if (tid == kHid) mine[kOffB3 + o] = __uint_as_float(r[o]);
+        }
+    } else {
+        if (tid == 0) atomicOr(&w.state->error, kErrTimeout);
+        mbar_wait(wbar, 0);
+        if (phase > 0) mbar_wait(mbar, (phase - 1) & 1);
+        for (int e = tid; e < kShadeParams; e += kRows) mine[e] = 0.0f;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, kBwdCols);
+}
+
+// Sum of the CTAs' weight-gradient shares, in a fixed order (fp64).
+__global__ void k_shade_reduce(const float* __restrict__ part, int n_part,
+                               float* __restrict__ grad_params) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= kShadeParams) return;
+    double s = 0.0;
+    for (int c = 0; c < n_part; ++c) s += (double)part[(size_t)c * kShadeParams + i];
+    grad_params[i] = (float)s;
+}
+
+// CTAs of a kernel resident per SM, from the documented limits: shared
+// memory (with the per-block reserve), registers, resident blocks, and no
+// more than the tensor memory (512 columns) holds.
+int resident(const void* kernel, int bytes, int tmem_cols) {
+    int dev = 0;
+    cudaFuncAttributes fa;
+    cudaDeviceProp pr;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaFuncGetAttributes(&fa, kernel) != cudaSuccess ||
+        cudaGetDeviceProperties(&pr, dev) != cudaSuccess)
+        return 0;
+    const size_t per_block = (size_t)bytes + fa.sharedSizeBytes + pr.reservedSharedMemPerBlock;
+    int n = (int)(pr.sharedMemPerMultiprocessor / per_block);
+    const int regs = fa.numRegs * kRows;
+    if (regs > 0 && pr.regsPerMultiprocessor / regs < n) n = pr.regsPerMultiprocessor / regs;
+    if (pr.maxBlocksPerMultiProcessor < n) n = pr.maxBlocksPerMultiProcessor;
+    if (512 / tmem_cols < n) n = 512 / tmem_cols;
+    return n;
 }
 
 }  // namespace
 
-cudaError_t prepare_shade() {
-    return cudaFuncSetAttribute(k_shade_forward, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                ShadeSmem::bytes);
+size_t shade_image_bytes() { return kImageBytes; }
+
+cudaError_t prepare_shade(ShadeLaunch* sl) {
+    cudaError_t e = cudaFuncSetAttribute(k_shade_forward,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, FwdSmem::bytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_shade_backward, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 BwdSmem::bytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_shade_forward, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 100);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_shade_backward, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 100);
+    if (e != cudaSuccess) return e;
+    sl->fwd_per_sm = resident((const void*)k_shade_forward, FwdSmem::bytes, kFwdCols);
+    sl->bwd_per_sm = resident((const void*)k_shade_backward, BwdSmem::bytes, kBwdCols);
+    return sl->fwd_per_sm > 0 && sl->bwd_per_sm > 0 ? cudaSuccess : cudaErrorInvalidConfiguration;
 }
 
 cudaError_t launch_shade_forward(const Frames& fs, const Workspace& w, const float* features,
-                                 const float* params, float* rgb, int n_sms, cudaStream_t stream) {
-    const uint32_t n_tiles = (fs.f[0].pix_all + kShadeThreads - 1) / kShadeThreads;
+                                 const float* params, float* rgb, int grid_cap,
+                                 cudaStream_t stream) {
+    const uint64_t n_tiles = (fs.f[0].pix_all + kRows - 1) / kRows;
     if (n_tiles == 0) return cudaSuccess;
-    const uint32_t cap = (uint32_t)(4 * n_sms);   // 4 CTAs of 128 TMEM columns fill an SM's 512
-    const int grid = (int)(n_tiles < cap ? n_tiles : cap);
-    k_shade_forward<<<grid, kShadeThreads, ShadeSmem::bytes, stream>>>(fs, w, features, params, rgb);
+    const int grid = (int)(n_tiles < (uint64_t)grid_cap ? n_tiles : (uint64_t)grid_cap);
+    k_shade_pack<<<(kPackElems + 255) / 256, 256, 0, stream>>>(params, w.shade_img);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    k_shade_forward<<<grid, kRows, FwdSmem::bytes, stream>>>(fs, w, features, w.shade_img, rgb);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_shade_backward(const Frames& fs, const Workspace& w, const float* features,
+                                  const float* params, const float* grad_rgb,
+                                  float* grad_features, float* grad_params, int grid_cap,
+                                  cudaStream_t stream) {
+    const uint64_t n_tiles = (fs.f[0].pix_all + kRows - 1) / kRows;
+    if (n_tiles == 0)
+        return cudaMemsetAsync(grad_params, 0, kShadeParams * sizeof(float), stream);
+    const int grid = (int)(n_tiles < (uint64_t)grid_cap ? n_tiles : (uint64_t)grid_cap);
+    k_shade_pack<<<(kPackElems + 255) / 256, 256, 0, stream>>>(params, w.shade_img);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    k_shade_backward<<<grid, kRows, BwdSmem::bytes, stream>>>(
+        fs, w, features, w.shade_img + FwdImage::bytes, grad_rgb, grad_features, w.shade_part);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    k_shade_reduce<<<(kShadeParams + 255) / 256, 256, 0, stream>>>(w.shade_part, grid, grad_params);
     return cudaGetLastError();
 }
 

@@ -53,7 +53,7 @@ class Params(ctypes.Structure):
 
 
 EXPORTS = ("pulsar_create", "pulsar_create_cams", "pulsar_destroy", "pulsar_project",
-           "pulsar_project_cams", "pulsar_bin", "pulsar_shade_forward",
+           "pulsar_project_cams", "pulsar_bin", "pulsar_shade_forward", "pulsar_shade_backward",
            "pulsar_forward", "pulsar_backward", "pulsar_status", "pulsar_strerror",
            "pulsar_debug_copy", "pulsar_render_noalloc")
 
@@ -78,6 +78,7 @@ def load(path: str = LIB_PATH):
                                         ctypes.POINTER(Params), P]
     lib.pulsar_bin.argtypes = [P, P]
     lib.pulsar_shade_forward.argtypes = [P, P, P, P, P]
+    lib.pulsar_shade_backward.argtypes = [P] * 7
     lib.pulsar_forward.argtypes = [P, P, P, P, P]
     lib.pulsar_backward.argtypes = [P] + [P] * 9 + [P]
     lib.pulsar_status.argtypes = [P, P, ctypes.POINTER(I64), ctypes.POINTER(I64)]
@@ -189,6 +190,14 @@ def shade_forward(ctx, features, params, rgb, stream=None):
     pulsar_shade_forward in include/pulsar.h)."""
     _check(load().pulsar_shade_forward(ctx, _ptr(features), _ptr(params), _ptr(rgb),
                                        _stream(stream)), "pulsar_shade_forward")
+
+
+def shade_backward(ctx, features, params, grad_rgb, grad_features, grad_params, stream=None):
+    """Gradients of the shading MLP (see pulsar_shade_backward in
+    include/pulsar.h); grad_features may be None."""
+    _check(load().pulsar_shade_backward(ctx, _ptr(features), _ptr(params), _ptr(grad_rgb),
+                                        _ptr(grad_features), _ptr(grad_params),
+                                        _stream(stream)), "pulsar_shade_backward")
 
 
 def bin(ctx, stream=None):  # noqa: A001  (same name as the C entry point)
@@ -313,6 +322,17 @@ class Renderer:
                               dtype=torch.float32)
         shade_forward(self.ctx, features, params, rgb, stream)
         return rgb
+
+    def shade_backward(self, features, params, grad_rgb, grad_features=None, grad_params=None,
+                       stream=None):
+        """(dL/dfeatures, dL/dparams) of the shading for dL/drgb."""
+        import torch
+        if grad_features is None:
+            grad_features = torch.empty_like(features)
+        if grad_params is None:
+            grad_params = torch.empty_like(params)
+        shade_backward(self.ctx, features, params, grad_rgb, grad_features, grad_params, stream)
+        return grad_features, grad_params
 
     def status(self, stream=None, raise_on_error: bool = True):
         return status(self.ctx, stream, raise_on_error)

@@ -1,47 +1,19 @@
-"""Per-pixel shading MLP on the tensor cores (pulsar_shade_forward) against
-the oracle (oracle/mlp.py) on seeded inputs.
+"""Per-pixel shading MLP on the tensor cores (pulsar_shade_forward,
+pulsar_shade_backward) against the oracle (oracle/mlp.py) on seeded inputs.
 
-Tolerance, derived from the arithmetic: both sides round the same operands
-to bfloat16 and multiply them exactly; the GPU sums in fp32 (error below
-1e-5 of the sum of absolute products) where the oracle sums in fp64.  That
-difference can move a hidden activation across a bfloat16 rounding boundary
-(or a pre-activation across 0): such pixels are rare and bounded by one
-bfloat16 ulp (2^-8 relative) of every hidden activation, propagated.
+Every GPU value must lie in the interval tests/shade_bounds.py derives from
+the arithmetic (fp32 against fp64 sums of the same bf16 products, and every
+rounding or ReLU decision that this difference can move).
 """
 from __future__ import annotations
 
 import numpy as np
 import pytest
 
-from oracle import mlp
 from splat_rendering_gb300 import scenes
+import shade_bounds as sb
 
 pytestmark = pytest.mark.gpu
-
-
-def _bounds(ref, params):
-    """Per-pixel tight and one-ulp bounds on |y_gpu - y_oracle| [P, 3]."""
-    P = mlp.unpack(params)
-    W3 = np.abs(mlp.bf16(P["W3"]))
-    W2 = np.abs(mlp.bf16(P["W2"]))
-    W1 = np.abs(mlp.bf16(P["W1"]))
-    a1 = np.abs(ref["x"]) @ W1.T + np.abs(np.asarray(P["b1"], np.float32))
-    a2 = np.abs(ref["h1"]) @ W2.T + np.abs(np.asarray(P["b2"], np.float32))
-    a3 = np.abs(ref["h2"]) @ W3.T + np.abs(np.asarray(P["b3"], np.float32))
-    tight = 1e-5 * (a3 + (a2 @ W3.T) + (a1 @ W2.T) @ W3.T) + 1e-6
-    ulp = 2.0 ** -8
-    # one ulp in x, h1 and h2 (and the accumulation error), propagated to y
-    flip = ulp * (a3 + a2 @ W3.T + a1 @ W2.T @ W3.T) + tight
-    return tight, flip
-
-
-def _check(rgb, ref, params, what):
-    tight, flip = _bounds(ref, params)
-    err = np.abs(rgb.reshape(-1, 3).astype(np.float64) - ref["y"])
-    over = (err > tight).any(1)
-    assert (err <= flip).all(), f"{what}: beyond the one-ulp bound (worst {(err / flip).max():.3g}x)"
-    assert over.mean() < 2e-3, f"{what}: {over.sum()} of {len(over)} pixels past the tight bound"
-    return int(over.sum())
 
 
 def _renderer_for(cams, C=16):
@@ -76,8 +48,9 @@ def test_shading_matches_oracle(ortho):
     rgb = r.shade(torch.from_numpy(F).cuda(), torch.from_numpy(params).cuda())
     code = r.status(raise_on_error=False)[0]
     assert code == 0
-    ref = mlp.forward(F.reshape(-1, 16), cam, params.astype(np.float64))
-    _check(rgb.cpu().numpy(), ref, params.astype(np.float64), f"shade ortho={ortho}")
+    ref = sb.oracle_batch(F[None], [cam], params.astype(np.float64))
+    sb.check(dict(y=rgb.cpu().numpy()), ref, params.astype(np.float64), f"shade ortho={ortho}",
+             backward=False)
     r.close()
 
 
@@ -94,9 +67,8 @@ def test_shading_camera_batch_and_ragged_tile():
     _project(r, cams)
     rgb = r.shade(torch.from_numpy(F).cuda(), torch.from_numpy(params).cuda()).cpu().numpy()
     assert r.status(raise_on_error=False)[0] == 0
-    for k, cam in enumerate(cams):
-        ref = mlp.forward(F[k].reshape(-1, 16), cam, params.astype(np.float64))
-        _check(rgb[k], ref, params.astype(np.float64), f"camera {k}")
+    ref = sb.oracle_batch(F, cams, params.astype(np.float64))
+    sb.check(dict(y=rgb), ref, params.astype(np.float64), "camera batch", backward=False)
     r.close()
 
 
@@ -112,7 +84,80 @@ def test_shading_full_size_frame():
     _project(r, [cam])
     rgb = r.shade(torch.from_numpy(F).cuda(), torch.from_numpy(params).cuda())
     assert r.status(raise_on_error=False)[0] == 0
-    ref = mlp.forward(F.reshape(-1, 16), cam, params.astype(np.float64))
-    n = _check(rgb.cpu().numpy(), ref, params.astype(np.float64), "full size")
-    print("pixels past the tight bound:", n)
+    ref = sb.oracle_batch(F[None], [cam], params.astype(np.float64))
+    print(sb.check(dict(y=rgb.cpu().numpy()), ref, params.astype(np.float64), "full size",
+                   backward=False))
     r.close()
+
+
+# ------------------------------------------------------------------ backward --
+def _run_backward(cams, F, dY, params):
+    import torch
+    r = _renderer_for(cams)
+    _project(r, cams)
+    Fd, Pd, dYd = (torch.from_numpy(a).cuda() for a in (F, params, dY))
+    gF, gP = r.shade_backward(Fd, Pd, dYd)
+    gP2 = torch.empty_like(gP)
+    from splat_rendering_gb300 import pulsar as pl
+    pl.shade_backward(r.ctx, Fd, Pd, dYd, None, gP2)   # dF skipped
+    torch.cuda.synchronize()
+    assert r.status(raise_on_error=False)[0] == 0
+    gF, gP, gP2 = gF.cpu().numpy(), gP.cpu().numpy(), gP2.cpu().numpy()
+    r.close()
+    # the fixed summation order makes the weight gradient reproducible bit for bit
+    assert np.array_equal(gP.view(np.uint32), gP2.view(np.uint32))
+    return gF, gP
+
+
+@pytest.mark.parametrize("ortho", [False, True])
+def test_shading_backward_matches_oracle(ortho):
+    cam = scenes._camera(np.eye(3), np.zeros(3), 180.0, 200, 150, 1.0, 9.0, fy=170.0,
+                         cx=97.3, cy=77.1, orthographic=ortho)
+    rng = np.random.default_rng(131 + ortho)
+    F = rng.standard_normal((1, cam.height, cam.width, 16)).astype(np.float32)
+    dY = rng.standard_normal((1, cam.height, cam.width, 3)).astype(np.float32)
+    params = scenes.shading_mlp(9)
+    gF, gP = _run_backward([cam], F, dY, params)
+    ref = sb.oracle_batch(F, [cam], params.astype(np.float64), dY)
+    print(sb.check(dict(dF=gF, params=gP), ref, params.astype(np.float64),
+                   f"backward ortho={ortho}"))
+
+
+def test_shading_backward_batch_many_tiles_per_cta():
+    """Three 250 x 199 cameras: more tiles than resident CTAs (each CTA
+    accumulates several tiles in tensor memory) and a ragged last tile."""
+    cams = [scenes._camera(np.eye(3), np.zeros(3), f, 250, 199, 1.0, 9.0, cx=cx, cy=101.0)
+            for f, cx in ((200.0, 120.0), (260.0, 131.5), (150.0, 100.0))]
+    rng = np.random.default_rng(133)
+    F = rng.standard_normal((3, 199, 250, 16)).astype(np.float32)
+    dY = rng.standard_normal((3, 199, 250, 3)).astype(np.float32)
+    params = scenes.shading_mlp(10)
+    gF, gP = _run_backward(cams, F, dY, params)
+    ref = sb.oracle_batch(F, cams, params.astype(np.float64), dY)
+    print(sb.check(dict(dF=gF, params=gP), ref, params.astype(np.float64), "batch"))
+
+
+def test_shading_backward_tiny_frame():
+    """A 5 x 3 frame: one partly filled tile (rows past the frame add nothing)."""
+    cam = scenes._camera(np.eye(3), np.zeros(3), 4.0, 5, 3, 1.0, 9.0, cx=2.6, cy=1.4)
+    rng = np.random.default_rng(134)
+    F = rng.standard_normal((1, 3, 5, 16)).astype(np.float32)
+    dY = rng.standard_normal((1, 3, 5, 3)).astype(np.float32)
+    params = scenes.shading_mlp(11)
+    gF, gP = _run_backward([cam], F, dY, params)
+    ref = sb.oracle_batch(F, [cam], params.astype(np.float64), dY)
+    sb.check(dict(dF=gF, params=gP), ref, params.astype(np.float64), "tiny")
+
+
+def test_shading_backward_full_size_frame():
+    """1024 x 1024 (the neural configuration's image size): every CTA runs
+    many tiles, the weight gradient sums a million pixels."""
+    sc = scenes.make("neural", n=1000)
+    cam = sc.cameras[0]
+    rng = np.random.default_rng(135)
+    F = rng.standard_normal((1, cam.height, cam.width, 16)).astype(np.float32)
+    dY = rng.standard_normal((1, cam.height, cam.width, 3)).astype(np.float32)
+    params = scenes.shading_mlp(12)
+    gF, gP = _run_backward([cam], F, dY, params)
+    ref = sb.oracle_batch(F, [cam], params.astype(np.float64), dY)
+    print(sb.check(dict(dF=gF, params=gP), ref, params.astype(np.float64), "full size"))
