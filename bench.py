@@ -36,10 +36,15 @@ WORKLOADS = {
     "neural": "neural: 1,000,000 spheres, 1024x1024, 16 channels, n_track 8, R/t/K gradients",
     "driving": "driving rig: 2,000,000 spheres, six 1920x1080 cameras in one batched launch, "
                "3 channels, n_track 5, R/t/K gradients; value in camera frames/s",
+    "neural_shaded": "neural pipeline: the neural scene (1,000,000 spheres, 1024x1024, 16 "
+                     "channels, n_track 8) rendered, shaded to RGB by the per-pixel MLP "
+                     "(19-64-64-3, bf16 tensor cores), MLP backward, render backward fed with "
+                     "dL/dF; gradients of spheres, camera and MLP weights",
 }
 METRIC = "fwd+bwd frames/s at 1M spheres 1024^2"
 UNIT = "frames/s"
 KERNELS_PER_STEP = 8   # project, tile_scan, emit, tile_sort, forward, backward, finalize, camera_reduce
+SHADE_KERNELS = 5      # weight pack + shade forward, weight pack + shade backward + reduce
 
 
 def args_parse():
@@ -179,6 +184,16 @@ def algorithmic_flops(stage, N, M, P, C, T, H, Ht):
     return 0
 
 
+# Shading MLP per pixel: compulsory HBM bytes (features 64 B in, rgb 12 B out;
+# backward: features and dL/drgb in, dL/dF 64 B out) and tensor-core flops
+# (forward 2 x (19*64 + 64*64 + 64*3); backward: the two hidden layers again,
+# W3^T, W2^T, W1^T[:16] products, and the weight and bias gradients).
+SHADE_BYTES_PER_PIXEL = {"shade_forward": 64 + 12, "shade_backward": 64 + 12 + 64}
+SHADE_FLOPS_PER_PIXEL = {"shade_forward": 2 * (19 * 64 + 64 * 64 + 64 * 3),
+                         "shade_backward": 2 * (19 * 64 + 64 * 64 + 3 * 64 + 64 * 64 + 64 * 16
+                                                + 64 * 20 + 64 * 65 + 3 * 65)}
+
+
 def traffic_from_profile(kernel: str, source: str, workload: str):
     """DRAM bytes per launch recorded by the committed ncu summary of `kernel`,
     if it was taken on the current source; else None."""
@@ -199,20 +214,32 @@ def traffic_from_profile(kernel: str, source: str, workload: str):
 
 
 # ------------------------------------------------------------- reference --
-def oracle_sample(scene, target_s: float, rows: int | None = None):
-    """Time the CPU oracle on a band of rows of the frame (forward + backward).
-    With rows=None the band grows until it takes about target_s.
-    Returns (frames/s extrapolated by the pixel fraction, rows, seconds, cores)."""
+def oracle_sample(scene, target_s: float, rows: int | None = None, shade=None):
+    """Time the CPU oracle on a band of rows of the frame (forward + backward;
+    with shade = (mlp weights, dL/drgb): forward, the shading MLP forward and
+    backward, and the render backward fed with its dL/dF).  With rows=None
+    the band grows until it takes about target_s.  Returns (frames/s
+    extrapolated by the pixel fraction, rows, seconds, cores)."""
+    import dataclasses
+
     import numpy as np
     import oracle
+    from oracle import mlp
     cam = scene.cameras[0]
     fixed = rows is not None
     rows = rows or 16
     while True:
         win = (0, 0, cam.width, rows)
         G = np.zeros_like(scene.grad_images[0])
-        G[:rows] = scene.grad_images[0][:rows]
         t0 = time.perf_counter()
+        if shade is None:
+            G[:rows] = scene.grad_images[0][:rows]
+        else:
+            F = oracle.render(scene.pos, scene.radius, scene.opacity, scene.features, cam,
+                              scene.params, scene.bg, window=win)["image"]
+            band = dataclasses.replace(cam, height=rows)
+            g = mlp.backward(F.reshape(-1, 16), band, shade[0], shade[1][:rows].reshape(-1, 3))
+            G[:rows] = g["grad_features"].reshape(rows, cam.width, 16)
         oracle.render(scene.pos, scene.radius, scene.opacity, scene.features, cam, scene.params,
                       scene.bg, grad_image=G, window=win)
         dt = time.perf_counter() - t0
@@ -270,7 +297,8 @@ def run_gb300(a):
     pl.load()
     dev = torch.device("cuda", local)
 
-    scene = scenes.make(a.scene)
+    shaded = a.scene == "neural_shaded"
+    scene = scenes.make("neural" if shaded else a.scene)
     # the driving rig renders its six cameras as one batch; the others one camera
     cams = scene.cameras if a.scene == "driving" else scene.cameras[:1]
     K = len(cams)
@@ -294,10 +322,23 @@ def run_gb300(a):
     cap = 4 * N
     r = pl.Renderer(max_spheres=N, max_pairs=cap, max_width=cam.width, max_height=cam.height,
                     max_channels=C, max_track=T, device=local, max_cams=K)
+    if shaded:
+        # per-pixel MLP shading: rgb = MLP(F); dL/drgb seeded; dL/dF feeds the render backward
+        mlp_host = scenes.shading_mlp(5)
+        drgb_host = scenes.shading_grad(7, cam.height, cam.width)
+        mlp_w, drgb = dev_t(mlp_host), dev_t(drgb_host)
+        rgb = torch.empty((cam.height, cam.width, 3), device=dev)
+        gF = torch.empty_like(image)
+        grads["mlp"] = torch.empty_like(mlp_w)
 
     def step():
         r.render(pos, rad, opa, feat, c_cam, c_prm, bg, image=image)
-        r.backward(G, out=grads)
+        if shaded:
+            r.shade(image, mlp_w, rgb)
+            r.shade_backward(image, mlp_w, drgb, gF, grads["mlp"])
+            r.backward(gF, out=grads)
+        else:
+            r.backward(G, out=grads)
 
     step()
     code, M, H = r.status(raise_on_error=False)
@@ -360,11 +401,12 @@ def run_gb300(a):
         dist.barrier()
 
     # ---- per-stage breakdown (same kernels, eager, events between ABI calls)
-    stages = ("project", "bin", "forward", "backward")
+    stages = ("project", "bin", "forward") + (("shade_forward", "shade_backward") if shaded
+                                             else ()) + ("backward",)
     per = {k: [] for k in stages}
     for _ in range(a.steps):
         flush.zero_()
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
         ev[0].record()
         if K > 1:
             pl.project_cams(r.ctx, pos, rad, opa, N, c_cam, c_prm)
@@ -375,9 +417,16 @@ def run_gb300(a):
         ev[2].record()
         pl.forward(r.ctx, feat, bg, image)
         ev[3].record()
-        pl.backward(r.ctx, feat, bg, image, G, grads["pos"], grads["radius"], grads["opacity"],
-                    grads["features"], grads["cam"])
-        ev[4].record()
+        G_in = G
+        if shaded:
+            pl.shade_forward(r.ctx, image, mlp_w, rgb)
+            ev[4].record()
+            pl.shade_backward(r.ctx, image, mlp_w, drgb, gF, grads["mlp"])
+            ev[5].record()
+            G_in = gF
+        pl.backward(r.ctx, feat, bg, image, G_in, grads["pos"], grads["radius"],
+                    grads["opacity"], grads["features"], grads["cam"])
+        ev[-1].record()
         torch.cuda.synchronize()
         for i, k in enumerate(stages):
             per[k].append(ev[i].elapsed_time(ev[i + 1]))
@@ -385,10 +434,11 @@ def run_gb300(a):
     breakdown = {k: statistics.median(v) for k, v in per.items()}
 
     # ---- end to end through the API with host buffers (pinned), copies timed
-    host_in = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in
-               (("pos", scene.pos), ("radius", scene.radius), ("opacity", scene.opacity),
-                ("features", scene.features), ("G", G_host))}
-    host_out = {"image": torch.empty(image.shape).pin_memory()}
+    ins = [("pos", scene.pos), ("radius", scene.radius), ("opacity", scene.opacity),
+           ("features", scene.features)]
+    ins += [("mlp", mlp_host), ("drgb", drgb_host)] if shaded else [("G", G_host)]
+    host_in = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in ins}
+    host_out = {"image": torch.empty((rgb if shaded else image).shape).pin_memory()}
     for k, v in grads.items():
         host_out[k] = torch.empty(v.shape).pin_memory()
     d_in = {k: torch.empty(v.shape, device=dev) for k, v in host_in.items()}
@@ -400,8 +450,14 @@ def run_gb300(a):
             d_in[k].copy_(v, non_blocking=True)
         r.render(d_in["pos"], d_in["radius"], d_in["opacity"], d_in["features"], c_cam, c_prm,
                  bg, image=image)
-        r.backward(d_in["G"], out=grads)
-        host_out["image"].copy_(image, non_blocking=True)
+        if shaded:
+            r.shade(image, d_in["mlp"], rgb)
+            r.shade_backward(image, d_in["mlp"], d_in["drgb"], gF, grads["mlp"])
+            r.backward(gF, out=grads)
+            host_out["image"].copy_(rgb, non_blocking=True)
+        else:
+            r.backward(d_in["G"], out=grads)
+            host_out["image"].copy_(image, non_blocking=True)
         for k, v in grads.items():
             host_out[k].copy_(v, non_blocking=True)
 
@@ -436,8 +492,21 @@ def run_gb300(a):
                 "peak_source": f"FP32: {SMS} SMs x {FP32_LANES} lanes x 2 x "
                                f"{peaks.get('sm_max_mhz', 2070.0)} MHz ({peak_src} clock); "
                                f"HBM: {peak_src} hbm_gbs {hbm}"}
-    path_bytes = sum(algorithmic_bytes(k, N, M, P, C, T) for k in stages)
-    path_flops = sum(algorithmic_flops(k, N, M, P, C, T, H, Ht) for k in stages)
+    render_stages = ("project", "bin", "forward", "backward")
+    path_bytes = sum(algorithmic_bytes(k, N, M, P, C, T) for k in render_stages)
+    path_flops = sum(algorithmic_flops(k, N, M, P, C, T, H, Ht) for k in render_stages)
+    shade_roof = None
+    if shaded:
+        bf16 = float(peaks.get("bf16_tflops_sustained", 1700.0))   # inside a long step
+        shade_roof = {}
+        for k in ("shade_forward", "shade_backward"):
+            b, fl = SHADE_BYTES_PER_PIXEL[k] * P, SHADE_FLOPS_PER_PIXEL[k] * P
+            t_s = breakdown[k] * 1e-3
+            shade_roof[k] = {"bound": "hbm", "achieved": b / t_s / 1e9, "peak": hbm,
+                             "unit": "GB/s", "frac": b / t_s / 1e9 / hbm,
+                             "algorithmic_bytes": b, "tensor_flops": fl,
+                             "tensor_frac": fl / t_s / 1e12 / bf16}
+            path_bytes += b
     path_time = max(path_bytes / (hbm * 1e9), path_flops / (fp32 * 1e12))
     path = {"algorithmic_bytes": path_bytes, "algorithmic_flops": path_flops,
             "hbm_time_ms": path_bytes / (hbm * 1e9) * 1e3,
@@ -496,14 +565,18 @@ def run_gb300(a):
             "breakdown_ms": breakdown,
             "path_roofline": path,
             "roofline": roofline,
+            **({"shade_roofline": shade_roof} if shaded else {}),
             "e2e": {"value": job_rate(world, K, a.steps, e2e_total), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": KERNELS_PER_STEP * a.steps,
+            "gpu_launches": (KERNELS_PER_STEP + (SHADE_KERNELS if shaded else 0)) * a.steps,
             "clocks": clk, "wall_s_timed": t_wall}
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
-        v, rows, dt, cores = oracle_sample(scene, a.cpu_seconds)
+        v, rows, dt, cores = oracle_sample(scene, a.cpu_seconds,
+                                           shade=(mlp_host.astype(np.float64), drgb_host)
+                                           if shaded else None)
+        what = "fwd, MLP fwd+bwd, bwd" if shaded else "fwd+bwd"
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": f"fp64 oracle fwd+bwd on rows [0,{rows}) x 1024 of "
+                                "sample": f"fp64 oracle {what} on rows [0,{rows}) x 1024 of "
                                           f"the same frame ({dt:.1f} s), scaled by {rows}/1024"}
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -274,6 +274,11 @@ def shading_mlp(seed: int = 5) -> np.ndarray:
     return _f32(np.concatenate([np.asarray(q).reshape(-1) for q in parts]))
 
 
+def shading_grad(seed: int, height: int, width: int) -> np.ndarray:
+    """Seeded dL/d rgb [H, W, 3] (N(0,1)) for the shading MLP's backward."""
+    return _f32(np.random.default_rng(seed).standard_normal((height, width, 3)))
+
+
 CONFIGS = {
     "tiny": tiny,
     "medium": medium,
