@@ -255,43 +255,83 @@ __device__ __forceinline__ void st_row16(unsigned char* tile, int row, int k, in
 
 // Hidden layer epilogue: h = bf16(ReLU(D)) (D holds the bias) of this
 // thread's row into columns k0 .. k0 + 63 of a K-column A operand; the bf16x2
-// words stay in h for the backward's ReLU masks.
+// words stay in h for the backward's ReLU masks.  kBatch columns are read
+// from tensor memory per wait (registers against latency).
+template <int kBatch>
 __device__ __forceinline__ void relu_row(uint32_t taddr, unsigned char* tile, int row, int K,
                                          int k0, uint32_t (&h)[kHid / 2]) {
 #pragma unroll
-    for (int c0 = 0; c0 < kHid; c0 += 32) {
-        uint32_t r[2][16];
-        tmem_ld16(taddr + (uint32_t)c0, r[0]);
-        tmem_ld16(taddr + (uint32_t)(c0 + 16), r[1]);
+    for (int c0 = 0; c0 < kHid; c0 += kBatch) {
+        uint32_t r[kBatch / 16][16];
+#pragma unroll
+        for (int q = 0; q < kBatch / 16; ++q) tmem_ld16(taddr + (uint32_t)(c0 + 16 * q), r[q]);
         tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
+        for (int j = 0; j < kBatch / 2; ++j)
             h[c0 / 2 + j] = bf16x2_relu(__uint_as_float(r[j / 8][(2 * j) % 16]),
                                         __uint_as_float(r[j / 8][(2 * j + 1) % 16]));
 #pragma unroll
-        for (int q = 0; q < 4; ++q) st_row16(tile, row, k0 + c0 + 8 * q, K, h + c0 / 2 + 4 * q);
+        for (int q = 0; q < kBatch / 8; ++q)
+            st_row16(tile, row, k0 + c0 + 8 * q, K, h + c0 / 2 + 4 * q);
     }
 }
 
 // Backward epilogue: Q(D * [h > 0]) of this thread's row into columns
-// k0 .. k0 + 63 (h: the layer's ReLU output words).
+// k0 .. k0 + 63 (h: the layer's ReLU output words), all 64 columns per wait.
 __device__ __forceinline__ void masked_row(uint32_t taddr, const uint32_t (&h)[kHid / 2],
                                            unsigned char* tile, int row, int K, int k0) {
+    uint32_t r[4][16];
 #pragma unroll
-    for (int c0 = 0; c0 < kHid; c0 += 32) {
-        uint32_t r[2][16];
-        tmem_ld16(taddr + (uint32_t)c0, r[0]);
-        tmem_ld16(taddr + (uint32_t)(c0 + 16), r[1]);
-        tmem_wait_ld();
-        uint32_t g[16];
+    for (int q = 0; q < 4; ++q) tmem_ld16(taddr + (uint32_t)(16 * q), r[q]);
+    tmem_wait_ld();
+    uint32_t g[kHid / 2];
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-            g[j] = bf16x2(__uint_as_float(r[j / 8][(2 * j) % 16]),
-                          __uint_as_float(r[j / 8][(2 * j + 1) % 16])) &
-                   nonzero_mask(h[c0 / 2 + j]);
+    for (int j = 0; j < kHid / 2; ++j)
+        g[j] = bf16x2(__uint_as_float(r[j / 8][(2 * j) % 16]),
+                      __uint_as_float(r[j / 8][(2 * j + 1) % 16])) &
+               nonzero_mask(h[j]);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) st_row16(tile, row, k0 + c0 + 8 * q, K, g + 4 * q);
+    for (int q = 0; q < kHid / 8; ++q) st_row16(tile, row, k0 + 8 * q, K, g + 4 * q);
+}
+
+// Both epilogues of the backward's second round from one wait: h2 =
+// bf16(ReLU(z2)) into the h2 tile, then Q(g2 * [h2 > 0]) into the g tile.
+__device__ __forceinline__ void relu_and_masked_row(uint32_t tz, uint32_t tg, unsigned char* htile,
+                                                    int hK, unsigned char* gtile, int gK, int gk0,
+                                                    int row) {
+    uint32_t z[4][16], g[4][16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        tmem_ld16(tz + (uint32_t)(16 * q), z[q]);
+        tmem_ld16(tg + (uint32_t)(16 * q), g[q]);
     }
+    tmem_wait_ld();
+    uint32_t h[kHid / 2], w[kHid / 2];
+#pragma unroll
+    for (int j = 0; j < kHid / 2; ++j) {
+        h[j] = bf16x2_relu(__uint_as_float(z[j / 8][(2 * j) % 16]),
+                           __uint_as_float(z[j / 8][(2 * j + 1) % 16]));
+        w[j] = bf16x2(__uint_as_float(g[j / 8][(2 * j) % 16]),
+                      __uint_as_float(g[j / 8][(2 * j + 1) % 16])) &
+               nonzero_mask(h[j]);
+    }
+#pragma unroll
+    for (int q = 0; q < kHid / 8; ++q) {
+        st_row16(htile, row, 8 * q, hK, h + 4 * q);
+        st_row16(gtile, row, gk0 + 8 * q, gK, w + 4 * q);
+    }
+}
+
+// Step `bytes` into the operand a descriptor describes (the address field
+// counts 16-byte units; shared addresses stay far below its 2^18-byte range).
+__device__ __forceinline__ uint64_t desc_at(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+
+// One K-major MMA chain: D = sum over `steps` K = 16 steps of A_s B_s^T, A
+// and B advancing 256 bytes (two core matrices) per step.
+__device__ __forceinline__ void mma_chain(uint32_t d, uint64_t a, uint64_t b, int steps,
+                                          uint32_t idesc, uint32_t acc0) {
+    for (int s = 0; s < steps; ++s)
+        mma_bf16(d, desc_at(a, 256u * s), desc_at(b, 256u * s), idesc, s > 0 ? 1u : acc0);
 }
 
 // ================================================================ weights --
@@ -402,15 +442,6 @@ struct FwdSmem {
     static constexpr int bytes = taddr + 8;
 };
 
-// Issue one layer: D = A[:, a_k0 .. a_k0 + K) B^T over K / 16 steps (A rows
-// are kXH columns wide; B is N x K).
-__device__ __forceinline__ void issue_layer(uint32_t d, uint32_t a, int a_k0, int a_cols,
-                                            uint32_t b, int K, int N) {
-    for (int k0 = 0; k0 < K; k0 += 16)
-        mma_bf16(d, smem_desc(a + ((a_k0 + k0) / 8) * 128, 128, (a_cols / 8) * 128),
-                 smem_desc(b + (k0 / 8) * 128, 128, (K / 8) * 128), idesc_bf16(kRows, N), k0 > 0);
-}
-
 __global__ void __launch_bounds__(kRows)
 k_shade_forward(Frames fs, Workspace w, const float* __restrict__ features,
                 const unsigned char* __restrict__ img, float* __restrict__ rgb) {
@@ -436,9 +467,11 @@ k_shade_forward(Frames fs, Workspace w, const float* __restrict__ features,
     operands_ready();
     const uint32_t tmem = *s_taddr;
     const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);   // this warp's TMEM lanes
-    const uint32_t sact = smem_u32(smem + L::act);
-    const uint32_t sw1 = smem_u32(smem + L::w1), sw2 = smem_u32(smem + L::w2),
-                   sw3 = smem_u32(smem + L::w3);
+    // K-major descriptors: core matrices 128 B apart along K, a row block apart along M/N
+    const uint64_t d_xh = smem_desc(smem_u32(smem + L::act), 128, (kXH / 8) * 128);
+    const uint64_t d_w1 = smem_desc(smem_u32(smem + L::w1), 128, (kIn / 8) * 128);
+    const uint64_t d_w2 = smem_desc(smem_u32(smem + L::w2), 128, (kKB / 8) * 128);
+    const uint64_t d_w3 = smem_desc(smem_u32(smem + L::w3), 128, (kKB / 8) * 128);
     uint32_t phase = 0;
     bool ok = true;
     uint32_t h[kHid / 2];
@@ -459,27 +492,27 @@ k_shade_forward(Frames fs, Workspace w, const float* __restrict__ features,
         load_features(features, p + stride, p + stride < n_pix, fcur);
         operands_ready();
         if (tid == 0) {
-            issue_layer(tmem, sact, 0, kXH, sw1, kIn, kHid);
+            mma_chain(tmem, d_xh, d_w1, kIn / 16, idesc_bf16(kRows, kHid), 0);
             mma_commit(mbar);
         }
         ok = __syncthreads_and(mbar_wait(mbar, phase & 1));   // one decision for all
         ++phase;
         tc_fence_after();
         if (!ok) break;
-        relu_row(trow, smem + L::act, tid, kXH, kIn, h);   // h1 (layer 1 is complete)
+        relu_row<32>(trow, smem + L::act, tid, kXH, kIn, h);   // h1 (layer 1 is complete)
         operands_ready();
-        if (tid == 0) {
-            issue_layer(tmem, sact, 16, kXH, sw2, kKB, kHid);
+        if (tid == 0) {   // the bias step over x's columns 16-31, then the 64 hidden units
+            mma_chain(tmem, desc_at(d_xh, 256), d_w2, kKB / 16, idesc_bf16(kRows, kHid), 0);
             mma_commit(mbar);
         }
         ok = __syncthreads_and(mbar_wait(mbar, phase & 1));
         ++phase;
         tc_fence_after();
         if (!ok) break;
-        relu_row(trow, smem + L::act, tid, kXH, kIn, h);   // h2 replaces h1 (layer 2 is complete)
+        relu_row<32>(trow, smem + L::act, tid, kXH, kIn, h);   // h2 replaces h1 (layer 2 is complete)
         operands_ready();
         if (tid == 0) {
-            issue_layer(tmem, sact, 16, kXH, sw3, kKB, kOutPad);
+            mma_chain(tmem, desc_at(d_xh, 256), d_w3, kKB / 16, idesc_bf16(kRows, kOutPad), 0);
             mma_commit(mbar);
         }
         ok = __syncthreads_and(mbar_wait(mbar, phase & 1));
@@ -536,8 +569,9 @@ struct BwdSmem {
     static constexpr int w3t = img + BwdImage::w3t;
     static constexpr int w2t = img + BwdImage::w2t;
     static constexpr int w1t = img + BwdImage::w1t;
-    static constexpr int mbar = img + BwdImage::bytes;      // u64: MMA completion
-    static constexpr int wbar = mbar + 8;                   // u64: weights landed
+    static constexpr int mbar = img + BwdImage::bytes;      // u64: the dF chain's MMAs
+    static constexpr int gbar = mbar + 8;                   // u64: the weight-gradient MMAs
+    static constexpr int wbar = gbar + 8;                   // u64: weights landed
     static constexpr int taddr = wbar + 8;
     static constexpr int bytes = taddr + 8;
 };
@@ -555,6 +589,7 @@ k_shade_backward(Frames fs, Workspace w, const float* __restrict__ features,
     using L = BwdSmem;
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + L::mbar);
+    uint64_t* gbar = reinterpret_cast<uint64_t*>(smem + L::gbar);
     uint64_t* wbar = reinterpret_cast<uint64_t*>(smem + L::wbar);
     uint32_t* s_taddr = reinterpret_cast<uint32_t*>(smem + L::taddr);
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -570,6 +605,7 @@ k_shade_backward(Frames fs, Workspace w, const float* __restrict__ features,
     }
     if (tid == 0) {
         mbar_init(mbar);
+        mbar_init(gbar);
         mbar_init(wbar);
         fence_async_smem();
         bulk_load(smem + L::img, img, BwdImage::bytes, wbar);
@@ -580,13 +616,26 @@ k_shade_backward(Frames fs, Workspace w, const float* __restrict__ features,
     const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
     const uint32_t sxh = smem_u32(smem + L::xh), sgg = smem_u32(smem + L::gg),
                    sh2 = smem_u32(smem + L::h2), sdy = smem_u32(smem + L::dy);
-    const uint32_t sw1 = smem_u32(smem + L::w1), sw2 = smem_u32(smem + L::w2),
-                   sw3t = smem_u32(smem + L::w3t), sw2t = smem_u32(smem + L::w2t),
-                   sw1t = smem_u32(smem + L::w1t);
-    uint32_t phase = 0;
+    // K-major descriptors: core matrices 128 B apart along K, a row block apart along M/N
+    const uint64_t d_xh = smem_desc(sxh, 128, (kXH / 8) * 128);
+    const uint64_t d_gg = smem_desc(sgg, 128, (kGG / 8) * 128);
+    const uint64_t d_dy = smem_desc(sdy, 128, (kDY / 8) * 128);
+    const uint64_t d_w1 = smem_desc(smem_u32(smem + L::w1), 128, (kIn / 8) * 128);
+    const uint64_t d_w2 = smem_desc(smem_u32(smem + L::w2), 128, (kKB / 8) * 128);
+    const uint64_t d_w3t = smem_desc(smem_u32(smem + L::w3t), 128, (kDY / 8) * 128);
+    const uint64_t d_w2t = smem_desc(smem_u32(smem + L::w2t), 128, (kHid / 8) * 128);
+    const uint64_t d_w1t = smem_desc(smem_u32(smem + L::w1t), 128, (kHid / 8) * 128);
+    // MN-major descriptors of the pixel contractions: groups of 8 units 128 B
+    // apart (M/N), groups of 8 pixels one row block apart (K); 16 pixels per
+    // instruction = two row blocks
+    const uint64_t m_gg = smem_desc(sgg, (kGG / 8) * 128, 128);
+    const uint64_t m_xh = smem_desc(sxh, (kXH / 8) * 128, 128);
+    const uint64_t m_h2 = smem_desc(sh2, (kH2 / 8) * 128, 128);
+    const uint64_t m_dy = smem_desc(sdy, (kDY / 8) * 128, 128);
+    uint32_t phase = 0, gphase = 0;
     bool ok = true;
     uint32_t acc = 0;   // 0 until the first tile's weight-gradient MMAs are issued
-    uint32_t h1[kHid / 2], h2[kHid / 2];
+    uint32_t h1[kHid / 2];
 
     uint64_t p = (uint64_t)blockIdx.x * kRows + tid;
     float4 fcur[4];
@@ -597,6 +646,11 @@ k_shade_backward(Frames fs, Workspace w, const float* __restrict__ features,
     ok = __syncthreads_and(mbar_wait(wbar, 0));   // the weights are in
     for (uint32_t tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, p += stride) {
         const bool valid = p < n_pix;
+        if (acc) {   // the previous tile's weight-gradient MMAs still read x, h1, g, dy
+            ok = __syncthreads_and(mbar_wait(gbar, gphase & 1));
+            ++gphase;
+            if (!ok) break;
+        }
         {
             float in[kIn];
             input_row(fs, P1, p, valid, fcur, in);
@@ -617,40 +671,38 @@ k_shade_backward(Frames fs, Workspace w, const float* __restrict__ features,
         operands_ready();
         // ---- round 1: z1 = W1 Q(x) + b1
         if (tid == 0) {
-            issue_layer(tmem + kColZ1, sxh, 0, kXH, sw1, kIn, kHid);
+            mma_chain(tmem + kColZ1, d_xh, d_w1, kIn / 16, idesc_bf16(kRows, kHid), 0);
             mma_commit(mbar);
         }
         ok = __syncthreads_and(mbar_wait(mbar, phase & 1));
         ++phase;
         tc_fence_after();
         if (!ok) break;
-        relu_row(trow + kColZ1, smem + L::xh, tid, kXH, kIn, h1);
+        relu_row<64>(trow + kColZ1, smem + L::xh, tid, kXH, kIn, h1);
         operands_ready();
-        // ---- round 2: z2 = W2 Q(h1) + b2, and W3^T Q(dY)
+        // ---- round 2: z2 = W2 Q(h1) + b2 (bias step over x's columns 16-31), and W3^T Q(dY)
         if (tid == 0) {
-            issue_layer(tmem + kColZ2, sxh, 16, kXH, sw2, kKB, kHid);
-            mma_bf16(tmem + kColG2, smem_desc(sdy, 128, (kDY / 8) * 128),
-                     smem_desc(sw3t, 128, (kDY / 8) * 128), idesc_bf16(kRows, kHid), 0);
+            mma_chain(tmem + kColZ2, desc_at(d_xh, 256), d_w2, kKB / 16, idesc_bf16(kRows, kHid), 0);
+            mma_bf16(tmem + kColG2, d_dy, d_w3t, idesc_bf16(kRows, kHid), 0);
             mma_commit(mbar);
         }
         ok = __syncthreads_and(mbar_wait(mbar, phase & 1));
         ++phase;
         tc_fence_after();
         if (!ok) break;
-        relu_row(trow + kColZ2, smem + L::h2, tid, kH2, 0, h2);
-        masked_row(trow + kColG2, h2, smem + L::gg, tid, kGG, kHid);   // Q(g2)
+        relu_and_masked_row(trow + kColZ2, trow + kColG2, smem + L::h2, kH2, smem + L::gg, kGG,
+                            kHid, tid);   // h2, Q(g2)
         operands_ready();
-        // ---- round 3: W2^T Q(g2); accumulate [Q(h2) ; 1] Q(dY)^T over the tile's pixels
+        // ---- round 3: W2^T Q(g2) (committed alone); then accumulate
+        // [Q(h2) ; 1] Q(dY)^T over the tile's pixels behind it
         if (tid == 0) {
-            issue_layer(tmem + kColG1, sgg, kHid, kGG, sw2t, kHid, kHid);
-            // MN-major: groups of 8 units 128 B apart, groups of 8 pixels one
-            // row block of the tile apart; K = 16 pixels per instruction
+            mma_chain(tmem + kColG1, desc_at(d_gg, kHid / 8 * 128), d_w2t, kHid / 16,
+                      idesc_bf16(kRows, kHid), 0);
+            mma_commit(mbar);
             for (int q = 0; q < kRows; q += 16)
-                mma_bf16(tmem + kColAccY,
-                         smem_desc(sh2 + (q / 8) * (kH2 / 8) * 128, (kH2 / 8) * 128, 128),
-                         smem_desc(sdy + (q / 8) * (kDY / 8) * 128, (kDY / 8) * 128, 128),
-                         idesc_bf16(kRows, kDY, true), acc | (uint32_t)(q > 0));
-            mma_commit(mbar);
+                mma_bf16(tmem + kColAccY, desc_at(m_h2, (q / 8) * (kH2 / 8) * 128),
+                         desc_at(m_dy, (q / 8) * (kDY / 8) * 128), idesc_bf16(kRows, kDY, true),
+                         acc | (uint32_t)(q > 0));
         }
         ok = __syncthreads_and(mbar_wait(mbar, phase & 1));
         ++phase;
@@ -658,15 +710,16 @@ k_shade_backward(Frames fs, Workspace w, const float* __restrict__ features,
         if (!ok) break;
         masked_row(trow + kColG1, h1, smem + L::gg, tid, kGG, 0);   // Q(g1)
         operands_ready();
-        // ---- round 4: dF = (W1^T Q(g1))[:16]; accumulate [Q(g1) ; Q(g2)] [Q(x), 1 | Q(h1)]^T
+        // ---- round 4: dF = (W1^T Q(g1))[:16] (committed alone); then accumulate
+        // [Q(g1) ; Q(g2)] [Q(x), 1 | Q(h1)]^T behind it, on its own barrier
         if (tid == 0) {
-            issue_layer(tmem + kColDX, sgg, 0, kGG, sw1t, kHid, 16);
-            for (int q = 0; q < kRows; q += 16)
-                mma_bf16(tmem + kColAccXH,
-                         smem_desc(sgg + (q / 8) * (kGG / 8) * 128, (kGG / 8) * 128, 128),
-                         smem_desc(sxh + (q / 8) * (kXH / 8) * 128, (kXH / 8) * 128, 128),
-                         idesc_bf16(kRows, kXH, true), acc | (uint32_t)(q > 0));
+            mma_chain(tmem + kColDX, d_gg, d_w1t, kHid / 16, idesc_bf16(kRows, 16), 0);
             mma_commit(mbar);
+            for (int q = 0; q < kRows; q += 16)
+                mma_bf16(tmem + kColAccXH, desc_at(m_gg, (q / 8) * (kGG / 8) * 128),
+                         desc_at(m_xh, (q / 8) * (kXH / 8) * 128), idesc_bf16(kRows, kXH, true),
+                         acc | (uint32_t)(q > 0));
+            mma_commit(gbar);
         }
         acc = 1;
         ok = __syncthreads_and(mbar_wait(mbar, phase & 1));
@@ -686,6 +739,11 @@ k_shade_backward(Frames fs, Workspace w, const float* __restrict__ features,
                                         __uint_as_float(r[4 * q + 3]));
             }
         }
+    }
+    if (ok && acc) {   // the last tile's weight-gradient MMAs
+        ok = __syncthreads_and(mbar_wait(gbar, gphase & 1));
+        ++gphase;
+        tc_fence_after();
     }
     // ---- this CTA's share of the weight gradients: TMEM lane = output row
     float* mine = part + (size_t)blockIdx.x * kShadeParams;
@@ -715,9 +773,12 @@ k_shade_backward(Frames fs, Workspace w, const float* __restrict__ features,
             if (tid == kHid) mine[kOffB3 + o] = __uint_as_float(r[o]);
         }
     } else {
+        // a copy or an MMA did not complete in time: report it, give each
+        // barrier one more bounded wait, then release the tensor memory
         if (tid == 0) atomicOr(&w.state->error, kErrTimeout);
         mbar_wait(wbar, 0);
         if (phase > 0) mbar_wait(mbar, (phase - 1) & 1);
+        if (acc) mbar_wait(gbar, gphase & 1);
         for (int e = tid; e < kShadeParams; e += kRows) mine[e] = 0.0f;
     }
     tc_fence_before();
@@ -726,14 +787,34 @@ k_shade_backward(Frames fs, Workspace w, const float* __restrict__ features,
     if (warp == 0) tmem_dealloc(tmem, kBwdCols);
 }
 
-// Sum of the CTAs' weight-gradient shares, in a fixed order (fp64).
-__global__ void k_shade_reduce(const float* __restrict__ part, int n_part,
-                               float* __restrict__ grad_params) {
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= kShadeParams) return;
-    double s = 0.0;
-    for (int c = 0; c < n_part; ++c) s += (double)part[(size_t)c * kShadeParams + i];
-    grad_params[i] = (float)s;
+// Sum of the CTAs' weight-gradient shares in a fixed order (fp64): a block
+// takes 32 parameters; warp w sums the shares w, w + 16, ... with four
+// independent accumulators (loads in flight), the warps combine in order.
+constexpr int kReduceWarps = 16;
+
+__global__ void __launch_bounds__(32 * kReduceWarps)
+k_shade_reduce(const float* __restrict__ part, int n_part, float* __restrict__ grad_params) {
+    __shared__ double acc[kReduceWarps][32];
+    const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
+    const int i = blockIdx.x * 32 + lane;
+    double s[4] = {0.0, 0.0, 0.0, 0.0};
+    if (i < kShadeParams) {
+        int c = wp;
+        for (; c + 3 * kReduceWarps < n_part; c += 4 * kReduceWarps) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                s[u] += (double)part[(size_t)(c + u * kReduceWarps) * kShadeParams + i];
+        }
+        for (; c < n_part; c += kReduceWarps) s[0] += (double)part[(size_t)c * kShadeParams + i];
+    }
+    acc[wp][lane] = (s[0] + s[1]) + (s[2] + s[3]);
+    __syncthreads();
+    if (wp == 0 && i < kShadeParams) {
+        double t = 0.0;
+#pragma unroll
+        for (int w2 = 0; w2 < kReduceWarps; ++w2) t += acc[w2][lane];
+        grad_params[i] = (float)t;
+    }
 }
 
 // CTAs of a kernel resident per SM, from the documented limits: shared
@@ -805,7 +886,8 @@ cudaError_t launch_shade_backward(const Frames& fs, const Workspace& w, const fl
         fs, w, features, w.shade_img + FwdImage::bytes, grad_rgb, grad_features, w.shade_part);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    k_shade_reduce<<<(kShadeParams + 255) / 256, 256, 0, stream>>>(w.shade_part, grid, grad_params);
+    k_shade_reduce<<<(kShadeParams + 31) / 32, 32 * kReduceWarps, 0, stream>>>(w.shade_part, grid,
+                                                                              grad_params);
     return cudaGetLastError();
 }
 
