@@ -489,6 +489,10 @@ def run_gb300(a):
                             if a.scene == "headline" else None),
                 "algorithmic_flops": fwd_flops, "algorithmic_bytes": fwd_bytes,
                 "hbm_frac": fwd_bytes / fwd_s / 1e9 / hbm,
+                # secondary ceiling: two MUFU operations (exp2, rsqrt) per hit at
+                # 16 per SM and clock
+                "mufu_time_us": 2 * H / (SMS * 16 * float(peaks.get("sm_max_mhz", 2070.0))
+                                         * 1e6) * 1e6,
                 "peak_source": f"FP32: {SMS} SMs x {FP32_LANES} lanes x 2 x "
                                f"{peaks.get('sm_max_mhz', 2070.0)} MHz ({peak_src} clock); "
                                f"HBM: {peak_src} hbm_gbs {hbm}"}
@@ -559,6 +563,11 @@ def run_gb300(a):
                        "l2": "flushed between steps (256 MB write, outside the timed events)",
                        "timing": "CUDA events around a CUDA-graph replay of one step"},
             "msphere_pixel_per_s": world * H / (total_ms / a.steps * 1e-3) / 1e6,
+            "msphere_pixel_per_s_fwd_bwd": H / ((breakdown["forward"] + breakdown["backward"])
+                                                * 1e-3) / 1e6,
+            "step_ms_quantiles": {q: float(np.quantile(step_ms, v)) for q, v in
+                                  (("p10", 0.1), ("p50", 0.5), ("p90", 0.9))},
+            "candidate_tests_per_frame": 256 * M,
             **({"cameras_per_step": K, "camera_by_camera_ms_per_step": per_cam_loop}
                if K > 1 else {}),
             "hits_per_frame": H, "pairs_per_frame": M, "tracked_hits_per_frame": Ht,

@@ -161,3 +161,49 @@ def test_shading_backward_full_size_frame():
     gF, gP = _run_backward([cam], F, dY, params)
     ref = sb.oracle_batch(F, [cam], params.astype(np.float64), dY)
     print(sb.check(dict(dF=gF, params=gP), ref, params.astype(np.float64), "full size"))
+
+
+def test_shading_errors_and_empty_frame():
+    """Call order, channel count and alignment errors; a frame whose pixel
+    count is 0 cannot be made (the ABI rejects width 0), so the smallest frame
+    (1 x 1, one partly filled tile) stands for it."""
+    import torch
+    from splat_rendering_gb300 import pulsar as pl
+    params = torch.from_numpy(scenes.shading_mlp(13)).cuda()
+    cam = scenes._camera(np.eye(3), np.zeros(3), 2.0, 1, 1, 1.0, 9.0, cx=0.4, cy=0.6)
+    r = _renderer_for([cam])
+    F = torch.randn(1, 1, 16, device="cuda")
+    rgb = torch.empty(1, 1, 3, device="cuda")
+    with pytest.raises(pl.PulsarError) as e:      # no frame yet
+        pl.shade_forward(r.ctx, F, params, rgb)
+    assert e.value.code == pl.ERR_STATE
+    with pytest.raises(pl.PulsarError) as e:
+        pl.shade_backward(r.ctx, F, params, rgb, None, torch.empty_like(params))
+    assert e.value.code == pl.ERR_STATE
+    _project(r, [cam])
+    raw = torch.randn(1 * 16 + 1, device="cuda")
+    with pytest.raises(pl.PulsarError) as e:      # features not 16-byte aligned
+        pl.shade_forward(r.ctx, raw[1:], params, rgb)
+    assert e.value.code == pl.ERR_ARG
+    gF = torch.empty(17, device="cuda")
+    with pytest.raises(pl.PulsarError) as e:      # dF not 16-byte aligned
+        pl.shade_backward(r.ctx, F, params, torch.zeros(1, 1, 3, device="cuda"), gF[1:],
+                          torch.empty_like(params))
+    assert e.value.code == pl.ERR_ARG
+    # the 1 x 1 frame against the oracle
+    y = r.shade(F, params)
+    dY = torch.randn(1, 1, 3, device="cuda")
+    gF1, gP1 = r.shade_backward(F, params, dY)
+    assert r.status(raise_on_error=False)[0] == 0
+    Fn, Pn, dYn = F.cpu().numpy(), params.cpu().numpy().astype(np.float64), dY.cpu().numpy()
+    ref = sb.oracle_batch(Fn[None], [cam], Pn, dYn[None])
+    sb.check(dict(y=y.cpu().numpy(), dF=gF1.cpu().numpy(), params=gP1.cpu().numpy()), ref, Pn,
+             "1x1 frame")
+    r.close()
+    # a frame of 3 channels is not a shading input
+    r3 = _renderer_for([cam], C=3)
+    _project(r3, [cam], C=3)
+    with pytest.raises(pl.PulsarError) as e:
+        pl.shade_forward(r3.ctx, F, params, rgb)
+    assert e.value.code == pl.ERR_ARG
+    r3.close()
