@@ -112,6 +112,43 @@ __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Store 16 / 32 consecutive 32-bit columns of this thread's TMEM lane; the
+// stores are complete after tmem_wait_st().
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+        "r"(v[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::
+            "r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+        "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+        "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+        "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// MMA with the A operand in tensor memory (lane = row, two bf16 per column,
+// the even K element in the low half) and B in shared memory.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -427,12 +464,18 @@ __global__ void k_shade_pack(const float* __restrict__ params, unsigned char* __
 }
 
 // ================================================================ forward --
-constexpr int kFwdCols = 64;   // every layer's accumulator at column 0
-constexpr int kXH = kIn + kHid;   // A tile columns: x (32), then the hidden units (64)
+// Every A operand lives in tensor memory, written by the threads with
+// tcgen05.st (two bf16 per 32-bit column, the pixel's row = its lane), so
+// shared memory holds only the weights and no operand passes through it.
+// Columns: the accumulator 0-63 (every layer), x 64-79 (32 inputs; its
+// columns 72-79 -- view direction, ones -- are the bias step of layers 2
+// and 3), the hidden units 80-111.
+constexpr int kFwdCols = 128;
+constexpr uint32_t kColX = 64, kColH = 80;
+constexpr int kXH = kIn + kHid;   // backward A tile columns: x (32), then h1 (64)
 
 struct FwdSmem {
-    static constexpr int act = 0;                         // A [128 x 96]: x | h1, then x | h2
-    static constexpr int img = act + kRows * kXH * 2;     // FwdImage
+    static constexpr int img = 0;                         // FwdImage
     static constexpr int w1 = img + FwdImage::w1;
     static constexpr int w2 = img + FwdImage::w2;
     static constexpr int w3 = img + FwdImage::w3;
@@ -441,6 +484,15 @@ struct FwdSmem {
     static constexpr int taddr = wbar + 8;                // u32
     static constexpr int bytes = taddr + 8;
 };
+
+// The threads' tensor-memory stores are complete, and every thread's earlier
+// tensor-memory accesses are ordered before the MMAs issued next.
+__device__ __forceinline__ void tmem_operands_ready() {
+    tmem_wait_st();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+}
 
 __global__ void __launch_bounds__(kRows)
 k_shade_forward(Frames fs, Workspace w, const float* __restrict__ features,
@@ -467,14 +519,12 @@ k_shade_forward(Frames fs, Workspace w, const float* __restrict__ features,
     operands_ready();
     const uint32_t tmem = *s_taddr;
     const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);   // this warp's TMEM lanes
-    // K-major descriptors: core matrices 128 B apart along K, a row block apart along M/N
-    const uint64_t d_xh = smem_desc(smem_u32(smem + L::act), 128, (kXH / 8) * 128);
+    // B descriptors (K-major; core matrices 128 B apart along K, a row block apart along N)
     const uint64_t d_w1 = smem_desc(smem_u32(smem + L::w1), 128, (kIn / 8) * 128);
     const uint64_t d_w2 = smem_desc(smem_u32(smem + L::w2), 128, (kKB / 8) * 128);
     const uint64_t d_w3 = smem_desc(smem_u32(smem + L::w3), 128, (kKB / 8) * 128);
     uint32_t phase = 0;
     bool ok = true;
-    uint32_t h[kHid / 2];
 
     uint64_t p = (uint64_t)blockIdx.x * kRows + tid;
     float4 fcur[4];
@@ -485,42 +535,56 @@ k_shade_forward(Frames fs, Workspace w, const float* __restrict__ features,
         {
             float in[kIn];
             input_row(fs, P1, p, valid, fcur, in);
+            uint32_t xw[16];
 #pragma unroll
-            for (int j = 0; j < kIn / 8; ++j) put8(smem + L::act, tid, 8 * j, kXH, in + 8 * j);
+            for (int j = 0; j < 16; ++j) xw[j] = bf16x2(in[2 * j], in[2 * j + 1]);
+            tmem_st16(trow + kColX, xw);
         }
         // the next tile's features load while this tile runs through the tensor cores
         load_features(features, p + stride, p + stride < n_pix, fcur);
-        operands_ready();
+        tmem_operands_ready();
         if (tid == 0) {
-            mma_chain(tmem, d_xh, d_w1, kIn / 16, idesc_bf16(kRows, kHid), 0);
+#pragma unroll
+            for (int s2 = 0; s2 < kIn / 16; ++s2)
+                mma_bf16_ta(tmem, tmem + kColX + 8 * s2, desc_at(d_w1, 256u * s2),
+                            idesc_bf16(kRows, kHid), s2 > 0);
             mma_commit(mbar);
         }
         ok = __syncthreads_and(mbar_wait(mbar, phase & 1));   // one decision for all
         ++phase;
         tc_fence_after();
         if (!ok) break;
-        relu_row<32>(trow, smem + L::act, tid, kXH, kIn, h);   // h1 (layer 1 is complete)
-        operands_ready();
-        if (tid == 0) {   // the bias step over x's columns 16-31, then the 64 hidden units
-            mma_chain(tmem, desc_at(d_xh, 256), d_w2, kKB / 16, idesc_bf16(kRows, kHid), 0);
-            mma_commit(mbar);
+#pragma unroll
+        for (int layer = 2; layer <= 3; ++layer) {
+            {   // h = bf16(ReLU(D)) of this row into the hidden columns
+                uint32_t r[4][16], h[32];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) tmem_ld16(trow + (uint32_t)(16 * q), r[q]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    h[j] = bf16x2_relu(__uint_as_float(r[j / 8][(2 * j) % 16]),
+                                       __uint_as_float(r[j / 8][(2 * j + 1) % 16]));
+                tmem_st32(trow + kColH, h);
+            }
+            tmem_operands_ready();
+            if (tid == 0) {   // the bias step over x's columns 16-31, then the 64 hidden units
+                const uint64_t d_w = layer == 2 ? d_w2 : d_w3;
+                const uint32_t id = idesc_bf16(kRows, layer == 2 ? kHid : kOutPad);
+                mma_bf16_ta(tmem, tmem + kColX + 8, d_w, id, 0);
+#pragma unroll
+                for (int s2 = 0; s2 < kHid / 16; ++s2)
+                    mma_bf16_ta(tmem, tmem + kColH + 8 * s2, desc_at(d_w, 256u * (s2 + 1)), id, 1);
+                mma_commit(mbar);
+            }
+            ok = __syncthreads_and(mbar_wait(mbar, phase & 1));
+            ++phase;
+            tc_fence_after();
+            if (!ok) break;
         }
-        ok = __syncthreads_and(mbar_wait(mbar, phase & 1));
-        ++phase;
-        tc_fence_after();
         if (!ok) break;
-        relu_row<32>(trow, smem + L::act, tid, kXH, kIn, h);   // h2 replaces h1 (layer 2 is complete)
-        operands_ready();
-        if (tid == 0) {
-            mma_chain(tmem, desc_at(d_xh, 256), d_w3, kKB / 16, idesc_bf16(kRows, kOutPad), 0);
-            mma_commit(mbar);
-        }
-        ok = __syncthreads_and(mbar_wait(mbar, phase & 1));
-        ++phase;
-        tc_fence_after();
-        if (!ok) break;
-        // y = D3; the next tile's operand writes need no further barrier:
-        // layer 3 is complete and this row's accumulator is read here
+        // y = D3; the next tile's stores need no further barrier: layer 3 is
+        // complete and this row's accumulator is read here
         uint32_t r[16];
         tmem_ld16(trow, r);
         tmem_wait_ld();
