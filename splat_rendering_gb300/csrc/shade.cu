@@ -9,15 +9,18 @@
 //   fp32 biases)
 //
 // Both kernels run persistent CTAs of 128 threads over 128-pixel tiles, one
-// thread per pixel (one row of M = 128).  A thread writes its row of a
-// layer's A operand into shared memory (no-swizzle K-major layout: 8-row x
-// 16-byte core matrices), one thread issues the layer's tcgen05.mma into the
-// CTA's tensor memory and commits to an mbarrier, and every thread reads its
-// row of the accumulator back with tcgen05.ld for the epilogue (bias, ReLU,
-// bf16 rounding) that writes the next operand.  Weights are staged once per
-// CTA as B operands (N x K, K-major).  Every mbarrier wait is bounded: on
-// timeout the CTA latches an error, stops issuing and frees its tensor
-// memory.
+// thread per pixel (one row of M = 128, one TMEM lane).  Per layer the
+// threads write their rows of the A operand, one thread issues the layer's
+// tcgen05.mma into the CTA's tensor memory and commits to an mbarrier, and
+// every thread reads its accumulator row back with tcgen05.ld for the
+// epilogue (ReLU and the bf16 rounding in one convert; the biases are added
+// by the MMA itself, see the weight images).  The forward keeps every A
+// operand in tensor memory (tcgen05.st by the threads, A-from-TMEM MMAs);
+// the backward writes them to shared memory (no-swizzle K-major layout:
+// 8-row x 16-byte core matrices), where its weight-gradient MMAs need them.
+// Weights are packed once per call and bulk-copied by every CTA as the B
+// operands (N x K, K-major).  Every mbarrier wait is bounded: on timeout the
+// CTA latches an error, stops issuing and frees its tensor memory.
 //
 // The backward contracts over pixels for the weight gradients: the
 // activation tiles the thread rows wrote (pixel x unit, K-major) are the
