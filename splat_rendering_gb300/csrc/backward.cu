@@ -114,8 +114,11 @@ k_backward(Frames fs, Workspace w, const float* __restrict__ features,
     const float mg = inside ? w.mg[p] : 0.0f;
     const float iw = inside ? 1.0f / w.wsum[p] : 0.0f;
     float gk[4] = {0.f, 0.f, 0.f, 0.f};   // d/d(fx, fy, cx, cy)
-    const int pos0 = inside ? w.ids[p] : -1;     // slot 0 of the backward-information buffer
-    const float d0 = inside ? w.dtr[p] : 0.0f;
+    // the pixel's tracked slots are in list order, so the slots of one batch
+    // are a run: a cursor walks them across the batches, each slot read once
+    int k = 0;
+    int pos = inside ? w.ids[p] : -1;   // slot k's list position (-1: no more hits)
+    float d = inside ? w.dtr[p] : 0.0f;
 
     for (uint32_t b0 = start; b0 < end; b0 += NB) {
         const int nb = (int)min((uint32_t)NB, end - b0);
@@ -126,20 +129,17 @@ k_backward(Frames fs, Workspace w, const float* __restrict__ features,
         cp_async_wait_all();
         __syncthreads();
         const int base = (int)(b0 - start);
-        // slot k+1's position and distance factor are loaded while slot k is processed
-        int pos_next = pos0;
-        float d_next = d0;
-        for (int k = 0; k < f.n_track; ++k) {
-            // this pixel's k-th tracked hit, if its list position is in the batch
-            const int pos = pos_next;
-            const float d = d_next;
-            if (__ballot_sync(0xffffffffu, pos >= 0) == 0u) break;   // -1 padded at the end
-            if (k + 1 < f.n_track && inside) {
-                pos_next = w.ids[(uint32_t)(k + 1) * P + p];
-                d_next = w.dtr[(uint32_t)(k + 1) * P + p];
-            }
+        for (;;) {
+            // this pixel's next tracked hit, if its list position is in the batch
+            const bool valid = pos >= base && pos < base + nb;
+            if (__ballot_sync(0xffffffffu, valid) == 0u) break;
             const int j = pos - base;
-            const bool valid = pos >= 0 && j >= 0 && j < nb;
+            const float dk = d;
+            if (valid) {   // slot k+1 loads while slot k is processed
+                ++k;
+                pos = k < f.n_track ? w.ids[(uint32_t)k * P + p] : -1;
+                d = k < f.n_track ? w.dtr[(uint32_t)k * P + p] : 0.0f;
+            }
             float v[NV];
 #pragma unroll
             for (int q = 0; q < NV; ++q) v[q] = 0.0f;
@@ -155,7 +155,7 @@ k_backward(Frames fs, Workspace w, const float* __restrict__ features,
                 const float rq = sqrtf(Q * iqq);                 // rho / c.z (orthographic: rho)
                 const float o = ex.z;
                 const float E = exp2f(__fsub_rn(ex.x, mg) + ex.y);   // exponents in log2 units
-                const float wt = o * d * E;
+                const float wt = o * dk * E;
                 float sdot = 0.0f;
 #pragma unroll
                 for (int c = 0; c < CMAX; ++c) {
@@ -166,7 +166,7 @@ k_backward(Frames fs, Workspace w, const float* __restrict__ features,
                     }
                 }
                 const float sj = sdot * iw;                      // dL/dw = <G, f - F> / W
-                v[4] = sj * d * E * (1.0f + ex.x * 0.693147181f);   // dw/do = d E (1 + o z~/gamma)
+                v[4] = sj * dk * E * (1.0f + ex.x * 0.693147181f);   // dw/do = d E (1 + o z~/gamma)
                 if (want_geom && !cut) {
                     const float Z = geo.z, reff = geo.w;
                     const float ireff = 1.0f / reff;
@@ -186,7 +186,7 @@ k_backward(Frames fs, Workspace w, const float* __restrict__ features,
                     // -d'(x) rho / r_eff^2; linear d' = -1, Gaussian d' = -9 x exp(-4.5
                     // x^2) / (1 - e^-4.5) = -9 x (d + e^-4.5 / (1 - e^-4.5))
                     const float ddx = (f.flags & kParamGaussian)
-                                          ? -9.0f * rho * ireff * (d + kGaussTailRatio)
+                                          ? -9.0f * rho * ireff * (dk + kGaussTailRatio)
                                           : -1.0f;
                     const float g_rho = sE * ddx * ireff;
                     const float g_reff = -sE * ddx * rho * ireff * ireff;
