@@ -42,7 +42,7 @@ __device__ __forceinline__ void red_add_v4(float4* addr, float a, float b, float
 // smem < 48 KB).
 template <int CMAX>
 struct BwdBatch {
-    static constexpr int n = CMAX <= 4 ? 512 : (CMAX <= 16 ? 256 : (CMAX <= 32 ? 192 : 128));
+    static constexpr int n = CMAX <= 4 ? 512 : (CMAX <= 8 ? 256 : (CMAX <= 16 ? 384 : (CMAX <= 32 ? 192 : 128)));
 };
 
 template <int CMAX, bool MULTI>
