@@ -65,7 +65,7 @@ struct FwdSmem {
 };
 
 template <int CMAX, bool MULTI>
-__global__ void __launch_bounds__(kFwdThreads, CMAX <= 4 ? 4 : (CMAX <= 16 ? 2 : 1))
+__global__ void __launch_bounds__(kFwdThreads, CMAX <= 4 ? 4 : (CMAX <= 16 ? 3 : 1))
 k_forward(Frames fs, Workspace w, const float* __restrict__ features, const float* __restrict__ bg,
           float* __restrict__ image) {
     using L = FwdSmem<CMAX>;
