@@ -50,6 +50,7 @@ __global__ void __launch_bounds__(kBwdThreads, CMAX <= 4 ? 4 : (CMAX <= 16 ? 2 :
 k_backward(Frames fs, Workspace w, const float* __restrict__ features,
            const float* __restrict__ image, const float* __restrict__ grad_image,
            float* __restrict__ grad_opacity, float* __restrict__ grad_features, int mode) {
+    pdl_begin();
     // mode bit 0: geometry gradients wanted; bit 1: feature gradient rows are
     // 16-byte aligned with C a multiple of 4 (vector reductions)
     const bool want_geom = (mode & 1) != 0;
@@ -314,6 +315,7 @@ __global__ void __launch_bounds__(kFinThreads)
 k_finalize_one_cam(Frames fs, Workspace w, const float* __restrict__ pos, float* __restrict__ grad_pos,
            float* __restrict__ grad_radius, float* __restrict__ grad_opacity,
            float* __restrict__ grad_features, int vec_ok) {
+    pdl_begin();
     __shared__ float s_part[kFinThreads / 32][12];
     const Frame& f = fs.f[0];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -399,6 +401,7 @@ __global__ void __launch_bounds__(kFinThreads, 4)
 k_finalize_cams(Frames fs, Workspace w, const float* __restrict__ pos, float* __restrict__ grad_pos,
            float* __restrict__ grad_radius, float* __restrict__ grad_opacity,
            float* __restrict__ grad_features, int vec_ok) {
+    pdl_begin();
     __shared__ float s_part[kFinThreads / 32][12];
     const Frame& f0 = fs.f[0];
     const int n = f0.n, n_cams = f0.n_cams;
@@ -518,6 +521,7 @@ k_finalize_cams(Frames fs, Workspace w, const float* __restrict__ pos, float* __
 // loads and combine through shared memory.
 __global__ void __launch_bounds__(kCamThreads)
 k_camera_reduce(Frames fs, Workspace w, int fin_blocks, float* __restrict__ grad_cam) {
+    pdl_begin();
     static_assert(kCamThreads == 1024, "two warps per output");
     __shared__ float2 s_half[16][2];
     const int cam = blockIdx.x;
@@ -556,15 +560,15 @@ k_camera_reduce(Frames fs, Workspace w, int fin_blocks, float* __restrict__ grad
 }
 
 template <int CMAX>
-void launch_bwd_c(const Frames& fs, const Workspace& w, const float* features, const float* image,
-                  const float* grad_image, float* grad_opacity, float* grad_features,
-                  int mode, cudaStream_t stream) {
+cudaError_t launch_bwd_c(const Frames& fs, const Workspace& w, const float* features,
+                         const float* image, const float* grad_image, float* grad_opacity,
+                         float* grad_features, int mode, cudaStream_t stream) {
+    const dim3 grid(fs.f[0].n_tiles_all), block(kBwdThreads);
     if (fs.f[0].n_cams == 1)
-        k_backward<CMAX, false><<<fs.f[0].n_tiles_all, kBwdThreads, 0, stream>>>(
-            fs, w, features, image, grad_image, grad_opacity, grad_features, mode);
-    else
-        k_backward<CMAX, true><<<fs.f[0].n_tiles_all, kBwdThreads, 0, stream>>>(
-            fs, w, features, image, grad_image, grad_opacity, grad_features, mode);
+        return launch_pdl(k_backward<CMAX, false>, grid, block, 0, stream, fs, w, features, image,
+                          grad_image, grad_opacity, grad_features, mode);
+    return launch_pdl(k_backward<CMAX, true>, grid, block, 0, stream, fs, w, features, image,
+                      grad_image, grad_opacity, grad_features, mode);
 }
 
 }  // namespace
@@ -578,24 +582,26 @@ cudaError_t launch_backward(const Frames& fs, const Workspace& w, const float* p
     const int feat_v4 = (f.channels % 4 == 0 && grad_features &&
                          (reinterpret_cast<uintptr_t>(grad_features) & 15u) == 0) ? 2 : 0;
     const int mode = want_geom | feat_v4;
+    cudaError_t e;
     if (f.channels == 3)
-        launch_bwd_c<3>(fs, w, features, image, grad_image, grad_opacity, grad_features,
-                        mode, stream);
+        e = launch_bwd_c<3>(fs, w, features, image, grad_image, grad_opacity, grad_features, mode,
+                            stream);
     else if (f.channels <= 4)
-        launch_bwd_c<4>(fs, w, features, image, grad_image, grad_opacity, grad_features,
-                        mode, stream);
+        e = launch_bwd_c<4>(fs, w, features, image, grad_image, grad_opacity, grad_features, mode,
+                            stream);
     else if (f.channels <= 8)
-        launch_bwd_c<8>(fs, w, features, image, grad_image, grad_opacity, grad_features,
-                        mode, stream);
+        e = launch_bwd_c<8>(fs, w, features, image, grad_image, grad_opacity, grad_features, mode,
+                            stream);
     else if (f.channels <= 16)
-        launch_bwd_c<16>(fs, w, features, image, grad_image, grad_opacity, grad_features,
-                         mode, stream);
+        e = launch_bwd_c<16>(fs, w, features, image, grad_image, grad_opacity, grad_features,
+                             mode, stream);
     else if (f.channels <= 32)
-        launch_bwd_c<32>(fs, w, features, image, grad_image, grad_opacity, grad_features,
-                         mode, stream);
+        e = launch_bwd_c<32>(fs, w, features, image, grad_image, grad_opacity, grad_features,
+                             mode, stream);
     else
-        launch_bwd_c<kMaxChannels>(fs, w, features, image, grad_image, grad_opacity,
-                                   grad_features, mode, stream);
+        e = launch_bwd_c<kMaxChannels>(fs, w, features, image, grad_image, grad_opacity,
+                                       grad_features, mode, stream);
+    if (e != cudaSuccess) return e;
     const bool norm = (f.flags & kParamNormalize) != 0;
     if (want_geom || norm) {
         const int blocks = (f.n + 4 * kFinThreads - 1) / (4 * kFinThreads);
@@ -603,15 +609,16 @@ cudaError_t launch_backward(const Frames& fs, const Workspace& w, const float* p
         const int vec_ok = ((reinterpret_cast<uintptr_t>(pos) | reinterpret_cast<uintptr_t>(grad_pos) |
                              reinterpret_cast<uintptr_t>(grad_radius)) & 15u) == 0;
         if (blocks > 0 && f.n_cams == 1)
-            k_finalize_one_cam<<<blocks, kFinThreads, 0, stream>>>(
-                fs, w, pos, grad_pos, grad_radius, grad_opacity, grad_features, vec_ok);
+            e = launch_pdl(k_finalize_one_cam, dim3(blocks), dim3(kFinThreads), 0, stream, fs, w,
+                           pos, grad_pos, grad_radius, grad_opacity, grad_features, vec_ok);
         else if (blocks > 0)
-            k_finalize_cams<<<blocks, kFinThreads, 0, stream>>>(
-                fs, w, pos, grad_pos, grad_radius, grad_opacity, grad_features, vec_ok);
-        if (want_geom)
-            k_camera_reduce<<<f.n_cams, kCamThreads, 0, stream>>>(fs, w, blocks, grad_cam);
+            e = launch_pdl(k_finalize_cams, dim3(blocks), dim3(kFinThreads), 0, stream, fs, w, pos,
+                           grad_pos, grad_radius, grad_opacity, grad_features, vec_ok);
+        if (e == cudaSuccess && want_geom)
+            e = launch_pdl(k_camera_reduce, dim3(f.n_cams), dim3(kCamThreads), 0, stream, fs, w,
+                           blocks, grad_cam);
     }
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace pulsar

@@ -29,6 +29,7 @@ constexpr int kSortCap = 2048;
 constexpr int kWarpSortMax = 512;   // lists sorted by one warp in registers
 
 __global__ void __launch_bounds__(kScanThreads) k_tile_scan(Frames fs, Workspace w) {
+    pdl_begin();
     __shared__ uint32_t s_warp[kScanThreads / 32];
     const Frame& f = fs.f[0];
     const int n_tiles = (int)f.n_tiles_all;   // every camera's tiles, camera after camera
@@ -73,6 +74,7 @@ __global__ void __launch_bounds__(kScanThreads) k_tile_scan(Frames fs, Workspace
 }
 
 __global__ void __launch_bounds__(kEmitThreads) k_emit(Frames fs, Workspace w) {
+    pdl_begin();
     const Frame& f = fs.f[0];
     const uint32_t m = w.state->n_pairs;
     if (m > f.max_pairs) return;   // overflowed frame: the capacity error is latched
@@ -289,6 +291,7 @@ __device__ void block_sort_long(const Workspace& w, uint32_t start, int n, unsig
 // list has at most kWarpSortMax entries, then the block sorts the longer ones
 // together.
 __global__ void __launch_bounds__(kSortThreads) k_tile_sort(Frames fs, Workspace w) {
+    pdl_begin();
     const Frame& f = fs.f[0];
     const int n_tiles = (int)f.n_tiles_all;
     __shared__ unsigned long long s[kSortCap];                        // 16 KB
@@ -326,13 +329,15 @@ __global__ void __launch_bounds__(kSortThreads) k_tile_sort(Frames fs, Workspace
 
 cudaError_t launch_bin(const Frames& fs, const Workspace& w, cudaStream_t stream) {
     const Frame& f = fs.f[0];
-    k_tile_scan<<<1, kScanThreads, 0, stream>>>(fs, w);
-    if (f.n > 0) {
-        k_emit<<<152 * 8, kEmitThreads, 0, stream>>>(fs, w);
-        k_tile_sort<<<((int)f.n_tiles_all + kTilesPerSortBlock - 1) / kTilesPerSortBlock,
-                      kSortThreads, 0, stream>>>(fs, w);
+    cudaError_t e = launch_pdl(k_tile_scan, dim3(1), dim3(kScanThreads), 0, stream, fs, w);
+    if (e == cudaSuccess && f.n > 0) {
+        e = launch_pdl(k_emit, dim3(152 * 8), dim3(kEmitThreads), 0, stream, fs, w);
+        if (e == cudaSuccess)
+            e = launch_pdl(k_tile_sort,
+                           dim3(((int)f.n_tiles_all + kTilesPerSortBlock - 1) / kTilesPerSortBlock),
+                           dim3(kSortThreads), 0, stream, fs, w);
     }
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace pulsar

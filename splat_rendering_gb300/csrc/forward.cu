@@ -68,6 +68,7 @@ template <int CMAX, bool MULTI>
 __global__ void __launch_bounds__(kFwdThreads, CMAX <= 4 ? 4 : (CMAX <= 16 ? 3 : 1))
 k_forward(Frames fs, Workspace w, const float* __restrict__ features, const float* __restrict__ bg,
           float* __restrict__ image) {
+    pdl_begin();
     using L = FwdSmem<CMAX>;
     constexpr int NB = L::NB;
     constexpr int FS = L::FS;
@@ -366,13 +367,12 @@ template <int CMAX>
 cudaError_t launch_c(const Frames& fs, const Workspace& w, const float* features, const float* bg,
                      float* image, cudaStream_t stream) {
     constexpr int bytes = FwdSmem<CMAX>::bytes;
+    const dim3 grid(fs.f[0].n_tiles_all), block(kFwdThreads);
     if (fs.f[0].n_cams == 1)
-        k_forward<CMAX, false><<<fs.f[0].n_tiles_all, kFwdThreads, bytes, stream>>>(
-            fs, w, features, bg, image);
-    else
-        k_forward<CMAX, true><<<fs.f[0].n_tiles_all, kFwdThreads, bytes, stream>>>(
-            fs, w, features, bg, image);
-    return cudaGetLastError();
+        return launch_pdl(k_forward<CMAX, false>, grid, block, bytes, stream, fs, w, features, bg,
+                          image);
+    return launch_pdl(k_forward<CMAX, true>, grid, block, bytes, stream, fs, w, features, bg,
+                      image);
 }
 
 template <int CMAX>

@@ -20,6 +20,7 @@ constexpr int kProjectThreads = 256;
 __global__ void __launch_bounds__(kProjectThreads, 8)
 k_project(Frames fs, Workspace w, const float* __restrict__ pos, const float* __restrict__ radius,
           const float* __restrict__ opacity) {
+    pdl_begin();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     const int lane = threadIdx.x & 31;
     const int n = fs.f[0].n;
@@ -160,8 +161,8 @@ cudaError_t launch_project(const Frames& fs, const Workspace& w, const float* po
     const int n = fs.f[0].n;
     if (n == 0) return cudaSuccess;
     const int blocks = (n + kProjectThreads - 1) / kProjectThreads;
-    k_project<<<blocks, kProjectThreads, 0, stream>>>(fs, w, pos, radius, opacity);
-    return cudaGetLastError();
+    return launch_pdl(k_project, dim3(blocks), dim3(kProjectThreads), 0, stream, fs, w, pos, radius,
+                      opacity);
 }
 
 }  // namespace pulsar

@@ -303,6 +303,19 @@ __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
     const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(dst));
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(s), "l"(src) : "memory");
 }
+// Programmatic dependent launch: the kernels of the render path are launched
+// with programmatic stream serialization, so a kernel's grid is set up while
+// the previous one finishes, and each begins by waiting until the previous
+// grid has completed and its memory is visible -- before any global memory
+// access, so no read or write overlaps the previous kernel.  (No early
+// trigger: CTAs launched early and parked on the wait cost the previous
+// kernel's tail more than they saved, measured on the headline step.)
+// Launched without the attribute, or with no previous grid in flight, the
+// wait returns at once.
+__device__ __forceinline__ void pdl_begin() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
@@ -412,6 +425,24 @@ inline void fill_frame(Frame& f, const float R[9], const float t[3], float fx, f
 
 // ---------------------------------------------------------- launchers --
 // (defined in the .cu files; all enqueue on `stream` and never synchronise)
+// Launch with programmatic stream serialization (the kernel must begin with
+// pdl_begin()).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 cudaError_t launch_project(const Frames& fs, const Workspace& w, const float* pos,
                            const float* radius, const float* opacity, cudaStream_t stream);
 cudaError_t launch_bin(const Frames& fs, const Workspace& w, cudaStream_t stream);
