@@ -452,6 +452,7 @@ constexpr int kPackElems = kHid * kIn * 2 + kHid * kKB * 2 + kOutPad * kKB + kHi
                            kHid * kHid + 16 * kHid;
 
 __global__ void k_shade_pack(const float* __restrict__ params, unsigned char* __restrict__ img) {
+    pdl_begin();
     int e = blockIdx.x * blockDim.x + threadIdx.x;
 #pragma unroll
     for (int s = 0; s < (int)(sizeof(kPack) / sizeof(kPack[0])); ++s) {
@@ -500,6 +501,7 @@ __device__ __forceinline__ void tmem_operands_ready() {
 __global__ void __launch_bounds__(kRows)
 k_shade_forward(Frames fs, Workspace w, const float* __restrict__ features,
                 const unsigned char* __restrict__ img, float* __restrict__ rgb) {
+    pdl_begin();
     using L = FwdSmem;
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + L::mbar);
@@ -653,6 +655,7 @@ __global__ void __launch_bounds__(kRows, 2)
 k_shade_backward(Frames fs, Workspace w, const float* __restrict__ features,
                  const unsigned char* __restrict__ img, const float* __restrict__ grad_rgb,
                  float* __restrict__ grad_features, float* __restrict__ part) {
+    pdl_begin();
     using L = BwdSmem;
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + L::mbar);
@@ -861,6 +864,7 @@ constexpr int kReduceWarps = 16;
 
 __global__ void __launch_bounds__(32 * kReduceWarps)
 k_shade_reduce(const float* __restrict__ part, int n_part, float* __restrict__ grad_params) {
+    pdl_begin();
     __shared__ double acc[kReduceWarps][32];
     const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
     const int i = blockIdx.x * 32 + lane;
@@ -931,11 +935,11 @@ cudaError_t launch_shade_forward(const Frames& fs, const Workspace& w, const flo
     const uint64_t n_tiles = (fs.f[0].pix_all + kRows - 1) / kRows;
     if (n_tiles == 0) return cudaSuccess;
     const int grid = (int)(n_tiles < (uint64_t)grid_cap ? n_tiles : (uint64_t)grid_cap);
-    k_shade_pack<<<(kPackElems + 255) / 256, 256, 0, stream>>>(params, w.shade_img);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(k_shade_pack, dim3((kPackElems + 255) / 256), dim3(256), 0, stream,
+                               params, w.shade_img);
     if (e != cudaSuccess) return e;
-    k_shade_forward<<<grid, kRows, FwdSmem::bytes, stream>>>(fs, w, features, w.shade_img, rgb);
-    return cudaGetLastError();
+    return launch_pdl(k_shade_forward, dim3(grid), dim3(kRows), FwdSmem::bytes, stream, fs, w,
+                      features, (const unsigned char*)w.shade_img, rgb);
 }
 
 cudaError_t launch_shade_backward(const Frames& fs, const Workspace& w, const float* features,
@@ -946,16 +950,15 @@ cudaError_t launch_shade_backward(const Frames& fs, const Workspace& w, const fl
     if (n_tiles == 0)
         return cudaMemsetAsync(grad_params, 0, kShadeParams * sizeof(float), stream);
     const int grid = (int)(n_tiles < (uint64_t)grid_cap ? n_tiles : (uint64_t)grid_cap);
-    k_shade_pack<<<(kPackElems + 255) / 256, 256, 0, stream>>>(params, w.shade_img);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(k_shade_pack, dim3((kPackElems + 255) / 256), dim3(256), 0, stream,
+                               params, w.shade_img);
     if (e != cudaSuccess) return e;
-    k_shade_backward<<<grid, kRows, BwdSmem::bytes, stream>>>(
-        fs, w, features, w.shade_img + FwdImage::bytes, grad_rgb, grad_features, w.shade_part);
-    e = cudaGetLastError();
+    e = launch_pdl(k_shade_backward, dim3(grid), dim3(kRows), BwdSmem::bytes, stream, fs, w,
+                   features, (const unsigned char*)(w.shade_img + FwdImage::bytes), grad_rgb,
+                   grad_features, w.shade_part);
     if (e != cudaSuccess) return e;
-    k_shade_reduce<<<(kShadeParams + 31) / 32, 32 * kReduceWarps, 0, stream>>>(w.shade_part, grid,
-                                                                              grad_params);
-    return cudaGetLastError();
+    return launch_pdl(k_shade_reduce, dim3((kShadeParams + 31) / 32), dim3(32 * kReduceWarps), 0,
+                      stream, (const float*)w.shade_part, grid, grad_params);
 }
 
 }  // namespace pulsar
