@@ -235,6 +235,16 @@ int pulsar_shade_backward(pulsar_ctx_t ctx, const float* features, const float* 
                           const float* grad_rgb, float* grad_features, float* grad_params,
                           void* stream);
 
+/* Test hook for failure detection without a GPU fault.  With
+ * PULSAR_INJECT_SHADE_TIMEOUT the shading kernels issue no tensor-core work,
+ * so their bounded waits (0.25 s of wall time each) run out: the call still
+ * completes, frees its tensor memory, and pulsar_status reports
+ * PULSAR_ERR_TIMEOUT.  The injection stays armed until pulsar_status has
+ * reported (which clears it); 0 disarms it.  Enqueued on `stream`.  Errors:
+ * PULSAR_ERR_ARG (NULL context, unknown bits). */
+#define PULSAR_INJECT_SHADE_TIMEOUT 1
+int pulsar_debug_inject(pulsar_ctx_t ctx, int what, void* stream);
+
 /* Static string for an error code. */
 const char* pulsar_strerror(int code);
 

@@ -310,6 +310,10 @@ int pulsar_status(pulsar_ctx_t c, void* stream, int64_t* n_pairs, int64_t* n_hit
     const DevState& h = *c->host_state;
     if (n_pairs) *n_pairs = (int64_t)h.n_pairs;
     if (n_hits) *n_hits = (int64_t)h.hits;
+    if (h.inject) {
+        const uint32_t zero = 0;
+        cudaMemcpy(&c->ws.state->inject, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    }
     if (h.error) {
         const uint32_t zero = 0;
         cudaMemcpy(&c->ws.state->error, &zero, sizeof(zero), cudaMemcpyHostToDevice);
@@ -317,6 +321,14 @@ int pulsar_status(pulsar_ctx_t c, void* stream, int64_t* n_pairs, int64_t* n_hit
         if (h.error & kErrTimeout) return PULSAR_ERR_TIMEOUT;
     }
     return PULSAR_OK;
+}
+
+int pulsar_debug_inject(pulsar_ctx_t c, int what, void* stream) {
+    if (!c || (what & ~(int)kInjectShadeTimeout) != 0) return PULSAR_ERR_ARG;
+    DeviceGuard guard(c->device);
+    const uint32_t v = (uint32_t)what;
+    return cuda_err(cudaMemcpyAsync(&c->ws.state->inject, &v, sizeof(v), cudaMemcpyHostToDevice,
+                                    as_stream(stream)));
 }
 
 int64_t pulsar_debug_copy(pulsar_ctx_t c, int what, void* dst, int64_t bytes, void* stream) {

@@ -29,6 +29,7 @@ constexpr float kPi = 3.14159265358979f;
 // Device error bits (latched in DevState::error).
 constexpr uint32_t kErrCapacity = 1u;
 constexpr uint32_t kErrTimeout = 2u;    // a bounded wait on the tensor cores gave up
+constexpr uint32_t kInjectShadeTimeout = 1u;   // shading kernels issue no tensor-core work
 
 // Per-camera constants of a frame (all cameras of a batch share the image
 // size, the parameters and the spheres).
@@ -68,7 +69,7 @@ struct DevState {
     unsigned long long hits;    // hit pairs composited by the last forward
     uint32_t n_pairs;           // M of the last bin
     uint32_t error;             // latched kErr* bits
-    uint32_t pad;
+    uint32_t inject;            // test hook bits (kInject*), cleared by pulsar_status
     uint32_t pair_cursor;       // staged pairs reserved by the projection (zero between frames)
 };
 

@@ -39,7 +39,7 @@ constexpr int kRows = 128;           // pixels per tile (M = 128), one thread ea
 constexpr int kIn = 32;              // 19 inputs, zero padded to two K = 16 steps
 constexpr int kHid = 64;
 constexpr int kOutPad = 16;          // 3 outputs padded to the smallest N for M = 128
-constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr unsigned long long kWaitNs = 250000000ull;   // bound of every mbarrier wait (0.25 s)
 
 // flat parameter layout: W1 [64][19], b1 [64], W2 [64][64], b2 [64], W3 [3][64], b3 [3]
 constexpr int kOffB1 = kHid * 19;
@@ -85,9 +85,18 @@ __device__ __forceinline__ void mma_commit(uint64_t* mbar) {
         : "memory");
 }
 
-// Bounded wait for the mbarrier phase of the given parity; false on timeout.
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the mbarrier phase of the given parity, at most kWaitNs of wall
+// time (try_wait itself may suspend for an unspecified while, so the bound is
+// on the global timer, not on the number of polls); false on timeout.
 __device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity) {
-    for (uint32_t it = 0; it < kWaitLimit; ++it) {
+    const unsigned long long t0 = global_ns();
+    for (;;) {
         uint32_t done;
         asm volatile(
             "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
@@ -96,8 +105,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity) {
             : "r"(smem_u32(mbar)), "r"(parity)
             : "memory");
         if (done) return true;
+        if (global_ns() - t0 > kWaitNs) return false;
     }
-    return false;
 }
 
 // 16 consecutive fp32 columns of this thread's TMEM lane (warp w owns lanes
@@ -531,6 +540,8 @@ k_shade_forward(Frames fs, Workspace w, const float* __restrict__ features,
     uint32_t phase = 0;
     bool ok = true;
 
+    // test hook: issue nothing, so the first wait runs out
+    const bool issue = (w.state->inject & kInjectShadeTimeout) == 0u;
     uint64_t p = (uint64_t)blockIdx.x * kRows + tid;
     float4 fcur[4];
     load_features(features, p, p < n_pix, fcur);
@@ -548,7 +559,7 @@ k_shade_forward(Frames fs, Workspace w, const float* __restrict__ features,
         // the next tile's features load while this tile runs through the tensor cores
         load_features(features, p + stride, p + stride < n_pix, fcur);
         tmem_operands_ready();
-        if (tid == 0) {
+        if (tid == 0 && issue) {
 #pragma unroll
             for (int s2 = 0; s2 < kIn / 16; ++s2)
                 mma_bf16_ta(tmem, tmem + kColX + 8 * s2, desc_at(d_w1, 256u * s2),
@@ -707,6 +718,8 @@ k_shade_backward(Frames fs, Workspace w, const float* __restrict__ features,
     uint32_t acc = 0;   // 0 until the first tile's weight-gradient MMAs are issued
     uint32_t h1[kHid / 2];
 
+    // test hook: issue nothing, so the first wait runs out
+    const bool issue = (w.state->inject & kInjectShadeTimeout) == 0u;
     uint64_t p = (uint64_t)blockIdx.x * kRows + tid;
     float4 fcur[4];
     float dcur[3];
@@ -740,7 +753,7 @@ k_shade_backward(Frames fs, Workspace w, const float* __restrict__ features,
         }
         operands_ready();
         // ---- round 1: z1 = W1 Q(x) + b1
-        if (tid == 0) {
+        if (tid == 0 && issue) {
             mma_chain(tmem + kColZ1, d_xh, d_w1, kIn / 16, idesc_bf16(kRows, kHid), 0);
             mma_commit(mbar);
         }

@@ -55,7 +55,7 @@ class Params(ctypes.Structure):
 EXPORTS = ("pulsar_create", "pulsar_create_cams", "pulsar_destroy", "pulsar_project",
            "pulsar_project_cams", "pulsar_bin", "pulsar_shade_forward", "pulsar_shade_backward",
            "pulsar_forward", "pulsar_backward", "pulsar_status", "pulsar_strerror",
-           "pulsar_debug_copy", "pulsar_render_noalloc")
+           "pulsar_debug_copy", "pulsar_debug_inject", "pulsar_render_noalloc")
 
 
 def load(path: str = LIB_PATH):
@@ -85,6 +85,7 @@ def load(path: str = LIB_PATH):
     lib.pulsar_strerror.argtypes = [ctypes.c_int]
     lib.pulsar_strerror.restype = ctypes.c_char_p
     lib.pulsar_debug_copy.argtypes = [P, ctypes.c_int, P, I64, P]
+    lib.pulsar_debug_inject.argtypes = [P, ctypes.c_int, P]
     lib.pulsar_debug_copy.restype = I64
     lib.pulsar_render_noalloc.argtypes = [P, P, P, P, I64, ctypes.POINTER(Camera),
                                           ctypes.POINTER(Params), P, P, P]
@@ -339,3 +340,11 @@ class Renderer:
 
     def debug(self, what: str, stream=None) -> np.ndarray:
         return debug_copy(self.ctx, what, stream)
+
+
+INJECT_SHADE_TIMEOUT = 1
+
+
+def debug_inject(ctx, what: int, stream=None):
+    """Arm a test failure (see pulsar_debug_inject in include/pulsar.h)."""
+    _check(load().pulsar_debug_inject(ctx, int(what), _stream(stream)), "pulsar_debug_inject")

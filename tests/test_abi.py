@@ -53,6 +53,7 @@ def test_strerror_and_host_side_argument_errors(lib):
     assert lib.pulsar_destroy(None) == pl.ERR_ARG
     assert lib.pulsar_shade_forward(None, None, None, None, None) == pl.ERR_ARG
     assert lib.pulsar_shade_backward(None, None, None, None, None, None, None) == pl.ERR_ARG
+    assert lib.pulsar_debug_inject(None, 1, None) == pl.ERR_ARG
 
 
 def test_struct_layouts_match_header():

@@ -207,3 +207,42 @@ def test_shading_errors_and_empty_frame():
         pl.shade_forward(r3.ctx, F, params, rgb)
     assert e.value.code == pl.ERR_ARG
     r3.close()
+
+
+def test_shading_wait_timeout_is_reported_and_the_context_recovers():
+    """Failure detection without a GPU fault: the injected failure makes the
+    shading kernels issue no tensor-core work, so their bounded waits (0.25 s
+    of wall time) run out; the call completes and frees its tensor memory,
+    pulsar_status reports PULSAR_ERR_TIMEOUT (and disarms the injection), and
+    the same context then shades correctly."""
+    import time
+
+    import torch
+    from splat_rendering_gb300 import pulsar as pl
+    cam = scenes._camera(np.eye(3), np.zeros(3), 40.0, 48, 40, 1.0, 9.0, cx=23.3, cy=19.9)
+    rng = np.random.default_rng(141)
+    F = rng.standard_normal((1, 40, 48, 16)).astype(np.float32)
+    dY = rng.standard_normal((1, 40, 48, 3)).astype(np.float32)
+    params = scenes.shading_mlp(14)
+    r = _renderer_for([cam])
+    _project(r, [cam])
+    Fd, Pd, dYd = (torch.from_numpy(a).cuda() for a in (F[0], params, dY[0]))
+    for backward in (False, True):
+        pl.debug_inject(r.ctx, pl.INJECT_SHADE_TIMEOUT)
+        t0 = time.perf_counter()
+        if backward:
+            r.shade_backward(Fd, Pd, dYd)
+        else:
+            r.shade(Fd, Pd)
+        code = r.status(raise_on_error=False)[0]
+        waited = time.perf_counter() - t0
+        assert code == pl.ERR_TIMEOUT, pl.strerror(code)
+        assert waited < 10.0, waited          # the waits are bounded
+        # disarmed by the status call: the next call runs normally
+        y = r.shade(Fd, Pd)
+        gF, gP = r.shade_backward(Fd, Pd, dYd)
+        assert r.status(raise_on_error=False)[0] == 0
+        ref = sb.oracle_batch(F, [cam], params.astype(np.float64), dY)
+        sb.check(dict(y=y.cpu().numpy(), dF=gF.cpu().numpy(), params=gP.cpu().numpy()), ref,
+                 params.astype(np.float64), f"after an injected timeout (backward={backward})")
+    r.close()
