@@ -50,8 +50,8 @@ SHADE_KERNELS = 5      # weight pack + shade forward, weight pack + shade backwa
 def args_parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -688,6 +688,17 @@ def run_gb300(a):
                                                  shade=(mlp_host.astype(np.float64), drgb_host)
                                                  if shaded else None)
         what = "fwd, MLP fwd+bwd, bwd" if shaded else "fwd+bwd"
+        # the same oracle on one core, on a band sized for a few seconds
+        import oracle
+        oracle.set_threads(1)
+        v1, rows1, dt1, _, _ = oracle_sample(scene, max(2.0, a.cpu_seconds / 4),
+                                             rows=max(8, rows // max(1, cores)),
+                                             shade=(mlp_host.astype(np.float64), drgb_host)
+                                             if shaded else None)
+        oracle.set_threads(0)
+        line["cpu_baseline_1core"] = {"value": v1, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                      "sample": f"rows [0,{rows1}) x 1024 once ({dt1:.1f} s), "
+                                                f"scaled by {rows1}/1024"}
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                                 "sample": f"fp64 oracle {what} on rows [0,{rows}) x 1024 of "
                                           f"the same frame, {reps} time(s) ({dt:.1f} s), "

@@ -69,6 +69,7 @@ def _load():
         lib = ctypes.CDLL(_LIB)
         P = ctypes.c_void_p
         lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_set_threads.argtypes = [ctypes.c_int]
         lib.oracle_project.restype = ctypes.c_int
         lib.oracle_project.argtypes = [P, P, P, ctypes.c_int64, P, P] + [P] * 9
         lib.oracle_tile_lists.restype = ctypes.c_int64
@@ -82,6 +83,11 @@ def _load():
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_threads(n: int) -> None:
+    """Threads of the following oracle calls (n <= 0: all host cores)."""
+    _load().oracle_set_threads(int(n))
 
 
 def _ptr(a):

@@ -406,6 +406,15 @@ extern "C" {
 
 int oracle_num_threads() { return num_threads(); }
 
+// Threads of the following calls (n <= 0: all of the host's); timing only.
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+    omp_set_num_threads(n > 0 ? n : omp_get_num_procs());
+#else
+    (void)n;
+#endif
+}
+
 // Per-sphere decision outputs (fp32 decision path) for bit-exact comparison.
 int oracle_project(const double* pos, const double* radius, const double* opacity, int64_t n,
                    const ocam_t* cam, const oparams_t* prm, int32_t* keep, float* uv4,
