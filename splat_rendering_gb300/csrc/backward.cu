@@ -294,6 +294,34 @@ k_backward(Frames fs, Workspace w, const float* __restrict__ features,
     }
 }
 
+// Warp sums of twelve per-lane values in 16 shuffles (slots padded to 16):
+// at every butterfly step a lane keeps half of its slots, adds its partner's
+// copies of them and hands over the other half, so the live slots halve per
+// step; afterwards lanes 2s and 2s + 1 both hold the warp total of slot s.
+// The pairing is that of a shuffle-down tree, in a fixed order.
+__device__ __forceinline__ float warp_sum12(const float (&a)[12], int lane) {
+    float v[8];
+    const bool b4 = (lane & 16) != 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {   // v[j]: slot j + 8 b4
+        const float lo = a[j], hi = j + 8 < 12 ? a[j + 8] : 0.0f;
+        v[j] = (b4 ? hi : lo) + __shfl_xor_sync(0xffffffffu, b4 ? lo : hi, 16);
+    }
+    float u[4];
+    const bool b3 = (lane & 8) != 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)     // u[j]: slot j + 4 b3 + 8 b4
+        u[j] = (b3 ? v[j + 4] : v[j]) + __shfl_xor_sync(0xffffffffu, b3 ? v[j] : v[j + 4], 8);
+    float t[2];
+    const bool b2 = (lane & 4) != 0;
+#pragma unroll
+    for (int j = 0; j < 2; ++j)     // t[j]: slot j + 2 b2 + 4 b3 + 8 b4
+        t[j] = (b2 ? u[j + 2] : u[j]) + __shfl_xor_sync(0xffffffffu, b2 ? u[j] : u[j + 2], 4);
+    const bool b1 = (lane & 2) != 0;   // slot lane >> 1
+    float r = (b1 ? t[1] : t[0]) + __shfl_xor_sync(0xffffffffu, b1 ? t[0] : t[1], 2);
+    return r + __shfl_xor_sync(0xffffffffu, r, 1);
+}
+
 // Finalize of one sphere; adds its share of dL/dR and dL/dt to acc.
 __device__ __forceinline__ void finalize_one(const Frame& f, float4 g, float px, float py, float pz,
                                              float* gp, float* acc) {
@@ -375,12 +403,9 @@ k_finalize_one_cam(Frames fs, Workspace w, const float* __restrict__ pos, float*
             if (grad_radius) grad_radius[i] = g.w * sph;
         }
     }
-#pragma unroll
-    for (int q = 0; q < 12; ++q) {
-        float s = acc[q];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
-        if (lane == 0) s_part[warp][q] = s;
+    {
+        const float s = warp_sum12(acc, lane);
+        if ((lane & 1) == 0 && (lane >> 1) < 12) s_part[warp][lane >> 1] = s;
     }
     __syncthreads();
     if (tid < 12) {
@@ -496,12 +521,9 @@ k_finalize_cams(Frames fs, Workspace w, const float* __restrict__ pos, float* __
                 }
             }
         }
-#pragma unroll
-        for (int q = 0; q < 12; ++q) {
-            float s = acc[q];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
-            if (lane == 0) s_part[warp][q] = s;
+        {
+            const float s = warp_sum12(acc, lane);
+            if ((lane & 1) == 0 && (lane >> 1) < 12) s_part[warp][lane >> 1] = s;
         }
         __syncthreads();
         if (tid < 12) {
@@ -517,44 +539,90 @@ k_finalize_cams(Frames fs, Workspace w, const float* __restrict__ pos, float* __
 // partials and dL/d(fx, fy, cx, cy) from its tiles' partials, summed in a
 // fixed order in float-pair arithmetic (deterministic, ~1e-14 relative;
 // Pulsar Sec. B.2's device-wide camera reduction).  The partials of each of
-// the 16 outputs are contiguous; two warps sum each output with coalesced
-// loads and combine through shared memory.
+// the 16 outputs are contiguous.  The 32 warps are dealt out in proportion
+// to the outputs' lengths (a function of the two lengths only, so the order
+// of the sums is fixed for a given frame), each warp sums a contiguous part
+// with eight independent accumulators per lane (eight loads in flight), and
+// the parts of an output are combined in order through shared memory.
+constexpr int kCamAcc = 8;
+
 __global__ void __launch_bounds__(kCamThreads)
 k_camera_reduce(Frames fs, Workspace w, int fin_blocks, float* __restrict__ grad_cam) {
     pdl_begin();
-    static_assert(kCamThreads == 1024, "two warps per output");
-    __shared__ float2 s_half[16][2];
+    static_assert(kCamThreads == 1024, "32 warps");
+    __shared__ float2 s_part[32];
     const int cam = blockIdx.x;
     const Frame& f = fs.f[cam];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int q = warp >> 1, half = warp & 1;
-    const float2* src;
-    int len;
-    if (q < 12) {
-        src = w.rtpart + ((size_t)cam * 12 + q) * fin_blocks;
-        len = fin_blocks;
-    } else {
-        src = w.kpart + (size_t)(q - 12) * f.n_tiles_all + f.tile_base;
-        len = f.n_tiles;
+    const int len_rt = fin_blocks, len_k = f.n_tiles;
+    // warps per K output: round(32 len_k / total) within 1..5; the rest shared
+    // by the 12 R/t outputs (at least one each)
+    const long long total = 12LL * len_rt + 4LL * len_k;
+    int wk = total > 0 ? (int)((32LL * len_k + total / 2) / total) : 1;
+    wk = wk < 1 ? 1 : (wk > 5 ? 5 : wk);
+    const int wr = (32 - 4 * wk) / 12;
+    int q = -1, part = 0, parts = 1;
+    if (warp < 12 * wr) {
+        q = warp / wr;
+        part = warp % wr;
+        parts = wr;
+    } else if (warp < 12 * wr + 4 * wk) {
+        q = 12 + (warp - 12 * wr) / wk;
+        part = (warp - 12 * wr) % wk;
+        parts = wk;
     }
-    const int lo = half ? len / 2 : 0, hi = half ? len : len / 2;
-    FPair v = {0.0f, 0.0f};
-#pragma unroll 4
-    for (int b = lo + lane; b < hi; b += 32) {
-        const float2 t = src[b];
-        v = pp_add(v, FPair{t.x, t.y});
-    }
+    if (q >= 0) {
+        const float2* src;
+        int len;
+        if (q < 12) {
+            src = w.rtpart + ((size_t)cam * 12 + q) * fin_blocks;
+            len = len_rt;
+        } else {
+            src = w.kpart + (size_t)(q - 12) * f.n_tiles_all + f.tile_base;
+            len = len_k;
+        }
+        const int lo = (int)((long long)len * part / parts);
+        const int hi = (int)((long long)len * (part + 1) / parts);
+        FPair v[kCamAcc];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const FPair t = {__shfl_down_sync(0xffffffffu, v.hi, o),
-                         __shfl_down_sync(0xffffffffu, v.lo, o)};
-        v = pp_add(v, t);
+        for (int u = 0; u < kCamAcc; ++u) v[u] = FPair{0.0f, 0.0f};
+        int b = lo + lane;
+        for (; b + 32 * (kCamAcc - 1) < hi; b += 32 * kCamAcc) {
+            float2 t[kCamAcc];
+#pragma unroll
+            for (int u = 0; u < kCamAcc; ++u) t[u] = src[b + 32 * u];
+#pragma unroll
+            for (int u = 0; u < kCamAcc; ++u) v[u] = pp_add(v[u], FPair{t[u].x, t[u].y});
+        }
+#pragma unroll
+        for (int u = 0; u < kCamAcc - 1; ++u) {   // the tail: fewer than kCamAcc loads
+            if (b + 32 * u < hi) {
+                const float2 t = src[b + 32 * u];
+                v[u] = pp_add(v[u], FPair{t.x, t.y});
+            }
+        }
+#pragma unroll
+        for (int h = kCamAcc / 2; h > 0; h >>= 1)
+#pragma unroll
+            for (int u = 0; u < h; ++u) v[u] = pp_add(v[u], v[u + h]);
+        FPair r = v[0];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const FPair t = {__shfl_down_sync(0xffffffffu, r.hi, o),
+                             __shfl_down_sync(0xffffffffu, r.lo, o)};
+            r = pp_add(r, t);
+        }
+        if (lane == 0) s_part[warp] = make_float2(r.hi, r.lo);
     }
-    if (lane == 0) s_half[q][half] = make_float2(v.hi, v.lo);
     __syncthreads();
     if (tid < 16) {
-        const float2 a = s_half[tid][0], b = s_half[tid][1];
-        const FPair s = pp_add(FPair{a.x, a.y}, FPair{b.x, b.y});
+        const int w0 = tid < 12 ? tid * wr : 12 * wr + (tid - 12) * wk;
+        const int nw = tid < 12 ? wr : wk;
+        FPair s = {0.0f, 0.0f};
+        for (int k = 0; k < nw; ++k) {
+            const float2 t = s_part[w0 + k];
+            s = pp_add(s, FPair{t.x, t.y});
+        }
         if (grad_cam) grad_cam[16 * cam + tid] = __fadd_rn(s.hi, s.lo);
     }
 }
