@@ -10,7 +10,8 @@
 //                (f32 bits of c.z - r_eff) << 32 | sphere id, which is unique,
 //                so the list does not depend on the bucket's arrival order.
 //                Lists up to kWarpSortMax entries are sorted in registers as
-//                packed 32-bit keys (bitonic network); longer ones by the
+//                packed 32-bit keys (bitonic networks on two runs of at most
+//                256, merged by merge path); longer ones by the
 //                warp's block, in shared memory up to kSortCap entries, and
 //                beyond that in chunks merged pairwise through global memory
 //                (merge path).
@@ -159,65 +160,112 @@ __device__ __forceinline__ void warp_bitonic(uint32_t (&e)[16], int lane) {
     }
 }
 
-// One warp sorts one tile's n <= 32 E pairs (key bits << 32 | id).  It sorts
-// 32-bit keys: the key bits (positive floats, so their bit patterns are
-// monotone) minus the tile minimum, shifted down to 23 bits, above the
-// element's 9-bit position in the bucket.  Equal shifted keys come out
-// ordered by position; such rare runs are put in exact (key, id) order by an
-// insertion pass, so the result is the (key, id) order.  s64 holds the
-// bucket (512 entries), s32 the transposition buffer (512 words), whose
-// XOR swizzle keeps both the coalesced and the lane-major access free of
-// bank conflicts; it then holds the sorted positions.
+// Ascending bitonic sort of the k <= 32 E unique 32-bit keys at keys[0 .. k)
+// in place (the buffer holds 32 E words; entries k .. 32 E - 1 are padded
+// with ~0u, above every key).  Lane l holds elements E l .. E l + E - 1.
 template <int E>
-__device__ void warp_sort_tile(const Workspace& w, uint32_t start, int n,
-                               unsigned long long* s64, uint32_t* s32, int lane) {
-    uint32_t kmin = 0xffffffffu, kmax = 0u;
+__device__ __forceinline__ void sort_keys(uint32_t* keys, int k, int lane) {
+    for (int i = k + lane; i < 32 * E; i += 32) keys[i] = 0xffffffffu;
+    __syncwarp();
+    uint32_t e[16];
+    uint32_t* mine = keys + E * lane;
+    if constexpr (E >= 4) {
 #pragma unroll
-    for (int r = 0; r < E; ++r) {
-        const int i = 32 * r + lane;
-        if (i < n) {
-            const unsigned long long v = w.pairs[start + i];
-            s64[i] = v;
-            const uint32_t kb = (uint32_t)(v >> 32);
-            kmin = min(kmin, kb);
-            kmax = max(kmax, kb);
+        for (int q = 0; q < E / 4; ++q) {
+            const uint4 v = reinterpret_cast<const uint4*>(mine)[q];
+            e[4 * q] = v.x; e[4 * q + 1] = v.y; e[4 * q + 2] = v.z; e[4 * q + 3] = v.w;
         }
+    } else {
+#pragma unroll
+        for (int r = 0; r < E; ++r) e[r] = mine[r];
+    }
+    warp_bitonic<E>(e, lane);
+    __syncwarp();
+    if constexpr (E >= 4) {
+#pragma unroll
+        for (int q = 0; q < E / 4; ++q)
+            reinterpret_cast<uint4*>(mine)[q] = make_uint4(e[4 * q], e[4 * q + 1], e[4 * q + 2], e[4 * q + 3]);
+    } else {
+#pragma unroll
+        for (int r = 0; r < E; ++r) mine[r] = e[r];
+    }
+}
+
+// Number of elements taken from a (length la) among the first k outputs of
+// merging the sorted runs a and b (length lb) of unique keys.
+__device__ __forceinline__ int merge_split32(const uint32_t* a, int la, const uint32_t* b, int lb,
+                                             int k) {
+    int lo = max(0, k - lb), hi = min(k, la);
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (a[mid] < b[k - 1 - mid]) lo = mid + 1; else hi = mid;
+    }
+    return lo;
+}
+
+// One warp sorts one tile's n <= kWarpSortMax pairs (key bits << 32 | id).
+// It sorts 32-bit keys: the key bits (positive floats, so their bit patterns
+// are monotone) minus the tile minimum, shifted down to 23 bits, above the
+// element's 9-bit position in the bucket.  The first 256 keys and the rest
+// are sorted as two runs, each by the smallest register network that holds
+// it (a list of 300 keys costs a 256- and a 64-key network, not a 512-key
+// one), and merged by merge path, a contiguous span of outputs per lane.
+// Equal shifted keys come out ordered by position; such rare runs, seen
+// while merging, are put in exact (key, id) order by an insertion pass, so
+// the result is the (key, id) order.  s64 holds the bucket, s32 the keys
+// (512 words each) and, once they are merged, the sorted positions.
+__device__ void warp_sort_tile(const Workspace& w, uint32_t start, int n, unsigned long long* s64,
+                               uint32_t* s32, int lane) {
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+    for (int i = lane; i < n; i += 32) {
+        const unsigned long long v = w.pairs[start + i];
+        s64[i] = v;
+        const uint32_t kb = (uint32_t)(v >> 32);
+        kmin = min(kmin, kb);
+        kmax = max(kmax, kb);
     }
     const uint32_t lo = __reduce_min_sync(0xffffffffu, kmin);
     const uint32_t span = __reduce_max_sync(0xffffffffu, kmax) - lo;
     const int shift = max(0, 32 - __clz((int)span) - 23);
     __syncwarp();
-#pragma unroll
-    for (int r = 0; r < E; ++r) {
-        const int i = 32 * r + lane;
-        const uint32_t key =
-            i < n ? ((((uint32_t)(s64[i] >> 32) - lo) >> shift) << 9) | (uint32_t)i : 0xffffffffu;
-        s32[i ^ (r & (E - 1))] = key;
+    for (int i = lane; i < n; i += 32)
+        s32[i] = ((((uint32_t)(s64[i] >> 32) - lo) >> shift) << 9) | (uint32_t)i;
+    const int la = min(n, 256), lb = n - la;
+#pragma unroll 1
+    for (int c = 0; c < (lb > 0 ? 2 : 1); ++c) {
+        uint32_t* keys = s32 + 256 * c;
+        const int k = c ? lb : la;
+        if (k <= 32) sort_keys<1>(keys, k, lane);
+        else if (k <= 64) sort_keys<2>(keys, k, lane);
+        else if (k <= 128) sort_keys<4>(keys, k, lane);
+        else sort_keys<8>(keys, k, lane);
     }
     __syncwarp();
-    uint32_t e[16];
-#pragma unroll
-    for (int r = 0; r < E; ++r) {
-        const int i = E * lane + r;
-        e[r] = s32[i ^ ((i >> 5) & (E - 1))];
-    }
-    warp_bitonic<E>(e, lane);
-    // equal shifted keys next to each other (ranks below n)?
-    const uint32_t prev_last = __shfl_up_sync(0xffffffffu, e[E - 1], 1);
+    const uint32_t* A = s32;
+    const uint32_t* B = s32 + 256;
+    const int per = (n + 31) >> 5;
+    const int k0 = min(n, lane * per), k1 = min(n, k0 + per);
+    int ia = merge_split32(A, la, B, lb, k0), ib = k0 - ia;
+    uint32_t prev = max(ia > 0 ? A[ia - 1] : 0u, ib > 0 ? B[ib - 1] : 0u);
     bool tie = false;
+    uint16_t out[kWarpSortMax / 32];   // this lane's span of sorted positions
 #pragma unroll
-    for (int r = 0; r < E; ++r) {
-        const int i = E * lane + r;
-        const uint32_t prev = r == 0 ? prev_last : e[r - 1];
-        tie |= i > 0 && i < n && (prev >> 9) == (e[r] >> 9);
+    for (int t = 0; t < kWarpSortMax / 32; ++t) {
+        const int k = k0 + t;
+        if (k < k1) {
+            const bool take_a = ib >= lb || (ia < la && A[ia] < B[ib]);
+            const uint32_t v = take_a ? A[ia++] : B[ib++];
+            tie |= k > 0 && (prev >> 9) == (v >> 9);
+            prev = v;
+            out[t] = (uint16_t)(v & 511u);
+        }
     }
     const bool any_tie = __any_sync(0xffffffffu, tie);
+    __syncwarp();   // every lane's merge has read its keys: the positions take their place
     uint16_t* s_pos = reinterpret_cast<uint16_t*>(s32);
 #pragma unroll
-    for (int r = 0; r < E; ++r) {
-        const int i = E * lane + r;
-        if (i < n) s_pos[i] = (uint16_t)(e[r] & 511u);
-    }
+    for (int t = 0; t < kWarpSortMax / 32; ++t)
+        if (k0 + t < k1) s_pos[k0 + t] = out[t];
     __syncwarp();
     if (any_tie && lane == 0) {
         // sorted except inside runs of equal shifted keys: insertion sort on
@@ -294,8 +342,8 @@ __global__ void __launch_bounds__(kSortThreads) k_tile_sort(Frames fs, Workspace
     pdl_begin();
     const Frame& f = fs.f[0];
     const int n_tiles = (int)f.n_tiles_all;
-    __shared__ unsigned long long s[kSortCap];                        // 16 KB
-    __shared__ uint32_t s_keys[kTilesPerSortBlock][kWarpSortMax];      // 8 KB
+    __shared__ unsigned long long s[kSortCap];                                 // 16 KB
+    __shared__ __align__(16) uint32_t s_keys[kTilesPerSortBlock][kWarpSortMax]; // 8 KB
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile0 = blockIdx.x * kTilesPerSortBlock;
     {
@@ -305,13 +353,7 @@ __global__ void __launch_bounds__(kSortThreads) k_tile_sort(Frames fs, Workspace
             // (a frame over capacity has its error latched; its lists are not sorted)
             if (end <= f.max_pairs && end > start && end - start <= (uint32_t)kWarpSortMax) {
                 const int n = (int)(end - start);
-                unsigned long long* s64 = s + warp * kWarpSortMax;
-                uint32_t* s32 = s_keys[warp];
-                if (n <= 32) warp_sort_tile<1>(w, start, n, s64, s32, lane);
-                else if (n <= 64) warp_sort_tile<2>(w, start, n, s64, s32, lane);
-                else if (n <= 128) warp_sort_tile<4>(w, start, n, s64, s32, lane);
-                else if (n <= 256) warp_sort_tile<8>(w, start, n, s64, s32, lane);
-                else warp_sort_tile<16>(w, start, n, s64, s32, lane);
+                warp_sort_tile(w, start, n, s + warp * kWarpSortMax, s_keys[warp], lane);
             }
         }
     }
