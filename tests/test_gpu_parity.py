@@ -92,6 +92,31 @@ def test_edge_cases(oracle_lib, case):
         assert np.diff(offs).max() > 2048
 
 
+@pytest.mark.parametrize("n", [3000, 6000, 12000])
+def test_equal_depth_keys(oracle_lib, n):
+    """Spheres on three depth planes with two radii: a handful of distinct
+    sort keys, so every tile list is made of long runs of equal keys ordered
+    by sphere id alone (Pulsar Sec. 3.2 sorts by earliest possible
+    intersection; the id tie-break makes the list unique).  About 190, 375
+    and 750 candidates per tile: one register network, two merged runs, the
+    block sort."""
+    sc = scenes.random_scene(59, n, 64, 64, f=64.0, zrange=(3.0, 4.5), rrange=(0.02, 0.08))
+    rng = np.random.default_rng(60)
+    sc.pos[:, 2] = rng.choice(np.float32([3.0, 4.0, 4.5]), n)
+    sc.radius[:] = rng.choice(np.float32([0.03, 0.05]), n)
+    o, d, offs, ids = _oracle_all(oracle_lib, sc)
+    kept = d["key"][ids]
+    assert len(np.unique(kept)) <= 6
+    lens = np.diff(offs)
+    lo, hi = {3000: (129, 256), 6000: (257, 512), 12000: (513, 2048)}[n]
+    assert ((lens >= lo) & (lens <= hi)).sum() >= 4, lens
+    g = gh.run_gpu(sc, max_pairs=len(ids) + 64)
+    assert g["code"] == 0
+    gh.assert_decisions_equal(g, d)
+    _check_lists(g, offs, ids)
+    gh.compare_frame(g, o, f"equal keys n={n}")
+
+
 def test_zero_opacity_spheres(oracle_lib):
     sc = scenes.random_scene(58, 400, 48, 48, rrange=(0.02, 0.3))
     sc.opacity[::3] = 0.0
