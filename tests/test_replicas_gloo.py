@@ -1,5 +1,5 @@
-"""Multi-process form of the benchmark (replicas, SURVEY's "replicas only")
-on CPU with the gloo backend, world size 2: every rank renders its own frame,
+"""Multi-process form of the benchmark (independent replicas: the renderer
+has no exchange step) on CPU with the gloo backend, world size 2: every rank renders its own frame,
 the only collective is the max over ranks of the timed region, and only
 rank 0 reports.  No GPU."""
 from __future__ import annotations
