@@ -70,6 +70,12 @@ EDGE = {
                    f=30.0, fy=41.0, cx=15.3, cy=9.1, rrange=(0.01, 0.3)),
     "one_channel": dict(seed=52, n=400, width=48, height=40, channels=1, n_track=1),
     "wide_payload": dict(seed=53, n=300, width=40, height=33, channels=33, n_track=16),
+    # the largest payload and tracking depth the ABI accepts (98% of the pixels
+    # fill all 16 slots), and the 17-32 channel build
+    "max_payload": dict(seed=61, n=1500, width=40, height=33, channels=64, n_track=16,
+                        rrange=(0.1, 0.5)),
+    "payload_32": dict(seed=62, n=1200, width=45, height=31, channels=32, n_track=12,
+                       rrange=(0.08, 0.4)),
     "five_channels": dict(seed=54, n=300, width=50, height=30, channels=5, n_track=9),
     "no_cutoff": dict(seed=55, n=500, width=64, height=48, geom_cutoff=False, rrange=(0.005, 0.2)),
     # big spheres: tile lists longer than one shared-memory sort (merge path)
