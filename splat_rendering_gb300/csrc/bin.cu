@@ -210,19 +210,32 @@ __device__ __forceinline__ int merge_split32(const uint32_t* a, int la, const ui
 // are sorted as two runs, each by the smallest register network that holds
 // it (a list of 300 keys costs a 256- and a 64-key network, not a 512-key
 // one), and merged by merge path, a contiguous span of outputs per lane.
-// Equal shifted keys come out ordered by position; such rare runs, seen
-// while merging, are put in exact (key, id) order by an insertion pass, so
-// the result is the (key, id) order.  s64 holds the bucket, s32 the keys
+// Equal shifted keys come out ordered by position; such rare runs, marked
+// while merging, are put in exact (key, id) order by insertion sorts, each
+// run by the lane in whose span it starts, so the result is the (key, id)
+// order.  s64 holds the bucket, s32 the keys
 // (512 words each) and, once they are merged, the sorted positions.
 __device__ void warp_sort_tile(const Workspace& w, uint32_t start, int n, unsigned long long* s64,
                                uint32_t* s32, int lane) {
     uint32_t kmin = 0xffffffffu, kmax = 0u;
-    for (int i = lane; i < n; i += 32) {
-        const unsigned long long v = w.pairs[start + i];
-        s64[i] = v;
-        const uint32_t kb = (uint32_t)(v >> 32);
-        kmin = min(kmin, kb);
-        kmax = max(kmax, kb);
+    // the bucket, eight loads in flight per lane
+    for (int i0 = 0; i0 < n; i0 += 256) {
+        unsigned long long v[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            const int i = i0 + 32 * r + lane;
+            v[r] = i < n ? w.pairs[start + i] : 0ull;
+        }
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            const int i = i0 + 32 * r + lane;
+            if (i < n) {
+                s64[i] = v[r];
+                const uint32_t kb = (uint32_t)(v[r] >> 32);
+                kmin = min(kmin, kb);
+                kmax = max(kmax, kb);
+            }
+        }
     }
     const uint32_t lo = __reduce_min_sync(0xffffffffu, kmin);
     const uint32_t span = __reduce_max_sync(0xffffffffu, kmax) - lo;
@@ -247,7 +260,7 @@ __device__ void warp_sort_tile(const Workspace& w, uint32_t start, int n, unsign
     const int k0 = min(n, lane * per), k1 = min(n, k0 + per);
     int ia = merge_split32(A, la, B, lb, k0), ib = k0 - ia;
     uint32_t prev = max(ia > 0 ? A[ia - 1] : 0u, ib > 0 ? B[ib - 1] : 0u);
-    bool tie = false;
+    uint32_t tmask = 0;                 // bit t: output k0 + t ties with its predecessor
     uint16_t out[kWarpSortMax / 32];   // this lane's span of sorted positions
 #pragma unroll
     for (int t = 0; t < kWarpSortMax / 32; ++t) {
@@ -255,30 +268,42 @@ __device__ void warp_sort_tile(const Workspace& w, uint32_t start, int n, unsign
         if (k < k1) {
             const bool take_a = ib >= lb || (ia < la && A[ia] < B[ib]);
             const uint32_t v = take_a ? A[ia++] : B[ib++];
-            tie |= k > 0 && (prev >> 9) == (v >> 9);
+            tmask |= (uint32_t)(k > 0 && (prev >> 9) == (v >> 9)) << t;
             prev = v;
             out[t] = (uint16_t)(v & 511u);
         }
     }
-    const bool any_tie = __any_sync(0xffffffffu, tie);
-    __syncwarp();   // every lane's merge has read its keys: the positions take their place
-    uint16_t* s_pos = reinterpret_cast<uint16_t*>(s32);
+    const bool any_tie = __any_sync(0xffffffffu, tmask != 0u);
+    __syncwarp();   // every lane's merge has read its keys: positions and tie masks take their place
+    uint16_t* s_pos = reinterpret_cast<uint16_t*>(s32);          // words 0 .. 255
+    uint16_t* s_tie = reinterpret_cast<uint16_t*>(s32 + 384);    // one 16-bit mask per lane
 #pragma unroll
     for (int t = 0; t < kWarpSortMax / 32; ++t)
         if (k0 + t < k1) s_pos[k0 + t] = out[t];
+    if (any_tie) s_tie[lane] = (uint16_t)tmask;
     __syncwarp();
-    if (any_tie && lane == 0) {
-        // sorted except inside runs of equal shifted keys: insertion sort on
-        // the exact 64-bit (key, id) finishes it
-        for (int i = 1; i < n; ++i) {
-            const uint16_t v = s_pos[i];
-            const unsigned long long kv = s64[v];
-            int q = i - 1;
-            while (q >= 0 && s64[s_pos[q]] > kv) {
-                s_pos[q + 1] = s_pos[q];
-                --q;
+    if (any_tie) {
+        // sorted except inside runs of equal shifted keys: each lane puts the
+        // runs that start in its span in exact (key, id) order (insertion
+        // sort); the runs are disjoint and the masks are only read here
+        auto tied = [&](int k) {
+            const int l = k / per;
+            return ((s_tie[l] >> (k - l * per)) & 1u) != 0u;
+        };
+        for (int k = k0; k < k1; ++k) {
+            if (tied(k) || k + 1 >= n || !tied(k + 1)) continue;
+            int e = k + 2;
+            while (e < n && tied(e)) ++e;
+            for (int i = k + 1; i < e; ++i) {
+                const uint16_t v = s_pos[i];
+                const unsigned long long kv = s64[v];
+                int q = i - 1;
+                while (q >= k && s64[s_pos[q]] > kv) {
+                    s_pos[q + 1] = s_pos[q];
+                    --q;
+                }
+                s_pos[q + 1] = v;
             }
-            s_pos[q + 1] = v;
         }
     }
     __syncwarp();
