@@ -2,8 +2,9 @@
 // intersection; Sec. B.1.1 depth sort; Sec. B.1.2 16x16 blocks).
 //
 //   k_tile_scan  one block: exclusive scan of the per-tile pair counts -> tile
-//                offsets and M (the counters are cleared for the next frame);
-//                latches a capacity error if M > max_pairs.
+//                offsets and M (the counters are cleared for the next frame),
+//                and the list of tiles whose bucket is longer than one warp
+//                sorts; latches a capacity error if M > max_pairs.
 //   k_emit       one thread per staged pair (the projection gave each pair
 //                its slot in its tile): scatter (key, id) to offset + slot.
 //   k_tile_sort  one warp per tile: sort the bucket by the 64-bit key
@@ -11,10 +12,11 @@
 //                so the list does not depend on the bucket's arrival order.
 //                Lists up to kWarpSortMax entries are sorted in registers as
 //                packed 32-bit keys (bitonic networks on two runs of at most
-//                256, merged by merge path); longer ones by the
-//                warp's block, in shared memory up to kSortCap entries, and
-//                beyond that in chunks merged pairwise through global memory
-//                (merge path).
+//                256, merged by merge path).
+//   k_tile_sort_long  persistent blocks take the longer lists from a work
+//                counter: up to kLongCap entries sorted in one piece in
+//                shared memory, beyond that in chunks merged pairwise through
+//                global memory (merge path).
 //
 // The pairs live in L2-sized buffers for the shipped workloads (M ~ 1e6).
 #include "pulsar_internal.cuh"
@@ -29,48 +31,98 @@ constexpr int kTilesPerSortBlock = kSortThreads / 32;
 constexpr int kSortCap = 2048;
 constexpr int kWarpSortMax = 512;   // lists sorted by one warp in registers
 
-__global__ void __launch_bounds__(kScanThreads) k_tile_scan(Frames fs, Workspace w) {
-    pdl_begin();
-    __shared__ uint32_t s_warp[kScanThreads / 32];
-    const Frame& f = fs.f[0];
-    const int n_tiles = (int)f.n_tiles_all;   // every camera's tiles, camera after camera
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int per = (n_tiles + kScanThreads - 1) / kScanThreads;
-    const int b0 = tid * per;
-    const int b1 = min(b0 + per, n_tiles);
-    uint32_t local = 0;
-    for (int b = b0; b < b1; ++b) local += w.tile_count[b];
-    uint32_t incl = local;
+// Block-wide exclusive scan of one value per thread; returns the thread's
+// exclusive prefix, *total the block's sum (s: 32 words of scratch).
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* s, uint32_t* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t incl = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
+        const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
     }
-    if (lane == 31) s_warp[warp] = incl;
+    if (lane == 31) s[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        uint32_t v = s_warp[lane];
-        uint32_t vi = v;
+        const uint32_t t = lane < (int)(blockDim.x >> 5) ? s[lane] : 0u;
+        uint32_t ti = t;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t u = __shfl_up_sync(0xffffffffu, vi, o);
-            if (lane >= o) vi += u;
+            const uint32_t u = __shfl_up_sync(0xffffffffu, ti, o);
+            if (lane >= o) ti += u;
         }
-        s_warp[lane] = vi - v;   // exclusive prefix of warp totals
+        s[lane] = ti - t;   // exclusive prefix of the warp totals
+        if (lane == 31) s[32] = ti;
     }
     __syncthreads();
-    uint32_t run = s_warp[warp] + incl - local;
-    for (int b = b0; b < b1; ++b) {
-        w.tile_start[b] = run;
-        run += w.tile_count[b];
-        w.tile_count[b] = 0u;
+    const uint32_t r = s[warp] + incl - v;
+    *total = s[32];
+    __syncthreads();   // s is free for the next scan
+    return r;
+}
+
+// One block walks the tiles in chunks of kScanChunk, each thread owning
+// kScanPer consecutive tiles (coalesced 16-byte loads and stores): the tile
+// offsets, the counters cleared for the next frame, and the list of tiles
+// whose bucket is too long for one warp's sort, in tile order.
+constexpr int kScanPer = 4;
+constexpr int kScanChunk = kScanThreads * kScanPer;
+
+__global__ void __launch_bounds__(kScanThreads) k_tile_scan(Frames fs, Workspace w) {
+    pdl_begin();
+    __shared__ uint32_t s_scan[33];
+    const Frame& f = fs.f[0];
+    const int n_tiles = (int)f.n_tiles_all;   // every camera's tiles, camera after camera
+    uint32_t carry = 0, lcarry = 0;            // pairs and long tiles before the chunk
+    for (int c0 = 0; c0 < n_tiles; c0 += kScanChunk) {
+        const int b = c0 + kScanPer * (int)threadIdx.x;
+        uint32_t cnt[kScanPer];
+        if (b + kScanPer <= n_tiles) {
+            const uint4 v = *reinterpret_cast<const uint4*>(w.tile_count + b);
+            cnt[0] = v.x; cnt[1] = v.y; cnt[2] = v.z; cnt[3] = v.w;
+        } else {
+#pragma unroll
+            for (int q = 0; q < kScanPer; ++q) cnt[q] = b + q < n_tiles ? w.tile_count[b + q] : 0u;
+        }
+        uint32_t local = 0, llocal = 0;
+#pragma unroll
+        for (int q = 0; q < kScanPer; ++q) {
+            local += cnt[q];
+            llocal += cnt[q] > (uint32_t)kWarpSortMax ? 1u : 0u;
+        }
+        uint32_t total, ltotal;
+        uint32_t run = carry + block_exclusive_scan(local, s_scan, &total);
+        uint32_t lrun = lcarry + block_exclusive_scan(llocal, s_scan, &ltotal);
+        uint32_t st[kScanPer];
+#pragma unroll
+        for (int q = 0; q < kScanPer; ++q) {
+            st[q] = run;
+            run += cnt[q];
+            if (cnt[q] > (uint32_t)kWarpSortMax) w.long_tiles[lrun++] = (uint32_t)(b + q);
+        }
+        if (b + kScanPer <= n_tiles) {
+            *reinterpret_cast<uint4*>(w.tile_start + b) = make_uint4(st[0], st[1], st[2], st[3]);
+            *reinterpret_cast<uint4*>(w.tile_count + b) = make_uint4(0u, 0u, 0u, 0u);
+        } else {
+#pragma unroll
+            for (int q = 0; q < kScanPer; ++q) {
+                if (b + q < n_tiles) {
+                    w.tile_start[b + q] = st[q];
+                    w.tile_count[b + q] = 0u;
+                }
+            }
+        }
+        carry += total;
+        lcarry += ltotal;
     }
-    if (tid == kScanThreads - 1) {
-        w.tile_start[n_tiles] = run;
-        w.state->n_pairs = run;
+    if (threadIdx.x == 0) {
+        w.tile_start[n_tiles] = carry;
+        w.state->n_pairs = carry;
+        w.state->n_long = lcarry;
+        w.state->long_next = 0u;
         w.state->hits = 0ull;
         w.state->pair_cursor = 0u;
-        if (run > f.max_pairs) atomicOr(&w.state->error, kErrCapacity);
+        if (carry > f.max_pairs) atomicOr(&w.state->error, kErrCapacity);
     }
 }
 
@@ -360,39 +412,70 @@ __device__ void block_sort_long(const Workspace& w, uint32_t start, int n, unsig
     for (int t = threadIdx.x; t < n; t += blockDim.x) w.tile_ids[start + t] = (uint32_t)src[t];
 }
 
-// Block b covers tiles 4b .. 4b+3: first each warp sorts its own tile if the
-// list has at most kWarpSortMax entries, then the block sorts the longer ones
-// together.
+// Block b covers tiles 4b .. 4b+3, one warp each; lists longer than
+// kWarpSortMax are left to k_tile_sort_long.
 __global__ void __launch_bounds__(kSortThreads) k_tile_sort(Frames fs, Workspace w) {
     pdl_begin();
     const Frame& f = fs.f[0];
     const int n_tiles = (int)f.n_tiles_all;
-    __shared__ unsigned long long s[kSortCap];                                 // 16 KB
+    __shared__ unsigned long long s[kTilesPerSortBlock * kWarpSortMax];        // 16 KB
     __shared__ __align__(16) uint32_t s_keys[kTilesPerSortBlock][kWarpSortMax]; // 8 KB
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tile0 = blockIdx.x * kTilesPerSortBlock;
-    {
-        const int tile = tile0 + warp;
-        if (tile < n_tiles) {
-            const uint32_t start = w.tile_start[tile], end = w.tile_start[tile + 1];
-            // (a frame over capacity has its error latched; its lists are not sorted)
-            if (end <= f.max_pairs && end > start && end - start <= (uint32_t)kWarpSortMax) {
-                const int n = (int)(end - start);
-                warp_sort_tile(w, start, n, s + warp * kWarpSortMax, s_keys[warp], lane);
-            }
-        }
-    }
-    for (int q = 0; q < kTilesPerSortBlock; ++q) {
-        const int tile = tile0 + q;
-        if (tile >= n_tiles) break;
+    const int tile = blockIdx.x * kTilesPerSortBlock + warp;
+    if (tile >= n_tiles) return;
+    const uint32_t start = w.tile_start[tile], end = w.tile_start[tile + 1];
+    // (a frame over capacity has its error latched; its lists are not sorted)
+    if (end <= f.max_pairs && end > start && end - start <= (uint32_t)kWarpSortMax)
+        warp_sort_tile(w, start, (int)(end - start), s + warp * kWarpSortMax, s_keys[warp], lane);
+}
+
+// The long lists: persistent blocks take the tiles of long_tiles one at a
+// time from a work counter (the lengths are very uneven).  A list of at most
+// kLongCap keys is sorted in one piece in shared memory (bitonic network on
+// the 64-bit keys); a longer one in kSortCap chunks merged through global
+// memory.
+constexpr int kLongThreads = 512;
+constexpr int kLongCap = 8192;                       // 64 KB of keys
+constexpr int kLongSmem = kLongCap * 8;
+constexpr int kLongBlocksPerSm = 2;
+
+__global__ void __launch_bounds__(kLongThreads) k_tile_sort_long(Frames fs, Workspace w) {
+    pdl_begin();
+    extern __shared__ __align__(16) unsigned long long s_long[];
+    __shared__ uint32_t s_item;
+    const Frame& f = fs.f[0];
+    const uint32_t n_long = w.state->n_long;
+    if (w.state->n_pairs > f.max_pairs) return;   // overflowed frame: nothing to sort
+    for (;;) {
+        if (threadIdx.x == 0) s_item = atomicAdd(&w.state->long_next, 1u);
+        __syncthreads();
+        const uint32_t item = s_item;
+        __syncthreads();   // every thread has the item before it is overwritten
+        if (item >= n_long) break;
+        const uint32_t tile = w.long_tiles[item];
         const uint32_t start = w.tile_start[tile], end = w.tile_start[tile + 1];
-        if (end > f.max_pairs || end <= start || end - start <= (uint32_t)kWarpSortMax) continue;
-        __syncthreads();   // the shared buffer is free
-        block_sort_long(w, start, (int)(end - start), s);
+        const int n = (int)(end - start);
+        if (n <= kLongCap) {
+            const int np = next_pow2(n);
+            for (int t = threadIdx.x; t < np; t += blockDim.x)
+                s_long[t] = t < n ? w.pairs[start + t] : ~0ull;
+            __syncthreads();
+            block_bitonic(s_long, np);
+            for (int t = threadIdx.x; t < n; t += blockDim.x)
+                w.tile_ids[start + t] = (uint32_t)s_long[t];
+        } else {
+            block_sort_long(w, start, n, s_long);
+        }
+        __syncthreads();   // the shared buffer is free for the next tile
     }
 }
 
 }  // namespace
+
+cudaError_t prepare_bin() {
+    return cudaFuncSetAttribute(k_tile_sort_long, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kLongSmem);
+}
 
 cudaError_t launch_bin(const Frames& fs, const Workspace& w, cudaStream_t stream) {
     const Frame& f = fs.f[0];
@@ -403,6 +486,9 @@ cudaError_t launch_bin(const Frames& fs, const Workspace& w, cudaStream_t stream
             e = launch_pdl(k_tile_sort,
                            dim3(((int)f.n_tiles_all + kTilesPerSortBlock - 1) / kTilesPerSortBlock),
                            dim3(kSortThreads), 0, stream, fs, w);
+        if (e == cudaSuccess)
+            e = launch_pdl(k_tile_sort_long, dim3(152 * kLongBlocksPerSm), dim3(kLongThreads),
+                           kLongSmem, stream, fs, w);
     }
     return e;
 }

@@ -25,7 +25,7 @@
 //
 // The first call on a device looks up the arena's device address with
 // cudaGetSymbolAddress (with that device current) and prepares the forward
-// kernels; make that first call before capturing any stream.  The call
+// and sort kernels; make that first call before capturing any stream.  The call
 // synchronises the stream at its end to read the frame's status.
 #include <cuda_runtime.h>
 
@@ -52,7 +52,8 @@ constexpr size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 constexpr size_t kOffRec = 0;
 constexpr size_t kOffCount = align256(kOffRec + sizeof(SphereRec) * kMaxSpheres);
 constexpr size_t kOffStart = align256(kOffCount + 4 * kMaxTilesNA);
-constexpr size_t kOffStaged = align256(kOffStart + 4 * (kMaxTilesNA + 1));
+constexpr size_t kOffLong = align256(kOffStart + 4 * (kMaxTilesNA + 1));
+constexpr size_t kOffStaged = align256(kOffLong + 4 * (size_t)kMaxTilesNA);
 constexpr size_t kOffPairs = align256(kOffStaged + 16 * (size_t)kMaxPairs);
 constexpr size_t kOffPairsAlt = align256(kOffPairs + 8 * (size_t)kMaxPairs);
 constexpr size_t kOffTileIds = align256(kOffPairsAlt + 8 * (size_t)kMaxPairs);
@@ -80,7 +81,7 @@ int arena_for_current_device(unsigned char** out) {
     if (!g_arena_dev[dev]) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_arena) != cudaSuccess || !p) return PULSAR_ERR_CUDA;
-        if (prepare_forward() != cudaSuccess) return PULSAR_ERR_CUDA;
+        if (prepare_forward() != cudaSuccess || prepare_bin() != cudaSuccess) return PULSAR_ERR_CUDA;
         g_arena_dev[dev] = static_cast<unsigned char*>(p);
     }
     *out = g_arena_dev[dev];
@@ -117,6 +118,7 @@ extern "C" int pulsar_render_noalloc(const float* pos, const float* radius, cons
     w.hitcnt = nullptr;
     w.tile_count = reinterpret_cast<uint32_t*>(a + kOffCount);
     w.tile_start = reinterpret_cast<uint32_t*>(a + kOffStart);
+    w.long_tiles = reinterpret_cast<uint32_t*>(a + kOffLong);
     w.staged = reinterpret_cast<uint4*>(a + kOffStaged);
     w.pairs = reinterpret_cast<unsigned long long*>(a + kOffPairs);
     w.pairs_alt = reinterpret_cast<unsigned long long*>(a + kOffPairsAlt);

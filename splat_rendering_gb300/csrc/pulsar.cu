@@ -130,6 +130,7 @@ int pulsar_create_cams(pulsar_ctx_t* out, int device, int64_t max_spheres, int64
     Workspace& w = c->ws;
     bool ok = alloc(c, &w.rec, K * N) && alloc(c, &w.gacc, K * N) && alloc(c, &w.hitcnt, K * N) &&
               alloc(c, &w.tile_count, K * B) && alloc(c, &w.tile_start, K * B + 1) &&
+              alloc(c, &w.long_tiles, K * B) &&
               alloc(c, &w.staged, (size_t)max_pairs) &&
               alloc(c, &w.pairs, (size_t)max_pairs) && alloc(c, &w.pairs_alt, (size_t)max_pairs) &&
               alloc(c, &w.tile_ids, (size_t)max_pairs) && alloc(c, &w.mg, K * P) &&
@@ -138,7 +139,8 @@ int pulsar_create_cams(pulsar_ctx_t* out, int device, int64_t max_spheres, int64
               alloc(c, &w.kpart, K * B * 4) && alloc(c, &w.rtpart, (N + 255) / 256 * K * 12) &&
               alloc(c, &w.state, 1);
     if (ok) ok = cudaMallocHost(&c->host_state, sizeof(DevState)) == cudaSuccess;
-    if (ok) ok = prepare_forward() == cudaSuccess && prepare_shade(&c->shade) == cudaSuccess;
+    if (ok) ok = prepare_forward() == cudaSuccess && prepare_bin() == cudaSuccess &&
+                 prepare_shade(&c->shade) == cudaSuccess;
     if (ok) ok = cudaDeviceGetAttribute(&c->n_sms, cudaDevAttrMultiProcessorCount, device) ==
                  cudaSuccess;
     if (ok)

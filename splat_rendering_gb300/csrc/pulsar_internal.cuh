@@ -71,6 +71,8 @@ struct DevState {
     uint32_t error;             // latched kErr* bits
     uint32_t inject;            // test hook bits (kInject*), cleared by pulsar_status
     uint32_t pair_cursor;       // staged pairs reserved by the projection (zero between frames)
+    uint32_t n_long;            // tiles whose list is longer than one warp sorts, this frame
+    uint32_t long_next;         // next entry of long_tiles to sort (reset by the tile scan)
 };
 
 // ------------------------------------------------ error-free transforms --
@@ -355,6 +357,7 @@ struct Workspace {
                        // (zero between frames)
     uint32_t* tile_count;   // [maxB] (zero between frames)
     uint32_t* tile_start;   // [maxB+1]
+    uint32_t* long_tiles;   // [maxB] tiles with lists longer than one warp sorts, in tile order
     uint4* staged;          // [max_pairs] (tile, slot in tile, key bits, id) from the projection
     unsigned long long* pairs;      // [max_pairs] (key bits << 32 | id), bucketed by tile
     unsigned long long* pairs_alt;  // [max_pairs] merge scratch for long tiles
@@ -448,6 +451,7 @@ cudaError_t launch_project(const Frames& fs, const Workspace& w, const float* po
                            const float* radius, const float* opacity, cudaStream_t stream);
 cudaError_t launch_bin(const Frames& fs, const Workspace& w, cudaStream_t stream);
 cudaError_t prepare_forward();   // opt the forward kernels into their shared memory
+cudaError_t prepare_bin();       // opt the long-list sort into its shared memory
 cudaError_t launch_forward(const Frames& fs, const Workspace& w, const float* features,
                            const float* bg, float* image, int max_pairs_stride,
                            cudaStream_t stream);
