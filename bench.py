@@ -43,7 +43,8 @@ WORKLOADS = {
 }
 METRIC = "fwd+bwd frames/s at 1M spheres 1024^2"
 UNIT = "frames/s"
-KERNELS_PER_STEP = 8   # project, tile_scan, emit, tile_sort, forward, backward, finalize, camera_reduce
+KERNELS_PER_STEP = 9   # project, tile_scan, emit, tile_sort, tile_sort_long, forward, backward,
+                       # finalize, camera_reduce
 SHADE_KERNELS = 5      # weight pack + shade forward, weight pack + shade backward + reduce
 
 
