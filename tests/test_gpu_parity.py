@@ -78,9 +78,14 @@ EDGE = {
                        rrange=(0.08, 0.4)),
     "five_channels": dict(seed=54, n=300, width=50, height=30, channels=5, n_track=9),
     "no_cutoff": dict(seed=55, n=500, width=64, height=48, geom_cutoff=False, rrange=(0.005, 0.2)),
-    # big spheres: tile lists longer than one shared-memory sort (merge path)
+    # big spheres: lists of ~4,200 keys, each sorted whole in shared memory
     "long_lists": dict(seed=56, n=20000, width=64, height=64, f=64.0, zrange=(2.5, 6.5),
                        rrange=(0.5, 1.5), spread=1.5),
+    # many one-pixel spheres: lists of ~20,600 keys, past one shared-memory
+    # sort, so sorted in chunks merged through global memory (four merge
+    # passes), at ~150 hits per pixel
+    "huge_lists": dict(seed=63, n=80000, width=32, height=32, f=32.0, zrange=(2.5, 6.5),
+                       rrange=(0.001, 0.01)),
     "spill_outside": dict(seed=57, n=2000, width=80, height=60, spread=2.5, rrange=(0.01, 0.5)),
 }
 
@@ -96,6 +101,8 @@ def test_edge_cases(oracle_lib, case):
     gh.compare_frame(g, o, case)
     if case == "long_lists":
         assert np.diff(offs).max() > 2048
+    if case == "huge_lists":
+        assert np.diff(offs).min() > 16384
 
 
 @pytest.mark.parametrize("n", [3000, 6000, 12000])
