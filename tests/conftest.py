@@ -32,3 +32,27 @@ def oracle_lib():
     import oracle
     oracle.build()
     return oracle
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    # how much the gradient tolerance's widening terms did in this session
+    try:
+        import gpu_helpers
+    except Exception:
+        return
+    rows = gpu_helpers.WIDENING
+    if not rows:
+        return
+    tr = terminalreporter
+    tr.section("gradient comparisons: entries passing only through the A or S terms")
+    tr.write_line(f"{'comparison':58s} {'entries':>9s} {'> plain':>8s} {'worst/plain':>11s} "
+                  f"{'cond needed':>11s} {'need S':>7s}")
+    for what, n, wid, worst, need, no_s in rows:
+        tr.write_line(f"{what[:58]:58s} {n:9d} {wid:8d} {worst:11.3g} {need:11.3g} {no_s:7d}")
+    path = os.environ.get("PULSAR_WIDENING_LOG")
+    if path:
+        import json
+        with open(path, "w") as f:
+            json.dump([dict(what=r[0], entries=r[1], outside_plain=r[2], worst_over_plain=r[3],
+                            cond_needed=r[4], outside_without_sens=r[5]) for r in rows], f,
+                      indent=1)
