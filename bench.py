@@ -55,10 +55,14 @@ def args_parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-scenes", action="store_true",
+                    help="headline only: skip timing the neural and driving configurations")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle sample")
     ap.add_argument("--scene", default="headline", choices=sorted(WORKLOADS),
                     help="workload (the default is the headline configuration)")
+    ap.add_argument("--cams", type=int, default=0,
+                    help="driving rig: render only its first CAMS cameras (0: all six)")
     ap.add_argument("--frames-only", type=int, default=0,
                     help="render and differentiate this many frames eagerly, print nothing "
                          "(a short fixed launch sequence for profilers)")
@@ -146,13 +150,13 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "sm_max_mhz": 2070.0}, "fallback"
 
 
-# FP32 peak of the ALU-bound kernels: 152 SMs x 128 FP32 lanes x 2 flops (FMA) at
-# the maximum SM clock of MEASURED_PEAKS (2070 MHz) = 80.5 TFLOP/s.
-SMS, FP32_LANES = 152, 128
+# FP32 peak of the ALU-bound kernels: SMs (read from the device) x 128 FP32
+# lanes x 2 flops (FMA) at the maximum SM clock of MEASURED_PEAKS (2070 MHz).
+FP32_LANES = 128
 
 
-def fp32_peak_tflops(peaks) -> float:
-    return SMS * FP32_LANES * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
+def fp32_peak_tflops(peaks, sms: int) -> float:
+    return sms * FP32_LANES * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
 
 
 def algorithmic_bytes(stage, N, M, P, C, T):
@@ -293,13 +297,245 @@ def run_reference(a):
 
 
 # ----------------------------------------------------------------- gb300 --
+class Workload:
+    """One configuration on one device: inputs resident in HBM, a context sized
+    for it, and one step (project -> bin -> forward [-> shading] -> backward)."""
+
+    def __init__(self, name, dev, local, cams=0):
+        import numpy as np
+        import torch
+
+        from splat_rendering_gb300 import pulsar as pl
+        from splat_rendering_gb300 import scenes
+        self.name, self.dev, self.pl = name, dev, pl
+        self.shaded = name == "neural_shaded"
+        scene = scenes.make("neural" if self.shaded else name)
+        self.scene = scene
+        # the driving rig renders its six cameras as one batch; the others one camera
+        cams = scene.cameras[:cams or None] if name == "driving" else scene.cameras[:1]
+        self.cams, self.K = cams, len(cams)
+        K = self.K
+        cam, prm = cams[0], scene.params
+        self.cam, self.prm = cam, prm
+        self.N, self.C, self.T = scene.n, prm.channels, prm.n_track
+        self.P = cam.width * cam.height * K
+
+        def dev_t(x):
+            return torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+
+        self.dev_t = dev_t
+        self.pos, self.rad, self.opa, self.feat = (dev_t(scene.pos), dev_t(scene.radius),
+                                                   dev_t(scene.opacity), dev_t(scene.features))
+        self.G_host = np.stack(scene.grad_images[:K]) if K > 1 else scene.grad_images[0]
+        self.bg, self.G = dev_t(scene.bg), dev_t(self.G_host)
+        self.c_cam = [pl.camera(c) for c in cams] if K > 1 else pl.camera(cam)
+        self.c_prm = pl.params(prm)
+        N, C = self.N, self.C
+        self.image = torch.empty(((K,) if K > 1 else ()) + (cam.height, cam.width, C), device=dev)
+        self.grads = {"pos": torch.empty((N, 3), device=dev), "radius": torch.empty(N, device=dev),
+                      "opacity": torch.empty(N, device=dev),
+                      "features": torch.empty((N, C), device=dev),
+                      "cam": torch.empty(((K,) if K > 1 else ()) + (16,), device=dev)}
+        self.cap = 4 * N
+        self.local = local
+        self.r = self._renderer(self.cap)
+        if self.shaded:
+            # per-pixel MLP shading: rgb = MLP(F); dL/drgb seeded; dL/dF feeds the render backward
+            self.mlp_host = scenes.shading_mlp(5)
+            self.drgb_host = scenes.shading_grad(7, cam.height, cam.width)
+            self.mlp_w, self.drgb = dev_t(self.mlp_host), dev_t(self.drgb_host)
+            self.rgb = torch.empty((cam.height, cam.width, 3), device=dev)
+            self.gF = torch.empty_like(self.image)
+            self.grads["mlp"] = torch.empty_like(self.mlp_w)
+
+    def _renderer(self, cap):
+        return self.pl.Renderer(max_spheres=self.N, max_pairs=cap, max_width=self.cam.width,
+                                max_height=self.cam.height, max_channels=self.C,
+                                max_track=self.T, device=self.local, max_cams=self.K)
+
+    def step(self):
+        r = self.r
+        r.render(self.pos, self.rad, self.opa, self.feat, self.c_cam, self.c_prm, self.bg,
+                 image=self.image)
+        if self.shaded:
+            r.shade(self.image, self.mlp_w, self.rgb)
+            r.shade_backward(self.image, self.mlp_w, self.drgb, self.gF, self.grads["mlp"])
+            r.backward(self.gF, out=self.grads)
+        else:
+            r.backward(self.G, out=self.grads)
+
+    def first_frame(self):
+        """Render once; grow the pair capacity if needed.  Sets M, H, Ht."""
+        import numpy as np
+        import torch
+        pl = self.pl
+        self.step()
+        code, M, H = self.r.status(raise_on_error=False)
+        if code == pl.ERR_CAPACITY:
+            self.r.close()
+            self.r = self._renderer(2 * M)
+            self.step()
+            code, M, H = self.r.status()
+        assert code == 0, pl.strerror(code)
+        ids = torch.from_numpy(self.r.debug("ids").view(np.int32))
+        self.M, self.H, self.Ht = M, H, int((ids >= 0).sum())
+
+    def graph(self):
+        import torch
+        s = torch.cuda.Stream(device=self.dev)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for _ in range(2):
+                self.step()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.step()
+        torch.cuda.synchronize()
+        return g
+
+    def stages(self):
+        return ("project", "bin", "forward") + (("shade_forward", "shade_backward")
+                                                if self.shaded else ()) + ("backward",)
+
+    def breakdown(self, steps, flush):
+        """Per-stage device times: the same kernels eagerly, CUDA events between
+        the ABI calls on the stream they launch on, L2 flushed before each step."""
+        import torch
+        pl, r, stages = self.pl, self.r, self.stages()
+        per = {k: [] for k in stages}
+        for _ in range(steps):
+            flush.zero_()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
+            ev[0].record()
+            if self.K > 1:
+                pl.project_cams(r.ctx, self.pos, self.rad, self.opa, self.N, self.c_cam,
+                                self.c_prm)
+            else:
+                pl.project(r.ctx, self.pos, self.rad, self.opa, self.N, self.c_cam, self.c_prm)
+            ev[1].record()
+            pl.bin(r.ctx)
+            ev[2].record()
+            pl.forward(r.ctx, self.feat, self.bg, self.image)
+            ev[3].record()
+            G_in = self.G
+            if self.shaded:
+                pl.shade_forward(r.ctx, self.image, self.mlp_w, self.rgb)
+                ev[4].record()
+                pl.shade_backward(r.ctx, self.image, self.mlp_w, self.drgb, self.gF,
+                                  self.grads["mlp"])
+                ev[5].record()
+                G_in = self.gF
+            g = self.grads
+            pl.backward(r.ctx, self.feat, self.bg, self.image, G_in, g["pos"], g["radius"],
+                        g["opacity"], g["features"], g["cam"])
+            ev[-1].record()
+            torch.cuda.synchronize()
+            for i, k in enumerate(stages):
+                per[k].append(ev[i].elapsed_time(ev[i + 1]))
+        return {k: statistics.median(v) for k, v in per.items()}
+
+    def rooflines(self, breakdown, step_ms, peaks, peak_src, sms):
+        """Forward-kernel roofline and the whole path's, from the algorithmic
+        byte and flop counts of each stage."""
+        N, M, P, C, T, H, Ht = self.N, self.M, self.P, self.C, self.T, self.H, self.Ht
+        hbm = float(peaks["hbm_gbs"])
+        fp32 = fp32_peak_tflops(peaks, sms)
+        clk = float(peaks.get("sm_max_mhz", 2070.0))
+        fwd_flops = algorithmic_flops("forward", N, M, P, C, T, H, Ht)
+        fwd_bytes = algorithmic_bytes("forward", N, M, P, C, T)
+        fwd_s = breakdown["forward"] * 1e-3
+        achieved = fwd_flops / fwd_s / 1e12
+        roofline = {"bound": "alu", "kernel": "k_forward", "achieved": achieved, "peak": fp32,
+                    "unit": "TFLOP/s", "frac": achieved / fp32,
+                    "traffic": (traffic_from_profile("k_forward", "forward.cu", "headline")
+                                if self.name == "headline" else None),
+                    "algorithmic_flops": fwd_flops, "algorithmic_bytes": fwd_bytes,
+                    "hbm_frac": fwd_bytes / fwd_s / 1e9 / hbm,
+                    # secondary ceiling: two MUFU operations (exp2, rsqrt) per hit at
+                    # 16 per SM and clock
+                    "mufu_time_us": 2 * H / (sms * 16 * clk * 1e6) * 1e6,
+                    "peak_source": f"FP32: {sms} SMs (read from the device) x {FP32_LANES} "
+                                   f"lanes x 2 x {clk} MHz ({peak_src} clock); "
+                                   f"HBM: {peak_src} hbm_gbs {hbm}"}
+        render_stages = ("project", "bin", "forward", "backward")
+        path_bytes = sum(algorithmic_bytes(k, N, M, P, C, T) for k in render_stages)
+        path_flops = sum(algorithmic_flops(k, N, M, P, C, T, H, Ht) for k in render_stages)
+        shade_roof = None
+        if self.shaded:
+            bf16 = float(peaks.get("bf16_tflops_sustained", 1700.0))   # inside a long step
+            shade_roof = {}
+            for k in ("shade_forward", "shade_backward"):
+                b, fl = SHADE_BYTES_PER_PIXEL[k] * P, SHADE_FLOPS_PER_PIXEL[k] * P
+                t_s = breakdown[k] * 1e-3
+                shade_roof[k] = {"bound": "hbm", "achieved": b / t_s / 1e9, "peak": hbm,
+                                 "unit": "GB/s", "frac": b / t_s / 1e9 / hbm,
+                                 "algorithmic_bytes": b, "tensor_flops": fl,
+                                 "tensor_frac": fl / t_s / 1e12 / bf16}
+                path_bytes += b
+        path_time = max(path_bytes / (hbm * 1e9), path_flops / (fp32 * 1e12))
+        path = {"algorithmic_bytes": path_bytes, "algorithmic_flops": path_flops,
+                "hbm_time_ms": path_bytes / (hbm * 1e9) * 1e3,
+                "fp32_time_ms": path_flops / (fp32 * 1e12) * 1e3,
+                "frac": path_time * 1e3 / step_ms}
+        return roofline, path, shade_roof
+
+    def close(self):
+        self.r.close()
+
+
+def time_graph(graph, steps, flush):
+    """Per-step device times of graph replays, L2 flushed before each (outside
+    the events)."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    torch.cuda.synchronize()
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record()
+        graph.replay()
+        e1.record()
+    torch.cuda.synchronize()
+    return [e0.elapsed_time(e1) for e0, e1 in evs]
+
+
+def side_scene(name, dev, local, steps, warmup, flush, peaks, peak_src, sms):
+    """A further configuration timed the same way as the headline (graph replay
+    of one step, L2 flushed between steps), for the run's record."""
+    import numpy as np
+    wl = Workload(name, dev, local)
+    wl.first_frame()
+    g = wl.graph()
+    for _ in range(warmup):
+        flush.zero_()
+        g.replay()
+    step_ms = time_graph(g, steps, flush)
+    ms = statistics.median(step_ms)
+    bd = wl.breakdown(max(3, steps // 2), flush)
+    roof, path, shade = wl.rooflines(bd, ms, peaks, peak_src, sms)
+    out = {"workload": WORKLOADS[name], "steps": steps, "ms_per_step": ms,
+           "value": wl.K / (ms * 1e-3), "unit": UNIT if wl.K == 1 else "camera frames/s",
+           "step_ms_quantiles": {q: float(np.quantile(step_ms, v)) for q, v in
+                                 (("p10", 0.1), ("p90", 0.9))},
+           "breakdown_ms": bd, "path_roofline": path,
+           "forward_roofline": {k: roof[k] for k in ("achieved", "peak", "unit", "frac",
+                                                      "hbm_frac")},
+           "pairs_per_frame": wl.M, "hits_per_frame": wl.H, "tracked_hits_per_frame": wl.Ht}
+    if shade:
+        out["shade_roofline"] = shade
+    del g
+    wl.close()
+    return out
+
+
 def run_gb300(a):
     import numpy as np
     import torch
 
     from splat_rendering_gb300 import build as pbuild
     from splat_rendering_gb300 import pulsar as pl
-    from splat_rendering_gb300 import scenes
 
     world, rank, local = dist_env()
     torch.cuda.set_device(local)
@@ -310,85 +546,27 @@ def run_gb300(a):
     pbuild.build()
     pl.load()
     dev = torch.device("cuda", local)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
 
-    shaded = a.scene == "neural_shaded"
-    scene = scenes.make("neural" if shaded else a.scene)
-    # the driving rig renders its six cameras as one batch; the others one camera
-    cams = scene.cameras if a.scene == "driving" else scene.cameras[:1]
-    K = len(cams)
-    cam, prm = cams[0], scene.params
-    N, C, T = scene.n, prm.channels, prm.n_track
-    P = cam.width * cam.height * K
-
-    def dev_t(x):
-        return torch.from_numpy(np.ascontiguousarray(x)).to(dev)
-
-    pos, rad, opa, feat = dev_t(scene.pos), dev_t(scene.radius), dev_t(scene.opacity), \
-        dev_t(scene.features)
-    G_host = np.stack(scene.grad_images[:K]) if K > 1 else scene.grad_images[0]
-    bg, G = dev_t(scene.bg), dev_t(G_host)
-    c_cam = [pl.camera(c) for c in cams] if K > 1 else pl.camera(cam)
-    c_prm = pl.params(prm)
-    image = torch.empty(((K,) if K > 1 else ()) + (cam.height, cam.width, C), device=dev)
-    grads = {"pos": torch.empty((N, 3), device=dev), "radius": torch.empty(N, device=dev),
-             "opacity": torch.empty(N, device=dev), "features": torch.empty((N, C), device=dev),
-             "cam": torch.empty(((K,) if K > 1 else ()) + (16,), device=dev)}
-    cap = 4 * N
-    r = pl.Renderer(max_spheres=N, max_pairs=cap, max_width=cam.width, max_height=cam.height,
-                    max_channels=C, max_track=T, device=local, max_cams=K)
-    if shaded:
-        # per-pixel MLP shading: rgb = MLP(F); dL/drgb seeded; dL/dF feeds the render backward
-        mlp_host = scenes.shading_mlp(5)
-        drgb_host = scenes.shading_grad(7, cam.height, cam.width)
-        mlp_w, drgb = dev_t(mlp_host), dev_t(drgb_host)
-        rgb = torch.empty((cam.height, cam.width, 3), device=dev)
-        gF = torch.empty_like(image)
-        grads["mlp"] = torch.empty_like(mlp_w)
-
-    def step():
-        r.render(pos, rad, opa, feat, c_cam, c_prm, bg, image=image)
-        if shaded:
-            r.shade(image, mlp_w, rgb)
-            r.shade_backward(image, mlp_w, drgb, gF, grads["mlp"])
-            r.backward(gF, out=grads)
-        else:
-            r.backward(G, out=grads)
-
-    step()
-    code, M, H = r.status(raise_on_error=False)
+    wl = Workload(a.scene, dev, local, a.cams)
     if a.frames_only:
-        for _ in range(a.frames_only - 1):
-            step()
+        for _ in range(a.frames_only):
+            wl.step()
         torch.cuda.synchronize()
-        assert r.status()[0] == 0
-        r.close()
+        assert wl.r.status()[0] == 0
+        wl.close()
         return
-    if code == pl.ERR_CAPACITY:
-        r.close()
-        r = pl.Renderer(max_spheres=N, max_pairs=2 * M, max_width=cam.width,
-                        max_height=cam.height, max_channels=C, max_track=T, device=local,
-                        max_cams=K)
-        step()
-        code, M, H = r.status()
-    assert code == 0, pl.strerror(code)
-    ids = torch.from_numpy(r.debug("ids").view(np.int32))
-    Ht = int((ids >= 0).sum())
+    wl.first_frame()
+    K, N, C, T, P = wl.K, wl.N, wl.C, wl.T, wl.P
+    M, H, Ht = wl.M, wl.H, wl.Ht
+    r, shaded, cam = wl.r, wl.shaded, wl.cam
+    image, grads = wl.image, wl.grads
+    c_cam, c_prm, bg = wl.c_cam, wl.c_prm, wl.bg
 
     flush = torch.empty(64 * 1024 * 1024, dtype=torch.int32, device=dev)   # 256 MB > L2
 
     # ---- CUDA graph of one step
-    s = torch.cuda.Stream(device=dev)
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
-        for _ in range(2):
-            step()
-    torch.cuda.current_stream().wait_stream(s)
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        step()
-    torch.cuda.synchronize()
-
+    graph = wl.graph()
     for _ in range(a.warmup):
         flush.zero_()
         graph.replay()
@@ -406,56 +584,19 @@ def run_gb300(a):
         torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(a.steps)]
     torch.cuda.synchronize()
     t_wall0 = time.perf_counter()
-    for e0, e1 in evs:
-        flush.zero_()
-        e0.record()
-        graph.replay()
-        e1.record()
-    torch.cuda.synchronize()
+    step_ms = time_graph(graph, a.steps, flush)
     t_wall = time.perf_counter() - t_wall0
     clk = clocks.stop()
     if clk:
         clk["window"] = "nvidia-smi every 50 ms over ~0.4 s of identical steps and the timed steps"
-    step_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
     total_ms = max_over_ranks(sum(step_ms), dist, dev)
     if dist:
         dist.barrier()
 
     # ---- per-stage breakdown (same kernels, eager, events between ABI calls)
-    stages = ("project", "bin", "forward") + (("shade_forward", "shade_backward") if shaded
-                                             else ()) + ("backward",)
-    per = {k: [] for k in stages}
-    for _ in range(a.steps):
-        flush.zero_()
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
-        ev[0].record()
-        if K > 1:
-            pl.project_cams(r.ctx, pos, rad, opa, N, c_cam, c_prm)
-        else:
-            pl.project(r.ctx, pos, rad, opa, N, c_cam, c_prm)
-        ev[1].record()
-        pl.bin(r.ctx)
-        ev[2].record()
-        pl.forward(r.ctx, feat, bg, image)
-        ev[3].record()
-        G_in = G
-        if shaded:
-            pl.shade_forward(r.ctx, image, mlp_w, rgb)
-            ev[4].record()
-            pl.shade_backward(r.ctx, image, mlp_w, drgb, gF, grads["mlp"])
-            ev[5].record()
-            G_in = gF
-        pl.backward(r.ctx, feat, bg, image, G_in, grads["pos"], grads["radius"],
-                    grads["opacity"], grads["features"], grads["cam"])
-        ev[-1].record()
-        torch.cuda.synchronize()
-        for i, k in enumerate(stages):
-            per[k].append(ev[i].elapsed_time(ev[i + 1]))
-    breakdown = {k: statistics.median(v) for k, v in per.items()}
+    breakdown = wl.breakdown(a.steps, flush)
 
     # ---- end to end through the API with host buffers (pinned), copies timed.
     # Every step uploads its inputs from pinned host memory and downloads its
@@ -463,11 +604,12 @@ def run_gb300(a):
     # call): step i+1's uploads and step i-1's downloads run on the copy
     # engines while step i computes, inputs and outputs double-buffered on the
     # device.  The same steps one at a time are reported as e2e_serial.
+    scene = wl.scene
     ins = [("pos", scene.pos), ("radius", scene.radius), ("opacity", scene.opacity),
            ("features", scene.features)]
-    ins += [("mlp", mlp_host), ("drgb", drgb_host)] if shaded else [("G", G_host)]
+    ins += [("mlp", wl.mlp_host), ("drgb", wl.drgb_host)] if shaded else [("G", wl.G_host)]
     host_in = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in ins}
-    host_out = {"image": torch.empty((rgb if shaded else image).shape).pin_memory()}
+    host_out = {"image": torch.empty((wl.rgb if shaded else image).shape).pin_memory()}
     for k, v in grads.items():
         host_out[k] = torch.empty(v.shape).pin_memory()
     h2d = sum(v.numel() * 4 for v in host_in.values())
@@ -478,7 +620,7 @@ def run_gb300(a):
               "image": torch.empty_like(image),
               "grads": {k: torch.empty_like(v) for k, v in grads.items()}}
         if shaded:
-            st["rgb"], st["gF"] = torch.empty_like(rgb), torch.empty_like(gF)
+            st["rgb"], st["gF"] = torch.empty_like(wl.rgb), torch.empty_like(wl.gF)
         sets.append(st)
 
     def compute(st, stream):
@@ -572,63 +714,26 @@ def run_gb300(a):
         torch.cuda.synchronize()
         serial_ms.append(e0.elapsed_time(e1))
     e2e_serial_total = max_over_ranks(sum(serial_ms), dist, dev)
+    del cgraphs, sets
 
     # ---- roofline of the dominant kernel (the forward) and of the whole path
     peaks, peak_src = measured_peaks()
-    hbm = float(peaks["hbm_gbs"])
-    fp32 = fp32_peak_tflops(peaks)
-    fwd_flops = algorithmic_flops("forward", N, M, P, C, T, H, Ht)
-    fwd_bytes = algorithmic_bytes("forward", N, M, P, C, T)
-    fwd_s = breakdown["forward"] * 1e-3
-    achieved = fwd_flops / fwd_s / 1e12
-    roofline = {"bound": "alu", "kernel": "k_forward", "achieved": achieved, "peak": fp32,
-                "unit": "TFLOP/s", "frac": achieved / fp32,
-                "traffic": (traffic_from_profile("k_forward", "forward.cu", "headline")
-                            if a.scene == "headline" else None),
-                "algorithmic_flops": fwd_flops, "algorithmic_bytes": fwd_bytes,
-                "hbm_frac": fwd_bytes / fwd_s / 1e9 / hbm,
-                # secondary ceiling: two MUFU operations (exp2, rsqrt) per hit at
-                # 16 per SM and clock
-                "mufu_time_us": 2 * H / (SMS * 16 * float(peaks.get("sm_max_mhz", 2070.0))
-                                         * 1e6) * 1e6,
-                "peak_source": f"FP32: {SMS} SMs x {FP32_LANES} lanes x 2 x "
-                               f"{peaks.get('sm_max_mhz', 2070.0)} MHz ({peak_src} clock); "
-                               f"HBM: {peak_src} hbm_gbs {hbm}"}
-    render_stages = ("project", "bin", "forward", "backward")
-    path_bytes = sum(algorithmic_bytes(k, N, M, P, C, T) for k in render_stages)
-    path_flops = sum(algorithmic_flops(k, N, M, P, C, T, H, Ht) for k in render_stages)
-    shade_roof = None
-    if shaded:
-        bf16 = float(peaks.get("bf16_tflops_sustained", 1700.0))   # inside a long step
-        shade_roof = {}
-        for k in ("shade_forward", "shade_backward"):
-            b, fl = SHADE_BYTES_PER_PIXEL[k] * P, SHADE_FLOPS_PER_PIXEL[k] * P
-            t_s = breakdown[k] * 1e-3
-            shade_roof[k] = {"bound": "hbm", "achieved": b / t_s / 1e9, "peak": hbm,
-                             "unit": "GB/s", "frac": b / t_s / 1e9 / hbm,
-                             "algorithmic_bytes": b, "tensor_flops": fl,
-                             "tensor_frac": fl / t_s / 1e12 / bf16}
-            path_bytes += b
-    path_time = max(path_bytes / (hbm * 1e9), path_flops / (fp32 * 1e12))
-    path = {"algorithmic_bytes": path_bytes, "algorithmic_flops": path_flops,
-            "hbm_time_ms": path_bytes / (hbm * 1e9) * 1e3,
-            "fp32_time_ms": path_flops / (fp32 * 1e12) * 1e3,
-            "frac": path_time * 1e3 / (total_ms / a.steps)}
+    roofline, path, shade_roof = wl.rooflines(breakdown, total_ms / a.steps, peaks, peak_src, sms)
 
     value = job_rate(world, K, a.steps, total_ms)   # camera frames (K per step)
     per_cam_loop = None
     if K > 1:
         # the same rig rendered camera by camera through one single-camera
         # context (a graph of K render + backward calls), timed the same way
-        r1 = pl.Renderer(max_spheres=N, max_pairs=cap, max_width=cam.width,
+        r1 = pl.Renderer(max_spheres=N, max_pairs=wl.cap, max_width=cam.width,
                          max_height=cam.height, max_channels=C, max_track=T, device=local)
-        singles = [pl.camera(c) for c in cams]
+        singles = [pl.camera(c) for c in wl.cams]
         g1 = {k: (v[0] if k == "cam" else v) for k, v in grads.items()}
 
         def loop_step():
             for k in range(K):
-                r1.render(pos, rad, opa, feat, singles[k], c_prm, bg, image=image[k])
-                r1.backward(G[k], out=g1)
+                r1.render(wl.pos, wl.rad, wl.opa, wl.feat, singles[k], c_prm, bg, image=image[k])
+                r1.backward(wl.G[k], out=g1)
 
         s1 = torch.cuda.Stream(device=dev)
         s1.wait_stream(torch.cuda.current_stream())
@@ -643,16 +748,8 @@ def run_gb300(a):
         for _ in range(a.warmup):
             flush.zero_()
             graph1.replay()
-        torch.cuda.synchronize()
-        ev1 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(a.steps)]
-        for e0, e1 in ev1:
-            flush.zero_()
-            e0.record()
-            graph1.replay()
-            e1.record()
-        torch.cuda.synchronize()
-        per_cam_loop = sum(e0.elapsed_time(e1) for e0, e1 in ev1) / a.steps
+        per_cam_loop = sum(time_graph(graph1, a.steps, flush)) / a.steps
+        del graph1
         r1.close()
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
             "warmup": a.warmup, "ms_per_step": total_ms / a.steps, "higher_is_better": True,
@@ -684,18 +781,24 @@ def run_gb300(a):
                                      "stream, L2 flushed between steps"},
             "gpu_launches": (KERNELS_PER_STEP + (SHADE_KERNELS if shaded else 0)) * a.steps,
             "clocks": clk, "wall_s_timed": t_wall}
+    del graph
+    wl.close()
+    if a.scene == "headline" and rank == 0 and world == 1 and not a.no_scenes:
+        # the other large configurations, timed in the same run the same way
+        # (not part of the metric: the headline is)
+        line["scenes"] = {name: side_scene(name, dev, local, min(a.steps, 20), 3, flush, peaks,
+                                           peak_src, sms)
+                          for name in ("neural", "driving")}
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
-        v, rows, dt, cores, reps = oracle_sample(scene, a.cpu_seconds,
-                                                 shade=(mlp_host.astype(np.float64), drgb_host)
-                                                 if shaded else None)
+        shade_args = (wl.mlp_host.astype(np.float64), wl.drgb_host) if shaded else None
+        v, rows, dt, cores, reps = oracle_sample(scene, a.cpu_seconds, shade=shade_args)
         what = "fwd, MLP fwd+bwd, bwd" if shaded else "fwd+bwd"
         # the same oracle on one core, on a band sized for a few seconds
         import oracle
         oracle.set_threads(1)
         v1, rows1, dt1, _, _ = oracle_sample(scene, max(2.0, a.cpu_seconds / 4),
                                              rows=max(8, rows // max(1, cores)),
-                                             shade=(mlp_host.astype(np.float64), drgb_host)
-                                             if shaded else None)
+                                             shade=shade_args)
         oracle.set_threads(0)
         line["cpu_baseline_1core"] = {"value": v1, "unit": UNIT, "cores": 1, "kind": "oracle",
                                       "sample": f"rows [0,{rows1}) x 1024 once ({dt1:.1f} s), "
@@ -706,7 +809,6 @@ def run_gb300(a):
                                           f"scaled by {rows}/1024"}
     if rank == 0:
         print(json.dumps(line), flush=True)
-    r.close()
     if dist:
         dist.destroy_process_group()
 

@@ -51,7 +51,9 @@ extern "C" {
 #define PULSAR_ERR_CAPACITY -3  /* more sphere-tile pairs than max_pairs */
 #define PULSAR_ERR_STATE    -4  /* call out of order (e.g. forward before bin) */
 #define PULSAR_ERR_NOMEM    -5  /* workspace allocation failed */
-#define PULSAR_ERR_TIMEOUT  -6  /* a bounded wait on the tensor cores gave up (frame invalid) */
+#define PULSAR_ERR_TIMEOUT  -6  /* a bounded wait on the tensor cores gave up: the frame is
+                                  invalid and, since work may still have been in flight,
+                                  the context should be destroyed and recreated */
 
 /* --------------------------------------------------------------- flags -- */
 /* Drop position/radius gradients (and the sphere's share of the camera
@@ -280,13 +282,14 @@ int64_t pulsar_debug_copy(pulsar_ctx_t ctx, int what, void* dst, int64_t bytes, 
 
 /* Forward render of one small frame that allocates no memory (the pages have
  * no counterpart: this entry point exists for callers that cannot call
- * cudaMalloc -- code running while a stream is captured into a graph,
- * plugins whose host framework owns the device memory budget, fixed-footprint
- * real-time renderers).  It runs the kernels of pulsar_project, pulsar_bin and
- * pulsar_forward with all intermediate arrays in one static device arena of
- * about 8 MB that the library reserves on every GPU that loads it, until the
- * process exits.  No context is needed; inputs and outputs are as for
- * pulsar_project and pulsar_forward.
+ * cudaMalloc while they render -- plugins whose host framework owns the device
+ * memory budget, fixed-footprint real-time renderers that must not risk an
+ * allocation failure or its implicit synchronisation mid-frame).  It runs the
+ * kernels of pulsar_project, pulsar_bin and pulsar_forward with all
+ * intermediate arrays in one static device arena of about 8 MB that the
+ * library reserves on every GPU that loads it, until the process exits.  No
+ * context is needed; inputs and outputs are as for pulsar_project and
+ * pulsar_forward.
  *   Limits: n <= 16384 spheres, at most 65536 sphere-tile pairs, width and
  *   height <= 256, n_track <= 8, channels <= 64.  Larger sizes return
  *   PULSAR_ERR_ARG without enqueueing anything; a frame with more pairs returns
@@ -295,8 +298,9 @@ int64_t pulsar_debug_copy(pulsar_ctx_t ctx, int what, void* dst, int64_t bytes, 
  *   clears what must start at zero.  Calls that overlap on the GPU race: the
  *   caller must serialise them.
  *   The first call on a device looks up the arena's device address and
- *   prepares the kernels; make it before capturing any stream.  The call
- *   synchronises `stream` at its end to read the frame's status. */
+ *   prepares the kernels; that first call should come before any stream
+ *   capture.  Every call synchronises `stream` at its end to read the frame's
+ *   status. */
 int pulsar_render_noalloc(const float* pos, const float* radius, const float* opacity,
                           const float* features, int64_t n, const pulsar_camera_t* cam,
                           const pulsar_params_t* params, const float* bg, float* image,

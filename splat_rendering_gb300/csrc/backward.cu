@@ -12,13 +12,16 @@
 //             the warp-level aggregation of DISTWAR (arxiver abstract); a
 //             warp's two pixel rows are interleaved column by column, so the
 //             footprint of a small sphere is a single run.  dL/dc and
-//             dL/dr go to a float4 accumulator with one vector reduction;
-//             opacity and feature gradients go straight to the caller's
+//             dL/dr go to a float4 accumulator with one vector reduction; with
+//             at most three channels dL/do and dL/df go to a second one (two
+//             reductions per run in all), otherwise straight to the caller's
 //             (zeroed) arrays.  The intrinsics' gradient is summed per thread
 //             and reduced per block.
 // k_finalize_one_cam, k_finalize_cams  four spheres per thread: dL/dp =
-//             R^T dL/dc and dL/dr out of the accumulator (which it zeroes for
-//             the next frame), summed over the cameras of a batch;
+//             R^T dL/dc and dL/dr out of the accumulator, and dL/do, dL/df out
+//             of the second one, summed over the cameras of a batch (the
+//             accumulators are zeroed right before the backward, so the lines
+//             its reductions touch are fresh in L2);
 //             dL/dR = sum dL/dc p^T and dL/dt = sum dL/dc of every camera
 //             reduced per block (Pulsar Sec. B.2: sphere-wise camera-gradient
 //             accumulation).
@@ -52,9 +55,11 @@ k_backward(Frames fs, Workspace w, const float* __restrict__ features,
            float* __restrict__ grad_opacity, float* __restrict__ grad_features, int mode) {
     pdl_begin();
     // mode bit 0: geometry gradients wanted; bit 1: feature gradient rows are
-    // 16-byte aligned with C a multiple of 4 (vector reductions)
+    // 16-byte aligned with C a multiple of 4 (vector reductions); bit 2: C <= 3,
+    // opacity and feature gradients into the second accumulator
     const bool want_geom = (mode & 1) != 0;
     const bool feat_v4 = (mode & 2) != 0;
+    const bool acc2 = CMAX <= 4 && (mode & 4) != 0;
     constexpr int NB = BwdBatch<CMAX>::n;
     constexpr int NV = 5 + CMAX;   // dL/dc.xyz, dL/dr, dL/do, dL/df[CMAX]
     __shared__ float4 s_uv[NB];
@@ -83,6 +88,7 @@ k_backward(Frames fs, Workspace w, const float* __restrict__ features,
     uint32_t start = w.tile_start[tile_g], end = w.tile_start[tile_g + 1];
     const SphereRec* __restrict__ rec = w.rec + f.rec_base;   // this camera's records
     float4* __restrict__ gacc = w.gacc + f.rec_base;
+    float4* __restrict__ gacc2 = w.gacc2;   // one for all cameras: their sum is wanted
     end = min(end, f.max_pairs);
     start = min(start, end);
     // a batch's records and features are copied by cp.async; the first batch
@@ -252,8 +258,12 @@ k_backward(Frames fs, Workspace w, const float* __restrict__ features,
                 const int id = s_id[j];
                 if (f.flags & kParamNormalize) atomicAdd(&w.hitcnt[f.rec_base + id], (float)gsz);
                 if (want_geom && !cut) red_add_v4(&gacc[id], v[0], v[1], v[2], v[3]);
-                if (grad_opacity) atomicAdd(&grad_opacity[id], v[4]);
-                if (grad_features) {
+                if constexpr (CMAX <= 4) {
+                    // channels beyond C hold zeros
+                    if (acc2) red_add_v4(&gacc2[id], v[4], v[5], v[6], v[7]);
+                }
+                if (!acc2 && grad_opacity) atomicAdd(&grad_opacity[id], v[4]);
+                if (!acc2 && grad_features) {
                     float* gf = grad_features + (size_t)id * C;
                     bool done_v4 = false;
                     if constexpr (CMAX % 4 == 0) {
@@ -334,34 +344,84 @@ __device__ __forceinline__ void finalize_one(const Frame& f, float4 g, float px,
     acc[9] += g.x; acc[10] += g.y; acc[11] += g.z;
 }
 
+// dL/do and dL/df[0..C) (C <= 3) of four consecutive spheres out of the
+// second accumulator's q[4], as 16-byte stores (the arrays are 16-byte
+// aligned and i0 is a multiple of 4, so C floats per sphere are whole float4s).
+__device__ __forceinline__ void store_acc2_v4(const float4 (&q)[4], int i0, int C,
+                                              float* __restrict__ grad_opacity,
+                                              float* __restrict__ grad_features) {
+    if (grad_opacity)
+        *reinterpret_cast<float4*>(grad_opacity + i0) = make_float4(q[0].x, q[1].x, q[2].x, q[3].x);
+    if (grad_features) {
+        float v[12];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            v[3 * k] = q[k].y;
+            v[3 * k + 1] = q[k].z;
+            v[3 * k + 2] = q[k].w;
+        }
+        float4* o4 = reinterpret_cast<float4*>(grad_features + (size_t)C * i0);
+        if (C == 3) {
+            o4[0] = make_float4(v[0], v[1], v[2], v[3]);
+            o4[1] = make_float4(v[4], v[5], v[6], v[7]);
+            o4[2] = make_float4(v[8], v[9], v[10], v[11]);
+        } else if (C == 2) {
+            o4[0] = make_float4(q[0].y, q[0].z, q[1].y, q[1].z);
+            o4[1] = make_float4(q[2].y, q[2].z, q[3].y, q[3].z);
+        } else {
+            o4[0] = make_float4(q[0].y, q[1].y, q[2].y, q[3].y);
+        }
+    }
+}
+
+// The same for one sphere i, scaled by sph.
+__device__ __forceinline__ void store_acc2_one(float4 q, int i, int C, float sph,
+                                               float* __restrict__ grad_opacity,
+                                               float* __restrict__ grad_features) {
+    if (grad_opacity) grad_opacity[i] = q.x * sph;
+    if (grad_features) {
+        float* gf = grad_features + (size_t)i * C;
+        gf[0] = q.y * sph;
+        if (C > 1) gf[1] = q.z * sph;
+        if (C > 2) gf[2] = q.w * sph;
+    }
+}
+
 // One camera: four consecutive spheres per thread with 16-byte loads and
 // stores, so each thread has seven independent loads in flight.  With normalised gradients
 // (Pulsar Sec. B.2) a sphere's gradients are divided by the number of pixels
 // tracking it and its share of dL/dR, dL/dt is scaled by 1e-3 / A (A its
 // rendered disc's area in px^2, as for dL/dK in the backward).
+// mode bit 0: 16-byte accesses allowed (aligned arrays); bit 1: dL/do, dL/df
+// are in the second accumulator (C <= 3).
 __global__ void __launch_bounds__(kFinThreads)
 k_finalize_one_cam(Frames fs, Workspace w, const float* __restrict__ pos, float* __restrict__ grad_pos,
            float* __restrict__ grad_radius, float* __restrict__ grad_opacity,
-           float* __restrict__ grad_features, int vec_ok) {
+           float* __restrict__ grad_features, int mode) {
     pdl_begin();
     __shared__ float s_part[kFinThreads / 32][12];
     const Frame& f = fs.f[0];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int i0 = 4 * (blockIdx.x * blockDim.x + tid);
+    const bool vec_ok = (mode & 1) != 0, acc2 = (mode & 2) != 0;
+    const int C = f.channels;
     float acc[12];
 #pragma unroll
     for (int q = 0; q < 12; ++q) acc[q] = 0.0f;
     const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
     const bool norm = (f.flags & kParamNormalize) != 0;
     if (!norm && vec_ok && i0 + 3 < f.n) {
-        float4 g[4];
+        float4 g[4], q[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) g[k] = w.gacc[i0 + k];
+        if (acc2) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) q[k] = w.gacc2[i0 + k];
+        }
         const float4* p4 = reinterpret_cast<const float4*>(pos + 3 * i0);
         const float4 pa = p4[0], pb = p4[1], pc = p4[2];
         const float p[12] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w, pc.x, pc.y, pc.z, pc.w};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) w.gacc[i0 + k] = z4;
         float gp[12];
 #pragma unroll
         for (int k = 0; k < 4; ++k)
@@ -374,23 +434,25 @@ k_finalize_one_cam(Frames fs, Workspace w, const float* __restrict__ pos, float*
         }
         if (grad_radius)
             *reinterpret_cast<float4*>(grad_radius + i0) = make_float4(g[0].w, g[1].w, g[2].w, g[3].w);
+        if (acc2) store_acc2_v4(q, i0, C, grad_opacity, grad_features);
     } else {
         // ragged tail, unaligned arrays or normalised gradients
         for (int i = i0; i < min(i0 + 4, f.n); ++i) {
-            float4 g = w.gacc[i];
-            w.gacc[i] = z4;
+            const float4 g = w.gacc[i];
             float sph = 1.0f, cams = 1.0f;
             if (norm) {
                 const float cnt = w.hitcnt[i];
-                w.hitcnt[i] = 0.0f;
                 sph = cnt > 0.0f ? 1.0f / cnt : 1.0f;
                 const float4 geo = w.rec[i].geo;          // c.z in z, r_eff in w (0: culled)
                 const float rz = f.fmin * (f.ortho ? geo.w : geo.w / geo.z);
                 cams = rz > 0.0f ? 1e-3f / (kPi * rz * rz) : 0.0f;
-                if (grad_opacity) grad_opacity[i] *= sph;
-                if (grad_features)
-                    for (int c = 0; c < f.channels; ++c) grad_features[(size_t)i * f.channels + c] *= sph;
+                if (!acc2) {
+                    if (grad_opacity) grad_opacity[i] *= sph;
+                    if (grad_features)
+                        for (int c = 0; c < C; ++c) grad_features[(size_t)i * C + c] *= sph;
+                }
             }
+            if (acc2) store_acc2_one(w.gacc2[i], i, C, sph, grad_opacity, grad_features);
             float gp[3];
             const float4 gc = make_float4(g.x * cams, g.y * cams, g.z * cams, g.w);
             finalize_one(f, gc, pos[3 * i], pos[3 * i + 1], pos[3 * i + 2], gp, acc);
@@ -416,25 +478,27 @@ k_finalize_one_cam(Frames fs, Workspace w, const float* __restrict__ pos, float*
 }
 
 // A batch of cameras: four consecutive spheres per thread with 16-byte
-// loads and stores.  For every camera of the batch: dL/dp += R^T dL/dc, dL/dr += its part, and the sphere's share of
-// that camera's dL/dR = sum dL/dc p^T, dL/dt = sum dL/dc goes into per-block
+// loads and stores.  For every camera of the batch: dL/dp += R^T dL/dc, dL/dr
+// += its part, dL/do and dL/df += theirs, and the sphere's share of that
+// camera's dL/dR = sum dL/dc p^T, dL/dt = sum dL/dc goes into per-block
 // partials.  With normalised gradients (Pulsar Sec. B.2; one camera) a
 // sphere's gradients are divided by the number of pixels tracking it and its
 // share of dL/dR, dL/dt is scaled by 1e-3 / A (A its rendered disc's area in
-// px^2, as for dL/dK in the backward).
-__global__ void __launch_bounds__(kFinThreads, 4)
+// px^2, as for dL/dK in the backward).  mode as for k_finalize_one_cam.
+// (3 blocks per SM: at 4 the per-camera sums of the second accumulator spill)
+__global__ void __launch_bounds__(kFinThreads, 3)
 k_finalize_cams(Frames fs, Workspace w, const float* __restrict__ pos, float* __restrict__ grad_pos,
            float* __restrict__ grad_radius, float* __restrict__ grad_opacity,
-           float* __restrict__ grad_features, int vec_ok) {
+           float* __restrict__ grad_features, int mode) {
     pdl_begin();
     __shared__ float s_part[kFinThreads / 32][12];
     const Frame& f0 = fs.f[0];
-    const int n = f0.n, n_cams = f0.n_cams;
+    const int n = f0.n, n_cams = f0.n_cams, C = f0.channels;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int i0 = 4 * (blockIdx.x * blockDim.x + tid);
     const int cnt = i0 < n ? min(4, n - i0) : 0;
     const bool norm = (f0.flags & kParamNormalize) != 0;
-    const bool vec = vec_ok && cnt == 4;
+    const bool vec = (mode & 1) != 0 && cnt == 4, acc2 = (mode & 2) != 0;
     const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
     float p[12];
     if (vec) {
@@ -447,14 +511,12 @@ k_finalize_cams(Frames fs, Workspace w, const float* __restrict__ pos, float* __
 #pragma unroll
         for (int q = 0; q < 12; ++q) p[q] = q < 3 * cnt ? pos[3 * i0 + q] : 0.0f;
     }
+    float sph_last[4] = {1.0f, 1.0f, 1.0f, 1.0f};
     for (int cam = 0; cam < n_cams; ++cam) {
         const Frame& f = fs.f[cam];
         float4 g[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) g[k] = k < cnt ? w.gacc[f.rec_base + i0 + k] : z4;
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            if (k < cnt) w.gacc[f.rec_base + i0 + k] = z4;
         float acc[12], gp[12], gr[4];
 #pragma unroll
         for (int q = 0; q < 12; ++q) acc[q] = 0.0f;
@@ -464,15 +526,16 @@ k_finalize_cams(Frames fs, Workspace w, const float* __restrict__ pos, float* __
             if (norm && k < cnt) {
                 const int i = i0 + k;
                 const float c = w.hitcnt[f.rec_base + i];
-                w.hitcnt[f.rec_base + i] = 0.0f;
                 sph = c > 0.0f ? 1.0f / c : 1.0f;
                 const float4 geo = w.rec[f.rec_base + i].geo;   // c.z in z, r_eff in w (0: culled)
                 const float rz = f.fmin * (f.ortho ? geo.w : geo.w / geo.z);
                 cams = rz > 0.0f ? 1e-3f / (kPi * rz * rz) : 0.0f;
-                if (grad_opacity) grad_opacity[i] *= sph;
-                if (grad_features)
-                    for (int ch = 0; ch < f.channels; ++ch)
-                        grad_features[(size_t)i * f.channels + ch] *= sph;
+                if (!acc2) {
+                    if (grad_opacity) grad_opacity[i] *= sph;
+                    if (grad_features)
+                        for (int ch = 0; ch < C; ++ch) grad_features[(size_t)i * C + ch] *= sph;
+                }
+                sph_last[k] = sph;
             }
             const float4 gk = g[k];
             gp[3 * k + 0] = (f.R[0] * gk.x + f.R[3] * gk.y + f.R[6] * gk.z) * sph;
@@ -532,6 +595,18 @@ k_finalize_cams(Frames fs, Workspace w, const float* __restrict__ pos, float* __
             w.rtpart[((size_t)cam * 12 + tid) * gridDim.x + blockIdx.x] = make_float2(s.hi, s.lo);
         }
         __syncthreads();   // s_part is reused by the next camera
+    }
+    if (acc2) {   // dL/do, dL/df: one accumulator summed over the cameras
+        float4 q[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) q[k] = k < cnt ? w.gacc2[i0 + k] : z4;
+        if (vec && !norm) {
+            store_acc2_v4(q, i0, C, grad_opacity, grad_features);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (k < cnt) store_acc2_one(q[k], i0 + k, C, sph_last[k], grad_opacity, grad_features);
+        }
     }
 }
 
@@ -649,8 +724,20 @@ cudaError_t launch_backward(const Frames& fs, const Workspace& w, const float* p
     const int want_geom = (grad_pos || grad_radius || grad_cam) ? 1 : 0;
     const int feat_v4 = (f.channels % 4 == 0 && grad_features &&
                          (reinterpret_cast<uintptr_t>(grad_features) & 15u) == 0) ? 2 : 0;
-    const int mode = want_geom | feat_v4;
-    cudaError_t e;
+    // C <= 3: dL/do and dL/df in the second accumulator, written by the finalize
+    const bool acc2 = f.channels <= 3 && (grad_opacity || grad_features);
+    const int mode = want_geom | feat_v4 | (acc2 ? 4 : 0);
+    const bool norm = (f.flags & kParamNormalize) != 0;
+    // zero the accumulators the kernel reduces into: written here, their lines
+    // sit in L2 when the reductions arrive (zeroed a frame earlier they would
+    // be read back from DRAM)
+    const size_t nk = (size_t)f.n * f.n_cams;
+    cudaError_t e = cudaSuccess;
+    if (want_geom && nk) e = cudaMemsetAsync(w.gacc, 0, nk * sizeof(float4), stream);
+    if (e == cudaSuccess && acc2 && f.n)
+        e = cudaMemsetAsync(w.gacc2, 0, (size_t)f.n * sizeof(float4), stream);
+    if (e == cudaSuccess && norm && nk) e = cudaMemsetAsync(w.hitcnt, 0, nk * sizeof(float), stream);
+    if (e != cudaSuccess) return e;
     if (f.channels == 3)
         e = launch_bwd_c<3>(fs, w, features, image, grad_image, grad_opacity, grad_features, mode,
                             stream);
@@ -670,18 +757,20 @@ cudaError_t launch_backward(const Frames& fs, const Workspace& w, const float* p
         e = launch_bwd_c<kMaxChannels>(fs, w, features, image, grad_image, grad_opacity,
                                        grad_features, mode, stream);
     if (e != cudaSuccess) return e;
-    const bool norm = (f.flags & kParamNormalize) != 0;
-    if (want_geom || norm) {
+    if (want_geom || norm || acc2) {
         const int blocks = (f.n + 4 * kFinThreads - 1) / (4 * kFinThreads);
         // 16-byte accesses need 16-byte aligned arrays (true for torch allocations)
         const int vec_ok = ((reinterpret_cast<uintptr_t>(pos) | reinterpret_cast<uintptr_t>(grad_pos) |
-                             reinterpret_cast<uintptr_t>(grad_radius)) & 15u) == 0;
+                             reinterpret_cast<uintptr_t>(grad_radius) |
+                             reinterpret_cast<uintptr_t>(grad_opacity) |
+                             reinterpret_cast<uintptr_t>(grad_features)) & 15u) == 0;
+        const int fmode = (vec_ok ? 1 : 0) | (acc2 ? 2 : 0);
         if (blocks > 0 && f.n_cams == 1)
             e = launch_pdl(k_finalize_one_cam, dim3(blocks), dim3(kFinThreads), 0, stream, fs, w,
-                           pos, grad_pos, grad_radius, grad_opacity, grad_features, vec_ok);
+                           pos, grad_pos, grad_radius, grad_opacity, grad_features, fmode);
         else if (blocks > 0)
             e = launch_pdl(k_finalize_cams, dim3(blocks), dim3(kFinThreads), 0, stream, fs, w, pos,
-                           grad_pos, grad_radius, grad_opacity, grad_features, vec_ok);
+                           grad_pos, grad_radius, grad_opacity, grad_features, fmode);
         if (e == cudaSuccess && want_geom)
             e = launch_pdl(k_camera_reduce, dim3(f.n_cams), dim3(kCamThreads), 0, stream, fs, w,
                            blocks, grad_cam);

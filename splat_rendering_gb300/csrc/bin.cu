@@ -479,15 +479,20 @@ cudaError_t prepare_bin() {
 
 cudaError_t launch_bin(const Frames& fs, const Workspace& w, cudaStream_t stream) {
     const Frame& f = fs.f[0];
-    cudaError_t e = launch_pdl(k_tile_scan, dim3(1), dim3(kScanThreads), 0, stream, fs, w);
+    // both grids below loop over their work; they are sized by the SM count
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(k_tile_scan, dim3(1), dim3(kScanThreads), 0, stream, fs, w);
     if (e == cudaSuccess && f.n > 0) {
-        e = launch_pdl(k_emit, dim3(152 * 8), dim3(kEmitThreads), 0, stream, fs, w);
+        e = launch_pdl(k_emit, dim3(sms * 8), dim3(kEmitThreads), 0, stream, fs, w);
         if (e == cudaSuccess)
             e = launch_pdl(k_tile_sort,
                            dim3(((int)f.n_tiles_all + kTilesPerSortBlock - 1) / kTilesPerSortBlock),
                            dim3(kSortThreads), 0, stream, fs, w);
         if (e == cudaSuccess)
-            e = launch_pdl(k_tile_sort_long, dim3(152 * kLongBlocksPerSm), dim3(kLongThreads),
+            e = launch_pdl(k_tile_sort_long, dim3(sms * kLongBlocksPerSm), dim3(kLongThreads),
                            kLongSmem, stream, fs, w);
     }
     return e;

@@ -1,16 +1,16 @@
 // pulsar_render_noalloc: a forward render of a small frame that allocates no
 // memory at all.
 //
-// Some callers cannot call cudaMalloc: code running while a CUDA stream is
-// being captured into a graph (allocation is not a capturable operation),
-// plugins hosted by a framework that owns the whole device memory budget and
-// forbids other allocators, and fixed-footprint real-time renderers that must
-// not risk an out-of-memory failure or an implicit device synchronisation in
-// the middle of a frame.  For them this entry point runs the same projection,
-// binning and forward kernels as pulsar_project / pulsar_bin /
-// pulsar_forward, but every intermediate array lives in one file-scope
-// static device arena of fixed size (below), reserved when the library is
-// loaded and held by every GPU that loads it until the process exits.
+// Some callers cannot call cudaMalloc while they render: plugins hosted by a
+// framework that owns the whole device memory budget and forbids other
+// allocators, and fixed-footprint real-time renderers that must not risk an
+// out-of-memory failure, or the implicit device synchronisation that
+// cudaMalloc and cudaFree may bring, in the middle of a frame.  For them this
+// entry point runs the same projection, binning and forward kernels as
+// pulsar_project / pulsar_bin / pulsar_forward, but every intermediate array
+// lives in one file-scope static device arena of fixed size (below),
+// reserved when the library is loaded and held by every GPU that loads it
+// until the process exits.
 //
 // Limits (the arena's capacity): at most kMaxSpheres spheres, kMaxPairs
 // sphere-tile pairs, images up to kMaxSide x kMaxSide, n_track <= kMaxTrackNA,
@@ -25,8 +25,8 @@
 //
 // The first call on a device looks up the arena's device address with
 // cudaGetSymbolAddress (with that device current) and prepares the forward
-// and sort kernels; make that first call before capturing any stream.  The call
-// synchronises the stream at its end to read the frame's status.
+// and sort kernels; that first call should come before any stream capture.
+// Every call synchronises the stream at its end to read the frame's status.
 #include <cuda_runtime.h>
 
 #include <cstring>
@@ -115,6 +115,7 @@ extern "C" int pulsar_render_noalloc(const float* pos, const float* radius, cons
     Workspace w{};
     w.rec = reinterpret_cast<SphereRec*>(a + kOffRec);
     w.gacc = nullptr;   // forward only
+    w.gacc2 = nullptr;
     w.hitcnt = nullptr;
     w.tile_count = reinterpret_cast<uint32_t*>(a + kOffCount);
     w.tile_start = reinterpret_cast<uint32_t*>(a + kOffStart);

@@ -128,7 +128,8 @@ int pulsar_create_cams(pulsar_ctx_t* out, int device, int64_t max_spheres, int64
     const size_t N = (size_t)(max_spheres > 0 ? max_spheres : 1);
     const size_t B = (size_t)c->max_tiles, P = (size_t)c->max_pix;
     Workspace& w = c->ws;
-    bool ok = alloc(c, &w.rec, K * N) && alloc(c, &w.gacc, K * N) && alloc(c, &w.hitcnt, K * N) &&
+    bool ok = alloc(c, &w.rec, K * N) && alloc(c, &w.gacc, K * N) &&
+              alloc(c, &w.gacc2, N) && alloc(c, &w.hitcnt, K * N) &&
               alloc(c, &w.tile_count, K * B) && alloc(c, &w.tile_start, K * B + 1) &&
               alloc(c, &w.long_tiles, K * B) &&
               alloc(c, &w.staged, (size_t)max_pairs) &&
@@ -149,6 +150,7 @@ int pulsar_create_cams(pulsar_ctx_t* out, int device, int64_t max_spheres, int64
     // zero-between-frames invariants
     if (ok)
         ok = cudaMemset(w.gacc, 0, K * N * sizeof(float4)) == cudaSuccess &&
+             cudaMemset(w.gacc2, 0, N * sizeof(float4)) == cudaSuccess &&
              cudaMemset(w.hitcnt, 0, K * N * sizeof(float)) == cudaSuccess &&
              cudaMemset(w.tile_count, 0, K * B * sizeof(uint32_t)) == cudaSuccess &&
              cudaMemset(w.tile_start, 0, (K * B + 1) * sizeof(uint32_t)) == cudaSuccess &&
@@ -265,11 +267,16 @@ int pulsar_backward(pulsar_ctx_t c, const float* features, const float* bg, cons
     cudaStream_t s = as_stream(stream);
     const Frame& f = c->frames.f[0];
     const size_t n = (size_t)f.n;
-    if (grad_opacity && n && cudaMemsetAsync(grad_opacity, 0, n * 4, s) != cudaSuccess)
-        return PULSAR_ERR_CUDA;
-    if (grad_features && n &&
-        cudaMemsetAsync(grad_features, 0, n * (size_t)f.channels * 4, s) != cudaSuccess)
-        return PULSAR_ERR_CUDA;
+    // with C <= 3 the opacity and feature gradients are accumulated in the
+    // workspace and written out by the finalize; otherwise straight into the
+    // caller's arrays, which start at zero
+    if (f.channels > 3) {
+        if (grad_opacity && n && cudaMemsetAsync(grad_opacity, 0, n * 4, s) != cudaSuccess)
+            return PULSAR_ERR_CUDA;
+        if (grad_features && n &&
+            cudaMemsetAsync(grad_features, 0, n * (size_t)f.channels * 4, s) != cudaSuccess)
+            return PULSAR_ERR_CUDA;
+    }
     cudaError_t e = launch_backward(c->frames, c->ws, c->pos, features, image, grad_image, grad_pos,
                                     grad_radius, grad_opacity, grad_features, grad_cam, s);
     return cuda_err(e);

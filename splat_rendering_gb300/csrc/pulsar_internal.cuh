@@ -352,9 +352,11 @@ struct __align__(16) SphereRec {
 struct Workspace {
     SphereRec* rec;    // [maxN]
     // per camera of a batch: [maxCams][...] blocks, camera after camera
-    float4* gacc;      // [maxN] dL/dc.xyz, dL/dr accumulators (zero between frames)
+    float4* gacc;      // [maxN] dL/dc.xyz, dL/dr accumulators (zeroed by each backward)
+    float4* gacc2;     // [maxN] dL/do, dL/df[0..2] accumulators for C <= 3, one for all
+                       // cameras (zeroed by each backward; the finalize writes them out)
     float* hitcnt;     // [maxN] pixels tracking each sphere, for normalised gradients
-                       // (zero between frames)
+                       // (zeroed by each backward)
     uint32_t* tile_count;   // [maxB] (zero between frames)
     uint32_t* tile_start;   // [maxB+1]
     uint32_t* long_tiles;   // [maxB] tiles with lists longer than one warp sorts, in tile order

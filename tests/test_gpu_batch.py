@@ -75,13 +75,17 @@ def check_batch(oracle_lib, sc, cams, grads, window=None, p=None):
         assert np.array_equal(g["tile_offsets"][k * B:(k + 1) * B + 1] - lo, offs), what
         assert np.array_equal(g["tile_ids"][lo:hi], ids.astype(np.int64)), what
         gh.compare_frame(gk, o, what, window=window, grads=False)
+        sl = (slice(None), slice(None)) if window is None else \
+            (slice(window[1], window[3]), slice(window[0], window[2]))
+        dF = gh.image_err(gk["image"][sl], o["image"])
+        dF_all = max(dF_all, dF) if k else dF
         gh.assert_close(g["grad_cam"][k], o["grad_cam"], gh.GRAD_RTOL, gh.GRAD_ATOL,
-                        f"{what} grad_cam", o["abs_grad_cam"], o["sens_grad_cam"])
+                        f"{what} grad_cam", o["abs_grad_cam"], o["sens_grad_cam"], dF)
     for key in ("grad_pos", "grad_radius", "grad_opacity", "grad_features"):
         ref = sum(x[0][key] for x in per)
         a = sum(x[0]["abs_" + key] for x in per)
         s = sum(x[0]["sens_" + key] for x in per)
-        gh.assert_close(g[key], ref, gh.GRAD_RTOL, gh.GRAD_ATOL, f"batch {key}", a, s)
+        gh.assert_close(g[key], ref, gh.GRAD_RTOL, gh.GRAD_ATOL, f"batch {key}", a, s, dF_all)
     return g
 
 

@@ -240,13 +240,15 @@ def test_partial_gradient_requests(oracle_lib):
     o, _, _, _ = _oracle_all(oracle_lib, sc)
     g = gh.run_gpu(sc, want=("opacity",))
     assert set(k for k in g if k.startswith("grad_")) == {"grad_opacity"}
+    dF = gh.image_err(g["image"], o["image"])
     gh.assert_close(g["grad_opacity"], o["grad_opacity"], gh.GRAD_RTOL, gh.GRAD_ATOL, "opacity",
-                    o["abs_grad_opacity"], o["sens_grad_opacity"])
+                    o["abs_grad_opacity"], o["sens_grad_opacity"], dF)
     g = gh.run_gpu(sc, want=("cam", "features"))
+    dF = gh.image_err(g["image"], o["image"])
     gh.assert_close(g["grad_cam"], o["grad_cam"], gh.GRAD_RTOL, gh.GRAD_ATOL, "cam",
-                    o["abs_grad_cam"], o["sens_grad_cam"])
+                    o["abs_grad_cam"], o["sens_grad_cam"], dF)
     gh.assert_close(g["grad_features"], o["grad_features"], gh.GRAD_RTOL, gh.GRAD_ATOL, "feat",
-                    o["abs_grad_features"], o["sens_grad_features"])
+                    o["abs_grad_features"], o["sens_grad_features"], dF)
 
 
 def test_repeat_frames_and_determinism(oracle_lib):
@@ -289,7 +291,8 @@ def test_unaligned_gradient_arrays(oracle_lib):
     grad = rbuf[1:]
     pl.backward(r.ctx, feat, bg, img, t(sc.grad_images[0]), grad_pos=gpos, grad_radius=grad)
     assert r.status()[0] == 0
+    dF = gh.image_err(img.cpu().numpy(), o["image"])
     gh.assert_close(gpos.cpu().numpy(), o["grad_pos"], gh.GRAD_RTOL, gh.GRAD_ATOL, "pos",
-                    o["abs_grad_pos"], o["sens_grad_pos"])
+                    o["abs_grad_pos"], o["sens_grad_pos"], dF)
     gh.assert_close(grad.cpu().numpy(), o["grad_radius"], gh.GRAD_RTOL, gh.GRAD_ATOL, "radius",
-                    o["abs_grad_radius"], o["sens_grad_radius"])
+                    o["abs_grad_radius"], o["sens_grad_radius"], dF)

@@ -1,12 +1,15 @@
 """The allocation-free render entry point (pulsar_render_noalloc) against the
-context-based one (pulsar_project / pulsar_bin / pulsar_forward).
+context-based one (pulsar_project / pulsar_bin / pulsar_forward) and the
+oracle.
 
-Some callers cannot allocate device memory while they render -- a stream being
-captured into a graph, a plugin whose host owns the device memory budget, a
-fixed-footprint real-time renderer -- so the library offers one entry point
-whose scratch arrays live in a static device arena.  Its image must equal the
-regular path's within the forward tolerance, call after call (the arena keeps
-the previous call's contents).  This file is collected last on purpose.
+Some callers cannot allocate device memory while they render -- a plugin
+whose host framework owns the device memory budget, a fixed-footprint
+real-time renderer that must not risk an allocation failure mid-frame -- so
+the library offers one entry point whose scratch arrays live in a static
+device arena.  Its image must equal the regular path's within the forward
+tolerance, call after call (the arena keeps the previous call's contents),
+and a frame that overflows the arena must be refused without disturbing the
+next one.  This file is collected last on purpose.
 """
 from __future__ import annotations
 
@@ -17,6 +20,8 @@ import gpu_helpers as gh
 from splat_rendering_gb300 import scenes
 
 pytestmark = pytest.mark.gpu
+
+ARENA_PAIRS = 65536   # sphere-tile pairs the arena holds
 
 
 def _noalloc_image(sc):
@@ -44,6 +49,38 @@ def test_noalloc_render_matches_context_path_on_consecutive_calls():
         assert ref["code"] == 0
         img = _noalloc_image(sc)
         gh.assert_close(img, ref["image"], gh.FWD_RTOL, gh.FWD_ATOL, f"noalloc {sc.name}")
+
+
+def test_noalloc_render_matches_oracle(oracle_lib):
+    sc = scenes.random_scene(75, 2500, 160, 130, rot_deg=6, rrange=(0.01, 0.25))
+    img = _noalloc_image(sc)
+    o = oracle_lib.render_scene(sc, with_grads=False)
+    gh.assert_close(img, o["image"], gh.FWD_RTOL, gh.FWD_ATOL, "noalloc vs oracle")
+
+
+def test_noalloc_capacity_overflow_then_recovers(oracle_lib):
+    """A frame with more sphere-tile pairs than the arena holds is refused with
+    PULSAR_ERR_CAPACITY and leaves the image untouched; the next call, on the
+    arena the overflowing one left behind, renders correctly."""
+    from splat_rendering_gb300 import pulsar as pl
+    import torch
+    big = scenes.random_scene(76, 2000, 256, 256, rrange=(0.5, 1.5))   # spheres of many tiles
+    pairs = oracle_lib.tile_lists(big.pos, big.radius, big.opacity, big.cameras[0],
+                                  big.params)[1].size
+    assert pairs > ARENA_PAIRS
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()  # noqa: E731
+    cam = big.cameras[0]
+    img = torch.full((cam.height, cam.width, 3), float("nan"), device="cuda")
+    with pytest.raises(pl.PulsarError) as e:
+        pl.render_noalloc(t(big.pos), t(big.radius), t(big.opacity), t(big.features), big.n,
+                          pl.camera(cam), pl.params(big.params), t(big.bg), img)
+    assert e.value.code == pl.ERR_CAPACITY
+    assert torch.isnan(img).all(), "an overflowing frame must not write the image"
+    small = scenes.random_scene(77, 1200, 256, 200, rot_deg=4, rrange=(0.01, 0.2))
+    ref = gh.run_gpu(small, want=False, debug=False)
+    assert ref["code"] == 0
+    gh.assert_close(_noalloc_image(small), ref["image"], gh.FWD_RTOL, gh.FWD_ATOL,
+                    "noalloc after an overflow")
 
 
 def test_noalloc_rejects_sizes_beyond_its_arena():
