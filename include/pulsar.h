@@ -51,6 +51,8 @@ extern "C" {
 #define PULSAR_ERR_CAPACITY -3  /* more sphere-tile pairs than max_pairs */
 #define PULSAR_ERR_STATE    -4  /* call out of order (e.g. forward before bin) */
 #define PULSAR_ERR_NOMEM    -5  /* workspace allocation failed */
+#define PULSAR_ERR_INTERNAL -7  /* debug build only: a device index check failed (the access
+                                  was skipped; the frame is invalid) */
 #define PULSAR_ERR_TIMEOUT  -6  /* a bounded wait on the tensor cores gave up: the frame is
                                   invalid and, since work may still have been in flight,
                                   the context should be destroyed and recreated */
@@ -193,7 +195,8 @@ int pulsar_backward(pulsar_ctx_t ctx, const float* features, const float* bg,
                     float* grad_cam, void* stream);
 
 /* Synchronise `stream`, then report the latched device error of the last
- * frame (PULSAR_OK, PULSAR_ERR_CAPACITY) and clear it.  n_pairs (M) and
+ * frame (PULSAR_OK, PULSAR_ERR_CAPACITY, PULSAR_ERR_TIMEOUT; the debug build
+ * also PULSAR_ERR_INTERNAL) and clear it.  n_pairs (M) and
  * n_hits (hit pairs composited by the last forward) may be NULL. */
 int pulsar_status(pulsar_ctx_t ctx, void* stream, int64_t* n_pairs, int64_t* n_hits);
 

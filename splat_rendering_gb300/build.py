@@ -1,10 +1,14 @@
 """Build the CUDA library libpulsar.so in-tree with nvcc for sm_103a.
 
-    python -m splat_rendering_gb300.build [--verbose] [--ptxas-info]
+    python -m splat_rendering_gb300.build [--verbose] [--ptxas-info] [--debug] [--nvtx]
 
 Each translation unit under csrc/ is compiled in parallel, then linked into
 splat_rendering_gb300/libpulsar.so (static CUDA runtime).  Nothing here needs
-a GPU.
+a GPU.  Two optional builds go to their own files next to it:
+  --debug  libpulsar_debug.so: device index checks that latch an error
+           (PULSAR_ERR_INTERNAL from pulsar_status) and skip the access;
+  --nvtx   NVTX ranges around every C entry point (header-only NVTX3);
+both together: libpulsar_debug_nvtx.so.
 """
 from __future__ import annotations
 
@@ -31,12 +35,21 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _flags(ptxas_info: bool):
+def _flags(ptxas_info: bool, debug: bool = False, nvtx: bool = False):
     f = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                 "-Xcompiler", "-ffp-contract=off", f"-I{INCLUDE}", "--expt-relaxed-constexpr"]
     if ptxas_info:
         f += ["-Xptxas", "-v"]
+    if debug:
+        f += ["-DPULSAR_DEBUG"]
+    if nvtx:
+        f += ["-DPULSAR_NVTX"]
     return f
+
+
+def lib_path(debug: bool = False, nvtx: bool = False) -> str:
+    suffix = ("_debug" if debug else "") + ("_nvtx" if nvtx else "")
+    return os.path.join(HERE, f"libpulsar{suffix}.so")
 
 
 def _stale(lib: str, deps) -> bool:
@@ -46,17 +59,20 @@ def _stale(lib: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          debug: bool = False, nvtx: bool = False) -> str:
+    lib = lib_path(debug, nvtx)
     deps = [os.path.join(CSRC, s) for s in SOURCES] + [
         os.path.join(CSRC, "pulsar_internal.cuh"), os.path.join(INCLUDE, "pulsar.h"), __file__]
-    if not force and not ptxas_info and not _stale(LIB, deps):
-        return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
+    if not force and not ptxas_info and not _stale(lib, deps):
+        return lib
+    out_dir = os.path.join(OUT_DIR, os.path.basename(lib)[:-3]) if (debug or nvtx) else OUT_DIR
+    os.makedirs(out_dir, exist_ok=True)
     cc = nvcc()
-    flags = _flags(ptxas_info)
+    flags = _flags(ptxas_info, debug, nvtx)
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(out_dir, os.path.splitext(src)[0] + ".o")
         cmd = [cc, "-c", os.path.join(CSRC, src), "-o", obj] + flags
         r = subprocess.run(cmd, capture_output=True, text=True)
         return src, obj, cmd, r
@@ -71,15 +87,15 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
             if r.returncode != 0:
                 raise RuntimeError(f"nvcc failed on {src}:\n{r.stderr}")
             objs.append(obj)
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [cc, "-shared", "-o", tmp] + objs + ARCH + ["-Xcompiler", "-fPIC"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    build(force=True, verbose="--verbose" in sys.argv, ptxas_info="--ptxas-info" in sys.argv)
-    print(LIB)
+    print(build(force=True, verbose="--verbose" in sys.argv, ptxas_info="--ptxas-info" in sys.argv,
+                debug="--debug" in sys.argv, nvtx="--nvtx" in sys.argv))

@@ -95,7 +95,8 @@ k_backward(Frames fs, Workspace w, const float* __restrict__ features,
     // is started before the per-pixel loads so that the two latencies overlap
     auto stage = [&](uint32_t b0, int nb) {
         for (int t = tid; t < nb; t += kBwdThreads) {
-            const int id = (int)w.tile_ids[b0 + t];
+            int id = (int)w.tile_ids[b0 + t];
+            if (!PULSAR_CHECK(w.state, (uint32_t)id < (uint32_t)f.n)) id = 0;
             const float4* src = reinterpret_cast<const float4*>(rec + id);
             cp_async16(&s_uv[t], src + 0);
             cp_async16(&s_ex[t], src + 1);

@@ -133,6 +133,7 @@ __global__ void __launch_bounds__(kEmitThreads) k_emit(Frames fs, Workspace w) {
     if (m > f.max_pairs) return;   // overflowed frame: the capacity error is latched
     for (uint32_t p = blockIdx.x * blockDim.x + threadIdx.x; p < m; p += gridDim.x * blockDim.x) {
         const uint4 s = w.staged[p];
+        if (!PULSAR_CHECK(w.state, s.x < f.n_tiles_all)) continue;
         const uint32_t at = w.tile_start[s.x] + s.y;
         if (at < m) w.pairs[at] = ((unsigned long long)s.z << 32) | s.w;
     }

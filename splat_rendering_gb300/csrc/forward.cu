@@ -34,6 +34,22 @@ namespace {
 constexpr int kFwdThreads = kTilePix;
 constexpr int kWarps = kFwdThreads / 32;
 constexpr int kTestCap = 256;     // tests per chunk: entries of a warp's d buffer
+// The fp32 decision test of the specification, term by term: pixel centre
+// (px, py) with ray slopes (a, b) and qq = 1 + a^2 + b^2 (formed by the caller
+// as fp32 ops in that order) against a candidate's projected centre uv and
+// s2 = (r_eff / c.z)^2.
+__device__ __forceinline__ bool hit_test32(const float4& uv, float s2, float px, float py, float a,
+                                           float b, float qq, const Frame& f) {
+    const float U = __fmul_rn(__fsub_rn(__fsub_rn(px, uv.x), uv.y), f.ifx);
+    const float V = __fmul_rn(__fsub_rn(__fsub_rn(py, uv.z), uv.w), f.ify);
+    const float X = __fmaf_rn(U, b, -__fmul_rn(V, a));
+    const float Q = __fmaf_rn(U, U, __fmaf_rn(V, V, __fmul_rn(X, X)));
+    return Q < __fmul_rn(s2, qq);
+}
+
+__device__ __forceinline__ float qq32(float a, float b) {
+    return __fadd_rn(__fadd_rn(1.0f, __fmul_rn(a, a)), __fmul_rn(b, b));
+}
 
 // Shared-memory layout of one block (dynamic, 16-byte aligned pieces).
 template <int CMAX>
@@ -138,6 +154,7 @@ k_forward(Frames fs, Workspace w, const float* __restrict__ features, const floa
     // 16-byte pieces and the features by cp.async, the id by a plain store
     auto stage = [&](int buf, int id) {
         unsigned char* B = smem + buf * L::buf_bytes;
+        if (!PULSAR_CHECK(w.state, (uint32_t)id < (uint32_t)f.n)) id = 0;
         const float4* src = reinterpret_cast<const float4*>(rec + id);
         cp_async16(B + L::rec_uv + tid * 16, src + 0);
         cp_async16(B + L::rec_ex + tid * 16, src + 1);
@@ -167,6 +184,42 @@ k_forward(Frames fs, Workspace w, const float* __restrict__ features, const floa
     int nh = 0;
     bool done = !inside;
     const int lx = lane & 15, ly = lane >> 4;     // the lane's pixel within the warp's rows
+    const bool gaussian = (f.flags & kParamGaussian) != 0;
+
+    // blend hit j of the current batch (record in shared memory, distance
+    // factor d) into the pixel's max-shifted running sums; the first n_track
+    // hits go to the backward-information buffer
+    auto blend = [&](const unsigned char* B, int j, float d, uint32_t list_pos) {
+        const float4 ex = reinterpret_cast<const float4*>(B + L::rec_ex)[j];
+        if (ex.x > mg || (ex.x == mg && ex.y > mgl)) {
+            const float sc = ex2_approx(__fsub_rn(mg, ex.x) + __fsub_rn(mgl, ex.y));
+            wsum *= sc;
+#pragma unroll
+            for (int cc = 0; cc < CMAX; ++cc) acc[cc] *= sc;
+            mg = ex.x;
+            mgl = ex.y;
+        }
+        const float wt = ex.z * d * ex2_approx(__fsub_rn(ex.x, mg) + __fsub_rn(ex.y, mgl));
+        wsum += wt;
+        if (L::kStageFeat) {
+            const float* s_feat = reinterpret_cast<const float*>(B + L::rec_feat);
+#pragma unroll
+            for (int cc = 0; cc < CMAX; ++cc)
+                if (cc < C) acc[cc] += wt * s_feat[j * FS + cc];
+        } else {
+            const float* fp = features + (size_t)reinterpret_cast<const int*>(B + L::rec_id)[j] * C;
+#pragma unroll
+            for (int cc = 0; cc < CMAX; ++cc)
+                if (cc < C) acc[cc] += wt * __ldg(fp + cc);
+        }
+        if (nh < f.n_track) {
+            // backward-information buffer: the hit's position in the tile list
+            // and its distance factor
+            w.ids[(uint32_t)nh * P + p] = (int)list_pos;
+            w.dtr[(uint32_t)nh * P + p] = d;
+        }
+        ++nh;
+    };
 
     int buf = 0;
     for (uint32_t b0 = start; b0 < end; b0 += NB, buf ^= 1) {
@@ -186,8 +239,6 @@ k_forward(Frames fs, Workspace w, const float* __restrict__ features, const floa
         const float4* s_ex = reinterpret_cast<const float4*>(B + L::rec_ex);
         const float4* s_geo = reinterpret_cast<const float4*>(B + L::rec_geo);
         const uint4* s_rk = reinterpret_cast<const uint4*>(B + L::rec_rk);
-        const float* s_feat = reinterpret_cast<const float*>(B + L::rec_feat);
-        const int* s_id = reinterpret_cast<const int*>(B + L::rec_id);
         const int nb = (int)min((uint32_t)NB, end - b0);
 
         // compact this warp's candidates, in list order
@@ -259,17 +310,11 @@ k_forward(Frames fs, Workspace w, const float* __restrict__ features, const floa
                         const int xx = o_xa + q - second * o_wd;
                         const int yy = o_ya + second;
                         const float4 uv = s_uv[j];
-                        // the decision test of the specification, term by term
                         const float a = s_a[xx - tx0];
                         const float b = s_b[yy - ty0];
                         const float px = __fadd_rn(__int2float_rn(xx), 0.5f);
                         const float py = __fadd_rn(__int2float_rn(yy), 0.5f);
-                        const float U = __fmul_rn(__fsub_rn(__fsub_rn(px, uv.x), uv.y), f.ifx);
-                        const float V = __fmul_rn(__fsub_rn(__fsub_rn(py, uv.z), uv.w), f.ify);
-                        const float X = __fmaf_rn(U, b, -__fmul_rn(V, a));
-                        const float Q = __fmaf_rn(U, U, __fmaf_rn(V, V, __fmul_rn(X, X)));
-                        const float qq = __fadd_rn(__fadd_rn(1.0f, __fmul_rn(a, a)), __fmul_rn(b, b));
-                        if (Q < __fmul_rn(__uint_as_float(s_rk[j].z), qq)) {
+                        if (hit_test32(uv, __uint_as_float(s_rk[j].z), px, py, a, b, qq32(a, b), f)) {
                             const int pl = (yy - ty0) * kTile + (xx - tx0);   // pixel in tile
                             const float2 apv = s_ap[xx - tx0];
                             const float2 bpv = s_bp[yy - ty0];
@@ -281,7 +326,7 @@ k_forward(Frames fs, Workspace w, const float* __restrict__ features, const floa
                             pq.qq = {qqv.x, qqv.y};
                             pq.iqq = s_iqq[pl];
                             s_dbuf[warp][t] = distance_factor(uv, geo.x, geo.y, px, py, pq, f,
-                                                              (f.flags & kParamGaussian) != 0);
+                                                              gaussian);
                             atomicOr(&s_hmask[warp][(yy - row0) * kTile + (xx - tx0)], 1u << own);
                         }
                     }
@@ -295,36 +340,8 @@ k_forward(Frames fs, Workspace w, const float* __restrict__ features, const floa
                     const uint32_t dc = s_desc[warp][c];
                     const int ti = (int)(dc & 511u) + (ly - (int)((dc >> 13) & 1u)) * (int)(dc >> 14) +
                                    (lx - (int)((dc >> 9) & 15u));
-                    const float d = s_dbuf[warp][ti];
                     const int j = s_list[warp][k0 + c];
-                    const float4 ex = s_ex[j];
-                    if (ex.x > mg || (ex.x == mg && ex.y > mgl)) {
-                        const float sc = ex2_approx(__fsub_rn(mg, ex.x) + __fsub_rn(mgl, ex.y));
-                        wsum *= sc;
-#pragma unroll
-                        for (int cc = 0; cc < CMAX; ++cc) acc[cc] *= sc;
-                        mg = ex.x;
-                        mgl = ex.y;
-                    }
-                    const float wt = ex.z * d * ex2_approx(__fsub_rn(ex.x, mg) + __fsub_rn(ex.y, mgl));
-                    wsum += wt;
-                    if (L::kStageFeat) {
-#pragma unroll
-                        for (int cc = 0; cc < CMAX; ++cc)
-                            if (cc < C) acc[cc] += wt * s_feat[j * FS + cc];
-                    } else {
-                        const float* fp = features + (size_t)s_id[j] * C;
-#pragma unroll
-                        for (int cc = 0; cc < CMAX; ++cc)
-                            if (cc < C) acc[cc] += wt * __ldg(fp + cc);
-                    }
-                    if (nh < f.n_track) {
-                        // backward-information buffer: the hit's position in the tile
-                        // list and its distance factor
-                        w.ids[(uint32_t)nh * P + p] = (int)(b0 - start) + j;
-                        w.dtr[(uint32_t)nh * P + p] = d;
-                    }
-                    ++nh;
+                    blend(B, j, s_dbuf[warp][ti], (b0 - start) + (uint32_t)j);
                 }
                 __syncwarp();   // the chunk's descriptors, masks and d buffer are free
                 k0 += nc;

@@ -145,6 +145,7 @@ k_project(Frames fs, Workspace w, const float* __restrict__ pos, const float* __
                 const int k = j - (own_incl - own_cnt);
                 const int tile = (int)f.tile_base + (own_ty0 + k / own_ntx) * f.tiles_x + own_tx0 +
                                  k % own_ntx;
+                if (!PULSAR_CHECK(w.state, (uint32_t)tile < f.n_tiles_all)) continue;
                 const uint32_t slot = atomicAdd(&w.tile_count[tile], 1u);
                 const uint32_t at = base + (uint32_t)j;
                 if (at < f.max_pairs)

@@ -12,6 +12,22 @@
 #include "../../include/pulsar.h"
 #include "pulsar_internal.cuh"
 
+// NVTX ranges around the entry points (build with -DPULSAR_NVTX: header-only
+// NVTX3, no link dependency, no cost when no tool is attached); compiled out
+// by default.
+#ifdef PULSAR_NVTX
+#include <nvtx3/nvToolsExt.h>
+namespace {
+struct NvtxScope {
+    explicit NvtxScope(const char* name) { nvtxRangePushA(name); }
+    ~NvtxScope() { nvtxRangePop(); }
+};
+}  // namespace
+#define PULSAR_TRACE(name) NvtxScope pulsar_trace_scope_(name)
+#else
+#define PULSAR_TRACE(name) ((void)0)
+#endif
+
 using namespace pulsar;
 
 struct pulsar_ctx {
@@ -83,6 +99,7 @@ const char* pulsar_strerror(int code) {
         case PULSAR_ERR_STATE: return "call out of order";
         case PULSAR_ERR_NOMEM: return "workspace allocation failed";
         case PULSAR_ERR_TIMEOUT: return "a bounded wait on the tensor cores gave up";
+        case PULSAR_ERR_INTERNAL: return "a device index check failed (debug build)";
         default: return "unknown error";
     }
 }
@@ -97,6 +114,7 @@ int pulsar_create(pulsar_ctx_t* out, int device, int64_t max_spheres, int64_t ma
 int pulsar_create_cams(pulsar_ctx_t* out, int device, int64_t max_spheres, int64_t max_pairs,
                        int32_t max_width, int32_t max_height, int32_t max_channels,
                        int32_t max_track, int32_t max_cams) {
+    PULSAR_TRACE("pulsar_create_cams");
     if (!out) return PULSAR_ERR_ARG;
     *out = nullptr;
     if (max_spheres < 0 || max_spheres > 0x7fffffffLL || max_pairs < 1 ||
@@ -167,6 +185,7 @@ int pulsar_create_cams(pulsar_ctx_t* out, int device, int64_t max_spheres, int64
 }
 
 int pulsar_destroy(pulsar_ctx_t c) {
+    PULSAR_TRACE("pulsar_destroy");
     if (!c) return PULSAR_ERR_ARG;
     DeviceGuard guard(c->device);
     cudaDeviceSynchronize();
@@ -184,6 +203,7 @@ int pulsar_project(pulsar_ctx_t c, const float* pos, const float* radius, const 
 int pulsar_project_cams(pulsar_ctx_t c, const float* pos, const float* radius,
                         const float* opacity, int64_t n, const pulsar_camera_t* cams,
                         int32_t n_cams, const pulsar_params_t* prm, void* stream) {
+    PULSAR_TRACE("pulsar_project_cams");
     if (!c || !cams || !prm || n < 0 || n > c->max_n || n_cams < 1 || n_cams > c->max_cams)
         return PULSAR_ERR_ARG;
     if (n > 0 && (!pos || !radius || !opacity)) return PULSAR_ERR_ARG;
@@ -231,6 +251,7 @@ int pulsar_project_cams(pulsar_ctx_t c, const float* pos, const float* radius,
 }
 
 int pulsar_bin(pulsar_ctx_t c, void* stream) {
+    PULSAR_TRACE("pulsar_bin");
     if (!c) return PULSAR_ERR_ARG;
     if (c->stage < 1) return PULSAR_ERR_STATE;
     if (c->stage >= 2) return PULSAR_ERR_STATE;   // counts were consumed by the first bin
@@ -244,6 +265,7 @@ int pulsar_bin(pulsar_ctx_t c, void* stream) {
 
 int pulsar_forward(pulsar_ctx_t c, const float* features, const float* bg, float* image,
                    void* stream) {
+    PULSAR_TRACE("pulsar_forward");
     if (!c || !bg || !image) return PULSAR_ERR_ARG;
     if (c->frames.f[0].n > 0 && !features) return PULSAR_ERR_ARG;
     if (c->stage < 2) return PULSAR_ERR_STATE;
@@ -257,6 +279,7 @@ int pulsar_forward(pulsar_ctx_t c, const float* features, const float* bg, float
 int pulsar_backward(pulsar_ctx_t c, const float* features, const float* bg, const float* image,
                     const float* grad_image, float* grad_pos, float* grad_radius,
                     float* grad_opacity, float* grad_features, float* grad_cam, void* stream) {
+    PULSAR_TRACE("pulsar_backward");
     (void)bg;   // the background enters through the forward image only
     if (!c) return PULSAR_ERR_ARG;
     if (c->stage < 3) return PULSAR_ERR_STATE;
@@ -284,6 +307,7 @@ int pulsar_backward(pulsar_ctx_t c, const float* features, const float* bg, cons
 
 int pulsar_shade_forward(pulsar_ctx_t c, const float* features, const float* params, float* rgb,
                          void* stream) {
+    PULSAR_TRACE("pulsar_shade_forward");
     if (!c || !features || !params || !rgb) return PULSAR_ERR_ARG;
     if ((reinterpret_cast<uintptr_t>(features) & 15u) != 0) return PULSAR_ERR_ARG;
     if (c->stage < 1) return PULSAR_ERR_STATE;
@@ -296,6 +320,7 @@ int pulsar_shade_forward(pulsar_ctx_t c, const float* features, const float* par
 int pulsar_shade_backward(pulsar_ctx_t c, const float* features, const float* params,
                           const float* grad_rgb, float* grad_features, float* grad_params,
                           void* stream) {
+    PULSAR_TRACE("pulsar_shade_backward");
     if (!c || !features || !params || !grad_rgb || !grad_params) return PULSAR_ERR_ARG;
     if ((reinterpret_cast<uintptr_t>(features) & 15u) != 0 ||
         (reinterpret_cast<uintptr_t>(grad_features) & 15u) != 0)
@@ -309,6 +334,7 @@ int pulsar_shade_backward(pulsar_ctx_t c, const float* features, const float* pa
 }
 
 int pulsar_status(pulsar_ctx_t c, void* stream, int64_t* n_pairs, int64_t* n_hits) {
+    PULSAR_TRACE("pulsar_status");
     if (!c) return PULSAR_ERR_ARG;
     DeviceGuard guard(c->device);
     cudaStream_t s = as_stream(stream);
@@ -328,11 +354,13 @@ int pulsar_status(pulsar_ctx_t c, void* stream, int64_t* n_pairs, int64_t* n_hit
         cudaMemcpy(&c->ws.state->error, &zero, sizeof(zero), cudaMemcpyHostToDevice);
         if (h.error & kErrCapacity) return PULSAR_ERR_CAPACITY;
         if (h.error & kErrTimeout) return PULSAR_ERR_TIMEOUT;
+        if (h.error & kErrBounds) return PULSAR_ERR_INTERNAL;
     }
     return PULSAR_OK;
 }
 
 int pulsar_debug_inject(pulsar_ctx_t c, int what, void* stream) {
+    PULSAR_TRACE("pulsar_debug_inject");
     if (!c || (what & ~(int)kInjectShadeTimeout) != 0) return PULSAR_ERR_ARG;
     DeviceGuard guard(c->device);
     const uint32_t v = (uint32_t)what;
@@ -341,6 +369,7 @@ int pulsar_debug_inject(pulsar_ctx_t c, int what, void* stream) {
 }
 
 int64_t pulsar_debug_copy(pulsar_ctx_t c, int what, void* dst, int64_t bytes, void* stream) {
+    PULSAR_TRACE("pulsar_debug_copy");
     if (!c || bytes < 0) return PULSAR_ERR_ARG;
     DeviceGuard guard(c->device);
     cudaStream_t s = as_stream(stream);

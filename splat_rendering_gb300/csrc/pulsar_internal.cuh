@@ -29,7 +29,19 @@ constexpr float kPi = 3.14159265358979f;
 // Device error bits (latched in DevState::error).
 constexpr uint32_t kErrCapacity = 1u;
 constexpr uint32_t kErrTimeout = 2u;    // a bounded wait on the tensor cores gave up
+constexpr uint32_t kErrBounds = 4u;     // debug build: a device index check failed
 constexpr uint32_t kInjectShadeTimeout = 1u;   // shading kernels issue no tensor-core work
+
+// Index checks of the debug build (compiled with -DPULSAR_DEBUG): a failed
+// check latches kErrBounds in the device state (pulsar_status then returns
+// PULSAR_ERR_INTERNAL) and evaluates to false, so the guarded access is
+// skipped; no trap.  The release build compiles them to `true`.
+#ifdef PULSAR_DEBUG
+#define PULSAR_CHECK(state, cond) \
+    ((cond) ? true : (atomicOr(&(state)->error, ::pulsar::kErrBounds), false))
+#else
+#define PULSAR_CHECK(state, cond) true
+#endif
 
 // Per-camera constants of a frame (all cameras of a batch share the image
 // size, the parameters and the spheres).
@@ -317,6 +329,55 @@ __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
 // wait returns at once.
 __device__ __forceinline__ void pdl_begin() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ------------------------------------------------- mbarrier / bulk copy --
+constexpr unsigned long long kWaitNs = 250000000ull;   // bound of every mbarrier wait (0.25 s)
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* mbar) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(mbar)));
+}
+
+// Wait for the mbarrier phase of the given parity, at most kWaitNs of wall
+// time (try_wait itself may suspend for an unspecified while, so the bound is
+// on the global timer, not on the number of polls); false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity) {
+    const unsigned long long t0 = global_ns();
+    for (;;) {
+        uint32_t done;
+        asm volatile(
+            "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            "selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(done)
+            : "r"(smem_u32(mbar)), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if (global_ns() - t0 > kWaitNs) return false;
+    }
+}
+
+// Bulk copy (TMA engine) of `bytes` bytes global -> shared, completing on
+// mbar: both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* mbar) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(mbar)),
+                 "r"(bytes)
+                 : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(mbar))
+        : "memory");
 }
 
 __device__ __forceinline__ void cp_async_commit() {

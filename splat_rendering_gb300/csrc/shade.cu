@@ -39,7 +39,6 @@ constexpr int kRows = 128;           // pixels per tile (M = 128), one thread ea
 constexpr int kIn = 32;              // 19 inputs, zero padded to two K = 16 steps
 constexpr int kHid = 64;
 constexpr int kOutPad = 16;          // 3 outputs padded to the smallest N for M = 128
-constexpr unsigned long long kWaitNs = 250000000ull;   // bound of every mbarrier wait (0.25 s)
 
 // flat parameter layout: W1 [64][19], b1 [64], W2 [64][64], b2 [64], W3 [3][64], b3 [3]
 constexpr int kOffB1 = kHid * 19;
@@ -50,9 +49,6 @@ constexpr int kOffB3 = kOffW3 + 3 * kHid;
 static_assert(kOffB3 + 3 == kShadeParams, "shading parameter layout");
 
 // ------------------------------------------------------------ tcgen05 --
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
 
 // Shared-memory matrix descriptor, no swizzle: start address, the byte offset
 // between core matrices along K (lbo) and along M/N (sbo) -- the same roles
@@ -85,29 +81,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* mbar) {
         : "memory");
 }
 
-__device__ __forceinline__ unsigned long long global_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Wait for the mbarrier phase of the given parity, at most kWaitNs of wall
-// time (try_wait itself may suspend for an unspecified while, so the bound is
-// on the global timer, not on the number of polls); false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity) {
-    const unsigned long long t0 = global_ns();
-    for (;;) {
-        uint32_t done;
-        asm volatile(
-            "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-            "selp.u32 %0, 1, 0, p;\n}\n"
-            : "=r"(done)
-            : "r"(smem_u32(mbar)), "r"(parity)
-            : "memory");
-        if (done) return true;
-        if (global_ns() - t0 > kWaitNs) return false;
-    }
-}
 
 // 16 consecutive fp32 columns of this thread's TMEM lane (warp w owns lanes
 // 32w .. 32w + 31); the values are valid after tmem_wait_ld().
@@ -214,22 +187,6 @@ __device__ __forceinline__ void put8(unsigned char* tile, int row, int k, int K,
     *reinterpret_cast<uint4*>(tile + kmajor_off(row, k, K)) = pack8(v);
 }
 
-// Bulk copy (TMA engine) of `bytes` bytes global -> shared, completing on mbar.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
-                                          uint64_t* mbar) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(mbar)),
-                 "r"(bytes)
-                 : "memory");
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-            "r"(smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(mbar))
-        : "memory");
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* mbar) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(mbar)));
-}
 
 // The pixel's unit view direction (camera space) from its camera.
 __device__ __forceinline__ void view_dir(const Frame& f, uint32_t local, float* v) {

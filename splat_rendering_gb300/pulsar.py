@@ -22,6 +22,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpulsar.so")
 
 OK, ERR_ARG, ERR_CUDA, ERR_CAPACITY, ERR_STATE, ERR_NOMEM, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5, -6
+ERR_INTERNAL = -7   # debug build: a device index check failed
 FLAG_GEOM_CUTOFF = 0x1
 FLAG_COUNT_HITS = 0x2
 FLAG_NORMALIZE_GRADS = 0x4

@@ -73,3 +73,15 @@ def test_missing_library_fails_loudly(tmp_path):
             pl.load(str(tmp_path / "libpulsar.so"))
     finally:
         pl._lib = saved
+
+
+def test_debug_and_nvtx_builds_export_the_same_symbols():
+    """The optional builds (device index checks; NVTX ranges) compile for sm_103a
+    without a GPU and export every declared entry point."""
+    from splat_rendering_gb300 import build
+    path = build.build(debug=True, nvtx=True)
+    dbg = ctypes.CDLL(path)
+    for name in _declared():
+        assert hasattr(dbg, name), name
+    dbg.pulsar_strerror.restype = ctypes.c_char_p
+    assert b"index check" in dbg.pulsar_strerror(-7)
