@@ -62,11 +62,14 @@ k_backward(Frames fs, Workspace w, const float* __restrict__ features,
     const bool acc2 = CMAX <= 4 && (mode & 4) != 0;
     constexpr int NB = BwdBatch<CMAX>::n;
     constexpr int NV = 5 + CMAX;   // dL/dc.xyz, dL/dr, dL/do, dL/df[CMAX]
+    // feature row stride in words: odd, so that lanes reading different
+    // candidates' rows hit different banks
+    constexpr int FSP = CMAX | 1;
     __shared__ float4 s_uv[NB];
     __shared__ float4 s_ex[NB];          // exponent hi, lo, o, flags
     __shared__ float4 s_geo[NB];         // (c.z/r_eff)^2 hi, lo, c.z, r_eff
     __shared__ int s_id[NB];
-    __shared__ float s_feat[NB * CMAX];
+    __shared__ float s_feat[NB * FSP];
     __shared__ float s_k[kBwdThreads / 32][4];
     // the block's camera and its tile in that camera's image (a single camera
     // is indexed statically, so its constants stay instruction operands)
@@ -104,7 +107,7 @@ k_backward(Frames fs, Workspace w, const float* __restrict__ features,
             s_id[t] = id;
 #pragma unroll
             for (int c = 0; c < CMAX; ++c)
-                if (c < C) cp_async4(&s_feat[t * CMAX + c], features + (size_t)id * C + c);
+                if (c < C) cp_async4(&s_feat[t * FSP + c], features + (size_t)id * C + c);
         }
         cp_async_commit();
     };
@@ -168,7 +171,7 @@ k_backward(Frames fs, Workspace w, const float* __restrict__ features,
 #pragma unroll
                 for (int c = 0; c < CMAX; ++c) {
                     if (c < C) {
-                        const float fc = s_feat[j * CMAX + c];
+                        const float fc = s_feat[j * FSP + c];
                         sdot += G[c] * (fc - F[c]);
                         v[5 + c] = wt * iw * G[c];               // dL/df = (w / W) G
                     }
@@ -720,7 +723,8 @@ cudaError_t launch_bwd_c(const Frames& fs, const Workspace& w, const float* feat
 cudaError_t launch_backward(const Frames& fs, const Workspace& w, const float* pos,
                             const float* features, const float* image, const float* grad_image,
                             float* grad_pos, float* grad_radius, float* grad_opacity,
-                            float* grad_features, float* grad_cam, cudaStream_t stream) {
+                            float* grad_features, float* grad_cam, bool zeroed,
+                            cudaStream_t stream) {
     const Frame& f = fs.f[0];
     const int want_geom = (grad_pos || grad_radius || grad_cam) ? 1 : 0;
     const int feat_v4 = (f.channels % 4 == 0 && grad_features &&
@@ -729,16 +733,18 @@ cudaError_t launch_backward(const Frames& fs, const Workspace& w, const float* p
     const bool acc2 = f.channels <= 3 && (grad_opacity || grad_features);
     const int mode = want_geom | feat_v4 | (acc2 ? 4 : 0);
     const bool norm = (f.flags & kParamNormalize) != 0;
-    // zero the accumulators the kernel reduces into: written here, their lines
-    // sit in L2 when the reductions arrive (zeroed a frame earlier they would
-    // be read back from DRAM)
+    // the accumulators the kernel reduces into start at zero: the frame's
+    // forward zeroed them; a further backward of the same frame zeroes them here
     const size_t nk = (size_t)f.n * f.n_cams;
     cudaError_t e = cudaSuccess;
-    if (want_geom && nk) e = cudaMemsetAsync(w.gacc, 0, nk * sizeof(float4), stream);
-    if (e == cudaSuccess && acc2 && f.n)
-        e = cudaMemsetAsync(w.gacc2, 0, (size_t)f.n * sizeof(float4), stream);
-    if (e == cudaSuccess && norm && nk) e = cudaMemsetAsync(w.hitcnt, 0, nk * sizeof(float), stream);
-    if (e != cudaSuccess) return e;
+    if (!zeroed) {
+        if (want_geom && nk) e = cudaMemsetAsync(w.gacc, 0, nk * sizeof(float4), stream);
+        if (e == cudaSuccess && acc2 && f.n)
+            e = cudaMemsetAsync(w.gacc2, 0, (size_t)f.n * sizeof(float4), stream);
+        if (e == cudaSuccess && norm && nk)
+            e = cudaMemsetAsync(w.hitcnt, 0, nk * sizeof(float), stream);
+        if (e != cudaSuccess) return e;
+    }
     if (f.channels == 3)
         e = launch_bwd_c<3>(fs, w, features, image, grad_image, grad_opacity, grad_features, mode,
                             stream);

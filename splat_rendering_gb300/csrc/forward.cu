@@ -57,14 +57,18 @@ struct FwdSmem {
     static constexpr int NB = 192;                   // candidates per batch
     static constexpr bool kStageFeat = CMAX <= 16;   // wider features are read from global
     static constexpr int FS = kStageFeat ? CMAX : 0;
+    // feature row stride in words: odd, so that lanes reading different
+    // candidates' rows hit different banks (16 floats per row would put 32
+    // lanes on two banks)
+    static constexpr int FSP = kStageFeat ? (CMAX | 1) : 0;
     // two batch buffers, each: uv, ex, geo, rk (float4 / uint4 [NB]) of the
-    // record, then features float [NB][FS] and ids int [NB]
+    // record, then features float [NB][FSP] and ids int [NB]
     static constexpr int rec_uv = 0;
     static constexpr int rec_ex = NB * 16;
     static constexpr int rec_geo = 2 * NB * 16;
     static constexpr int rec_rk = 3 * NB * 16;
     static constexpr int rec_feat = 4 * NB * 16;
-    static constexpr int rec_id = rec_feat + NB * FS * 4;
+    static constexpr int rec_id = rec_feat + NB * FSP * 4;
     static constexpr int buf_bytes = rec_id + NB * 4;
     static constexpr int list = 2 * buf_bytes;                       // u16 [8][NB]
     static constexpr int dbuf = list + kWarps * NB * 2;              // float [8][kTestCap]
@@ -85,9 +89,25 @@ __global__ void __launch_bounds__(kFwdThreads, CMAX <= 4 ? 4 : (CMAX <= 16 ? 3 :
 k_forward(Frames fs, Workspace w, const float* __restrict__ features, const float* __restrict__ bg,
           float* __restrict__ image) {
     pdl_begin();
+    // zero the backward's accumulators of this frame on the way (plain
+    // coalesced stores that never wait: this kernel is bound by its own
+    // instruction stream and latencies, so they cost next to nothing here,
+    // against a separate memset pass before the backward)
+    if (w.gacc) {
+        const Frame& f0 = fs.f[0];
+        const size_t nk = (size_t)f0.n * (size_t)f0.n_cams;
+        const size_t stride = (size_t)gridDim.x * blockDim.x;
+        const size_t i0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+        const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (size_t i = i0; i < nk; i += stride) w.gacc[i] = z4;
+        for (size_t i = i0; i < (size_t)f0.n; i += stride) w.gacc2[i] = z4;
+        if (f0.flags & kParamNormalize)
+            for (size_t i = i0; i < nk; i += stride) w.hitcnt[i] = 0.0f;
+    }
     using L = FwdSmem<CMAX>;
     constexpr int NB = L::NB;
     constexpr int FS = L::FS;
+    constexpr int FSP = L::FSP;
     extern __shared__ __align__(16) unsigned char smem[];
     uint16_t (*s_list)[NB] = reinterpret_cast<uint16_t (*)[NB]>(smem + L::list);
     float (*s_dbuf)[kTestCap] = reinterpret_cast<float (*)[kTestCap]>(smem + L::dbuf);
@@ -164,7 +184,7 @@ k_forward(Frames fs, Workspace w, const float* __restrict__ features, const floa
 #pragma unroll
             for (int c = 0; c < FS; ++c)
                 if (c < C)
-                    cp_async4(B + L::rec_feat + (tid * FS + c) * 4, features + (size_t)id * C + c);
+                    cp_async4(B + L::rec_feat + (tid * FSP + c) * 4, features + (size_t)id * C + c);
         }
         reinterpret_cast<int*>(B + L::rec_id)[tid] = id;
     };
@@ -205,7 +225,7 @@ k_forward(Frames fs, Workspace w, const float* __restrict__ features, const floa
             const float* s_feat = reinterpret_cast<const float*>(B + L::rec_feat);
 #pragma unroll
             for (int cc = 0; cc < CMAX; ++cc)
-                if (cc < C) acc[cc] += wt * s_feat[j * FS + cc];
+                if (cc < C) acc[cc] += wt * s_feat[j * FSP + cc];
         } else {
             const float* fp = features + (size_t)reinterpret_cast<const int*>(B + L::rec_id)[j] * C;
 #pragma unroll

@@ -44,6 +44,7 @@ struct pulsar_ctx {
     const float* pos = nullptr;        // inputs of the current frame
     int stage = 0;                     // 0 none, 1 projected, 2 binned, 3 forward done
     bool counts_dirty = false;         // tile counts hold a frame that was never binned
+    bool acc_zeroed = false;           // the forward zeroed the backward's accumulators
     static constexpr int kMaxAllocs = 32;
     void* allocs[kMaxAllocs] = {};
     int n_allocs = 0;
@@ -273,6 +274,7 @@ int pulsar_forward(pulsar_ctx_t c, const float* features, const float* bg, float
     cudaError_t e = launch_forward(c->frames, c->ws, features, bg, image, 0, as_stream(stream));
     if (e != cudaSuccess) return PULSAR_ERR_CUDA;
     c->stage = 3;
+    c->acc_zeroed = true;
     return PULSAR_OK;
 }
 
@@ -301,7 +303,9 @@ int pulsar_backward(pulsar_ctx_t c, const float* features, const float* bg, cons
             return PULSAR_ERR_CUDA;
     }
     cudaError_t e = launch_backward(c->frames, c->ws, c->pos, features, image, grad_image, grad_pos,
-                                    grad_radius, grad_opacity, grad_features, grad_cam, s);
+                                    grad_radius, grad_opacity, grad_features, grad_cam,
+                                    c->acc_zeroed, s);
+    c->acc_zeroed = false;
     return cuda_err(e);
 }
 

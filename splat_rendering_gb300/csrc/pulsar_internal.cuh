@@ -413,11 +413,12 @@ struct __align__(16) SphereRec {
 struct Workspace {
     SphereRec* rec;    // [maxN]
     // per camera of a batch: [maxCams][...] blocks, camera after camera
-    float4* gacc;      // [maxN] dL/dc.xyz, dL/dr accumulators (zeroed by each backward)
+    float4* gacc;      // [maxN] dL/dc.xyz, dL/dr accumulators (zeroed by the forward; by
+                       // the backward's launcher when a frame is differentiated again)
     float4* gacc2;     // [maxN] dL/do, dL/df[0..2] accumulators for C <= 3, one for all
-                       // cameras (zeroed by each backward; the finalize writes them out)
+                       // cameras (zeroed as gacc; the finalize writes them out)
     float* hitcnt;     // [maxN] pixels tracking each sphere, for normalised gradients
-                       // (zeroed by each backward)
+                       // (zeroed as gacc)
     uint32_t* tile_count;   // [maxB] (zero between frames)
     uint32_t* tile_start;   // [maxB+1]
     uint32_t* long_tiles;   // [maxB] tiles with lists longer than one warp sorts, in tile order
@@ -531,9 +532,12 @@ cudaError_t launch_shade_backward(const Frames& fs, const Workspace& w, const fl
                                   const float* params, const float* grad_rgb,
                                   float* grad_features, float* grad_params, int grid_cap,
                                   cudaStream_t stream);
+// zeroed: the accumulators were zeroed by this frame's forward and not used
+// since (else the launcher zeroes them first)
 cudaError_t launch_backward(const Frames& fs, const Workspace& w, const float* pos,
                             const float* features, const float* image, const float* grad_image,
                             float* grad_pos, float* grad_radius, float* grad_opacity,
-                            float* grad_features, float* grad_cam, cudaStream_t stream);
+                            float* grad_features, float* grad_cam, bool zeroed,
+                            cudaStream_t stream);
 
 }  // namespace pulsar

@@ -296,3 +296,26 @@ def test_unaligned_gradient_arrays(oracle_lib):
                     o["abs_grad_pos"], o["sens_grad_pos"], dF)
     gh.assert_close(grad.cpu().numpy(), o["grad_radius"], gh.GRAD_RTOL, gh.GRAD_ATOL, "radius",
                     o["abs_grad_radius"], o["sens_grad_radius"], dF)
+
+
+def test_backward_twice_on_one_frame(oracle_lib):
+    """The forward zeroes the backward's accumulators; a second backward of the
+    same frame (another upstream gradient) must start from zero again, so both
+    calls match the oracle."""
+    import torch
+    from splat_rendering_gb300 import pulsar as pl
+    sc = scenes.random_scene(67, 1200, 64, 48, rrange=(0.02, 0.3), rot_deg=4)
+    o, _, _, _ = _oracle_all(oracle_lib, sc)
+    r = pl.Renderer(max_spheres=sc.n, max_pairs=1 << 16, max_width=64, max_height=48)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    img = r.render(t(sc.pos), t(sc.radius), t(sc.opacity), t(sc.features),
+                   pl.camera(sc.cameras[0]), pl.params(sc.params), t(sc.bg))
+    G = t(sc.grad_images[0])
+    first = {k: v.cpu().numpy() for k, v in r.backward(G).items()}
+    second = {k: v.cpu().numpy() for k, v in r.backward(G).items()}
+    assert r.status()[0] == 0
+    dF = gh.image_err(img.cpu().numpy(), o["image"])
+    for g in (first, second):
+        for k in ("pos", "radius", "opacity", "features", "cam"):
+            gh.assert_close(g[k], o["grad_" + k], gh.GRAD_RTOL, gh.GRAD_ATOL, f"twice {k}",
+                            o["abs_grad_" + k], o["sens_grad_" + k], dF)
