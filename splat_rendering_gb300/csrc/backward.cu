@@ -163,9 +163,12 @@ k_backward(Frames fs, Workspace w, const float* __restrict__ features,
                 cut = (fl & kFlagCut) != 0u;
                 float U, V;
                 const float Q = ray_offset_q(uv, ray, f.ifx, f.ify, &U, &V);
-                const float rq = sqrtf(Q * iqq);                 // rho / c.z (orthographic: rho)
+                // value path only (the hit set is the forward's): the hardware's
+                // approximate square root and reciprocals, a few ulps, are plenty
+                const float qi = Q * iqq;
+                const float rq = qi > 0.0f ? qi * rsqrtf(qi) : 0.0f;   // rho / c.z (orthographic: rho)
                 const float o = ex.z;
-                const float E = exp2f(__fsub_rn(ex.x, mg) + ex.y);   // exponents in log2 units
+                const float E = ex2_approx(__fsub_rn(ex.x, mg) + ex.y);   // exponents in log2 units
                 const float wt = o * dk * E;
                 float sdot = 0.0f;
 #pragma unroll
@@ -180,7 +183,7 @@ k_backward(Frames fs, Workspace w, const float* __restrict__ features,
                 v[4] = sj * dk * E * (1.0f + ex.x * 0.693147181f);   // dw/do = d E (1 + o z~/gamma)
                 if (want_geom && !cut) {
                     const float Z = geo.z, reff = geo.w;
-                    const float ireff = 1.0f / reff;
+                    const float ireff = __fdividef(1.0f, reff);
                     // normalised gradients: the sphere's share of the K gradient
                     // is scaled by 1e-3 / A, A = pi (f_min r_eff / c.z)^2 px^2
                     // (orthographic: pi (f_min r_eff)^2)
@@ -214,7 +217,7 @@ k_backward(Frames fs, Workspace w, const float* __restrict__ features,
                     if (Q > 0.0f) {
                         // drho/dc = e_perp / rho, e = c - c.z q = -c.z (U, V, 0)
                         const float kq = (U * ray.a + V * ray.b) * iqq;
-                        const float irq = 1.0f / rq;
+                        const float irq = __fdividef(1.0f, rq);
                         const float n0 = -(U - kq * ray.a) * irq;
                         const float n1 = -(V - kq * ray.b) * irq;
                         const float n2 = kq * irq;
