@@ -57,10 +57,16 @@ struct FwdSmem {
     static constexpr int NB = 192;                   // candidates per batch
     static constexpr bool kStageFeat = CMAX <= 16;   // wider features are read from global
     static constexpr int FS = kStageFeat ? CMAX : 0;
-    // feature row stride in words: odd, so that lanes reading different
-    // candidates' rows hit different banks (16 floats per row would put 32
-    // lanes on two banks)
-    static constexpr int FSP = kStageFeat ? (CMAX | 1) : 0;
+    // features of 8 and 16 channels are staged and read 16 bytes at a time
+    // (one cp.async and one 128-bit load per four channels) when the caller's
+    // rows allow it
+    static constexpr bool kVecFeat = kStageFeat && CMAX >= 8 && CMAX % 4 == 0;
+    // feature row stride in words: 16-byte rows padded by four words for the
+    // vector form (8 rows of a quarter-warp then fall on distinct bank groups
+    // when their candidates are consecutive); otherwise odd, so that lanes
+    // reading different candidates' rows hit different banks (16 floats per
+    // row would put 32 lanes on two banks)
+    static constexpr int FSP = kStageFeat ? (kVecFeat ? CMAX + 4 : (CMAX | 1)) : 0;
     // two batch buffers, each: uv, ex, geo, rk (float4 / uint4 [NB]) of the
     // record, then features float [NB][FSP] and ids int [NB]
     static constexpr int rec_uv = 0;
@@ -170,6 +176,10 @@ k_forward(Frames fs, Workspace w, const float* __restrict__ features, const floa
     end = min(end, f.max_pairs);
     start = min(start, end);
 
+    // 16-byte feature copies and loads: every row is whole (C == CMAX) and
+    // 16-byte aligned
+    const bool fvec = L::kVecFeat && C == CMAX &&
+                      (reinterpret_cast<uintptr_t>(features) & 15u) == 0;
     // thread t < NB stages candidate t of every batch: the record's four
     // 16-byte pieces and the features by cp.async, the id by a plain store
     auto stage = [&](int buf, int id) {
@@ -181,10 +191,17 @@ k_forward(Frames fs, Workspace w, const float* __restrict__ features, const floa
         cp_async16(B + L::rec_geo + tid * 16, src + 2);
         cp_async16(B + L::rec_rk + tid * 16, src + 3);
         if (L::kStageFeat) {
+            if (fvec) {
 #pragma unroll
-            for (int c = 0; c < FS; ++c)
-                if (c < C)
-                    cp_async4(B + L::rec_feat + (tid * FSP + c) * 4, features + (size_t)id * C + c);
+                for (int q = 0; q < FS / 4; ++q)
+                    cp_async16(B + L::rec_feat + (tid * FSP + 4 * q) * 4,
+                               features + (size_t)id * FS + 4 * q);
+            } else {
+#pragma unroll
+                for (int c = 0; c < FS; ++c)
+                    if (c < C)
+                        cp_async4(B + L::rec_feat + (tid * FSP + c) * 4, features + (size_t)id * C + c);
+            }
         }
         reinterpret_cast<int*>(B + L::rec_id)[tid] = id;
     };
@@ -223,9 +240,20 @@ k_forward(Frames fs, Workspace w, const float* __restrict__ features, const floa
         wsum += wt;
         if (L::kStageFeat) {
             const float* s_feat = reinterpret_cast<const float*>(B + L::rec_feat);
+            if (L::kVecFeat && fvec) {
 #pragma unroll
-            for (int cc = 0; cc < CMAX; ++cc)
-                if (cc < C) acc[cc] += wt * s_feat[j * FSP + cc];
+                for (int q = 0; q < CMAX / 4; ++q) {
+                    const float4 fq = *reinterpret_cast<const float4*>(s_feat + j * FSP + 4 * q);
+                    acc[4 * q] += wt * fq.x;
+                    acc[4 * q + 1] += wt * fq.y;
+                    acc[4 * q + 2] += wt * fq.z;
+                    acc[4 * q + 3] += wt * fq.w;
+                }
+            } else {
+#pragma unroll
+                for (int cc = 0; cc < CMAX; ++cc)
+                    if (cc < C) acc[cc] += wt * s_feat[j * FSP + cc];
+            }
         } else {
             const float* fp = features + (size_t)reinterpret_cast<const int*>(B + L::rec_id)[j] * C;
 #pragma unroll
