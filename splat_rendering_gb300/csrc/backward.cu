@@ -41,11 +41,19 @@ __device__ __forceinline__ void red_add_v4(float4* addr, float a, float b, float
                  :: "l"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
-// Shared-memory batch of the backward: candidates staged per batch (static
-// smem < 48 KB).
+// Shared-memory batch of the backward: candidates staged per batch; the
+// records in static shared memory, the features in dynamic shared memory.
 template <int CMAX>
 struct BwdBatch {
     static constexpr int n = CMAX <= 4 ? 512 : (CMAX <= 8 ? 256 : (CMAX <= 16 ? 384 : (CMAX <= 32 ? 192 : 128)));
+    // features of 8 and more channels (a multiple of 4) are staged and read
+    // 16 bytes at a time when the caller's rows allow it: rows padded by four
+    // words to keep them 16-byte aligned; otherwise an odd row stride in
+    // words, so that lanes reading different candidates' rows hit different
+    // banks
+    static constexpr bool vec = CMAX >= 8 && CMAX % 4 == 0;
+    static constexpr int fsp = vec ? CMAX + 4 : (CMAX | 1);
+    static constexpr int feat_bytes = n * fsp * 4;
 };
 
 template <int CMAX, bool MULTI>
@@ -62,14 +70,12 @@ k_backward(Frames fs, Workspace w, const float* __restrict__ features,
     const bool acc2 = CMAX <= 4 && (mode & 4) != 0;
     constexpr int NB = BwdBatch<CMAX>::n;
     constexpr int NV = 5 + CMAX;   // dL/dc.xyz, dL/dr, dL/do, dL/df[CMAX]
-    // feature row stride in words: odd, so that lanes reading different
-    // candidates' rows hit different banks
-    constexpr int FSP = CMAX | 1;
+    constexpr int FSP = BwdBatch<CMAX>::fsp;
     __shared__ float4 s_uv[NB];
     __shared__ float4 s_ex[NB];          // exponent hi, lo, o, flags
     __shared__ float4 s_geo[NB];         // (c.z/r_eff)^2 hi, lo, c.z, r_eff
     __shared__ int s_id[NB];
-    __shared__ float s_feat[NB * FSP];
+    extern __shared__ __align__(16) float s_feat[];   // [NB][FSP]
     __shared__ float s_k[kBwdThreads / 32][4];
     // the block's camera and its tile in that camera's image (a single camera
     // is indexed statically, so its constants stay instruction operands)
@@ -94,6 +100,10 @@ k_backward(Frames fs, Workspace w, const float* __restrict__ features,
     float4* __restrict__ gacc2 = w.gacc2;   // one for all cameras: their sum is wanted
     end = min(end, f.max_pairs);
     start = min(start, end);
+    // 16-byte feature copies and loads: every row is whole (C == CMAX) and
+    // 16-byte aligned
+    const bool fvec = BwdBatch<CMAX>::vec && C == CMAX &&
+                      (reinterpret_cast<uintptr_t>(features) & 15u) == 0;
     // a batch's records and features are copied by cp.async; the first batch
     // is started before the per-pixel loads so that the two latencies overlap
     auto stage = [&](uint32_t b0, int nb) {
@@ -105,9 +115,15 @@ k_backward(Frames fs, Workspace w, const float* __restrict__ features,
             cp_async16(&s_ex[t], src + 1);
             cp_async16(&s_geo[t], src + 2);
             s_id[t] = id;
+            if (fvec) {
 #pragma unroll
-            for (int c = 0; c < CMAX; ++c)
-                if (c < C) cp_async4(&s_feat[t * FSP + c], features + (size_t)id * C + c);
+                for (int q = 0; q < CMAX / 4; ++q)
+                    cp_async16(&s_feat[t * FSP + 4 * q], features + (size_t)id * CMAX + 4 * q);
+            } else {
+#pragma unroll
+                for (int c = 0; c < CMAX; ++c)
+                    if (c < C) cp_async4(&s_feat[t * FSP + c], features + (size_t)id * C + c);
+            }
         }
         cp_async_commit();
     };
@@ -171,12 +187,26 @@ k_backward(Frames fs, Workspace w, const float* __restrict__ features,
                 const float E = ex2_approx(__fsub_rn(ex.x, mg) + ex.y);   // exponents in log2 units
                 const float wt = o * dk * E;
                 float sdot = 0.0f;
+                if (BwdBatch<CMAX>::vec && fvec) {
 #pragma unroll
-                for (int c = 0; c < CMAX; ++c) {
-                    if (c < C) {
-                        const float fc = s_feat[j * FSP + c];
-                        sdot += G[c] * (fc - F[c]);
-                        v[5 + c] = wt * iw * G[c];               // dL/df = (w / W) G
+                    for (int q = 0; q < CMAX / 4; ++q) {
+                        const float4 fq = *reinterpret_cast<const float4*>(&s_feat[j * FSP + 4 * q]);
+                        const float fv[4] = {fq.x, fq.y, fq.z, fq.w};
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            const int c = 4 * q + r;
+                            sdot += G[c] * (fv[r] - F[c]);
+                            v[5 + c] = wt * iw * G[c];           // dL/df = (w / W) G
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < CMAX; ++c) {
+                        if (c < C) {
+                            const float fc = s_feat[j * FSP + c];
+                            sdot += G[c] * (fc - F[c]);
+                            v[5 + c] = wt * iw * G[c];           // dL/df = (w / W) G
+                        }
                     }
                 }
                 const float sj = sdot * iw;                      // dL/dw = <G, f - F> / W
@@ -714,14 +744,39 @@ cudaError_t launch_bwd_c(const Frames& fs, const Workspace& w, const float* feat
                          const float* image, const float* grad_image, float* grad_opacity,
                          float* grad_features, int mode, cudaStream_t stream) {
     const dim3 grid(fs.f[0].n_tiles_all), block(kBwdThreads);
+    constexpr int smem = BwdBatch<CMAX>::feat_bytes;
     if (fs.f[0].n_cams == 1)
-        return launch_pdl(k_backward<CMAX, false>, grid, block, 0, stream, fs, w, features, image,
-                          grad_image, grad_opacity, grad_features, mode);
-    return launch_pdl(k_backward<CMAX, true>, grid, block, 0, stream, fs, w, features, image,
+        return launch_pdl(k_backward<CMAX, false>, grid, block, smem, stream, fs, w, features,
+                          image, grad_image, grad_opacity, grad_features, mode);
+    return launch_pdl(k_backward<CMAX, true>, grid, block, smem, stream, fs, w, features, image,
                       grad_image, grad_opacity, grad_features, mode);
 }
 
+// Opt the backward kernels into their dynamic shared memory (the
+// 16-channel batch's records and features exceed 48 KB together).
+template <int CMAX>
+cudaError_t prepare_bwd_c() {
+    cudaError_t e = cudaFuncSetAttribute(k_backward<CMAX, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         BwdBatch<CMAX>::feat_bytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_backward<CMAX, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 BwdBatch<CMAX>::feat_bytes);
+    return e;
+}
+
 }  // namespace
+
+cudaError_t prepare_backward() {
+    cudaError_t e = prepare_bwd_c<3>();
+    if (e == cudaSuccess) e = prepare_bwd_c<4>();
+    if (e == cudaSuccess) e = prepare_bwd_c<8>();
+    if (e == cudaSuccess) e = prepare_bwd_c<16>();
+    if (e == cudaSuccess) e = prepare_bwd_c<32>();
+    if (e == cudaSuccess) e = prepare_bwd_c<kMaxChannels>();
+    return e;
+}
 
 cudaError_t launch_backward(const Frames& fs, const Workspace& w, const float* pos,
                             const float* features, const float* image, const float* grad_image,

@@ -160,6 +160,7 @@ int pulsar_create_cams(pulsar_ctx_t* out, int device, int64_t max_spheres, int64
               alloc(c, &w.state, 1);
     if (ok) ok = cudaMallocHost(&c->host_state, sizeof(DevState)) == cudaSuccess;
     if (ok) ok = prepare_forward() == cudaSuccess && prepare_bin() == cudaSuccess &&
+                 prepare_backward() == cudaSuccess &&
                  prepare_shade(&c->shade) == cudaSuccess;
     if (ok) ok = cudaDeviceGetAttribute(&c->n_sms, cudaDevAttrMultiProcessorCount, device) ==
                  cudaSuccess;

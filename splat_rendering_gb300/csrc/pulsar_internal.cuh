@@ -516,6 +516,7 @@ cudaError_t launch_project(const Frames& fs, const Workspace& w, const float* po
 cudaError_t launch_bin(const Frames& fs, const Workspace& w, cudaStream_t stream);
 cudaError_t prepare_forward();   // opt the forward kernels into their shared memory
 cudaError_t prepare_bin();       // opt the long-list sort into its shared memory
+cudaError_t prepare_backward();  // opt the backward kernels into their shared memory
 cudaError_t launch_forward(const Frames& fs, const Workspace& w, const float* features,
                            const float* bg, float* image, int max_pairs_stride,
                            cudaStream_t stream);
