@@ -62,6 +62,9 @@ k_backward(Frames fs, Workspace w, const float* __restrict__ features,
            const float* __restrict__ image, const float* __restrict__ grad_image,
            float* __restrict__ grad_opacity, float* __restrict__ grad_features, int mode) {
     pdl_begin();
+    // the frame's pair count and the tile's list bounds, loaded together
+    const uint32_t n_pairs = w.state->n_pairs;
+    uint32_t start = w.tile_start[blockIdx.x], end = w.tile_start[blockIdx.x + 1];
     // mode bit 0: geometry gradients wanted; bit 1: feature gradient rows are
     // 16-byte aligned with C a multiple of 4 (vector reductions); bit 2: C <= 3,
     // opacity and feature gradients into the second accumulator
@@ -83,7 +86,7 @@ k_backward(Frames fs, Workspace w, const float* __restrict__ features,
     const int cam = MULTI ? tile_g / fs.f[0].n_tiles : 0;
     const Frame& f = fs.f[MULTI ? cam : 0];
     const int tile = tile_g - cam * f.n_tiles;
-    if (w.state->n_pairs > f.max_pairs) return;   // overflowed frame: no valid buffer
+    if (n_pairs > f.max_pairs) return;   // overflowed frame: no valid buffer
     const int C = f.channels;
     const int tyi = tile / f.tiles_x, txi = tile - tyi * f.tiles_x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -94,7 +97,6 @@ k_backward(Frames fs, Workspace w, const float* __restrict__ features,
     // the pixel in the batch's buffers; planes of ids / d are pix_all apart
     const uint32_t P = f.pix_all;
     const uint32_t p = f.pix_base + (uint32_t)(inside ? y * f.width + x : 0);
-    uint32_t start = w.tile_start[tile_g], end = w.tile_start[tile_g + 1];
     const SphereRec* __restrict__ rec = w.rec + f.rec_base;   // this camera's records
     float4* __restrict__ gacc = w.gacc + f.rec_base;
     float4* __restrict__ gacc2 = w.gacc2;   // one for all cameras: their sum is wanted

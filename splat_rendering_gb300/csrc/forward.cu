@@ -95,6 +95,10 @@ __global__ void __launch_bounds__(kFwdThreads, CMAX <= 4 ? 4 : (CMAX <= 16 ? 3 :
 k_forward(Frames fs, Workspace w, const float* __restrict__ features, const float* __restrict__ bg,
           float* __restrict__ image) {
     pdl_begin();
+    // the frame's pair count and the tile's list bounds, loaded together
+    // ahead of the set-up below, which hides their latency
+    const uint32_t n_pairs = w.state->n_pairs;
+    uint32_t start = w.tile_start[blockIdx.x], end = w.tile_start[blockIdx.x + 1];
     // zero the backward's accumulators of this frame on the way (plain
     // coalesced stores that never wait: this kernel is bound by its own
     // instruction stream and latencies, so they cost next to nothing here,
@@ -133,13 +137,16 @@ k_forward(Frames fs, Workspace w, const float* __restrict__ features, const floa
     const int cam = MULTI ? tile_g / fs.f[0].n_tiles : 0;
     const Frame& f = fs.f[MULTI ? cam : 0];
     const int tile = tile_g - cam * f.n_tiles;
-    // a frame whose pairs overflowed max_pairs has unsorted lists: render nothing
-    // (the capacity error is latched and reported by pulsar_status)
-    if (w.state->n_pairs > f.max_pairs) return;
+    end = min(end, f.max_pairs);
+    start = min(start, end);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // the ids of the first two batches (a read of the list is in bounds even
+    // for an overflowed frame; its ids are used only after the check below)
+    const int id_first = (tid < NB && start + tid < end) ? (int)w.tile_ids[start + tid] : -1;
+    int id_next = (tid < NB && start + NB + tid < end) ? (int)w.tile_ids[start + NB + tid] : -1;
     const int C = f.channels;
     const int tyi = tile / f.tiles_x, txi = tile - tyi * f.tiles_x;
     const int tx0 = txi * kTile, ty0 = tyi * kTile;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int x = tx0 + (tid & 15), y = ty0 + (tid >> 4);
     const int row0 = ty0 + 2 * warp;              // the warp's two pixel rows
     const bool inside = x < f.width && y < f.height;
@@ -170,11 +177,11 @@ k_forward(Frames fs, Workspace w, const float* __restrict__ features, const floa
         s_iqq[tid] = pq.iqq;
     }
     if (tid == 0) *s_hits = 0ull;
+    // a frame whose pairs overflowed max_pairs has unsorted lists: render nothing
+    // (the capacity error is latched and reported by pulsar_status)
+    if (n_pairs > f.max_pairs) return;
 
-    uint32_t start = w.tile_start[tile_g], end = w.tile_start[tile_g + 1];
     const SphereRec* __restrict__ rec = w.rec + f.rec_base;   // this camera's records
-    end = min(end, f.max_pairs);
-    start = min(start, end);
 
     // 16-byte feature copies and loads: every row is whole (C == CMAX) and
     // 16-byte aligned
@@ -205,9 +212,8 @@ k_forward(Frames fs, Workspace w, const float* __restrict__ features, const floa
         }
         reinterpret_cast<int*>(B + L::rec_id)[tid] = id;
     };
-    if (tid < NB && start + tid < end) stage(0, (int)w.tile_ids[start + tid]);
+    if (id_first >= 0) stage(0, id_first);
     cp_async_commit();
-    int id_next = (tid < NB && start + NB + tid < end) ? (int)w.tile_ids[start + NB + tid] : -1;
 
     // running max of eps/gamma and o z~/gamma (log2 units), as a float pair
     float mg = f.eg_hi, mgl = f.eg_lo;
