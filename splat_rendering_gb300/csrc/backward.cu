@@ -86,7 +86,6 @@ k_backward(Frames fs, Workspace w, const float* __restrict__ features,
     const int cam = MULTI ? tile_g / fs.f[0].n_tiles : 0;
     const Frame& f = fs.f[MULTI ? cam : 0];
     const int tile = tile_g - cam * f.n_tiles;
-    if (n_pairs > f.max_pairs) return;   // overflowed frame: no valid buffer
     const int C = f.channels;
     const int tyi = tile / f.tiles_x, txi = tile - tyi * f.tiles_x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -106,8 +105,23 @@ k_backward(Frames fs, Workspace w, const float* __restrict__ features,
     // 16-byte aligned
     const bool fvec = BwdBatch<CMAX>::vec && C == CMAX &&
                       (reinterpret_cast<uintptr_t>(features) & 15u) == 0;
-    // a batch's records and features are copied by cp.async; the first batch
-    // is started before the per-pixel loads so that the two latencies overlap
+    // the pixel's inputs, loaded together with the list bounds (the buffers
+    // are read in bounds also for an overflowed frame, whose values go unused)
+    float G[CMAX], F[CMAX];
+#pragma unroll
+    for (int c = 0; c < CMAX; ++c) {
+        G[c] = (inside && c < C) ? grad_image[(size_t)p * C + c] : 0.0f;
+        F[c] = (inside && c < C) ? image[(size_t)p * C + c] : 0.0f;
+    }
+    const float mg = inside ? w.mg[p] : 0.0f;
+    const float wsum = inside ? w.wsum[p] : 1.0f;
+    // the pixel's tracked slots are in list order, so the slots of one batch
+    // are a run: a cursor walks them across the batches, each slot read once
+    int k = 0;
+    int pos = inside ? w.ids[p] : -1;   // slot k's list position (-1: no more hits)
+    float d = inside ? w.dtr[p] : 0.0f;
+    if (n_pairs > f.max_pairs) return;   // overflowed frame: no valid buffer
+    // a batch's records and features are copied by cp.async
     auto stage = [&](uint32_t b0, int nb) {
         for (int t = tid; t < nb; t += kBwdThreads) {
             int id = (int)w.tile_ids[b0 + t];
@@ -133,21 +147,8 @@ k_backward(Frames fs, Workspace w, const float* __restrict__ features,
 
     const PixelRay ray = pixel_ray(x, y, f);
     const float iqq = __frcp_rn(ray.qq);
-
-    float G[CMAX], F[CMAX];
-#pragma unroll
-    for (int c = 0; c < CMAX; ++c) {
-        G[c] = (inside && c < C) ? grad_image[(size_t)p * C + c] : 0.0f;
-        F[c] = (inside && c < C) ? image[(size_t)p * C + c] : 0.0f;
-    }
-    const float mg = inside ? w.mg[p] : 0.0f;
-    const float iw = inside ? 1.0f / w.wsum[p] : 0.0f;
+    const float iw = inside ? 1.0f / wsum : 0.0f;
     float gk[4] = {0.f, 0.f, 0.f, 0.f};   // d/d(fx, fy, cx, cy)
-    // the pixel's tracked slots are in list order, so the slots of one batch
-    // are a run: a cursor walks them across the batches, each slot read once
-    int k = 0;
-    int pos = inside ? w.ids[p] : -1;   // slot k's list position (-1: no more hits)
-    float d = inside ? w.dtr[p] : 0.0f;
 
     for (uint32_t b0 = start; b0 < end; b0 += NB) {
         const int nb = (int)min((uint32_t)NB, end - b0);
