@@ -25,8 +25,9 @@
 //             dL/dR = sum dL/dc p^T and dL/dt = sum dL/dc of every camera
 //             reduced per block (Pulsar Sec. B.2: sphere-wise camera-gradient
 //             accumulation).
-// k_camera_reduce  one block per camera sums all its per-block partials in a
-//             fixed order into its grad_cam (the device-wide reduction).
+// k_camera_reduce  one block per output of each camera's grad_cam sums that
+//             output's per-block partials in a fixed order (the device-wide
+//             reduction).
 #include "pulsar_internal.cuh"
 
 namespace pulsar {
@@ -650,95 +651,67 @@ k_finalize_cams(Frames fs, Workspace w, const float* __restrict__ pos, float* __
     }
 }
 
-// One block per camera: its dL/dR and dL/dt from the finalize blocks'
-// partials and dL/d(fx, fy, cx, cy) from its tiles' partials, summed in a
-// fixed order in float-pair arithmetic (deterministic, ~1e-14 relative;
-// Pulsar Sec. B.2's device-wide camera reduction).  The partials of each of
-// the 16 outputs are contiguous.  The 32 warps are dealt out in proportion
-// to the outputs' lengths (a function of the two lengths only, so the order
-// of the sums is fixed for a given frame), each warp sums a contiguous part
-// with eight independent accumulators per lane (eight loads in flight), and
-// the parts of an output are combined in order through shared memory.
-constexpr int kCamAcc = 8;
+// One block per (output, camera): output q of the camera's 16 -- dL/dR and
+// dL/dt from the finalize blocks' partials, dL/d(fx, fy, cx, cy) from its
+// tiles' partials -- summed in a fixed order in float-pair arithmetic
+// (deterministic, ~1e-14 relative; Pulsar Sec. B.2's device-wide camera
+// reduction).  The partials of an output are contiguous: thread t sums
+// elements t, t + 1024, ... with kCamAcc of them in flight, then the block
+// combines the threads' sums in a fixed tree.  The order is a function of
+// the output's length only.
+constexpr int kCamAcc = 4;
 
 __global__ void __launch_bounds__(kCamThreads)
 k_camera_reduce(Frames fs, Workspace w, int fin_blocks, float* __restrict__ grad_cam) {
     pdl_begin();
     static_assert(kCamThreads == 1024, "32 warps");
     __shared__ float2 s_part[32];
-    const int cam = blockIdx.x;
+    const int q = blockIdx.x, cam = blockIdx.y;
     const Frame& f = fs.f[cam];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int len_rt = fin_blocks, len_k = f.n_tiles;
-    // warps per K output: round(32 len_k / total) within 1..5; the rest shared
-    // by the 12 R/t outputs (at least one each)
-    const long long total = 12LL * len_rt + 4LL * len_k;
-    int wk = total > 0 ? (int)((32LL * len_k + total / 2) / total) : 1;
-    wk = wk < 1 ? 1 : (wk > 5 ? 5 : wk);
-    const int wr = (32 - 4 * wk) / 12;
-    int q = -1, part = 0, parts = 1;
-    if (warp < 12 * wr) {
-        q = warp / wr;
-        part = warp % wr;
-        parts = wr;
-    } else if (warp < 12 * wr + 4 * wk) {
-        q = 12 + (warp - 12 * wr) / wk;
-        part = (warp - 12 * wr) % wk;
-        parts = wk;
+    const float2* src;
+    int len;
+    if (q < 12) {
+        src = w.rtpart + ((size_t)cam * 12 + q) * fin_blocks;
+        len = fin_blocks;
+    } else {
+        src = w.kpart + (size_t)(q - 12) * f.n_tiles_all + f.tile_base;
+        len = f.n_tiles;
     }
-    if (q >= 0) {
-        const float2* src;
-        int len;
-        if (q < 12) {
-            src = w.rtpart + ((size_t)cam * 12 + q) * fin_blocks;
-            len = len_rt;
-        } else {
-            src = w.kpart + (size_t)(q - 12) * f.n_tiles_all + f.tile_base;
-            len = len_k;
-        }
-        const int lo = (int)((long long)len * part / parts);
-        const int hi = (int)((long long)len * (part + 1) / parts);
-        FPair v[kCamAcc];
+    FPair v[kCamAcc];
 #pragma unroll
-        for (int u = 0; u < kCamAcc; ++u) v[u] = FPair{0.0f, 0.0f};
-        int b = lo + lane;
-        for (; b + 32 * (kCamAcc - 1) < hi; b += 32 * kCamAcc) {
-            float2 t[kCamAcc];
+    for (int u = 0; u < kCamAcc; ++u) v[u] = FPair{0.0f, 0.0f};
+    for (int b = tid; b < len; b += kCamAcc * kCamThreads) {
+        float2 t[kCamAcc];
 #pragma unroll
-            for (int u = 0; u < kCamAcc; ++u) t[u] = src[b + 32 * u];
+        for (int u = 0; u < kCamAcc; ++u)
+            t[u] = b + u * kCamThreads < len ? src[b + u * kCamThreads] : make_float2(0.0f, 0.0f);
 #pragma unroll
-            for (int u = 0; u < kCamAcc; ++u) v[u] = pp_add(v[u], FPair{t[u].x, t[u].y});
-        }
+        for (int u = 0; u < kCamAcc; ++u) v[u] = pp_add(v[u], FPair{t[u].x, t[u].y});
+    }
 #pragma unroll
-        for (int u = 0; u < kCamAcc - 1; ++u) {   // the tail: fewer than kCamAcc loads
-            if (b + 32 * u < hi) {
-                const float2 t = src[b + 32 * u];
-                v[u] = pp_add(v[u], FPair{t.x, t.y});
-            }
-        }
+    for (int h = kCamAcc / 2; h > 0; h >>= 1)
 #pragma unroll
-        for (int h = kCamAcc / 2; h > 0; h >>= 1)
+        for (int u = 0; u < h; ++u) v[u] = pp_add(v[u], v[u + h]);
+    FPair r = v[0];
 #pragma unroll
-            for (int u = 0; u < h; ++u) v[u] = pp_add(v[u], v[u + h]);
-        FPair r = v[0];
+    for (int o = 16; o > 0; o >>= 1) {
+        const FPair t = {__shfl_down_sync(0xffffffffu, r.hi, o),
+                         __shfl_down_sync(0xffffffffu, r.lo, o)};
+        r = pp_add(r, t);
+    }
+    if (lane == 0) s_part[warp] = make_float2(r.hi, r.lo);
+    __syncthreads();
+    if (warp == 0) {
+        const float2 t0 = s_part[lane];
+        r = FPair{t0.x, t0.y};
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             const FPair t = {__shfl_down_sync(0xffffffffu, r.hi, o),
                              __shfl_down_sync(0xffffffffu, r.lo, o)};
             r = pp_add(r, t);
         }
-        if (lane == 0) s_part[warp] = make_float2(r.hi, r.lo);
-    }
-    __syncthreads();
-    if (tid < 16) {
-        const int w0 = tid < 12 ? tid * wr : 12 * wr + (tid - 12) * wk;
-        const int nw = tid < 12 ? wr : wk;
-        FPair s = {0.0f, 0.0f};
-        for (int k = 0; k < nw; ++k) {
-            const float2 t = s_part[w0 + k];
-            s = pp_add(s, FPair{t.x, t.y});
-        }
-        if (grad_cam) grad_cam[16 * cam + tid] = __fadd_rn(s.hi, s.lo);
+        if (lane == 0 && grad_cam) grad_cam[16 * cam + q] = __fadd_rn(r.hi, r.lo);
     }
 }
 
@@ -840,7 +813,7 @@ cudaError_t launch_backward(const Frames& fs, const Workspace& w, const float* p
             e = launch_pdl(k_finalize_cams, dim3(blocks), dim3(kFinThreads), 0, stream, fs, w, pos,
                            grad_pos, grad_radius, grad_opacity, grad_features, fmode);
         if (e == cudaSuccess && want_geom)
-            e = launch_pdl(k_camera_reduce, dim3(f.n_cams), dim3(kCamThreads), 0, stream, fs, w,
+            e = launch_pdl(k_camera_reduce, dim3(16, f.n_cams), dim3(kCamThreads), 0, stream, fs, w,
                            blocks, grad_cam);
     }
     return e;
