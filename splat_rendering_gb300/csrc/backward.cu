@@ -484,9 +484,14 @@ k_finalize_one_cam(Frames fs, Workspace w, const float* __restrict__ pos, float*
             if (norm) {
                 const float cnt = w.hitcnt[i];
                 sph = cnt > 0.0f ? 1.0f / cnt : 1.0f;
-                const float4 geo = w.rec[i].geo;          // c.z in z, r_eff in w (0: culled)
-                const float rz = f.fmin * (f.ortho ? geo.w : geo.w / geo.z);
-                cams = rz > 0.0f ? 1e-3f / (kPi * rz * rz) : 0.0f;
+                // a sphere no pixel tracks has no gradient (and may be culled,
+                // its record's second half unwritten)
+                cams = 0.0f;
+                if (cnt > 0.0f) {
+                    const float4 geo = w.rec[i].geo;          // c.z in z, r_eff in w
+                    const float rz = f.fmin * (f.ortho ? geo.w : geo.w / geo.z);
+                    cams = rz > 0.0f ? 1e-3f / (kPi * rz * rz) : 0.0f;
+                }
                 if (!acc2) {
                     if (grad_opacity) grad_opacity[i] *= sph;
                     if (grad_features)
@@ -568,9 +573,14 @@ k_finalize_cams(Frames fs, Workspace w, const float* __restrict__ pos, float* __
                 const int i = i0 + k;
                 const float c = w.hitcnt[f.rec_base + i];
                 sph = c > 0.0f ? 1.0f / c : 1.0f;
-                const float4 geo = w.rec[f.rec_base + i].geo;   // c.z in z, r_eff in w (0: culled)
-                const float rz = f.fmin * (f.ortho ? geo.w : geo.w / geo.z);
-                cams = rz > 0.0f ? 1e-3f / (kPi * rz * rz) : 0.0f;
+                // a sphere no pixel tracks has no gradient (and may be culled,
+                // its record's second half unwritten)
+                cams = 0.0f;
+                if (c > 0.0f) {
+                    const float4 geo = w.rec[f.rec_base + i].geo;   // c.z in z, r_eff in w
+                    const float rz = f.fmin * (f.ortho ? geo.w : geo.w / geo.z);
+                    cams = rz > 0.0f ? 1e-3f / (kPi * rz * rz) : 0.0f;
+                }
                 if (!acc2) {
                     if (grad_opacity) grad_opacity[i] *= sph;
                     if (grad_features)

@@ -109,8 +109,13 @@ k_project(Frames fs, Workspace w, const float* __restrict__ pos, const float* __
             SphereRec* out = w.rec + f.rec_base + i;
             out->uv = r0;
             out->ex = r1;
-            out->geo = r2;
-            out->rk = make_uint4(rc.x, rc.y, __float_as_uint(s2), __float_as_uint(key));
+            // the second 32-byte half is read only through the tile lists,
+            // i.e. for kept spheres: a culled sphere writes the first half
+            // alone (flags 0), a whole sector
+            if (flags & kFlagKeep) {
+                out->geo = r2;
+                out->rk = make_uint4(rc.x, rc.y, __float_as_uint(s2), __float_as_uint(key));
+            }
         }
         // warp-cooperative tile counting: flatten the warp's (sphere, tile) pairs
         int incl = count;
