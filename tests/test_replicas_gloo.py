@@ -4,6 +4,7 @@ the only collective is the max over ranks of the timed region, and only
 rank 0 reports.  No GPU."""
 from __future__ import annotations
 
+import json
 import multiprocessing as mp
 import os
 import socket
@@ -74,3 +75,28 @@ def test_reference_arm_runs_on_rank_zero_only(capsys, monkeypatch):
     monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference"])
     bench.run_reference(bench.args_parse())
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_prints_one_contract_line(capsys, monkeypatch):
+    """Rank 0 of the reference arm times the oracle on the host cores and
+    prints one JSON line with the keys the bench contract names (a one-second
+    sample here)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--steps", "1",
+                                      "--warmup", "0", "--cpu-seconds", "1"])
+    bench.run_reference(bench.args_parse())
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.strip()]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference"
+    assert line["metric"] == bench.METRIC and line["unit"] == bench.UNIT
+    assert line["higher_is_better"] is True and line["value"] > 0
+    assert line["ms_per_step"] == pytest.approx(1e3 / line["value"])
+    assert line["steps"] == 1 and line["warmup"] == 0 and line["n_gpus"] == 1
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"],
+                           "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
