@@ -116,8 +116,9 @@ typedef struct pulsar_ctx* pulsar_ctx_t;
  * most max_spheres spheres, max_pairs sphere-tile pairs, images up to
  * max_width x max_height, max_channels channels and max_track tracked hits.
  * The workspace is owned by the context and freed by pulsar_destroy.
- * Errors: PULSAR_ERR_ARG (NULL out, non-positive limit, max_track > 16,
- * max_channels > 64, max_pairs >= 2^32), PULSAR_ERR_NOMEM, PULSAR_ERR_CUDA. */
+ * Errors: PULSAR_ERR_ARG (NULL out, non-positive limit, max_spheres >
+ * 0x7fff0000 (sphere indices are 32-bit), max_track > 16, max_channels > 64,
+ * max_pairs >= 2^32), PULSAR_ERR_NOMEM, PULSAR_ERR_CUDA. */
 int pulsar_create(pulsar_ctx_t* out, int device, int64_t max_spheres, int64_t max_pairs,
                   int32_t max_width, int32_t max_height, int32_t max_channels,
                   int32_t max_track);

@@ -459,16 +459,15 @@ k_finalize_one_cam(Frames fs, Workspace w, const float* __restrict__ pos, float*
 #pragma unroll
             for (int k = 0; k < 4; ++k) q[k] = w.gacc2[i0 + k];
         }
-        const float4* p4 = reinterpret_cast<const float4*>(pos + 3 * i0);
+        const float4* p4 = reinterpret_cast<const float4*>(pos + 3 * (size_t)i0);
         const float4 pa = p4[0], pb = p4[1], pc = p4[2];
         const float p[12] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w, pc.x, pc.y, pc.z, pc.w};
-#pragma unroll
         float gp[12];
 #pragma unroll
         for (int k = 0; k < 4; ++k)
             finalize_one(f, g[k], p[3 * k], p[3 * k + 1], p[3 * k + 2], gp + 3 * k, acc);
         if (grad_pos) {
-            float4* o4 = reinterpret_cast<float4*>(grad_pos + 3 * i0);
+            float4* o4 = reinterpret_cast<float4*>(grad_pos + 3 * (size_t)i0);
             o4[0] = make_float4(gp[0], gp[1], gp[2], gp[3]);
             o4[1] = make_float4(gp[4], gp[5], gp[6], gp[7]);
             o4[2] = make_float4(gp[8], gp[9], gp[10], gp[11]);
@@ -501,12 +500,13 @@ k_finalize_one_cam(Frames fs, Workspace w, const float* __restrict__ pos, float*
             if (acc2) store_acc2_one(w.gacc2[i], i, C, sph, grad_opacity, grad_features);
             float gp[3];
             const float4 gc = make_float4(g.x * cams, g.y * cams, g.z * cams, g.w);
-            finalize_one(f, gc, pos[3 * i], pos[3 * i + 1], pos[3 * i + 2], gp, acc);
+            finalize_one(f, gc, pos[3 * (size_t)i], pos[3 * (size_t)i + 1], pos[3 * (size_t)i + 2], gp, acc);
             if (grad_pos) {
                 // R^T dL/dc of the unscaled g, averaged
-                grad_pos[3 * i] = (f.R[0] * g.x + f.R[3] * g.y + f.R[6] * g.z) * sph;
-                grad_pos[3 * i + 1] = (f.R[1] * g.x + f.R[4] * g.y + f.R[7] * g.z) * sph;
-                grad_pos[3 * i + 2] = (f.R[2] * g.x + f.R[5] * g.y + f.R[8] * g.z) * sph;
+                const size_t i3 = 3 * (size_t)i;
+                grad_pos[i3] = (f.R[0] * g.x + f.R[3] * g.y + f.R[6] * g.z) * sph;
+                grad_pos[i3 + 1] = (f.R[1] * g.x + f.R[4] * g.y + f.R[7] * g.z) * sph;
+                grad_pos[i3 + 2] = (f.R[2] * g.x + f.R[5] * g.y + f.R[8] * g.z) * sph;
             }
             if (grad_radius) grad_radius[i] = g.w * sph;
         }
@@ -548,14 +548,14 @@ k_finalize_cams(Frames fs, Workspace w, const float* __restrict__ pos, float* __
     const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
     float p[12];
     if (vec) {
-        const float4* p4 = reinterpret_cast<const float4*>(pos + 3 * i0);
+        const float4* p4 = reinterpret_cast<const float4*>(pos + 3 * (size_t)i0);
         const float4 pa = p4[0], pb = p4[1], pc = p4[2];
         p[0] = pa.x; p[1] = pa.y; p[2] = pa.z; p[3] = pa.w;
         p[4] = pb.x; p[5] = pb.y; p[6] = pb.z; p[7] = pb.w;
         p[8] = pc.x; p[9] = pc.y; p[10] = pc.z; p[11] = pc.w;
     } else {
 #pragma unroll
-        for (int q = 0; q < 12; ++q) p[q] = q < 3 * cnt ? pos[3 * i0 + q] : 0.0f;
+        for (int q = 0; q < 12; ++q) p[q] = q < 3 * cnt ? pos[3 * (size_t)i0 + q] : 0.0f;
     }
     float sph_last[4] = {1.0f, 1.0f, 1.0f, 1.0f};
     for (int cam = 0; cam < n_cams; ++cam) {
@@ -603,7 +603,7 @@ k_finalize_cams(Frames fs, Workspace w, const float* __restrict__ pos, float* __
         // dL/dp and dL/dr: the first camera writes, the others add
         if (vec) {
             if (grad_pos) {
-                float4* o4 = reinterpret_cast<float4*>(grad_pos + 3 * i0);
+                float4* o4 = reinterpret_cast<float4*>(grad_pos + 3 * (size_t)i0);
                 if (cam > 0) {
                     const float4 a = o4[0], b = o4[1], c = o4[2];
                     gp[0] += a.x; gp[1] += a.y; gp[2] += a.z; gp[3] += a.w;
@@ -630,7 +630,7 @@ k_finalize_cams(Frames fs, Workspace w, const float* __restrict__ pos, float* __
                     const int i = i0 + k;
                     if (grad_pos)
                         for (int l = 0; l < 3; ++l)
-                            grad_pos[3 * i + l] = gp[3 * k + l] + (cam > 0 ? grad_pos[3 * i + l] : 0.0f);
+                            grad_pos[3 * (size_t)i + l] = gp[3 * k + l] + (cam > 0 ? grad_pos[3 * (size_t)i + l] : 0.0f);
                     if (grad_radius) grad_radius[i] = gr[k] + (cam > 0 ? grad_radius[i] : 0.0f);
                 }
             }

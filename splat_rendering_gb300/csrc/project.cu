@@ -26,9 +26,10 @@ k_project(Frames fs, Workspace w, const float* __restrict__ pos, const float* __
     const int n = fs.f[0].n;
     float px = 0.f, py = 0.f, pz = 0.f, r = 0.f, op = 0.f;
     if (i < n) {
-        px = pos[3 * i];
-        py = pos[3 * i + 1];
-        pz = pos[3 * i + 2];
+        const size_t i3 = 3 * (size_t)i;   // 64-bit: 3 i passes 2^31 beyond 715M spheres
+        px = pos[i3];
+        py = pos[i3 + 1];
+        pz = pos[i3 + 2];
         r = radius[i];
         op = opacity[i];
     }

@@ -118,7 +118,8 @@ int pulsar_create_cams(pulsar_ctx_t* out, int device, int64_t max_spheres, int64
     PULSAR_TRACE("pulsar_create_cams");
     if (!out) return PULSAR_ERR_ARG;
     *out = nullptr;
-    if (max_spheres < 0 || max_spheres > 0x7fffffffLL || max_pairs < 1 ||
+    // sphere indices stay 32-bit with a launch's worth of margin below 2^31
+    if (max_spheres < 0 || max_spheres > 0x7fff0000LL || max_pairs < 1 ||
         max_pairs >= 0xffffffffLL || max_width < 1 || max_width > 65535 || max_height < 1 ||
         max_height > 65535 || max_channels < 1 || max_channels > kMaxChannels ||
         max_track < 1 || max_track > kMaxTrack || max_cams < 1 || max_cams > kMaxCams)

@@ -46,6 +46,8 @@ def test_strerror_and_host_side_argument_errors(lib):
     assert lib.pulsar_create(ctypes.byref(h), 0, 10, 10, 16, 16, 65, 5) == pl.ERR_ARG
     assert lib.pulsar_create(ctypes.byref(h), 0, 10, 0, 16, 16, 3, 5) == pl.ERR_ARG
     assert lib.pulsar_create(ctypes.byref(h), 0, 10, 10, 70000, 16, 3, 5) == pl.ERR_ARG
+    # sphere indices are 32-bit with a launch's margin: at most 0x7fff0000 spheres
+    assert lib.pulsar_create(ctypes.byref(h), 0, 0x7fff0001, 10, 16, 16, 3, 5) == pl.ERR_ARG
     # NULL context
     assert lib.pulsar_bin(None, None) == pl.ERR_ARG
     assert lib.pulsar_forward(None, None, None, None, None) == pl.ERR_ARG
