@@ -131,7 +131,9 @@ __global__ void __launch_bounds__(kEmitThreads) k_emit(Frames fs, Workspace w) {
     const Frame& f = fs.f[0];
     const uint32_t m = w.state->n_pairs;
     if (m > f.max_pairs) return;   // overflowed frame: the capacity error is latched
-    for (uint32_t p = blockIdx.x * blockDim.x + threadIdx.x; p < m; p += gridDim.x * blockDim.x) {
+    // 64-bit cursor: m may lie within one grid stride of 2^32
+    for (uint64_t p = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; p < m;
+         p += (uint64_t)gridDim.x * blockDim.x) {
         const uint4 s = w.staged[p];
         if (!PULSAR_CHECK(w.state, s.x < f.n_tiles_all)) continue;
         const uint32_t at = w.tile_start[s.x] + s.y;
