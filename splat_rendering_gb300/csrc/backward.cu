@@ -109,10 +109,24 @@ k_backward(Frames fs, Workspace w, const float* __restrict__ features,
     // the pixel's inputs, loaded together with the list bounds (the buffers
     // are read in bounds also for an overflowed frame, whose values go unused)
     float G[CMAX], F[CMAX];
+    if (CMAX % 4 == 0 && C == CMAX &&
+        ((reinterpret_cast<uintptr_t>(image) | reinterpret_cast<uintptr_t>(grad_image)) & 15u) == 0) {
+        // whole 16-byte-aligned rows: 16-byte loads
+        const float4* g4 = reinterpret_cast<const float4*>(grad_image + (size_t)p * CMAX);
+        const float4* f4 = reinterpret_cast<const float4*>(image + (size_t)p * CMAX);
 #pragma unroll
-    for (int c = 0; c < CMAX; ++c) {
-        G[c] = (inside && c < C) ? grad_image[(size_t)p * C + c] : 0.0f;
-        F[c] = (inside && c < C) ? image[(size_t)p * C + c] : 0.0f;
+        for (int q = 0; q < CMAX / 4; ++q) {
+            const float4 gq = inside ? g4[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 fq = inside ? f4[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+            G[4 * q] = gq.x; G[4 * q + 1] = gq.y; G[4 * q + 2] = gq.z; G[4 * q + 3] = gq.w;
+            F[4 * q] = fq.x; F[4 * q + 1] = fq.y; F[4 * q + 2] = fq.z; F[4 * q + 3] = fq.w;
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < CMAX; ++c) {
+            G[c] = (inside && c < C) ? grad_image[(size_t)p * C + c] : 0.0f;
+            F[c] = (inside && c < C) ? image[(size_t)p * C + c] : 0.0f;
+        }
     }
     const float mg = inside ? w.mg[p] : 0.0f;
     const float wsum = inside ? w.wsum[p] : 1.0f;

@@ -415,9 +415,18 @@ k_forward(Frames fs, Workspace w, const float* __restrict__ features, const floa
 
     if (inside) {
         const float iw = 1.0f / wsum;
+        if (CMAX % 4 == 0 && C == CMAX && (reinterpret_cast<uintptr_t>(image) & 15u) == 0) {
+            // whole 16-byte-aligned rows: 16-byte stores
+            float4* o4 = reinterpret_cast<float4*>(image + (size_t)p * CMAX);
 #pragma unroll
-        for (int c = 0; c < CMAX; ++c)
-            if (c < C) image[(size_t)p * C + c] = acc[c] * iw;
+            for (int q = 0; q < CMAX / 4; ++q)
+                o4[q] = make_float4(acc[4 * q] * iw, acc[4 * q + 1] * iw, acc[4 * q + 2] * iw,
+                                    acc[4 * q + 3] * iw);
+        } else {
+#pragma unroll
+            for (int c = 0; c < CMAX; ++c)
+                if (c < C) image[(size_t)p * C + c] = acc[c] * iw;
+        }
         // store the stabiliser's high part; fold its low part into the normaliser
         w.mg[p] = mg;
         w.wsum[p] = wsum * ex2_approx(mgl);
