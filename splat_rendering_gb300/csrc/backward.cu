@@ -20,8 +20,8 @@
 // k_finalize_one_cam, k_finalize_cams  four spheres per thread: dL/dp =
 //             R^T dL/dc and dL/dr out of the accumulator, and dL/do, dL/df out
 //             of the second one, summed over the cameras of a batch (the
-//             accumulators are zeroed right before the backward, so the lines
-//             its reductions touch are fresh in L2);
+//             frame's forward zeroed both accumulators; a second backward of
+//             the same frame has its launcher zero them again);
 //             dL/dR = sum dL/dc p^T and dL/dt = sum dL/dc of every camera
 //             reduced per block (Pulsar Sec. B.2: sphere-wise camera-gradient
 //             accumulation).
