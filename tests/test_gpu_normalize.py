@@ -53,3 +53,30 @@ def test_normalisation_leaves_the_next_frame_plain(oracle_lib):
         assert g["code"] == 0
         gh.compare_frame(g, o, f"sequence normalize={sc.params.normalize_grads}")
     r.close()
+
+
+def test_normalised_gradients_over_stale_culled_records(oracle_lib):
+    """A culled sphere writes only the first half of its record, so one that
+    the previous frame of the same context kept still holds that frame's
+    geometry in the second half.  The normalised finalize reads a record's
+    geometry only for spheres some pixel tracks: moving the camera 3 units
+    forward culls about half the spheres of the first frame, and the
+    normalised gradients of the second frame still match the oracle."""
+    import numpy as np
+    from splat_rendering_gb300 import pulsar as pl
+    base = scenes.random_scene(96, 2000, 64, 48, rrange=(0.01, 0.3))
+    cam = base.cameras[0]
+    moved = replace(cam, t=(cam.t - np.array([0.0, 0.0, 3.0], np.float32)).astype(np.float32))
+    second = replace(base, cameras=[moved], params=replace(base.params, normalize_grads=True))
+    r = pl.Renderer(max_spheres=2000, max_pairs=1 << 16, max_width=64, max_height=48,
+                    max_channels=3, max_track=5)
+    culled = []
+    for sc in (base, second):
+        o, d, offs, ids = _oracle_all(oracle_lib, sc)
+        culled.append(int((d["keep"] == 0).sum()))
+        g = gh.run_gpu(sc, renderer=r)
+        assert g["code"] == 0
+        gh.assert_decisions_equal(g, d)
+        gh.compare_frame(g, o, f"{sc.name} normalize={sc.params.normalize_grads}")
+    r.close()
+    assert culled[1] > culled[0] + 500, culled
