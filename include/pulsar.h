@@ -261,7 +261,9 @@ const char* pulsar_strerror(int code);
  * For a batch of K cameras every array holds K per-camera blocks, camera
  * after camera (records [K][n], tiles [K*B], pixels [K*H*W]); the tile lists
  * of all cameras share one offsets array.
- *   PULSAR_DBG_RECORDS   [n] 64-byte sphere records, 16 x 32-bit words:
+ *   PULSAR_DBG_RECORDS   [n] 64-byte sphere records, 16 x 32-bit words (written for
+ *                        the frame's kept spheres only; a culled sphere's record
+ *                        holds whatever it held before):
  *                        0-3   u_hi, u_lo, v_hi, v_lo  projected centre (float pairs)
  *                        4-6   exponent log2(e) o z~/gamma as hi, lo; opacity o
  *                        7     flags: 1 kept, 2 radius on the kappa floor, 4 geometry cut

@@ -498,7 +498,7 @@ k_finalize_one_cam(Frames fs, Workspace w, const float* __restrict__ pos, float*
                 const float cnt = w.hitcnt[i];
                 sph = cnt > 0.0f ? 1.0f / cnt : 1.0f;
                 // a sphere no pixel tracks has no gradient (and may be culled,
-                // its record's second half unwritten)
+                // its record not written this frame)
                 cams = 0.0f;
                 if (cnt > 0.0f) {
                     const float4 geo = w.rec[i].geo;          // c.z in z, r_eff in w
@@ -588,7 +588,7 @@ k_finalize_cams(Frames fs, Workspace w, const float* __restrict__ pos, float* __
                 const float c = w.hitcnt[f.rec_base + i];
                 sph = c > 0.0f ? 1.0f / c : 1.0f;
                 // a sphere no pixel tracks has no gradient (and may be culled,
-                // its record's second half unwritten)
+                // its record not written this frame)
                 cams = 0.0f;
                 if (c > 0.0f) {
                     const float4 geo = w.rec[f.rec_base + i].geo;   // c.z in z, r_eff in w

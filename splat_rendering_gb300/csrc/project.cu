@@ -106,14 +106,13 @@ k_project(Frames fs, Workspace w, const float* __restrict__ pos, const float* __
                     key_out = key;
                 }
             }
-            r1.w = __uint_as_float(flags);
-            SphereRec* out = w.rec + f.rec_base + i;
-            out->uv = r0;
-            out->ex = r1;
-            // the second 32-byte half is read only through the tile lists,
-            // i.e. for kept spheres: a culled sphere writes the first half
-            // alone (flags 0), a whole sector
+            // records are read only through the tile lists, i.e. for kept
+            // spheres: a culled sphere writes none
             if (flags & kFlagKeep) {
+                r1.w = __uint_as_float(flags);
+                SphereRec* out = w.rec + f.rec_base + i;
+                out->uv = r0;
+                out->ex = r1;
                 out->geo = r2;
                 out->rk = make_uint4(rc.x, rc.y, __float_as_uint(s2), __float_as_uint(key));
             }

@@ -403,8 +403,9 @@ __device__ __forceinline__ float ex2_approx(float x) {
 //   geo : ir2_hi, ir2_lo, c.z, r_eff          ir2 = (c.z / r_eff)^2 as a pair
 //   rk  : x0 | x1 << 16, y0 | y1 << 16, bits of s2 = (r_eff/c.z)^2, bits of
 //         the depth key c.z - r_eff           (decision quantities)
-// A culled sphere's record has uv and ex zero (flags 0: not kept); its geo and
-// rk are not written, since only tile lists (kept spheres) lead to them.
+// Only kept spheres' records are written (the tile lists, which hold kept
+// spheres only, are the one way to them); a culled sphere's record keeps
+// whatever it held.
 struct __align__(16) SphereRec {
     float4 uv;
     float4 ex;
