@@ -827,34 +827,41 @@ k_shade_backward(Frames fs, Workspace w, const float* __restrict__ features,
     if (warp == 0) tmem_dealloc(tmem, kBwdCols);
 }
 
-// Sum of the CTAs' weight-gradient shares in a fixed order (fp64): a block
-// takes 32 parameters; warp w sums the shares w, w + 16, ... with four
-// independent accumulators (loads in flight), the warps combine in order.
+// Sum of the CTAs' weight-gradient shares in a fixed order, in float-pair
+// arithmetic (Knuth's TwoSum per addition, ~2^-44 relative: the accuracy of
+// an fp64 sum of these few hundred terms at fp32 speed, where this part's
+// fp64 rate is a small fraction of it): a block takes 32 parameters; warp w
+// sums the shares w, w + 16, ... with four independent accumulators (loads in
+// flight), the warps combine in order.
 constexpr int kReduceWarps = 16;
 
 __global__ void __launch_bounds__(32 * kReduceWarps)
 k_shade_reduce(const float* __restrict__ part, int n_part, float* __restrict__ grad_params) {
     pdl_begin();
-    __shared__ double acc[kReduceWarps][32];
+    __shared__ float2 acc[kReduceWarps][32];
     const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
     const int i = blockIdx.x * 32 + lane;
-    double s[4] = {0.0, 0.0, 0.0, 0.0};
+    FPair s[4] = {{0.0f, 0.0f}, {0.0f, 0.0f}, {0.0f, 0.0f}, {0.0f, 0.0f}};
     if (i < kShadeParams) {
         int c = wp;
         for (; c + 3 * kReduceWarps < n_part; c += 4 * kReduceWarps) {
+            float v[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-                s[u] += (double)part[(size_t)(c + u * kReduceWarps) * kShadeParams + i];
+            for (int u = 0; u < 4; ++u) v[u] = part[(size_t)(c + u * kReduceWarps) * kShadeParams + i];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) s[u] = pp_add(s[u], FPair{v[u], 0.0f});
         }
-        for (; c < n_part; c += kReduceWarps) s[0] += (double)part[(size_t)c * kShadeParams + i];
+        for (; c < n_part; c += kReduceWarps)
+            s[0] = pp_add(s[0], FPair{part[(size_t)c * kShadeParams + i], 0.0f});
     }
-    acc[wp][lane] = (s[0] + s[1]) + (s[2] + s[3]);
+    const FPair t4 = pp_add(pp_add(s[0], s[1]), pp_add(s[2], s[3]));
+    acc[wp][lane] = make_float2(t4.hi, t4.lo);
     __syncthreads();
     if (wp == 0 && i < kShadeParams) {
-        double t = 0.0;
+        FPair t = {0.0f, 0.0f};
 #pragma unroll
-        for (int w2 = 0; w2 < kReduceWarps; ++w2) t += acc[w2][lane];
-        grad_params[i] = (float)t;
+        for (int w2 = 0; w2 < kReduceWarps; ++w2) t = pp_add(t, FPair{acc[w2][lane].x, acc[w2][lane].y});
+        grad_params[i] = __fadd_rn(t.hi, t.lo);
     }
 }
 
