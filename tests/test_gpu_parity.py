@@ -319,3 +319,41 @@ def test_backward_twice_on_one_frame(oracle_lib):
         for k in ("pos", "radius", "opacity", "features", "cam"):
             gh.assert_close(g[k], o["grad_" + k], gh.GRAD_RTOL, gh.GRAD_ATOL, f"twice {k}",
                             o["abs_grad_" + k], o["sens_grad_" + k], dF)
+
+
+def test_unaligned_sixteen_channel_rows(oracle_lib):
+    """Rows of 16 channels that are not 16-byte aligned (features, image and
+    image gradient at a 4-byte offset) take the scalar paths of the forward's
+    feature staging and image stores and of the backward's feature staging and
+    pixel loads: the image and the tracked ids come out bit for bit as with
+    aligned rows, and the gradients match the oracle."""
+    import torch
+    from splat_rendering_gb300 import pulsar as pl
+    sc = scenes.random_scene(67, 600, 48, 40, channels=16, n_track=8, rrange=(0.05, 0.4))
+    o, _, _, _ = _oracle_all(oracle_lib, sc)
+    r = pl.Renderer(max_spheres=sc.n, max_pairs=1 << 16, max_width=48, max_height=40,
+                    max_channels=16, max_track=8)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+
+    def offset(a):   # a copy of a at a 4-byte offset from a 16-byte boundary
+        buf = torch.zeros(a.numel() + 1, device="cuda")
+        v = buf[1:].view(a.shape)
+        v.copy_(a)
+        return v
+
+    pos, rad, opa, bg = t(sc.pos), t(sc.radius), t(sc.opacity), t(sc.bg)
+    cam, prm = pl.camera(sc.cameras[0]), pl.params(sc.params)
+    feat = t(sc.features)
+    img_aligned = r.render(pos, rad, opa, feat, cam, prm, bg)
+    ids_aligned = r.debug("ids").copy()
+    feat_u = offset(feat)
+    img_u = offset(torch.zeros_like(img_aligned))
+    r.render(pos, rad, opa, feat_u, cam, prm, bg, image=img_u)
+    assert torch.equal(img_u, img_aligned)
+    assert np.array_equal(r.debug("ids"), ids_aligned)
+    grads = r.backward(offset(t(sc.grad_images[0])))
+    assert r.status()[0] == 0
+    dF = gh.image_err(img_u.cpu().numpy(), o["image"])
+    for k in ("pos", "radius", "opacity", "features", "cam"):
+        gh.assert_close(grads[k].cpu().numpy(), o["grad_" + k], gh.GRAD_RTOL, gh.GRAD_ATOL, k,
+                        o["abs_grad_" + k], o["sens_grad_" + k], dF)
