@@ -57,8 +57,11 @@ struct BwdBatch {
     static constexpr int feat_bytes = n * fsp * 4;
 };
 
+// Blocks per SM: 4 up to four channels, 3 up to eight (76 registers, no
+// spills; 176 vs 218 us at two blocks on the headline frame with eight
+// channels), 2 up to sixteen (three spill, 268 vs 244 us), 1 beyond.
 template <int CMAX, bool MULTI>
-__global__ void __launch_bounds__(kBwdThreads, CMAX <= 4 ? 4 : (CMAX <= 16 ? 2 : 1))
+__global__ void __launch_bounds__(kBwdThreads, CMAX <= 4 ? 4 : (CMAX <= 8 ? 3 : (CMAX <= 16 ? 2 : 1)))
 k_backward(Frames fs, Workspace w, const float* __restrict__ features,
            const float* __restrict__ image, const float* __restrict__ grad_image,
            float* __restrict__ grad_opacity, float* __restrict__ grad_features, int mode) {
