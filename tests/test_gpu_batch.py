@@ -138,3 +138,14 @@ def test_batch_renders_each_camera_as_the_single_path():
         assert np.array_equal(g["image"][k], s["image"]), k
         assert np.array_equal(g["ids"][k], s["ids"]), k
         assert np.array_equal(g["mg"][k], s["mg"]), k
+
+
+def test_sixteen_channel_rig(oracle_lib):
+    """Three cameras (one orthographic) with 16 channels and n_track 8: the
+    batched instantiations of the wide-feature forward and backward, and the
+    finalize that sums feature and opacity gradients over the cameras."""
+    sc = scenes.random_scene(103, 1500, 48, 40, channels=16, n_track=8, rrange=(0.02, 0.3))
+    cams = _rig(103, 3, 48, 40, ortho_at=(1,))
+    rng = np.random.default_rng(9)
+    grads = [rng.standard_normal((40, 48, 16)).astype(np.float32) for _ in cams]
+    check_batch(oracle_lib, sc, cams, grads)
